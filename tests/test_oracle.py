@@ -1,0 +1,424 @@
+"""Pins of the float64 oracle against facts fixed by the pages and by mathematics.
+
+Nothing here compares the oracle with itself by retyping a formula: each pin is a
+closed form, an exact rational evaluation, a different algorithm (pair sum vs serial
+recurrence vs chunked scan vs matrix form), an invariant, or finite differences.
+A final group plants plausible mistakes in copies of the oracle and checks that the
+pins catch every one of them.
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import cref
+from oracle import hla2_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(B, H, n, d, dv, seed=0, positive=False):
+    r = np.random.default_rng(seed)
+    q = r.standard_normal((B, H, n, d)) / np.sqrt(d)
+    k = r.standard_normal((B, H, n, d)) / np.sqrt(d)
+    v = r.standard_normal((B, H, n, dv))
+    if positive:
+        q, k = np.log1p(np.exp(q * np.sqrt(d))), np.log1p(np.exp(k * np.sqrt(d)))
+    return q, k, v
+
+
+def rel(a, b):
+    return np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300)
+
+
+# ---------------------------------------------------------------------------
+# Closed forms and exact values
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("g", [1.0, 0.7])
+def test_single_token_closed_form(g):
+    """n = 1: o_1 = (q_1 . k_1)^2 v_1 whatever the decay."""
+    q, k, v = rnd(1, 1, 1, 5, 3, seed=1)
+    o = O.serial_forward(q, k, v, [g])
+    expect = (q[0, 0, 0] @ k[0, 0, 0]) ** 2 * v[0, 0, 0]
+    np.testing.assert_allclose(o[0, 0, 0], expect, rtol=1e-13)
+
+
+@pytest.mark.parametrize("g", [1.0, 0.6])
+def test_two_token_closed_form(g):
+    """n = 2: o_2 = g^2 (q2.k1)(k1.q1) v1 + g (q2.k1)^2 v2 + (q2.k2)^2 v2.
+    The pair (key 2, value 1) is absent: that is the mask."""
+    q, k, v = rnd(1, 1, 2, 4, 3, seed=2)
+    q1, q2 = q[0, 0]
+    k1, k2 = k[0, 0]
+    v1, v2 = v[0, 0]
+    expect = g * g * (q2 @ k1) * (k1 @ q1) * v1 + g * (q2 @ k1) ** 2 * v2 + (q2 @ k2) ** 2 * v2
+    o = O.serial_forward(q, k, v, [g])
+    np.testing.assert_allclose(o[0, 0, 1], expect, rtol=1e-12)
+    leaked = g * (q2 @ k2) * (k2 @ q1) * v1
+    assert np.max(np.abs(leaked)) > 1e-3  # the excluded pair is not negligible here
+
+
+def test_scalar_feature_closed_form():
+    """d = 1: o_t = q_t * sum_{i<=j<=t} g^((t-i)+(t-j)) k_i^2 q_j v_j."""
+    q, k, v = rnd(1, 1, 7, 1, 2, seed=3)
+    g = 0.8
+    o = O.serial_forward(q, k, v, [g])
+    Q, K, V = q[0, 0, :, 0], k[0, 0, :, 0], v[0, 0]
+    for t in range(7):
+        s = sum(g ** ((t - i) + (t - j)) * K[i] ** 2 * Q[j] * V[j]
+                for j in range(t + 1) for i in range(j + 1))
+        np.testing.assert_allclose(o[0, 0, t], Q[t] * s, rtol=1e-12)
+
+
+@pytest.mark.parametrize("name", ["n2_d1", "n5_d2", "n4_d3_nodecay"])
+@pytest.mark.parametrize("impl", ["numpy", "c"])
+def test_exact_rational_fixtures(name, impl):
+    """Serial float64 recurrence against exact rational pair sums (tests/golden)."""
+    with open(os.path.join(GOLDEN, f"{name}.json")) as f:
+        doc = json.load(f)
+    q = np.array(doc["q"], dtype=np.float64)[None, None]
+    k = np.array(doc["k"], dtype=np.float64)[None, None]
+    v = np.array(doc["v"], dtype=np.float64)[None, None]
+    g = float(Fraction(doc["gamma"]))
+    out = np.array([[float(Fraction(x)) for x in row] for row in doc["out"]])
+    den = np.array([float(Fraction(x)) for x in doc["den"]])
+    if impl == "numpy":
+        o = O.serial_forward(q, k, v, [g])[0, 0]
+        on = O.serial_forward(q, k, v, [g], normalize=True, eps=0.0)[0, 0]
+    else:
+        o = cref.forward(q, k, v, [g])[0, 0]
+        on = cref.forward(q, k, v, [g], normalize=True, eps=0.0)[0, 0]
+    np.testing.assert_allclose(o, out, rtol=1e-13, atol=1e-12)
+    np.testing.assert_allclose(on, out / den[:, None], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Three algorithms, one function
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("g", [None, 0.9])
+@pytest.mark.parametrize("normalize", [False, True])
+def test_brute_force_equals_serial(g, normalize):
+    q, k, v = rnd(2, 2, 9, 3, 2, seed=4, positive=normalize)
+    gam = None if g is None else [g, g * 0.95]
+    a = O.brute_force_forward(q, k, v, gam, normalize=normalize)
+    b = O.serial_forward(q, k, v, gam, normalize=normalize)
+    assert rel(b, a) < 1e-12
+
+
+def test_matrix_form_equals_serial():
+    """Matrix form (A A^T V structure of the technical summary, item 2, with masks):
+    with A = Q K^T and Atil = lower-triangular part of A (i <= j),
+        W = ((A * Gam) Atil^T) * Gam_low,   O = W V,
+    where Gam[t, i] = g^(t-i) and Gam_low[t, j] = g^(t-j) [j <= t]."""
+    q, k, v = rnd(1, 1, 23, 5, 4, seed=5)
+    g = 0.93
+    Q, K, V = q[0, 0], k[0, 0], v[0, 0]
+    n = Q.shape[0]
+    A = Q @ K.T
+    idx = np.arange(n)
+    lag = idx[:, None] - idx[None, :]
+    Gam = g ** lag.astype(np.float64)
+    Atil = np.tril(A)
+    W = ((A * np.where(lag >= 0, Gam, 0.0)) @ Atil.T) * np.where(lag >= 0, Gam, 0.0)
+    o = O.serial_forward(q, k, v, [g])[0, 0]
+    assert rel(o, W @ V) < 1e-12
+
+
+@pytest.mark.parametrize("chunk", [1, 2, 3, 4, 5, 16, 13])
+def test_chunked_scan_equals_serial_any_width(chunk):
+    """Chunk-width independence ([PS] §4, [TS4]): the scan reproduces the serial
+    recurrence for every chunk width, including non-divisors of n."""
+    q, k, v = rnd(1, 2, 13, 3, 2, seed=6)
+    gam = [0.85, 1.0]
+    a, sa = O.serial_forward(q, k, v, gam, return_state=True)
+    b, sb = O.chunked_scan_forward(q, k, v, gam, chunk=chunk, return_state=True)
+    assert rel(b, a) < 1e-12
+    for key in ("S", "C", "m", "G", "h"):
+        assert rel(sb[key], sa[key]) < 1e-12
+
+
+def test_chunked_scan_normalized_and_init_state():
+    q, k, v = rnd(1, 1, 10, 3, 2, seed=7, positive=True)
+    q0, k0, v0 = rnd(1, 1, 6, 3, 2, seed=8, positive=True)
+    _, init = O.serial_forward(q0, k0, v0, [0.9], return_state=True)
+    a = O.serial_forward(q, k, v, [0.9], normalize=True, init_state=init)
+    b = O.chunked_scan_forward(q, k, v, [0.9], chunk=4, normalize=True, init_state=init)
+    assert rel(b, a) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# Algebra of the combine
+# ---------------------------------------------------------------------------
+
+def _rand_tuple(r, d, dv):
+    return {"S": r.standard_normal((d, d)), "C": r.standard_normal((d, dv)),
+            "m": r.standard_normal(d), "G": r.standard_normal((d, dv)),
+            "h": r.standard_normal(d), "rho": float(r.uniform(0.2, 1.0))}
+
+
+def test_combine_associative():
+    r = np.random.default_rng(9)
+    for _ in range(20):
+        a, b, c = (_rand_tuple(r, 4, 3) for _ in range(3))
+        x = O.combine(O.combine(a, b), c)
+        y = O.combine(a, O.combine(b, c))
+        for key in ("S", "C", "m", "G", "h"):
+            assert rel(x[key], y[key]) < 1e-13
+        assert abs(x["rho"] - y["rho"]) < 1e-15
+
+
+def test_combine_identity():
+    r = np.random.default_rng(10)
+    a = _rand_tuple(r, 3, 2)
+    e = O.identity_element(3, 2)
+    for x in (O.combine(a, e), O.combine(e, a)):
+        for key in ("S", "C", "m", "G", "h"):
+            np.testing.assert_array_equal(x[key], a[key])
+
+
+def test_combine_not_commutative():
+    """Time order matters: swapping segments changes the masked summaries."""
+    r = np.random.default_rng(11)
+    a, b = _rand_tuple(r, 3, 2), _rand_tuple(r, 3, 2)
+    assert rel(O.combine(a, b)["G"], O.combine(b, a)["G"]) > 1e-3
+
+
+def test_blelloch_matches_sequential_fold():
+    r = np.random.default_rng(12)
+    items = [_rand_tuple(r, 3, 2) for _ in range(11)]
+    pre = O.blelloch_exclusive_scan(items, 3, 2)
+    acc = O.identity_element(3, 2)
+    for i, it in enumerate(items):
+        for key in ("S", "C", "m", "G", "h"):
+            np.testing.assert_allclose(pre[i][key], acc[key], rtol=1e-12, atol=1e-12)
+        acc = O.combine(acc, it)
+
+
+# ---------------------------------------------------------------------------
+# Invariants
+# ---------------------------------------------------------------------------
+
+def test_gamma_one_equals_no_decay():
+    q, k, v = rnd(1, 3, 8, 3, 2, seed=13)
+    a = O.serial_forward(q, k, v, None)
+    b = O.serial_forward(q, k, v, [1.0, 1.0, 1.0])
+    np.testing.assert_array_equal(a, b)
+    # and as g -> 1 the decayed output converges to it
+    c = O.serial_forward(q, k, v, [1 - 1e-9] * 3)
+    assert rel(c, a) < 1e-7
+
+
+def test_z_form_identity():
+    """q^T (S_t C_t - G_t) = q^T Z_t with Z_t = g^2 Z_{t-1} + S_t q_t v_t^T; and the
+    denominator S_t m_t - h_t = y_t with y_t = g^2 y_{t-1} + S_t q_t."""
+    q, k, v = rnd(1, 1, 17, 4, 3, seed=14, positive=True)
+    g = 0.91
+    o, st = O.serial_forward(q, k, v, [g], return_state=True)
+    Q, K, V = q[0, 0], k[0, 0], v[0, 0]
+    S = np.zeros((4, 4))
+    Z = np.zeros((4, 3))
+    y = np.zeros(4)
+    for t in range(17):
+        S = g * S + np.outer(K[t], K[t])
+        p = S @ Q[t]
+        Z = g * g * Z + np.outer(p, V[t])
+        y = g * g * y + p
+        np.testing.assert_allclose(Q[t] @ Z, o[0, 0, t], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(Z, st["S"][0, 0] @ st["C"][0, 0] - st["G"][0, 0], rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(y, st["S"][0, 0] @ st["m"][0, 0] - st["h"][0, 0], rtol=1e-11, atol=1e-13)
+
+
+def test_causality():
+    q, k, v = rnd(1, 1, 12, 3, 2, seed=15)
+    o = O.serial_forward(q, k, v, [0.9])
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    r = np.random.default_rng(16)
+    q2[..., 7:, :] += r.standard_normal(q2[..., 7:, :].shape)
+    k2[..., 7:, :] += r.standard_normal(k2[..., 7:, :].shape)
+    v2[..., 7:, :] += r.standard_normal(v2[..., 7:, :].shape)
+    o2 = O.serial_forward(q2, k2, v2, [0.9])
+    np.testing.assert_array_equal(o[..., :7, :], o2[..., :7, :])
+    assert rel(o2[..., 7:, :], o[..., 7:, :]) > 1e-3
+
+
+def test_masked_vs_unmasked_difference_is_G():
+    """q^T S_t C_t - o_t = q^T G_t, and G_t equals the pair sum over key index > value index."""
+    q, k, v = rnd(1, 1, 6, 3, 2, seed=17)
+    g = 0.8
+    o, st = O.serial_forward(q, k, v, [g], return_state=True)
+    Q, K, V = q[0, 0], k[0, 0], v[0, 0]
+    t = 5
+    unmasked = Q[t] @ st["S"][0, 0] @ st["C"][0, 0]
+    np.testing.assert_allclose(unmasked - o[0, 0, t], Q[t] @ st["G"][0, 0], rtol=1e-12)
+    Gb = sum(g ** ((t - i) + (t - j)) * np.outer(K[i], K[i]) @ np.outer(Q[j], V[j])
+             for i in range(t + 1) for j in range(i))
+    np.testing.assert_allclose(st["G"][0, 0], Gb, rtol=1e-12)
+
+
+def test_streaming_equals_forward_and_continuation():
+    """Token-at-a-time decode from zero equals the forward; splitting the sequence
+    and continuing from the first part's final state equals one pass."""
+    q, k, v = rnd(2, 3, 14, 4, 3, seed=18)
+    gam = [0.9, 0.97, 1.0]
+    full, fst = O.serial_forward(q, k, v, gam, return_state=True)
+    _, s1 = O.serial_forward(q[:, :, :9], k[:, :, :9], v[:, :, :9], gam, return_state=True)
+    tail, s2 = O.serial_forward(q[:, :, 9:], k[:, :, 9:], v[:, :, 9:], gam, init_state=s1,
+                                return_state=True)
+    assert rel(tail, full[:, :, 9:]) < 1e-13
+    for key in fst:
+        assert rel(s2[key], fst[key]) < 1e-13
+    # packed layout round trip
+    np.testing.assert_array_equal(O.pack_state(O.unpack_state(O.pack_state(fst), 4, 3)),
+                                  O.pack_state(fst))
+
+
+# ---------------------------------------------------------------------------
+# Gradients ([PS] §4.2 reverse mode)
+# ---------------------------------------------------------------------------
+
+def _loss(q, k, v, dO, g):
+    return float(np.sum(O.serial_forward(q, k, v, g) * dO))
+
+
+def test_adjoint_matches_finite_differences():
+    q, k, v = rnd(1, 1, 7, 3, 2, seed=19)
+    dO = np.random.default_rng(20).standard_normal(v.shape)
+    g = [0.88]
+    dq, dk, dvv = O.serial_backward(q, k, v, dO, g)
+    eps = 1e-6
+    for arr, grad in ((q, dq), (k, dk), (v, dvv)):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            a0 = arr[idx]
+            arr[idx] = a0 + eps
+            lp = _loss(q, k, v, dO, g)
+            arr[idx] = a0 - eps
+            lm = _loss(q, k, v, dO, g)
+            arr[idx] = a0
+            num[idx] = (lp - lm) / (2 * eps)
+        assert rel(grad, num) < 1e-7
+
+
+def test_adjoint_matches_pairsum_gradients():
+    q, k, v = rnd(1, 2, 8, 3, 2, seed=21)
+    dO = np.random.default_rng(22).standard_normal(v.shape)
+    g = [0.9, 1.0]
+    a = O.serial_backward(q, k, v, dO, g)
+    b = O.pairsum_grads(q, k, v, dO, g)
+    for x, y in zip(a, b):
+        assert rel(x, y) < 1e-11
+
+
+def test_adjoint_dot_test():
+    """<dO, J dx> = <J^T dO, dx> for a random direction dx (linearisation by central
+    differences of the forward)."""
+    q, k, v = rnd(1, 1, 9, 3, 3, seed=23)
+    r = np.random.default_rng(24)
+    dO = r.standard_normal(v.shape)
+    dq_, dk_, dv_ = (r.standard_normal(x.shape) for x in (q, k, v))
+    g = [0.95]
+    h = 1e-6
+    fp = O.serial_forward(q + h * dq_, k + h * dk_, v + h * dv_, g)
+    fm = O.serial_forward(q - h * dq_, k - h * dk_, v - h * dv_, g)
+    lhs = np.sum(dO * (fp - fm) / (2 * h))
+    gq, gk, gv = O.serial_backward(q, k, v, dO, g)
+    rhs = np.sum(gq * dq_) + np.sum(gk * dk_) + np.sum(gv * dv_)
+    assert abs(lhs - rhs) / abs(rhs) < 1e-7
+
+
+# ---------------------------------------------------------------------------
+# The C oracle agrees with the numpy oracle
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("normalize", [False, True])
+def test_c_oracle_forward_matches_numpy(normalize):
+    q, k, v = rnd(2, 3, 40, 8, 5, seed=25, positive=normalize)
+    q, k, v = (x.astype(np.float32).astype(np.float64) for x in (q, k, v))
+    gam = [0.9, 0.99, 1.0]
+    a, sa = O.serial_forward(q, k, v, gam, normalize=normalize, return_state=True)
+    b, sb = cref.forward(q, k, v, gam, normalize=normalize, return_state=True)
+    assert rel(b, a) < 1e-12
+    assert rel(sb, O.pack_state(sa)) < 1e-12
+    # continuation from a packed state
+    c = cref.forward(q, k, v, gam, normalize=normalize, init_state=sb)
+    d_ = O.serial_forward(q, k, v, gam, normalize=normalize, init_state=sa)
+    assert rel(c, d_) < 1e-12
+
+
+def test_c_oracle_decode_matches_numpy():
+    q, k, v = rnd(3, 2, 5, 6, 4, seed=26)
+    q, k, v = (x.astype(np.float32).astype(np.float64) for x in (q, k, v))
+    gam = [0.9, 0.999]
+    st = np.zeros((3, 2, O.state_floats(6, 4)))
+    outs = []
+    for t in range(5):
+        outs.append(cref.decode_step(st, q[:, :, t], k[:, :, t], v[:, :, t], gam))
+    a = O.serial_forward(q, k, v, gam)
+    assert rel(np.stack(outs, axis=2), a) < 1e-12
+
+
+def test_c_oracle_backward_matches_numpy():
+    q, k, v = rnd(1, 2, 37, 5, 4, seed=27)
+    q, k, v = (x.astype(np.float32).astype(np.float64) for x in (q, k, v))
+    dO = np.random.default_rng(28).standard_normal(v.shape).astype(np.float32).astype(np.float64)
+    gam = [0.93, 1.0]
+    a = O.serial_backward(q, k, v, dO, gam)
+    b = cref.backward(q, k, v, dO, gam)
+    for x, y in zip(a, b):
+        assert rel(y, x) < 1e-11
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes: each plausible error in the recurrence breaks a pin
+# ---------------------------------------------------------------------------
+
+def _mutant_step(kind):
+    def step(state, q_t, k_t, v_t, g, normalize=False, eps=1e-6):
+        gg = g[None, :]
+        S, C, m, G, h = state["S"], state["C"], state["m"], state["G"], state["h"]
+        gG = gg * gg if kind != "G_decay_once" else gg
+        S1 = gg[..., None, None] * S + np.einsum("bha,bhc->bhac", k_t, k_t)
+        C1 = gg[..., None, None] * C + np.einsum("bha,bhe->bhae", q_t, v_t)
+        Csrc = C1 if kind == "G_uses_new_C" else C
+        kC = np.einsum("bha,bhae->bhe", k_t, Csrc)
+        sign = -1.0 if kind == "G_sign" else 1.0
+        G1 = gG[..., None, None] * G + sign * gg[..., None, None] * np.einsum("bha,bhe->bhae", k_t, kC)
+        if kind == "G_transposed_key":
+            G1 = gG[..., None, None] * G + gg[..., None, None] * np.einsum("bha,bhe->bhae", q_t, kC)
+        m1 = gg[..., None] * m + q_t
+        u = np.einsum("bha,bhac->bhc", q_t, S1)
+        o = np.einsum("bhc,bhce->bhe", u, C1) - np.einsum("bha,bhae->bhe", q_t, G1)
+        return {"S": S1, "C": C1, "m": m1, "G": G1, "h": h}, o
+    return step
+
+
+@pytest.mark.parametrize("kind", ["G_uses_new_C", "G_decay_once", "G_sign", "G_transposed_key"])
+def test_planted_mistakes_are_caught(kind, monkeypatch):
+    q, k, v = rnd(1, 1, 6, 3, 2, seed=29)
+    g = [0.8]
+    truth = O.brute_force_forward(q, k, v, g)
+    monkeypatch.setattr(O, "step", _mutant_step(kind))
+    bad = O.serial_forward(q, k, v, g)
+    assert rel(bad, truth) > 1e-3
+
+
+def test_planted_combine_mistake_is_caught(monkeypatch):
+    """Cross term on the wrong side (S_A C_B instead of S_B C_A) breaks chunk-width
+    independence."""
+    q, k, v = rnd(1, 1, 8, 3, 3, seed=30)
+    truth = O.serial_forward(q, k, v, [0.9])
+    orig = O.combine
+
+    def wrong(A, B):
+        out = orig(A, B)
+        r = B["rho"]
+        out["G"] = r * r * A["G"] + B["G"] + r * (A["S"] @ B["C"])
+        return out
+
+    monkeypatch.setattr(O, "combine", wrong)
+    bad = O.chunked_scan_forward(q, k, v, [0.9], chunk=4)
+    assert rel(bad, truth) > 1e-3
