@@ -1,0 +1,137 @@
+/*
+ * hla2.h -- C ABI of the GB300 (sm_103a) library for masked second-order
+ * Higher-order Linear Attention (HLA-2).
+ *
+ * What the library computes (page "Higher-order Linear Attention", technical summary,
+ * item "1. Zweite Ordnung HLA"; section summary §2, §3.1, §4.3), per head and token t:
+ *
+ *   S_t = g S_{t-1} + k_t k_t^T          (key second moment,        d x d)
+ *   C_t = g C_{t-1} + q_t v_t^T          (query-value accumulator,   d x dv)
+ *   m_t = g m_{t-1} + q_t                (query mass,                d)
+ *   G_t = g^2 G_{t-1} + g k_t (k_t^T C_{t-1})   (cross summary,      d x dv)
+ *   h_t = g^2 h_{t-1} + g k_t (k_t^T m_{t-1})   (cross summary,      d)
+ *   o_t = q_t^T (S_t C_t - G_t)                 (masked output,      dv)
+ *   den_t = q_t^T (S_t m_t - h_t);  normalised output o_t / (den_t + eps)
+ *
+ * g is a fixed per-head decay in (0, 1] (1 = no decay).  Equivalently
+ * o_t = sum_{i <= j <= t} g^((t-i)+(t-j)) (q_t . k_i)(k_i . q_j) v_j: the key index
+ * never comes after the value index, and the pair i == j is kept.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer is a DEVICE pointer unless stated otherwise; the caller owns every
+ *     buffer.  The library allocates no device or host memory and keeps no state
+ *     across calls except a thread-local error message.
+ *   - Tensors are contiguous, head-major, row-vector layout:
+ *       q, k [B, H, n, d];  v, out, dout [B, H, n, dv];  dq, dk [B, H, n, d];
+ *       dv [B, H, n, dv].  Element type given by hla2_opts.dtype (HLA2_F32 or
+ *       HLA2_BF16; every tensor of one call has the same type).
+ *   - gamma: device float array [H], or NULL for no decay.  Values must lie in (0, 1];
+ *     they are read on the device only and are not validated there.
+ *   - Packed state of one head (decode layout), float32:
+ *       [ S d*d (row-major) | C d*dv | G d*dv | m d | h d ]   (hla2_state_floats)
+ *     init_state / final_state / the decode state are [B or N, H] such blocks.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *     Return value: HLA2_OK or a negative error code; hla2_last_error() describes the
+ *     last failure on the calling host thread.  Argument errors are detected on the
+ *     host before anything is launched; launch errors map to HLA2_ERR_CUDA.
+ *   - Supported sizes: d, dv in {16, 32, 64, 128}; chunk in {16, 32, 64, 128};
+ *     any n >= 0 (the last chunk may be partial); B, H >= 0.  Pointers must be
+ *     16-byte aligned.  A combination the kernels do not cover returns
+ *     HLA2_ERR_UNSUPPORTED.
+ */
+#ifndef HLA2_H_
+#define HLA2_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
+typedef struct CUstream_st* hla2_stream_t;
+
+enum {
+    HLA2_OK = 0,
+    HLA2_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad size, bad flag       */
+    HLA2_ERR_UNSUPPORTED = -2, /* valid request outside the compiled kernel set      */
+    HLA2_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required         */
+    HLA2_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed        */
+    HLA2_ERR_TIMEOUT = -5      /* reserved: a bounded device-side wait gave up       */
+};
+
+enum { HLA2_F32 = 0, HLA2_BF16 = 1 };
+
+/* Options that trail the positional arguments.  Zero-initialise and set what you use. */
+typedef struct {
+    int dtype;              /* HLA2_F32 | HLA2_BF16: type of q, k, v, out, dout, grads      */
+    float eps;              /* ratio-normalisation epsilon (used when normalize != 0)         */
+    void* workspace;        /* device scratch of >= the size the *_workspace_bytes query gives */
+    size_t workspace_bytes; /* its size in bytes                                              */
+    const float* init_state;/* nullable: packed state [B, H] to continue from (forward only)  */
+    float* final_state;     /* nullable: receives the packed state after token n (forward)   */
+} hla2_opts;
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int hla2_version(void);
+
+/* Message describing the last error returned on this host thread ("" if none). */
+const char* hla2_last_error(void);
+
+/* Floats in one packed head state: d*d + 2*d*dv + 2*d. */
+size_t hla2_state_floats(int d, int dv);
+
+/*
+ * Scratch bytes hla2_forward needs for these arguments (0 is a valid answer).
+ * Depends on the arguments and on the number of SMs of the current device.
+ * Returns (size_t)-1 for arguments hla2_forward would reject.
+ */
+size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
+                                    int normalize, int want_final_state);
+
+/*
+ * Strictly causal masked HLA-2 forward, chunk-parallel (section summary §4, §4.2, §5;
+ * technical summary item "4. Paralleles Training durch assoziative Scans").
+ * q, k, v -> out.  The sequence is cut into chunks of width `chunk`; chunks are
+ * grouped into segments; per-segment summaries are combined by an exclusive scan
+ * with the masked semidirect product (cross term S_B C_A) to give each segment
+ * its carry-in; every token's output is then formed from its inclusive state.
+ * normalize != 0 divides by the masked denominator (+ opts->eps).
+ * opts must be non-NULL (dtype and workspace).  init_state continues a previous
+ * sequence; final_state receives the state after the last token (prefill for
+ * hla2_decode_step).
+ */
+int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
+                 int d, int dv, const float* gamma, int normalize, int chunk,
+                 hla2_stream_t stream, const hla2_opts* opts);
+
+/* Scratch bytes hla2_backward needs; (size_t)-1 for rejected arguments. */
+size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype);
+
+/*
+ * Reverse-mode chunk scan (section summary §4.2: gradients equal to those of the
+ * serial recurrence) of the UNNORMALISED forward: given dout = dL/dout, writes
+ * dq, dk, dv.  normalize != 0 returns HLA2_ERR_UNSUPPORTED.  init_state and
+ * final_state in opts must be NULL (gradients start from the empty state).
+ */
+int hla2_backward(const void* q, const void* k, const void* v, const void* dout, void* dq,
+                  void* dk, void* dv_out, int B, int H, int n, int d, int dv,
+                  const float* gamma, int normalize, int chunk, hla2_stream_t stream,
+                  const hla2_opts* opts);
+
+/*
+ * One streaming decode step for N*H independent heads (section summary §3.1: online
+ * updates at O(d^2 + d dv) per token, constant state).  state [N, H] packed float32
+ * blocks, updated in place; q, k [N, H, d]; v, out [N, H, dv].  The cross summaries
+ * G, h are advanced from the pre-update C, m; the output uses the updated state.
+ * opts may be NULL (then dtype = HLA2_BF16, eps = 1e-6); no workspace is used.
+ */
+int hla2_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
+                     int N, int H, int d, int dv, const float* gamma, int normalize,
+                     hla2_stream_t stream, const hla2_opts* opts);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HLA2_H_ */
