@@ -1,0 +1,360 @@
+#!/usr/bin/env python
+"""Benchmark of the masked HLA-2 forward on the long-context workload.
+
+Workload: B=1, H=16, n=65536, d=dv=64, bf16 inputs, fp32 state, unnormalised, per-head
+decay linspace(0.99, 0.9999), chunk width 64 (1,048,576 tokens per step; 536.9 MB of
+algorithmic traffic, larger than the 129 MB L2, so no flush is needed between steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own replica
+of the workload (weak scaling, no collective in the data path); the timed region is
+bracketed by barriers and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "HLA-2 masked fwd tokens/s (B·H·n/s) at n=64K,d=64; % tensor/HBM roofline"
+WORKLOAD = "long"
+CONFIG_NAME = ("long-context masked HLA-2 forward: B=1 H=16 n=65536 d=dv=64 bf16 in/out, "
+               "fp32 state, decay linspace(0.99,0.9999), unnormalised, chunk 64")
+PHASES = ("carry_init", "segment_summaries", "segment_scan", "output_pass", "final_state")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------
+# distributed plumbing (control plane only)
+# ---------------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self, backend):
+        import torch
+        import torch.distributed as dist
+        self.dist = dist
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.on = self.world > 1
+        if self.on:
+            dist.init_process_group(backend=backend)
+        self.torch = torch
+
+    def barrier(self):
+        if self.on:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.on:
+            return x
+        t = self.torch.tensor([x], dtype=self.torch.float64,
+                              device="cuda" if self.dist.get_backend() == "nccl" else "cpu")
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.on:
+            self.dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.fh = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t_begin, t_end):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.flush()
+        self.fh.seek(0)
+        rows = [r.strip().split(",") for r in self.fh.read().splitlines() if r.strip()]
+        os.unlink(self.fh.name)
+        if not rows:
+            return None
+        # nvidia-smi prints at a fixed period; map rows to wall time linearly
+        n = len(rows)
+        span = max(t_end, time.time()) - self.t0
+        times = [self.t0 + span * (i + 0.5) / n for i in range(n)]
+        inside = [r for r, t in zip(rows, times) if t_begin <= t <= t_end] or rows[-3:]
+        sm = [float(r[1]) for r in inside if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in inside if r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in inside:
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------------
+# CPU oracle timing (baseline / reference arm)
+# ---------------------------------------------------------------------------------
+
+def oracle_sample(target_s: float):
+    """Time the float64 C oracle on the first n_s tokens of every head of the workload,
+    n_s sized for about ``target_s`` seconds.  Returns (tokens/s, cores, description)."""
+    import torch
+
+    from chunked_scan_mixer_gb300 import inputs
+    from oracle import cref
+
+    w = inputs.WORKLOADS[WORKLOAD]
+    cref.build()
+    g = inputs.gammas(w).double().numpy()
+    probe = 512
+    x = inputs.make(w, n=probe)
+    f = lambda t: t.to(torch.float32).numpy()  # noqa: E731
+    t = time.perf_counter()
+    cref.forward(f(x["q"]), f(x["k"]), f(x["v"]), g)
+    rate = w.B * w.H * probe / (time.perf_counter() - t)
+    n_s = int(min(w.n, max(probe, rate * target_s / (w.B * w.H))))
+    x = inputs.make(w, n=n_s)
+    q, k, v = f(x["q"]), f(x["k"]), f(x["v"])
+    t = time.perf_counter()
+    cref.forward(q, k, v, g)
+    dt = time.perf_counter() - t
+    tokens = w.B * w.H * n_s
+    desc = (f"float64 C serial recurrence (OpenMP over heads) on the first {n_s} tokens of all "
+            f"{w.B * w.H} heads ({tokens} tokens, {dt:.1f} s)")
+    return tokens / dt, cref.threads(), desc
+
+
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        return
+    from oracle import cref
+
+    cref.build()
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        value, cores, desc = oracle_sample(target_s=2.0)
+        if i >= args.warmup:
+            per_step.append(value)
+    value = statistics.median(per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": CONFIG_NAME, "B": 1, "H": 16, "n": 65536, "d": 64, "dv": 64, "chunk": 64},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------
+# our CUDA path
+# ---------------------------------------------------------------------------------
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for rel in ("chunked_scan_mixer_gb300/csrc/fwd_chunk_mma.cuh", "chunked_scan_mixer_gb300/csrc/common.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, if it matches today's source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(kernel)
+    if not ent or ent.get("source_sha") != kernel_source_sha():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+def run_ours(args, dist: Dist):
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    torch.cuda.set_device(dist.local)
+    dev = torch.device("cuda", dist.local)
+    w = inputs.WORKLOADS[WORKLOAD]
+    tokens = w.B * w.H * w.n
+    x = inputs.make(w, device=dev, seed=w.seed + 1000 * dist.rank)
+    q, k, v = x["q"], x["k"], x["v"]
+    gamma = x["gamma"].to(dev)
+    out = torch.empty_like(v)
+    nseg, seg_chunks, launches = hla.forward_plan(w.B, w.H, w.n, w.d, w.dv, w.chunk)
+
+    def step(evs=None):
+        hla.forward(q, k, v, gamma=gamma, chunk=w.chunk, out=out, phase_events=evs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for e in evs:  # create the CUDA events outside the timed region
+        for ev in e:
+            ev.record()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record()
+    for i in range(K):
+        step(evs[i])
+    t_end.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    dist.barrier()
+    clk = clocks.stop(wall0, wall1)
+    ms_total = dist.max(t_start.elapsed_time(t_end))
+    ms_per_step = ms_total / K
+    value = dist.world * tokens / (ms_per_step * 1e-3)
+
+    # per-phase device time (events on the launching stream)
+    ph = {name: 0.0 for name in PHASES}
+    for e in evs:
+        for j, name in enumerate(PHASES):
+            ph[name] += e[j].elapsed_time(e[j + 1])
+    ph = {name: t / K for name, t in ph.items()}
+
+    hbm_gbs, bf16_tflops, peak_kind = peaks()
+    # algorithmic bytes per launch: q, k, v read (bf16) and out written (bf16) for the
+    # tokens the launch processes
+    out_bytes = tokens * (2 * w.d + w.dv) * 2 + tokens * w.dv * 2
+    summary_tokens = w.B * w.H * min(w.n, (nseg - 1) * seg_chunks * w.chunk)
+    summ_bytes = summary_tokens * (2 * w.d + w.dv) * 2
+    if ph["output_pass"] >= ph["segment_summaries"]:
+        kname, kbytes, kms = "output_pass", out_bytes, ph["output_pass"]
+    else:
+        kname, kbytes, kms = "segment_summaries", summ_bytes, ph["segment_summaries"]
+    achieved = kbytes / (kms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved / hbm_gbs, "traffic": recorded_traffic(kname),
+                "kernel": kname, "peak_source": peak_kind,
+                "algorithmic_bytes_per_launch": kbytes, "ms_per_launch": kms}
+    # whole-step fractions against both roofs (flops of the method at chunk 64)
+    flops_per_token = 98304
+    step_bytes = out_bytes
+    whole = {"hbm_frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm_gbs,
+             "tensor_frac": tokens * flops_per_token / (ms_per_step * 1e-3) / 1e12 / bf16_tflops,
+             "roofline_time_us": max(step_bytes / (hbm_gbs * 1e9), tokens * flops_per_token / (bf16_tflops * 1e12)) * 1e6}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (t.to("cpu").pin_memory() for t in (q, k, v))
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        Ke = max(3, min(K, 50))
+        for _ in range(2):
+            hla.forward(qh, kh, vh, gamma=gamma, chunk=w.chunk, out=oh)
+        torch.cuda.synchronize()
+        dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(Ke):
+            hla.forward(qh, kh, vh, gamma=gamma, chunk=w.chunk, out=oh)
+        torch.cuda.synchronize()
+        dt = dist.max(time.perf_counter() - t0) / Ke
+        e2e = {"value": dist.world * tokens / dt, "unit": "tokens/s",
+               "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
+               "d2h_bytes_per_step": out.numel() * out.element_size(), "steps": Ke}
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        val, cores, desc = oracle_sample(target_s=15.0)
+        cpu = {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": CONFIG_NAME, "B": w.B, "H": w.H, "n": w.n, "d": w.d, "dv": w.dv,
+                       "chunk": w.chunk, "segments_per_head": nseg, "chunks_per_segment": seg_chunks,
+                       "l2": "inputs (402.7 MB) + output (134.2 MB) exceed the 129 MB L2; no flush"},
+            "roofline": roofline, "whole_step": whole, "phases_ms": ph, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches * K, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    dist = Dist("gloo" if args.impl == "reference" else "nccl")
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,332 @@
+// C ABI of the HLA-2 library: argument checks, segmentation plan, kernel dispatch.
+// The declarations and their documentation are in include/hla2.h.
+#include <math.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include <string>
+
+#include "kernels.h"
+
+namespace hla2 {
+int launch_fwd_chunk_mma_d16(const ChunkArgs&, int, bool, bool, cudaStream_t);
+int launch_fwd_chunk_mma_d32(const ChunkArgs&, int, bool, bool, cudaStream_t);
+int launch_fwd_chunk_mma_d64(const ChunkArgs&, int, bool, bool, cudaStream_t);
+int launch_fwd_chunk_mma_d128(const ChunkArgs&, int, bool, bool, cudaStream_t);
+size_t fwd_chunk_mma_smem_d16(int, bool);
+size_t fwd_chunk_mma_smem_d32(int, bool);
+size_t fwd_chunk_mma_smem_d64(int, bool);
+size_t fwd_chunk_mma_smem_d128(int, bool);
+
+int launch_fwd_chunk_mma(const ChunkArgs& a, int d, int dv, int W, bool summary, bool cm,
+                         cudaStream_t st) {
+    if (d != dv) return -2;
+    switch (d) {
+        case 16: return launch_fwd_chunk_mma_d16(a, W, summary, cm, st);
+        case 32: return launch_fwd_chunk_mma_d32(a, W, summary, cm, st);
+        case 64: return launch_fwd_chunk_mma_d64(a, W, summary, cm, st);
+        case 128: return launch_fwd_chunk_mma_d128(a, W, summary, cm, st);
+        default: return -2;
+    }
+}
+
+size_t fwd_chunk_mma_smem(int d, int dv, int W, bool cm) {
+    if (d != dv) return 0;
+    switch (d) {
+        case 16: return fwd_chunk_mma_smem_d16(W, cm);
+        case 32: return fwd_chunk_mma_smem_d32(W, cm);
+        case 64: return fwd_chunk_mma_smem_d64(W, cm);
+        case 128: return fwd_chunk_mma_smem_d128(W, cm);
+        default: return 0;
+    }
+}
+}  // namespace hla2
+
+using namespace hla2;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+int succeed() {
+    g_last_error.clear();
+    return HLA2_OK;
+}
+
+int cuda_fail(const char* what) {
+    const cudaError_t e = cudaGetLastError();
+    return fail(HLA2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool dim_ok(int x) { return x == 16 || x == 32 || x == 64 || x == 128; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DevInfo {
+    int sms = 152;             // GB300 when no device can be queried
+    int smem_optin = 232448;   // 227 KB
+};
+
+DevInfo dev_info() {
+    DevInfo di;
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return di;
+    }
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        di.sms = v;
+    else
+        cudaGetLastError();
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess)
+        di.smem_optin = v;
+    else
+        cudaGetLastError();
+    return di;
+}
+
+// Cut each head's chunks into segments so that the summary and output passes have
+// about two CTAs per SM in total.
+Plan make_plan(int B, int H, int n, int d, int dv, int W, int sms) {
+    Plan p;
+    p.BH = B * H;
+    p.H = H;
+    p.n = n;
+    p.d = d;
+    p.dv = dv;
+    p.W = W;
+    p.nchunks = (n + W - 1) / W;
+    if (p.nchunks == 0 || p.BH == 0) {
+        p.seg_chunks = 1;
+        p.nseg = 0;
+        return p;
+    }
+    const long target = 2L * sms;
+    long per_head = (target + p.BH - 1) / p.BH;
+    if (per_head < 1) per_head = 1;
+    if (per_head > p.nchunks) per_head = p.nchunks;
+    p.seg_chunks = (int)((p.nchunks + per_head - 1) / per_head);
+    p.nseg = (p.nchunks + p.seg_chunks - 1) / p.seg_chunks;
+    return p;
+}
+
+enum class Path { kMma, kSimt, kNone };
+
+Path choose_forward_path(int dtype, int d, int dv, int W, const DevInfo& di) {
+    if (dtype == HLA2_BF16) {
+        const size_t s = fwd_chunk_mma_smem(d, dv, W, true);
+        if (s > 0 && s <= (size_t)di.smem_optin) return Path::kMma;
+    }
+    if (fwd_chunk_simt_smem(d, dv, W, true) <= (size_t)di.smem_optin) return Path::kSimt;
+    return Path::kNone;
+}
+
+int check_common(int B, int H, int n, int d, int dv, int dtype, int normalize) {
+    if (B < 0 || H < 0 || n < 0) return fail(HLA2_ERR_INVALID_ARG, "B, H, n must be >= 0 (got %d, %d, %d)", B, H, n);
+    if ((long)B * H > (1L << 30)) return fail(HLA2_ERR_INVALID_ARG, "B*H too large");
+    if (!dim_ok(d) || !dim_ok(dv))
+        return fail(HLA2_ERR_INVALID_ARG, "d and dv must be 16, 32, 64 or 128 (got %d, %d)", d, dv);
+    if (dtype != HLA2_F32 && dtype != HLA2_BF16) return fail(HLA2_ERR_INVALID_ARG, "dtype must be HLA2_F32 or HLA2_BF16");
+    if (normalize != 0 && normalize != 1) return fail(HLA2_ERR_INVALID_ARG, "normalize must be 0 or 1");
+    return HLA2_OK;
+}
+
+size_t forward_ws(const Plan& p) { return p.nseg > 0 ? fwd_layout(p).total * sizeof(float) : 0; }
+
+}  // namespace
+
+extern "C" {
+
+int hla2_version(void) { return 100; }
+
+const char* hla2_last_error(void) { return g_last_error.c_str(); }
+
+size_t hla2_state_floats(int d, int dv) { return raw_state_floats(d, dv); }
+
+size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
+                                    int normalize, int want_final_state) {
+    (void)want_final_state;
+    if (check_common(B, H, n, d, dv, dtype, normalize) != HLA2_OK || !dim_ok(chunk)) return (size_t)-1;
+    const DevInfo di = dev_info();
+    return forward_ws(make_plan(B, H, n, d, dv, chunk, di.sms));
+}
+
+int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
+                 int d, int dv, const float* gamma, int normalize, int chunk, hla2_stream_t stream,
+                 const hla2_opts* opts) {
+    if (!opts) return fail(HLA2_ERR_INVALID_ARG, "opts must not be NULL");
+    int rc = check_common(B, H, n, d, dv, opts->dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
+    if (normalize && !isfinite(opts->eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
+    const long BH = (long)B * H;
+    const bool want_final = opts->final_state != nullptr;
+    if ((opts->init_state && !aligned16(opts->init_state)) || (want_final && !aligned16(opts->final_state)))
+        return fail(HLA2_ERR_INVALID_ARG, "init_state / final_state must be 16-byte aligned");
+    if (BH == 0) return succeed();
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t sf = raw_state_floats(d, dv);
+    if (n == 0) {
+        // no tokens: the final state is the initial one (or the empty prefix)
+        if (want_final) {
+            cudaError_t e = opts->init_state
+                                ? cudaMemcpyAsync(opts->final_state, opts->init_state, BH * sf * sizeof(float),
+                                                  cudaMemcpyDeviceToDevice, st)
+                                : cudaMemsetAsync(opts->final_state, 0, BH * sf * sizeof(float), st);
+            if (e != cudaSuccess) return cuda_fail("final state copy");
+        }
+        return succeed();
+    }
+    if (!q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must not be NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
+
+    const DevInfo di = dev_info();
+    const Path path = choose_forward_path(opts->dtype, d, dv, chunk, di);
+    if (path == Path::kNone)
+        return fail(HLA2_ERR_UNSUPPORTED, "no kernel for dtype %d, d %d, dv %d, chunk %d", opts->dtype, d, dv, chunk);
+    const Plan p = make_plan(B, H, n, d, dv, chunk, di.sms);
+    const FwdLayout L = fwd_layout(p);
+    const size_t need = L.total * sizeof(float);
+    if (!opts->workspace || opts->workspace_bytes < need)
+        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
+                    opts->workspace ? opts->workspace_bytes : (size_t)0);
+    if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+
+    ChunkArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.BH = (int)BH;
+    a.H = H;
+    a.n = n;
+    a.W = chunk;
+    a.nchunks = p.nchunks;
+    a.seg_chunks = p.seg_chunks;
+    a.nseg = p.nseg;
+    a.gamma = gamma;
+    a.normalize = normalize;
+    a.eps = opts->eps;
+    a.want_final = want_final ? 1 : 0;
+    a.ws = static_cast<float*>(opts->workspace);
+    a.L = L;
+
+    const bool bf = opts->dtype == HLA2_BF16;
+    auto chunk_pass = [&](int seg0, int count, bool summary, bool cm) -> int {
+        ChunkArgs b = a;
+        b.seg0 = seg0;
+        b.nseg_launch = count;
+        if (path == Path::kMma) return launch_fwd_chunk_mma(b, d, dv, chunk, summary, cm, st);
+        return launch_fwd_chunk_simt(b, d, dv, chunk, summary, cm, bf, st);
+    };
+
+    auto mark = [&](int i) {
+        if (opts->phase_events && i < opts->n_phase_events && opts->phase_events[i] &&
+            cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[i]), st) != cudaSuccess)
+            cudaGetLastError();  // a bad profiling handle must not fail the computation
+    };
+    cudaGetLastError();  // launch errors below are ours
+    mark(0);
+    if (launch_init_carry(a, d, dv, opts->init_state, st)) return cuda_fail("carry-in initialisation");
+    mark(1);
+    if (p.nseg > 1) {
+        const int steps = p.nseg - 1, seg_tokens = p.seg_chunks * chunk;
+        const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
+        if (chunk_pass(0, steps, true, true)) return cuda_fail("segment summaries");
+        mark(2);
+        if (launch_linear_scan(a.ws + L.SB, a.ws + L.Sin, a.BH, H, steps, dd, steps * dd, p.nseg * dd, true,
+                               gamma, seg_tokens, 1, st))
+            return cuda_fail("key-moment scan");
+        if (want_final) {
+            if (launch_linear_scan(a.ws + L.CB, a.ws + L.Clast, a.BH, H, steps, ddv, steps * ddv, ddv, false,
+                                   gamma, seg_tokens, 1, st) ||
+                launch_linear_scan(a.ws + L.mB, a.ws + L.mlast, a.BH, H, steps, d, steps * (size_t)d, d, false,
+                                   gamma, seg_tokens, 1, st))
+                return cuda_fail("query-value scan");
+        }
+        if (launch_cross(a, d, dv, st)) return cuda_fail("cross terms");
+        if (launch_linear_scan(a.ws + L.ZB, a.ws + L.Zin, a.BH, H, steps, ddv, steps * ddv, p.nseg * ddv, true,
+                               gamma, seg_tokens, 2, st) ||
+            launch_linear_scan(a.ws + L.yB, a.ws + L.yin, a.BH, H, steps, d, steps * (size_t)d, p.nseg * (size_t)d,
+                               true, gamma, seg_tokens, 2, st))
+            return cuda_fail("masked-summary scan");
+    } else {
+        mark(2);
+    }
+    mark(3);
+    if (want_final && p.nseg > 1) {
+        if (chunk_pass(0, p.nseg - 1, false, false) || chunk_pass(p.nseg - 1, 1, false, true))
+            return cuda_fail("output pass");
+    } else {
+        if (chunk_pass(0, p.nseg, false, want_final)) return cuda_fail("output pass");
+    }
+    mark(4);
+    if (want_final && launch_finalize(a, d, dv, opts->final_state, st)) return cuda_fail("final state");
+    mark(5);
+    return succeed();
+}
+
+int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, int want_final_state,
+                      int* nseg, int* seg_chunks, int* launches) {
+    int rc = check_common(B, H, n, d, dv, dtype, 0);
+    if (rc != HLA2_OK) return rc;
+    if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
+    const Plan p = make_plan(B, H, n, d, dv, chunk, dev_info().sms);
+    int l = 0;
+    if (p.nseg > 0) {
+        l = 2;                                                   // carry-in, output pass
+        if (p.nseg > 1) l += 5 + (want_final_state ? 2 : 0);     // summary, scans, cross
+        if (want_final_state) l += 1 + (p.nseg > 1 ? 1 : 0);     // finalize, last-segment pass
+    } else if (want_final_state && (long)B * H > 0) {
+        l = 0;                                                   // a copy or memset only
+    }
+    if (nseg) *nseg = p.nseg;
+    if (seg_chunks) *seg_chunks = p.seg_chunks;
+    if (launches) *launches = l;
+    return succeed();
+}
+
+size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype) {
+    (void)B, (void)H, (void)n, (void)d, (void)dv, (void)chunk, (void)dtype;
+    return (size_t)-1;
+}
+
+int hla2_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
+                  void* dv_out, int B, int H, int n, int d, int dv, const float* gamma, int normalize,
+                  int chunk, hla2_stream_t stream, const hla2_opts* opts) {
+    (void)q, (void)k, (void)v, (void)dout, (void)dq, (void)dk, (void)dv_out, (void)B, (void)H, (void)n;
+    (void)d, (void)dv, (void)gamma, (void)normalize, (void)chunk, (void)stream, (void)opts;
+    return fail(HLA2_ERR_UNSUPPORTED, "backward is not available in this build");
+}
+
+int hla2_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
+                     int d, int dv, const float* gamma, int normalize, hla2_stream_t stream,
+                     const hla2_opts* opts) {
+    const int dtype = opts ? opts->dtype : HLA2_BF16;
+    const float eps = opts ? opts->eps : 1e-6f;
+    int rc = check_common(N, H, 0, d, dv, dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (normalize && !isfinite(eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
+    if ((long)N * H == 0) return succeed();
+    if (!state || !q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "state, q, k, v, out must not be NULL");
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(HLA2_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    cudaGetLastError();
+    if (launch_decode_step(state, q, k, v, out, N, H, d, dv, gamma, normalize, eps, dtype == HLA2_BF16,
+                           reinterpret_cast<cudaStream_t>(stream)))
+        return cuda_fail("decode step");
+    return succeed();
+}
+
+}  // extern "C"

@@ -1,0 +1,220 @@
+// Single-token streaming decode step of masked HLA-2 (page "Higher-order Linear
+// Attention", section summary §3.1: online updates at O(d^2 + d dv) per token with a
+// constant-size state; technical summary item "1. Zweite Ordnung HLA").
+//
+// One CTA per head.  The state (S, C, G, m, h) is read and written exactly once, in
+// three passes that each stream one matrix with 128-bit accesses:
+//   pass S:  S' = g S + k k^T,                 u = S' q
+//   pass C:  r = C^T k (old C),  C' = g C + q v^T,   w = C'^T u
+//   pass G:  G' = g^2 G + g k r^T,             z = G'^T q
+//   out = w - z  (= q^T (S' C' - G')),  den = u . m' - q . h'
+// with m' = g m + q and h' = g^2 h + g k (k . m).  G and h use the pre-update C, m.
+#include "kernels.h"
+
+namespace hla2 {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxDim = 128;
+
+__device__ __forceinline__ float4 ld_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ void st_stream(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
+
+__device__ __forceinline__ float block_sum(float x, float* red) {
+    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += red[w];
+    return s;
+}
+
+// Column sums of a d x dv pass: each thread holds partial sums for 4 columns
+// (column group tid % (dv/4)); combine threads that share a column group.
+__device__ __forceinline__ void column_reduce(float4 p, int dv, float* red /*[kWarps][kMaxDim]*/,
+                                              float* result /*[dv]*/) {
+    const int lpc = dv / 4;  // lanes per row (<= 32, power of two)
+    for (int o = lpc; o < 32; o <<= 1) {
+        p.x += __shfl_xor_sync(0xffffffffu, p.x, o);
+        p.y += __shfl_xor_sync(0xffffffffu, p.y, o);
+        p.z += __shfl_xor_sync(0xffffffffu, p.z, o);
+        p.w += __shfl_xor_sync(0xffffffffu, p.w, o);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane < lpc) *reinterpret_cast<float4*>(&red[warp * kMaxDim + lane * 4]) = p;
+    __syncthreads();
+    for (int c = threadIdx.x; c < dv; c += kThreads) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += red[w * kMaxDim + c];
+        result[c] = s;
+    }
+    __syncthreads();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    decode_step_kernel(float* __restrict__ state, const T* __restrict__ q, const T* __restrict__ k,
+                       const T* __restrict__ v, T* __restrict__ out, int H, int d, int dv,
+                       const float* __restrict__ gamma, int normalize, float eps) {
+    __shared__ __align__(16) float qs[kMaxDim], ks[kMaxDim], vs[kMaxDim], us[kMaxDim];
+    __shared__ __align__(16) float rs[kMaxDim], ws[kMaxDim], zs[kMaxDim];
+    __shared__ __align__(16) float red[kWarps * kMaxDim];
+    const int head = blockIdx.x, tid = threadIdx.x;
+    const float g = head_decay(gamma, head, H), g2 = g * g;
+    float* S = state + (size_t)head * raw_state_floats(d, dv);
+    const PackOff po = pack_off(d, dv);
+    float *C = S + po.C, *G = S + po.G, *m = S + po.m, *hh = S + po.h;
+
+    for (int i = tid; i < d; i += kThreads) {
+        qs[i] = to_f32(q[(size_t)head * d + i]);
+        ks[i] = to_f32(k[(size_t)head * d + i]);
+    }
+    for (int i = tid; i < dv; i += kThreads) vs[i] = to_f32(v[(size_t)head * dv + i]);
+    __syncthreads();
+
+    // m' = g m + q;  h' = g^2 h + g k (k . m_old)
+    float km = 0.f;
+    for (int i = tid; i < d; i += kThreads) km += ks[i] * m[i];
+    km = block_sum(km, red);
+    float mh_dot = 0.f;  // this thread's part of u . m' - q . h', formed after pass S
+
+    // ---- pass S ----------------------------------------------------------------------
+    {
+        const int lpr = d / 4;               // lanes per row
+        const int n4 = d * d / 4;
+        for (int base = 0; base < n4; base += kThreads * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = base + u * kThreads + tid;
+                if (i < n4) x[u] = ld_stream(S + (size_t)i * 4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = base + u * kThreads + tid;
+                float part = 0.f;
+                const int a = (i * 4) / d, c = (i * 4) % d;
+                if (i < n4) {
+                    const float ka = ks[a];
+                    float4 y = x[u];
+                    y.x = g * y.x + ka * ks[c + 0];
+                    y.y = g * y.y + ka * ks[c + 1];
+                    y.z = g * y.z + ka * ks[c + 2];
+                    y.w = g * y.w + ka * ks[c + 3];
+                    st_stream(S + (size_t)i * 4, y);
+                    part = y.x * qs[c] + y.y * qs[c + 1] + y.z * qs[c + 2] + y.w * qs[c + 3];
+                }
+                // all lanes of a row group take part (rows are aligned to lpr lanes)
+                for (int o = lpr >> 1; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (i < n4 && (i % lpr) == 0) us[a] = part;
+            }
+        }
+    }
+    __syncthreads();
+
+    // m, h and the denominator's vector terms
+    for (int i = tid; i < d; i += kThreads) {
+        const float mn = g * m[i] + qs[i];
+        const float hn = g2 * hh[i] + g * ks[i] * km;
+        m[i] = mn;
+        hh[i] = hn;
+        mh_dot += us[i] * mn - qs[i] * hn;
+    }
+
+    // ---- pass C ------------------------------------------------------------------------
+    {
+        const int lpc = dv / 4;
+        const int rows_per = kThreads / lpc;
+        const int c4 = (tid % lpc) * 4;
+        float4 pr = make_float4(0.f, 0.f, 0.f, 0.f), pw = pr;
+        for (int a0 = tid / lpc; a0 < d; a0 += rows_per * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a < d) x[u] = ld_stream(C + (size_t)a * dv + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a >= d) continue;
+                const float ka = ks[a], qa = qs[a], ua = us[a];
+                float4 y = x[u];
+                pr.x += ka * y.x; pr.y += ka * y.y; pr.z += ka * y.z; pr.w += ka * y.w;
+                y.x = g * y.x + qa * vs[c4 + 0];
+                y.y = g * y.y + qa * vs[c4 + 1];
+                y.z = g * y.z + qa * vs[c4 + 2];
+                y.w = g * y.w + qa * vs[c4 + 3];
+                pw.x += ua * y.x; pw.y += ua * y.y; pw.z += ua * y.z; pw.w += ua * y.w;
+                st_stream(C + (size_t)a * dv + c4, y);
+            }
+        }
+        column_reduce(pr, dv, red, rs);
+        column_reduce(pw, dv, red, ws);
+    }
+
+    // ---- pass G ------------------------------------------------------------------------
+    {
+        const int lpc = dv / 4;
+        const int rows_per = kThreads / lpc;
+        const int c4 = (tid % lpc) * 4;
+        float4 pz = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 r4 = *reinterpret_cast<const float4*>(&rs[c4]);
+        for (int a0 = tid / lpc; a0 < d; a0 += rows_per * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a < d) x[u] = ld_stream(G + (size_t)a * dv + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a >= d) continue;
+                const float gk = g * ks[a], qa = qs[a];
+                float4 y = x[u];
+                y.x = g2 * y.x + gk * r4.x;
+                y.y = g2 * y.y + gk * r4.y;
+                y.z = g2 * y.z + gk * r4.z;
+                y.w = g2 * y.w + gk * r4.w;
+                pz.x += qa * y.x; pz.y += qa * y.y; pz.z += qa * y.z; pz.w += qa * y.w;
+                st_stream(G + (size_t)a * dv + c4, y);
+            }
+        }
+        column_reduce(pz, dv, red, zs);
+    }
+
+    float inv = 1.f;
+    if (normalize) {
+        const float den = block_sum(mh_dot, red);
+        inv = 1.f / (den + eps);
+    }
+    for (int e = tid; e < dv; e += kThreads)
+        out[(size_t)head * dv + e] = from_f32<T>((ws[e] - zs[e]) * inv);
+}
+
+}  // namespace
+
+int launch_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
+                       int N, int H, int d, int dv, const float* gamma, int normalize, float eps,
+                       bool is_bf16, cudaStream_t st) {
+    const long heads = (long)N * H;
+    if (heads <= 0) return 0;
+    if (is_bf16)
+        decode_step_kernel<bf16><<<(unsigned)heads, kThreads, 0, st>>>(
+            state, static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
+            static_cast<bf16*>(out), H, d, dv, gamma, normalize, eps);
+    else
+        decode_step_kernel<float><<<(unsigned)heads, kThreads, 0, st>>>(
+            state, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+            static_cast<float*>(out), H, d, dv, gamma, normalize, eps);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace hla2

@@ -1,0 +1,24 @@
+// Instantiations of the tensor-core chunk kernel for d = dv = 128.
+#include "fwd_chunk_mma.cuh"
+
+namespace hla2 {
+
+int launch_fwd_chunk_mma_d128(const ChunkArgs& a, int W, bool summary, bool cm, cudaStream_t st) {
+    switch (W) {
+        case 16: return launch_fwd_chunk_mma_t<128, 128, 16>(a, summary, cm, st);
+        case 32: return launch_fwd_chunk_mma_t<128, 128, 32>(a, summary, cm, st);
+        case 64: return launch_fwd_chunk_mma_t<128, 128, 64>(a, summary, cm, st);
+        default: return -2;
+    }
+}
+
+size_t fwd_chunk_mma_smem_d128(int W, bool cm) {
+    switch (W) {
+        case 16: return fwd_chunk_mma_smem_t<128, 128, 16>(cm);
+        case 32: return fwd_chunk_mma_smem_t<128, 128, 32>(cm);
+        case 64: return fwd_chunk_mma_smem_t<128, 128, 64>(cm);
+        default: return 0;
+    }
+}
+
+}  // namespace hla2

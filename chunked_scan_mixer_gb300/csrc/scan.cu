@@ -1,0 +1,190 @@
+// Inter-segment scan of the masked HLA-2 forward (float32).
+//
+// Segment summaries (S_B, C_B, Z_B, m_B, y_B) of consecutive segments A (earlier)
+// and B combine with the masked semidirect product (page "Higher-order Linear
+// Attention", section summary §4.2, §4.3; technical summary item "4. Paralleles
+// Training durch assoziative Scans", cross term S^K_B C^QV_A).  In the (S, C, m, Z, y)
+// coordinates used on the GPU (Z = S C - G, y = S m - h) the combine with
+// rho = g^len(B) reads
+//     S = rho S_A + S_B,   C = rho C_A + C_B,   m = rho m_A + m_B,
+//     Z = rho^2 Z_A + Z_B + rho S_A C_B,   y = rho^2 y_A + y_B + rho S_A m_B,
+// (the pairs with key in A and value in B are kept by the mask).  The exclusive scan
+// over segments therefore splits into
+//   1. a decayed prefix sum of S (elementwise, linear_scan_kernel),
+//   2. independent products X_s = Z_B[s] + rho S_in[s] C_B[s] (cross_kernel),
+//   3. a decayed (rho^2) prefix sum of X (linear_scan_kernel again).
+#include "kernels.h"
+
+namespace hla2 {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// Carry into segment 0 from the optional packed initial state (S, C, G, m, h):
+// Z0 = S0 C0 - G0 and y0 = S0 m0 - h0; zero without an initial state.
+__global__ void __launch_bounds__(kThreads)
+    init_carry_kernel(const ChunkArgs a, int D, int DV, const float* init) {
+    const int bh = blockIdx.x, tid = threadIdx.x;
+    const size_t s0 = (size_t)bh * a.nseg;  // segment 0 of this head
+    float* Sin = a.ws + a.L.Sin + s0 * D * D;
+    float* Zin = a.ws + a.L.Zin + s0 * D * DV;
+    float* yin = a.ws + a.L.yin + s0 * D;
+    float* Cl = a.ws + a.L.Clast + (size_t)bh * D * DV;
+    float* ml = a.ws + a.L.mlast + (size_t)bh * D;
+    if (!init) {
+        for (int i = tid; i < D * D; i += kThreads) Sin[i] = 0.f;
+        for (int i = tid; i < D * DV; i += kThreads) Zin[i] = Cl[i] = 0.f;
+        for (int i = tid; i < D; i += kThreads) yin[i] = ml[i] = 0.f;
+        return;
+    }
+    const PackOff po = pack_off(D, DV);
+    const float* st = init + (size_t)bh * (size_t)raw_state_floats(D, DV);
+    const float *S0 = st + po.S, *C0 = st + po.C, *G0 = st + po.G, *m0 = st + po.m, *h0 = st + po.h;
+    for (int i = tid; i < D * D; i += kThreads) Sin[i] = S0[i];
+    for (int i = tid; i < D * DV; i += kThreads) {
+        const int r = i / DV, c = i % DV;
+        float s = 0.f;
+        for (int x = 0; x < D; ++x) s += S0[r * D + x] * C0[x * DV + c];
+        Zin[i] = s - G0[i];
+        Cl[i] = C0[i];
+    }
+    for (int r = tid; r < D; r += kThreads) {
+        float s = 0.f;
+        for (int x = 0; x < D; ++x) s += S0[r * D + x] * m0[x];
+        yin[r] = s - h0[r];
+        ml[r] = m0[r];
+    }
+}
+
+// Decayed prefix over segments, one thread per element:
+//   acc_0 = dst[head][0][e];  acc_{s+1} = rho_h^power acc_s + src[head][s][e]
+// with rho_h = g_h^step_tokens.  store_all writes every acc_s (s >= 1) to
+// dst[head][s][e]; otherwise only the last one to dst[head][0][e].
+__global__ void __launch_bounds__(kThreads)
+    linear_scan_kernel(const float* __restrict__ src, float* __restrict__ dst, int BH, int H,
+                       int nsteps, size_t E, size_t src_hs, size_t dst_hs, int store_all,
+                       const float* gamma, int step_tokens, int power) {
+    const size_t gid = (size_t)blockIdx.x * kThreads + threadIdx.x;
+    if (gid >= (size_t)BH * E) return;
+    const int bh = (int)(gid / E);
+    const size_t e = gid % E;
+    const float rho = pow_decay(log2f(head_decay(gamma, bh, H)), (float)step_tokens * (float)power);
+    const float* s = src + (size_t)bh * src_hs + e;
+    float* d = dst + (size_t)bh * dst_hs + e;
+    float acc = d[0];
+    constexpr int U = 8;
+    int t = 0;
+    for (; t + U <= nsteps; t += U) {
+        float x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) x[u] = s[(size_t)(t + u) * E];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            acc = rho * acc + x[u];
+            if (store_all) d[(size_t)(t + u + 1) * E] = acc;
+        }
+    }
+    for (; t < nsteps; ++t) {
+        acc = rho * acc + s[(size_t)t * E];
+        if (store_all) d[(size_t)(t + 1) * E] = acc;
+    }
+    if (!store_all) d[0] = acc;
+}
+
+// X_s = Z_B[s] + rho S_in[s] C_B[s] and Xy_s = y_B[s] + rho S_in[s] m_B[s], in place.
+__global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int D, int DV, int seg_tokens) {
+    extern __shared__ __align__(16) float sm[];
+    float* Ss = sm;                 // D x D
+    float* Cs = sm + (size_t)D * D; // D x DV
+    float* ms = Cs + (size_t)D * DV;
+    const int s = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+    const size_t sb = (size_t)bh * (a.nseg - 1) + s;  // summary index
+    const size_t si = (size_t)bh * a.nseg + s;        // carry index
+    const float* Sin = a.ws + a.L.Sin + si * D * D;
+    const float* CB = a.ws + a.L.CB + sb * D * DV;
+    const float* mB = a.ws + a.L.mB + sb * D;
+    float* ZB = a.ws + a.L.ZB + sb * D * DV;
+    float* yB = a.ws + a.L.yB + sb * D;
+    for (int i = tid; i < D * D; i += kThreads) Ss[i] = Sin[i];
+    for (int i = tid; i < D * DV; i += kThreads) Cs[i] = CB[i];
+    for (int i = tid; i < D; i += kThreads) ms[i] = mB[i];
+    __syncthreads();
+    const float rho = pow_decay(log2f(head_decay(a.gamma, bh, a.H)), (float)seg_tokens);
+    for (int i = tid; i < D * DV; i += kThreads) {
+        const int r = i / DV, c = i % DV;
+        float acc = 0.f;
+        for (int x = 0; x < D; ++x) acc += Ss[r * D + x] * Cs[x * DV + c];
+        ZB[i] += rho * acc;
+    }
+    for (int r = tid; r < D; r += kThreads) {
+        float acc = 0.f;
+        for (int x = 0; x < D; ++x) acc += Ss[r * D + x] * ms[x];
+        yB[r] += rho * acc;
+    }
+}
+
+// Raw final (S, C, m, Z, y) -> packed public state (S, C, G = S C - Z, m, h = S m - y).
+__global__ void __launch_bounds__(kThreads)
+    finalize_kernel(const ChunkArgs a, int D, int DV, float* final_state) {
+    const int bh = blockIdx.x, tid = threadIdx.x;
+    const RawOff ro = raw_off(D, DV);
+    const PackOff po = pack_off(D, DV);
+    const float* r = a.ws + a.L.fin + (size_t)bh * raw_state_floats(D, DV);
+    float* o = final_state + (size_t)bh * raw_state_floats(D, DV);
+    const float *S = r + ro.S, *C = r + ro.C, *m = r + ro.m, *Z = r + ro.Z, *y = r + ro.y;
+    for (int i = tid; i < D * D; i += kThreads) o[po.S + i] = S[i];
+    for (int i = tid; i < D * DV; i += kThreads) {
+        const int x = i / DV, c = i % DV;
+        float acc = 0.f;
+        for (int j = 0; j < D; ++j) acc += S[x * D + j] * C[j * DV + c];
+        o[po.C + i] = C[i];
+        o[po.G + i] = acc - Z[i];
+    }
+    for (int x = tid; x < D; x += kThreads) {
+        float acc = 0.f;
+        for (int j = 0; j < D; ++j) acc += S[x * D + j] * m[j];
+        o[po.m + x] = m[x];
+        o[po.h + x] = acc - y[x];
+    }
+}
+
+int finish_launch() { return cudaPeekAtLastError() == cudaSuccess ? 0 : -1; }
+
+}  // namespace
+
+int launch_init_carry(const ChunkArgs& a, int d, int dv, const float* init_state, cudaStream_t st) {
+    if (a.BH <= 0) return 0;
+    init_carry_kernel<<<a.BH, kThreads, 0, st>>>(a, d, dv, init_state);
+    return finish_launch();
+}
+
+int launch_linear_scan(const float* src, float* dst, int BH, int H, int nsteps, size_t E,
+                       size_t src_hs, size_t dst_hs, bool store_all, const float* gamma,
+                       int step_tokens, int power, cudaStream_t st) {
+    const size_t total = (size_t)BH * E;
+    if (total == 0 || nsteps <= 0) return 0;
+    const unsigned blocks = (unsigned)((total + kThreads - 1) / kThreads);
+    linear_scan_kernel<<<blocks, kThreads, 0, st>>>(src, dst, BH, H, nsteps, E, src_hs, dst_hs,
+                                                    store_all ? 1 : 0, gamma, step_tokens, power);
+    return finish_launch();
+}
+
+int launch_cross(const ChunkArgs& a, int d, int dv, cudaStream_t st) {
+    if (a.nseg <= 1 || a.BH <= 0) return 0;
+    const size_t smem = ((size_t)d * d + (size_t)d * dv + d) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(cross_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return -1;
+    dim3 grid(a.nseg - 1, a.BH);
+    cross_kernel<<<grid, kThreads, smem, st>>>(a, d, dv, a.seg_chunks * a.W);
+    return finish_launch();
+}
+
+int launch_finalize(const ChunkArgs& a, int d, int dv, float* final_state, cudaStream_t st) {
+    if (a.BH <= 0) return 0;
+    finalize_kernel<<<a.BH, kThreads, 0, st>>>(a, d, dv, final_state);
+    return finish_launch();
+}
+
+}  // namespace hla2

@@ -1,0 +1,252 @@
+"""Python binding of the HLA-2 C ABI (include/hla2.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA library
+``_build/libhla2.so``.  PyTorch provides device memory and streams.  If the library
+has not been built, every call raises ``RuntimeError``; there is no other code path.
+
+Tensors given on the CPU are copied to the current CUDA device, processed there and
+copied back (the end-to-end path); CUDA tensors are processed in place on the
+current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libhla2.so")
+
+HLA2_F32 = 0
+HLA2_BF16 = 1
+_DTYPES = {torch.float32: HLA2_F32, torch.bfloat16: HLA2_BF16}
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+class HLA2Error(RuntimeError):
+    """A C-ABI call returned an error code."""
+
+    def __init__(self, func, code, message):
+        super().__init__(f"{func} failed with code {code}: {message}")
+        self.code = code
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("eps", ctypes.c_float),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("init_state", ctypes.c_void_p),
+        ("final_state", ctypes.c_void_p),
+        ("phase_events", ctypes.POINTER(ctypes.c_void_p)),
+        ("n_phase_events", ctypes.c_int),
+    ]
+
+
+def lib():
+    """Load libhla2.so (once).  Raises RuntimeError when it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"HLA-2 CUDA library not found at {LIB_PATH}; build it with "
+                "`python -m chunked_scan_mixer_gb300.build` (there is no fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, Z, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+        L.hla2_version.restype = I
+        L.hla2_last_error.restype = ctypes.c_char_p
+        L.hla2_state_floats.argtypes = [I, I]
+        L.hla2_state_floats.restype = Z
+        L.hla2_forward_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I]
+        L.hla2_forward_workspace_bytes.restype = Z
+        L.hla2_forward.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
+        L.hla2_forward.restype = I
+        L.hla2_forward_plan.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I),
+                                        ctypes.POINTER(I)]
+        L.hla2_forward_plan.restype = I
+        L.hla2_backward_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+        L.hla2_backward_workspace_bytes.restype = Z
+        L.hla2_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
+        L.hla2_backward.restype = I
+        L.hla2_decode_step.argtypes = [P, P, P, P, P, I, I, I, I, P, I, P, ctypes.POINTER(Opts)]
+        L.hla2_decode_step.restype = I
+        _lib = L
+        return L
+
+
+EXPORTED_SYMBOLS = (
+    "hla2_version", "hla2_last_error", "hla2_state_floats", "hla2_forward_workspace_bytes",
+    "hla2_forward", "hla2_forward_plan", "hla2_backward_workspace_bytes", "hla2_backward", "hla2_decode_step",
+)
+
+
+def _check(func, rc):
+    if rc != 0:
+        raise HLA2Error(func, rc, lib().hla2_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(nbytes, device, stream_handle):
+    """Scratch reused per (device, stream); grown on demand."""
+    if nbytes == 0:
+        return None
+    key = (device.index, stream_handle.value)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def state_floats(d, dv):
+    return int(lib().hla2_state_floats(d, dv))
+
+
+def forward_workspace_bytes(B, H, n, d, dv, chunk=64, dtype=torch.bfloat16, normalize=False,
+                            want_final_state=False):
+    r = lib().hla2_forward_workspace_bytes(B, H, n, d, dv, chunk, _DTYPES[dtype], int(normalize),
+                                           int(want_final_state))
+    if r == ctypes.c_size_t(-1).value:
+        raise ValueError("arguments rejected by hla2_forward")
+    return int(r)
+
+
+def forward_plan(B, H, n, d, dv, chunk=64, dtype=torch.bfloat16, want_final_state=False):
+    """(segments per head, chunks per segment, kernel launches per call)."""
+    ns, sc, nl = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check("hla2_forward_plan", lib().hla2_forward_plan(B, H, n, d, dv, chunk, _DTYPES[dtype],
+                                                        int(want_final_state), ctypes.byref(ns),
+                                                        ctypes.byref(sc), ctypes.byref(nl)))
+    return ns.value, sc.value, nl.value
+
+
+def _gamma_tensor(gamma, H, device):
+    if gamma is None:
+        return None
+    g = torch.as_tensor(gamma, dtype=torch.float32)
+    if g.numel() == 1 and H != 1:
+        g = g.reshape(1).expand(H)
+    g = g.reshape(H).to(device=device, dtype=torch.float32).contiguous()
+    return g
+
+
+def _to_device(t, device):
+    if t is None:
+        return None
+    if t.device.type == "cuda":
+        return t.contiguous()
+    return t.contiguous().to(device, non_blocking=True)
+
+
+def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state=None,
+            return_final_state=False, out=None, phase_events=None):
+    """Masked HLA-2 forward.  q, k [B,H,n,d]; v [B,H,n,dv] (float32 or bfloat16).
+
+    gamma: None, a scalar, or [H] per-head decay in (0, 1].  init_state: packed
+    [B,H,state_floats] float32 state to continue from.  Returns out [B,H,n,dv] (and the
+    packed final state when ``return_final_state``).  phase_events: optional list of
+    torch.cuda.Event recorded at the phase boundaries (see hla2_opts)."""
+    host = q.device.type == "cpu"
+    device = torch.device("cuda", torch.cuda.current_device()) if host else q.device
+    L = lib()
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must all be float32 or all bfloat16")
+    B, H, n, d = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3]:
+        raise ValueError("shape mismatch between q, k, v")
+    qd, kd, vd = (_to_device(t, device) for t in (q, k, v))
+    g = _gamma_tensor(gamma, H, device)
+    init = None
+    if init_state is not None:
+        init = _to_device(init_state, device).to(torch.float32).contiguous()
+        if init.shape != (B, H, state_floats(d, dv)):
+            raise ValueError("init_state must be [B, H, state_floats(d, dv)]")
+    o = out if (out is not None and not host) else torch.empty((B, H, n, dv), dtype=q.dtype, device=device)
+    fin = torch.empty((B, H, state_floats(d, dv)), dtype=torch.float32, device=device) \
+        if return_final_state else None
+    sh = _stream_handle(device)
+    nbytes = forward_workspace_bytes(B, H, n, d, dv, chunk, q.dtype, normalize, return_final_state)
+    ws = _workspace(nbytes, device, sh)
+    opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), nbytes,
+                None if init is None else init.data_ptr(), None if fin is None else fin.data_ptr(),
+                None, 0)
+    if phase_events:
+        for e in phase_events:
+            if not e.cuda_event:  # torch creates its events lazily
+                e.record()
+        ev = (ctypes.c_void_p * len(phase_events))(*[e.cuda_event for e in phase_events])
+        opts.phase_events = ctypes.cast(ev, ctypes.POINTER(ctypes.c_void_p))
+        opts.n_phase_events = len(phase_events)
+    rc = L.hla2_forward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), B, H, n, d, dv, _ptr(g), int(normalize),
+                        chunk, sh, ctypes.byref(opts))
+    _check("hla2_forward", rc)
+    if host:
+        o = o.to("cpu") if out is None else out.copy_(o)
+        fin = None if fin is None else fin.to("cpu")
+    return (o, fin) if return_final_state else o
+
+
+def backward(q, k, v, dout, gamma=None, chunk=64, dq=None, dk=None, dv=None):
+    """Gradients (dq, dk, dv) of the unnormalised forward for upstream dout."""
+    host = q.device.type == "cpu"
+    device = torch.device("cuda", torch.cuda.current_device()) if host else q.device
+    L = lib()
+    B, H, n, d = q.shape
+    dvdim = v.shape[-1]
+    qd, kd, vd, dod = (_to_device(t, device) for t in (q, k, v, dout))
+    g = _gamma_tensor(gamma, H, device)
+    gq = torch.empty_like(qd) if dq is None or host else dq
+    gk = torch.empty_like(kd) if dk is None or host else dk
+    gv = torch.empty_like(vd) if dv is None or host else dv
+    sh = _stream_handle(device)
+    nbytes = L.hla2_backward_workspace_bytes(B, H, n, d, dvdim, chunk, _DTYPES[q.dtype])
+    if nbytes == ctypes.c_size_t(-1).value:
+        nbytes = 0
+    ws = _workspace(int(nbytes), device, sh)
+    opts = Opts(_DTYPES[q.dtype], 1e-6, None if ws is None else ws.data_ptr(), int(nbytes), None, None,
+                None, 0)
+    rc = L.hla2_backward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(dod), _ptr(gq), _ptr(gk), _ptr(gv), B, H, n, d,
+                         dvdim, _ptr(g), 0, chunk, sh, ctypes.byref(opts))
+    _check("hla2_backward", rc)
+    if host:
+        return gq.cpu(), gk.cpu(), gv.cpu()
+    return gq, gk, gv
+
+
+def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6, out=None):
+    """One decode step; ``state`` [N,H,state_floats] float32 on the GPU is updated in
+    place.  q, k [N,H,d]; v [N,H,dv].  Returns out [N,H,dv]."""
+    L = lib()
+    if state.device.type != "cuda" or state.dtype != torch.float32 or not state.is_contiguous():
+        raise ValueError("state must be a contiguous float32 CUDA tensor")
+    device = state.device
+    N, H, d = q.shape
+    dv = v.shape[-1]
+    qd, kd, vd = (_to_device(t, device) for t in (q, k, v))
+    g = _gamma_tensor(gamma, H, device)
+    o = out if out is not None else torch.empty((N, H, dv), dtype=q.dtype, device=device)
+    opts = Opts(_DTYPES[q.dtype], float(eps), None, 0, None, None, None, 0)
+    rc = L.hla2_decode_step(_ptr(state), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), N, H, d, dv, _ptr(g),
+                            int(normalize), _stream_handle(device), ctypes.byref(opts))
+    _check("hla2_decode_step", rc)
+    return o

@@ -3,9 +3,10 @@
 This module draws random inputs and nothing else: it holds none of the method's
 arithmetic, so both the CUDA path and the float64 oracle can be fed from it.
 
-Every draw uses a torch CPU generator seeded per workload (the tiny check uses
-seed 0, the others their index 2..5), draws q, k, v (then dO) in float32 in that
-order, applies the workload's transform, and finally casts to the workload dtype.
+Every draw uses a torch generator (CPU unless a device is asked for) seeded per
+workload (the tiny check uses seed 0, the others their index 2..5), draws q, k, v
+(then dO) in float32 in that order, applies the workload's transform, and casts each
+tensor to the workload dtype.
 The oracle receives the cast values upcast to float32/float64, so both sides see
 exactly the same numbers.
 
@@ -77,43 +78,49 @@ def gammas(w: Workload) -> torch.Tensor | None:
     return torch.linspace(lo, hi, w.H, dtype=torch.float64).to(torch.float32)
 
 
-def _draw_qkv(gen, B, H, n, d, dv, qk, v_scale):
-    q = torch.randn((B, H, n, d), generator=gen, dtype=torch.float32)
-    k = torch.randn((B, H, n, d), generator=gen, dtype=torch.float32)
-    v = torch.randn((B, H, n, dv), generator=gen, dtype=torch.float32)
-    if qk == "softplus":
-        q = torch.nn.functional.softplus(q)
-        k = torch.nn.functional.softplus(k)
-    else:
-        q = q / math.sqrt(d)
-        k = k / math.sqrt(d)
-    if v_scale == "gauss_sqrt_d":
-        v = v / math.sqrt(dv)
+def _draw_qkv(gen, B, H, n, d, dv, qk, v_scale, dtype=torch.float32):
+    """q, k, v drawn in float32 in that order, transformed, then cast one at a time."""
+    dev = gen.device
+
+    def one(shape, kind, dim):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32, device=dev)
+        if kind == "softplus":
+            x = torch.nn.functional.softplus(x)
+        elif kind in ("gauss", "gauss_sqrt_d"):
+            x = x / math.sqrt(dim)
+        return x.to(dtype)
+
+    q = one((B, H, n, d), qk, d)
+    k = one((B, H, n, d), qk, d)
+    v = one((B, H, n, dv), v_scale, dv)
     return q, k, v
 
 
 def make(w: Workload | str, n: int | None = None, B: int | None = None, H: int | None = None,
-         seed: int | None = None):
-    """Draw a workload's inputs on the CPU, cast to its dtype.
+         seed: int | None = None, device="cpu"):
+    """Draw a workload's inputs, cast to its dtype.
 
     ``n``, ``B``, ``H`` and ``seed`` override the workload's values to make smaller
-    cases with the same distributions.  Returns a dict with q, k, v (and dout),
-    gamma [H] float32 or None, and the workload flags.
+    cases with the same distributions.  ``device`` selects the generator (a CUDA
+    generator draws different numbers than the CPU one for the same seed; the oracle
+    then receives copies of the drawn values).  Returns a dict with q, k, v (and dout),
+    gamma [H] float32 (on the CPU) or None, and the workload flags.
     """
     if isinstance(w, str):
         w = WORKLOADS[w]
     B = w.B if B is None else B
     H = w.H if H is None else H
     n = w.n if n is None else n
-    gen = torch.Generator(device="cpu")
+    gen = torch.Generator(device=device)
     gen.manual_seed(w.seed if seed is None else seed)
-    q, k, v = _draw_qkv(gen, B, H, n, w.d, w.dv, w.qk, w.v_scale)
+    q, k, v = _draw_qkv(gen, B, H, n, w.d, w.dv, w.qk, w.v_scale, dtype=w.dtype)
     out = {
-        "q": q.to(w.dtype), "k": k.to(w.dtype), "v": v.to(w.dtype),
+        "q": q, "k": k, "v": v,
         "normalize": w.normalize, "eps": w.eps, "chunk": w.chunk,
     }
     if w.with_dout:
-        out["dout"] = torch.randn((B, H, n, w.dv), generator=gen, dtype=torch.float32).to(w.dtype)
+        out["dout"] = torch.randn((B, H, n, w.dv), generator=gen, dtype=torch.float32,
+                                  device=device).to(w.dtype)
     g = gammas(w)
     if g is not None and H != w.H:
         g = torch.linspace(w.gamma[0], w.gamma[-1], H, dtype=torch.float64).to(torch.float32) \
@@ -130,8 +137,8 @@ def make_custom(B, H, n, d, dv, dtype=torch.bfloat16, seed=0, qk="gauss", v_scal
     """
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
-    q, k, v = _draw_qkv(gen, B, H, n, d, dv, qk, v_scale)
-    out = {"q": q.to(dtype), "k": k.to(dtype), "v": v.to(dtype)}
+    q, k, v = _draw_qkv(gen, B, H, n, d, dv, qk, v_scale, dtype=dtype)
+    out = {"q": q, "k": k, "v": v}
     if with_dout:
         out["dout"] = torch.randn((B, H, n, dv), generator=gen, dtype=torch.float32).to(dtype)
     if gamma is None:

@@ -70,6 +70,13 @@ typedef struct {
     size_t workspace_bytes; /* its size in bytes                                              */
     const float* init_state;/* nullable: packed state [B, H] to continue from (forward only)  */
     float* final_state;     /* nullable: receives the packed state after token n (forward)   */
+    /* Optional profiling hook: cudaEvent_t handles recorded on `stream` at phase
+     * boundaries of hla2_forward: [0] start, [1] after the carry-in set-up, [2] after
+     * the segment-summary pass, [3] after the inter-segment scan, [4] after the output
+     * pass, [5] after the final-state conversion.  The first n_phase_events are used;
+     * NULL / 0 records nothing.  The caller creates and owns the events. */
+    void* const* phase_events;
+    int n_phase_events;
 } hla2_opts;
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
@@ -104,6 +111,14 @@ size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chun
 int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
                  int d, int dv, const float* gamma, int normalize, int chunk,
                  hla2_stream_t stream, const hla2_opts* opts);
+
+/*
+ * The segmentation hla2_forward will use for these arguments on the current device:
+ * *nseg segments of *seg_chunks chunks per head, and *launches kernel launches per
+ * call.  Any output pointer may be NULL.  Returns HLA2_OK or HLA2_ERR_INVALID_ARG.
+ */
+int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, int want_final_state,
+                      int* nseg, int* seg_chunks, int* launches);
 
 /* Scratch bytes hla2_backward needs; (size_t)-1 for rejected arguments. */
 size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype);

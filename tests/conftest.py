@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionstart(session):
+    """Build the CUDA library and the C oracle if they are missing or stale."""
+    from chunked_scan_mixer_gb300 import build as cuda_build
+    from oracle import cref
+
+    cuda_build.build()
+    cref.build()

@@ -1,0 +1,42 @@
+"""Shared test helpers: error metric, oracle adapters, header parsing."""
+import os
+import re
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hla2.h")
+
+# Parity bars: max|gpu - oracle| / max|oracle|
+TOL_F32 = 1e-4
+TOL_BF16 = 2e-2
+
+
+def tol_for(dtype):
+    return TOL_F32 if dtype == torch.float32 else TOL_BF16
+
+
+def rel_err(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = np.max(np.abs(ref))
+    if scale == 0.0:
+        return float(np.max(np.abs(got)))
+    return float(np.max(np.abs(got - ref)) / scale)
+
+
+def np64(t):
+    """Exact float64 copy of a (possibly bf16) tensor for the oracle."""
+    return t.detach().to("cpu", torch.float32).numpy().astype(np.float64)
+
+
+def np32(t):
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+def header_functions():
+    """Names of the functions declared in include/hla2.h."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hla2_[a-z0-9_]+)\s*\(", src)))

@@ -1,0 +1,93 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+
+import pytest
+
+import chunked_scan_mixer_gb300 as hla
+from chunked_scan_mixer_gb300.hla2 import EXPORTED_SYMBOLS, Opts
+
+from .helpers import header_functions
+
+
+@pytest.fixture(scope="module")
+def L():
+    return hla.lib()
+
+
+def test_exports_every_declared_function(L):
+    declared = header_functions()
+    assert declared, "no declarations parsed from include/hla2.h"
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in hla2.h but not exported"
+    assert set(declared) == set(EXPORTED_SYMBOLS)
+
+
+def test_version_and_sizes(L):
+    assert L.hla2_version() >= 100
+    assert hla.state_floats(128, 128) == 128 * 128 + 2 * 128 * 128 + 2 * 128
+    assert hla.state_floats(16, 32) == 16 * 16 + 2 * 16 * 32 + 2 * 16
+
+
+def _fwd(L, **kw):
+    args = dict(q=ctypes.c_void_p(16), k=ctypes.c_void_p(16), v=ctypes.c_void_p(16),
+                out=ctypes.c_void_p(16), B=1, H=1, n=16, d=16, dv=16, gamma=None, normalize=0,
+                chunk=16, stream=None, opts=Opts(1, 1e-6, None, 0, None, None))
+    args.update(kw)
+    o = args.pop("opts")
+    rc = L.hla2_forward(args["q"], args["k"], args["v"], args["out"], args["B"], args["H"], args["n"],
+                        args["d"], args["dv"], args["gamma"], args["normalize"], args["chunk"],
+                        args["stream"], None if o is None else ctypes.byref(o))
+    return rc, L.hla2_last_error().decode()
+
+
+@pytest.mark.parametrize("kw, code", [
+    (dict(opts=None), -1),
+    (dict(d=48), -1),
+    (dict(dv=8), -1),
+    (dict(chunk=24), -1),
+    (dict(n=-1), -1),
+    (dict(normalize=2), -1),
+    (dict(opts=Opts(7, 1e-6, None, 0, None, None)), -1),
+    (dict(q=None), -1),
+    (dict(k=ctypes.c_void_p(18)), -1),
+    (dict(), -3),  # no workspace
+])
+def test_forward_rejects_bad_arguments(L, kw, code):
+    rc, msg = _fwd(L, **kw)
+    assert rc == code, msg
+    assert msg
+
+
+def test_forward_empty_is_ok(L):
+    rc, msg = _fwd(L, B=0)
+    assert rc == 0, msg
+    rc, msg = _fwd(L, n=0, q=None, k=None, v=None, out=None)
+    assert rc == 0, msg
+
+
+def test_workspace_query(L):
+    assert hla.forward_workspace_bytes(1, 16, 65536, 64, 64) > 0
+    assert hla.forward_workspace_bytes(1, 1, 0, 64, 64) == 0
+    with pytest.raises(ValueError):
+        hla.forward_workspace_bytes(1, 1, 16, 40, 64)
+
+
+def test_decode_rejects_bad_arguments(L):
+    o = Opts(1, 1e-6, None, 0, None, None)
+    rc = L.hla2_decode_step(None, ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                            ctypes.c_void_p(16), 1, 1, 16, 16, None, 0, None, ctypes.byref(o))
+    assert rc == -1
+    rc = L.hla2_decode_step(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                            ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 1, 20, 16, None, 0, None,
+                            ctypes.byref(o))
+    assert rc == -1
+    rc = L.hla2_decode_step(None, None, None, None, None, 0, 4, 16, 16, None, 0, None, ctypes.byref(o))
+    assert rc == 0
+
+
+def test_backward_rejects_normalized(L):
+    o = Opts(1, 1e-6, None, 0, None, None)
+    p = ctypes.c_void_p(16)
+    rc = L.hla2_backward(p, p, p, p, p, p, p, 1, 1, 16, 16, 16, None, 1, 16, None, ctypes.byref(o))
+    assert rc == -2

@@ -1,0 +1,99 @@
+"""GPU decode step against the float64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import chunked_scan_mixer_gb300 as hla
+from chunked_scan_mixer_gb300 import inputs
+from oracle import cref
+from oracle import hla2_oracle as O
+
+from .helpers import np32, np64, rel_err, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def prefill_state(N, H, d, dv, n, seed, gamma):
+    """A realistic packed state: the oracle's final state after n random tokens."""
+    x = inputs.make_custom(N, H, n, d, dv, torch.float32, seed=seed, gamma=gamma)
+    g = None if x["gamma"] is None else x["gamma"].double().numpy()
+    _, st = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), g, return_state=True)
+    return st, x["gamma"]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d, dv", [(16, 16), (64, 64), (128, 128), (32, 64), (64, 32)])
+@pytest.mark.parametrize("normalize", [False, True])
+def test_decode_steps_match_oracle(dtype, d, dv, normalize):
+    N, H = 3, 2
+    st, gamma = prefill_state(N, H, d, dv, 40, seed=d + dv, gamma=(0.95, 0.999))
+    if normalize:  # positive queries/keys keep the denominator away from zero
+        st_q = inputs.make_custom(N, H, 6, d, dv, torch.float32, seed=99, qk="softplus", gamma=(0.95, 0.999))
+        g = st_q["gamma"].double().numpy()
+        _, st = cref.forward(np32(st_q["q"]), np32(st_q["k"]), np32(st_q["v"]), g, return_state=True)
+    state_gpu = torch.from_numpy(st.astype(np.float32)).cuda()
+    state_ref = st.astype(np.float32).astype(np.float64).copy()
+    for step in range(5):
+        q, k, v = inputs.decode_step_inputs(step, N, H, d, dv, dtype=dtype)
+        if normalize:
+            q, k = q.float().abs().to(dtype), k.float().abs().to(dtype)
+        o = hla.decode_step(state_gpu, q.cuda(), k.cuda(), v.cuda(), gamma=gamma.cuda(),
+                            normalize=normalize, eps=1e-6)
+        ref = cref.decode_step(state_ref, np32(q), np32(k), np32(v), gamma.double().numpy(),
+                               normalize=normalize, eps=1e-6)
+        assert rel_err(np64(o.cpu()), ref) <= tol_for(dtype), step
+    assert rel_err(state_gpu.cpu().double().numpy(), state_ref) <= 1e-5
+
+
+def test_decode_from_zero_equals_forward():
+    N, H, d, n = 2, 3, 64, 37
+    x = inputs.make_custom(N, H, n, d, d, torch.float32, seed=5, gamma=(0.9, 0.99))
+    state = torch.zeros(N, H, hla.state_floats(d, d), device="cuda")
+    outs = []
+    for t in range(n):
+        outs.append(hla.decode_step(state, x["q"][:, :, t].cuda(), x["k"][:, :, t].cuda(),
+                                    x["v"][:, :, t].cuda(), gamma=x["gamma"].cuda()))
+    o = torch.stack(outs, dim=2).cpu()
+    ref, ref_state = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), x["gamma"].double().numpy(),
+                                  return_state=True)
+    assert rel_err(np64(o), ref) <= 1e-4
+    assert rel_err(state.cpu().double().numpy(), ref_state) <= 1e-5
+
+
+def test_prefill_then_decode_matches_uninterrupted_oracle():
+    """Checkpoint/resume: a GPU prefill's final state continues exactly like the oracle
+    run over prefill + decode tokens."""
+    N, H, d, n = 2, 4, 128, 300
+    x = inputs.make_custom(N, H, n, d, d, torch.bfloat16, seed=6, gamma=0.999)
+    _, fin = hla.forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), gamma=x["gamma"].cuda(), chunk=64,
+                         return_final_state=True)
+    g = x["gamma"].double().numpy()
+    _, ref_state = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), g, return_state=True)
+    assert rel_err(fin.cpu().double().numpy(), ref_state) <= 2e-2
+    state_ref = ref_state.copy()
+    for step in range(4):
+        q, k, v = inputs.decode_step_inputs(step, N, H, d, d)
+        o = hla.decode_step(fin, q.cuda(), k.cuda(), v.cuda(), gamma=x["gamma"].cuda())
+        ref = cref.decode_step(state_ref, np32(q), np32(k), np32(v), g)
+        assert rel_err(np64(o.cpu()), ref) <= 2e-2
+
+
+def test_decode_workload_full_width_sampled():
+    """256 sequences x 32 heads, d = dv = 128: a 4096-token bf16 prefill through the
+    forward (final state), then decode steps; sequences 0..3 (128 heads) are compared
+    with the oracle run over the same tokens."""
+    w = inputs.WORKLOADS["decode_prefill"]
+    x = inputs.make(w, device="cuda")
+    g = x["gamma"].cuda()
+    _, state = hla.forward(x["q"], x["k"], x["v"], gamma=g, chunk=w.chunk, return_final_state=True)
+    sub = slice(0, 4)
+    gd = x["gamma"].double().numpy()
+    _, st_ref = cref.forward(np32(x["q"][sub]), np32(x["k"][sub]), np32(x["v"][sub]), gd, return_state=True)
+    del x
+    assert rel_err(state[sub].cpu().double().numpy(), st_ref) <= 2e-2
+    for step in range(3):
+        q, k, v = inputs.decode_step_inputs(step, w.B, w.H, w.d, w.dv, device="cuda")
+        o = hla.decode_step(state, q, k, v, gamma=g)
+        ref = cref.decode_step(st_ref, np32(q[sub]), np32(k[sub]), np32(v[sub]), gd)
+        assert rel_err(np64(o[sub].cpu()), ref) <= 2e-2, step
+        assert torch.isfinite(o.float()).all()
