@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--n", type=int, default=None,
+                    help="override the sequence length (smaller case for ncu --set full captures; "
+                         "the reported metric is only valid at the default)")
     return ap.parse_args()
 
 
@@ -237,6 +240,9 @@ def run_ours(args, dist: Dist):
     torch.cuda.set_device(dist.local)
     dev = torch.device("cuda", dist.local)
     w = inputs.WORKLOADS[WORKLOAD]
+    if args.n is not None:
+        import dataclasses
+        w = dataclasses.replace(w, n=args.n)
     tokens = w.B * w.H * w.n
     x = inputs.make(w, device=dev, seed=w.seed + 1000 * dist.rank)
     q, k, v = x["q"], x["k"], x["v"]
@@ -288,6 +294,7 @@ def run_ours(args, dist: Dist):
     # algorithmic bytes per launch: q, k, v read (bf16) and out written (bf16) for the
     # tokens the launch processes
     out_bytes = tokens * (2 * w.d + w.dv) * 2 + tokens * w.dv * 2
+    io_mb = tokens * (2 * w.d + 2 * w.dv) * 2 / 1e6
     summary_tokens = w.B * w.H * min(w.n, (nseg - 1) * seg_chunks * w.chunk)
     summ_bytes = summary_tokens * (2 * w.d + w.dv) * 2
     if ph["output_pass"] >= ph["segment_summaries"]:
@@ -337,7 +344,7 @@ def run_ours(args, dist: Dist):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": CONFIG_NAME, "B": w.B, "H": w.H, "n": w.n, "d": w.d, "dv": w.dv,
                        "chunk": w.chunk, "segments_per_head": nseg, "chunks_per_segment": seg_chunks,
-                       "l2": "inputs (402.7 MB) + output (134.2 MB) exceed the 129 MB L2; no flush"},
+                       "l2": f"inputs + output ({io_mb:.1f} MB) exceed the 129 MB L2; no flush"},
             "roofline": roofline, "whole_step": whole, "phases_ms": ph, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches * K, "clocks": clk,
         }

@@ -10,24 +10,53 @@
 #include "kernels.h"
 
 namespace hla2 {
-int launch_fwd_chunk_mma_d16(const ChunkArgs&, int, bool, bool, cudaStream_t);
-int launch_fwd_chunk_mma_d32(const ChunkArgs&, int, bool, bool, cudaStream_t);
-int launch_fwd_chunk_mma_d64(const ChunkArgs&, int, bool, bool, cudaStream_t);
-int launch_fwd_chunk_mma_d128(const ChunkArgs&, int, bool, bool, cudaStream_t);
+int launch_fwd_chunk_mma_d16(const ChunkArgs&, int, int, bool, cudaStream_t);
+int launch_fwd_chunk_mma_d32(const ChunkArgs&, int, int, bool, cudaStream_t);
+int launch_fwd_chunk_mma_d64(const ChunkArgs&, int, int, bool, cudaStream_t);
+int launch_fwd_chunk_mma_d128(const ChunkArgs&, int, int, bool, cudaStream_t);
 size_t fwd_chunk_mma_smem_d16(int, bool);
 size_t fwd_chunk_mma_smem_d32(int, bool);
 size_t fwd_chunk_mma_smem_d64(int, bool);
 size_t fwd_chunk_mma_smem_d128(int, bool);
 
-int launch_fwd_chunk_mma(const ChunkArgs& a, int d, int dv, int W, bool summary, bool cm,
+int launch_fwd_chunk_mma(const ChunkArgs& a, int d, int dv, int W, int mode, bool cm,
                          cudaStream_t st) {
     if (d != dv) return -2;
     switch (d) {
-        case 16: return launch_fwd_chunk_mma_d16(a, W, summary, cm, st);
-        case 32: return launch_fwd_chunk_mma_d32(a, W, summary, cm, st);
-        case 64: return launch_fwd_chunk_mma_d64(a, W, summary, cm, st);
-        case 128: return launch_fwd_chunk_mma_d128(a, W, summary, cm, st);
+        case 16: return launch_fwd_chunk_mma_d16(a, W, mode, cm, st);
+        case 32: return launch_fwd_chunk_mma_d32(a, W, mode, cm, st);
+        case 64: return launch_fwd_chunk_mma_d64(a, W, mode, cm, st);
+        case 128: return launch_fwd_chunk_mma_d128(a, W, mode, cm, st);
         default: return -2;
+    }
+}
+
+int launch_bwd_chunk_mma_d16(const BwdArgs&, int, bool, cudaStream_t);
+int launch_bwd_chunk_mma_d32(const BwdArgs&, int, bool, cudaStream_t);
+int launch_bwd_chunk_mma_d64(const BwdArgs&, int, bool, cudaStream_t);
+int launch_bwd_chunk_mma_d128(const BwdArgs&, int, bool, cudaStream_t);
+size_t bwd_chunk_mma_smem_d16(int);
+size_t bwd_chunk_mma_smem_d32(int);
+size_t bwd_chunk_mma_smem_d64(int);
+size_t bwd_chunk_mma_smem_d128(int);
+
+int launch_bwd_chunk_mma(const BwdArgs& a, int d, int W, bool rsum, cudaStream_t st) {
+    switch (d) {
+        case 16: return launch_bwd_chunk_mma_d16(a, W, rsum, st);
+        case 32: return launch_bwd_chunk_mma_d32(a, W, rsum, st);
+        case 64: return launch_bwd_chunk_mma_d64(a, W, rsum, st);
+        case 128: return launch_bwd_chunk_mma_d128(a, W, rsum, st);
+        default: return -2;
+    }
+}
+
+size_t bwd_chunk_mma_smem(int d, int W) {
+    switch (d) {
+        case 16: return bwd_chunk_mma_smem_d16(W);
+        case 32: return bwd_chunk_mma_smem_d32(W);
+        case 64: return bwd_chunk_mma_smem_d64(W);
+        case 128: return bwd_chunk_mma_smem_d128(W);
+        default: return 0;
     }
 }
 
@@ -141,7 +170,7 @@ int check_common(int B, int H, int n, int d, int dv, int dtype, int normalize) {
     return HLA2_OK;
 }
 
-size_t forward_ws(const Plan& p) { return p.nseg > 0 ? fwd_layout(p).total * sizeof(float) : 0; }
+size_t forward_ws(const Plan& p) { return p.nseg > 0 ? fwd_layout(p, p.nseg - 1).total * sizeof(float) : 0; }
 
 }  // namespace
 
@@ -196,7 +225,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     if (path == Path::kNone)
         return fail(HLA2_ERR_UNSUPPORTED, "no kernel for dtype %d, d %d, dv %d, chunk %d", opts->dtype, d, dv, chunk);
     const Plan p = make_plan(B, H, n, d, dv, chunk, di.sms);
-    const FwdLayout L = fwd_layout(p);
+    const FwdLayout L = fwd_layout(p, p.nseg - 1);
     const size_t need = L.total * sizeof(float);
     if (!opts->workspace || opts->workspace_bytes < need)
         return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
@@ -215,6 +244,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     a.nchunks = p.nchunks;
     a.seg_chunks = p.seg_chunks;
     a.nseg = p.nseg;
+    a.nsum = p.nseg - 1;
     a.gamma = gamma;
     a.normalize = normalize;
     a.eps = opts->eps;
@@ -227,7 +257,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         ChunkArgs b = a;
         b.seg0 = seg0;
         b.nseg_launch = count;
-        if (path == Path::kMma) return launch_fwd_chunk_mma(b, d, dv, chunk, summary, cm, st);
+        if (path == Path::kMma) return launch_fwd_chunk_mma(b, d, dv, chunk, summary ? kSummary : kOutput, cm, st);
         return launch_fwd_chunk_simt(b, d, dv, chunk, summary, cm, bf, st);
     };
 
@@ -245,20 +275,20 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
         if (chunk_pass(0, steps, true, true)) return cuda_fail("segment summaries");
         mark(2);
-        if (launch_linear_scan(a.ws + L.SB, a.ws + L.Sin, a.BH, H, steps, dd, steps * dd, p.nseg * dd, true,
+        if (launch_linear_scan(a.ws + L.SB, a.ws + L.Sin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true,
                                gamma, seg_tokens, 1, st))
             return cuda_fail("key-moment scan");
         if (want_final) {
-            if (launch_linear_scan(a.ws + L.CB, a.ws + L.Clast, a.BH, H, steps, ddv, steps * ddv, ddv, false,
+            if (launch_linear_scan(a.ws + L.CB, a.ws + L.Clast, a.BH, H, steps, ddv, a.nsum * ddv, ddv, false,
                                    gamma, seg_tokens, 1, st) ||
-                launch_linear_scan(a.ws + L.mB, a.ws + L.mlast, a.BH, H, steps, d, steps * (size_t)d, d, false,
+                launch_linear_scan(a.ws + L.mB, a.ws + L.mlast, a.BH, H, steps, d, a.nsum * (size_t)d, d, false,
                                    gamma, seg_tokens, 1, st))
                 return cuda_fail("query-value scan");
         }
         if (launch_cross(a, d, dv, st)) return cuda_fail("cross terms");
-        if (launch_linear_scan(a.ws + L.ZB, a.ws + L.Zin, a.BH, H, steps, ddv, steps * ddv, p.nseg * ddv, true,
+        if (launch_linear_scan(a.ws + L.ZB, a.ws + L.Zin, a.BH, H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true,
                                gamma, seg_tokens, 2, st) ||
-            launch_linear_scan(a.ws + L.yB, a.ws + L.yin, a.BH, H, steps, d, steps * (size_t)d, p.nseg * (size_t)d,
+            launch_linear_scan(a.ws + L.yB, a.ws + L.yin, a.BH, H, steps, d, a.nsum * (size_t)d, p.nseg * (size_t)d,
                                true, gamma, seg_tokens, 2, st))
             return cuda_fail("masked-summary scan");
     } else {
@@ -297,17 +327,163 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     return succeed();
 }
 
+}  // extern "C"
+
+namespace {
+
+// The backward runs its chunk passes at the largest width <= chunk whose kernels are
+// compiled and fit in shared memory (the result does not depend on the width).
+int backward_width(int d, int chunk, const DevInfo& di) {
+    for (int W = chunk; W >= 16; W /= 2) {
+        const size_t sb = bwd_chunk_mma_smem(d, W), sf = fwd_chunk_mma_smem(d, d, W, true);
+        if (sb > 0 && sf > 0 && sb <= (size_t)di.smem_optin && sf <= (size_t)di.smem_optin) return W;
+    }
+    return 0;
+}
+
+struct BwdLayout {
+    FwdLayout F;              // forward pieces (nseg summaries)
+    size_t states_bytes_off;  // byte offset of the bf16 chunk states
+    size_t ZhB, ShB, Zh_end, Sh_end;  // float offsets
+    size_t total_bytes;
+};
+
+BwdLayout bwd_layout(const Plan& p) {
+    BwdLayout L;
+    L.F = fwd_layout(p, p.nseg);
+    const size_t BH = p.BH, ns = p.nseg, dd = (size_t)p.d * p.d, ddv = (size_t)p.d * p.dv;
+    size_t o = L.F.total;
+    L.ZhB = o;    o = align64(o + BH * ns * ddv);
+    L.ShB = o;    o = align64(o + BH * ns * dd);
+    L.Zh_end = o; o = align64(o + BH * ns * ddv);
+    L.Sh_end = o; o = align64(o + BH * ns * dd);
+    L.states_bytes_off = o * sizeof(float);
+    L.total_bytes = L.states_bytes_off + BH * (size_t)p.nchunks * (dd + ddv) * sizeof(bf16);
+    return L;
+}
+
+int check_backward(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
+    int rc = check_common(B, H, n, d, dv, dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
+    if (normalize) return fail(HLA2_ERR_UNSUPPORTED, "the backward covers the unnormalised output only");
+    if (dtype != HLA2_BF16 || d != dv)
+        return fail(HLA2_ERR_UNSUPPORTED, "the backward needs bf16 tensors and d == dv");
+    return HLA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype) {
-    (void)B, (void)H, (void)n, (void)d, (void)dv, (void)chunk, (void)dtype;
-    return (size_t)-1;
+    if (check_backward(B, H, n, d, dv, chunk, dtype, 0) != HLA2_OK) return (size_t)-1;
+    const DevInfo di = dev_info();
+    const int W = backward_width(d, chunk, di);
+    if (!W) return (size_t)-1;
+    const Plan p = make_plan(B, H, n, d, dv, W, di.sms);
+    return p.nseg > 0 ? bwd_layout(p).total_bytes : 0;
 }
 
 int hla2_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
                   void* dv_out, int B, int H, int n, int d, int dv, const float* gamma, int normalize,
                   int chunk, hla2_stream_t stream, const hla2_opts* opts) {
-    (void)q, (void)k, (void)v, (void)dout, (void)dq, (void)dk, (void)dv_out, (void)B, (void)H, (void)n;
-    (void)d, (void)dv, (void)gamma, (void)normalize, (void)chunk, (void)stream, (void)opts;
-    return fail(HLA2_ERR_UNSUPPORTED, "backward is not available in this build");
+    if (!opts) return fail(HLA2_ERR_INVALID_ARG, "opts must not be NULL");
+    int rc = check_backward(B, H, n, d, dv, chunk, opts->dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (opts->init_state || opts->final_state)
+        return fail(HLA2_ERR_INVALID_ARG, "the backward takes no init_state / final_state");
+    const long BH = (long)B * H;
+    if (BH == 0 || n == 0) return succeed();
+    if (!q || !k || !v || !dout || !dq || !dk || !dv_out)
+        return fail(HLA2_ERR_INVALID_ARG, "q, k, v, dout, dq, dk, dv must not be NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv_out))
+        return fail(HLA2_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    const DevInfo di = dev_info();
+    const int W = backward_width(d, chunk, di);
+    if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no backward kernel for d %d, chunk %d", d, chunk);
+    const Plan p = make_plan(B, H, n, d, dv, W, di.sms);
+    const BwdLayout L = bwd_layout(p);
+    if (!opts->workspace || opts->workspace_bytes < L.total_bytes)
+        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.total_bytes,
+                    opts->workspace ? opts->workspace_bytes : (size_t)0);
+    if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    float* ws = static_cast<float*>(opts->workspace);
+    bf16* states = reinterpret_cast<bf16*>(static_cast<char*>(opts->workspace) + L.states_bytes_off);
+
+    ChunkArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = nullptr;
+    a.BH = (int)BH;
+    a.H = H;
+    a.n = n;
+    a.W = W;
+    a.nchunks = p.nchunks;
+    a.seg_chunks = p.seg_chunks;
+    a.nseg = p.nseg;
+    a.nsum = p.nseg;
+    a.gamma = gamma;
+    a.ws = ws;
+    a.L = L.F;
+    a.chunk_states = states;
+
+    BwdArgs b{};
+    b.q = static_cast<const bf16*>(q);
+    b.k = static_cast<const bf16*>(k);
+    b.v = static_cast<const bf16*>(v);
+    b.dout = static_cast<const bf16*>(dout);
+    b.dq = static_cast<bf16*>(dq);
+    b.dk = static_cast<bf16*>(dk);
+    b.dv = static_cast<bf16*>(dv_out);
+    b.BH = (int)BH;
+    b.H = H;
+    b.n = n;
+    b.W = W;
+    b.nchunks = p.nchunks;
+    b.seg_chunks = p.seg_chunks;
+    b.nseg = p.nseg;
+    b.gamma = gamma;
+    b.ws = ws;
+    b.ZhB = L.ZhB;
+    b.ShB = L.ShB;
+    b.Zh_end = L.Zh_end;
+    b.Sh_end = L.Sh_end;
+    b.chunk_states = states;
+
+    const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
+    const int seg_tokens = p.seg_chunks * W;
+    auto pass = [&](int mode) {
+        ChunkArgs c = a;
+        c.seg0 = 0;
+        c.nseg_launch = p.nseg;
+        return launch_fwd_chunk_mma(c, d, dv, W, mode, false, st);
+    };
+    cudaGetLastError();
+    // forward carries at segment starts, then the forward state at every chunk start
+    if (launch_init_carry(a, d, dv, nullptr, st)) return cuda_fail("carry-in initialisation");
+    if (p.nseg > 1) {
+        const int steps = p.nseg - 1;
+        if (pass(kSummary)) return cuda_fail("segment summaries");
+        if (launch_linear_scan(ws + L.F.SB, ws + L.F.Sin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true, gamma,
+                               seg_tokens, 1, st) ||
+            launch_cross(a, d, dv, st) ||
+            launch_linear_scan(ws + L.F.ZB, ws + L.F.Zin, a.BH, H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true, gamma,
+                               seg_tokens, 2, st))
+            return cuda_fail("forward segment scan");
+    }
+    if (pass(kStates)) return cuda_fail("forward state export");
+    // reverse summaries, reverse scan with the cross term Zh_end C_B^T, gradients
+    if (launch_bwd_chunk_mma(b, d, W, true, st)) return cuda_fail("reverse summaries");
+    if (launch_reverse_scan(ws + L.ZhB, ws + L.Zh_end, a.BH, H, p.nseg, ddv, gamma, n, W, p.seg_chunks, 2, st) ||
+        launch_reverse_cross(b, ws + L.F.CB, d, dv, st) ||
+        launch_reverse_scan(ws + L.ShB, ws + L.Sh_end, a.BH, H, p.nseg, dd, gamma, n, W, p.seg_chunks, 1, st))
+        return cuda_fail("reverse segment scan");
+    if (launch_bwd_chunk_mma(b, d, W, false, st)) return cuda_fail("gradient pass");
+    return succeed();
 }
 
 int hla2_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,

@@ -1,0 +1,24 @@
+// Instantiations of the reverse-mode chunk kernel for d = dv = 64.
+#include "bwd_chunk_mma.cuh"
+
+namespace hla2 {
+
+int launch_bwd_chunk_mma_d64(const BwdArgs& a, int W, bool rsum, cudaStream_t st) {
+    switch (W) {
+        case 16: return launch_bwd_chunk_mma_t<64, 64, 16>(a, rsum, st);
+        case 32: return launch_bwd_chunk_mma_t<64, 64, 32>(a, rsum, st);
+        case 64: return launch_bwd_chunk_mma_t<64, 64, 64>(a, rsum, st);
+        default: return -2;
+    }
+}
+
+size_t bwd_chunk_mma_smem_d64(int W) {
+    switch (W) {
+        case 16: return BwdCfg<64, 64, 16>::BYTES;
+        case 32: return BwdCfg<64, 64, 32>::BYTES;
+        case 64: return BwdCfg<64, 64, 64>::BYTES;
+        default: return 0;
+    }
+}
+
+}  // namespace hla2

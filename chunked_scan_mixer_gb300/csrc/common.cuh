@@ -26,7 +26,7 @@ struct Plan {
 
 // Float offsets of the forward workspace arrays (each 64-float aligned).
 struct FwdLayout {
-    size_t SB, CB, ZB, mB, yB;   // summaries, [BH][nseg-1][...]
+    size_t SB, CB, ZB, mB, yB;   // summaries, [BH][nsum][...]
     size_t Sin, Zin, yin;        // carries,   [BH][nseg][...]
     size_t Clast, mlast;         // C, m carried into the last segment, [BH][...]
     size_t fin;                  // raw final (S, C, m, Z, y), [BH][...]
@@ -39,9 +39,10 @@ __host__ __device__ inline size_t raw_state_floats(int d, int dv) {
     return (size_t)d * d + 2 * (size_t)d * dv + 2 * (size_t)d;
 }
 
-inline FwdLayout fwd_layout(const Plan& p) {
+// nsum: summaries kept per head (the forward needs nseg - 1, the backward nseg).
+inline FwdLayout fwd_layout(const Plan& p, int nsum) {
     FwdLayout L;
-    const size_t BH = p.BH, ns = p.nseg, nsm = p.nseg > 0 ? p.nseg - 1 : 0;
+    const size_t BH = p.BH, ns = p.nseg, nsm = nsum > 0 ? nsum : 0;
     const size_t dd = (size_t)p.d * p.d, ddv = (size_t)p.d * p.dv, d = p.d;
     size_t o = 0;
     L.SB = o;    o = align64(o + BH * nsm * dd);

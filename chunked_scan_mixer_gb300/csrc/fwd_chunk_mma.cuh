@@ -18,9 +18,11 @@
 //   S  <- g^Wc S0 + K~^T K,    K~ = diag(g^(Wc-1-i)) K
 //   Z  <- g^(2Wc) Z0 + P~^T V, P~ = diag(g^(2(Wc-1-j))) P;   y likewise with V -> 1
 //   C  <- g^Wc C0 + Q~^T V,    Q~ = diag(g^(Wc-1-j)) Q;      m likewise
-// SUMMARY mode starts from zero and stores (S, C, Z, m, y) of the segment (its
-// summary for the inter-segment scan); output mode starts from the segment's
-// carry-in and writes out (and the raw final state for the last segment).
+// kSummary starts from zero and stores (S, C, Z, m, y) of the segment (its summary
+// for the inter-segment scan); kOutput starts from the segment's carry-in and writes
+// out (and the raw final state for the last segment); kStates starts from the carry-in
+// and exports the bf16 (S, Z) at every chunk start (the forward states that the
+// reverse-mode pass consumes).
 #pragma once
 
 #include "common.cuh"
@@ -53,9 +55,10 @@ struct MmaCfg {
     static constexpr size_t bytes(bool cm) { return oQt + (cm ? ROWS_D : 0); }
 };
 
-template <int D, int DV, int W, bool SUMMARY, bool CM>
+template <int D, int DV, int W, int MODE, bool CM>
 __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
     fwd_chunk_mma_kernel(const ChunkArgs a) {
+    constexpr bool SUMMARY = MODE == kSummary, OUTPUT = MODE == kOutput;
     using Cfg = MmaCfg<D, DV, W>;
     constexpr int NW = Cfg::NW, NT = Cfg::NT, LD = Cfg::LD, LDV = Cfg::LDV, LW = Cfg::LW;
     constexpr int TW = Cfg::TW, TD = Cfg::TD, TV = Cfg::TV;
@@ -195,6 +198,19 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         cp_async_wait_all();
         __syncthreads();
 
+        if (MODE == kStates) {  // export the state at this chunk start
+            bf16* dst = a.chunk_states + ((size_t)bh * a.nchunks + c) * (size_t)(D * D + D * DV);
+            for (int i = tid; i < D * D / 8; i += NT) {
+                const int r = (i * 8) / D, f = (i * 8) % D;
+                *reinterpret_cast<uint4*>(dst + (size_t)r * D + f) = *reinterpret_cast<const uint4*>(&Sst[r * LD + f]);
+            }
+            for (int i = tid; i < D * DV / 8; i += NT) {
+                const int r = (i * 8) / DV, f = (i * 8) % DV;
+                *reinterpret_cast<uint4*>(dst + (size_t)D * D + (size_t)r * DV + f) =
+                    *reinterpret_cast<const uint4*>(&Zst[r * LDV + f]);
+            }
+        }
+
         // ---- scaled copies, query mass, denominator carry term ----------------------
         for (int i = tid; i < W * D; i += NT) {
             const int r = i / D, f = i % D;
@@ -202,7 +218,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
             Kt[r * LD + f] = from_f32<bf16>(w1 * to_f32(Ks[r * LD + f]));
             if (CM) Qt[r * LD + f] = from_f32<bf16>(w1 * to_f32(Qs[r * LD + f]));
         }
-        if (!SUMMARY && a.normalize) {
+        if (OUTPUT && a.normalize) {
             for (int r = tid; r < W; r += NT) {
                 float s = 0.f;
                 for (int f = 0; f < D; ++f) s += to_f32(Qs[r * LD + f]) * ys[f];
@@ -275,7 +291,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         }
         __syncthreads();
 
-        if (!SUMMARY) {
+        if (OUTPUT) {
             // ---- B~ = mask(Q P^T) (+ row sums for the denominator) -----------------------
             for (int t = warp; t < TW * TW; t += NW) {
                 const int rb = t / TW, jb = t % TW;
@@ -379,13 +395,13 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
     // ---- epilogue: segment summary, or the raw final state --------------------------------
     float *dS = nullptr, *dC = nullptr, *dZ = nullptr, *dm = nullptr, *dy = nullptr;
     if (SUMMARY) {
-        const size_t sidx = (size_t)bh * (nseg - 1) + seg;
+        const size_t sidx = (size_t)bh * a.nsum + seg;
         dS = a.ws + a.L.SB + sidx * D * D;
         dC = a.ws + a.L.CB + sidx * D * DV;
         dZ = a.ws + a.L.ZB + sidx * D * DV;
         dm = a.ws + a.L.mB + sidx * D;
         dy = a.ws + a.L.yB + sidx * D;
-    } else if (CM && last_seg && a.want_final) {
+    } else if (OUTPUT && CM && last_seg && a.want_final) {
         const RawOff ro = raw_off(D, DV);
         float* base = a.ws + a.L.fin + (size_t)bh * raw_state_floats(D, DV);
         dS = base + ro.S;
@@ -428,29 +444,31 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
     }
 }
 
+template <int D, int DV, int W, int MODE, bool CM>
+cudaError_t launch_mode(const ChunkArgs& a, size_t smem, cudaStream_t st) {
+    auto kfn = fwd_chunk_mma_kernel<D, DV, W, MODE, CM>;
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kfn<<<dim3(a.nseg_launch, a.BH), MmaCfg<D, DV, W>::NT, smem, st>>>(a);
+    return cudaPeekAtLastError();
+}
+
 template <int D, int DV, int W>
-int launch_fwd_chunk_mma_t(const ChunkArgs& a, bool summary, bool track_cm, cudaStream_t st) {
+int launch_fwd_chunk_mma_t(const ChunkArgs& a, int mode, bool track_cm, cudaStream_t st) {
     using Cfg = MmaCfg<D, DV, W>;
-    const size_t smem = Cfg::bytes(summary || track_cm);
-    const int nblocks_x = a.nseg_launch;
-    if (nblocks_x <= 0 || a.BH <= 0) return 0;
-    dim3 grid(nblocks_x, a.BH), block(Cfg::NT);
+    const bool cm = mode == kSummary || track_cm;
+    const size_t smem = Cfg::bytes(cm);
+    if (a.nseg_launch <= 0 || a.BH <= 0) return 0;
     cudaError_t e;
-    if (summary) {
-        auto kfn = fwd_chunk_mma_kernel<D, DV, W, true, true>;
-        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) kfn<<<grid, block, smem, st>>>(a);
-    } else if (track_cm) {
-        auto kfn = fwd_chunk_mma_kernel<D, DV, W, false, true>;
-        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) kfn<<<grid, block, smem, st>>>(a);
-    } else {
-        auto kfn = fwd_chunk_mma_kernel<D, DV, W, false, false>;
-        e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess) kfn<<<grid, block, smem, st>>>(a);
-    }
-    if (e != cudaSuccess) return -1;
-    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+    if (mode == kSummary)
+        e = launch_mode<D, DV, W, kSummary, true>(a, smem, st);
+    else if (mode == kStates)
+        e = launch_mode<D, DV, W, kStates, false>(a, smem, st);
+    else if (track_cm)
+        e = launch_mode<D, DV, W, kOutput, true>(a, smem, st);
+    else
+        e = launch_mode<D, DV, W, kOutput, false>(a, smem, st);
+    return e == cudaSuccess ? 0 : -1;
 }
 
 template <int D, int DV, int W>

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kSimtThreads)
 
     float *dS = nullptr, *dC = nullptr, *dZ = nullptr, *dm = nullptr, *dy = nullptr;
     if (summary) {
-        const size_t si = (size_t)bh * (nseg - 1) + seg;
+        const size_t si = (size_t)bh * a.nsum + seg;
         dS = a.ws + a.L.SB + si * D * D;
         dC = a.ws + a.L.CB + si * D * DV;
         dZ = a.ws + a.L.ZB + si * D * DV;

@@ -3,12 +3,12 @@
 
 namespace hla2 {
 
-int launch_fwd_chunk_mma_d64(const ChunkArgs& a, int W, bool summary, bool cm, cudaStream_t st) {
+int launch_fwd_chunk_mma_d64(const ChunkArgs& a, int W, int mode, bool cm, cudaStream_t st) {
     switch (W) {
-        case 16: return launch_fwd_chunk_mma_t<64, 64, 16>(a, summary, cm, st);
-        case 32: return launch_fwd_chunk_mma_t<64, 64, 32>(a, summary, cm, st);
-        case 64: return launch_fwd_chunk_mma_t<64, 64, 64>(a, summary, cm, st);
-        case 128: return launch_fwd_chunk_mma_t<64, 64, 128>(a, summary, cm, st);
+        case 16: return launch_fwd_chunk_mma_t<64, 64, 16>(a, mode, cm, st);
+        case 32: return launch_fwd_chunk_mma_t<64, 64, 32>(a, mode, cm, st);
+        case 64: return launch_fwd_chunk_mma_t<64, 64, 64>(a, mode, cm, st);
+        case 128: return launch_fwd_chunk_mma_t<64, 64, 128>(a, mode, cm, st);
         default: return -2;
     }
 }

@@ -19,17 +19,51 @@ struct ChunkArgs {
     int nchunks, seg_chunks, nseg;
     int seg0;         // first segment of this launch (blockIdx.x + seg0)
     int nseg_launch;  // segments in this launch (grid.x)
+    int nsum;         // segment summaries stored per head (nseg - 1, or nseg)
     const float* gamma;
     int normalize;
     float eps;
     int want_final;
     float* ws;        // forward workspace (floats)
     FwdLayout L;
+    bf16* chunk_states;  // state-export pass: bf16 (S | Z) at every chunk start, [BH][nchunks][d*d + d*dv]
 };
+
+// Chunk-kernel passes.
+enum ChunkMode { kSummary = 0, kOutput = 1, kStates = 2 };
+
+// Arguments of the reverse-mode chunk kernel (bf16, d == dv).
+struct BwdArgs {
+    const bf16* q;
+    const bf16* k;
+    const bf16* v;
+    const bf16* dout;
+    bf16* dq;
+    bf16* dk;
+    bf16* dv;
+    int BH, H, n, W, nchunks, seg_chunks, nseg;
+    const float* gamma;
+    float* ws;
+    size_t ZhB, ShB;           // reverse summaries, float offsets, [BH][nseg][...]
+    size_t Zh_end, Sh_end;     // reverse carries at segment ends, [BH][nseg][...]
+    const bf16* chunk_states;  // forward (S | Z) bf16 at every chunk start
+};
+
+// Reverse-mode chunk kernel: rsum = true stores each segment's reverse summary,
+// false writes dq, dk, dv.  d == dv in {16,32,64,128}; W in {16,32,64} (32 max for d = 128).
+int launch_bwd_chunk_mma(const BwdArgs& a, int d, int W, bool rsum, cudaStream_t st);
+size_t bwd_chunk_mma_smem(int d, int W);  // 0 if not compiled
+
+// Reverse decayed suffix scan over segments (segment lengths from n, W, seg_chunks):
+//   dst[nseg-1] = 0;  dst[s-1] = g^(power L_s) dst[s] + src[s]
+int launch_reverse_scan(const float* src, float* dst, int BH, int H, int nseg, size_t E,
+                        const float* gamma, int n, int W, int seg_chunks, int power, cudaStream_t st);
+// In place: ShB[s] += g^(L_s) Zh_end[s] C_B[s]^T for s >= 1.
+int launch_reverse_cross(const BwdArgs& b, const float* CB, int d, int dv, cudaStream_t st);
 
 // Tensor-core (mma.sync bf16) chunk kernel: d == dv in {16,32,64,128}, W in {16,32,64,128}.
 // Returns 0 on success, -1 on a CUDA error, -2 if the shape is not compiled.
-int launch_fwd_chunk_mma(const ChunkArgs& a, int d, int dv, int W, bool summary, bool track_cm,
+int launch_fwd_chunk_mma(const ChunkArgs& a, int d, int dv, int W, int mode, bool track_cm,
                          cudaStream_t st);
 size_t fwd_chunk_mma_smem(int d, int dv, int W, bool track_cm);  // 0 if not compiled
 

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int 
     float* Cs = sm + (size_t)D * D; // D x DV
     float* ms = Cs + (size_t)D * DV;
     const int s = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
-    const size_t sb = (size_t)bh * (a.nseg - 1) + s;  // summary index
+    const size_t sb = (size_t)bh * a.nsum + s;        // summary index
     const size_t si = (size_t)bh * a.nseg + s;        // carry index
     const float* Sin = a.ws + a.L.Sin + si * D * D;
     const float* CB = a.ws + a.L.CB + sb * D * DV;
@@ -185,6 +185,85 @@ int launch_finalize(const ChunkArgs& a, int d, int dv, float* final_state, cudaS
     if (a.BH <= 0) return 0;
     finalize_kernel<<<a.BH, kThreads, 0, st>>>(a, d, dv, final_state);
     return finish_launch();
+}
+
+}  // namespace hla2
+
+namespace hla2 {
+
+namespace {
+
+__device__ __forceinline__ int segment_tokens(int s, int n, int W, int seg_chunks) {
+    const long start = (long)s * seg_chunks * W;
+    const long len = (long)seg_chunks * W;
+    return (int)(n - start < len ? n - start : len);
+}
+
+// Reverse decayed suffix over segments, one thread per element:
+//   acc = 0 (nothing after the last segment); for s = nseg-1 .. 1:
+//   acc = g^(power L_s) acc + src[s];  dst[s-1] = acc.   dst[nseg-1] = 0.
+__global__ void __launch_bounds__(kThreads)
+    reverse_scan_kernel(const float* __restrict__ src, float* __restrict__ dst, int BH, int H, int nseg,
+                        size_t E, const float* gamma, int n, int W, int seg_chunks, int power) {
+    const size_t gid = (size_t)blockIdx.x * kThreads + threadIdx.x;
+    if (gid >= (size_t)BH * E) return;
+    const int bh = (int)(gid / E);
+    const size_t e = gid % E;
+    const float log2g = log2f(head_decay(gamma, bh, H));
+    const float* s_ = src + (size_t)bh * nseg * E + e;
+    float* d_ = dst + (size_t)bh * nseg * E + e;
+    float acc = 0.f;
+    d_[(size_t)(nseg - 1) * E] = 0.f;
+    for (int s = nseg - 1; s >= 1; --s) {
+        const float rho = pow_decay(log2g, (float)power * (float)segment_tokens(s, n, W, seg_chunks));
+        acc = rho * acc + s_[(size_t)s * E];
+        d_[(size_t)(s - 1) * E] = acc;
+    }
+}
+
+// ShB[s][f][a] += g^(L_s) sum_e Zh_end[s][f][e] C_B[s][a][e], for s >= 1.
+__global__ void __launch_bounds__(kThreads)
+    reverse_cross_kernel(const BwdArgs b, const float* CB, int D, int DV) {
+    extern __shared__ __align__(16) float sm[];
+    float* Zs = sm;                   // D x DV
+    float* Cs = sm + (size_t)D * DV;  // D x DV
+    const int s = blockIdx.x + 1, bh = blockIdx.y, tid = threadIdx.x;
+    const size_t si = (size_t)bh * b.nseg + s;
+    const float* Zh = b.ws + b.Zh_end + si * D * DV;
+    const float* C = CB + si * D * DV;
+    float* Sh = b.ws + b.ShB + si * D * D;
+    for (int i = tid; i < D * DV; i += kThreads) {
+        Zs[i] = Zh[i];
+        Cs[i] = C[i];
+    }
+    __syncthreads();
+    const float rho = pow_decay(log2f(head_decay(b.gamma, bh, b.H)), (float)segment_tokens(s, b.n, b.W, b.seg_chunks));
+    for (int i = tid; i < D * D; i += kThreads) {
+        const int f = i / D, x = i % D;
+        float acc = 0.f;
+        for (int e = 0; e < DV; ++e) acc += Zs[f * DV + e] * Cs[x * DV + e];
+        Sh[i] += rho * acc;
+    }
+}
+
+}  // namespace
+
+int launch_reverse_scan(const float* src, float* dst, int BH, int H, int nseg, size_t E, const float* gamma,
+                        int n, int W, int seg_chunks, int power, cudaStream_t st) {
+    const size_t total = (size_t)BH * E;
+    if (total == 0 || nseg <= 0) return 0;
+    reverse_scan_kernel<<<(unsigned)((total + kThreads - 1) / kThreads), kThreads, 0, st>>>(
+        src, dst, BH, H, nseg, E, gamma, n, W, seg_chunks, power);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_reverse_cross(const BwdArgs& b, const float* CB, int d, int dv, cudaStream_t st) {
+    if (b.nseg <= 1 || b.BH <= 0) return 0;
+    const size_t smem = 2 * (size_t)d * dv * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(reverse_cross_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return -1;
+    reverse_cross_kernel<<<dim3(b.nseg - 1, b.BH), kThreads, smem, st>>>(b, CB, d, dv);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace hla2

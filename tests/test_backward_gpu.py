@@ -1,0 +1,82 @@
+"""GPU reverse-mode chunk scan (dQ, dK, dV) against the float64 oracle's reverse sweep of
+the serial recurrence, through the C ABI.  Bar: max|gpu - oracle| / max|oracle| <= 2e-2
+per gradient (bf16 inputs; the oracle runs on the same bf16-rounded values)."""
+import pytest
+import torch
+
+import chunked_scan_mixer_gb300 as hla
+from chunked_scan_mixer_gb300 import HLA2Error, inputs
+from oracle import cref
+
+from .helpers import np32, np64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def run(x, chunk):
+    g = None if x["gamma"] is None else x["gamma"].cuda()
+    return hla.backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), gamma=g, chunk=chunk)
+
+
+def oracle(x):
+    g = None if x["gamma"] is None else x["gamma"].double().numpy()
+    return cref.backward(np32(x["q"]), np32(x["k"]), np32(x["v"]), np32(x["dout"]), g)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_gradients_match_oracle(d, chunk):
+    n = 3 * chunk + 7
+    x = inputs.make_custom(1, 3, n, d, d, torch.bfloat16, seed=d * 7 + chunk, gamma=(0.9, 0.999),
+                           with_dout=True)
+    got = run(x, chunk)
+    ref = oracle(x)
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, ref):
+        assert torch.isfinite(gg.float()).all(), name
+        assert rel_err(np64(gg.cpu()), rr) <= 2e-2, name
+
+
+@pytest.mark.parametrize("n", [1, 5, 64, 200, 1000])
+def test_lengths_and_segments(n):
+    x = inputs.make_custom(2, 2, n, 64, 64, torch.bfloat16, seed=n, gamma=(0.95, 0.995), with_dout=True)
+    got = run(x, 64)
+    ref = oracle(x)
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, ref):
+        assert rel_err(np64(gg.cpu()), rr) <= 2e-2, (name, n)
+
+
+def test_no_decay():
+    x = inputs.make_custom(1, 2, 500, 32, 32, torch.bfloat16, seed=3, gamma=None, with_dout=True)
+    got = run(x, 32)
+    ref = oracle(x)
+    for gg, rr in zip(got, ref):
+        assert rel_err(np64(gg.cpu()), rr) <= 2e-2
+
+
+def test_chunk_width_independence():
+    x = inputs.make_custom(1, 2, 333, 64, 64, torch.bfloat16, seed=4, gamma=(0.97, 0.999), with_dout=True)
+    a = [np64(t.cpu()) for t in run(x, 16)]
+    b = [np64(t.cpu()) for t in run(x, 64)]
+    for u, w in zip(a, b):
+        assert rel_err(u, w) <= 2e-2
+
+
+def test_training_workload_full_size_sampled():
+    """B=4, H=16, n=8192, d=dv=128, decay 0.995: the whole batch runs on the GPU; heads
+    (b=0, h=0), (b=1, h=7), (b=3, h=15) are compared with the oracle."""
+    w = inputs.WORKLOADS["train"]
+    x = inputs.make(w, device="cuda")
+    g = x["gamma"].cuda()
+    dq, dk, dv = hla.backward(x["q"], x["k"], x["v"], x["dout"], gamma=g, chunk=w.chunk)
+    for b, h in ((0, 0), (1, 7), (3, 15)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = cref.backward(np32(x["q"][sl]), np32(x["k"][sl]), np32(x["v"][sl]), np32(x["dout"][sl]),
+                            x["gamma"][h:h + 1].double().numpy())
+        for name, gg, rr in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+            assert rel_err(np64(gg[sl].cpu()), rr) <= 2e-2, (name, b, h)
+
+
+def test_unsupported_variants_are_reported():
+    x = inputs.make_custom(1, 1, 32, 16, 16, torch.float32, seed=5, with_dout=True)
+    with pytest.raises(HLA2Error):
+        run(x, 16)
