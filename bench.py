@@ -2,7 +2,7 @@
 """Benchmark of the masked HLA-2 forward on the long-context workload.
 
 Workload: B=1, H=16, n=65536, d=dv=64, bf16 inputs, fp32 state, unnormalised, per-head
-decay linspace(0.99, 0.9999), chunk width 64 (1,048,576 tokens per step; 536.9 MB of
+decay linspace(0.99, 0.9999), chunk width 128 (1,048,576 tokens per step; 536.9 MB of
 algorithmic traffic, larger than the 129 MB L2, so no flush is needed between steps).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -29,7 +29,7 @@ sys.path.insert(0, ROOT)
 METRIC = "HLA-2 masked fwd tokens/s (B·H·n/s) at n=64K,d=64; % tensor/HBM roofline"
 WORKLOAD = "long"
 CONFIG_NAME = ("long-context masked HLA-2 forward: B=1 H=16 n=65536 d=dv=64 bf16 in/out, "
-               "fp32 state, decay linspace(0.99,0.9999), unnormalised, chunk 64")
+               "fp32 state, decay linspace(0.99,0.9999), unnormalised, chunk 128")
 PHASES = ("carry_init", "segment_summaries", "segment_scan", "output_pass", "final_state")
 
 
@@ -202,7 +202,7 @@ def run_reference(args, dist: Dist):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": CONFIG_NAME, "B": 1, "H": 16, "n": 65536, "d": 64, "dv": 64, "chunk": 64},
+        "config": {"workload": CONFIG_NAME, "B": 1, "H": 16, "n": 65536, "d": 64, "dv": 64, "chunk": 128},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -215,7 +215,8 @@ def run_reference(args, dist: Dist):
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for rel in ("chunked_scan_mixer_gb300/csrc/fwd_chunk_mma.cuh", "chunked_scan_mixer_gb300/csrc/common.cuh"):
+    for rel in ("chunked_scan_mixer_gb300/csrc/fwd_chunk_tc.cu", "chunked_scan_mixer_gb300/csrc/tc_common.cuh",
+                "chunked_scan_mixer_gb300/csrc/common.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

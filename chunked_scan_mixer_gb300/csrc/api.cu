@@ -5,6 +5,9 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <stdlib.h>
+#include <string.h>
+
 #include <string>
 
 #include "kernels.h"
@@ -149,9 +152,19 @@ Plan make_plan(int B, int H, int n, int d, int dv, int W, int sms) {
     return p;
 }
 
-enum class Path { kMma, kSimt, kNone };
+enum class Path { kTc, kMma, kSimt, kNone };
 
-Path choose_forward_path(int dtype, int d, int dv, int W, const DevInfo& di) {
+// HLA2_KERNEL=mma forces the mma.sync chunk kernel where the tcgen05 one would be chosen
+// (used to test both paths on the same inputs).
+bool tc_disabled() {
+    const char* e = getenv("HLA2_KERNEL");
+    return e && strcmp(e, "mma") == 0;
+}
+
+Path choose_forward_path(int dtype, int d, int dv, int W, int normalize, bool want_final, const DevInfo& di) {
+    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !normalize && !want_final && !tc_disabled() &&
+        fwd_chunk_tc_smem() <= (size_t)di.smem_optin && fwd_chunk_tc_available())
+        return Path::kTc;
     if (dtype == HLA2_BF16) {
         const size_t s = fwd_chunk_mma_smem(d, dv, W, true);
         if (s > 0 && s <= (size_t)di.smem_optin) return Path::kMma;
@@ -221,7 +234,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
 
     const DevInfo di = dev_info();
-    const Path path = choose_forward_path(opts->dtype, d, dv, chunk, di);
+    const Path path = choose_forward_path(opts->dtype, d, dv, chunk, normalize, want_final, di);
     if (path == Path::kNone)
         return fail(HLA2_ERR_UNSUPPORTED, "no kernel for dtype %d, d %d, dv %d, chunk %d", opts->dtype, d, dv, chunk);
     const Plan p = make_plan(B, H, n, d, dv, chunk, di.sms);
@@ -257,6 +270,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         ChunkArgs b = a;
         b.seg0 = seg0;
         b.nseg_launch = count;
+        if (path == Path::kTc) return launch_fwd_chunk_tc(b, summary ? kSummary : kOutput, reinterpret_cast<int*>(a.ws), st);
         if (path == Path::kMma) return launch_fwd_chunk_mma(b, d, dv, chunk, summary ? kSummary : kOutput, cm, st);
         return launch_fwd_chunk_simt(b, d, dv, chunk, summary, cm, bf, st);
     };
@@ -304,6 +318,17 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     mark(4);
     if (want_final && launch_finalize(a, d, dv, opts->final_state, st)) return cuda_fail("final state");
     mark(5);
+    return succeed();
+}
+
+int hla2_workspace_status(const void* workspace, hla2_stream_t stream) {
+    if (!workspace) return fail(HLA2_ERR_INVALID_ARG, "workspace must not be NULL");
+    int code = 0;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&code, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return cuda_fail("status read");
+    if (code != 0) return fail(HLA2_ERR_TIMEOUT, "a bounded device-side wait gave up (site %d)", code);
     return succeed();
 }
 

@@ -24,7 +24,10 @@ struct Plan {
     int nseg;        // segments per head
 };
 
-// Float offsets of the forward workspace arrays (each 64-float aligned).
+// Float offsets of the forward workspace arrays (each 64-float aligned).  The first 64
+// floats hold the status word (an int at offset 0): kernels with bounded waits write a
+// nonzero code there when a wait gives up.
+constexpr size_t kStatusFloats = 64;
 struct FwdLayout {
     size_t SB, CB, ZB, mB, yB;   // summaries, [BH][nsum][...]
     size_t Sin, Zin, yin;        // carries,   [BH][nseg][...]
@@ -44,7 +47,7 @@ inline FwdLayout fwd_layout(const Plan& p, int nsum) {
     FwdLayout L;
     const size_t BH = p.BH, ns = p.nseg, nsm = nsum > 0 ? nsum : 0;
     const size_t dd = (size_t)p.d * p.d, ddv = (size_t)p.d * p.dv, d = p.d;
-    size_t o = 0;
+    size_t o = kStatusFloats;
     L.SB = o;    o = align64(o + BH * nsm * dd);
     L.CB = o;    o = align64(o + BH * nsm * ddv);
     L.ZB = o;    o = align64(o + BH * nsm * ddv);

@@ -67,6 +67,13 @@ int launch_fwd_chunk_mma(const ChunkArgs& a, int d, int dv, int W, int mode, boo
                          cudaStream_t st);
 size_t fwd_chunk_mma_smem(int d, int dv, int W, bool track_cm);  // 0 if not compiled
 
+// tcgen05 chunk kernel (bf16, d = dv = 64, chunk 128, unnormalised, modes kSummary and
+// kOutput).  status: int word in the workspace set on a wait timeout.  Returns 0, -1 (CUDA
+// error) or -2 (tensor maps unavailable).
+bool fwd_chunk_tc_available();
+size_t fwd_chunk_tc_smem();
+int launch_fwd_chunk_tc(const ChunkArgs& a, int mode, int* status, cudaStream_t st);
+
 // SIMT fp32-arithmetic chunk kernel, any d, dv <= 128 (multiples of 8), W <= 128;
 // inputs float32 (is_bf16 = false) or bf16.
 int launch_fwd_chunk_simt(const ChunkArgs& a, int d, int dv, int W, bool summary, bool track_cm,

@@ -26,6 +26,7 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(kThreads)
     init_carry_kernel(const ChunkArgs a, int D, int DV, const float* init) {
     const int bh = blockIdx.x, tid = threadIdx.x;
+    if (bh == 0 && tid == 0) *reinterpret_cast<int*>(a.ws) = 0;  // clear the status word
     const size_t s0 = (size_t)bh * a.nseg;  // segment 0 of this head
     float* Sin = a.ws + a.L.Sin + s0 * D * D;
     float* Zin = a.ws + a.L.Zin + s0 * D * DV;

@@ -73,6 +73,8 @@ def lib():
         L.hla2_forward_plan.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I),
                                         ctypes.POINTER(I)]
         L.hla2_forward_plan.restype = I
+        L.hla2_workspace_status.argtypes = [P, P]
+        L.hla2_workspace_status.restype = I
         L.hla2_backward_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
         L.hla2_backward_workspace_bytes.restype = Z
         L.hla2_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
@@ -85,7 +87,8 @@ def lib():
 
 EXPORTED_SYMBOLS = (
     "hla2_version", "hla2_last_error", "hla2_state_floats", "hla2_forward_workspace_bytes",
-    "hla2_forward", "hla2_forward_plan", "hla2_backward_workspace_bytes", "hla2_backward", "hla2_decode_step",
+    "hla2_forward", "hla2_forward_plan", "hla2_workspace_status", "hla2_backward_workspace_bytes",
+    "hla2_backward", "hla2_decode_step",
 )
 
 
@@ -115,6 +118,16 @@ def _workspace(nbytes, device, stream_handle):
         buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
         _ws_cache[key] = buf
     return buf
+
+
+def check_status(device=None):
+    """Raise HLA2Error if a kernel that used this stream's cached workspace reported a
+    timed-out wait.  Synchronises the current stream."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    sh = _stream_handle(device)
+    buf = _ws_cache.get((device.index, sh.value))
+    if buf is not None:
+        _check("hla2_workspace_status", lib().hla2_workspace_status(ctypes.c_void_p(buf.data_ptr()), sh))
 
 
 def state_floats(d, dv):

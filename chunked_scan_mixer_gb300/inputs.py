@@ -15,7 +15,7 @@ Workloads (sizes and distributions of the benchmark configurations):
   normed    B=2 H=8  n=2048  d=dv=64  bf16; q,k = softplus(N(0,1)), v ~ N(0,1);
             ratio-normalised (eps 1e-6); decay linspace(0.95, 0.999, H); chunk 64
   long      B=1 H=16 n=65536 d=dv=64  bf16; q,k,v ~ N(0,1)/sqrt(d); unnormalised;
-            decay linspace(0.99, 0.9999, H); chunk 64
+            decay linspace(0.99, 0.9999, H); chunk 128
   decode    256 sequences x H=32, d=dv=128; 4096-token bf16 prefill, N(0,1)/sqrt(d),
             decay 0.999; then single-token steps with fresh draws (seed 4000 + step)
   train     B=4 H=16 n=8192  d=dv=128 bf16; q,k,v ~ N(0,1)/sqrt(d); dO ~ N(0,1);
@@ -58,7 +58,7 @@ WORKLOADS = {
     "normed": Workload("normed", 2, 8, 2048, 64, 64, torch.bfloat16, 2, "softplus", "unit",
                        (0.95, 0.999), True, 1e-6, 64),
     "long": Workload("long", 1, 16, 65536, 64, 64, torch.bfloat16, 3, "gauss", "gauss_sqrt_d",
-                     (0.99, 0.9999), False, 1e-6, 64),
+                     (0.99, 0.9999), False, 1e-6, 128),
     "decode_prefill": Workload("decode_prefill", 256, 32, 4096, 128, 128, torch.bfloat16, 4,
                                "gauss", "gauss_sqrt_d", (0.999,), False, 1e-6, 64),
     "train": Workload("train", 4, 16, 8192, 128, 128, torch.bfloat16, 5, "gauss",

@@ -120,6 +120,14 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
 int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, int want_final_state,
                       int* nseg, int* seg_chunks, int* launches);
 
+/*
+ * Reads the status word at the start of a workspace used by hla2_forward / hla2_backward:
+ * HLA2_OK, or HLA2_ERR_TIMEOUT when a bounded device-side wait of a kernel gave up (the
+ * kernel then drained and returned; its outputs are not valid).  The word is cleared by
+ * the next call that uses the workspace.  Synchronises `stream`.
+ */
+int hla2_workspace_status(const void* workspace, hla2_stream_t stream);
+
 /* Scratch bytes hla2_backward needs; (size_t)-1 for rejected arguments. */
 size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype);
 

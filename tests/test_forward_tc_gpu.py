@@ -1,0 +1,70 @@
+"""The tcgen05 chunk kernels (bf16, d = dv = 64, chunk 128, unnormalised) against the float64
+oracle and against the mma.sync chunk kernels on the same inputs, through the C ABI."""
+import os
+
+import pytest
+import torch
+
+import chunked_scan_mixer_gb300 as hla
+from chunked_scan_mixer_gb300 import inputs
+from oracle import cref
+
+from .helpers import np32, np64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def run(x, kernel=None):
+    old = os.environ.pop("HLA2_KERNEL", None)
+    if kernel:
+        os.environ["HLA2_KERNEL"] = kernel
+    try:
+        g = None if x["gamma"] is None else x["gamma"].cuda()
+        o = hla.forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), gamma=g, chunk=128)
+        hla.check_status()
+        return o.cpu()
+    finally:
+        os.environ.pop("HLA2_KERNEL", None)
+        if old is not None:
+            os.environ["HLA2_KERNEL"] = old
+
+
+def oracle(x):
+    g = None if x["gamma"] is None else x["gamma"].double().numpy()
+    return cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), g)
+
+
+@pytest.mark.parametrize("n", [1, 64, 127, 128, 129, 300, 1000, 4096 + 33])
+def test_lengths(n):
+    x = inputs.make_custom(1, 3, n, 64, 64, torch.bfloat16, seed=n, gamma=(0.97, 0.9999))
+    o = run(x)
+    assert torch.isfinite(o.float()).all()
+    assert rel_err(np64(o), oracle(x)) <= 2e-2
+
+
+@pytest.mark.parametrize("gamma", [None, 0.9, (0.5, 0.999)])
+def test_decays(gamma):
+    x = inputs.make_custom(2, 2, 700, 64, 64, torch.bfloat16, seed=7, gamma=gamma)
+    assert rel_err(np64(run(x)), oracle(x)) <= 2e-2
+
+
+def test_matches_mma_path():
+    x = inputs.make_custom(1, 4, 2000, 64, 64, torch.bfloat16, seed=8, gamma=(0.99, 0.9999))
+    a = np64(run(x))
+    b = np64(run(x, kernel="mma"))
+    ref = oracle(x)
+    assert rel_err(a, ref) <= 2e-2 and rel_err(b, ref) <= 2e-2
+    assert rel_err(a, b) <= 2e-2
+
+
+def test_many_heads_one_segment_each():
+    x = inputs.make_custom(4, 80, 256, 64, 64, torch.bfloat16, seed=9, gamma=0.995)
+    o = run(x)
+    ref = oracle(x)
+    assert rel_err(np64(o), ref) <= 2e-2
+
+
+def test_repeated_calls_are_identical():
+    x = inputs.make_custom(1, 2, 1500, 64, 64, torch.bfloat16, seed=10, gamma=(0.98, 0.999))
+    a, b = run(x), run(x)
+    assert torch.equal(a, b)
