@@ -94,11 +94,15 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // X_s = Z_B[s] + rho S_in[s] C_B[s] and Xy_s = y_B[s] + rho S_in[s] m_B[s], in place.
-__global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int D, int DV, int seg_tokens) {
+// 256 threads in a 16 x 16 grid, each computing a (D/16) x (DV/16) block of X in fp32 from
+// shared-memory copies of S_in[s] and C_B[s].
+template <int TM, int TN>
+__global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int seg_tokens) {
+    constexpr int D = 16 * TM, DV = 16 * TN;
     extern __shared__ __align__(16) float sm[];
-    float* Ss = sm;                 // D x D
-    float* Cs = sm + (size_t)D * D; // D x DV
-    float* ms = Cs + (size_t)D * DV;
+    float* Ss = sm;            // D x D
+    float* Cs = Ss + D * D;    // D x DV
+    float* ms = Cs + D * DV;   // D
     const int s = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     const size_t sb = (size_t)bh * a.nsum + s;        // summary index
     const size_t si = (size_t)bh * a.nseg + s;        // carry index
@@ -112,16 +116,31 @@ __global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int 
     for (int i = tid; i < D; i += kThreads) ms[i] = mB[i];
     __syncthreads();
     const float rho = pow_decay(log2f(head_decay(a.gamma, bh, a.H)), (float)seg_tokens);
-    for (int i = tid; i < D * DV; i += kThreads) {
-        const int r = i / DV, c = i % DV;
-        float acc = 0.f;
-        for (int x = 0; x < D; ++x) acc += Ss[r * D + x] * Cs[x * DV + c];
-        ZB[i] += rho * acc;
+    const int tr = tid / 16, tcn = tid % 16;
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+    for (int x = 0; x < D; ++x) {
+        float av[TM], bv[TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) av[i] = Ss[(tr + 16 * i) * D + x];
+#pragma unroll
+        for (int j = 0; j < TN; ++j) bv[j] = Cs[x * DV + tcn + 16 * j];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] += av[i] * bv[j];
     }
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) ZB[(size_t)(tr + 16 * i) * DV + tcn + 16 * j] += rho * acc[i][j];
     for (int r = tid; r < D; r += kThreads) {
-        float acc = 0.f;
-        for (int x = 0; x < D; ++x) acc += Ss[r * D + x] * ms[x];
-        yB[r] += rho * acc;
+        float t = 0.f;
+        for (int x = 0; x < D; ++x) t += Ss[r * D + x] * ms[x];
+        yB[r] += rho * t;
     }
 }
 
@@ -171,15 +190,31 @@ int launch_linear_scan(const float* src, float* dst, int BH, int H, int nsteps, 
     return finish_launch();
 }
 
+template <int TM, int TN>
+int launch_cross_t(const ChunkArgs& a, cudaStream_t st) {
+    constexpr int D = 16 * TM, DV = 16 * TN;
+    const size_t smem = (size_t)(D * D + D * DV + D) * sizeof(float);
+    if (cudaFuncSetAttribute(cross_kernel<TM, TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return -1;
+    cross_kernel<TM, TN><<<dim3(a.nseg - 1, a.BH), kThreads, smem, st>>>(a, a.seg_chunks * a.W);
+    return finish_launch();
+}
+
+// d, dv in {16, 32, 64, 128}; the largest (128 x 128) needs 128 KB of shared memory.
 int launch_cross(const ChunkArgs& a, int d, int dv, cudaStream_t st) {
     if (a.nseg <= 1 || a.BH <= 0) return 0;
-    const size_t smem = ((size_t)d * d + (size_t)d * dv + d) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(cross_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return -1;
-    dim3 grid(a.nseg - 1, a.BH);
-    cross_kernel<<<grid, kThreads, smem, st>>>(a, d, dv, a.seg_chunks * a.W);
-    return finish_launch();
+#define HLA2_CROSS(DD, VV)                                   \
+    if (d == DD && dv == VV) {                               \
+        constexpr int TM = DD / 16, TN = VV / 16;             \
+        return launch_cross_t<TM, TN>(a, st);               \
+    }
+    HLA2_CROSS(16, 16) HLA2_CROSS(16, 32) HLA2_CROSS(16, 64) HLA2_CROSS(16, 128)
+    HLA2_CROSS(32, 16) HLA2_CROSS(32, 32) HLA2_CROSS(32, 64) HLA2_CROSS(32, 128)
+    HLA2_CROSS(64, 16) HLA2_CROSS(64, 32) HLA2_CROSS(64, 64) HLA2_CROSS(64, 128)
+    HLA2_CROSS(128, 16) HLA2_CROSS(128, 32) HLA2_CROSS(128, 64) HLA2_CROSS(128, 128)
+#undef HLA2_CROSS
+    return -1;
 }
 
 int launch_finalize(const ChunkArgs& a, int d, int dv, float* final_state, cudaStream_t st) {
