@@ -295,6 +295,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float first = r >= cb ? gp[r - cb] : 0.f;
                 masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, ginv);
             }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[BAT]);
+            // K~ (and Q~ in summary mode) rows, features 32h .. 32h+31, while MMA2 runs; they
+            // are first read by the MMAs issued after EPI2 / EPI3 (fenced there)
             {
                 const float w1 = r < Wc ? gp[Wc - 1 - r] : 0.f;
 #pragma unroll
@@ -305,11 +311,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                         *reinterpret_cast<uint4*>(sP + off) = scale_chunk(*reinterpret_cast<const uint4*>(sQ + off), w1);
                 }
             }
-            tc::tmem_wait_st();
-            tc::fence_proxy_async();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[BAT]);
 
             // ---- EPI2: P = g^(r+1) Q S0 + A~ K;  P, P~ -> smem ---------------------------
             tc::mbar_wait(&bars[BP], ph, abort, status, 14);

@@ -48,15 +48,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity.  Gives up after a bounded number of tries
-// (each try_wait may suspend for a short while): then it raises *abort and records `where`
-// in the status word, so that every waiter drains instead of hanging.
-constexpr uint32_t kWaitLimit = 1u << 24;
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity by polling (no suspension, so the waiter resumes
+// as soon as the phase completes).  Gives up after a bounded number of polls (well over a
+// second): then it raises *abort and records `where` in the status word, so that every
+// waiter drains instead of hanging.
+constexpr uint32_t kWaitLimit = 1u << 27;
 __device__ __forceinline__ void mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
                                           int where) {
     for (uint32_t it = 0; it < kWaitLimit; ++it) {
-        if (mbar_try_wait(bar, parity)) return;
-        if (*abort) return;
+        if (mbar_test_wait(bar, parity)) return;
+        if ((it & 63) == 63 && *abort) return;
     }
     *abort = 1;
     if (status) atomicCAS(status, 0, where);
