@@ -96,6 +96,23 @@ int succeed() {
     return HLA2_OK;
 }
 
+}  // namespace
+
+namespace hla2 {
+// Records the message returned by hla2_last_error() for entry points in other files.
+int set_last_error(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+}  // namespace hla2
+
+namespace {
+
 int cuda_fail(const char* what) {
     const cudaError_t e = cudaGetLastError();
     return fail(HLA2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));

@@ -81,6 +81,8 @@ def lib():
         L.hla2_backward.restype = I
         L.hla2_decode_step.argtypes = [P, P, P, P, P, I, I, I, I, P, I, P, ctypes.POINTER(Opts)]
         L.hla2_decode_step.restype = I
+        L.hla2_forward_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, I, F, P]
+        L.hla2_forward_noalloc.restype = I
         _lib = L
         return L
 
@@ -88,7 +90,7 @@ def lib():
 EXPORTED_SYMBOLS = (
     "hla2_version", "hla2_last_error", "hla2_state_floats", "hla2_forward_workspace_bytes",
     "hla2_forward", "hla2_forward_plan", "hla2_workspace_status", "hla2_backward_workspace_bytes",
-    "hla2_backward", "hla2_decode_step",
+    "hla2_backward", "hla2_decode_step", "hla2_forward_noalloc",
 )
 
 

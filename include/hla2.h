@@ -153,6 +153,29 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
                      int N, int H, int d, int dv, const float* gamma, int normalize,
                      hla2_stream_t stream, const hla2_opts* opts);
 
+/*
+ * hla2_forward for callers that cannot allocate device memory (no counterpart in the
+ * paper: it exists for the library's users).  Some callers have no way to provide the
+ * scratch workspace that hla2_forward needs: code running inside a CUDA graph capture,
+ * where allocation calls are not allowed, plug-in hosts that hand a kernel only its input
+ * and output buffers, or programs with no device allocator of their own.  This entry point
+ * takes the same tensors and flags as hla2_forward (dtype and eps given directly; no
+ * initial or final state) and allocates nothing: its scratch is a fixed 32 MiB array in
+ * the library's device memory, present on every GPU on which the library's kernels are
+ * loaded and held until the process exits.
+ *   - Sizes whose workspace (hla2_forward_workspace_bytes) exceeds 32 MiB are rejected
+ *     with HLA2_ERR_WORKSPACE and a message; use hla2_forward with a workspace for them.
+ *   - The first call on a device looks up the array's device address for that device;
+ *     make that first call before any stream capture on the device.
+ *   - All calls on a device share the array, which keeps the last call's contents (nothing
+ *     in it needs to start at zero).  Calls whose executions overlap on the GPU (different
+ *     streams, or graphs running concurrently) race on it and give wrong results:
+ *     serialise them.
+ */
+int hla2_forward_noalloc(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
+                         int d, int dv, const float* gamma, int normalize, int chunk, int dtype,
+                         float eps, hla2_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
