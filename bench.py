@@ -91,6 +91,16 @@ class Dist:
             self.dist.destroy_process_group()
 
 
+def replica_seed(base: int, rank: int) -> int:
+    """Seed of rank ``rank``'s replica: every rank draws its own copy of the workload."""
+    return base + 1000 * rank
+
+
+def weak_scaling_value(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: all ranks' tokens over the slowest rank's time per step."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 # ---------------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------------
@@ -249,7 +259,7 @@ def run_ours(args, dist: Dist):
         import dataclasses
         w = dataclasses.replace(w, n=args.n)
     tokens = w.B * w.H * w.n
-    x = inputs.make(w, device=dev, seed=w.seed + 1000 * dist.rank)
+    x = inputs.make(w, device=dev, seed=replica_seed(w.seed, dist.rank))
     q, k, v = x["q"], x["k"], x["v"]
     gamma = x["gamma"].to(dev)
     out = torch.empty_like(v)
@@ -286,7 +296,7 @@ def run_ours(args, dist: Dist):
     clk = clocks.stop(wall0, wall1)
     ms_total = dist.max(t_start.elapsed_time(t_end))
     ms_per_step = ms_total / K
-    value = dist.world * tokens / (ms_per_step * 1e-3)
+    value = weak_scaling_value(dist.world, tokens, ms_per_step)
 
     # per-phase device time (events on the launching stream)
     ph = {name: 0.0 for name in PHASES}
@@ -333,7 +343,7 @@ def run_ours(args, dist: Dist):
             hla.forward(qh, kh, vh, gamma=gamma, chunk=w.chunk, out=oh)
         torch.cuda.synchronize()
         dt = dist.max(time.perf_counter() - t0) / Ke
-        e2e = {"value": dist.world * tokens / dt, "unit": "tokens/s",
+        e2e = {"value": weak_scaling_value(dist.world, tokens, dt * 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
                "d2h_bytes_per_step": out.numel() * out.element_size(), "steps": Ke}
 
