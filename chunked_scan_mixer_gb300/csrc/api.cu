@@ -316,11 +316,13 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
                                    gamma, seg_tokens, 1, st))
                 return cuda_fail("query-value scan");
         }
-        if (launch_cross(a, d, dv, st)) return cuda_fail("cross terms");
+        // the denominator moment y is read only by the normalised output and the final state
+        const bool with_y = normalize || want_final;
+        if (launch_cross(a, d, dv, with_y, st)) return cuda_fail("cross terms");
         if (launch_linear_scan(a.ws + L.ZB, a.ws + L.Zin, a.BH, H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true,
                                gamma, seg_tokens, 2, st) ||
-            launch_linear_scan(a.ws + L.yB, a.ws + L.yin, a.BH, H, steps, d, a.nsum * (size_t)d, p.nseg * (size_t)d,
-                               true, gamma, seg_tokens, 2, st))
+            (with_y && launch_linear_scan(a.ws + L.yB, a.ws + L.yin, a.BH, H, steps, d, a.nsum * (size_t)d,
+                                          p.nseg * (size_t)d, true, gamma, seg_tokens, 2, st)))
             return cuda_fail("masked-summary scan");
     } else {
         mark(2);
@@ -349,16 +351,17 @@ int hla2_workspace_status(const void* workspace, hla2_stream_t stream) {
     return succeed();
 }
 
-int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, int want_final_state,
-                      int* nseg, int* seg_chunks, int* launches) {
-    int rc = check_common(B, H, n, d, dv, dtype, 0);
+int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize,
+                      int want_final_state, int* nseg, int* seg_chunks, int* launches) {
+    int rc = check_common(B, H, n, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
     if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
     const Plan p = make_plan(B, H, n, d, dv, chunk, dev_info().sms);
     int l = 0;
     if (p.nseg > 0) {
         l = 2;                                                   // carry-in, output pass
-        if (p.nseg > 1) l += 5 + (want_final_state ? 2 : 0);     // summary, scans, cross
+        if (p.nseg > 1)                                          // summary, S/Z scans, cross; y, C, m scans
+            l += 4 + (normalize || want_final_state ? 1 : 0) + (want_final_state ? 2 : 0);
         if (want_final_state) l += 1 + (p.nseg > 1 ? 1 : 0);     // finalize, last-segment pass
     } else if (want_final_state && (long)B * H > 0) {
         l = 0;                                                   // a copy or memset only
@@ -512,7 +515,7 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
         if (pass(kSummary)) return cuda_fail("segment summaries");
         if (launch_linear_scan(ws + L.F.SB, ws + L.F.Sin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true, gamma,
                                seg_tokens, 1, st) ||
-            launch_cross(a, d, dv, st) ||
+            launch_cross(a, d, dv, false, st) ||
             launch_linear_scan(ws + L.F.ZB, ws + L.F.Zin, a.BH, H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true, gamma,
                                seg_tokens, 2, st))
             return cuda_fail("forward segment scan");

@@ -85,7 +85,7 @@ int launch_init_carry(const ChunkArgs& a, int d, int dv, const float* init_state
 int launch_linear_scan(const float* src, float* dst, int BH, int H, int nsteps, size_t E,
                        size_t src_head_stride, size_t dst_head_stride, bool store_all,
                        const float* gamma, int step_tokens, int power, cudaStream_t st);
-int launch_cross(const ChunkArgs& a, int d, int dv, cudaStream_t st);
+int launch_cross(const ChunkArgs& a, int d, int dv, bool with_y, cudaStream_t st);
 int launch_finalize(const ChunkArgs& a, int d, int dv, float* final_state, cudaStream_t st);
 
 // Decode step.

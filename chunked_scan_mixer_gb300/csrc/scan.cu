@@ -93,10 +93,30 @@ __global__ void __launch_bounds__(kThreads)
     if (!store_all) d[0] = acc;
 }
 
-// X_s = Z_B[s] + rho S_in[s] C_B[s] and Xy_s = y_B[s] + rho S_in[s] m_B[s], in place.
-// 256 threads in a 16 x 16 grid, each computing a (D/16) x (DV/16) block of X in fp32 from
-// shared-memory copies of S_in[s] and C_B[s].
-template <int TM, int TN>
+// Copy n floats (n a multiple of 4, both pointers 16-byte aligned) from global to shared
+// memory: every load of a thread is issued before its first store, so that the L2 round
+// trips overlap.
+template <int N>
+__device__ __forceinline__ void copy_to_smem(float* dst, const float* __restrict__ src, int tid) {
+    static_assert(N % 4 == 0, "float4 copies");
+    constexpr int N4 = N / 4, IT = (N4 + kThreads - 1) / kThreads;
+    float4 r[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+        const int i = tid + k * kThreads;
+        if (i < N4) r[k] = reinterpret_cast<const float4*>(src)[i];
+    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+        const int i = tid + k * kThreads;
+        if (i < N4) reinterpret_cast<float4*>(dst)[i] = r[k];
+    }
+}
+
+// X_s = Z_B[s] + rho S_in[s] C_B[s] (and, with WITH_Y, Xy_s = y_B[s] + rho S_in[s] m_B[s]),
+// in place.  256 threads in a 16 x 16 grid; thread (tr, tc) computes rows tr + 16 i and the
+// TN consecutive columns TN tc .. of X in fp32 from shared-memory copies of S_in[s], C_B[s].
+template <int TM, int TN, bool WITH_Y>
 __global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int seg_tokens) {
     constexpr int D = 16 * TM, DV = 16 * TN;
     extern __shared__ __align__(16) float sm[];
@@ -108,26 +128,32 @@ __global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int 
     const size_t si = (size_t)bh * a.nseg + s;        // carry index
     const float* Sin = a.ws + a.L.Sin + si * D * D;
     const float* CB = a.ws + a.L.CB + sb * D * DV;
-    const float* mB = a.ws + a.L.mB + sb * D;
     float* ZB = a.ws + a.L.ZB + sb * D * DV;
-    float* yB = a.ws + a.L.yB + sb * D;
-    for (int i = tid; i < D * D; i += kThreads) Ss[i] = Sin[i];
-    for (int i = tid; i < D * DV; i += kThreads) Cs[i] = CB[i];
-    for (int i = tid; i < D; i += kThreads) ms[i] = mB[i];
+    copy_to_smem<D * D>(Ss, Sin, tid);
+    copy_to_smem<D * DV>(Cs, CB, tid);
+    if (WITH_Y)
+        for (int i = tid; i < D; i += kThreads) ms[i] = a.ws[a.L.mB + sb * D + i];
+    const int tr = tid / 16, tc0 = (tid % 16) * TN;
+    // this thread's part of Z_B, loaded while the copies land
+    float zb[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) zb[i][j] = ZB[(size_t)(tr + 16 * i) * DV + tc0 + j];
     __syncthreads();
     const float rho = pow_decay(log2f(head_decay(a.gamma, bh, a.H)), (float)seg_tokens);
-    const int tr = tid / 16, tcn = tid % 16;
     float acc[TM][TN];
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
     for (int x = 0; x < D; ++x) {
         float av[TM], bv[TN];
 #pragma unroll
         for (int i = 0; i < TM; ++i) av[i] = Ss[(tr + 16 * i) * D + x];
 #pragma unroll
-        for (int j = 0; j < TN; ++j) bv[j] = Cs[x * DV + tcn + 16 * j];
+        for (int j = 0; j < TN; ++j) bv[j] = Cs[x * DV + tc0 + j];
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -136,11 +162,14 @@ __global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int 
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < TN; ++j) ZB[(size_t)(tr + 16 * i) * DV + tcn + 16 * j] += rho * acc[i][j];
-    for (int r = tid; r < D; r += kThreads) {
-        float t = 0.f;
-        for (int x = 0; x < D; ++x) t += Ss[r * D + x] * ms[x];
-        yB[r] += rho * t;
+        for (int j = 0; j < TN; ++j) ZB[(size_t)(tr + 16 * i) * DV + tc0 + j] = zb[i][j] + rho * acc[i][j];
+    if (WITH_Y) {
+        float* yB = a.ws + a.L.yB + sb * D;
+        for (int r = tid; r < D; r += kThreads) {
+            float t = 0.f;
+            for (int x = 0; x < D; ++x) t += Ss[r * D + x] * ms[x];
+            yB[r] += rho * t;
+        }
     }
 }
 
@@ -190,24 +219,26 @@ int launch_linear_scan(const float* src, float* dst, int BH, int H, int nsteps, 
     return finish_launch();
 }
 
-template <int TM, int TN>
+template <int TM, int TN, bool WITH_Y>
 int launch_cross_t(const ChunkArgs& a, cudaStream_t st) {
     constexpr int D = 16 * TM, DV = 16 * TN;
     const size_t smem = (size_t)(D * D + D * DV + D) * sizeof(float);
-    if (cudaFuncSetAttribute(cross_kernel<TM, TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(cross_kernel<TM, TN, WITH_Y>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return -1;
-    cross_kernel<TM, TN><<<dim3(a.nseg - 1, a.BH), kThreads, smem, st>>>(a, a.seg_chunks * a.W);
+    cross_kernel<TM, TN, WITH_Y><<<dim3(a.nseg - 1, a.BH), kThreads, smem, st>>>(a, a.seg_chunks * a.W);
     return finish_launch();
 }
 
 // d, dv in {16, 32, 64, 128}; the largest (128 x 128) needs 128 KB of shared memory.
-int launch_cross(const ChunkArgs& a, int d, int dv, cudaStream_t st) {
+// with_y adds the denominator moment's cross term (needed by the normalised output and the
+// final state only).
+int launch_cross(const ChunkArgs& a, int d, int dv, bool with_y, cudaStream_t st) {
     if (a.nseg <= 1 || a.BH <= 0) return 0;
-#define HLA2_CROSS(DD, VV)                                   \
-    if (d == DD && dv == VV) {                               \
-        constexpr int TM = DD / 16, TN = VV / 16;             \
-        return launch_cross_t<TM, TN>(a, st);               \
+#define HLA2_CROSS(DD, VV)                                                                   \
+    if (d == DD && dv == VV) {                                                               \
+        constexpr int TM = DD / 16, TN = VV / 16;                                             \
+        return with_y ? launch_cross_t<TM, TN, true>(a, st) : launch_cross_t<TM, TN, false>(a, st); \
     }
     HLA2_CROSS(16, 16) HLA2_CROSS(16, 32) HLA2_CROSS(16, 64) HLA2_CROSS(16, 128)
     HLA2_CROSS(32, 16) HLA2_CROSS(32, 32) HLA2_CROSS(32, 64) HLA2_CROSS(32, 128)

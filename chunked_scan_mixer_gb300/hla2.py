@@ -70,7 +70,7 @@ def lib():
         L.hla2_forward_workspace_bytes.restype = Z
         L.hla2_forward.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
         L.hla2_forward.restype = I
-        L.hla2_forward_plan.argtypes = [I, I, I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I),
+        L.hla2_forward_plan.argtypes = [I, I, I, I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I),
                                         ctypes.POINTER(I)]
         L.hla2_forward_plan.restype = I
         L.hla2_workspace_status.argtypes = [P, P]
@@ -145,10 +145,10 @@ def forward_workspace_bytes(B, H, n, d, dv, chunk=64, dtype=torch.bfloat16, norm
     return int(r)
 
 
-def forward_plan(B, H, n, d, dv, chunk=64, dtype=torch.bfloat16, want_final_state=False):
+def forward_plan(B, H, n, d, dv, chunk=64, dtype=torch.bfloat16, normalize=False, want_final_state=False):
     """(segments per head, chunks per segment, kernel launches per call)."""
     ns, sc, nl = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    _check("hla2_forward_plan", lib().hla2_forward_plan(B, H, n, d, dv, chunk, _DTYPES[dtype],
+    _check("hla2_forward_plan", lib().hla2_forward_plan(B, H, n, d, dv, chunk, _DTYPES[dtype], int(normalize),
                                                         int(want_final_state), ctypes.byref(ns),
                                                         ctypes.byref(sc), ctypes.byref(nl)))
     return ns.value, sc.value, nl.value

@@ -115,10 +115,11 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
 /*
  * The segmentation hla2_forward will use for these arguments on the current device:
  * *nseg segments of *seg_chunks chunks per head, and *launches kernel launches per
- * call.  Any output pointer may be NULL.  Returns HLA2_OK or HLA2_ERR_INVALID_ARG.
+ * call (normalize and want_final_state as passed to hla2_forward).  Any output pointer
+ * may be NULL.  Returns HLA2_OK or HLA2_ERR_INVALID_ARG.
  */
-int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, int want_final_state,
-                      int* nseg, int* seg_chunks, int* launches);
+int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize,
+                      int want_final_state, int* nseg, int* seg_chunks, int* launches);
 
 /*
  * Reads the status word at the start of a workspace used by hla2_forward / hla2_backward:

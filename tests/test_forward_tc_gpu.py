@@ -68,3 +68,13 @@ def test_repeated_calls_are_identical():
     x = inputs.make_custom(1, 2, 1500, 64, 64, torch.bfloat16, seed=10, gamma=(0.98, 0.999))
     a, b = run(x), run(x)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("B,H,n", [(4, 80, 1000), (1, 16, 128 * 60 + 77), (1, 8, 128 * 100 + 1), (1, 2, 128 * 500 + 64)])
+def test_multi_chunk_segments(B, H, n):
+    """Segments of several chunks (odd and even counts, ragged last chunk): exercises the
+    double-buffered key loads and the carried state inside one CTA."""
+    nseg, seg_chunks, _ = hla.forward_plan(B, H, n, 64, 64, 128)
+    assert seg_chunks >= 3
+    x = inputs.make_custom(B, H, n, 64, 64, torch.bfloat16, seed=n % 1000, gamma=(0.98, 0.9999))
+    assert rel_err(np64(run(x)), oracle(x)) <= 2e-2
