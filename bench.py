@@ -7,6 +7,10 @@ algorithmic traffic, larger than the 129 MB L2, so no flush is needed between st
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+After the timed headline it measures two more rows of the path on their own workloads
+(reported under "secondary"): the decode step (256 sequences x 32 heads, d = dv = 128)
+and a training step (forward + backward, B=4 H=16 n=8192 d = dv = 128).
+
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own replica
 of the workload (weak scaling, no collective in the data path); the timed region is
 bracketed by barriers and the slowest rank's time is reported.
@@ -41,6 +45,8 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the decode and training rows measured after the headline")
     ap.add_argument("--n", type=int, default=None,
                     help="override the sequence length (smaller case for ncu --set full captures; "
                          "the reported metric is only valid at the default)")
@@ -246,6 +252,96 @@ def recorded_traffic(kernel: str):
     return ent.get("bytes_per_launch")
 
 
+def _device_ms(fn, steps, warmup, stream_sync):
+    """Mean device time of fn() over `steps` calls after `warmup` calls (CUDA events on the
+    current stream, synchronised on both sides)."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    stream_sync()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        fn()
+    t1.record()
+    stream_sync()
+    return t0.elapsed_time(t1) / steps
+
+
+def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5):
+    """Decode row: 256 sequences x 32 heads, d = dv = 128, one single-token step per
+    iteration on a resident fp32 state (the state's values do not change the work: it
+    starts from N(0, 1e-4) draws instead of a 4096-token prefill).  Inputs of every step
+    are drawn before timing (seed 4000 + step); the 1.6 GB state exceeds the L2."""
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = inputs.WORKLOADS["decode_prefill"]
+    N, H, d, dv = w.B, w.H, w.d, w.dv
+    sf = hla.state_floats(d, dv)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(replica_seed(w.seed, dist.rank))
+    state = torch.randn((N, H, sf), generator=gen, device=dev, dtype=torch.float32) * 1e-2
+    gamma = inputs.gammas(w).to(dev)
+    xs = [inputs.decode_step_inputs(i, N, H, d, dv, w.dtype, device=dev) for i in range(steps)]
+    out = torch.empty((N, H, dv), dtype=w.dtype, device=dev)
+    it = [0]
+
+    def one():
+        q, k, v = xs[it[0] % steps]
+        it[0] += 1
+        hla.decode_step(state, q, k, v, gamma=gamma, out=out)
+
+    ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
+    heads = N * H
+    nbytes = 2 * heads * sf * 4 + heads * (2 * d + dv) * 2 + heads * dv * 2
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"decode step: {N} sequences x H={H}, d=dv={d}, fp32 state, bf16 q/k/v/out, "
+                        f"decay {w.gamma[0]}, unnormalised",
+            "metric": "decode tokens/s (sequences x heads per second)", "unit": "tokens/s",
+            "value": dist.world * heads / (ms * 1e-3), "us_per_step": ms * 1e3, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes}}
+
+
+def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: int = 10, warmup: int = 3):
+    """Training row: B=4 H=16 n=8192 d=dv=128 bf16, decay 0.995, unnormalised; one step =
+    forward + backward (dq, dk, dv) through the public calls, inputs resident."""
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = inputs.WORKLOADS["train"]
+    x = inputs.make(w, device=dev, seed=replica_seed(w.seed, dist.rank))
+    q, k, v, do = x["q"], x["k"], x["v"], x["dout"]
+    gamma = x["gamma"].to(dev)
+    out = torch.empty_like(v)
+    gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def one():
+        hla.forward(q, k, v, gamma=gamma, chunk=w.chunk, out=out)
+        hla.backward(q, k, v, do, gamma=gamma, chunk=w.chunk, dq=gq, dk=gk, dv=gv)
+
+    ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
+    tokens = w.B * w.H * w.n
+    flops = 3 * tokens * 368640  # forward F(64) + backward 2 F(64) at d = dv = 128
+    nbytes = tokens * ((2 * w.d + w.dv) * 2 + w.dv * 2)  # forward
+    nbytes += tokens * ((2 * w.d + 2 * w.dv) * 2 + (2 * w.d + w.dv) * 2)  # backward reads, writes
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"workload": f"training step (forward + backward): B={w.B} H={w.H} n={w.n} d=dv={w.d} bf16, "
+                        f"decay {w.gamma[0]}, unnormalised, chunk {w.chunk}",
+            "metric": "training tokens/s (forward + backward)", "unit": "tokens/s",
+            "value": dist.world * tokens / (ms * 1e-3), "ms_per_step": ms, "steps": steps,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16_tflops, "unit": "TFLOP/s",
+                         "frac": achieved / bf16_tflops, "flops_per_step": flops,
+                         "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_gbs}}
+
+
 def run_ours(args, dist: Dist):
     import torch
 
@@ -263,7 +359,7 @@ def run_ours(args, dist: Dist):
     q, k, v = x["q"], x["k"], x["v"]
     gamma = x["gamma"].to(dev)
     out = torch.empty_like(v)
-    nseg, seg_chunks, launches = hla.forward_plan(w.B, w.H, w.n, w.d, w.dv, w.chunk)
+    nseg, seg_chunks, launches = hla.forward_plan(w.B, w.H, w.n, w.d, w.dv, w.chunk, normalize=w.normalize)
 
     def step(evs=None):
         hla.forward(q, k, v, gamma=gamma, chunk=w.chunk, out=out, phase_events=evs)
@@ -347,6 +443,11 @@ def run_ours(args, dist: Dist):
                "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
                "d2h_bytes_per_step": out.numel() * out.element_size(), "steps": Ke}
 
+    secondary = None
+    if not args.no_secondary and args.n is None:
+        secondary = {"decode": measure_decode(dev, dist, hbm_gbs),
+                     "train": measure_train(dev, dist, bf16_tflops, hbm_gbs)}
+
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         val, cores, desc = oracle_sample(target_s=15.0)
@@ -361,7 +462,7 @@ def run_ours(args, dist: Dist):
                        "chunk": w.chunk, "segments_per_head": nseg, "chunks_per_segment": seg_chunks,
                        "l2": f"inputs + output ({io_mb:.1f} MB) exceed the 129 MB L2; no flush"},
             "roofline": roofline, "whole_step": whole, "phases_ms": ph, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches * K, "clocks": clk,
+            "gpu_launches": launches * K, "clocks": clk, "secondary": secondary,
         }
         print(json.dumps(line), flush=True)
 
