@@ -288,29 +288,81 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// ShB[s][f][a] += g^(L_s) sum_e Zh_end[s][f][e] C_B[s][a][e], for s >= 1.
-__global__ void __launch_bounds__(kThreads)
-    reverse_cross_kernel(const BwdArgs b, const float* CB, int D, int DV) {
+// ShB[s][f][a] += g^(L_s) sum_e Zh_end[s][f][e] C_B[s][a][e], for s >= 1: X = Zh C_B^T.
+// 256 threads in a 16 x 16 grid; thread (tr, tc) computes rows tr + 16 i and the D/16
+// consecutive columns of X from shared-memory copies of Zh_end[s] and C_B[s]^T (the latter
+// stored with a row pitch of D + 1 floats).
+template <int D, int DV>
+__global__ void __launch_bounds__(kThreads) reverse_cross_kernel(const BwdArgs b, const float* CB) {
+    constexpr int TM = D / 16, TN = D / 16, CP = D + 1;
     extern __shared__ __align__(16) float sm[];
-    float* Zs = sm;                   // D x DV
-    float* Cs = sm + (size_t)D * DV;  // D x DV
+    float* Zs = sm;            // D x DV
+    float* Ct = sm + D * DV;   // DV x CP (transposed C_B)
     const int s = blockIdx.x + 1, bh = blockIdx.y, tid = threadIdx.x;
     const size_t si = (size_t)bh * b.nseg + s;
     const float* Zh = b.ws + b.Zh_end + si * D * DV;
     const float* C = CB + si * D * DV;
     float* Sh = b.ws + b.ShB + si * D * D;
-    for (int i = tid; i < D * DV; i += kThreads) {
-        Zs[i] = Zh[i];
-        Cs[i] = C[i];
+    copy_to_smem<D * DV>(Zs, Zh, tid);
+    {
+        constexpr int N4 = D * DV / 4, IT = (N4 + kThreads - 1) / kThreads;
+        float4 r[IT];
+#pragma unroll
+        for (int k = 0; k < IT; ++k) {
+            const int i = tid + k * kThreads;
+            if (i < N4) r[k] = reinterpret_cast<const float4*>(C)[i];
+        }
+#pragma unroll
+        for (int k = 0; k < IT; ++k) {
+            const int i = tid + k * kThreads;
+            if (i < N4) {
+                const int a = (4 * i) / DV, e = (4 * i) % DV;
+                Ct[(e + 0) * CP + a] = r[k].x;
+                Ct[(e + 1) * CP + a] = r[k].y;
+                Ct[(e + 2) * CP + a] = r[k].z;
+                Ct[(e + 3) * CP + a] = r[k].w;
+            }
+        }
     }
+    const int tr = tid / 16, tc0 = (tid % 16) * TN;
+    float sh[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) sh[i][j] = Sh[(size_t)(tr + 16 * i) * D + tc0 + j];
     __syncthreads();
     const float rho = pow_decay(log2f(head_decay(b.gamma, bh, b.H)), (float)segment_tokens(s, b.n, b.W, b.seg_chunks));
-    for (int i = tid; i < D * D; i += kThreads) {
-        const int f = i / D, x = i % D;
-        float acc = 0.f;
-        for (int e = 0; e < DV; ++e) acc += Zs[f * DV + e] * Cs[x * DV + e];
-        Sh[i] += rho * acc;
+    float acc[TM][TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+    for (int e = 0; e < DV; ++e) {
+        float av[TM], bv[TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) av[i] = Zs[(tr + 16 * i) * DV + e];
+#pragma unroll
+        for (int j = 0; j < TN; ++j) bv[j] = Ct[e * CP + tc0 + j];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) acc[i][j] += av[i] * bv[j];
     }
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) Sh[(size_t)(tr + 16 * i) * D + tc0 + j] = sh[i][j] + rho * acc[i][j];
+}
+
+template <int D, int DV>
+int launch_reverse_cross_t(const BwdArgs& b, const float* CB, cudaStream_t st) {
+    const size_t smem = ((size_t)D * DV + (size_t)DV * (D + 1)) * sizeof(float);
+    if (cudaFuncSetAttribute(reverse_cross_kernel<D, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return -1;
+    reverse_cross_kernel<D, DV><<<dim3(b.nseg - 1, b.BH), kThreads, smem, st>>>(b, CB);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace
@@ -326,11 +378,14 @@ int launch_reverse_scan(const float* src, float* dst, int BH, int H, int nseg, s
 
 int launch_reverse_cross(const BwdArgs& b, const float* CB, int d, int dv, cudaStream_t st) {
     if (b.nseg <= 1 || b.BH <= 0) return 0;
-    const size_t smem = 2 * (size_t)d * dv * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(reverse_cross_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return -1;
-    reverse_cross_kernel<<<dim3(b.nseg - 1, b.BH), kThreads, smem, st>>>(b, CB, d, dv);
-    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+#define HLA2_RCROSS(DD, VV) \
+    if (d == DD && dv == VV) return launch_reverse_cross_t<DD, VV>(b, CB, st);
+    HLA2_RCROSS(16, 16) HLA2_RCROSS(16, 32) HLA2_RCROSS(16, 64) HLA2_RCROSS(16, 128)
+    HLA2_RCROSS(32, 16) HLA2_RCROSS(32, 32) HLA2_RCROSS(32, 64) HLA2_RCROSS(32, 128)
+    HLA2_RCROSS(64, 16) HLA2_RCROSS(64, 32) HLA2_RCROSS(64, 64) HLA2_RCROSS(64, 128)
+    HLA2_RCROSS(128, 16) HLA2_RCROSS(128, 32) HLA2_RCROSS(128, 64) HLA2_RCROSS(128, 128)
+#undef HLA2_RCROSS
+    return -1;
 }
 
 }  // namespace hla2
