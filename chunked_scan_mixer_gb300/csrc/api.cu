@@ -122,8 +122,10 @@ bool dim_ok(int x) { return x == 16 || x == 32 || x == 64 || x == 128; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct DevInfo {
-    int sms = 152;             // GB300 when no device can be queried
-    int smem_optin = 232448;   // 227 KB
+    int sms = 152;                  // GB300 when no device can be queried
+    int smem_optin = 232448;        // 227 KB per block
+    int smem_per_sm = 233472;       // 228 KB per SM
+    int smem_reserved = 1024;       // per block
 };
 
 DevInfo dev_info() {
@@ -133,20 +135,34 @@ DevInfo dev_info() {
         cudaGetLastError();
         return di;
     }
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-        di.sms = v;
-    else
-        cudaGetLastError();
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess)
-        di.smem_optin = v;
-    else
-        cudaGetLastError();
+    auto get = [&](cudaDeviceAttr attr, int* dst) {
+        if (cudaDeviceGetAttribute(&v, attr, dev) == cudaSuccess)
+            *dst = v;
+        else
+            cudaGetLastError();
+    };
+    get(cudaDevAttrMultiProcessorCount, &di.sms);
+    get(cudaDevAttrMaxSharedMemoryPerBlockOptin, &di.smem_optin);
+    get(cudaDevAttrMaxSharedMemoryPerMultiprocessor, &di.smem_per_sm);
+    get(cudaDevAttrReservedSharedMemoryPerBlock, &di.smem_reserved);
     return di;
 }
 
-// Cut each head's chunks into segments so that the summary and output passes have
-// about two CTAs per SM in total.
-Plan make_plan(int B, int H, int n, int d, int dv, int W, int sms) {
+// CTAs of a chunk kernel resident on one SM, from its shared memory and thread count
+// (the kernels' register budgets allow at least this many), at most `cap`.
+int blocks_per_sm(size_t smem, int threads, int cap, const DevInfo& di) {
+    long b = (long)di.smem_per_sm / (long)(smem + (size_t)di.smem_reserved);
+    b = b < 2048 / threads ? b : 2048 / threads;
+    b = b < cap ? b : cap;
+    return b < 1 ? 1 : (int)b;
+}
+
+// Cut each head's chunks into segments.  The chunk passes run one CTA per segment and
+// process a segment's chunks one after another, so a pass takes about
+// waves x chunks-per-segment chunk steps, with waves = ceil(segments / resident CTAs).
+// The segment count per head minimises that (plus a small charge per segment for the
+// inter-segment scan), for `per_sm` resident CTAs per SM.
+Plan make_plan(int B, int H, int n, int d, int dv, int W, int sms, int per_sm) {
     Plan p;
     p.BH = B * H;
     p.H = H;
@@ -160,11 +176,23 @@ Plan make_plan(int B, int H, int n, int d, int dv, int W, int sms) {
         p.nseg = 0;
         return p;
     }
-    const long target = 2L * sms;
-    long per_head = (target + p.BH - 1) / p.BH;
-    if (per_head < 1) per_head = 1;
-    if (per_head > p.nchunks) per_head = p.nchunks;
-    p.seg_chunks = (int)((p.nchunks + per_head - 1) / per_head);
+    const long slots = (long)(per_sm < 1 ? 1 : per_sm) * (sms < 1 ? 1 : sms);
+    long max_ph = (4 * slots + p.BH - 1) / p.BH;
+    if (max_ph < 1) max_ph = 1;
+    if (max_ph > p.nchunks) max_ph = p.nchunks;
+    long best_sc = p.nchunks;
+    double best = -1.0;
+    for (long ph = 1; ph <= max_ph; ++ph) {
+        const long sc = (p.nchunks + ph - 1) / ph;
+        const long ns = (p.nchunks + sc - 1) / sc;
+        const long waves = ((long)p.BH * ns + slots - 1) / slots;
+        const double cost = (double)waves * (double)sc + 0.05 * (double)ns;
+        if (best < 0.0 || cost < best - 1e-9) {
+            best = cost;
+            best_sc = sc;
+        }
+    }
+    p.seg_chunks = (int)best_sc;
     p.nseg = (p.nchunks + p.seg_chunks - 1) / p.seg_chunks;
     return p;
 }
@@ -188,6 +216,24 @@ Path choose_forward_path(int dtype, int d, int dv, int W, int normalize, bool wa
     }
     if (fwd_chunk_simt_smem(d, dv, W, true) <= (size_t)di.smem_optin) return Path::kSimt;
     return Path::kNone;
+}
+
+int mma_threads(int d) { return 32 * (d <= 32 ? 4 : (d == 64 ? 8 : 16)); }
+
+// Resident CTAs per SM of the forward chunk kernels on `path`.
+int forward_per_sm(Path path, int d, int dv, int W, const DevInfo& di) {
+    switch (path) {
+        case Path::kTc: return blocks_per_sm(fwd_chunk_tc_smem(), 288, 2, di);
+        case Path::kMma: return blocks_per_sm(fwd_chunk_mma_smem(d, dv, W, false), mma_threads(d), 4, di);
+        case Path::kSimt: return blocks_per_sm(fwd_chunk_simt_smem(d, dv, W, false), 256, 4, di);
+        default: return 2;
+    }
+}
+
+Plan forward_plan(int B, int H, int n, int d, int dv, int W, int dtype, int normalize, bool want_final,
+                  const DevInfo& di) {
+    const Path path = choose_forward_path(dtype, d, dv, W, normalize, want_final, di);
+    return make_plan(B, H, n, d, dv, W, di.sms, forward_per_sm(path, d, dv, W, di));
 }
 
 int check_common(int B, int H, int n, int d, int dv, int dtype, int normalize) {
@@ -214,10 +260,9 @@ size_t hla2_state_floats(int d, int dv) { return raw_state_floats(d, dv); }
 
 size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
                                     int normalize, int want_final_state) {
-    (void)want_final_state;
     if (check_common(B, H, n, d, dv, dtype, normalize) != HLA2_OK || !dim_ok(chunk)) return (size_t)-1;
     const DevInfo di = dev_info();
-    return forward_ws(make_plan(B, H, n, d, dv, chunk, di.sms));
+    return forward_ws(forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, di));
 }
 
 int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
@@ -254,7 +299,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     const Path path = choose_forward_path(opts->dtype, d, dv, chunk, normalize, want_final, di);
     if (path == Path::kNone)
         return fail(HLA2_ERR_UNSUPPORTED, "no kernel for dtype %d, d %d, dv %d, chunk %d", opts->dtype, d, dv, chunk);
-    const Plan p = make_plan(B, H, n, d, dv, chunk, di.sms);
+    const Plan p = make_plan(B, H, n, d, dv, chunk, di.sms, forward_per_sm(path, d, dv, chunk, di));
     const FwdLayout L = fwd_layout(p, p.nseg - 1);
     const size_t need = L.total * sizeof(float);
     if (!opts->workspace || opts->workspace_bytes < need)
@@ -356,7 +401,7 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     int rc = check_common(B, H, n, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
     if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
-    const Plan p = make_plan(B, H, n, d, dv, chunk, dev_info().sms);
+    const Plan p = forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, dev_info());
     int l = 0;
     if (p.nseg > 0) {
         l = 2;                                                   // carry-in, output pass
@@ -384,6 +429,14 @@ int backward_width(int d, int chunk, const DevInfo& di) {
         if (sb > 0 && sf > 0 && sb <= (size_t)di.smem_optin && sf <= (size_t)di.smem_optin) return W;
     }
     return 0;
+}
+
+// Resident CTAs per SM of the backward's chunk passes (the forward passes at width W and
+// the reverse-mode passes run with the same segmentation).
+int backward_per_sm(int d, int W, const DevInfo& di) {
+    const int b = blocks_per_sm(bwd_chunk_mma_smem(d, W), mma_threads(d), 4, di);
+    const int f = blocks_per_sm(fwd_chunk_mma_smem(d, d, W, false), mma_threads(d), 4, di);
+    return b < f ? b : f;
 }
 
 struct BwdLayout {
@@ -426,7 +479,7 @@ size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chu
     const DevInfo di = dev_info();
     const int W = backward_width(d, chunk, di);
     if (!W) return (size_t)-1;
-    const Plan p = make_plan(B, H, n, d, dv, W, di.sms);
+    const Plan p = make_plan(B, H, n, d, dv, W, di.sms, backward_per_sm(d, W, di));
     return p.nseg > 0 ? bwd_layout(p).total_bytes : 0;
 }
 
@@ -448,7 +501,7 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
     const DevInfo di = dev_info();
     const int W = backward_width(d, chunk, di);
     if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no backward kernel for d %d, chunk %d", d, chunk);
-    const Plan p = make_plan(B, H, n, d, dv, W, di.sms);
+    const Plan p = make_plan(B, H, n, d, dv, W, di.sms, backward_per_sm(d, W, di));
     const BwdLayout L = bwd_layout(p);
     if (!opts->workspace || opts->workspace_bytes < L.total_bytes)
         return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.total_bytes,
