@@ -47,6 +47,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode and training rows measured after the headline")
+    ap.add_argument("--only", choices=("decode", "train"), default=None,
+                    help="measure only this row (for profiler captures; --steps/--warmup apply)")
+    ap.add_argument("--decode-seqs", type=int, default=256,
+                    help="sequences of the decode row (smaller case for ncu --set full captures)")
     ap.add_argument("--n", type=int, default=None,
                     help="override the sequence length (smaller case for ncu --set full captures; "
                          "the reported metric is only valid at the default)")
@@ -270,7 +274,7 @@ def _device_ms(fn, steps, warmup, stream_sync):
     return t0.elapsed_time(t1) / steps
 
 
-def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5):
+def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5, seqs: int = 256):
     """Decode row: 256 sequences x 32 heads, d = dv = 128, one single-token step per
     iteration on a resident fp32 state (the state's values do not change the work: it
     starts from N(0, 1e-4) draws instead of a 4096-token prefill).  Inputs of every step
@@ -281,7 +285,7 @@ def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int
     from chunked_scan_mixer_gb300 import inputs
 
     w = inputs.WORKLOADS["decode_prefill"]
-    N, H, d, dv = w.B, w.H, w.d, w.dv
+    N, H, d, dv = seqs, w.H, w.d, w.dv
     sf = hla.state_floats(d, dv)
     gen = torch.Generator(device=dev)
     gen.manual_seed(replica_seed(w.seed, dist.rank))
@@ -342,6 +346,16 @@ def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: in
                          "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_gbs}}
 
 
+def run_only(args, dist: Dist, dev):
+    hbm_gbs, bf16_tflops, _ = peaks()
+    if args.only == "decode":
+        row = measure_decode(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs)
+    else:
+        row = measure_train(dev, dist, bf16_tflops, hbm_gbs, steps=args.steps, warmup=args.warmup)
+    if dist.rank == 0:
+        print(json.dumps({"only": args.only, "n_gpus": dist.world, "secondary": {args.only: row}}), flush=True)
+
+
 def run_ours(args, dist: Dist):
     import torch
 
@@ -350,6 +364,8 @@ def run_ours(args, dist: Dist):
 
     torch.cuda.set_device(dist.local)
     dev = torch.device("cuda", dist.local)
+    if args.only:
+        return run_only(args, dist, dev)
     w = inputs.WORKLOADS[WORKLOAD]
     if args.n is not None:
         import dataclasses
