@@ -314,7 +314,8 @@ def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int
 
 def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: int = 10, warmup: int = 3):
     """Training row: B=4 H=16 n=8192 d=dv=128 bf16, decay 0.995, unnormalised; one step =
-    forward + backward (dq, dk, dv) through the public calls, inputs resident."""
+    forward (keeping the chunk states for the backward) + backward (dq, dk, dv) through the
+    public calls, inputs resident."""
     import torch
 
     import chunked_scan_mixer_gb300 as hla
@@ -328,8 +329,8 @@ def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: in
     gq, gk, gv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
     def one():
-        hla.forward(q, k, v, gamma=gamma, chunk=w.chunk, out=out)
-        hla.backward(q, k, v, do, gamma=gamma, chunk=w.chunk, dq=gq, dk=gk, dv=gv)
+        _, saved = hla.forward(q, k, v, gamma=gamma, chunk=w.chunk, out=out, save_for_backward=True)
+        hla.backward(q, k, v, do, gamma=gamma, chunk=w.chunk, dq=gq, dk=gk, dv=gv, saved=saved)
 
     ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
     tokens = w.B * w.H * w.n

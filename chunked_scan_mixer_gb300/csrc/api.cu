@@ -8,6 +8,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <functional>
 #include <string>
 
 #include "kernels.h"
@@ -250,6 +251,12 @@ size_t forward_ws(const Plan& p) { return p.nseg > 0 ? fwd_layout(p, p.nseg - 1)
 
 }  // namespace
 
+namespace {
+int forward_saving_for_backward(const void* q, const void* k, const void* v, void* out, int B, int H, int n, int d,
+                                int dv, const float* gamma, int normalize, int chunk, cudaStream_t st,
+                                const hla2_opts* opts);
+}  // namespace
+
 extern "C" {
 
 int hla2_version(void) { return 100; }
@@ -273,6 +280,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     if (rc != HLA2_OK) return rc;
     if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
     if (normalize && !isfinite(opts->eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
+    if (opts->flags & ~HLA2_FLAG_SAVE_FOR_BACKWARD) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_forward");
     const long BH = (long)B * H;
     const bool want_final = opts->final_state != nullptr;
     if ((opts->init_state && !aligned16(opts->init_state)) || (want_final && !aligned16(opts->final_state)))
@@ -294,6 +302,8 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     if (!q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must not be NULL");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
+    if (opts->flags & HLA2_FLAG_SAVE_FOR_BACKWARD)
+        return forward_saving_for_backward(q, k, v, out, B, H, n, d, dv, gamma, normalize, chunk, st, opts);
 
     const DevInfo di = dev_info();
     const Path path = choose_forward_path(opts->dtype, d, dv, chunk, normalize, want_final, di);
@@ -460,6 +470,68 @@ BwdLayout bwd_layout(const Plan& p) {
     return L;
 }
 
+// Chunk-pass arguments at the backward's width and segmentation.
+ChunkArgs backward_chunk_args(const void* q, const void* k, const void* v, void* out, long BH, int H, int n,
+                              const Plan& p, const float* gamma, void* workspace, const BwdLayout& L) {
+    ChunkArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.BH = (int)BH;
+    a.H = H;
+    a.n = n;
+    a.W = p.W;
+    a.nchunks = p.nchunks;
+    a.seg_chunks = p.seg_chunks;
+    a.nseg = p.nseg;
+    a.nsum = p.nseg;
+    a.gamma = gamma;
+    a.ws = static_cast<float*>(workspace);
+    a.L = L.F;
+    a.chunk_states = reinterpret_cast<bf16*>(static_cast<char*>(workspace) + L.states_bytes_off);
+    return a;
+}
+
+// The forward pieces the reverse-mode passes consume, at the backward's width: carries at
+// the segment starts (summaries of every segment, whose C_B the reverse cross term also
+// reads, and the inter-segment scan), then one chunk pass that exports the bf16 (S, Z) at
+// every chunk start (last_mode kStates) and also writes the output (kOutStates).
+int backward_forward_part(const ChunkArgs& a, const Plan& p, const BwdLayout& L, int d, int dv, int last_mode,
+                          cudaStream_t st, const std::function<void(int)>* mark) {
+    float* ws = a.ws;
+    const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
+    const int seg_tokens = p.seg_chunks * p.W;
+    auto pass = [&](int mode) {
+        ChunkArgs c = a;
+        c.seg0 = 0;
+        c.nseg_launch = p.nseg;
+        return launch_fwd_chunk_mma(c, d, dv, p.W, mode, false, st);
+    };
+    auto tick = [&](int i) {
+        if (mark) (*mark)(i);
+    };
+    if (launch_init_carry(a, d, dv, nullptr, st)) return cuda_fail("carry-in initialisation");
+    tick(1);
+    if (p.nseg > 1) {
+        const int steps = p.nseg - 1;
+        if (pass(kSummary)) return cuda_fail("segment summaries");
+        tick(2);
+        if (launch_linear_scan(ws + L.F.SB, ws + L.F.Sin, a.BH, a.H, steps, dd, a.nsum * dd, p.nseg * dd, true,
+                               a.gamma, seg_tokens, 1, st) ||
+            launch_cross(a, d, dv, false, st) ||
+            launch_linear_scan(ws + L.F.ZB, ws + L.F.Zin, a.BH, a.H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true,
+                               a.gamma, seg_tokens, 2, st))
+            return cuda_fail("forward segment scan");
+    } else {
+        tick(2);
+    }
+    tick(3);
+    if (pass(last_mode)) return cuda_fail(last_mode == kOutStates ? "output pass" : "forward state export");
+    tick(4);
+    return HLA2_OK;
+}
+
 int check_backward(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
     int rc = check_common(B, H, n, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
@@ -468,6 +540,35 @@ int check_backward(int B, int H, int n, int d, int dv, int chunk, int dtype, int
     if (dtype != HLA2_BF16 || d != dv)
         return fail(HLA2_ERR_UNSUPPORTED, "the backward needs bf16 tensors and d == dv");
     return HLA2_OK;
+}
+
+int forward_saving_for_backward(const void* q, const void* k, const void* v, void* out, int B, int H, int n, int d,
+                                int dv, const float* gamma, int normalize, int chunk, cudaStream_t st,
+                                const hla2_opts* opts) {
+    if (opts->dtype != HLA2_BF16 || d != dv || normalize || opts->init_state || opts->final_state)
+        return fail(HLA2_ERR_UNSUPPORTED,
+                    "saving for the backward needs bf16, d == dv, normalize == 0 and no init_state / final_state");
+    const DevInfo di = dev_info();
+    const int W = backward_width(d, chunk, di);
+    if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no backward kernel for d %d, chunk %d", d, chunk);
+    const Plan p = make_plan(B, H, n, d, dv, W, di.sms, backward_per_sm(d, W, di));
+    const BwdLayout L = bwd_layout(p);
+    if (!opts->workspace || opts->workspace_bytes < L.total_bytes)
+        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required to save for the backward (got %zu)",
+                    L.total_bytes, opts->workspace ? opts->workspace_bytes : (size_t)0);
+    if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    const ChunkArgs a = backward_chunk_args(q, k, v, out, (long)B * H, H, n, p, gamma, opts->workspace, L);
+    const std::function<void(int)> mark = [&](int i) {
+        if (opts->phase_events && i < opts->n_phase_events && opts->phase_events[i] &&
+            cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[i]), st) != cudaSuccess)
+            cudaGetLastError();
+    };
+    cudaGetLastError();
+    mark(0);
+    const int rc = backward_forward_part(a, p, L, d, dv, kOutStates, st, &mark);
+    if (rc != HLA2_OK) return rc;
+    mark(5);
+    return succeed();
 }
 
 }  // namespace
@@ -491,6 +592,7 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
     if (rc != HLA2_OK) return rc;
     if (opts->init_state || opts->final_state)
         return fail(HLA2_ERR_INVALID_ARG, "the backward takes no init_state / final_state");
+    if (opts->flags & ~HLA2_FLAG_STATES_SAVED) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_backward");
     const long BH = (long)B * H;
     if (BH == 0 || n == 0) return succeed();
     if (!q || !k || !v || !dout || !dq || !dk || !dv_out)
@@ -511,23 +613,7 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
     float* ws = static_cast<float*>(opts->workspace);
     bf16* states = reinterpret_cast<bf16*>(static_cast<char*>(opts->workspace) + L.states_bytes_off);
 
-    ChunkArgs a{};
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.out = nullptr;
-    a.BH = (int)BH;
-    a.H = H;
-    a.n = n;
-    a.W = W;
-    a.nchunks = p.nchunks;
-    a.seg_chunks = p.seg_chunks;
-    a.nseg = p.nseg;
-    a.nsum = p.nseg;
-    a.gamma = gamma;
-    a.ws = ws;
-    a.L = L.F;
-    a.chunk_states = states;
+    const ChunkArgs a = backward_chunk_args(q, k, v, nullptr, BH, H, n, p, gamma, opts->workspace, L);
 
     BwdArgs b{};
     b.q = static_cast<const bf16*>(q);
@@ -553,27 +639,11 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
     b.chunk_states = states;
 
     const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
-    const int seg_tokens = p.seg_chunks * W;
-    auto pass = [&](int mode) {
-        ChunkArgs c = a;
-        c.seg0 = 0;
-        c.nseg_launch = p.nseg;
-        return launch_fwd_chunk_mma(c, d, dv, W, mode, false, st);
-    };
     cudaGetLastError();
-    // forward carries at segment starts, then the forward state at every chunk start
-    if (launch_init_carry(a, d, dv, nullptr, st)) return cuda_fail("carry-in initialisation");
-    if (p.nseg > 1) {
-        const int steps = p.nseg - 1;
-        if (pass(kSummary)) return cuda_fail("segment summaries");
-        if (launch_linear_scan(ws + L.F.SB, ws + L.F.Sin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true, gamma,
-                               seg_tokens, 1, st) ||
-            launch_cross(a, d, dv, false, st) ||
-            launch_linear_scan(ws + L.F.ZB, ws + L.F.Zin, a.BH, H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true, gamma,
-                               seg_tokens, 2, st))
-            return cuda_fail("forward segment scan");
+    if (!(opts->flags & HLA2_FLAG_STATES_SAVED)) {
+        rc = backward_forward_part(a, p, L, d, dv, kStates, st, nullptr);
+        if (rc != HLA2_OK) return rc;
     }
-    if (pass(kStates)) return cuda_fail("forward state export");
     // reverse summaries, reverse scan with the cross term Zh_end C_B^T, gradients
     if (launch_bwd_chunk_mma(b, d, W, true, st)) return cuda_fail("reverse summaries");
     if (launch_reverse_scan(ws + L.ZhB, ws + L.Zh_end, a.BH, H, p.nseg, ddv, gamma, n, W, p.seg_chunks, 2, st) ||

@@ -22,7 +22,7 @@
 // for the inter-segment scan); kOutput starts from the segment's carry-in and writes
 // out (and the raw final state for the last segment); kStates starts from the carry-in
 // and exports the bf16 (S, Z) at every chunk start (the forward states that the
-// reverse-mode pass consumes).
+// reverse-mode pass consumes); kOutStates does both (the forward of a training step).
 #pragma once
 
 #include "common.cuh"
@@ -58,7 +58,8 @@ struct MmaCfg {
 template <int D, int DV, int W, int MODE, bool CM>
 __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
     fwd_chunk_mma_kernel(const ChunkArgs a) {
-    constexpr bool SUMMARY = MODE == kSummary, OUTPUT = MODE == kOutput;
+    constexpr bool SUMMARY = MODE == kSummary, OUTPUT = MODE == kOutput || MODE == kOutStates;
+    constexpr bool EXPORT = MODE == kStates || MODE == kOutStates;
     using Cfg = MmaCfg<D, DV, W>;
     constexpr int NW = Cfg::NW, NT = Cfg::NT, LD = Cfg::LD, LDV = Cfg::LDV, LW = Cfg::LW;
     constexpr int TW = Cfg::TW, TD = Cfg::TD, TV = Cfg::TV;
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         cp_async_wait_all();
         __syncthreads();
 
-        if (MODE == kStates) {  // export the state at this chunk start
+        if (EXPORT) {  // export the state at this chunk start
             bf16* dst = a.chunk_states + ((size_t)bh * a.nchunks + c) * (size_t)(D * D + D * DV);
             for (int i = tid; i < D * D / 8; i += NT) {
                 const int r = (i * 8) / D, f = (i * 8) % D;
@@ -464,6 +465,8 @@ int launch_fwd_chunk_mma_t(const ChunkArgs& a, int mode, bool track_cm, cudaStre
         e = launch_mode<D, DV, W, kSummary, true>(a, smem, st);
     else if (mode == kStates)
         e = launch_mode<D, DV, W, kStates, false>(a, smem, st);
+    else if (mode == kOutStates)
+        e = launch_mode<D, DV, W, kOutStates, false>(a, smem, st);
     else if (track_cm)
         e = launch_mode<D, DV, W, kOutput, true>(a, smem, st);
     else

@@ -30,7 +30,7 @@ struct ChunkArgs {
 };
 
 // Chunk-kernel passes.
-enum ChunkMode { kSummary = 0, kOutput = 1, kStates = 2 };
+enum ChunkMode { kSummary = 0, kOutput = 1, kStates = 2, kOutStates = 3 };
 
 // Arguments of the reverse-mode chunk kernel (bf16, d == dv).
 struct BwdArgs {

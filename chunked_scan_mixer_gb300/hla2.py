@@ -45,7 +45,21 @@ class Opts(ctypes.Structure):
         ("final_state", ctypes.c_void_p),
         ("phase_events", ctypes.POINTER(ctypes.c_void_p)),
         ("n_phase_events", ctypes.c_int),
+        ("flags", ctypes.c_int),
     ]
+
+
+FLAG_SAVE_FOR_BACKWARD = 1
+FLAG_STATES_SAVED = 2
+
+
+class SavedForBackward:
+    """What a training-step forward keeps for the backward on the same inputs: a device
+    workspace holding the segment summaries and the bf16 (S, Z) at every chunk start.
+    Pass it to backward(saved=...) once; the buffer is owned by this object."""
+
+    def __init__(self, ws, nbytes, key):
+        self.ws, self.nbytes, self.key = ws, nbytes, key
 
 
 def lib():
@@ -173,13 +187,15 @@ def _to_device(t, device):
 
 
 def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state=None,
-            return_final_state=False, out=None, phase_events=None):
+            return_final_state=False, out=None, phase_events=None, save_for_backward=False):
     """Masked HLA-2 forward.  q, k [B,H,n,d]; v [B,H,n,dv] (float32 or bfloat16).
 
     gamma: None, a scalar, or [H] per-head decay in (0, 1].  init_state: packed
     [B,H,state_floats] float32 state to continue from.  Returns out [B,H,n,dv] (and the
     packed final state when ``return_final_state``).  phase_events: optional list of
-    torch.cuda.Event recorded at the phase boundaries (see hla2_opts)."""
+    torch.cuda.Event recorded at the phase boundaries (see hla2_opts).
+    save_for_backward: also return a SavedForBackward for backward(saved=...), which then
+    skips recomputing the forward (bf16 device tensors, unnormalised, no state arguments)."""
     host = q.device.type == "cpu"
     device = torch.device("cuda", torch.cuda.current_device()) if host else q.device
     L = lib()
@@ -200,11 +216,21 @@ def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state
     fin = torch.empty((B, H, state_floats(d, dv)), dtype=torch.float32, device=device) \
         if return_final_state else None
     sh = _stream_handle(device)
-    nbytes = forward_workspace_bytes(B, H, n, d, dv, chunk, q.dtype, normalize, return_final_state)
-    ws = _workspace(nbytes, device, sh)
+    flags = 0
+    if save_for_backward:
+        if host:
+            raise ValueError("save_for_backward needs device tensors")
+        nbytes = L.hla2_backward_workspace_bytes(B, H, n, d, dv, chunk, _DTYPES[q.dtype])
+        if nbytes == ctypes.c_size_t(-1).value:
+            raise HLA2Error("hla2_backward_workspace_bytes", -2, "these arguments have no backward")
+        ws = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+        flags = FLAG_SAVE_FOR_BACKWARD
+    else:
+        nbytes = forward_workspace_bytes(B, H, n, d, dv, chunk, q.dtype, normalize, return_final_state)
+        ws = _workspace(nbytes, device, sh)
     opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), nbytes,
                 None if init is None else init.data_ptr(), None if fin is None else fin.data_ptr(),
-                None, 0)
+                None, 0, flags)
     if phase_events:
         for e in phase_events:
             if not e.cuda_event:  # torch creates its events lazily
@@ -215,14 +241,19 @@ def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state
     rc = L.hla2_forward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), B, H, n, d, dv, _ptr(g), int(normalize),
                         chunk, sh, ctypes.byref(opts))
     _check("hla2_forward", rc)
+    if save_for_backward:
+        saved = SavedForBackward(ws, int(nbytes), (B, H, n, d, dv, chunk, q.dtype, device))
+        return (o, fin, saved) if return_final_state else (o, saved)
     if host:
         o = o.to("cpu") if out is None else out.copy_(o)
         fin = None if fin is None else fin.to("cpu")
     return (o, fin) if return_final_state else o
 
 
-def backward(q, k, v, dout, gamma=None, chunk=64, dq=None, dk=None, dv=None):
-    """Gradients (dq, dk, dv) of the unnormalised forward for upstream dout."""
+def backward(q, k, v, dout, gamma=None, chunk=64, dq=None, dk=None, dv=None, saved=None):
+    """Gradients (dq, dk, dv) of the unnormalised forward for upstream dout.  saved: the
+    SavedForBackward of forward(..., save_for_backward=True) on the same q, k, v, gamma
+    and chunk (the forward is then not recomputed)."""
     host = q.device.type == "cpu"
     device = torch.device("cuda", torch.cuda.current_device()) if host else q.device
     L = lib()
@@ -234,12 +265,18 @@ def backward(q, k, v, dout, gamma=None, chunk=64, dq=None, dk=None, dv=None):
     gk = torch.empty_like(kd) if dk is None or host else dk
     gv = torch.empty_like(vd) if dv is None or host else dv
     sh = _stream_handle(device)
-    nbytes = L.hla2_backward_workspace_bytes(B, H, n, d, dvdim, chunk, _DTYPES[q.dtype])
-    if nbytes == ctypes.c_size_t(-1).value:
-        nbytes = 0
-    ws = _workspace(int(nbytes), device, sh)
+    flags = 0
+    if saved is not None:
+        if saved.key != (B, H, n, d, dvdim, chunk, q.dtype, device):
+            raise ValueError("saved was made for other sizes, chunk, dtype or device")
+        ws, nbytes, flags = saved.ws, saved.nbytes, FLAG_STATES_SAVED
+    else:
+        nbytes = L.hla2_backward_workspace_bytes(B, H, n, d, dvdim, chunk, _DTYPES[q.dtype])
+        if nbytes == ctypes.c_size_t(-1).value:
+            nbytes = 0
+        ws = _workspace(int(nbytes), device, sh)
     opts = Opts(_DTYPES[q.dtype], 1e-6, None if ws is None else ws.data_ptr(), int(nbytes), None, None,
-                None, 0)
+                None, 0, flags)
     rc = L.hla2_backward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(dod), _ptr(gq), _ptr(gk), _ptr(gv), B, H, n, d,
                          dvdim, _ptr(g), 0, chunk, sh, ctypes.byref(opts))
     _check("hla2_backward", rc)

@@ -77,7 +77,24 @@ typedef struct {
      * NULL / 0 records nothing.  The caller creates and owns the events. */
     void* const* phase_events;
     int n_phase_events;
+    /* HLA2_FLAG_* bits; 0 for plain calls. */
+    int flags;
 } hla2_opts;
+
+/*
+ * hla2_opts.flags for a training step, forward then backward on the same inputs:
+ *   HLA2_FLAG_SAVE_FOR_BACKWARD (hla2_forward): also keep in the workspace what the
+ *     backward would otherwise recompute: the segment summaries and the bf16 (S, Z) at
+ *     every chunk start, at the backward's chunk width.  The workspace must hold
+ *     hla2_backward_workspace_bytes(B, H, n, d, dv, chunk, dtype) bytes.  Only for what
+ *     hla2_backward covers: bf16, d == dv, normalize == 0, no init_state or final_state
+ *     (else HLA2_ERR_UNSUPPORTED).
+ *   HLA2_FLAG_STATES_SAVED (hla2_backward): the workspace holds those pieces from a
+ *     SAVE_FOR_BACKWARD forward with the same q, k, gamma, sizes and chunk, untouched since;
+ *     the backward then skips its forward recomputation.  The library cannot check that
+ *     the workspace is still intact: passing this flag otherwise gives wrong gradients.
+ */
+enum { HLA2_FLAG_SAVE_FOR_BACKWARD = 1, HLA2_FLAG_STATES_SAVED = 2 };
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int hla2_version(void);

@@ -91,3 +91,17 @@ def test_backward_rejects_normalized(L):
     p = ctypes.c_void_p(16)
     rc = L.hla2_backward(p, p, p, p, p, p, p, 1, 1, 16, 16, 16, None, 1, 16, None, ctypes.byref(o))
     assert rc == -2
+
+
+def test_unknown_flags_rejected(L):
+    """Flag bits outside HLA2_FLAG_* are argument errors, found before anything runs."""
+    p = ctypes.c_void_p(16)
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 4)
+    rc = L.hla2_forward(p, p, p, p, 0, 1, 16, 16, 16, None, 0, 16, None, ctypes.byref(o))
+    assert rc == -1 and b"flags" in L.hla2_last_error()
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 1)  # SAVE_FOR_BACKWARD is a forward flag
+    rc = L.hla2_backward(p, p, p, p, p, p, p, 0, 1, 16, 16, 16, None, 0, 16, None, ctypes.byref(o))
+    assert rc == -1
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 2)  # STATES_SAVED is a backward flag
+    rc = L.hla2_forward(p, p, p, p, 0, 1, 16, 16, 16, None, 0, 16, None, ctypes.byref(o))
+    assert rc == -1

@@ -80,3 +80,33 @@ def test_unsupported_variants_are_reported():
     x = inputs.make_custom(1, 1, 32, 16, 16, torch.float32, seed=5, with_dout=True)
     with pytest.raises(HLA2Error):
         run(x, 16)
+
+
+@pytest.mark.parametrize("B,H,n,d", [(1, 3, 333, 64), (2, 2, 2000, 64), (1, 4, 1000, 128), (4, 16, 300, 32)])
+def test_training_forward_saves_for_backward(B, H, n, d):
+    """forward(save_for_backward=True) writes the same output as the oracle, and
+    backward(saved=...) returns the gradients of a backward that recomputes the forward,
+    bit for bit (the same kernels on the same segmentation)."""
+    x = inputs.make_custom(B, H, n, d, d, torch.bfloat16, seed=n + d, gamma=(0.95, 0.999), with_dout=True)
+    q, k, v, do = (x[t].cuda() for t in ("q", "k", "v", "dout"))
+    g = x["gamma"].cuda()
+    o, saved = hla.forward(q, k, v, gamma=g, chunk=64, save_for_backward=True)
+    ref_o = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), x["gamma"].double().numpy())
+    assert rel_err(np64(o.cpu()), ref_o) <= 2e-2
+    fresh = hla.backward(q, k, v, do, gamma=g, chunk=64)
+    reused = hla.backward(q, k, v, do, gamma=g, chunk=64, saved=saved)
+    for a, b in zip(fresh, reused):
+        assert torch.equal(a, b)
+    ref = oracle(x)
+    for gg, rr in zip(reused, ref):
+        assert rel_err(np64(gg.cpu()), rr) <= 2e-2
+
+
+def test_save_for_backward_rejects_uncovered_requests():
+    x = inputs.make_custom(1, 2, 100, 64, 64, torch.bfloat16, seed=5, gamma=0.99)
+    q, k, v = (x[t].cuda() for t in ("q", "k", "v"))
+    with pytest.raises(HLA2Error):
+        hla.forward(q, k, v, gamma=x["gamma"].cuda(), normalize=True, save_for_backward=True)
+    _, saved = hla.forward(q, k, v, gamma=x["gamma"].cuda(), chunk=64, save_for_backward=True)
+    with pytest.raises(ValueError):  # other chunk than the saving forward
+        hla.backward(q, k, v, v, gamma=x["gamma"].cuda(), chunk=32, saved=saved)
