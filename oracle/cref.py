@@ -101,6 +101,24 @@ def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6):
     return out
 
 
+def backward_normalized(q, k, v, dout, gamma=None, eps=1e-6):
+    """Ratio-normalised gradients from the C recurrence, by the quotient rule of
+    ``hla2_oracle.serial_backward_normalized``: the unnormalised output num and the
+    denominator den (the same recurrence with v -> 1) from the C forward, then the C
+    reverse sweep once with (v, dO / (den + eps)) and once with
+    (1, -(dO . num) / (den + eps)^2).  Returns (dq, dk, dv) float64."""
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f64(dout)
+    ones = np.ones(v.shape[:-1] + (1,), dtype=np.float32)
+    num = forward(q, k, v, gamma)
+    den = forward(q, k, ones, gamma)[..., 0]
+    inv = 1.0 / (den + eps)
+    dnum = dout * inv[..., None]
+    dden = -np.sum(dout * num, axis=-1) * inv * inv
+    dq1, dk1, dv1 = backward(q, k, v, dnum, gamma)
+    dq2, dk2, _ = backward(q, k, ones, dden[..., None], gamma)
+    return dq1 + dq2, dk1 + dk2, dv1
+
+
 def backward(q, k, v, dout, gamma=None):
     """Reverse sweep of the unnormalised serial recurrence: returns (dq, dk, dv) float64."""
     q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)

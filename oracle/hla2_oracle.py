@@ -57,6 +57,7 @@ __all__ = [
     "blelloch_exclusive_scan",
     "chunked_scan_forward",
     "serial_backward",
+    "serial_backward_normalized",
     "pairsum_grads",
     "pack_state",
     "unpack_state",
@@ -371,6 +372,30 @@ def serial_backward(q, k, v, dout, gamma=None):
                 Sb = gh * Sb
                 Gb = gh * gh * Gb
     return dq, dk, dvv
+
+
+def serial_backward_normalized(q, k, v, dout, gamma=None, eps=1e-6):
+    """Gradients of L = sum_t dO_t . o_t for the ratio-normalised output
+    o_t = num_t / (den_t + eps) ([PS] §2, §5.1; reading R4), by the quotient rule:
+        dnum_t = dO_t / (den_t + eps),   dden_t = -(dO_t . num_t) / (den_t + eps)^2.
+    num is the unnormalised output and den the same pair sum with every v_j replaced by 1
+    (R4).  Both are linear in v, so each path goes through the unnormalised adjoint
+    ``serial_backward``: once with (v, dnum), once with (1, dden).  The second path
+    contributes to dq and dk only.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    dout = np.asarray(dout, dtype=np.float64)
+    ones = np.ones(v.shape[:-1] + (1,))
+    num = serial_forward(q, k, v, gamma)
+    den = serial_forward(q, k, ones, gamma)[..., 0]
+    inv = 1.0 / (den + eps)
+    dnum = dout * inv[..., None]
+    dden = -np.sum(dout * num, axis=-1) * inv * inv
+    dq1, dk1, dv1 = serial_backward(q, k, v, dnum, gamma)
+    dq2, dk2, _ = serial_backward(q, k, ones, dden[..., None], gamma)
+    return dq1 + dq2, dk1 + dk2, dv1
 
 
 def pairsum_grads(q, k, v, dout, gamma=None):

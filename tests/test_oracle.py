@@ -303,6 +303,69 @@ def test_adjoint_matches_finite_differences():
         assert rel(grad, num) < 1e-7
 
 
+def _fd_normalized(q, k, v, dO, g, eps, h=1e-6):
+    """Central differences of L = sum dO . o_norm with respect to q, k, v."""
+    def loss():
+        return float(np.sum(O.serial_forward(q, k, v, g, normalize=True, eps=eps) * dO))
+
+    out = []
+    for arr in (q, k, v):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            a0 = arr[idx]
+            arr[idx] = a0 + h
+            lp = loss()
+            arr[idx] = a0 - h
+            lm = loss()
+            arr[idx] = a0
+            num[idx] = (lp - lm) / (2 * h)
+        out.append(num)
+    return out
+
+
+def test_normalized_adjoint_matches_finite_differences():
+    """The quotient-rule adjoint of the ratio-normalised output ([PS] §5.1, reading R4)
+    against central differences of the normalised serial forward itself."""
+    q, k, v = rnd(1, 1, 6, 3, 2, seed=31, positive=True)
+    dO = np.random.default_rng(32).standard_normal(v.shape)
+    g, eps = [0.9], 1e-3
+    got = O.serial_backward_normalized(q, k, v, dO, g, eps)
+    for a, b in zip(got, _fd_normalized(q, k, v, dO, g, eps)):
+        assert rel(a, b) < 1e-6
+
+
+def test_normalized_adjoint_c_matches_numpy():
+    q, k, v = rnd(2, 2, 40, 4, 3, seed=33, positive=True)
+    dO = np.random.default_rng(34).standard_normal(v.shape)
+    g = [0.97, 0.999]
+    # the C path sees float32 inputs: round them first so both sides use the same values
+    q, k, v = (x.astype(np.float32).astype(np.float64) for x in (q, k, v))
+    a = O.serial_backward_normalized(q, k, v, dO, g, 1e-6)
+    b = cref.backward_normalized(q, k, v, dO, g, 1e-6)
+    for x, y in zip(a, b):
+        assert rel(x, y) < 1e-5
+
+
+def test_planted_dropped_denominator_path_is_caught(monkeypatch):
+    """Dropping the denominator's path of the quotient rule (a plausible mistake) makes the
+    normalised adjoint disagree with finite differences."""
+    q, k, v = rnd(1, 1, 5, 2, 2, seed=35, positive=True)
+    dO = np.random.default_rng(36).standard_normal(v.shape)
+    g, eps = [0.9], 1e-3
+    fd = _fd_normalized(q, k, v, dO, g, eps)
+    real = O.serial_backward
+
+    def numerator_only(q_, k_, v_, d_, g_=None):
+        if v_.shape[-1] == 1 and np.all(v_ == 1.0):
+            z = np.zeros_like(np.asarray(q_, dtype=np.float64))
+            return z, z.copy(), np.zeros_like(np.asarray(v_, dtype=np.float64))
+        return real(q_, k_, v_, d_, g_)
+
+    monkeypatch.setattr(O, "serial_backward", numerator_only)
+    bad = O.serial_backward_normalized(q, k, v, dO, g, eps)
+    assert rel(bad[0], fd[0]) > 1e-3 or rel(bad[1], fd[1]) > 1e-3
+
+
 def test_adjoint_matches_pairsum_gradients():
     q, k, v = rnd(1, 2, 8, 3, 2, seed=21)
     dO = np.random.default_rng(22).standard_normal(v.shape)
