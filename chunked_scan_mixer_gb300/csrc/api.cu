@@ -536,10 +536,42 @@ int check_backward(int B, int H, int n, int d, int dv, int chunk, int dtype, int
     int rc = check_common(B, H, n, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
     if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
-    if (normalize) return fail(HLA2_ERR_UNSUPPORTED, "the backward covers the unnormalised output only");
     if (dtype != HLA2_BF16 || d != dv)
         return fail(HLA2_ERR_UNSUPPORTED, "the backward needs bf16 tensors and d == dv");
     return HLA2_OK;
+}
+
+// Workspace of the ratio-normalised backward: one scratch region that the unnormalised
+// forward and backward calls use in turn (stream order keeps them apart), then eight bf16
+// [B, H, n, d] buffers: num, e_0, den output, dL/dnum, dL/dden (column 0), dq2, dk2, dv2.
+struct NormBwdLayout {
+    size_t sub_bytes = 0;
+    size_t buf[8] = {};
+    size_t total = 0;
+};
+
+size_t unnormalised_backward_bytes(int B, int H, int n, int d, int dv, int chunk, const DevInfo& di) {
+    const int W = backward_width(d, chunk, di);
+    if (!W) return (size_t)-1;
+    const Plan p = make_plan(B, H, n, d, dv, W, di.sms, backward_per_sm(d, W, di));
+    return p.nseg > 0 ? bwd_layout(p).total_bytes : 0;
+}
+
+NormBwdLayout norm_bwd_layout(int B, int H, int n, int d, int dv, int chunk, int dtype, const DevInfo& di) {
+    NormBwdLayout L;
+    const size_t fw = hla2_forward_workspace_bytes(B, H, n, d, dv, chunk, dtype, 0, 0);
+    const size_t bw = unnormalised_backward_bytes(B, H, n, d, dv, chunk, di);
+    if (fw == (size_t)-1 || bw == (size_t)-1) {
+        L.total = (size_t)-1;
+        return L;
+    }
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    L.sub_bytes = up(fw > bw ? fw : bw);
+    const size_t one = up((size_t)B * H * (size_t)n * (size_t)d * sizeof(bf16));
+    size_t o = L.sub_bytes;
+    for (int i = 0; i < 8; ++i, o += one) L.buf[i] = o;
+    L.total = o;
+    return L;
 }
 
 int forward_saving_for_backward(const void* q, const void* k, const void* v, void* out, int B, int H, int n, int d,
@@ -575,13 +607,11 @@ int forward_saving_for_backward(const void* q, const void* k, const void* v, voi
 
 extern "C" {
 
-size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype) {
-    if (check_backward(B, H, n, d, dv, chunk, dtype, 0) != HLA2_OK) return (size_t)-1;
+size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
+    if (check_backward(B, H, n, d, dv, chunk, dtype, normalize) != HLA2_OK) return (size_t)-1;
     const DevInfo di = dev_info();
-    const int W = backward_width(d, chunk, di);
-    if (!W) return (size_t)-1;
-    const Plan p = make_plan(B, H, n, d, dv, W, di.sms, backward_per_sm(d, W, di));
-    return p.nseg > 0 ? bwd_layout(p).total_bytes : 0;
+    if (normalize) return norm_bwd_layout(B, H, n, d, dv, chunk, dtype, di).total;
+    return unnormalised_backward_bytes(B, H, n, d, dv, chunk, di);
 }
 
 int hla2_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
@@ -601,6 +631,50 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
         !aligned16(dv_out))
         return fail(HLA2_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
     const DevInfo di = dev_info();
+    if (normalize) {
+        if (opts->flags & HLA2_FLAG_STATES_SAVED)
+            return fail(HLA2_ERR_UNSUPPORTED, "saved forward states cover the unnormalised output only");
+        if (!isfinite(opts->eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
+        const NormBwdLayout N = norm_bwd_layout(B, H, n, d, dv, chunk, opts->dtype, di);
+        if (N.total == (size_t)-1) return fail(HLA2_ERR_UNSUPPORTED, "no backward kernel for d %d, chunk %d", d, chunk);
+        if (!opts->workspace || opts->workspace_bytes < N.total)
+            return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", N.total,
+                        opts->workspace ? opts->workspace_bytes : (size_t)0);
+        if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+        char* base = static_cast<char*>(opts->workspace);
+        bf16* num = reinterpret_cast<bf16*>(base + N.buf[0]);
+        bf16* e0 = reinterpret_cast<bf16*>(base + N.buf[1]);
+        bf16* den = reinterpret_cast<bf16*>(base + N.buf[2]);
+        bf16* dnum = reinterpret_cast<bf16*>(base + N.buf[3]);
+        bf16* dden = reinterpret_cast<bf16*>(base + N.buf[4]);
+        bf16* dq2 = reinterpret_cast<bf16*>(base + N.buf[5]);
+        bf16* dk2 = reinterpret_cast<bf16*>(base + N.buf[6]);
+        bf16* dv2 = reinterpret_cast<bf16*>(base + N.buf[7]);
+        hla2_opts so{};
+        so.dtype = HLA2_BF16;
+        so.eps = opts->eps;
+        so.workspace = base;
+        so.workspace_bytes = N.sub_bytes;
+        cudaStream_t s2 = reinterpret_cast<cudaStream_t>(stream);
+        const size_t rows = (size_t)BH * (size_t)n;
+        cudaGetLastError();
+        // num = unnormalised output; den = unnormalised output for the value rows e_0
+        if ((rc = hla2_forward(q, k, v, num, B, H, n, d, dv, gamma, 0, chunk, stream, &so)) != HLA2_OK) return rc;
+        if (launch_unit_first_column(e0, rows, d, s2)) return cuda_fail("unit value rows");
+        if ((rc = hla2_forward(q, k, e0, den, B, H, n, d, d, gamma, 0, chunk, stream, &so)) != HLA2_OK) return rc;
+        if (launch_quotient_rule(static_cast<const bf16*>(dout), num, den, dnum, dden, rows, dv, d, opts->eps, s2))
+            return cuda_fail("quotient rule");
+        if ((rc = hla2_backward(q, k, v, dnum, dq, dk, dv_out, B, H, n, d, dv, gamma, 0, chunk, stream, &so)) !=
+            HLA2_OK)
+            return rc;
+        if ((rc = hla2_backward(q, k, e0, dden, dq2, dk2, dv2, B, H, n, d, d, gamma, 0, chunk, stream, &so)) !=
+            HLA2_OK)
+            return rc;
+        if (launch_add_into(static_cast<bf16*>(dq), dq2, rows * (size_t)d, s2) ||
+            launch_add_into(static_cast<bf16*>(dk), dk2, rows * (size_t)d, s2))
+            return cuda_fail("gradient sum");
+        return succeed();
+    }
     const int W = backward_width(d, chunk, di);
     if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no backward kernel for d %d, chunk %d", d, chunk);
     const Plan p = make_plan(B, H, n, d, dv, W, di.sms, backward_per_sm(d, W, di));

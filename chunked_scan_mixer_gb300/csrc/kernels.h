@@ -61,6 +61,12 @@ int launch_reverse_scan(const float* src, float* dst, int BH, int H, int nseg, s
 // In place: ShB[s] += g^(L_s) Zh_end[s] C_B[s]^T for s >= 1.
 int launch_reverse_cross(const BwdArgs& b, const float* CB, int d, int dv, cudaStream_t st);
 
+// ratio-normalised backward: quotient-rule glue (bwd_normalize.cu)
+int launch_unit_first_column(bf16* e0, size_t rows, int d, cudaStream_t st);
+int launch_quotient_rule(const bf16* dout, const bf16* num, const bf16* den_out, bf16* dnum, bf16* dden,
+                         size_t rows, int dv, int d, float eps, cudaStream_t st);
+int launch_add_into(bf16* a, const bf16* b, size_t count, cudaStream_t st);
+
 // Tensor-core (mma.sync bf16) chunk kernel: d == dv in {16,32,64,128}, W in {16,32,64,128}.
 // Returns 0 on success, -1 on a CUDA error, -2 if the shape is not compiled.
 int launch_fwd_chunk_mma(const ChunkArgs& a, int d, int dv, int W, int mode, bool track_cm,

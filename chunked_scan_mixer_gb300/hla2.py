@@ -89,7 +89,7 @@ def lib():
         L.hla2_forward_plan.restype = I
         L.hla2_workspace_status.argtypes = [P, P]
         L.hla2_workspace_status.restype = I
-        L.hla2_backward_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+        L.hla2_backward_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
         L.hla2_backward_workspace_bytes.restype = Z
         L.hla2_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
         L.hla2_backward.restype = I
@@ -220,7 +220,7 @@ def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state
     if save_for_backward:
         if host:
             raise ValueError("save_for_backward needs device tensors")
-        nbytes = L.hla2_backward_workspace_bytes(B, H, n, d, dv, chunk, _DTYPES[q.dtype])
+        nbytes = L.hla2_backward_workspace_bytes(B, H, n, d, dv, chunk, _DTYPES[q.dtype], 0)
         if nbytes == ctypes.c_size_t(-1).value:
             raise HLA2Error("hla2_backward_workspace_bytes", -2, "these arguments have no backward")
         ws = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
@@ -250,10 +250,12 @@ def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state
     return (o, fin) if return_final_state else o
 
 
-def backward(q, k, v, dout, gamma=None, chunk=64, dq=None, dk=None, dv=None, saved=None):
-    """Gradients (dq, dk, dv) of the unnormalised forward for upstream dout.  saved: the
+def backward(q, k, v, dout, gamma=None, chunk=64, dq=None, dk=None, dv=None, saved=None, normalize=False,
+             eps=1e-6):
+    """Gradients (dq, dk, dv) for upstream dout of the unnormalised forward, or with
+    ``normalize`` of the ratio-normalised one (o / (den + eps)).  saved: the
     SavedForBackward of forward(..., save_for_backward=True) on the same q, k, v, gamma
-    and chunk (the forward is then not recomputed)."""
+    and chunk (the forward is then not recomputed; unnormalised only)."""
     host = q.device.type == "cpu"
     device = torch.device("cuda", torch.cuda.current_device()) if host else q.device
     L = lib()
@@ -271,14 +273,14 @@ def backward(q, k, v, dout, gamma=None, chunk=64, dq=None, dk=None, dv=None, sav
             raise ValueError("saved was made for other sizes, chunk, dtype or device")
         ws, nbytes, flags = saved.ws, saved.nbytes, FLAG_STATES_SAVED
     else:
-        nbytes = L.hla2_backward_workspace_bytes(B, H, n, d, dvdim, chunk, _DTYPES[q.dtype])
+        nbytes = L.hla2_backward_workspace_bytes(B, H, n, d, dvdim, chunk, _DTYPES[q.dtype], int(normalize))
         if nbytes == ctypes.c_size_t(-1).value:
             nbytes = 0
         ws = _workspace(int(nbytes), device, sh)
-    opts = Opts(_DTYPES[q.dtype], 1e-6, None if ws is None else ws.data_ptr(), int(nbytes), None, None,
+    opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), int(nbytes), None, None,
                 None, 0, flags)
     rc = L.hla2_backward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(dod), _ptr(gq), _ptr(gk), _ptr(gv), B, H, n, d,
-                         dvdim, _ptr(g), 0, chunk, sh, ctypes.byref(opts))
+                         dvdim, _ptr(g), int(normalize), chunk, sh, ctypes.byref(opts))
     _check("hla2_backward", rc)
     if host:
         return gq.cpu(), gk.cpu(), gv.cpu()

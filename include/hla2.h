@@ -147,13 +147,19 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
 int hla2_workspace_status(const void* workspace, hla2_stream_t stream);
 
 /* Scratch bytes hla2_backward needs; (size_t)-1 for rejected arguments. */
-size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype);
+size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
+                                     int normalize);
 
 /*
  * Reverse-mode chunk scan (section summary §4.2: gradients equal to those of the
- * serial recurrence) of the UNNORMALISED forward: given dout = dL/dout, writes
- * dq, dk, dv.  normalize != 0 returns HLA2_ERR_UNSUPPORTED.  init_state and
- * final_state in opts must be NULL (gradients start from the empty state).
+ * serial recurrence): given dout = dL/dout, writes dq, dk, dv.  bf16 tensors, d == dv.
+ * normalize == 0: gradients of the unnormalised output.  normalize == 1: gradients of
+ * o / (den + opts->eps) by the quotient rule (section summary §5.1), as two unnormalised
+ * passes -- one with (v, dout / (den + eps)), one with the value rows (1, 0, ..., 0)
+ * and the upstream gradient -(dout . num) / (den + eps)^2 in column 0 -- after two
+ * unnormalised forwards for num and den; the workspace then also holds those
+ * intermediates (bf16).  init_state and final_state in opts must be NULL (gradients
+ * start from the empty state); HLA2_FLAG_STATES_SAVED needs normalize == 0.
  */
 int hla2_backward(const void* q, const void* k, const void* v, const void* dout, void* dq,
                   void* dk, void* dv_out, int B, int H, int n, int d, int dv,

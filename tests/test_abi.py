@@ -86,11 +86,20 @@ def test_decode_rejects_bad_arguments(L):
     assert rc == 0
 
 
-def test_backward_rejects_normalized(L):
-    o = Opts(1, 1e-6, None, 0, None, None)
+def test_normalized_backward_checks_before_launching(L):
+    """The ratio-normalised backward is argument-checked on the host: it needs its larger
+    workspace, finite eps, and cannot reuse saved (unnormalised) forward states."""
     p = ctypes.c_void_p(16)
+    o = Opts(1, 1e-6, None, 0, None, None)
+    rc = L.hla2_backward(p, p, p, p, p, p, p, 1, 1, 16, 16, 16, None, 1, 16, None, ctypes.byref(o))
+    assert rc == -3 and b"workspace" in L.hla2_last_error()
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 2)
     rc = L.hla2_backward(p, p, p, p, p, p, p, 1, 1, 16, 16, 16, None, 1, 16, None, ctypes.byref(o))
     assert rc == -2
+    n0 = L.hla2_backward_workspace_bytes(1, 2, 100, 32, 32, 32, 1, 0)
+    n1 = L.hla2_backward_workspace_bytes(1, 2, 100, 32, 32, 32, 1, 1)
+    assert 0 < n0 < n1 < 2**40
+    assert L.hla2_backward_workspace_bytes(1, 2, 100, 32, 16, 32, 1, 1) == ctypes.c_size_t(-1).value  # d != dv
 
 
 def test_unknown_flags_rejected(L):

@@ -1,6 +1,7 @@
 """GPU reverse-mode chunk scan (dQ, dK, dV) against the float64 oracle's reverse sweep of
 the serial recurrence, through the C ABI.  Bar: max|gpu - oracle| / max|oracle| <= 2e-2
 per gradient (bf16 inputs; the oracle runs on the same bf16-rounded values)."""
+import numpy as np
 import pytest
 import torch
 
@@ -110,3 +111,55 @@ def test_save_for_backward_rejects_uncovered_requests():
     _, saved = hla.forward(q, k, v, gamma=x["gamma"].cuda(), chunk=64, save_for_backward=True)
     with pytest.raises(ValueError):  # other chunk than the saving forward
         hla.backward(q, k, v, v, gamma=x["gamma"].cuda(), chunk=32, saved=saved)
+
+
+def _normalized_reference(x, eps):
+    """Oracle gradients of the normalised output and the conditioning of their quotient-rule
+    split: kappa = (max|numerator part| + max|denominator part|) / max|sum|, per gradient."""
+    q, k, v, do = (np32(x[t]) for t in ("q", "k", "v", "dout"))
+    g = x["gamma"].double().numpy()
+    ones = np.ones(v.shape[:-1] + (1,), dtype=np.float32)
+    num = cref.forward(q, k, v, g)
+    den = cref.forward(q, k, ones, g)[..., 0]
+    inv = 1.0 / (den + eps)
+    p1 = cref.backward(q, k, v, do * inv[..., None], g)
+    p2 = cref.backward(q, k, ones, (-np.sum(do * num, axis=-1) * inv * inv)[..., None], g)
+    ref = cref.backward_normalized(q, k, v, do, g, eps)
+    kappa = [(np.abs(a).max() + np.abs(b).max()) / np.abs(a + b).max() for a, b in zip(p1[:2], p2[:2])] + [1.0]
+    return ref, kappa
+
+
+@pytest.mark.parametrize("d,chunk,n", [(32, 32, 300), (64, 64, 1000), (64, 128, 777), (128, 64, 400)])
+def test_normalized_gradients_match_oracle(d, chunk, n):
+    """Ratio-normalised backward (quotient rule over unnormalised passes) against the oracle's
+    normalised adjoint on the normalised workload's recipe (positive q, k: den > 0).
+
+    dq and dk are a difference of a numerator part and a denominator part that can be many
+    times larger than the result. Four bf16 roundings enter each part: den, the two upstream
+    gradients and the pass's own operands, each within 2^-9 relative. So the bar is
+    max(2e-2, 2^-7 kappa), with kappa the parts' magnitude over the result's (from the
+    oracle, same inputs). dv has no such split."""
+    x = inputs.make_custom(2, 2, n, d, d, torch.bfloat16, seed=40 + d + n, qk="softplus", v_scale="unit",
+                           gamma=(0.95, 0.999), with_dout=True)
+    g = x["gamma"].cuda()
+    got = hla.backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), gamma=g, chunk=chunk,
+                       normalize=True, eps=1e-6)
+    ref, kappa = _normalized_reference(x, 1e-6)
+    for name, gg, rr, kk in zip(("dq", "dk", "dv"), got, ref, kappa):
+        assert torch.isfinite(gg.float()).all(), name
+        assert rel_err(np64(gg.cpu()), rr) <= max(2e-2, 2.0 ** -7 * kk), (name, kk)
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_normalized_gradients_short_memory(d):
+    """Positive q, k scaled by 1/sqrt(d) and a short memory (decay 0.8-0.9), under the same
+    conditioning-aware bar."""
+    x = inputs.make_custom(1, 3, 500, d, d, torch.bfloat16, seed=50 + d, qk="softplus", v_scale="unit",
+                           gamma=(0.8, 0.9), with_dout=True)
+    x["q"] = (x["q"].float() / d ** 0.5).to(torch.bfloat16)
+    x["k"] = (x["k"].float() / d ** 0.5).to(torch.bfloat16)
+    ref, kappa = _normalized_reference(x, 1e-6)
+    got = hla.backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), gamma=x["gamma"].cuda(),
+                       chunk=64, normalize=True, eps=1e-6)
+    for name, gg, rr, kk in zip(("dq", "dk", "dv"), got, ref, kappa):
+        assert rel_err(np64(gg.cpu()), rr) <= max(2e-2, 2.0 ** -7 * kk), (name, kk)
