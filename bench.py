@@ -7,9 +7,10 @@ algorithmic traffic, larger than the 129 MB L2, so no flush is needed between st
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-After the timed headline it measures two more rows of the path on their own workloads
-(reported under "secondary"): the decode step (256 sequences x 32 heads, d = dv = 128)
-and a training step (forward + backward, B=4 H=16 n=8192 d = dv = 128).
+After the timed headline it measures more rows of the path on their own workloads
+(reported under "secondary"): the decode step (256 sequences x 32 heads, d = dv = 128) on
+the packed and on the compact state, and a training step (forward + backward, B=4 H=16
+n=8192 d = dv = 128).
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own replica
 of the workload (weak scaling, no collective in the data path); the timed region is
@@ -47,7 +48,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode and training rows measured after the headline")
-    ap.add_argument("--only", choices=("decode", "train"), default=None,
+    ap.add_argument("--only", choices=("decode", "decode_compact", "train"), default=None,
                     help="measure only this row (for profiler captures; --steps/--warmup apply)")
     ap.add_argument("--decode-seqs", type=int, default=256,
                     help="sequences of the decode row (smaller case for ncu --set full captures)")
@@ -274,7 +275,8 @@ def _device_ms(fn, steps, warmup, stream_sync):
     return t0.elapsed_time(t1) / steps
 
 
-def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5, seqs: int = 256):
+def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5, seqs: int = 256,
+                   compact: bool = False):
     """Decode row: 256 sequences x 32 heads, d = dv = 128, one single-token step per
     iteration on a resident fp32 state (the state's values do not change the work: it
     starts from N(0, 1e-4) draws instead of a 4096-token prefill).  Inputs of every step
@@ -286,7 +288,7 @@ def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int
 
     w = inputs.WORKLOADS["decode_prefill"]
     N, H, d, dv = seqs, w.H, w.d, w.dv
-    sf = hla.state_floats(d, dv)
+    sf = hla.state_floats(d, dv, compact=compact)
     gen = torch.Generator(device=dev)
     gen.manual_seed(replica_seed(w.seed, dist.rank))
     state = torch.randn((N, H, sf), generator=gen, device=dev, dtype=torch.float32) * 1e-2
@@ -298,13 +300,14 @@ def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int
     def one():
         q, k, v = xs[it[0] % steps]
         it[0] += 1
-        hla.decode_step(state, q, k, v, gamma=gamma, out=out)
+        hla.decode_step(state, q, k, v, gamma=gamma, out=out, compact=compact)
 
     ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
     heads = N * H
     nbytes = 2 * heads * sf * 4 + heads * (2 * d + dv) * 2 + heads * dv * 2
     achieved = nbytes / (ms * 1e-3) / 1e9
-    return {"workload": f"decode step: {N} sequences x H={H}, d=dv={d}, fp32 state, bf16 q/k/v/out, "
+    layout = "compact state (S upper block triangle)" if compact else "packed state"
+    return {"workload": f"decode step: {N} sequences x H={H}, d=dv={d}, fp32 {layout}, bf16 q/k/v/out, "
                         f"decay {w.gamma[0]}, unnormalised",
             "metric": "decode tokens/s (sequences x heads per second)", "unit": "tokens/s",
             "value": dist.world * heads / (ms * 1e-3), "us_per_step": ms * 1e3, "steps": steps,
@@ -349,8 +352,9 @@ def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: in
 
 def run_only(args, dist: Dist, dev):
     hbm_gbs, bf16_tflops, _ = peaks()
-    if args.only == "decode":
-        row = measure_decode(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs)
+    if args.only in ("decode", "decode_compact"):
+        row = measure_decode(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs,
+                             compact=args.only == "decode_compact")
     else:
         row = measure_train(dev, dist, bf16_tflops, hbm_gbs, steps=args.steps, warmup=args.warmup)
     if dist.rank == 0:
@@ -463,6 +467,7 @@ def run_ours(args, dist: Dist):
     secondary = None
     if not args.no_secondary and args.n is None:
         secondary = {"decode": measure_decode(dev, dist, hbm_gbs),
+                     "decode_compact": measure_decode(dev, dist, hbm_gbs, compact=True),
                      "train": measure_train(dev, dist, bf16_tflops, hbm_gbs)}
 
     cpu = None

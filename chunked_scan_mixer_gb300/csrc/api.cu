@@ -733,18 +733,48 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
                      const hla2_opts* opts) {
     const int dtype = opts ? opts->dtype : HLA2_BF16;
     const float eps = opts ? opts->eps : 1e-6f;
+    const int flags = opts ? opts->flags : 0;
     int rc = check_common(N, H, 0, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
     if (normalize && !isfinite(eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
+    if (flags & ~HLA2_FLAG_COMPACT_STATE) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_decode_step");
     if ((long)N * H == 0) return succeed();
     if (!state || !q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "state, q, k, v, out must not be NULL");
     if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return fail(HLA2_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
     cudaGetLastError();
     if (launch_decode_step(state, q, k, v, out, N, H, d, dv, gamma, normalize, eps, dtype == HLA2_BF16,
-                           reinterpret_cast<cudaStream_t>(stream)))
+                           (flags & HLA2_FLAG_COMPACT_STATE) != 0, reinterpret_cast<cudaStream_t>(stream)))
         return cuda_fail("decode step");
     return succeed();
+}
+
+size_t hla2_compact_state_floats(int d, int dv) { return compact_state_floats(d, dv); }
+
+static int state_convert(const float* src, float* dst, int N, int H, int d, int dv, hla2_stream_t stream,
+                         bool to_compact) {
+    if (N < 0 || H < 0) return fail(HLA2_ERR_INVALID_ARG, "N, H must be >= 0 (got %d, %d)", N, H);
+    if (!dim_ok(d) || !dim_ok(dv))
+        return fail(HLA2_ERR_INVALID_ARG, "d and dv must be 16, 32, 64 or 128 (got %d, %d)", d, dv);
+    const long heads = (long)N * H;
+    if (heads == 0) return succeed();
+    if (!src || !dst) return fail(HLA2_ERR_INVALID_ARG, "state pointers must not be NULL");
+    const size_t nsrc = heads * (to_compact ? raw_state_floats(d, dv) : compact_state_floats(d, dv));
+    const size_t ndst = heads * (to_compact ? compact_state_floats(d, dv) : raw_state_floats(d, dv));
+    if (src < dst + ndst && dst < src + nsrc) return fail(HLA2_ERR_INVALID_ARG, "source and destination overlap");
+    cudaGetLastError();
+    if (launch_state_compact(src, dst, heads, d, dv, to_compact, reinterpret_cast<cudaStream_t>(stream)))
+        return cuda_fail("state layout conversion");
+    return succeed();
+}
+
+int hla2_state_to_compact(const float* state, float* compact, int N, int H, int d, int dv, hla2_stream_t stream) {
+    return state_convert(state, compact, N, H, d, dv, stream, true);
+}
+
+int hla2_state_from_compact(const float* compact, float* state, int N, int H, int d, int dv,
+                            hla2_stream_t stream) {
+    return state_convert(compact, state, N, H, d, dv, stream, false);
 }
 
 }  // extern "C"

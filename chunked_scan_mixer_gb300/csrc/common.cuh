@@ -91,6 +91,30 @@ __host__ __device__ inline PackOff pack_off(int d, int dv) {
     return r;
 }
 
+// Compact decode state of one head: S symmetric, stored block-triangularly -- row a holds
+// S[a][b] for b = 4 floor(a/4) .. d-1 (the upper triangle plus the lower half of the 4 x 4
+// diagonal blocks), rows back to back; then C, G, m, h as in the packed layout.  Every row
+// starts on a multiple of 4 floats.  S takes d (d + 4) / 2 floats.
+__host__ __device__ inline size_t compact_s_floats(int d) { return (size_t)d * (d + 4) / 2; }
+__host__ __device__ inline size_t compact_state_floats(int d, int dv) {
+    return compact_s_floats(d) + 2 * (size_t)d * dv + 2 * (size_t)d;
+}
+// float offset of row a of the compact S
+//   block row j = a / 4 starts after 4 rows of d - 4 j' floats for every j' < j
+__host__ __device__ inline size_t compact_row(int a, int d) {
+    const long long j = a >> 2, r = a & 3;
+    return (size_t)(4 * j * d - 8 * j * (j - 1) + r * (d - 4 * j));
+}
+__host__ __device__ inline PackOff compact_off(int d, int dv) {
+    PackOff r;
+    r.S = 0;
+    r.C = compact_s_floats(d);
+    r.G = r.C + (size_t)d * dv;
+    r.m = r.G + (size_t)d * dv;
+    r.h = r.m + d;
+    return r;
+}
+
 // ---------------------------------------------------------------------------
 // Element access
 // ---------------------------------------------------------------------------

@@ -57,7 +57,8 @@ __device__ __forceinline__ void column_reduce(float4 p, int dv, float* red /*[kW
     __syncthreads();
 }
 
-template <typename T>
+// COMPACT: the state uses the compact layout (S block-triangular, see compact_off).
+template <typename T, bool COMPACT>
 __global__ void __launch_bounds__(kThreads)
     decode_step_kernel(float* __restrict__ state, const T* __restrict__ q, const T* __restrict__ k,
                        const T* __restrict__ v, T* __restrict__ out, int H, int d, int dv,
@@ -67,8 +68,8 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ __align__(16) float red[kWarps * kMaxDim];
     const int head = blockIdx.x, tid = threadIdx.x;
     const float g = head_decay(gamma, head, H), g2 = g * g;
-    float* S = state + (size_t)head * raw_state_floats(d, dv);
-    const PackOff po = pack_off(d, dv);
+    float* S = state + (size_t)head * (COMPACT ? compact_state_floats(d, dv) : raw_state_floats(d, dv));
+    const PackOff po = COMPACT ? compact_off(d, dv) : pack_off(d, dv);
     float *C = S + po.C, *G = S + po.G, *m = S + po.m, *hh = S + po.h;
 
     for (int i = tid; i < d; i += kThreads) {
@@ -85,7 +86,52 @@ __global__ void __launch_bounds__(kThreads)
     float mh_dot = 0.f;  // this thread's part of u . m' - q . h', formed after pass S
 
     // ---- pass S ----------------------------------------------------------------------
-    {
+    if (COMPACT) {
+        // S' = g S + k k^T and u = S' q on the block-triangular storage.  As in the packed
+        // pass, d/4 lanes share a row and lane l owns column chunk l (columns 4l..4l+3);
+        // in row a it has data when l >= a/4 (the row's stored part starts at the diagonal
+        // block).  The row part S'[a][4l..] . q[4l..] is reduced across the row's lanes;
+        // right of the diagonal block the mirror S'[a][4l+e] q[a] (the entry S'[4l+e][a] of
+        // the lower triangle) is summed per lane and reduced over the rows at the end.
+        const int lpr = d / 4;
+        const int l = tid % lpr, c = 4 * l;
+        const int rows_per = kThreads / lpr;
+        float4 mir = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int a0 = tid / lpr; a0 < d; a0 += rows_per * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a < d && l >= (a >> 2)) x[u] = ld_stream(S + compact_row(a, d) + (size_t)(c - 4 * (a >> 2)));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                float part = 0.f;
+                if (a < d && l >= (a >> 2)) {
+                    const float ka = ks[a];
+                    float4 y = x[u];
+                    y.x = g * y.x + ka * ks[c + 0];
+                    y.y = g * y.y + ka * ks[c + 1];
+                    y.z = g * y.z + ka * ks[c + 2];
+                    y.w = g * y.w + ka * ks[c + 3];
+                    st_stream(S + compact_row(a, d) + (size_t)(c - 4 * (a >> 2)), y);
+                    part = y.x * qs[c] + y.y * qs[c + 1] + y.z * qs[c + 2] + y.w * qs[c + 3];
+                    if (l > (a >> 2)) {
+                        const float qa = qs[a];
+                        mir.x += y.x * qa;
+                        mir.y += y.y * qa;
+                        mir.z += y.z * qa;
+                        mir.w += y.w * qa;
+                    }
+                }
+                for (int o = lpr >> 1; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (a < d && l == 0) us[a] = part;
+            }
+        }
+        column_reduce(mir, d, red, zs);  // zs is free until pass G
+        for (int i = tid; i < d; i += kThreads) us[i] += zs[i];
+    } else {
         const int lpr = d / 4;               // lanes per row
         const int n4 = d * d / 4;
         for (int base = 0; base < n4; base += kThreads * 4) {
@@ -199,21 +245,70 @@ __global__ void __launch_bounds__(kThreads)
         out[(size_t)head * dv + e] = from_f32<T>((ws[e] - zs[e]) * inv);
 }
 
+// Packed [S d*d | C | G | m | h] -> compact (upper block triangle of S), one CTA per head.
+__global__ void __launch_bounds__(kThreads) state_to_compact_kernel(const float* __restrict__ full,
+                                                                   float* __restrict__ compact, int d, int dv) {
+    const size_t head = blockIdx.x;
+    const float* src = full + head * raw_state_floats(d, dv);
+    float* dst = compact + head * compact_state_floats(d, dv);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int a = warp; a < d; a += kWarps) {
+        const int b0 = 4 * (a >> 2);
+        float* row = dst + compact_row(a, d);
+        for (int b = b0 + lane; b < d; b += 32) row[b - b0] = src[(size_t)a * d + b];
+    }
+    const size_t tail = 2 * (size_t)d * dv + 2 * (size_t)d, cs = compact_s_floats(d), fs = (size_t)d * d;
+    for (size_t i = threadIdx.x; i < tail; i += kThreads) dst[cs + i] = src[fs + i];
+}
+
+// Compact -> packed, S mirrored from its stored upper block triangle.
+__global__ void __launch_bounds__(kThreads) state_from_compact_kernel(const float* __restrict__ compact,
+                                                                     float* __restrict__ full, int d, int dv) {
+    const size_t head = blockIdx.x;
+    const float* src = compact + head * compact_state_floats(d, dv);
+    float* dst = full + head * raw_state_floats(d, dv);
+    for (int e = threadIdx.x; e < d * d; e += kThreads) {
+        const int a = e / d, b = e % d;
+        dst[e] = b >= 4 * (a >> 2) ? src[compact_row(a, d) + (b - 4 * (a >> 2))]
+                                   : src[compact_row(b, d) + (a - 4 * (b >> 2))];
+    }
+    const size_t tail = 2 * (size_t)d * dv + 2 * (size_t)d, cs = compact_s_floats(d), fs = (size_t)d * d;
+    for (size_t i = threadIdx.x; i < tail; i += kThreads) dst[fs + i] = src[cs + i];
+}
+
+template <bool COMPACT>
+void launch_decode_t(float* state, const void* q, const void* k, const void* v, void* out, long heads, int H, int d,
+                     int dv, const float* gamma, int normalize, float eps, bool is_bf16, cudaStream_t st) {
+    if (is_bf16)
+        decode_step_kernel<bf16, COMPACT><<<(unsigned)heads, kThreads, 0, st>>>(
+            state, static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
+            static_cast<bf16*>(out), H, d, dv, gamma, normalize, eps);
+    else
+        decode_step_kernel<float, COMPACT><<<(unsigned)heads, kThreads, 0, st>>>(
+            state, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+            static_cast<float*>(out), H, d, dv, gamma, normalize, eps);
+}
+
 }  // namespace
 
 int launch_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
                        int N, int H, int d, int dv, const float* gamma, int normalize, float eps,
-                       bool is_bf16, cudaStream_t st) {
+                       bool is_bf16, bool compact, cudaStream_t st) {
     const long heads = (long)N * H;
     if (heads <= 0) return 0;
-    if (is_bf16)
-        decode_step_kernel<bf16><<<(unsigned)heads, kThreads, 0, st>>>(
-            state, static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
-            static_cast<bf16*>(out), H, d, dv, gamma, normalize, eps);
+    if (compact)
+        launch_decode_t<true>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
     else
-        decode_step_kernel<float><<<(unsigned)heads, kThreads, 0, st>>>(
-            state, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
-            static_cast<float*>(out), H, d, dv, gamma, normalize, eps);
+        launch_decode_t<false>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_state_compact(const float* src, float* dst, long heads, int d, int dv, bool to_compact, cudaStream_t st) {
+    if (heads <= 0) return 0;
+    if (to_compact)
+        state_to_compact_kernel<<<(unsigned)heads, kThreads, 0, st>>>(src, dst, d, dv);
+    else
+        state_from_compact_kernel<<<(unsigned)heads, kThreads, 0, st>>>(src, dst, d, dv);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

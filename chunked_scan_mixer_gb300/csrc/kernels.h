@@ -97,6 +97,7 @@ int launch_finalize(const ChunkArgs& a, int d, int dv, float* final_state, cudaS
 // Decode step.
 int launch_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
                        int N, int H, int d, int dv, const float* gamma, int normalize, float eps,
-                       bool is_bf16, cudaStream_t st);
+                       bool is_bf16, bool compact, cudaStream_t st);
+int launch_state_compact(const float* src, float* dst, long heads, int d, int dv, bool to_compact, cudaStream_t st);
 
 }  // namespace hla2

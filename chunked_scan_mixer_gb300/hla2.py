@@ -97,6 +97,11 @@ def lib():
         L.hla2_decode_step.restype = I
         L.hla2_forward_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, I, F, P]
         L.hla2_forward_noalloc.restype = I
+        L.hla2_compact_state_floats.argtypes = [I, I]
+        L.hla2_compact_state_floats.restype = Z
+        for name in ("hla2_state_to_compact", "hla2_state_from_compact"):
+            getattr(L, name).argtypes = [P, P, I, I, I, I, P]
+            getattr(L, name).restype = I
         _lib = L
         return L
 
@@ -104,8 +109,11 @@ def lib():
 EXPORTED_SYMBOLS = (
     "hla2_version", "hla2_last_error", "hla2_state_floats", "hla2_forward_workspace_bytes",
     "hla2_forward", "hla2_forward_plan", "hla2_workspace_status", "hla2_backward_workspace_bytes",
-    "hla2_backward", "hla2_decode_step", "hla2_forward_noalloc",
+    "hla2_backward", "hla2_decode_step", "hla2_forward_noalloc", "hla2_compact_state_floats",
+    "hla2_state_to_compact", "hla2_state_from_compact",
 )
+
+FLAG_COMPACT_STATE = 4
 
 
 def _check(func, rc):
@@ -146,8 +154,29 @@ def check_status(device=None):
         _check("hla2_workspace_status", lib().hla2_workspace_status(ctypes.c_void_p(buf.data_ptr()), sh))
 
 
-def state_floats(d, dv):
-    return int(lib().hla2_state_floats(d, dv))
+def state_floats(d, dv, compact=False):
+    """Floats in one head's decode state (packed layout, or the compact one)."""
+    return int(lib().hla2_compact_state_floats(d, dv) if compact else lib().hla2_state_floats(d, dv))
+
+
+def _convert_state(src, d, dv, to_compact):
+    if src.device.type != "cuda" or src.dtype != torch.float32 or not src.is_contiguous():
+        raise ValueError("state must be a contiguous float32 CUDA tensor")
+    N, H = src.shape[:2]
+    dst = torch.empty((N, H, state_floats(d, dv, compact=to_compact)), dtype=torch.float32, device=src.device)
+    fn = lib().hla2_state_to_compact if to_compact else lib().hla2_state_from_compact
+    _check(fn.__name__, fn(_ptr(src), _ptr(dst), N, H, d, dv, _stream_handle(src.device)))
+    return dst
+
+
+def state_to_compact(state, d, dv):
+    """[N, H, state_floats(d, dv)] packed states -> [N, H, state_floats(d, dv, compact=True)]."""
+    return _convert_state(state, d, dv, True)
+
+
+def state_from_compact(compact, d, dv):
+    """Compact states -> packed states (S mirrored from its stored upper block triangle)."""
+    return _convert_state(compact, d, dv, False)
 
 
 def forward_workspace_bytes(B, H, n, d, dv, chunk=64, dtype=torch.bfloat16, normalize=False,
@@ -287,9 +316,10 @@ def backward(q, k, v, dout, gamma=None, chunk=64, dq=None, dk=None, dv=None, sav
     return gq, gk, gv
 
 
-def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6, out=None):
-    """One decode step; ``state`` [N,H,state_floats] float32 on the GPU is updated in
-    place.  q, k [N,H,d]; v [N,H,dv].  Returns out [N,H,dv]."""
+def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6, out=None, compact=False):
+    """One decode step; ``state`` [N,H,state_floats(d, dv, compact)] float32 on the GPU is
+    updated in place (compact: the block-triangular S layout).  q, k [N,H,d]; v [N,H,dv].
+    Returns out [N,H,dv]."""
     L = lib()
     if state.device.type != "cuda" or state.dtype != torch.float32 or not state.is_contiguous():
         raise ValueError("state must be a contiguous float32 CUDA tensor")
@@ -299,7 +329,7 @@ def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6, out=None)
     qd, kd, vd = (_to_device(t, device) for t in (q, k, v))
     g = _gamma_tensor(gamma, H, device)
     o = out if out is not None else torch.empty((N, H, dv), dtype=q.dtype, device=device)
-    opts = Opts(_DTYPES[q.dtype], float(eps), None, 0, None, None, None, 0)
+    opts = Opts(_DTYPES[q.dtype], float(eps), None, 0, None, None, None, 0, FLAG_COMPACT_STATE if compact else 0)
     rc = L.hla2_decode_step(_ptr(state), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), N, H, d, dv, _ptr(g),
                             int(normalize), _stream_handle(device), ctypes.byref(opts))
     _check("hla2_decode_step", rc)

@@ -94,7 +94,7 @@ typedef struct {
  *     the backward then skips its forward recomputation.  The library cannot check that
  *     the workspace is still intact: passing this flag otherwise gives wrong gradients.
  */
-enum { HLA2_FLAG_SAVE_FOR_BACKWARD = 1, HLA2_FLAG_STATES_SAVED = 2 };
+enum { HLA2_FLAG_SAVE_FOR_BACKWARD = 1, HLA2_FLAG_STATES_SAVED = 2, HLA2_FLAG_COMPACT_STATE = 4 };
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int hla2_version(void);
@@ -176,6 +176,27 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
 int hla2_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
                      int N, int H, int d, int dv, const float* gamma, int normalize,
                      hla2_stream_t stream, const hla2_opts* opts);
+
+/*
+ * Compact decode state.  S is symmetric (a sum of decayed k k^T), so a head's state can
+ * keep only its upper block triangle: row a holds S[a][b] for b = 4*floor(a/4) .. d-1,
+ * rows back to back (d*(d+4)/2 floats; every row starts on 16 bytes), followed by C, G, m,
+ * h as in the packed layout.  hla2_decode_step with opts->flags & HLA2_FLAG_COMPACT_STATE
+ * reads and writes states in this layout, moving 16 % fewer bytes per step at
+ * d = dv = 128.  The same bit is an argument error for every other entry point.
+ */
+size_t hla2_compact_state_floats(int d, int dv);
+
+/*
+ * Convert N*H head states between the packed and the compact layouts (device pointers,
+ * asynchronous on stream, src and dst must not overlap).  To compact: S's upper block
+ * triangle is kept (a packed S that is not exactly symmetric loses its other triangle);
+ * from compact: S is mirrored.  Returns HLA2_OK, HLA2_ERR_INVALID_ARG or HLA2_ERR_CUDA.
+ */
+int hla2_state_to_compact(const float* state, float* compact, int N, int H, int d, int dv,
+                          hla2_stream_t stream);
+int hla2_state_from_compact(const float* compact, float* state, int N, int H, int d, int dv,
+                            hla2_stream_t stream);
 
 /*
  * hla2_forward for callers that cannot allocate device memory (no counterpart in the

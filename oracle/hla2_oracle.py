@@ -62,6 +62,9 @@ __all__ = [
     "pack_state",
     "unpack_state",
     "state_floats",
+    "compact_state_floats",
+    "compact_from_state",
+    "state_from_compact",
 ]
 
 
@@ -459,3 +462,38 @@ def unpack_state(flat, d, dv):
     m = flat[..., o:o + d].reshape(B, H, d); o += d
     h = flat[..., o:o + d].reshape(B, H, d); o += d
     return {"S": S, "C": C, "m": m, "G": G, "h": h}
+
+
+# ---------------------------------------------------------------------------
+# Compact decode layout (a storage choice of the GPU library, not of the pages): S is a
+# sum of decayed k k^T, hence symmetric, and only its upper block triangle is stored --
+# row a keeps S[a, b] for b = 4 floor(a/4) .. d-1 -- followed by C, G, m, h.
+# ---------------------------------------------------------------------------
+
+def compact_state_floats(d, dv):
+    return d * (d + 4) // 2 + 2 * d * dv + 2 * d
+
+
+def compact_from_state(flat, d, dv):
+    """[B, H, state_floats] packed states -> [B, H, compact_state_floats] (S's upper block
+    triangle, row by row, then C, G, m, h)."""
+    flat = np.asarray(flat, dtype=np.float64)
+    S = flat[..., :d * d].reshape(flat.shape[:-1] + (d, d))
+    rows = [S[..., a, 4 * (a // 4):] for a in range(d)]
+    return np.concatenate(rows + [flat[..., d * d:]], axis=-1)
+
+
+def state_from_compact(flat, d, dv):
+    """Inverse of compact_from_state with S mirrored from the stored triangle."""
+    flat = np.asarray(flat, dtype=np.float64)
+    S = np.zeros(flat.shape[:-1] + (d, d))
+    o = 0
+    for a in range(d):
+        b0 = 4 * (a // 4)
+        S[..., a, b0:] = flat[..., o:o + d - b0]
+        o += d - b0
+    for a in range(d):
+        for b in range(4 * (a // 4)):
+            S[..., a, b] = S[..., b, a]
+    return np.concatenate([S.reshape(flat.shape[:-1] + (d * d,)), flat[..., o:]], axis=-1)
+

@@ -114,3 +114,18 @@ def test_unknown_flags_rejected(L):
     o = Opts(1, 1e-6, None, 0, None, None, None, 0, 2)  # STATES_SAVED is a backward flag
     rc = L.hla2_forward(p, p, p, p, 0, 1, 16, 16, 16, None, 0, 16, None, ctypes.byref(o))
     assert rc == -1
+
+
+def test_compact_state_abi(L):
+    from oracle import hla2_oracle as O
+
+    for d, dv in ((16, 16), (64, 32), (128, 128)):
+        assert L.hla2_compact_state_floats(d, dv) == O.compact_state_floats(d, dv)
+    assert L.hla2_compact_state_floats(128, 128) == 41472  # 8448 for S instead of 16384
+    p = ctypes.c_void_p(16)
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 1)  # a forward flag on the decode step
+    rc = L.hla2_decode_step(p, p, p, p, p, 1, 1, 16, 16, None, 0, None, ctypes.byref(o))
+    assert rc == -1 and b"flags" in L.hla2_last_error()
+    assert L.hla2_state_to_compact(p, p, 1, 1, 20, 16, None) == -1      # bad d
+    assert L.hla2_state_to_compact(None, None, 0, 4, 16, 16, None) == 0  # nothing to do
+    assert L.hla2_state_from_compact(p, p, 1, 1, 16, 16, None) == -1     # overlapping buffers

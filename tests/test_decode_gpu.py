@@ -97,3 +97,68 @@ def test_decode_workload_full_width_sampled():
         ref = cref.decode_step(st_ref, np32(q[sub]), np32(k[sub]), np32(v[sub]), gd)
         assert rel_err(np64(o[sub].cpu()), ref) <= 2e-2, step
         assert torch.isfinite(o.float()).all()
+
+
+@pytest.mark.parametrize("d, dv", [(16, 16), (64, 64), (128, 128), (32, 64)])
+def test_compact_conversion_is_exact(d, dv):
+    """To-compact keeps S's upper block triangle bit for bit (the oracle's own packing of the
+    same layout); from-compact mirrors it back."""
+    st, _ = prefill_state(2, 3, d, dv, 30, seed=70 + d, gamma=(0.95, 0.999))
+    S = st[..., :d * d].reshape(2, 3, d, d)
+    st = st.copy()
+    st[..., :d * d] = (0.5 * (S + np.swapaxes(S, -1, -2))).reshape(2, 3, d * d)  # exactly symmetric
+    full = torch.from_numpy(st.astype(np.float32)).cuda()
+    c = hla.state_to_compact(full, d, dv)
+    ref_c = O.compact_from_state(st.astype(np.float32).astype(np.float64), d, dv)
+    assert np.array_equal(c.cpu().double().numpy(), ref_c)
+    back = hla.state_from_compact(c, d, dv)
+    assert torch.equal(back, full)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d, dv", [(16, 16), (64, 64), (128, 128), (64, 32)])
+@pytest.mark.parametrize("normalize", [False, True])
+def test_compact_decode_matches_oracle(dtype, d, dv, normalize):
+    """Decode steps on the compact state against the oracle's serial steps on the packed one."""
+    N, H = 3, 2
+    if normalize:
+        xs = inputs.make_custom(N, H, 6, d, dv, torch.float32, seed=98, qk="softplus", gamma=(0.95, 0.999))
+        gamma = xs["gamma"]
+        _, st = cref.forward(np32(xs["q"]), np32(xs["k"]), np32(xs["v"]), gamma.double().numpy(), return_state=True)
+    else:
+        st, gamma = prefill_state(N, H, d, dv, 40, seed=d + dv + 1, gamma=(0.95, 0.999))
+    st = st.astype(np.float32).astype(np.float64)
+    state_gpu = hla.state_to_compact(torch.from_numpy(st.astype(np.float32)).cuda(), d, dv)
+    # the oracle continues from the same S the compact state holds (its upper triangle)
+    state_ref = O.state_from_compact(O.compact_from_state(st, d, dv), d, dv).copy()
+    for step in range(5):
+        q, k, v = inputs.decode_step_inputs(step, N, H, d, dv, dtype=dtype)
+        if normalize:
+            q, k = q.float().abs().to(dtype), k.float().abs().to(dtype)
+        o = hla.decode_step(state_gpu, q.cuda(), k.cuda(), v.cuda(), gamma=gamma.cuda(), normalize=normalize,
+                            eps=1e-6, compact=True)
+        ref = cref.decode_step(state_ref, np32(q), np32(k), np32(v), gamma.double().numpy(), normalize=normalize,
+                               eps=1e-6)
+        assert rel_err(np64(o.cpu()), ref) <= tol_for(dtype), step
+    got = hla.state_from_compact(state_gpu, d, dv).cpu().double().numpy()
+    assert rel_err(got, state_ref) <= 1e-5
+
+
+def test_compact_decode_full_width_sampled():
+    """Full decode width (256 sequences x 32 heads, d = dv = 128), compact state: sampled
+    heads against the oracle."""
+    N, H, d = 256, 32, 128
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(11)
+    full = torch.randn((N, H, hla.state_floats(d, d)), generator=gen, device="cuda") * 1e-2
+    S = full[..., :d * d].view(N, H, d, d)
+    S.copy_(0.5 * (S + S.transpose(-1, -2)))
+    c = hla.state_to_compact(full, d, d)
+    g = torch.full((H,), 0.999, device="cuda")
+    q, k, v = inputs.decode_step_inputs(0, N, H, d, d, device="cuda")
+    o = hla.decode_step(c, q, k, v, gamma=g, compact=True)
+    for (n_, h_) in ((0, 0), (17, 5), (255, 31), (128, 16)):
+        st = full[n_:n_ + 1, h_:h_ + 1].double().cpu().numpy().copy()
+        ref = cref.decode_step(st, np32(q[n_:n_ + 1, h_:h_ + 1].cpu()), np32(k[n_:n_ + 1, h_:h_ + 1].cpu()),
+                               np32(v[n_:n_ + 1, h_:h_ + 1].cpu()), np.full(1, 0.999))
+        assert rel_err(np64(o[n_:n_ + 1, h_:h_ + 1].cpu()), ref) <= 2e-2

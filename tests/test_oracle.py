@@ -485,3 +485,34 @@ def test_planted_combine_mistake_is_caught(monkeypatch):
     monkeypatch.setattr(O, "combine", wrong)
     bad = O.chunked_scan_forward(q, k, v, [0.9], chunk=4)
     assert rel(bad, truth) > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# Compact decode layout (S symmetric: upper block triangle only)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d,dv", [(16, 16), (32, 64), (128, 128)])
+def test_compact_layout_size_and_roundtrip(d, dv):
+    """d (d + 4) / 2 floats for S (the upper triangle plus the lower halves of the 4 x 4
+    diagonal blocks); a symmetric S survives the round trip exactly."""
+    r = np.random.default_rng(d + dv)
+    A = r.standard_normal((2, 3, d, d))
+    S = A + np.swapaxes(A, -1, -2)
+    rest = r.standard_normal((2, 3, 2 * d * dv + 2 * d))
+    flat = np.concatenate([S.reshape(2, 3, d * d), rest], axis=-1)
+    c = O.compact_from_state(flat, d, dv)
+    assert c.shape[-1] == O.compact_state_floats(d, dv) == d * (d + 4) // 2 + 2 * d * dv + 2 * d
+    assert np.array_equal(O.state_from_compact(c, d, dv), flat)
+    # row 5 of S starts after rows 0..3 (d floats each) and row 4 (d - 4 floats)
+    assert np.array_equal(c[..., 4 * d + (d - 4): 4 * d + (d - 4) + (d - 4)], S[..., 5, 4:])
+
+
+def test_compact_state_continues_the_serial_recurrence():
+    """A decode step on the expanded compact state equals one on the original state: the
+    state's S is symmetric, so nothing is lost (serial recurrence of the pages)."""
+    q, k, v = rnd(1, 2, 9, 8, 4, seed=41)
+    _, st = O.serial_forward(q, k, v, [0.9, 0.99], return_state=True)
+    flat = O.pack_state(st)
+    back = O.unpack_state(O.state_from_compact(O.compact_from_state(flat, 8, 4), 8, 4), 8, 4)
+    for key in ("S", "C", "G", "m", "h"):
+        assert np.allclose(back[key], st[key], rtol=0, atol=1e-12)
