@@ -751,6 +751,107 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
 
 size_t hla2_compact_state_floats(int d, int dv) { return compact_state_floats(d, dv); }
 
+static int ahla_check(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
+    int rc = check_common(B, H, n, d, dv, dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
+    if (dtype != HLA2_BF16 || d != dv || (chunk != 32 && chunk != 64))
+        return fail(HLA2_ERR_UNSUPPORTED, "the AHLA forward covers bf16, d == dv and chunk 32 or 64");
+    return HLA2_OK;
+}
+
+static Plan ahla_plan(int B, int H, int n, int d, int chunk) {
+    const DevInfo di = dev_info();
+    return make_plan(B, H, n, d, d, chunk, di.sms,
+                     blocks_per_sm(ahla_chunk_smem(d, chunk), ahla_chunk_threads(d), 4, di));
+}
+
+size_t hla2_ahla_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
+    if (ahla_check(B, H, n, d, dv, chunk, dtype, normalize) != HLA2_OK) return (size_t)-1;
+    const Plan p = ahla_plan(B, H, n, d, chunk);
+    return p.nseg > 0 ? ahla_layout(p).total * sizeof(float) : 0;
+}
+
+int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n, int d, int dv,
+                      const float* gamma, int normalize, int chunk, hla2_stream_t stream, const hla2_opts* opts) {
+    if (!opts) return fail(HLA2_ERR_INVALID_ARG, "opts must not be NULL");
+    int rc = ahla_check(B, H, n, d, dv, chunk, opts->dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (normalize && !isfinite(opts->eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
+    if (opts->flags) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_ahla_forward");
+    if (opts->init_state || opts->final_state)
+        return fail(HLA2_ERR_UNSUPPORTED, "the AHLA forward takes no init_state / final_state");
+    const long BH = (long)B * H;
+    if (BH == 0 || n == 0) return succeed();
+    if (!q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must not be NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
+    const Plan p = ahla_plan(B, H, n, d, chunk);
+    const AhlaLayout L = ahla_layout(p);
+    const size_t need = L.total * sizeof(float);
+    if (!opts->workspace || opts->workspace_bytes < need)
+        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
+                    opts->workspace ? opts->workspace_bytes : (size_t)0);
+    if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    AhlaArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.BH = (int)BH;
+    a.H = H;
+    a.n = n;
+    a.W = chunk;
+    a.nchunks = p.nchunks;
+    a.seg_chunks = p.seg_chunks;
+    a.nseg = p.nseg;
+    a.nsum = p.nseg - 1;
+    a.gamma = gamma;
+    a.normalize = normalize;
+    a.eps = opts->eps;
+    a.ws = static_cast<float*>(opts->workspace);
+    a.L = L;
+    auto mark = [&](int i) {
+        if (opts->phase_events && i < opts->n_phase_events && opts->phase_events[i] &&
+            cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[i]), st) != cudaSuccess)
+            cudaGetLastError();
+    };
+    cudaGetLastError();
+    mark(0);
+    if (launch_ahla_init(a, d, st)) return cuda_fail("AHLA carry-in initialisation");
+    mark(1);
+    if (p.nseg > 1) {
+        const int steps = p.nseg - 1, seg_tokens = p.seg_chunks * chunk;
+        const size_t dd = (size_t)d * d;
+        AhlaArgs b = a;
+        b.seg0 = 0;
+        b.nseg_launch = steps;
+        if (launch_ahla_chunk(b, d, chunk, true, st)) return cuda_fail("AHLA segment summaries");
+        mark(2);
+        if (launch_linear_scan(a.ws + L.PB, a.ws + L.Pin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true, gamma,
+                               seg_tokens, 1, st) ||
+            (normalize && launch_linear_scan(a.ws + L.mB, a.ws + L.min, a.BH, H, steps, d, a.nsum * (size_t)d,
+                                             p.nseg * (size_t)d, true, gamma, seg_tokens, 1, st)) ||
+            launch_ahla_cross(a, d, st) ||
+            launch_linear_scan(a.ws + L.EB, a.ws + L.Ein, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true, gamma,
+                               seg_tokens, 1, st) ||
+            (normalize && launch_linear_scan(a.ws + L.nB, a.ws + L.nin, a.BH, H, steps, d, a.nsum * (size_t)d,
+                                             p.nseg * (size_t)d, true, gamma, seg_tokens, 1, st)))
+            return cuda_fail("AHLA segment scan");
+    } else {
+        mark(2);
+    }
+    mark(3);
+    AhlaArgs o = a;
+    o.seg0 = 0;
+    o.nseg_launch = p.nseg;
+    if (launch_ahla_chunk(o, d, chunk, false, st)) return cuda_fail("AHLA output pass");
+    mark(4);
+    mark(5);
+    return succeed();
+}
+
 static int state_convert(const float* src, float* dst, int N, int H, int d, int dv, hla2_stream_t stream,
                          bool to_compact) {
     if (N < 0 || H < 0) return fail(HLA2_ERR_INVALID_ARG, "N, H must be >= 0 (got %d, %d)", N, H);

@@ -8,6 +8,48 @@
 
 namespace hla2 {
 
+// Workspace of the AHLA forward (float offsets, d == dv): segment summaries P_B, E_B
+// (d x dv), R_B (d x d), m_B, n_B (d); carries P_in, E_in, m_in, n_in per segment start.
+struct AhlaLayout {
+    size_t PB, EB, RB, mB, nB, Pin, Ein, min, nin, total;
+};
+inline AhlaLayout ahla_layout(const Plan& p) {
+    AhlaLayout L;
+    const size_t BH = p.BH, ns = p.nseg, nsm = p.nseg > 1 ? p.nseg - 1 : 0;
+    const size_t dd = (size_t)p.d * p.d, d = p.d;
+    size_t o = kStatusFloats;
+    L.PB = o;  o = align64(o + BH * nsm * dd);
+    L.EB = o;  o = align64(o + BH * nsm * dd);
+    L.RB = o;  o = align64(o + BH * nsm * dd);
+    L.mB = o;  o = align64(o + BH * nsm * d);
+    L.nB = o;  o = align64(o + BH * nsm * d);
+    L.Pin = o; o = align64(o + BH * ns * dd);
+    L.Ein = o; o = align64(o + BH * ns * dd);
+    L.min = o; o = align64(o + BH * ns * d);
+    L.nin = o; o = align64(o + BH * ns * d);
+    L.total = o;
+    return L;
+}
+
+// Arguments of one AHLA chunk-kernel launch.
+struct AhlaArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    int BH, H, n, W, nchunks, seg_chunks, nseg, seg0, nseg_launch, nsum;
+    const float* gamma;
+    int normalize;
+    float eps;
+    float* ws;
+    AhlaLayout L;
+};
+int launch_ahla_chunk(const AhlaArgs& a, int d, int W, bool summary, cudaStream_t st);
+int launch_ahla_init(const AhlaArgs& a, int d, cudaStream_t st);
+int launch_ahla_cross(const AhlaArgs& a, int d, cudaStream_t st);
+size_t ahla_chunk_smem(int d, int W);
+int ahla_chunk_threads(int d);
+
 // Arguments of one chunk-kernel launch (summary or output pass of the forward).
 struct ChunkArgs {
     const void* q;

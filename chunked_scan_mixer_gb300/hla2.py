@@ -97,6 +97,10 @@ def lib():
         L.hla2_decode_step.restype = I
         L.hla2_forward_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, I, F, P]
         L.hla2_forward_noalloc.restype = I
+        L.hla2_ahla_forward_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
+        L.hla2_ahla_forward_workspace_bytes.restype = Z
+        L.hla2_ahla_forward.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
+        L.hla2_ahla_forward.restype = I
         L.hla2_compact_state_floats.argtypes = [I, I]
         L.hla2_compact_state_floats.restype = Z
         for name in ("hla2_state_to_compact", "hla2_state_from_compact"):
@@ -110,7 +114,7 @@ EXPORTED_SYMBOLS = (
     "hla2_version", "hla2_last_error", "hla2_state_floats", "hla2_forward_workspace_bytes",
     "hla2_forward", "hla2_forward_plan", "hla2_workspace_status", "hla2_backward_workspace_bytes",
     "hla2_backward", "hla2_decode_step", "hla2_forward_noalloc", "hla2_compact_state_floats",
-    "hla2_state_to_compact", "hla2_state_from_compact",
+    "hla2_state_to_compact", "hla2_state_from_compact", "hla2_ahla_forward_workspace_bytes", "hla2_ahla_forward",
 )
 
 FLAG_COMPACT_STATE = 4
@@ -277,6 +281,37 @@ def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state
         o = o.to("cpu") if out is None else out.copy_(o)
         fin = None if fin is None else fin.to("cpu")
     return (o, fin) if return_final_state else o
+
+
+def ahla_forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, out=None, phase_events=None):
+    """Asymmetric HLA forward (the masked left-cascaded product Q (K^T Q)(K^T V)).
+    bf16 q, k, v [B,H,n,d] on the GPU (d == dv); chunk 32 or 64.  Returns out [B,H,n,d]."""
+    L = lib()
+    if q.device.type != "cuda" or q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must be bfloat16 CUDA tensors")
+    B, H, n, d = q.shape
+    dv = v.shape[-1]
+    device = q.device
+    qd, kd, vd = (t.contiguous() for t in (q, k, v))
+    g = _gamma_tensor(gamma, H, device)
+    o = out if out is not None else torch.empty((B, H, n, dv), dtype=q.dtype, device=device)
+    sh = _stream_handle(device)
+    nbytes = L.hla2_ahla_forward_workspace_bytes(B, H, n, d, dv, chunk, _DTYPES[q.dtype], int(normalize))
+    if nbytes == ctypes.c_size_t(-1).value:
+        nbytes = 0
+    ws = _workspace(int(nbytes), device, sh)
+    opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), int(nbytes), None, None,
+                None, 0, 0)
+    if phase_events:
+        for e in phase_events:
+            if not e.cuda_event:
+                e.record()
+        ev = (ctypes.c_void_p * len(phase_events))(*[e.cuda_event for e in phase_events])
+        opts.phase_events = ctypes.cast(ev, ctypes.POINTER(ctypes.c_void_p))
+        opts.n_phase_events = len(phase_events)
+    _check("hla2_ahla_forward", L.hla2_ahla_forward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), B, H, n, d, dv, _ptr(g),
+                                                    int(normalize), chunk, sh, ctypes.byref(opts)))
+    return o
 
 
 def backward(q, k, v, dout, gamma=None, chunk=64, dq=None, dk=None, dv=None, saved=None, normalize=False,

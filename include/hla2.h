@@ -178,6 +178,23 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
                      hla2_stream_t stream, const hla2_opts* opts);
 
 /*
+ * Asymmetric HLA (AHLA, technical summary item "2. Asymmetrische Lineare Aufmerksamkeit
+ * hoeherer Ordnung"; section summary §6): the masked left-cascaded product
+ * Q (K^T Q)(K^T V),
+ *   o_t = sum_{j <= t} sum_{i <= j} g^(t-i) (q_t . k_j)(q_j . k_i) v_i,
+ * streamed with P_t = g P + k v^T, E_t = g E + k (q^T P_t), o_t = q_t^T E_t (and m, n for
+ * the denominator with v -> 1; normalised output o / (den + eps)).  Chunk-parallel over an
+ * exclusive scan of segment summaries (P, E, m, n, R = sum k q^T) (section summary §6.2).
+ * bf16 q, k, v, out [B, H, n, d], d == dv in {16, 32, 64, 128}, chunk 32 or 64; no
+ * init_state / final_state; opts->flags must be 0.  Workspace as for hla2_forward.
+ */
+size_t hla2_ahla_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
+                                         int normalize);
+int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
+                      int d, int dv, const float* gamma, int normalize, int chunk,
+                      hla2_stream_t stream, const hla2_opts* opts);
+
+/*
  * Compact decode state.  S is symmetric (a sum of decayed k k^T), so a head's state can
  * keep only its upper block triangle: row a holds S[a][b] for b = 4*floor(a/4) .. d-1,
  * rows back to back (d*(d+4)/2 floats; every row starts on 16 bytes), followed by C, G, m,

@@ -1,0 +1,86 @@
+"""GPU AHLA forward (chunk-parallel, mma.sync) against the float64 AHLA oracle, through the
+C ABI.  Bar: max|gpu - oracle| / max|oracle| <= 2e-2 (bf16 inputs; the oracle runs on the
+same bf16-rounded values)."""
+import numpy as np
+import pytest
+import torch
+
+import chunked_scan_mixer_gb300 as hla
+from chunked_scan_mixer_gb300 import HLA2Error, inputs
+from oracle import ahla_oracle as A
+
+from .helpers import np32, np64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def run(x, chunk, normalize=False):
+    g = None if x["gamma"] is None else x["gamma"].cuda()
+    return hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), gamma=g, chunk=chunk,
+                            normalize=normalize).cpu()
+
+
+def oracle(x, normalize=False):
+    g = None if x["gamma"] is None else x["gamma"].double().numpy()
+    return A.serial_forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), g, normalize=normalize)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("chunk", [32, 64])
+def test_matches_oracle(d, chunk):
+    x = inputs.make_custom(1, 3, 5 * chunk + 11, d, d, torch.bfloat16, seed=d + chunk, gamma=(0.9, 0.999))
+    assert rel_err(np64(run(x, chunk)), oracle(x)) <= 2e-2
+
+
+@pytest.mark.parametrize("n", [1, 17, 64, 300, 2049])
+def test_lengths(n):
+    x = inputs.make_custom(2, 2, n, 64, 64, torch.bfloat16, seed=n, gamma=(0.95, 0.9995))
+    o = run(x, 64)
+    assert torch.isfinite(o.float()).all()
+    assert rel_err(np64(o), oracle(x)) <= 2e-2
+
+
+@pytest.mark.parametrize("gamma", [None, 0.9, (0.5, 0.999)])
+def test_decays(gamma):
+    x = inputs.make_custom(2, 2, 700, 32, 32, torch.bfloat16, seed=7, gamma=gamma)
+    assert rel_err(np64(run(x, 32)), oracle(x)) <= 2e-2
+
+
+@pytest.mark.parametrize("d", [32, 64])
+def test_normalized(d):
+    """Positive q, k keep the denominator (the same cascade with v -> 1) away from zero."""
+    x = inputs.make_custom(2, 2, 900, d, d, torch.bfloat16, seed=11 + d, qk="softplus", v_scale="unit",
+                           gamma=(0.95, 0.999))
+    assert rel_err(np64(run(x, 64, normalize=True)), oracle(x, normalize=True)) <= 2e-2
+
+
+def test_many_segments_and_heads():
+    """Many heads and several chunks per segment: exercises the carried state inside a CTA,
+    the segment summaries (P, E, R) and the scan's cross term."""
+    x = inputs.make_custom(2, 16, 128 * 40 + 5, 64, 64, torch.bfloat16, seed=12, gamma=(0.98, 0.9999))
+    assert rel_err(np64(run(x, 64)), oracle(x)) <= 2e-2
+
+
+def test_long_context_two_heads():
+    """The long-context length (n = 65536, d = 64) on two heads of the decay range."""
+    x = inputs.make_custom(1, 2, 65536, 64, 64, torch.bfloat16, seed=13, gamma=(0.99, 0.9999))
+    assert rel_err(np64(run(x, 64)), oracle(x)) <= 2e-2
+
+
+def test_causality_bit_exact():
+    x = inputs.make_custom(1, 2, 1000, 64, 64, torch.bfloat16, seed=14, gamma=0.995)
+    a = run(x, 64)
+    y = {key: (t.clone() if isinstance(t, torch.Tensor) else t) for key, t in x.items()}
+    for key in ("q", "k", "v"):
+        y[key][:, :, 640:] = (y[key][:, :, 640:].float() * 2 + 1).to(torch.bfloat16)
+    b = run(y, 64)
+    assert torch.equal(a[:, :, :640], b[:, :, :640])
+
+
+def test_rejects_uncovered_requests():
+    x = inputs.make_custom(1, 1, 64, 64, 32, torch.bfloat16, seed=15)
+    with pytest.raises(HLA2Error):  # d != dv
+        hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), chunk=64)
+    x = inputs.make_custom(1, 1, 64, 64, 64, torch.bfloat16, seed=15)
+    with pytest.raises(HLA2Error):  # chunk 128 is not compiled for AHLA
+        hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), chunk=128)
