@@ -9,8 +9,8 @@ algorithmic traffic, larger than the 129 MB L2, so no flush is needed between st
 
 After the timed headline it measures more rows of the path on their own workloads
 (reported under "secondary"): the decode step (256 sequences x 32 heads, d = dv = 128) on
-the packed and on the compact state, and a training step (forward + backward, B=4 H=16
-n=8192 d = dv = 128).
+the packed and on the compact state, a training step (forward + backward, B=4 H=16
+n=8192 d = dv = 128), and the asymmetric variant (AHLA) on the long-context shapes.
 
 Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own replica
 of the workload (weak scaling, no collective in the data path); the timed region is
@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode and training rows measured after the headline")
-    ap.add_argument("--only", choices=("decode", "decode_compact", "train"), default=None,
+    ap.add_argument("--only", choices=("decode", "decode_compact", "train", "ahla"), default=None,
                     help="measure only this row (for profiler captures; --steps/--warmup apply)")
     ap.add_argument("--decode-seqs", type=int, default=256,
                     help="sequences of the decode row (smaller case for ncu --set full captures)")
@@ -350,11 +350,56 @@ def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: in
                          "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm_gbs}}
 
 
+def measure_ahla(dev, dist: Dist, hbm_gbs: float, bf16_tflops: float, steps: int = 50, warmup: int = 5,
+                 n: int | None = None):
+    """AHLA row: the asymmetric operator on the long-context shapes (B=1 H=16 n=65536
+    d=dv=64 bf16, decay linspace(0.99, 0.9999), unnormalised, chunk 64); 1,048,576 tokens
+    per step; inputs + output exceed the L2."""
+    import dataclasses
+
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = dataclasses.replace(inputs.WORKLOADS["long"], chunk=64)
+    if n is not None:
+        w = dataclasses.replace(w, n=n)
+    x = inputs.make(w, device=dev, seed=replica_seed(w.seed, dist.rank))
+    q, k, v = x["q"], x["k"], x["v"]
+    gamma = x["gamma"].to(dev)
+    out = torch.empty_like(v)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+
+    def one():
+        hla.ahla_forward(q, k, v, gamma=gamma, chunk=w.chunk, out=out)
+
+    ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
+    hla.ahla_forward(q, k, v, gamma=gamma, chunk=w.chunk, out=out, phase_events=ev)
+    torch.cuda.synchronize()
+    out_ms = ev[3].elapsed_time(ev[4])
+    tokens = w.B * w.H * w.n
+    nbytes = tokens * (2 * w.d + 2 * w.dv) * 2
+    # chunk products at width W, full (unmasked) counts per token:
+    # Q K^T 2 W d, A~ V and A~ Inner 4 W dv, Q P0, Q E0, K~^T V, K~^T Inner 8 d dv
+    flops = tokens * (2 * w.chunk * w.d + 4 * w.chunk * w.dv + 8 * w.d * w.dv)
+    achieved = nbytes / (out_ms * 1e-3) / 1e9
+    return {"workload": f"AHLA forward: B={w.B} H={w.H} n={w.n} d=dv={w.d} bf16, decay linspace(0.99,0.9999), "
+                        f"unnormalised, chunk {w.chunk}",
+            "metric": "AHLA fwd tokens/s", "unit": "tokens/s", "value": dist.world * tokens / (ms * 1e-3),
+            "ms_per_step": ms, "steps": steps, "output_pass_ms": out_ms,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "kernel": "output_pass", "algorithmic_bytes_per_launch": nbytes,
+                         "step_tensor_frac": flops / (ms * 1e-3) / 1e12 / bf16_tflops}}
+
+
 def run_only(args, dist: Dist, dev):
     hbm_gbs, bf16_tflops, _ = peaks()
     if args.only in ("decode", "decode_compact"):
         row = measure_decode(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs,
                              compact=args.only == "decode_compact")
+    elif args.only == "ahla":
+        row = measure_ahla(dev, dist, hbm_gbs, bf16_tflops, steps=args.steps, warmup=args.warmup, n=args.n)
     else:
         row = measure_train(dev, dist, bf16_tflops, hbm_gbs, steps=args.steps, warmup=args.warmup)
     if dist.rank == 0:
@@ -468,7 +513,8 @@ def run_ours(args, dist: Dist):
     if not args.no_secondary and args.n is None:
         secondary = {"decode": measure_decode(dev, dist, hbm_gbs),
                      "decode_compact": measure_decode(dev, dist, hbm_gbs, compact=True),
-                     "train": measure_train(dev, dist, bf16_tflops, hbm_gbs)}
+                     "train": measure_train(dev, dist, bf16_tflops, hbm_gbs),
+                     "ahla": measure_ahla(dev, dist, hbm_gbs, bf16_tflops)}
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
