@@ -353,8 +353,8 @@ def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: in
 def measure_ahla(dev, dist: Dist, hbm_gbs: float, bf16_tflops: float, steps: int = 50, warmup: int = 5,
                  n: int | None = None):
     """AHLA row: the asymmetric operator on the long-context shapes (B=1 H=16 n=65536
-    d=dv=64 bf16, decay linspace(0.99, 0.9999), unnormalised, chunk 64); 1,048,576 tokens
-    per step; inputs + output exceed the L2."""
+    d=dv=64 bf16, decay linspace(0.99, 0.9999), unnormalised, chunk 128); 1,048,576
+    tokens per step; inputs + output exceed the L2."""
     import dataclasses
 
     import torch
@@ -362,7 +362,7 @@ def measure_ahla(dev, dist: Dist, hbm_gbs: float, bf16_tflops: float, steps: int
     import chunked_scan_mixer_gb300 as hla
     from chunked_scan_mixer_gb300 import inputs
 
-    w = dataclasses.replace(inputs.WORKLOADS["long"], chunk=64)
+    w = inputs.WORKLOADS["long"]  # chunk 128: the tcgen05 kernel
     if n is not None:
         w = dataclasses.replace(w, n=n)
     x = inputs.make(w, device=dev, seed=replica_seed(w.seed, dist.rank))

@@ -755,15 +755,25 @@ static int ahla_check(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     int rc = check_common(B, H, n, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
     if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
-    if (dtype != HLA2_BF16 || d != dv || (chunk != 32 && chunk != 64))
-        return fail(HLA2_ERR_UNSUPPORTED, "the AHLA forward covers bf16, d == dv and chunk 32 or 64");
+    const bool tc = chunk == 128 && d == 64 && !normalize;
+    if (dtype != HLA2_BF16 || d != dv || (chunk != 32 && chunk != 64 && !tc))
+        return fail(HLA2_ERR_UNSUPPORTED,
+                    "the AHLA forward covers bf16, d == dv and chunk 32 or 64 (chunk 128: d = 64, unnormalised)");
+    if (tc && !ahla_tc_available()) return fail(HLA2_ERR_UNSUPPORTED, "tensor-map encoding is not available");
     return HLA2_OK;
 }
 
+// chunk 128 runs the tcgen05 kernel, chunks 32 and 64 the mma.sync one
 static Plan ahla_plan(int B, int H, int n, int d, int chunk) {
     const DevInfo di = dev_info();
-    return make_plan(B, H, n, d, d, chunk, di.sms,
-                     blocks_per_sm(ahla_chunk_smem(d, chunk), ahla_chunk_threads(d), 4, di));
+    const int per_sm = chunk == 128 ? blocks_per_sm(ahla_tc_smem(), 288, 2, di)
+                                    : blocks_per_sm(ahla_chunk_smem(d, chunk), ahla_chunk_threads(d), 4, di);
+    return make_plan(B, H, n, d, d, chunk, di.sms, per_sm);
+}
+
+static int ahla_pass(const AhlaArgs& a, int d, int chunk, bool summary, cudaStream_t st) {
+    if (chunk == 128) return launch_ahla_tc(a, summary, reinterpret_cast<int*>(a.ws), st);
+    return launch_ahla_chunk(a, d, chunk, summary, st);
 }
 
 size_t hla2_ahla_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
@@ -827,7 +837,7 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
         AhlaArgs b = a;
         b.seg0 = 0;
         b.nseg_launch = steps;
-        if (launch_ahla_chunk(b, d, chunk, true, st)) return cuda_fail("AHLA segment summaries");
+        if (ahla_pass(b, d, chunk, true, st)) return cuda_fail("AHLA segment summaries");
         mark(2);
         if (launch_linear_scan(a.ws + L.PB, a.ws + L.Pin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true, gamma,
                                seg_tokens, 1, st) ||
@@ -846,7 +856,7 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
     AhlaArgs o = a;
     o.seg0 = 0;
     o.nseg_launch = p.nseg;
-    if (launch_ahla_chunk(o, d, chunk, false, st)) return cuda_fail("AHLA output pass");
+    if (ahla_pass(o, d, chunk, false, st)) return cuda_fail("AHLA output pass");
     mark(4);
     mark(5);
     return succeed();

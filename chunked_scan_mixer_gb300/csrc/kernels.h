@@ -49,6 +49,10 @@ int launch_ahla_init(const AhlaArgs& a, int d, cudaStream_t st);
 int launch_ahla_cross(const AhlaArgs& a, int d, cudaStream_t st);
 size_t ahla_chunk_smem(int d, int W);
 int ahla_chunk_threads(int d);
+// tcgen05 AHLA chunk kernel (d = dv = 64, chunk 128, unnormalised; ahla_tc.cu)
+bool ahla_tc_available();
+size_t ahla_tc_smem();
+int launch_ahla_tc(const AhlaArgs& a, bool summary, int* status, cudaStream_t st);
 
 // Arguments of one chunk-kernel launch (summary or output pass of the forward).
 struct ChunkArgs {

@@ -185,8 +185,10 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
  * streamed with P_t = g P + k v^T, E_t = g E + k (q^T P_t), o_t = q_t^T E_t (and m, n for
  * the denominator with v -> 1; normalised output o / (den + eps)).  Chunk-parallel over an
  * exclusive scan of segment summaries (P, E, m, n, R = sum k q^T) (section summary §6.2).
- * bf16 q, k, v, out [B, H, n, d], d == dv in {16, 32, 64, 128}, chunk 32 or 64; no
- * init_state / final_state; opts->flags must be 0.  Workspace as for hla2_forward.
+ * bf16 q, k, v, out [B, H, n, d], d == dv in {16, 32, 64, 128}, chunk 32 or 64 (legacy
+ * tensor cores), or chunk 128 for d = dv = 64 unnormalised (tcgen05); no init_state /
+ * final_state; opts->flags must be 0.  Workspace as for hla2_forward; a timed-out
+ * device-side wait of the tcgen05 kernel is reported by hla2_workspace_status.
  */
 size_t hla2_ahla_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
                                          int normalize);

@@ -81,6 +81,47 @@ def test_rejects_uncovered_requests():
     x = inputs.make_custom(1, 1, 64, 64, 32, torch.bfloat16, seed=15)
     with pytest.raises(HLA2Error):  # d != dv
         hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), chunk=64)
-    x = inputs.make_custom(1, 1, 64, 64, 64, torch.bfloat16, seed=15)
-    with pytest.raises(HLA2Error):  # chunk 128 is not compiled for AHLA
+    x = inputs.make_custom(1, 1, 64, 32, 32, torch.bfloat16, seed=15)
+    with pytest.raises(HLA2Error):  # chunk 128 only for d = 64
         hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), chunk=128)
+
+
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 1000, 128 * 37 + 5])
+def test_tcgen05_path_lengths(n):
+    """chunk 128, d = dv = 64 runs the tcgen05 kernel."""
+    x = inputs.make_custom(1, 3, n, 64, 64, torch.bfloat16, seed=20 + n % 97, gamma=(0.97, 0.9999))
+    o = run(x, 128)
+    assert torch.isfinite(o.float()).all()
+    assert rel_err(np64(o), oracle(x)) <= 2e-2
+    hla.check_status()
+
+
+@pytest.mark.parametrize("gamma", [None, 0.9, (0.5, 0.999)])
+def test_tcgen05_path_decays_and_mma_agreement(gamma):
+    x = inputs.make_custom(2, 2, 1500, 64, 64, torch.bfloat16, seed=21, gamma=gamma)
+    a, b = np64(run(x, 128)), np64(run(x, 64))
+    ref = oracle(x)
+    assert rel_err(a, ref) <= 2e-2 and rel_err(b, ref) <= 2e-2
+
+
+def test_tcgen05_path_many_segments():
+    """Several chunks per segment and many segments per head (summaries, scan, carries)."""
+    x = inputs.make_custom(1, 16, 128 * 60 + 77, 64, 64, torch.bfloat16, seed=22, gamma=(0.98, 0.9999))
+    assert rel_err(np64(run(x, 128)), oracle(x)) <= 2e-2
+    hla.check_status()
+
+
+def test_tcgen05_path_long_context_and_causality():
+    x = inputs.make_custom(1, 2, 65536, 64, 64, torch.bfloat16, seed=23, gamma=(0.99, 0.9999))
+    a = run(x, 128)
+    assert rel_err(np64(a), oracle(x)) <= 2e-2
+    y = {key: (t.clone() if isinstance(t, torch.Tensor) else t) for key, t in x.items()}
+    for key in ("q", "k", "v"):
+        y[key][:, :, 40000:] = (y[key][:, :, 40000:].float() * -1.5).to(torch.bfloat16)
+    assert torch.equal(run(y, 128)[:, :, :40000], a[:, :, :40000])
+
+
+def test_tcgen05_path_rejects_normalized():
+    x = inputs.make_custom(1, 1, 64, 64, 64, torch.bfloat16, seed=24)
+    with pytest.raises(HLA2Error):
+        hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), chunk=128, normalize=True)
