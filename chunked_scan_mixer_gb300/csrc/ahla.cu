@@ -75,6 +75,9 @@ __global__ void __launch_bounds__(AhlaCfg<D, W>::NT) ahla_chunk_kernel(const Ahl
     const bf16* k = static_cast<const bf16*>(a.k) + (size_t)bh * a.n * D;
     const bf16* v = static_cast<const bf16*>(a.v) + (size_t)bh * a.n * DV;
     const bool norm = a.normalize != 0;
+    // the denominator's summaries m, n are carried when the output is normalised or the
+    // final state is asked for
+    const bool track = norm || a.final_state != nullptr;
 
     const float g = head_decay(a.gamma, bh, a.H);
     const float log2g = log2f(g);
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(AhlaCfg<D, W>::NT) ahla_chunk_kernel(const Ahl
             const int r = i / D, f = i % D;
             Kt[r * LD + f] = from_f32<bf16>((r < Wc ? gp[Wc - 1 - r] : 0.f) * to_f32(Ks[r * LD + f]));
         }
-        if (norm) {
+        if (track) {
             for (int r = tid; r < W; r += NT) {
                 float sm = 0.f, sn = 0.f;
                 for (int f = 0; f < D; ++f) {
@@ -183,7 +186,7 @@ __global__ void __launch_bounds__(AhlaCfg<D, W>::NT) ahla_chunk_kernel(const Ahl
         }
         __syncthreads();
         // tiles above the diagonal block row are never read: products stop at (rb + 1) * 16
-        if (norm) {  // idn = g^(r+1) q.m0 + row sums of A~
+        if (track) {  // idn = g^(r+1) q.m0 + row sums of A~
             for (int r = tid; r < W; r += NT) {
                 float s = 0.f;
                 for (int j = 0; j <= r; ++j) s += to_f32(AB[r * LW + j]);
@@ -274,7 +277,7 @@ __global__ void __launch_bounds__(AhlaCfg<D, W>::NT) ahla_chunk_kernel(const Ahl
             for (int r = 0; r < Wc; ++r) {
                 const float kf = to_f32(Kt[r * LD + f]);
                 sm += kf;
-                if (norm || SUMMARY) sn += kf * idn[r];
+                if (track) sn += kf * idn[r];
             }
             ms[f] = rho * ms[f] + sm;
             ns[f] = rho * ns[f] + sn;
@@ -285,6 +288,27 @@ __global__ void __launch_bounds__(AhlaCfg<D, W>::NT) ahla_chunk_kernel(const Ahl
     }
     __syncthreads();
 
+    if (!SUMMARY && a.final_state && seg == a.nseg - 1) {  // state after token n: P | E | m | n
+        float* fs = a.final_state + (size_t)bh * (2 * D * DV + 2 * D);
+#pragma unroll
+        for (int s = 0; s < Cfg::PER; ++s) {
+            const int t = warp + s * NW;
+            if (t >= Cfg::TILES) break;
+            const int m0 = (t / TD) * 16, n0 = (t % TD) * 16;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 4; i += 2) {
+                    const size_t e = (size_t)acc_row(m0, i) * DV + acc_col(n0, h, i);
+                    *reinterpret_cast<float2*>(&fs[e]) = make_float2(Pacc[s][h][i], Pacc[s][h][i + 1]);
+                    *reinterpret_cast<float2*>(&fs[D * DV + e]) = make_float2(Eacc[s][h][i], Eacc[s][h][i + 1]);
+                }
+        }
+        for (int f = tid; f < D; f += NT) {
+            fs[2 * D * DV + f] = ms[f];
+            fs[2 * D * DV + D + f] = ns[f];
+        }
+    }
     if (SUMMARY) {
         const size_t si = (size_t)bh * a.nsum + seg;
         float* dP = a.ws + a.L.PB + si * D * DV;
@@ -373,7 +397,7 @@ __global__ void __launch_bounds__(kScanThreads) ahla_cross_kernel(const AhlaArgs
     for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) E[(size_t)(tr + 16 * i) * D + tc0 + j] += rho * acc[i][j];
-    if (a.normalize) {
+    if (a.normalize || a.final_state) {
         float* nb = a.ws + a.L.nB + sb * D;
         for (int r = tid; r < D; r += kScanThreads) {
             float t = 0.f;

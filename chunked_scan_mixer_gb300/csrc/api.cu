@@ -751,6 +751,27 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
 
 size_t hla2_compact_state_floats(int d, int dv) { return compact_state_floats(d, dv); }
 
+size_t hla2_ahla_state_floats(int d, int dv) { return ahla_state_floats(d, dv); }
+
+int hla2_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H, int d,
+                          int dv, const float* gamma, int normalize, hla2_stream_t stream, const hla2_opts* opts) {
+    const int dtype = opts ? opts->dtype : HLA2_BF16;
+    const float eps = opts ? opts->eps : 1e-6f;
+    int rc = check_common(N, H, 0, d, dv, dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (normalize && !isfinite(eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
+    if (opts && opts->flags) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_ahla_decode_step");
+    if ((long)N * H == 0) return succeed();
+    if (!state || !q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "state, q, k, v, out must not be NULL");
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(HLA2_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    cudaGetLastError();
+    if (launch_ahla_decode_step(state, q, k, v, out, N, H, d, dv, gamma, normalize, eps, dtype == HLA2_BF16,
+                                reinterpret_cast<cudaStream_t>(stream)))
+        return cuda_fail("AHLA decode step");
+    return succeed();
+}
+
 static int ahla_check(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
     int rc = check_common(B, H, n, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
@@ -789,10 +810,20 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
     if (rc != HLA2_OK) return rc;
     if (normalize && !isfinite(opts->eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
     if (opts->flags) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_ahla_forward");
-    if (opts->init_state || opts->final_state)
-        return fail(HLA2_ERR_UNSUPPORTED, "the AHLA forward takes no init_state / final_state");
+    if (opts->init_state) return fail(HLA2_ERR_UNSUPPORTED, "the AHLA forward takes no init_state");
+    const bool want_final = opts->final_state != nullptr;
+    if (want_final && chunk == 128)
+        return fail(HLA2_ERR_UNSUPPORTED, "the AHLA final state comes from the chunk 32 / 64 kernels");
+    if (want_final && !aligned16(opts->final_state))
+        return fail(HLA2_ERR_INVALID_ARG, "final_state must be 16-byte aligned");
     const long BH = (long)B * H;
-    if (BH == 0 || n == 0) return succeed();
+    if (BH == 0) return succeed();
+    if (n == 0) {  // no tokens: the empty state
+        if (want_final && cudaMemsetAsync(opts->final_state, 0, BH * ahla_state_floats(d, dv) * sizeof(float),
+                                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return cuda_fail("final state");
+        return succeed();
+    }
     if (!q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must not be NULL");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
@@ -822,6 +853,8 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
     a.eps = opts->eps;
     a.ws = static_cast<float*>(opts->workspace);
     a.L = L;
+    a.final_state = opts->final_state;
+    const bool den_terms = normalize || want_final;  // m, n carried
     auto mark = [&](int i) {
         if (opts->phase_events && i < opts->n_phase_events && opts->phase_events[i] &&
             cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[i]), st) != cudaSuccess)
@@ -841,12 +874,12 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
         mark(2);
         if (launch_linear_scan(a.ws + L.PB, a.ws + L.Pin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true, gamma,
                                seg_tokens, 1, st) ||
-            (normalize && launch_linear_scan(a.ws + L.mB, a.ws + L.min, a.BH, H, steps, d, a.nsum * (size_t)d,
+            (den_terms && launch_linear_scan(a.ws + L.mB, a.ws + L.min, a.BH, H, steps, d, a.nsum * (size_t)d,
                                              p.nseg * (size_t)d, true, gamma, seg_tokens, 1, st)) ||
             launch_ahla_cross(a, d, st) ||
             launch_linear_scan(a.ws + L.EB, a.ws + L.Ein, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true, gamma,
                                seg_tokens, 1, st) ||
-            (normalize && launch_linear_scan(a.ws + L.nB, a.ws + L.nin, a.BH, H, steps, d, a.nsum * (size_t)d,
+            (den_terms && launch_linear_scan(a.ws + L.nB, a.ws + L.nin, a.BH, H, steps, d, a.nsum * (size_t)d,
                                              p.nseg * (size_t)d, true, gamma, seg_tokens, 1, st)))
             return cuda_fail("AHLA segment scan");
     } else {

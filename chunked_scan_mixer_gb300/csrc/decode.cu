@@ -245,6 +245,105 @@ __global__ void __launch_bounds__(kThreads)
         out[(size_t)head * dv + e] = from_f32<T>((ws[e] - zs[e]) * inv);
 }
 
+// AHLA decode step (technical summary item "2. ... (AHLA)": streaming summaries P^KV, m^K,
+// E, n; section summary §6.1), one CTA per head, state [P d*dv | E d*dv | m d | n d]:
+//   pass P:  P' = g P + k v^T,            inner = P'^T q
+//   pass E:  E' = g E + k inner^T,        o = E'^T q
+//   m' = g m + k,  n' = g n + k (q . m'),  den = q . n'
+// Each matrix is read and written once with 128-bit accesses.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    ahla_decode_kernel(float* __restrict__ state, const T* __restrict__ q, const T* __restrict__ k,
+                       const T* __restrict__ v, T* __restrict__ out, int H, int d, int dv,
+                       const float* __restrict__ gamma, int normalize, float eps) {
+    __shared__ __align__(16) float qs[kMaxDim], ks[kMaxDim], vs[kMaxDim], is[kMaxDim], os[kMaxDim];
+    __shared__ __align__(16) float red[kWarps * kMaxDim];
+    const int head = blockIdx.x, tid = threadIdx.x;
+    const float g = head_decay(gamma, head, H);
+    float* P = state + (size_t)head * (2 * (size_t)d * dv + 2 * (size_t)d);
+    float* E = P + (size_t)d * dv;
+    float* m = E + (size_t)d * dv;
+    float* nn = m + d;
+    for (int i = tid; i < d; i += kThreads) {
+        qs[i] = to_f32(q[(size_t)head * d + i]);
+        ks[i] = to_f32(k[(size_t)head * d + i]);
+    }
+    for (int i = tid; i < dv; i += kThreads) vs[i] = to_f32(v[(size_t)head * dv + i]);
+    __syncthreads();
+
+    const int lpc = dv / 4, rows_per = kThreads / lpc, c4 = (tid % lpc) * 4;
+    // pass P: P' = g P + k v^T and inner = P'^T q
+    {
+        float4 pi = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int a0 = tid / lpc; a0 < d; a0 += rows_per * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a < d) x[u] = ld_stream(P + (size_t)a * dv + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a >= d) continue;
+                const float ka = ks[a], qa = qs[a];
+                float4 y = x[u];
+                y.x = g * y.x + ka * vs[c4 + 0];
+                y.y = g * y.y + ka * vs[c4 + 1];
+                y.z = g * y.z + ka * vs[c4 + 2];
+                y.w = g * y.w + ka * vs[c4 + 3];
+                pi.x += qa * y.x; pi.y += qa * y.y; pi.z += qa * y.z; pi.w += qa * y.w;
+                st_stream(P + (size_t)a * dv + c4, y);
+            }
+        }
+        column_reduce(pi, dv, red, is);
+    }
+    // pass E: E' = g E + k inner^T and o = E'^T q
+    {
+        float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 i4 = *reinterpret_cast<const float4*>(&is[c4]);
+        for (int a0 = tid / lpc; a0 < d; a0 += rows_per * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a < d) x[u] = ld_stream(E + (size_t)a * dv + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a >= d) continue;
+                const float ka = ks[a], qa = qs[a];
+                float4 y = x[u];
+                y.x = g * y.x + ka * i4.x;
+                y.y = g * y.y + ka * i4.y;
+                y.z = g * y.z + ka * i4.z;
+                y.w = g * y.w + ka * i4.w;
+                po.x += qa * y.x; po.y += qa * y.y; po.z += qa * y.z; po.w += qa * y.w;
+                st_stream(E + (size_t)a * dv + c4, y);
+            }
+        }
+        column_reduce(po, dv, red, os);
+    }
+    // m' = g m + k;  n' = g n + k (q . m');  den = q . n'
+    float qm = 0.f;
+    for (int i = tid; i < d; i += kThreads) {
+        const float mn = g * m[i] + ks[i];
+        m[i] = mn;
+        qm += qs[i] * mn;
+    }
+    qm = block_sum(qm, red);
+    float qn = 0.f;
+    for (int i = tid; i < d; i += kThreads) {
+        const float nv = g * nn[i] + ks[i] * qm;
+        nn[i] = nv;
+        qn += qs[i] * nv;
+    }
+    float inv = 1.f;
+    if (normalize) inv = 1.f / (block_sum(qn, red) + eps);
+    for (int e = tid; e < dv; e += kThreads) out[(size_t)head * dv + e] = from_f32<T>(os[e] * inv);
+}
+
 // Packed [S d*d | C | G | m | h] -> compact (upper block triangle of S), one CTA per head.
 __global__ void __launch_bounds__(kThreads) state_to_compact_kernel(const float* __restrict__ full,
                                                                    float* __restrict__ compact, int d, int dv) {
@@ -300,6 +399,22 @@ int launch_decode_step(float* state, const void* q, const void* k, const void* v
         launch_decode_t<true>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
     else
         launch_decode_t<false>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
+                            int d, int dv, const float* gamma, int normalize, float eps, bool is_bf16,
+                            cudaStream_t st) {
+    const long heads = (long)N * H;
+    if (heads <= 0) return 0;
+    if (is_bf16)
+        ahla_decode_kernel<bf16><<<(unsigned)heads, kThreads, 0, st>>>(
+            state, static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
+            static_cast<bf16*>(out), H, d, dv, gamma, normalize, eps);
+    else
+        ahla_decode_kernel<float><<<(unsigned)heads, kThreads, 0, st>>>(
+            state, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+            static_cast<float*>(out), H, d, dv, gamma, normalize, eps);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

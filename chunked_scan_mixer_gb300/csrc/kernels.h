@@ -31,6 +31,9 @@ inline AhlaLayout ahla_layout(const Plan& p) {
     return L;
 }
 
+// AHLA streaming state of one head: P d*dv | E d*dv | m d | n d.
+inline size_t ahla_state_floats(int d, int dv) { return 2 * (size_t)d * dv + 2 * (size_t)d; }
+
 // Arguments of one AHLA chunk-kernel launch.
 struct AhlaArgs {
     const void* q;
@@ -43,6 +46,7 @@ struct AhlaArgs {
     float eps;
     float* ws;
     AhlaLayout L;
+    float* final_state;  // nullable: [BH][2 d dv + 2 d] = P | E | m | n after token n
 };
 int launch_ahla_chunk(const AhlaArgs& a, int d, int W, bool summary, cudaStream_t st);
 int launch_ahla_init(const AhlaArgs& a, int d, cudaStream_t st);
@@ -144,6 +148,9 @@ int launch_finalize(const ChunkArgs& a, int d, int dv, float* final_state, cudaS
 int launch_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
                        int N, int H, int d, int dv, const float* gamma, int normalize, float eps,
                        bool is_bf16, bool compact, cudaStream_t st);
+int launch_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
+                            int d, int dv, const float* gamma, int normalize, float eps, bool is_bf16,
+                            cudaStream_t st);
 int launch_state_compact(const float* src, float* dst, long heads, int d, int dv, bool to_compact, cudaStream_t st);
 
 }  // namespace hla2

@@ -101,6 +101,10 @@ def lib():
         L.hla2_ahla_forward_workspace_bytes.restype = Z
         L.hla2_ahla_forward.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
         L.hla2_ahla_forward.restype = I
+        L.hla2_ahla_state_floats.argtypes = [I, I]
+        L.hla2_ahla_state_floats.restype = Z
+        L.hla2_ahla_decode_step.argtypes = [P, P, P, P, P, I, I, I, I, P, I, P, ctypes.POINTER(Opts)]
+        L.hla2_ahla_decode_step.restype = I
         L.hla2_compact_state_floats.argtypes = [I, I]
         L.hla2_compact_state_floats.restype = Z
         for name in ("hla2_state_to_compact", "hla2_state_from_compact"):
@@ -115,6 +119,7 @@ EXPORTED_SYMBOLS = (
     "hla2_forward", "hla2_forward_plan", "hla2_workspace_status", "hla2_backward_workspace_bytes",
     "hla2_backward", "hla2_decode_step", "hla2_forward_noalloc", "hla2_compact_state_floats",
     "hla2_state_to_compact", "hla2_state_from_compact", "hla2_ahla_forward_workspace_bytes", "hla2_ahla_forward",
+    "hla2_ahla_state_floats", "hla2_ahla_decode_step",
 )
 
 FLAG_COMPACT_STATE = 4
@@ -283,9 +288,16 @@ def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state
     return (o, fin) if return_final_state else o
 
 
-def ahla_forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, out=None, phase_events=None):
+def ahla_state_floats(d, dv):
+    return int(lib().hla2_ahla_state_floats(d, dv))
+
+
+def ahla_forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, out=None, phase_events=None,
+                 return_final_state=False):
     """Asymmetric HLA forward (the masked left-cascaded product Q (K^T Q)(K^T V)).
-    bf16 q, k, v [B,H,n,d] on the GPU (d == dv); chunk 32 or 64.  Returns out [B,H,n,d]."""
+    bf16 q, k, v [B,H,n,d] on the GPU (d == dv); chunk 32 or 64 (or 128 at d = 64,
+    unnormalised).  Returns out [B,H,n,d] (and, with return_final_state, the state
+    [B,H,ahla_state_floats] = P | E | m | n after the last token; chunk 32 / 64)."""
     L = lib()
     if q.device.type != "cuda" or q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must be bfloat16 CUDA tensors")
@@ -300,8 +312,10 @@ def ahla_forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, out=N
     if nbytes == ctypes.c_size_t(-1).value:
         nbytes = 0
     ws = _workspace(int(nbytes), device, sh)
-    opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), int(nbytes), None, None,
-                None, 0, 0)
+    fin = torch.empty((B, H, ahla_state_floats(d, dv)), dtype=torch.float32, device=device) \
+        if return_final_state else None
+    opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), int(nbytes), None,
+                None if fin is None else fin.data_ptr(), None, 0, 0)
     if phase_events:
         for e in phase_events:
             if not e.cuda_event:
@@ -311,6 +325,25 @@ def ahla_forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, out=N
         opts.n_phase_events = len(phase_events)
     _check("hla2_ahla_forward", L.hla2_ahla_forward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), B, H, n, d, dv, _ptr(g),
                                                     int(normalize), chunk, sh, ctypes.byref(opts)))
+    return (o, fin) if return_final_state else o
+
+
+def ahla_decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6, out=None):
+    """One AHLA step; ``state`` [N,H,ahla_state_floats] float32 on the GPU is updated in
+    place.  q, k [N,H,d]; v [N,H,dv].  Returns out [N,H,dv]."""
+    L = lib()
+    if state.device.type != "cuda" or state.dtype != torch.float32 or not state.is_contiguous():
+        raise ValueError("state must be a contiguous float32 CUDA tensor")
+    device = state.device
+    N, H, d = q.shape
+    dv = v.shape[-1]
+    qd, kd, vd = (_to_device(t, device) for t in (q, k, v))
+    g = _gamma_tensor(gamma, H, device)
+    o = out if out is not None else torch.empty((N, H, dv), dtype=q.dtype, device=device)
+    opts = Opts(_DTYPES[q.dtype], float(eps), None, 0, None, None, None, 0, 0)
+    _check("hla2_ahla_decode_step", L.hla2_ahla_decode_step(_ptr(state), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), N, H,
+                                                            d, dv, _ptr(g), int(normalize), _stream_handle(device),
+                                                            ctypes.byref(opts)))
     return o
 
 

@@ -186,15 +186,30 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
  * the denominator with v -> 1; normalised output o / (den + eps)).  Chunk-parallel over an
  * exclusive scan of segment summaries (P, E, m, n, R = sum k q^T) (section summary §6.2).
  * bf16 q, k, v, out [B, H, n, d], d == dv in {16, 32, 64, 128}, chunk 32 or 64 (legacy
- * tensor cores), or chunk 128 for d = dv = 64 unnormalised (tcgen05); no init_state /
- * final_state; opts->flags must be 0.  Workspace as for hla2_forward; a timed-out
- * device-side wait of the tcgen05 kernel is reported by hla2_workspace_status.
+ * tensor cores), or chunk 128 for d = dv = 64 unnormalised (tcgen05); no init_state;
+ * opts->final_state (chunk 32 / 64 only) receives the AHLA state after token n, [B, H]
+ * blocks of hla2_ahla_state_floats = [P d*dv | E d*dv | m d | n d]; opts->flags must be 0.
+ * Workspace as for hla2_forward; a timed-out device-side wait of the tcgen05 kernel is
+ * reported by hla2_workspace_status.
  */
 size_t hla2_ahla_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
                                          int normalize);
 int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
                       int d, int dv, const float* gamma, int normalize, int chunk,
                       hla2_stream_t stream, const hla2_opts* opts);
+
+/* Floats in one head's AHLA state: 2*d*dv + 2*d. */
+size_t hla2_ahla_state_floats(int d, int dv);
+
+/*
+ * One AHLA streaming step for N*H heads (section summary §6.1: O(d dv) per token):
+ * state [N, H] blocks [P | E | m | n] float32 updated in place; q, k [N, H, d]; v, out
+ * [N, H, dv].  P, m are advanced first, the inner read q^T P uses the updated P, then E, n,
+ * and the output q^T E reads the updated E.  opts may be NULL (dtype HLA2_BF16, eps 1e-6).
+ */
+int hla2_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
+                          int N, int H, int d, int dv, const float* gamma, int normalize,
+                          hla2_stream_t stream, const hla2_opts* opts);
 
 /*
  * Compact decode state.  S is symmetric (a sum of decayed k k^T), so a head's state can

@@ -125,3 +125,61 @@ def test_tcgen05_path_rejects_normalized():
     x = inputs.make_custom(1, 1, 64, 64, 64, torch.bfloat16, seed=24)
     with pytest.raises(HLA2Error):
         hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), chunk=128, normalize=True)
+
+
+def _oracle_state_flat(st):
+    B, H = st["P"].shape[:2]
+    return np.concatenate([st["P"].reshape(B, H, -1), st["E"].reshape(B, H, -1), st["m"], st["n"]], axis=-1)
+
+
+@pytest.mark.parametrize("chunk", [32, 64])
+def test_final_state_matches_oracle(chunk):
+    """The state after the last token (P | E | m | n) equals the oracle's serial state."""
+    x = inputs.make_custom(2, 3, 777, 64, 64, torch.bfloat16, seed=30 + chunk, gamma=(0.95, 0.999))
+    g = x["gamma"].cuda()
+    o, fin = hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), gamma=g, chunk=chunk,
+                              return_final_state=True)
+    ref_o, st = A.serial_forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), x["gamma"].double().numpy(),
+                                 return_state=True)
+    assert rel_err(np64(o.cpu()), ref_o) <= 2e-2
+    ref = _oracle_state_flat(st)
+    got = fin.cpu().double().numpy()
+    d = 64
+    for lo, hi in ((0, d * d), (d * d, 2 * d * d), (2 * d * d, 2 * d * d + d), (2 * d * d + d, 2 * d * d + 2 * d)):
+        assert rel_err(got[..., lo:hi], ref[..., lo:hi]) <= 2e-2
+
+
+@pytest.mark.parametrize("d, dv", [(16, 16), (64, 64), (128, 128), (32, 64)])
+@pytest.mark.parametrize("normalize", [False, True])
+def test_decode_from_zero_equals_forward(d, dv, normalize):
+    """fp32 decode steps from the empty state reproduce the serial AHLA outputs."""
+    N, H, n = 2, 3, 23
+    x = inputs.make_custom(N, H, n, d, dv, torch.float32, seed=d + dv, qk="softplus" if normalize else "gauss",
+                           gamma=(0.9, 0.99))
+    state = torch.zeros((N, H, hla.ahla_state_floats(d, dv)), device="cuda")
+    outs = [hla.ahla_decode_step(state, x["q"][:, :, t].cuda(), x["k"][:, :, t].cuda(), x["v"][:, :, t].cuda(),
+                                 gamma=x["gamma"].cuda(), normalize=normalize, eps=1e-6) for t in range(n)]
+    o = torch.stack(outs, dim=2).cpu()
+    ref, st = A.serial_forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), x["gamma"].double().numpy(),
+                               normalize=normalize, eps=1e-6, return_state=True)
+    assert rel_err(np64(o), ref) <= 1e-4
+    assert rel_err(state.cpu().double().numpy(), _oracle_state_flat(st)) <= 1e-5
+
+
+def test_prefill_then_decode_matches_uninterrupted_oracle():
+    """A GPU prefill's final state continues like the oracle run over prefill + decode tokens."""
+    N, H, d, n, extra = 2, 4, 64, 500, 6
+    x = inputs.make_custom(N, H, n + extra, d, d, torch.bfloat16, seed=31, gamma=0.995)
+    g = x["gamma"].cuda()
+    _, fin = hla.ahla_forward(x["q"][:, :, :n].contiguous().cuda(), x["k"][:, :, :n].contiguous().cuda(),
+                              x["v"][:, :, :n].contiguous().cuda(), gamma=g, chunk=64, return_final_state=True)
+    ref = A.serial_forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), x["gamma"].double().numpy())
+    for t in range(n, n + extra):
+        o = hla.ahla_decode_step(fin, x["q"][:, :, t].cuda(), x["k"][:, :, t].cuda(), x["v"][:, :, t].cuda(), gamma=g)
+        assert rel_err(np64(o.cpu()), ref[:, :, t]) <= 2e-2, t
+
+
+def test_final_state_with_chunk_128_is_rejected():
+    x = inputs.make_custom(1, 1, 64, 64, 64, torch.bfloat16, seed=32)
+    with pytest.raises(HLA2Error):
+        hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), chunk=128, return_final_state=True)
