@@ -224,6 +224,63 @@ def _to_device(t, device):
     return t.contiguous().to(device, non_blocking=True)
 
 
+_side_streams: dict = {}
+
+
+def _pipelined_host_forward(q, k, v, gamma, normalize, chunk, eps, out):
+    """forward() on host tensors, overlapping the copies with the computation: the heads are
+    independent, so they go through in groups -- the inputs of group i+1 are copied in on one
+    stream while group i is computed on the current stream and group i-1's output is copied
+    out on a third (two device buffers per group slot).  Returns None when the heads cannot
+    be cut into at least two groups."""
+    B, H, n, d = q.shape
+    dv = v.shape[-1]
+    # heads per group: a divisor of H giving about eight groups (the copies then bound the
+    # call to within a group's compute and output copy of the link time), at least two
+    divisors = [c for c in range(H, 0, -1) if H % c == 0]
+    gh = next((c for c in divisors if B * H // c >= 8), next((c for c in divisors if B * H // c >= 2), 0))
+    if gh == 0 or not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        return None
+    device = torch.device("cuda", torch.cuda.current_device())
+    key = device.index
+    if key not in _side_streams:
+        _side_streams[key] = (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+    s_in, s_out = _side_streams[key]
+    cur = torch.cuda.current_stream(device)
+    g = _gamma_tensor(gamma, H, device)
+    res = out if out is not None else torch.empty((B, H, n, dv), dtype=q.dtype, pin_memory=True)
+    qf, kf, vf, rf = (t.view(B * H, n, t.shape[-1]) for t in (q, k, v, res))
+    stage = [[torch.empty((gh, n, x), dtype=q.dtype, device=device) for x in (d, d, dv, dv)] for _ in range(2)]
+    ev_in, ev_comp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+    s_in.wait_stream(cur)
+    s_out.wait_stream(cur)
+    for i, r0 in enumerate(range(0, B * H, gh)):
+        slot, r1, h0 = i % 2, r0 + gh, r0 % H
+        qd, kd, vd, od = stage[slot]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_comp[slot])  # group i-2 has read its inputs
+            qd.copy_(qf[r0:r1], non_blocking=True)
+            kd.copy_(kf[r0:r1], non_blocking=True)
+            vd.copy_(vf[r0:r1], non_blocking=True)
+            ev_in[slot].record(s_in)
+        cur.wait_event(ev_in[slot])
+        if i >= 2:
+            cur.wait_event(ev_out[slot])  # group i-2's output has left this slot
+        forward(qd.view(1, gh, n, d), kd.view(1, gh, n, d), vd.view(1, gh, n, dv),
+                gamma=None if g is None else g[h0:h0 + gh], normalize=normalize, chunk=chunk, eps=eps,
+                out=od.view(1, gh, n, dv))
+        ev_comp[slot].record(cur)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[slot])
+            rf[r0:r1].copy_(od, non_blocking=True)
+            ev_out[slot].record(s_out)
+    cur.wait_stream(s_in)
+    cur.wait_stream(s_out)
+    cur.synchronize()
+    return res
+
+
 def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state=None,
             return_final_state=False, out=None, phase_events=None, save_for_backward=False):
     """Masked HLA-2 forward.  q, k [B,H,n,d]; v [B,H,n,dv] (float32 or bfloat16).
@@ -239,6 +296,11 @@ def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state
     L = lib()
     if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must all be float32 or all bfloat16")
+    if (host and init_state is None and not return_final_state and phase_events is None and not save_for_backward
+            and k.device.type == "cpu" and v.device.type == "cpu" and (out is None or out.device.type == "cpu")):
+        res = _pipelined_host_forward(q, k, v, gamma, normalize, chunk, eps, out)
+        if res is not None:
+            return res
     B, H, n, d = q.shape
     dv = v.shape[-1]
     if k.shape != q.shape or v.shape[:3] != q.shape[:3]:

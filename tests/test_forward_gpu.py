@@ -180,6 +180,23 @@ def test_host_tensors_round_trip():
     assert rel_err(np64(o), oracle(x)) <= 2e-2
 
 
+@pytest.mark.parametrize("B,H,chunk", [(2, 8, 64), (1, 16, 128), (3, 4, 32)])
+def test_host_tensors_pipelined_by_head_groups(B, H, chunk):
+    """Host tensors go through in head groups (copies overlapped with the computation):
+    the result matches the oracle and the all-device call, with and without an out buffer."""
+    x = inputs.make_custom(B, H, 700, 64, 64, torch.bfloat16, seed=23 + H, gamma=(0.95, 0.999))
+    ref = oracle(x)
+    o = hla.forward(x["q"].pin_memory(), x["k"].pin_memory(), x["v"].pin_memory(), gamma=x["gamma"].cuda(),
+                    chunk=chunk)
+    assert o.device.type == "cpu" and rel_err(np64(o), ref) <= 2e-2
+    buf = torch.empty_like(x["v"]).pin_memory()
+    o2 = hla.forward(x["q"].pin_memory(), x["k"].pin_memory(), x["v"].pin_memory(), gamma=x["gamma"].cuda(),
+                     chunk=chunk, out=buf)
+    assert o2.data_ptr() == buf.data_ptr() and torch.equal(o2, o)
+    dev = run_gpu(x, chunk=chunk).cpu()
+    assert rel_err(np64(o), np64(dev)) <= 2e-2
+
+
 def test_workspace_too_small_is_reported():
     import ctypes
     x = inputs.make_custom(1, 1, 64, 16, 16, torch.bfloat16, seed=20)
