@@ -38,9 +38,9 @@ def _load():
         I = ctypes.c_int
         D = ctypes.c_double
         lib.hla2_oracle_threads.restype = I
-        lib.hla2_oracle_forward.argtypes = [P, P, P, P, L, L, L, I, I, P, I, D, P, P]
+        lib.hla2_oracle_forward.argtypes = [P, P, P, P, L, L, L, I, I, P, I, D, P, P, I]
         lib.hla2_oracle_forward.restype = I
-        lib.hla2_oracle_decode.argtypes = [P, P, P, P, P, L, L, I, I, P, I, D]
+        lib.hla2_oracle_decode.argtypes = [P, P, P, P, P, L, L, I, I, P, I, D, I]
         lib.hla2_oracle_decode.restype = I
         lib.hla2_oracle_backward.argtypes = [P, P, P, P, P, P, P, L, L, L, I, I, P]
         lib.hla2_oracle_backward.restype = I
@@ -65,7 +65,7 @@ def threads() -> int:
 
 
 def forward(q, k, v, gamma=None, normalize=False, eps=1e-6, init_state=None,
-            return_state=False):
+            return_state=False, masked=True):
     """Serial float64 forward.  q, k [B,H,n,d]; v [B,H,n,dv]; init_state packed
     [B,H,d*d+2*d*dv+2*d] (decode layout) or None.  Returns out [B,H,n,dv] float64
     (and the packed final state when ``return_state``)."""
@@ -79,13 +79,13 @@ def forward(q, k, v, gamma=None, normalize=False, eps=1e-6, init_state=None,
     fin = np.empty((B, H, sf), dtype=np.float64) if return_state else None
     rc = _load().hla2_oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B * H, H, n, d, dv,
                                      _ptr(g), int(bool(normalize)), float(eps), _ptr(init),
-                                     _ptr(fin))
+                                     _ptr(fin), int(bool(masked)))
     if rc != 0:
         raise RuntimeError(f"hla2_oracle_forward failed ({rc})")
     return (out, fin) if return_state else out
 
 
-def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6):
+def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6, masked=True):
     """One serial step on packed states [N,H,sf] float64 (modified in place).
     q, k [N,H,d]; v [N,H,dv].  Returns out [N,H,dv] float64."""
     assert state.dtype == np.float64 and state.flags.c_contiguous
@@ -95,7 +95,8 @@ def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6):
     out = np.empty((N, H, dv), dtype=np.float64)
     g = None if gamma is None else _f64(gamma).reshape(H)
     rc = _load().hla2_oracle_decode(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(out), N * H, H,
-                                    d, dv, _ptr(g), int(bool(normalize)), float(eps))
+                                    d, dv, _ptr(g), int(bool(normalize)), float(eps),
+                                    int(bool(masked)))
     if rc != 0:
         raise RuntimeError(f"hla2_oracle_decode failed ({rc})")
     return out

@@ -14,6 +14,9 @@
  *   m_t = g m_{t-1} + q_t                           (query mass)
  *   o_t = q_t^T (S_t C_t - G_t)  = (q_t^T S_t) C_t - q_t^T G_t
  *   den_t = q_t^T (S_t m_t - h_t);  normalised output o_t / (den_t + eps)
+ * With masked = 0 the output is the unmasked product q_t^T S_t C_t (and the denominator
+ * q_t^T S_t m_t): the "numerator-style bilinear form" of section summary §3, whose scan
+ * is the unmasked monoid of §4.1.  The state evolves the same way in both cases.
  * The gradient routine is the reverse sweep of exactly this recurrence (section
  * summary §4.2: the reverse-mode scan must reproduce these gradients), with states
  * recomputed from checkpoints every `ck` tokens.
@@ -64,7 +67,7 @@ static void hs_free(head_state* st) { free(st->S); }
 
 /* One online update then the output (see file header). */
 static void hs_step(head_state* st, const float* q, const float* k, const float* v,
-                    double g, int normalize, double eps, double* o) {
+                    double g, int normalize, double eps, int masked, double* o) {
     const int d = st->d, dv = st->dv;
     double *S = st->S, *C = st->C, *G = st->G, *m = st->m, *h = st->h;
     double *kC = st->kC, *u = st->u;
@@ -96,17 +99,18 @@ static void hs_step(head_state* st, const float* q, const float* k, const float*
         const double* Sa = S + (long)a * d;
         for (int c = 0; c < d; ++c) u[c] += qa * Sa[c];
     }
-    /* o = u C_t - q^T G_t */
+    /* o = u C_t - q^T G_t (unmasked: u C_t) */
+    const double mk = masked ? 1.0 : 0.0;
     for (int e = 0; e < dv; ++e) o[e] = 0.0;
     for (int a = 0; a < d; ++a) {
-        const double ua = u[a], qa = q[a];
+        const double ua = u[a], qa = mk * q[a];
         const double* Ca = C + (long)a * dv;
         const double* Ga = G + (long)a * dv;
         for (int e = 0; e < dv; ++e) o[e] += ua * Ca[e] - qa * Ga[e];
     }
     if (normalize) {
         double den = 0.0;
-        for (int a = 0; a < d; ++a) den += u[a] * m[a] - (double)q[a] * h[a];
+        for (int a = 0; a < d; ++a) den += u[a] * m[a] - mk * (double)q[a] * h[a];
         const double inv = 1.0 / (den + eps);
         for (int e = 0; e < dv; ++e) o[e] *= inv;
     }
@@ -119,7 +123,7 @@ static double head_gamma(const double* gamma, long bh, long H) {
 int hla2_oracle_forward(const float* q, const float* k, const float* v, double* out,
                         long BH, long H, long n, int d, int dv, const double* gamma,
                         int normalize, double eps, const double* init_state,
-                        double* final_state) {
+                        double* final_state, int masked) {
     if (BH < 0 || n < 0 || d <= 0 || dv <= 0 || H <= 0) return -1;
     const long sf = state_floats(d, dv);
     int err = 0;
@@ -135,7 +139,7 @@ int hla2_oracle_forward(const float* q, const float* k, const float* v, double* 
         const double g = head_gamma(gamma, bh, H);
         for (long t = 0; t < n; ++t) {
             const long row = bh * n + t;
-            hs_step(&st, q + row * d, k + row * d, v + row * dv, g, normalize, eps,
+            hs_step(&st, q + row * d, k + row * d, v + row * dv, g, normalize, eps, masked,
                     out + row * dv);
         }
         if (final_state) memcpy(final_state + bh * sf, st.S, (size_t)sf * sizeof(double));
@@ -147,7 +151,7 @@ int hla2_oracle_forward(const float* q, const float* k, const float* v, double* 
 /* One decode step for NH independent heads, state in place. */
 int hla2_oracle_decode(double* state, const float* q, const float* k, const float* v,
                        double* out, long NH, long H, int d, int dv, const double* gamma,
-                       int normalize, double eps) {
+                       int normalize, double eps, int masked) {
     if (NH < 0 || d <= 0 || dv <= 0 || H <= 0) return -1;
     const long sf = state_floats(d, dv);
     int err = 0;
@@ -161,7 +165,7 @@ int hla2_oracle_decode(double* state, const float* q, const float* k, const floa
         }
         memcpy(st.S, state + nh * sf, (size_t)sf * sizeof(double));
         hs_step(&st, q + nh * d, k + nh * d, v + nh * dv, head_gamma(gamma, nh, H),
-                normalize, eps, out + nh * dv);
+                normalize, eps, masked, out + nh * dv);
         memcpy(state + nh * sf, st.S, (size_t)sf * sizeof(double));
         hs_free(&st);
     }

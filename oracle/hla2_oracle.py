@@ -38,6 +38,11 @@ Readings where the pages leave a step open (each is pinned by a test in
   R3  No feature map: C = sum q v^T with the raw query ([TS]).
   R4  Denominator den_t = q_t^T (S_t m_t - h_t); normalised output o_t / (den_t + eps).
   R5  Row-vector convention: o_t has dv entries ([PS] §2).
+  R6  Unmasked variant ([PS] §3, the "numerator-style bilinear form"; [PS] §4.1): the
+      output is the naive product o_t = q_t^T S_t C_t (every pair i, j <= t, weight
+      g^((t-i) + (t-j))), normalised by q_t^T S_t m_t.  Its scan carries only (S, C, m)
+      and combines them by decayed addition, with no cross term (the unmasked monoid).
+      The state's G and h play no part in it; the unmasked chunked scan reports them as 0.
 
 Array conventions: q, k [B, H, n, d]; v, dout [B, H, n, dv]; gamma [H] (None means 1).
 State dict per head: S [B,H,d,d], C [B,H,d,dv], m [B,H,d], G [B,H,d,dv], h [B,H,d].
@@ -56,6 +61,9 @@ __all__ = [
     "combine",
     "blelloch_exclusive_scan",
     "chunked_scan_forward",
+    "unmasked_delta",
+    "unmasked_identity",
+    "combine_unmasked",
     "serial_backward",
     "serial_backward_normalized",
     "pairsum_grads",
@@ -89,8 +97,9 @@ def zero_state(B, H, d, dv):
     }
 
 
-def step(state, q_t, k_t, v_t, g, normalize=False, eps=1e-6):
-    """One online update followed by the masked output ([TS], [PS] §3.1; readings R1-R4).
+def step(state, q_t, k_t, v_t, g, normalize=False, eps=1e-6, masked=True):
+    """One online update followed by the masked output ([TS], [PS] §3.1; readings R1-R4),
+    or with ``masked=False`` the unmasked one, q^T S C (reading R6).
 
     q_t, k_t [B,H,d]; v_t [B,H,dv]; g [H].  Returns (new_state, o_t) with o_t [B,H,dv].
     The state is updated in the order the definitions require: G and h first (they
@@ -108,16 +117,21 @@ def step(state, q_t, k_t, v_t, g, normalize=False, eps=1e-6):
     m = gg[..., None] * m + q_t
     # o_t = q^T (S C - G), evaluated as (q^T S) C - q^T G so S C is never formed
     u = np.einsum("bha,bhac->bhc", q_t, S)
-    o = np.einsum("bhc,bhce->bhe", u, C) - np.einsum("bha,bhae->bhe", q_t, G)
+    o = np.einsum("bhc,bhce->bhe", u, C)
+    if masked:
+        o = o - np.einsum("bha,bhae->bhe", q_t, G)
     if normalize:
-        den = np.einsum("bhc,bhc->bh", u, m) - np.einsum("bha,bha->bh", q_t, h)
+        den = np.einsum("bhc,bhc->bh", u, m)
+        if masked:
+            den = den - np.einsum("bha,bha->bh", q_t, h)
         o = o / (den + eps)[..., None]
     return {"S": S, "C": C, "m": m, "G": G, "h": h}, o
 
 
 def serial_forward(q, k, v, gamma=None, normalize=False, eps=1e-6, init_state=None,
-                   return_state=False):
-    """Serial recurrence over all tokens: the streaming form of [TS] / [PS] §3.1."""
+                   return_state=False, masked=True):
+    """Serial recurrence over all tokens: the streaming form of [TS] / [PS] §3.1 (with
+    ``masked=False`` the unmasked output of reading R6; the state evolves the same way)."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -128,18 +142,19 @@ def serial_forward(q, k, v, gamma=None, normalize=False, eps=1e-6, init_state=No
         key: np.array(val, dtype=np.float64, copy=True) for key, val in init_state.items()}
     out = np.zeros((B, H, n, dv))
     for t in range(n):
-        st, out[:, :, t] = step(st, q[:, :, t], k[:, :, t], v[:, :, t], g, normalize, eps)
+        st, out[:, :, t] = step(st, q[:, :, t], k[:, :, t], v[:, :, t], g, normalize, eps, masked)
     return (out, st) if return_state else out
 
 
-def brute_force_forward(q, k, v, gamma=None, normalize=False, eps=1e-6):
+def brute_force_forward(q, k, v, gamma=None, normalize=False, eps=1e-6, masked=True):
     """The masked second-order output written as its pair sum (readings R1, R2):
 
         o_t = sum_{j <= t} sum_{i <= j} g^((t-i)+(t-j)) (q_t . k_i)(k_i . q_j) v_j
 
     i.e. the strictly causal mask of [PS] §2.1 applied to the bilinear form
-    q_t^T S_t C_t of [TS], keeping key index i at or before value index j.  The
-    denominator is the same sum with v_j replaced by 1.  O(n^3) per head: tiny n only.
+    q_t^T S_t C_t of [TS], keeping key index i at or before value index j.  With
+    ``masked=False`` i runs to t instead (reading R6: the whole product q_t^T S_t C_t).
+    The denominator is the same sum with v_j replaced by 1.  O(n^3) per head: tiny n only.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -156,7 +171,7 @@ def brute_force_forward(q, k, v, gamma=None, normalize=False, eps=1e-6):
                 den = 0.0
                 for j in range(t + 1):
                     w = 0.0
-                    for i in range(j + 1):
+                    for i in range(j + 1 if masked else t + 1):
                         w += g[hh] ** ((t - i) + (t - j)) * A[t, i] * A[j, i]
                     num += w * v[b, hh, j]
                     den += w
@@ -214,53 +229,78 @@ def combine(A, B):
     }
 
 
-def blelloch_exclusive_scan(items, d, dv):
+def unmasked_delta(q_t, k_t, v_t, g):
+    """Token delta of the unmasked monoid ([PS] §4.1; reading R6): (k k^T, q v^T, q)
+    with attenuation g."""
+    return {"S": np.outer(k_t, k_t), "C": np.outer(q_t, v_t),
+            "m": np.array(q_t, dtype=np.float64), "rho": float(g)}
+
+
+def unmasked_identity(d, dv):
+    """Neutral element of the unmasked monoid: empty segment, attenuation 1."""
+    return {"S": np.zeros((d, d)), "C": np.zeros((d, dv)), "m": np.zeros(d), "rho": 1.0}
+
+
+def combine_unmasked(A, B):
+    """Unmasked monoid ([PS] §4.1, with the decay of §4.3), A the earlier segment: each
+    moment is the later segment's plus the earlier one's attenuated by rho_B, with no
+    cross term, because the unmasked output keeps every (key, value) pair."""
+    r = B["rho"]
+    return {"S": r * A["S"] + B["S"], "C": r * A["C"] + B["C"], "m": r * A["m"] + B["m"],
+            "rho": A["rho"] * B["rho"]}
+
+
+def blelloch_exclusive_scan(items, d, dv, op=None, unit=None):
     """Exclusive Blelloch scan (up-sweep, then down-sweep) under ``combine`` ([PS] §4).
 
     The list is padded with identity elements to a power of two.  The operator is not
     commutative, so the down-sweep forms the right child's prefix as
     (parent prefix) (+) (left subtree total), keeping time order.
     Returns prefixes[t] = items[0] (+) ... (+) items[t-1] (identity for t = 0).
+    ``op`` and ``unit`` default to the masked ``combine`` and ``identity_element``.
     """
+    op = combine if op is None else op
+    unit = identity_element if unit is None else unit
     n = len(items)
     if n == 0:
         return []
     size = 1
     while size < n:
         size *= 2
-    tree = list(items) + [identity_element(d, dv) for _ in range(size - n)]
+    tree = list(items) + [unit(d, dv) for _ in range(size - n)]
     # up-sweep: tree[right] becomes the total of its subtree
     stride = 1
     while stride < size:
         for right in range(2 * stride - 1, size, 2 * stride):
             left = right - stride
-            tree[right] = combine(tree[left], tree[right])
+            tree[right] = op(tree[left], tree[right])
         stride *= 2
     # down-sweep
-    tree[size - 1] = identity_element(d, dv)
+    tree[size - 1] = unit(d, dv)
     stride = size // 2
     while stride >= 1:
         for right in range(2 * stride - 1, size, 2 * stride):
             left = right - stride
             left_total = tree[left]
             tree[left] = tree[right]
-            tree[right] = combine(tree[right], left_total)
+            tree[right] = op(tree[right], left_total)
         stride //= 2
     return tree[:n]
 
 
-def _output_from_state(st, q_t, normalize, eps):
-    """o_t = q^T (S C - G) and den_t = q^T (S m - h) on an inclusive state ([TS], R4)."""
+def _output_from_state(st, q_t, normalize, eps, masked=True):
+    """o_t = q^T (S C - G) and den_t = q^T (S m - h) on an inclusive state ([TS], R4);
+    unmasked, q^T S C and q^T S m (R6)."""
     u = q_t @ st["S"]
-    o = u @ st["C"] - q_t @ st["G"]
+    o = u @ st["C"] - (q_t @ st["G"] if masked else 0.0)
     if normalize:
-        den = u @ st["m"] - q_t @ st["h"]
+        den = u @ st["m"] - (q_t @ st["h"] if masked else 0.0)
         o = o / (den + eps)
     return o
 
 
 def chunked_scan_forward(q, k, v, gamma=None, chunk=16, normalize=False, eps=1e-6,
-                         init_state=None, return_state=False):
+                         init_state=None, return_state=False, masked=True):
     """Chunk-parallel forward in the order the pages give it ([PS] §4, §5; [TS4]):
 
       1. split [n] into chunks of width ``chunk`` (the last one may be shorter);
@@ -270,6 +310,9 @@ def chunked_scan_forward(q, k, v, gamma=None, chunk=16, normalize=False, eps=1e-
          seeded with the initial state, giving each chunk's carry-in;
       5. inclusive state of token t = carry (+) local prefix (+) delta_t;
       6. output from the inclusive state.
+
+    ``masked=False`` runs the same steps in the unmasked monoid on (S, C, m) and forms the
+    unmasked output (reading R6); its final state reports G = h = 0.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -279,27 +322,31 @@ def chunked_scan_forward(q, k, v, gamma=None, chunk=16, normalize=False, eps=1e-
     g = _gamma(gamma, H)
     out = np.zeros((B, H, n, dv))
     finals = zero_state(B, H, d, dv)
+    if masked:
+        delta, op, unit, keys = token_delta, combine, identity_element, ("S", "C", "m", "G", "h")
+    else:
+        delta, op, unit, keys = unmasked_delta, combine_unmasked, unmasked_identity, ("S", "C", "m")
     for b in range(B):
         for hh in range(H):
-            deltas = [token_delta(q[b, hh, t], k[b, hh, t], v[b, hh, t], g[hh]) for t in range(n)]
+            deltas = [delta(q[b, hh, t], k[b, hh, t], v[b, hh, t], g[hh]) for t in range(n)]
             chunks = [deltas[s:s + chunk] for s in range(0, n, chunk)]
-            local_prefix = [blelloch_exclusive_scan(c, d, dv) for c in chunks]
-            totals = [combine(pre[-1], c[-1]) for c, pre in zip(chunks, local_prefix)]
-            start = identity_element(d, dv)
+            local_prefix = [blelloch_exclusive_scan(c, d, dv, op, unit) for c in chunks]
+            totals = [op(pre[-1], c[-1]) for c, pre in zip(chunks, local_prefix)]
+            start = unit(d, dv)
             if init_state is not None:
-                for key in ("S", "C", "m", "G", "h"):
+                for key in keys:
                     start[key] = np.array(init_state[key][b, hh], dtype=np.float64)
             # exclusive scan of the chunk summaries; carry-in of chunk c = start (+) excl[c]
-            excl = blelloch_exclusive_scan(totals, d, dv)
+            excl = blelloch_exclusive_scan(totals, d, dv, op, unit)
             t = 0
             for ci, (c, pre) in enumerate(zip(chunks, local_prefix)):
-                carry = combine(start, excl[ci])
+                carry = op(start, excl[ci])
                 for li in range(len(c)):
-                    incl = combine(combine(carry, pre[li]), c[li])
-                    out[b, hh, t] = _output_from_state(incl, q[b, hh, t], normalize, eps)
+                    incl = op(op(carry, pre[li]), c[li])
+                    out[b, hh, t] = _output_from_state(incl, q[b, hh, t], normalize, eps, masked)
                     t += 1
-            fin = combine(start, combine(excl[-1], totals[-1])) if totals else start
-            for key in ("S", "C", "m", "G", "h"):
+            fin = op(start, op(excl[-1], totals[-1])) if totals else start
+            for key in keys:
                 finals[key][b, hh] = fin[key]
     return (out, finals) if return_state else out
 

@@ -397,30 +397,32 @@ def test_adjoint_dot_test():
 # The C oracle agrees with the numpy oracle
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("masked", [True, False])
 @pytest.mark.parametrize("normalize", [False, True])
-def test_c_oracle_forward_matches_numpy(normalize):
+def test_c_oracle_forward_matches_numpy(normalize, masked):
     q, k, v = rnd(2, 3, 40, 8, 5, seed=25, positive=normalize)
     q, k, v = (x.astype(np.float32).astype(np.float64) for x in (q, k, v))
     gam = [0.9, 0.99, 1.0]
-    a, sa = O.serial_forward(q, k, v, gam, normalize=normalize, return_state=True)
-    b, sb = cref.forward(q, k, v, gam, normalize=normalize, return_state=True)
+    a, sa = O.serial_forward(q, k, v, gam, normalize=normalize, return_state=True, masked=masked)
+    b, sb = cref.forward(q, k, v, gam, normalize=normalize, return_state=True, masked=masked)
     assert rel(b, a) < 1e-12
     assert rel(sb, O.pack_state(sa)) < 1e-12
     # continuation from a packed state
-    c = cref.forward(q, k, v, gam, normalize=normalize, init_state=sb)
-    d_ = O.serial_forward(q, k, v, gam, normalize=normalize, init_state=sa)
+    c = cref.forward(q, k, v, gam, normalize=normalize, init_state=sb, masked=masked)
+    d_ = O.serial_forward(q, k, v, gam, normalize=normalize, init_state=sa, masked=masked)
     assert rel(c, d_) < 1e-12
 
 
-def test_c_oracle_decode_matches_numpy():
+@pytest.mark.parametrize("masked", [True, False])
+def test_c_oracle_decode_matches_numpy(masked):
     q, k, v = rnd(3, 2, 5, 6, 4, seed=26)
     q, k, v = (x.astype(np.float32).astype(np.float64) for x in (q, k, v))
     gam = [0.9, 0.999]
     st = np.zeros((3, 2, O.state_floats(6, 4)))
     outs = []
     for t in range(5):
-        outs.append(cref.decode_step(st, q[:, :, t], k[:, :, t], v[:, :, t], gam))
-    a = O.serial_forward(q, k, v, gam)
+        outs.append(cref.decode_step(st, q[:, :, t], k[:, :, t], v[:, :, t], gam, masked=masked))
+    a = O.serial_forward(q, k, v, gam, masked=masked)
     assert rel(np.stack(outs, axis=2), a) < 1e-12
 
 
@@ -440,7 +442,7 @@ def test_c_oracle_backward_matches_numpy():
 # ---------------------------------------------------------------------------
 
 def _mutant_step(kind):
-    def step(state, q_t, k_t, v_t, g, normalize=False, eps=1e-6):
+    def step(state, q_t, k_t, v_t, g, normalize=False, eps=1e-6, masked=True):
         gg = g[None, :]
         S, C, m, G, h = state["S"], state["C"], state["m"], state["G"], state["h"]
         gG = gg * gg if kind != "G_decay_once" else gg
@@ -516,3 +518,120 @@ def test_compact_state_continues_the_serial_recurrence():
     back = O.unpack_state(O.state_from_compact(O.compact_from_state(flat, 8, 4), 8, 4), 8, 4)
     for key in ("S", "C", "G", "m", "h"):
         assert np.allclose(back[key], st[key], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Unmasked variant (reading R6): o_t = q_t^T S_t C_t, the unmasked monoid
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("g", [1.0, 0.7])
+def test_unmasked_closed_form_n2(g):
+    """n = 2 written out: every (key, value) pair of S_2 C_2 is kept, including the pair
+    (key 2, value 1) that the mask removes."""
+    q, k, v = rnd(1, 1, 2, 3, 2, seed=40)
+    Q, K, V = q[0, 0], k[0, 0], v[0, 0]
+    o = O.serial_forward(q, k, v, [g], masked=False)[0, 0]
+    assert np.allclose(o[0], (Q[0] @ K[0]) ** 2 * V[0], rtol=1e-13, atol=0)
+    S2 = g * np.outer(K[0], K[0]) + np.outer(K[1], K[1])
+    C2 = g * np.outer(Q[0], V[0]) + np.outer(Q[1], V[1])
+    assert np.allclose(o[1], Q[1] @ S2 @ C2, rtol=1e-13, atol=0)
+    masked = O.serial_forward(q, k, v, [g])[0, 0]
+    removed = g * (Q[1] @ K[1]) * (K[1] @ Q[0]) * V[0]   # key index 2 > value index 1
+    assert np.allclose(o[1] - masked[1], removed, rtol=1e-12, atol=1e-15)
+
+
+def test_unmasked_last_row_is_a_at_v():
+    """Without decay the last token sees the whole sequence, so its unmasked output is the
+    last row of A A^T V with A = Q K^T (the symmetric structure of the technical summary),
+    computed here with library matmuls."""
+    q, k, v = rnd(2, 2, 9, 4, 3, seed=41)
+    o = O.serial_forward(q, k, v, masked=False)
+    for b in range(2):
+        for h in range(2):
+            A = q[b, h] @ k[b, h].T
+            assert rel(o[b, h, -1], (A @ A.T @ v[b, h])[-1]) < 1e-12
+            # and every row t is the same product restricted to the first t + 1 tokens
+            t = 4
+            At = q[b, h, :t + 1] @ k[b, h, :t + 1].T
+            assert rel(o[b, h, t], (At @ At.T @ v[b, h, :t + 1])[-1]) < 1e-12
+
+
+@pytest.mark.parametrize("normalize", [False, True])
+def test_unmasked_brute_force_equals_serial(normalize):
+    q, k, v = rnd(1, 2, 8, 3, 2, seed=42, positive=normalize)
+    g = [1.0, 0.85]
+    assert rel(O.serial_forward(q, k, v, g, normalize, masked=False),
+               O.brute_force_forward(q, k, v, g, normalize, masked=False)) < 1e-12
+
+
+@pytest.mark.parametrize("chunk", [1, 2, 3, 5, 16])
+def test_unmasked_chunked_scan_equals_serial(chunk):
+    q, k, v = rnd(2, 2, 13, 3, 2, seed=43)
+    g = [0.9, 1.0]
+    out, fin = O.chunked_scan_forward(q, k, v, g, chunk, masked=False, return_state=True)
+    ref, st = O.serial_forward(q, k, v, g, masked=False, return_state=True)
+    assert rel(out, ref) < 1e-12
+    for key in ("S", "C", "m"):
+        assert rel(fin[key], st[key]) < 1e-12
+    assert not fin["G"].any() and not fin["h"].any()
+    qp, kp, vp = rnd(1, 1, 10, 3, 2, seed=44, positive=True)
+    assert rel(O.chunked_scan_forward(qp, kp, vp, [0.95], chunk, normalize=True, masked=False),
+               O.serial_forward(qp, kp, vp, [0.95], normalize=True, masked=False)) < 1e-12
+
+
+def test_unmasked_continuation_from_state():
+    """The unmasked scan seeded with the serial state after t0 tokens continues exactly."""
+    q, k, v = rnd(1, 2, 12, 3, 2, seed=45)
+    g = [0.9, 0.97]
+    full = O.serial_forward(q, k, v, g, masked=False)
+    _, st = O.serial_forward(q[:, :, :5], k[:, :, :5], v[:, :, :5], g, masked=False, return_state=True)
+    rest = O.chunked_scan_forward(q[:, :, 5:], k[:, :, 5:], v[:, :, 5:], g, 3, init_state=st, masked=False)
+    assert rel(rest, full[:, :, 5:]) < 1e-12
+
+
+def test_unmasked_monoid_algebra():
+    """Associative with an identity; at g = 1 it is commutative (plain sums), which the
+    masked semidirect product is not."""
+    r = np.random.default_rng(46)
+
+    def item(rho):
+        return {"S": r.standard_normal((3, 3)), "C": r.standard_normal((3, 2)),
+                "m": r.standard_normal(3), "rho": rho}
+
+    X, Y, Z = item(0.9), item(0.6), item(0.8)
+    left = O.combine_unmasked(O.combine_unmasked(X, Y), Z)
+    right = O.combine_unmasked(X, O.combine_unmasked(Y, Z))
+    for key in ("S", "C", "m"):
+        assert rel(left[key], right[key]) < 1e-13
+    e = O.unmasked_identity(3, 2)
+    for key in ("S", "C", "m"):
+        assert np.array_equal(O.combine_unmasked(e, X)[key], X[key])
+        assert np.array_equal(O.combine_unmasked(X, e)[key], X[key])
+    X1, Y1 = item(1.0), item(1.0)
+    for key in ("S", "C", "m"):
+        assert np.array_equal(O.combine_unmasked(X1, Y1)[key], O.combine_unmasked(Y1, X1)[key])
+
+
+def test_unmasked_planted_mistakes_are_caught(monkeypatch):
+    """A cross term in the unmasked monoid, or C decayed by g^2, breaks the agreement with
+    the serial recurrence; so does dropping the diagonal-and-later pairs (the masked sum)."""
+    q, k, v = rnd(1, 1, 9, 3, 2, seed=47)
+    truth = O.serial_forward(q, k, v, [0.9], masked=False)
+    assert rel(O.serial_forward(q, k, v, [0.9]), truth) > 1e-3
+    orig = O.combine_unmasked
+
+    def with_cross(A, B):
+        out = orig(A, B)
+        out["C"] = out["C"] + B["rho"] * (B["S"] @ A["C"])
+        return out
+
+    monkeypatch.setattr(O, "combine_unmasked", with_cross)
+    assert rel(O.chunked_scan_forward(q, k, v, [0.9], 3, masked=False), truth) > 1e-3
+
+    def c_decay_twice(A, B):
+        out = orig(A, B)
+        out["C"] = B["rho"] ** 2 * A["C"] + B["C"]
+        return out
+
+    monkeypatch.setattr(O, "combine_unmasked", c_decay_twice)
+    assert rel(O.chunked_scan_forward(q, k, v, [0.9], 3, masked=False), truth) > 1e-3
