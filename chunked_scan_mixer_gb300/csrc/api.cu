@@ -207,9 +207,10 @@ bool tc_disabled() {
     return e && strcmp(e, "mma") == 0;
 }
 
-Path choose_forward_path(int dtype, int d, int dv, int W, int normalize, bool want_final, const DevInfo& di) {
-    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !normalize && !want_final && !tc_disabled() &&
-        fwd_chunk_tc_smem() <= (size_t)di.smem_optin && fwd_chunk_tc_available())
+Path choose_forward_path(int dtype, int d, int dv, int W, int normalize, bool want_final, const DevInfo& di,
+                         bool unmasked = false) {
+    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !normalize && !want_final && !unmasked &&
+        !tc_disabled() && fwd_chunk_tc_smem() <= (size_t)di.smem_optin && fwd_chunk_tc_available())
         return Path::kTc;
     if (dtype == HLA2_BF16) {
         const size_t s = fwd_chunk_mma_smem(d, dv, W, true);
@@ -280,7 +281,11 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     if (rc != HLA2_OK) return rc;
     if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
     if (normalize && !isfinite(opts->eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
-    if (opts->flags & ~HLA2_FLAG_SAVE_FOR_BACKWARD) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_forward");
+    if (opts->flags & ~(HLA2_FLAG_SAVE_FOR_BACKWARD | HLA2_FLAG_UNMASKED))
+        return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_forward");
+    const bool unmasked = (opts->flags & HLA2_FLAG_UNMASKED) != 0;
+    if (unmasked && (opts->flags & HLA2_FLAG_SAVE_FOR_BACKWARD))
+        return fail(HLA2_ERR_UNSUPPORTED, "the backward covers the masked output only");
     const long BH = (long)B * H;
     const bool want_final = opts->final_state != nullptr;
     if ((opts->init_state && !aligned16(opts->init_state)) || (want_final && !aligned16(opts->final_state)))
@@ -289,12 +294,21 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t sf = raw_state_floats(d, dv);
     if (n == 0) {
-        // no tokens: the final state is the initial one (or the empty prefix)
+        // no tokens: the final state is the initial one (or the empty prefix); the unmasked
+        // variant reports G = h = 0 as for any other length
         if (want_final) {
             cudaError_t e = opts->init_state
                                 ? cudaMemcpyAsync(opts->final_state, opts->init_state, BH * sf * sizeof(float),
                                                   cudaMemcpyDeviceToDevice, st)
                                 : cudaMemsetAsync(opts->final_state, 0, BH * sf * sizeof(float), st);
+            if (e == cudaSuccess && unmasked && opts->init_state) {
+                const PackOff po = pack_off(d, dv);
+                e = cudaMemset2DAsync(opts->final_state + po.G, sf * sizeof(float), 0, (size_t)d * dv * sizeof(float),
+                                      (size_t)BH, st);
+                if (e == cudaSuccess)
+                    e = cudaMemset2DAsync(opts->final_state + po.h, sf * sizeof(float), 0, (size_t)d * sizeof(float),
+                                          (size_t)BH, st);
+            }
             if (e != cudaSuccess) return cuda_fail("final state copy");
         }
         return succeed();
@@ -306,10 +320,13 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         return forward_saving_for_backward(q, k, v, out, B, H, n, d, dv, gamma, normalize, chunk, st, opts);
 
     const DevInfo di = dev_info();
-    const Path path = choose_forward_path(opts->dtype, d, dv, chunk, normalize, want_final, di);
+    const Path path = choose_forward_path(opts->dtype, d, dv, chunk, normalize, want_final, di, unmasked);
     if (path == Path::kNone)
         return fail(HLA2_ERR_UNSUPPORTED, "no kernel for dtype %d, d %d, dv %d, chunk %d", opts->dtype, d, dv, chunk);
-    const Plan p = make_plan(B, H, n, d, dv, chunk, di.sms, forward_per_sm(path, d, dv, chunk, di));
+    // The unmasked output keeps the masked call's segmentation, so the workspace query
+    // (which has no flags) covers it: it uses a subset of the masked workspace.
+    const Plan p = unmasked ? forward_plan(B, H, n, d, dv, chunk, opts->dtype, normalize, want_final, di)
+                            : make_plan(B, H, n, d, dv, chunk, di.sms, forward_per_sm(path, d, dv, chunk, di));
     const FwdLayout L = fwd_layout(p, p.nseg - 1);
     const size_t need = L.total * sizeof(float);
     if (!opts->workspace || opts->workspace_bytes < need)
@@ -336,6 +353,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     a.want_final = want_final ? 1 : 0;
     a.ws = static_cast<float*>(opts->workspace);
     a.L = L;
+    a.unmasked = unmasked ? 1 : 0;
 
     const bool bf = opts->dtype == HLA2_BF16;
     auto chunk_pass = [&](int seg0, int count, bool summary, bool cm) -> int {
@@ -364,7 +382,15 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         if (launch_linear_scan(a.ws + L.SB, a.ws + L.Sin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true,
                                gamma, seg_tokens, 1, st))
             return cuda_fail("key-moment scan");
-        if (want_final) {
+        if (unmasked) {
+            // unmasked monoid: C and m (in the Z and y slots) are plain decayed prefixes
+            if (launch_linear_scan(a.ws + L.ZB, a.ws + L.Zin, a.BH, H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true,
+                                   gamma, seg_tokens, 1, st) ||
+                ((normalize || want_final) &&
+                 launch_linear_scan(a.ws + L.yB, a.ws + L.yin, a.BH, H, steps, d, a.nsum * (size_t)d,
+                                    p.nseg * (size_t)d, true, gamma, seg_tokens, 1, st)))
+                return cuda_fail("query-value scan");
+        } else if (want_final) {
             if (launch_linear_scan(a.ws + L.CB, a.ws + L.Clast, a.BH, H, steps, ddv, a.nsum * ddv, ddv, false,
                                    gamma, seg_tokens, 1, st) ||
                 launch_linear_scan(a.ws + L.mB, a.ws + L.mlast, a.BH, H, steps, d, a.nsum * (size_t)d, d, false,
@@ -373,17 +399,19 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         }
         // the denominator moment y is read only by the normalised output and the final state
         const bool with_y = normalize || want_final;
-        if (launch_cross(a, d, dv, with_y, st)) return cuda_fail("cross terms");
-        if (launch_linear_scan(a.ws + L.ZB, a.ws + L.Zin, a.BH, H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true,
-                               gamma, seg_tokens, 2, st) ||
-            (with_y && launch_linear_scan(a.ws + L.yB, a.ws + L.yin, a.BH, H, steps, d, a.nsum * (size_t)d,
-                                          p.nseg * (size_t)d, true, gamma, seg_tokens, 2, st)))
-            return cuda_fail("masked-summary scan");
+        if (!unmasked) {
+            if (launch_cross(a, d, dv, with_y, st)) return cuda_fail("cross terms");
+            if (launch_linear_scan(a.ws + L.ZB, a.ws + L.Zin, a.BH, H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true,
+                                   gamma, seg_tokens, 2, st) ||
+                (with_y && launch_linear_scan(a.ws + L.yB, a.ws + L.yin, a.BH, H, steps, d, a.nsum * (size_t)d,
+                                              p.nseg * (size_t)d, true, gamma, seg_tokens, 2, st)))
+                return cuda_fail("masked-summary scan");
+        }
     } else {
         mark(2);
     }
     mark(3);
-    if (want_final && p.nseg > 1) {
+    if (want_final && p.nseg > 1 && !unmasked) {
         if (chunk_pass(0, p.nseg - 1, false, false) || chunk_pass(p.nseg - 1, 1, false, true))
             return cuda_fail("output pass");
     } else {
@@ -737,14 +765,16 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
     int rc = check_common(N, H, 0, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
     if (normalize && !isfinite(eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
-    if (flags & ~HLA2_FLAG_COMPACT_STATE) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_decode_step");
+    if (flags & ~(HLA2_FLAG_COMPACT_STATE | HLA2_FLAG_UNMASKED))
+        return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_decode_step");
     if ((long)N * H == 0) return succeed();
     if (!state || !q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "state, q, k, v, out must not be NULL");
     if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return fail(HLA2_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
     cudaGetLastError();
     if (launch_decode_step(state, q, k, v, out, N, H, d, dv, gamma, normalize, eps, dtype == HLA2_BF16,
-                           (flags & HLA2_FLAG_COMPACT_STATE) != 0, reinterpret_cast<cudaStream_t>(stream)))
+                           (flags & HLA2_FLAG_COMPACT_STATE) != 0, (flags & HLA2_FLAG_UNMASKED) != 0,
+                           reinterpret_cast<cudaStream_t>(stream)))
         return cuda_fail("decode step");
     return succeed();
 }

@@ -9,6 +9,9 @@
 //   pass G:  G' = g^2 G + g k r^T,             z = G'^T q
 //   out = w - z  (= q^T (S' C' - G')),  den = u . m' - q . h'
 // with m' = g m + q and h' = g^2 h + g k (k . m).  G and h use the pre-update C, m.
+// The unmasked output (section summary §3: q^T S' C', denominator u . m') needs neither
+// G nor h: that variant skips pass G and the h update and leaves both untouched, so its
+// state traffic is S, C and m only.
 #include "kernels.h"
 
 namespace hla2 {
@@ -58,7 +61,8 @@ __device__ __forceinline__ void column_reduce(float4 p, int dv, float* red /*[kW
 }
 
 // COMPACT: the state uses the compact layout (S block-triangular, see compact_off).
-template <typename T, bool COMPACT>
+// UM: unmasked output (no G, h).
+template <typename T, bool COMPACT, bool UM>
 __global__ void __launch_bounds__(kThreads)
     decode_step_kernel(float* __restrict__ state, const T* __restrict__ q, const T* __restrict__ k,
                        const T* __restrict__ v, T* __restrict__ out, int H, int d, int dv,
@@ -81,8 +85,10 @@ __global__ void __launch_bounds__(kThreads)
 
     // m' = g m + q;  h' = g^2 h + g k (k . m_old)
     float km = 0.f;
-    for (int i = tid; i < d; i += kThreads) km += ks[i] * m[i];
-    km = block_sum(km, red);
+    if (!UM) {
+        for (int i = tid; i < d; i += kThreads) km += ks[i] * m[i];
+        km = block_sum(km, red);
+    }
     float mh_dot = 0.f;  // this thread's part of u . m' - q . h', formed after pass S
 
     // ---- pass S ----------------------------------------------------------------------
@@ -167,10 +173,13 @@ __global__ void __launch_bounds__(kThreads)
     // m, h and the denominator's vector terms
     for (int i = tid; i < d; i += kThreads) {
         const float mn = g * m[i] + qs[i];
-        const float hn = g2 * hh[i] + g * ks[i] * km;
         m[i] = mn;
-        hh[i] = hn;
-        mh_dot += us[i] * mn - qs[i] * hn;
+        mh_dot += us[i] * mn;
+        if (!UM) {
+            const float hn = g2 * hh[i] + g * ks[i] * km;
+            hh[i] = hn;
+            mh_dot -= qs[i] * hn;
+        }
     }
 
     // ---- pass C ------------------------------------------------------------------------
@@ -192,7 +201,7 @@ __global__ void __launch_bounds__(kThreads)
                 if (a >= d) continue;
                 const float ka = ks[a], qa = qs[a], ua = us[a];
                 float4 y = x[u];
-                pr.x += ka * y.x; pr.y += ka * y.y; pr.z += ka * y.z; pr.w += ka * y.w;
+                if (!UM) { pr.x += ka * y.x; pr.y += ka * y.y; pr.z += ka * y.z; pr.w += ka * y.w; }
                 y.x = g * y.x + qa * vs[c4 + 0];
                 y.y = g * y.y + qa * vs[c4 + 1];
                 y.z = g * y.z + qa * vs[c4 + 2];
@@ -201,12 +210,12 @@ __global__ void __launch_bounds__(kThreads)
                 st_stream(C + (size_t)a * dv + c4, y);
             }
         }
-        column_reduce(pr, dv, red, rs);
+        if (!UM) column_reduce(pr, dv, red, rs);
         column_reduce(pw, dv, red, ws);
     }
 
     // ---- pass G ------------------------------------------------------------------------
-    {
+    if (!UM) {
         const int lpc = dv / 4;
         const int rows_per = kThreads / lpc;
         const int c4 = (tid % lpc) * 4;
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(kThreads)
         inv = 1.f / (den + eps);
     }
     for (int e = tid; e < dv; e += kThreads)
-        out[(size_t)head * dv + e] = from_f32<T>((ws[e] - zs[e]) * inv);
+        out[(size_t)head * dv + e] = from_f32<T>((UM ? ws[e] : ws[e] - zs[e]) * inv);
 }
 
 // AHLA decode step (technical summary item "2. ... (AHLA)": streaming summaries P^KV, m^K,
@@ -375,15 +384,15 @@ __global__ void __launch_bounds__(kThreads) state_from_compact_kernel(const floa
     for (size_t i = threadIdx.x; i < tail; i += kThreads) dst[fs + i] = src[cs + i];
 }
 
-template <bool COMPACT>
+template <bool COMPACT, bool UM>
 void launch_decode_t(float* state, const void* q, const void* k, const void* v, void* out, long heads, int H, int d,
                      int dv, const float* gamma, int normalize, float eps, bool is_bf16, cudaStream_t st) {
     if (is_bf16)
-        decode_step_kernel<bf16, COMPACT><<<(unsigned)heads, kThreads, 0, st>>>(
+        decode_step_kernel<bf16, COMPACT, UM><<<(unsigned)heads, kThreads, 0, st>>>(
             state, static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
             static_cast<bf16*>(out), H, d, dv, gamma, normalize, eps);
     else
-        decode_step_kernel<float, COMPACT><<<(unsigned)heads, kThreads, 0, st>>>(
+        decode_step_kernel<float, COMPACT, UM><<<(unsigned)heads, kThreads, 0, st>>>(
             state, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
             static_cast<float*>(out), H, d, dv, gamma, normalize, eps);
 }
@@ -392,13 +401,17 @@ void launch_decode_t(float* state, const void* q, const void* k, const void* v, 
 
 int launch_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
                        int N, int H, int d, int dv, const float* gamma, int normalize, float eps,
-                       bool is_bf16, bool compact, cudaStream_t st) {
+                       bool is_bf16, bool compact, bool unmasked, cudaStream_t st) {
     const long heads = (long)N * H;
     if (heads <= 0) return 0;
-    if (compact)
-        launch_decode_t<true>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
+    if (compact && unmasked)
+        launch_decode_t<true, true>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
+    else if (compact)
+        launch_decode_t<true, false>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
+    else if (unmasked)
+        launch_decode_t<false, true>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
     else
-        launch_decode_t<false>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
+        launch_decode_t<false, false>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

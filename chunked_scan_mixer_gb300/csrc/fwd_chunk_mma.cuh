@@ -23,6 +23,14 @@
 // out (and the raw final state for the last segment); kStates starts from the carry-in
 // and exports the bf16 (S, Z) at every chunk start (the forward states that the
 // reverse-mode pass consumes); kOutStates does both (the forward of a training step).
+//
+// UM selects the unmasked output o_t = q_t^T S_t C_t = p_t^T C_t (section summary §3,
+// the bilinear form without the G correction; its scan is the unmasked monoid of §4.1).
+// It is a first-order scan with queries p, keys q and values v, so per chunk
+//   B~ = (P Q^T) * [j <= r] g^(r-j),   O = diag(g^(r+1)) P C0 + B~ V,
+//   den = diag(g^(r+1)) P m0 + B~ 1,   C <- g^Wc C0 + Q~^T V,   m likewise,
+// and the Z and y registers, tiles and workspace slots hold C and m instead.  The
+// summary pass then needs no A~ and no P at all.
 #pragma once
 
 #include "common.cuh"
@@ -55,10 +63,12 @@ struct MmaCfg {
     static constexpr size_t bytes(bool cm) { return oQt + (cm ? ROWS_D : 0); }
 };
 
-template <int D, int DV, int W, int MODE, bool CM>
+template <int D, int DV, int W, int MODE, bool CM, bool UM>
 __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
     fwd_chunk_mma_kernel(const ChunkArgs a) {
+    static_assert(!UM || (!CM && (MODE == kSummary || MODE == kOutput)), "unmasked: summary and output passes only");
     constexpr bool SUMMARY = MODE == kSummary, OUTPUT = MODE == kOutput || MODE == kOutStates;
+    constexpr bool NEED_P = !(UM && SUMMARY);  // the unmasked summary needs no p
     constexpr bool EXPORT = MODE == kStates || MODE == kOutStates;
     using Cfg = MmaCfg<D, DV, W>;
     constexpr int NW = Cfg::NW, NT = Cfg::NT, LD = Cfg::LD, LDV = Cfg::LDV, LW = Cfg::LW;
@@ -218,8 +228,16 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
             const float w1 = r < Wc ? gp[Wc - 1 - r] : 0.f;
             Kt[r * LD + f] = from_f32<bf16>(w1 * to_f32(Ks[r * LD + f]));
             if (CM) Qt[r * LD + f] = from_f32<bf16>(w1 * to_f32(Qs[r * LD + f]));
+            if (UM) Pt[r * LD + f] = from_f32<bf16>(w1 * to_f32(Qs[r * LD + f]));  // Q~
         }
-        if (OUTPUT && a.normalize) {
+        if (UM) {  // the query-mass increment, added to m (held in ys) after the chunk
+            for (int f = tid; f < D; f += NT) {
+                float s = 0.f;
+                for (int r = 0; r < Wc; ++r) s += gp[Wc - 1 - r] * to_f32(Qs[r * LD + f]);
+                yadd[f] = s;
+            }
+        }
+        if (OUTPUT && a.normalize && !UM) {
             for (int r = tid; r < W; r += NT) {
                 float s = 0.f;
                 for (int f = 0; f < D; ++f) s += to_f32(Qs[r * LD + f]) * ys[f];
@@ -236,7 +254,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         __syncthreads();
 
         // ---- A~ = mask(Q K^T) ---------------------------------------------------------
-        for (int t = warp; t < TW * TW; t += NW) {
+        for (int t = warp; NEED_P && t < TW * TW; t += NW) {
             const int rb = t / TW, cb = t % TW;
             if (cb > rb) continue;
             float acc[2][4];
@@ -255,7 +273,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         __syncthreads();
 
         // ---- P = diag(g^(r+1)) Q S0 + A~ K ; P~ ; y increment -------------------------
-        for (int t = warp; t < TW * TD; t += NW) {
+        for (int t = warp; NEED_P && t < TW * TD; t += NW) {
             const int rb = t / TD, fb = t % TD;
             float acc[2][4];
             zero_acc(acc);
@@ -271,13 +289,15 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
 #pragma unroll
                 for (int i = 0; i < 4; i += 2) {
                     const int r = acc_row(rb * 16, i), col = acc_col(fb * 16, h, i);
-                    const float w2 = r < Wc ? gp[2 * (Wc - 1 - r)] : 0.f;
                     *reinterpret_cast<uint32_t*>(&Ps[r * LD + col]) = pack_bf16x2(acc[h][i], acc[h][i + 1]);
+                    if (UM) continue;
+                    const float w2 = r < Wc ? gp[2 * (Wc - 1 - r)] : 0.f;
                     *reinterpret_cast<uint32_t*>(&Pt[r * LD + col]) =
                         pack_bf16x2(w2 * acc[h][i], w2 * acc[h][i + 1]);
                     colsum[h][0] += w2 * acc[h][i];
                     colsum[h][1] += w2 * acc[h][i + 1];
                 }
+            if (UM) continue;
             // reduce the 16 rows of the tile: lanes with equal (lane & 3) share columns
 #pragma unroll
             for (int h = 0; h < 2; ++h)
@@ -292,22 +312,35 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         }
         __syncthreads();
 
+        if (OUTPUT && UM && a.normalize) {  // denominator carry term g^(r+1) p_r . m0
+            for (int r = tid; r < W; r += NT) {
+                float s = 0.f;
+                for (int f = 0; f < D; ++f) s += to_f32(Ps[r * LD + f]) * ys[f];
+                den[r] = gp[r + 1] * s;
+            }
+            __syncthreads();
+        }
+
         if (OUTPUT) {
-            // ---- B~ = mask(Q P^T) (+ row sums for the denominator) -----------------------
+            // ---- B~ = mask(Q P^T) (+ row sums for the denominator); unmasked mask(P Q^T) --
+            constexpr int BP = UM ? 1 : 2;  // decay power of the second scan
             for (int t = warp; t < TW * TW; t += NW) {
                 const int rb = t / TW, jb = t % TW;
                 if (jb > rb) continue;
                 float acc[2][4];
                 zero_acc(acc);
-                warp_tile_mma<false, false>(acc, Qs, LD, rb * 16, Ps, LD, jb * 16, 0, D);
+                if (UM)
+                    warp_tile_mma<false, false>(acc, Ps, LD, rb * 16, Qs, LD, jb * 16, 0, D);
+                else
+                    warp_tile_mma<false, false>(acc, Qs, LD, rb * 16, Ps, LD, jb * 16, 0, D);
                 float rs[2] = {0.f, 0.f};
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int i = 0; i < 4; i += 2) {
                         const int r = acc_row(rb * 16, i), col = acc_col(jb * 16, h, i);
-                        const float v0 = col <= r ? gp[2 * (r - col)] * acc[h][i] : 0.f;
-                        const float v1 = col + 1 <= r ? gp[2 * (r - col - 1)] * acc[h][i + 1] : 0.f;
+                        const float v0 = col <= r ? gp[BP * (r - col)] * acc[h][i] : 0.f;
+                        const float v1 = col + 1 <= r ? gp[BP * (r - col - 1)] * acc[h][i + 1] : 0.f;
                         *reinterpret_cast<uint32_t*>(&AB[r * LW + col]) = pack_bf16x2(v0, v1);
                         rs[i >> 1] += v0 + v1;
                     }
@@ -323,17 +356,17 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
             }
             __syncthreads();
 
-            // ---- O = diag(g^(2(r+1))) Q Z0 + B~ V -> out ---------------------------------
+            // ---- O = diag(g^(2(r+1))) Q Z0 + B~ V -> out; unmasked g^(r+1) P C0 + B~ V --
             bf16* outp = static_cast<bf16*>(a.out) + ((size_t)bh * a.n + (size_t)c * W) * DV;
             for (int t = warp; t < TW * TV; t += NW) {
                 const int rb = t / TV, eb = t % TV;
                 float acc[2][4];
                 zero_acc(acc);
-                warp_tile_mma<false, true>(acc, Qs, LD, rb * 16, Zst, LDV, eb * 16, 0, D);
+                warp_tile_mma<false, true>(acc, UM ? Ps : Qs, LD, rb * 16, Zst, LDV, eb * 16, 0, D);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[h][i] *= gp[2 * (acc_row(rb * 16, i) + 1)];
+                    for (int i = 0; i < 4; ++i) acc[h][i] *= gp[BP * (acc_row(rb * 16, i) + 1)];
                 warp_tile_mma<false, true>(acc, AB, LW, rb * 16, Vs, LDV, eb * 16, 0, (rb + 1) * 16);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
@@ -352,8 +385,8 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
             }
         }
 
-        // ---- state updates in registers ---------------------------------------------------
-        const float rho = gp[Wc], rho2 = gp[2 * Wc];
+        // ---- state updates in registers (unmasked: Zacc holds C, Pt holds Q~) ---------------
+        const float rho = gp[Wc], rho2 = gp[UM ? Wc : 2 * Wc];
 #pragma unroll
         for (int s = 0; s < Cfg::S_PER; ++s) {
             const int t = warp + s * NW;
@@ -402,7 +435,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         dZ = a.ws + a.L.ZB + sidx * D * DV;
         dm = a.ws + a.L.mB + sidx * D;
         dy = a.ws + a.L.yB + sidx * D;
-    } else if (OUTPUT && CM && last_seg && a.want_final) {
+    } else if (OUTPUT && (CM || UM) && last_seg && a.want_final) {
         const RawOff ro = raw_off(D, DV);
         float* base = a.ws + a.L.fin + (size_t)bh * raw_state_floats(D, DV);
         dS = base + ro.S;
@@ -445,9 +478,9 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
     }
 }
 
-template <int D, int DV, int W, int MODE, bool CM>
+template <int D, int DV, int W, int MODE, bool CM, bool UM = false>
 cudaError_t launch_mode(const ChunkArgs& a, size_t smem, cudaStream_t st) {
-    auto kfn = fwd_chunk_mma_kernel<D, DV, W, MODE, CM>;
+    auto kfn = fwd_chunk_mma_kernel<D, DV, W, MODE, CM, UM>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kfn<<<dim3(a.nseg_launch, a.BH), MmaCfg<D, DV, W>::NT, smem, st>>>(a);
@@ -457,11 +490,18 @@ cudaError_t launch_mode(const ChunkArgs& a, size_t smem, cudaStream_t st) {
 template <int D, int DV, int W>
 int launch_fwd_chunk_mma_t(const ChunkArgs& a, int mode, bool track_cm, cudaStream_t st) {
     using Cfg = MmaCfg<D, DV, W>;
-    const bool cm = mode == kSummary || track_cm;
+    const bool cm = !a.unmasked && (mode == kSummary || track_cm);
     const size_t smem = Cfg::bytes(cm);
     if (a.nseg_launch <= 0 || a.BH <= 0) return 0;
     cudaError_t e;
-    if (mode == kSummary)
+    if (a.unmasked) {
+        if (mode == kSummary)
+            e = launch_mode<D, DV, W, kSummary, false, true>(a, smem, st);
+        else if (mode == kOutput)
+            e = launch_mode<D, DV, W, kOutput, false, true>(a, smem, st);
+        else
+            return -2;
+    } else if (mode == kSummary)
         e = launch_mode<D, DV, W, kSummary, true>(a, smem, st);
     else if (mode == kStates)
         e = launch_mode<D, DV, W, kStates, false>(a, smem, st);

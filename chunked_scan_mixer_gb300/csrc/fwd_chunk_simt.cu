@@ -2,7 +2,9 @@
 // tiles, runtime shapes.  Same per-chunk algebra as the tensor-core kernel
 // (fwd_chunk_mma.cuh), written as plain loops; it serves float32 inputs (where bf16
 // tensor-core operands would not meet a 1e-4 relative error) and bf16 shapes the
-// tensor-core kernel does not cover.
+// tensor-core kernel does not cover.  With a.unmasked it computes the unmasked output
+// q^T S C (section summary §3, §4.1): Z and y then hold C and m, the second product is
+// (P Q^T) * [j <= r] g^(r-j), and the carry term is g^(r+1) P C0.
 #include "kernels.h"
 
 namespace hla2 {
@@ -49,6 +51,9 @@ __global__ void __launch_bounds__(kSimtThreads)
     const T* q = static_cast<const T*>(a.q) + (size_t)bh * a.n * D;
     const T* k = static_cast<const T*>(a.k) + (size_t)bh * a.n * D;
     const T* v = static_cast<const T*>(a.v) + (size_t)bh * a.n * DV;
+    const bool um = a.unmasked != 0;
+    const bool need_p = !(summary && um);  // the unmasked summary needs no p
+    const int bp = um ? 1 : 2;             // decay power of the second scan
 
     const float log2g = log2f(head_decay(a.gamma, bh, a.H));
     for (int i = tid; i < 2 * W + 2; i += NT) gp[i] = pow_decay(log2g, (float)i);
@@ -79,14 +84,14 @@ __global__ void __launch_bounds__(kSimtThreads)
         __syncthreads();
 
         // A~[r, i] = [i <= r] g^(r-i) q_r . k_i ; den carry term
-        for (int e = tid; e < W * W; e += NT) {
+        for (int e = tid; need_p && e < W * W; e += NT) {
             const int r = e / W, i = e % W;
             float s = 0.f;
             if (i <= r)
                 for (int f = 0; f < D; ++f) s += Qs[r * D + f] * Ks[i * D + f];
             AB[e] = i <= r ? gp[r - i] * s : 0.f;
         }
-        if (!summary && a.normalize) {
+        if (!summary && a.normalize && !um) {
             for (int r = tid; r < W; r += NT) {
                 float s = 0.f;
                 for (int f = 0; f < D; ++f) s += Qs[r * D + f] * y[f];
@@ -96,7 +101,7 @@ __global__ void __launch_bounds__(kSimtThreads)
         __syncthreads();
 
         // P = diag(g^(r+1)) Q S0 + A~ K
-        for (int e = tid; e < W * D; e += NT) {
+        for (int e = tid; need_p && e < W * D; e += NT) {
             const int r = e / D, f = e % D;
             float s0 = 0.f, s1 = 0.f;
             for (int x = 0; x < D; ++x) s0 += Qs[r * D + x] * S[x * D + f];
@@ -106,13 +111,23 @@ __global__ void __launch_bounds__(kSimtThreads)
         __syncthreads();
 
         if (!summary) {
-            // B~[r, j] = [j <= r] g^(2(r-j)) q_r . p_j
+            if (um && a.normalize) {  // unmasked denominator carry g^(r+1) p_r . m0
+                for (int r = tid; r < W; r += NT) {
+                    float s = 0.f;
+                    for (int f = 0; f < D; ++f) s += Ps[r * D + f] * y[f];
+                    den[r] = gp[r + 1] * s;
+                }
+            }
+            // B~[r, j] = [j <= r] g^(2(r-j)) q_r . p_j   (unmasked: g^(r-j) p_r . q_j)
             for (int e = tid; e < W * W; e += NT) {
                 const int r = e / W, j = e % W;
                 float s = 0.f;
-                if (j <= r)
-                    for (int f = 0; f < D; ++f) s += Qs[r * D + f] * Ps[j * D + f];
-                AB[e] = j <= r ? gp[2 * (r - j)] * s : 0.f;
+                if (j <= r) {
+                    const float* x0 = um ? Ps + r * D : Qs + r * D;
+                    const float* x1 = um ? Qs + j * D : Ps + j * D;
+                    for (int f = 0; f < D; ++f) s += x0[f] * x1[f];
+                }
+                AB[e] = j <= r ? gp[bp * (r - j)] * s : 0.f;
             }
             __syncthreads();
             if (a.normalize) {
@@ -123,22 +138,25 @@ __global__ void __launch_bounds__(kSimtThreads)
                 }
                 __syncthreads();
             }
-            // O = diag(g^(2(r+1))) Q Z0 + B~ V
+            // O = diag(g^(2(r+1))) Q Z0 + B~ V   (unmasked: diag(g^(r+1)) P C0 + B~ V)
             T* out = static_cast<T*>(a.out) + ((size_t)bh * a.n + row0) * DV;
+            const float* lhs = um ? Ps : Qs;
             for (int e = tid; e < Wc * DV; e += NT) {
                 const int r = e / DV, x = e % DV;
                 float s0 = 0.f, s1 = 0.f;
-                for (int f = 0; f < D; ++f) s0 += Qs[r * D + f] * Z[f * DV + x];
+                for (int f = 0; f < D; ++f) s0 += lhs[r * D + f] * Z[f * DV + x];
                 for (int j = 0; j <= r; ++j) s1 += AB[r * W + j] * Vs[j * DV + x];
-                float o = gp[2 * (r + 1)] * s0 + s1;
+                float o = gp[bp * (r + 1)] * s0 + s1;
                 if (a.normalize) o /= (den[r] + a.eps);
                 out[e] = from_f32<T>(o);
             }
             __syncthreads();
         }
 
-        // state updates (each element owned by one thread)
-        const float rho = gp[Wc], rho2 = gp[2 * Wc];
+        // state updates (each element owned by one thread); unmasked, Z and y take the
+        // query-value and query-mass increments with decay g
+        const float rho = gp[Wc], rho2 = gp[bp * Wc];
+        const float* zl = um ? Qs : Ps;  // left factor of the Z and y increments
         for (int e = tid; e < D * D; e += NT) {
             const int x = e / D, f = e % D;
             float s = 0.f;
@@ -149,7 +167,7 @@ __global__ void __launch_bounds__(kSimtThreads)
             const int x = e / DV, f = e % DV;
             float s = 0.f, sc = 0.f;
             for (int j = 0; j < Wc; ++j) {
-                s += gp[2 * (Wc - 1 - j)] * Ps[j * D + x] * Vs[j * DV + f];
+                s += gp[bp * (Wc - 1 - j)] * zl[j * D + x] * Vs[j * DV + f];
                 if (cm) sc += gp[Wc - 1 - j] * Qs[j * D + x] * Vs[j * DV + f];
             }
             Z[e] = rho2 * Z[e] + s;
@@ -158,7 +176,7 @@ __global__ void __launch_bounds__(kSimtThreads)
         for (int x = tid; x < D; x += NT) {
             float s = 0.f, sm_ = 0.f;
             for (int j = 0; j < Wc; ++j) {
-                s += gp[2 * (Wc - 1 - j)] * Ps[j * D + x];
+                s += gp[bp * (Wc - 1 - j)] * zl[j * D + x];
                 sm_ += gp[Wc - 1 - j] * Qs[j * D + x];
             }
             y[x] = rho2 * y[x] + s;
@@ -175,7 +193,7 @@ __global__ void __launch_bounds__(kSimtThreads)
         dZ = a.ws + a.L.ZB + si * D * DV;
         dm = a.ws + a.L.mB + si * D;
         dy = a.ws + a.L.yB + si * D;
-    } else if (cm && seg == nseg - 1 && a.want_final) {
+    } else if ((cm || um) && seg == nseg - 1 && a.want_final) {
         const RawOff ro = raw_off(D, DV);
         float* base = a.ws + a.L.fin + (size_t)bh * raw_state_floats(D, DV);
         dS = base + ro.S;
@@ -188,7 +206,7 @@ __global__ void __launch_bounds__(kSimtThreads)
         for (int i = tid; i < D * D; i += NT) dS[i] = S[i];
         for (int i = tid; i < D * DV; i += NT) {
             dZ[i] = Z[i];
-            dC[i] = C[i];
+            if (cm) dC[i] = C[i];
         }
         for (int i = tid; i < D; i += NT) {
             dm[i] = m[i];
@@ -206,7 +224,7 @@ size_t fwd_chunk_simt_smem(int d, int dv, int W, bool track_cm) {
 int launch_fwd_chunk_simt(const ChunkArgs& a, int d, int dv, int W, bool summary, bool track_cm,
                           bool is_bf16, cudaStream_t st) {
     if (a.nseg_launch <= 0 || a.BH <= 0) return 0;
-    const bool cm = summary || track_cm;
+    const bool cm = !a.unmasked && (summary || track_cm);
     const size_t smem = fwd_chunk_simt_smem(d, dv, W, cm);
     dim3 grid(a.nseg_launch, a.BH), block(kSimtThreads);
     cudaError_t e;

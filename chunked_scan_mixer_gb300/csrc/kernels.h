@@ -77,6 +77,10 @@ struct ChunkArgs {
     float* ws;        // forward workspace (floats)
     FwdLayout L;
     bf16* chunk_states;  // state-export pass: bf16 (S | Z) at every chunk start, [BH][nchunks][d*d + d*dv]
+    // 1: unmasked output q^T S C (and denominator q^T S m).  The Z and y slots of the
+    // summaries, the carries and the raw final state then hold C and m, which decay by
+    // g per token, and no cross term enters the inter-segment scan.
+    int unmasked;
 };
 
 // Chunk-kernel passes.
@@ -118,7 +122,8 @@ int launch_quotient_rule(const bf16* dout, const bf16* num, const bf16* den_out,
 int launch_add_into(bf16* a, const bf16* b, size_t count, cudaStream_t st);
 
 // Tensor-core (mma.sync bf16) chunk kernel: d == dv in {16,32,64,128}, W in {16,32,64,128}.
-// Returns 0 on success, -1 on a CUDA error, -2 if the shape is not compiled.
+// Returns 0 on success, -1 on a CUDA error, -2 if the shape is not compiled.  With
+// a.unmasked only the kSummary and kOutput modes exist and track_cm is ignored.
 int launch_fwd_chunk_mma(const ChunkArgs& a, int d, int dv, int W, int mode, bool track_cm,
                          cudaStream_t st);
 size_t fwd_chunk_mma_smem(int d, int dv, int W, bool track_cm);  // 0 if not compiled
@@ -147,7 +152,7 @@ int launch_finalize(const ChunkArgs& a, int d, int dv, float* final_state, cudaS
 // Decode step.
 int launch_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
                        int N, int H, int d, int dv, const float* gamma, int normalize, float eps,
-                       bool is_bf16, bool compact, cudaStream_t st);
+                       bool is_bf16, bool compact, bool unmasked, cudaStream_t st);
 int launch_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
                             int d, int dv, const float* gamma, int normalize, float eps, bool is_bf16,
                             cudaStream_t st);

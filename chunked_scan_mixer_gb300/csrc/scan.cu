@@ -22,7 +22,8 @@ namespace {
 constexpr int kThreads = 256;
 
 // Carry into segment 0 from the optional packed initial state (S, C, G, m, h):
-// Z0 = S0 C0 - G0 and y0 = S0 m0 - h0; zero without an initial state.
+// Z0 = S0 C0 - G0 and y0 = S0 m0 - h0; zero without an initial state.  The unmasked
+// output carries C0 and m0 in those slots and ignores G0 and h0.
 __global__ void __launch_bounds__(kThreads)
     init_carry_kernel(const ChunkArgs a, int D, int DV, const float* init) {
     const int bh = blockIdx.x, tid = threadIdx.x;
@@ -43,6 +44,11 @@ __global__ void __launch_bounds__(kThreads)
     const float* st = init + (size_t)bh * (size_t)raw_state_floats(D, DV);
     const float *S0 = st + po.S, *C0 = st + po.C, *G0 = st + po.G, *m0 = st + po.m, *h0 = st + po.h;
     for (int i = tid; i < D * D; i += kThreads) Sin[i] = S0[i];
+    if (a.unmasked) {
+        for (int i = tid; i < D * DV; i += kThreads) Zin[i] = Cl[i] = C0[i];
+        for (int i = tid; i < D; i += kThreads) yin[i] = ml[i] = m0[i];
+        return;
+    }
     for (int i = tid; i < D * DV; i += kThreads) {
         const int r = i / DV, c = i % DV;
         float s = 0.f;
@@ -183,6 +189,17 @@ __global__ void __launch_bounds__(kThreads)
     float* o = final_state + (size_t)bh * raw_state_floats(D, DV);
     const float *S = r + ro.S, *C = r + ro.C, *m = r + ro.m, *Z = r + ro.Z, *y = r + ro.y;
     for (int i = tid; i < D * D; i += kThreads) o[po.S + i] = S[i];
+    if (a.unmasked) {  // C and m sit in the Z and y slots; G and h are not tracked
+        for (int i = tid; i < D * DV; i += kThreads) {
+            o[po.C + i] = Z[i];
+            o[po.G + i] = 0.f;
+        }
+        for (int x = tid; x < D; x += kThreads) {
+            o[po.m + x] = y[x];
+            o[po.h + x] = 0.f;
+        }
+        return;
+    }
     for (int i = tid; i < D * DV; i += kThreads) {
         const int x = i / DV, c = i % DV;
         float acc = 0.f;

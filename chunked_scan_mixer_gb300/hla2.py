@@ -123,6 +123,7 @@ EXPORTED_SYMBOLS = (
 )
 
 FLAG_COMPACT_STATE = 4
+FLAG_UNMASKED = 8
 
 
 def _check(func, rc):
@@ -227,7 +228,7 @@ def _to_device(t, device):
 _side_streams: dict = {}
 
 
-def _pipelined_host_forward(q, k, v, gamma, normalize, chunk, eps, out):
+def _pipelined_host_forward(q, k, v, gamma, normalize, chunk, eps, out, masked=True):
     """forward() on host tensors, overlapping the copies with the computation: the heads are
     independent, so they go through in groups -- the inputs of group i+1 are copied in on one
     stream while group i is computed on the current stream and group i-1's output is copied
@@ -269,7 +270,7 @@ def _pipelined_host_forward(q, k, v, gamma, normalize, chunk, eps, out):
             cur.wait_event(ev_out[slot])  # group i-2's output has left this slot
         forward(qd.view(1, gh, n, d), kd.view(1, gh, n, d), vd.view(1, gh, n, dv),
                 gamma=None if g is None else g[h0:h0 + gh], normalize=normalize, chunk=chunk, eps=eps,
-                out=od.view(1, gh, n, dv))
+                out=od.view(1, gh, n, dv), masked=masked)
         ev_comp[slot].record(cur)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[slot])
@@ -282,8 +283,9 @@ def _pipelined_host_forward(q, k, v, gamma, normalize, chunk, eps, out):
 
 
 def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state=None,
-            return_final_state=False, out=None, phase_events=None, save_for_backward=False):
+            return_final_state=False, out=None, phase_events=None, save_for_backward=False, masked=True):
     """Masked HLA-2 forward.  q, k [B,H,n,d]; v [B,H,n,dv] (float32 or bfloat16).
+    masked=False computes the unmasked output q^T S C instead (HLA2_FLAG_UNMASKED).
 
     gamma: None, a scalar, or [H] per-head decay in (0, 1].  init_state: packed
     [B,H,state_floats] float32 state to continue from.  Returns out [B,H,n,dv] (and the
@@ -298,7 +300,7 @@ def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state
         raise TypeError("q, k, v must all be float32 or all bfloat16")
     if (host and init_state is None and not return_final_state and phase_events is None and not save_for_backward
             and k.device.type == "cpu" and v.device.type == "cpu" and (out is None or out.device.type == "cpu")):
-        res = _pipelined_host_forward(q, k, v, gamma, normalize, chunk, eps, out)
+        res = _pipelined_host_forward(q, k, v, gamma, normalize, chunk, eps, out, masked)
         if res is not None:
             return res
     B, H, n, d = q.shape
@@ -316,7 +318,7 @@ def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state
     fin = torch.empty((B, H, state_floats(d, dv)), dtype=torch.float32, device=device) \
         if return_final_state else None
     sh = _stream_handle(device)
-    flags = 0
+    flags = 0 if masked else FLAG_UNMASKED
     if save_for_backward:
         if host:
             raise ValueError("save_for_backward needs device tensors")
@@ -324,7 +326,7 @@ def forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, init_state
         if nbytes == ctypes.c_size_t(-1).value:
             raise HLA2Error("hla2_backward_workspace_bytes", -2, "these arguments have no backward")
         ws = torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
-        flags = FLAG_SAVE_FOR_BACKWARD
+        flags |= FLAG_SAVE_FOR_BACKWARD
     else:
         nbytes = forward_workspace_bytes(B, H, n, d, dv, chunk, q.dtype, normalize, return_final_state)
         ws = _workspace(nbytes, device, sh)
@@ -446,10 +448,10 @@ def backward(q, k, v, dout, gamma=None, chunk=64, dq=None, dk=None, dv=None, sav
     return gq, gk, gv
 
 
-def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6, out=None, compact=False):
+def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6, out=None, compact=False, masked=True):
     """One decode step; ``state`` [N,H,state_floats(d, dv, compact)] float32 on the GPU is
     updated in place (compact: the block-triangular S layout).  q, k [N,H,d]; v [N,H,dv].
-    Returns out [N,H,dv]."""
+    masked=False: the unmasked output q^T S C (G and h untouched).  Returns out [N,H,dv]."""
     L = lib()
     if state.device.type != "cuda" or state.dtype != torch.float32 or not state.is_contiguous():
         raise ValueError("state must be a contiguous float32 CUDA tensor")
@@ -459,7 +461,8 @@ def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6, out=None,
     qd, kd, vd = (_to_device(t, device) for t in (q, k, v))
     g = _gamma_tensor(gamma, H, device)
     o = out if out is not None else torch.empty((N, H, dv), dtype=q.dtype, device=device)
-    opts = Opts(_DTYPES[q.dtype], float(eps), None, 0, None, None, None, 0, FLAG_COMPACT_STATE if compact else 0)
+    flags = (FLAG_COMPACT_STATE if compact else 0) | (0 if masked else FLAG_UNMASKED)
+    opts = Opts(_DTYPES[q.dtype], float(eps), None, 0, None, None, None, 0, flags)
     rc = L.hla2_decode_step(_ptr(state), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), N, H, d, dv, _ptr(g),
                             int(normalize), _stream_handle(device), ctypes.byref(opts))
     _check("hla2_decode_step", rc)

@@ -93,8 +93,22 @@ typedef struct {
  *     SAVE_FOR_BACKWARD forward with the same q, k, gamma, sizes and chunk, untouched since;
  *     the backward then skips its forward recomputation.  The library cannot check that
  *     the workspace is still intact: passing this flag otherwise gives wrong gradients.
+ * and for the unmasked output (hla2_forward, hla2_decode_step):
+ *   HLA2_FLAG_UNMASKED: o_t = q_t^T S_t C_t, the bilinear form of the prefix moments without
+ *     the G correction (section summary §3, "numerator-style bilinear form"), and with
+ *     normalize the denominator q_t^T S_t m_t.  Every (key, value) pair up to t counts,
+ *     weighted g^((t-i)+(t-j)); the chunk scan combines (S, C, m) by decayed addition (the
+ *     unmasked monoid, section summary §4.1).  G and h are not tracked: a forward's
+ *     final_state holds them as 0, init_state's are ignored, and the decode step leaves them
+ *     untouched.  Not with HLA2_FLAG_SAVE_FOR_BACKWARD (HLA2_ERR_UNSUPPORTED): the backward
+ *     covers the masked output.
  */
-enum { HLA2_FLAG_SAVE_FOR_BACKWARD = 1, HLA2_FLAG_STATES_SAVED = 2, HLA2_FLAG_COMPACT_STATE = 4 };
+enum {
+    HLA2_FLAG_SAVE_FOR_BACKWARD = 1,
+    HLA2_FLAG_STATES_SAVED = 2,
+    HLA2_FLAG_COMPACT_STATE = 4,
+    HLA2_FLAG_UNMASKED = 8
+};
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int hla2_version(void);
@@ -123,7 +137,8 @@ size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chun
  * normalize != 0 divides by the masked denominator (+ opts->eps).
  * opts must be non-NULL (dtype and workspace).  init_state continues a previous
  * sequence; final_state receives the state after the last token (prefill for
- * hla2_decode_step).
+ * hla2_decode_step).  opts->flags may hold HLA2_FLAG_SAVE_FOR_BACKWARD or
+ * HLA2_FLAG_UNMASKED (the unmasked output, with the same workspace size).
  */
 int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
                  int d, int dv, const float* gamma, int normalize, int chunk,
@@ -133,7 +148,9 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
  * The segmentation hla2_forward will use for these arguments on the current device:
  * *nseg segments of *seg_chunks chunks per head, and *launches kernel launches per
  * call (normalize and want_final_state as passed to hla2_forward).  Any output pointer
- * may be NULL.  Returns HLA2_OK or HLA2_ERR_INVALID_ARG.
+ * may be NULL.  Returns HLA2_OK or HLA2_ERR_INVALID_ARG.  The segmentation is the same
+ * with HLA2_FLAG_UNMASKED; the launch count is the masked output's (the unmasked one
+ * needs fewer).
  */
 int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize,
                       int want_final_state, int* nseg, int* seg_chunks, int* launches);
@@ -172,6 +189,8 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
  * blocks, updated in place; q, k [N, H, d]; v, out [N, H, dv].  The cross summaries
  * G, h are advanced from the pre-update C, m; the output uses the updated state.
  * opts may be NULL (then dtype = HLA2_BF16, eps = 1e-6); no workspace is used.
+ * opts->flags may hold HLA2_FLAG_COMPACT_STATE and HLA2_FLAG_UNMASKED (then G and h are
+ * neither read nor written).
  */
 int hla2_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
                      int N, int H, int d, int dv, const float* gamma, int normalize,

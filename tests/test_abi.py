@@ -116,6 +116,23 @@ def test_unknown_flags_rejected(L):
     assert rc == -1
 
 
+def test_unmasked_flag_abi(L):
+    """HLA2_FLAG_UNMASKED is accepted by the forward and the decode step, refused together
+    with SAVE_FOR_BACKWARD (the backward covers the masked output), and bit 16 is unknown."""
+    p = ctypes.c_void_p(16)
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 8)
+    assert L.hla2_forward(p, p, p, p, 0, 1, 16, 16, 16, None, 0, 16, None, ctypes.byref(o)) == 0
+    assert L.hla2_decode_step(p, p, p, p, p, 0, 1, 16, 16, None, 0, None, ctypes.byref(o)) == 0
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 8 | 4)
+    assert L.hla2_decode_step(p, p, p, p, p, 0, 1, 16, 16, None, 0, None, ctypes.byref(o)) == 0
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 8 | 1)
+    rc = L.hla2_forward(p, p, p, p, 1, 1, 16, 16, 16, None, 0, 16, None, ctypes.byref(o))
+    assert rc == -2 and b"masked" in L.hla2_last_error()
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 16)
+    assert L.hla2_forward(p, p, p, p, 0, 1, 16, 16, 16, None, 0, 16, None, ctypes.byref(o)) == -1
+    assert L.hla2_decode_step(p, p, p, p, p, 0, 1, 16, 16, None, 0, None, ctypes.byref(o)) == -1
+
+
 def test_compact_state_abi(L):
     from oracle import hla2_oracle as O
 
