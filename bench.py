@@ -48,10 +48,13 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode and training rows measured after the headline")
-    ap.add_argument("--only", choices=("decode", "decode_compact", "train", "ahla"), default=None,
+    ap.add_argument("--only", choices=("decode", "decode_compact", "decode_unmasked", "train", "ahla", "unmasked"),
+                    default=None,
                     help="measure only this row (for profiler captures; --steps/--warmup apply)")
     ap.add_argument("--decode-seqs", type=int, default=256,
                     help="sequences of the decode row (smaller case for ncu --set full captures)")
+    ap.add_argument("--chunk", type=int, default=None,
+                    help="chunk width of the unmasked row (--only unmasked)")
     ap.add_argument("--n", type=int, default=None,
                     help="override the sequence length (smaller case for ncu --set full captures; "
                          "the reported metric is only valid at the default)")
@@ -276,11 +279,12 @@ def _device_ms(fn, steps, warmup, stream_sync):
 
 
 def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5, seqs: int = 256,
-                   compact: bool = False):
+                   compact: bool = False, masked: bool = True):
     """Decode row: 256 sequences x 32 heads, d = dv = 128, one single-token step per
     iteration on a resident fp32 state (the state's values do not change the work: it
     starts from N(0, 1e-4) draws instead of a 4096-token prefill).  Inputs of every step
-    are drawn before timing (seed 4000 + step); the 1.6 GB state exceeds the L2."""
+    are drawn before timing (seed 4000 + step); the 1.6 GB state exceeds the L2.
+    masked=False: the unmasked output, which reads and writes S, C and m only."""
     import torch
 
     import chunked_scan_mixer_gb300 as hla
@@ -300,15 +304,16 @@ def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int
     def one():
         q, k, v = xs[it[0] % steps]
         it[0] += 1
-        hla.decode_step(state, q, k, v, gamma=gamma, out=out, compact=compact)
+        hla.decode_step(state, q, k, v, gamma=gamma, out=out, compact=compact, masked=masked)
 
     ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
     heads = N * H
-    nbytes = 2 * heads * sf * 4 + heads * (2 * d + dv) * 2 + heads * dv * 2
+    touched = sf if masked else sf - d * dv - d  # the unmasked step leaves G and h alone
+    nbytes = 2 * heads * touched * 4 + heads * (2 * d + dv) * 2 + heads * dv * 2
     achieved = nbytes / (ms * 1e-3) / 1e9
     layout = "compact state (S upper block triangle)" if compact else "packed state"
     return {"workload": f"decode step: {N} sequences x H={H}, d=dv={d}, fp32 {layout}, bf16 q/k/v/out, "
-                        f"decay {w.gamma[0]}, unnormalised",
+                        f"decay {w.gamma[0]}, {'masked' if masked else 'unmasked'}, unnormalised",
             "metric": "decode tokens/s (sequences x heads per second)", "unit": "tokens/s",
             "value": dist.world * heads / (ms * 1e-3), "us_per_step": ms * 1e3, "steps": steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
@@ -393,11 +398,53 @@ def measure_ahla(dev, dist: Dist, hbm_gbs: float, bf16_tflops: float, steps: int
                          "step_tensor_frac": flops / (ms * 1e-3) / 1e12 / bf16_tflops}}
 
 
+def measure_unmasked(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5, n: int | None = None,
+                     chunk: int = 64):
+    """Unmasked-output row: q^T S C on the long-context shapes (B=1 H=16 n=65536 d=dv=64
+    bf16, decay linspace(0.99, 0.9999), unnormalised) through the mma.sync chunk kernel;
+    1,048,576 tokens per step; inputs + output exceed the L2."""
+    import dataclasses
+
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = dataclasses.replace(inputs.WORKLOADS["long"], chunk=chunk)
+    if n is not None:
+        w = dataclasses.replace(w, n=n)
+    x = inputs.make(w, device=dev, seed=replica_seed(w.seed, dist.rank))
+    q, k, v = x["q"], x["k"], x["v"]
+    gamma = x["gamma"].to(dev)
+    out = torch.empty_like(v)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+
+    def one():
+        hla.forward(q, k, v, gamma=gamma, chunk=w.chunk, out=out, masked=False)
+
+    ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
+    hla.forward(q, k, v, gamma=gamma, chunk=w.chunk, out=out, masked=False, phase_events=ev)
+    torch.cuda.synchronize()
+    out_ms = ev[3].elapsed_time(ev[4])
+    tokens = w.B * w.H * w.n
+    nbytes = tokens * (2 * w.d + 2 * w.dv) * 2
+    achieved = nbytes / (out_ms * 1e-3) / 1e9
+    return {"workload": f"unmasked HLA-2 forward (q^T S C): B={w.B} H={w.H} n={w.n} d=dv={w.d} bf16, "
+                        f"decay linspace(0.99,0.9999), unnormalised, chunk {w.chunk}",
+            "metric": "unmasked fwd tokens/s", "unit": "tokens/s", "value": dist.world * tokens / (ms * 1e-3),
+            "ms_per_step": ms, "steps": steps, "output_pass_ms": out_ms,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "kernel": "output_pass", "algorithmic_bytes_per_launch": nbytes}}
+
+
 def run_only(args, dist: Dist, dev):
     hbm_gbs, bf16_tflops, _ = peaks()
-    if args.only in ("decode", "decode_compact"):
+    if args.only in ("decode", "decode_compact", "decode_unmasked"):
         row = measure_decode(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs,
-                             compact=args.only == "decode_compact")
+                             compact=args.only == "decode_compact", masked=args.only != "decode_unmasked")
+    elif args.only == "unmasked":
+        row = measure_unmasked(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n,
+                               chunk=args.chunk or 64)
     elif args.only == "ahla":
         row = measure_ahla(dev, dist, hbm_gbs, bf16_tflops, steps=args.steps, warmup=args.warmup, n=args.n)
     else:
@@ -513,8 +560,10 @@ def run_ours(args, dist: Dist):
     if not args.no_secondary and args.n is None:
         secondary = {"decode": measure_decode(dev, dist, hbm_gbs),
                      "decode_compact": measure_decode(dev, dist, hbm_gbs, compact=True),
+                     "decode_unmasked": measure_decode(dev, dist, hbm_gbs, masked=False),
                      "train": measure_train(dev, dist, bf16_tflops, hbm_gbs),
-                     "ahla": measure_ahla(dev, dist, hbm_gbs, bf16_tflops)}
+                     "ahla": measure_ahla(dev, dist, hbm_gbs, bf16_tflops),
+                     "unmasked": measure_unmasked(dev, dist, hbm_gbs, chunk=64)}
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
