@@ -43,6 +43,10 @@ Readings where the pages leave a step open (each is pinned by a test in
       g^((t-i) + (t-j))), normalised by q_t^T S_t m_t.  Its scan carries only (S, C, m)
       and combines them by decayed addition, with no cross term (the unmasked monoid).
       The state's G and h play no part in it; the unmasked chunked scan reports them as 0.
+  R7  Multi-query sharing ([PS] §5.2: it cuts the state from O(h d^2) to O(d^2 + h d dv)):
+      the heads of a group share the key and the value of each token, so they share S^K (one
+      per group, with one decay per group); C, G, m, h stay per head because they carry each
+      head's own query.
 
 Array conventions: q, k [B, H, n, d]; v, dout [B, H, n, dv]; gamma [H] (None means 1).
 State dict per head: S [B,H,d,d], C [B,H,d,dv], m [B,H,d], G [B,H,d,dv], h [B,H,d].
@@ -64,6 +68,7 @@ __all__ = [
     "unmasked_delta",
     "unmasked_identity",
     "combine_unmasked",
+    "mq_decode_step",
     "serial_backward",
     "serial_backward_normalized",
     "pairsum_grads",
@@ -544,3 +549,49 @@ def state_from_compact(flat, d, dv):
             S[..., a, b] = S[..., b, a]
     return np.concatenate([S.reshape(flat.shape[:-1] + (d * d,)), flat[..., o:]], axis=-1)
 
+
+
+# ---------------------------------------------------------------------------
+# Multi-query sharing of the key moment ([PS] §5.2: with keys shared by a group of heads,
+# S^K is shared and the state is O(d^2 + h d dv) per group; reading R7)
+# ---------------------------------------------------------------------------
+
+def mq_decode_step(S, heads, q_t, k_t, v_t, gamma, group, normalize=False, eps=1e-6, masked=True):
+    """One decode step with one key moment per group of ``group`` query heads (reading R7).
+
+    S [N, Hk, d, d] is shared by the heads g*group .. g*group+group-1 of key group g;
+    heads = {"C": [N,H,d,dv], "G": [N,H,d,dv], "m": [N,H,d], "h": [N,H,d]} with
+    H = Hk * group; q_t [N,H,d]; k_t [N,Hk,d] and v_t [N,Hk,dv] belong to the group;
+    gamma None or [Hk] (one decay per group, since the shared S carries it).
+    Returns (S, heads, o [N,H,dv]); the updates are those of ``step`` with the group's
+    key and value, and S is advanced once per group.
+    """
+    S = np.array(S, dtype=np.float64, copy=True)
+    hs = {key: np.array(val, dtype=np.float64, copy=True) for key, val in heads.items()}
+    q_t = np.asarray(q_t, dtype=np.float64)
+    k_t = np.asarray(k_t, dtype=np.float64)
+    v_t = np.asarray(v_t, dtype=np.float64)
+    N, Hk, d = k_t.shape
+    dv = v_t.shape[-1]
+    g = _gamma(gamma, Hk)
+    out = np.zeros((N, Hk * group, dv))
+    for b in range(N):
+        for j in range(Hk):
+            k, v, gj = k_t[b, j], v_t[b, j], g[j]
+            S[b, j] = gj * S[b, j] + np.outer(k, k)
+            for i in range(group):
+                hh = j * group + i
+                q = q_t[b, hh]
+                C, G, m, h = hs["C"][b, hh], hs["G"][b, hh], hs["m"][b, hh], hs["h"][b, hh]
+                kC, km = k @ C, k @ m                   # pre-update C and m (R1)
+                G = gj * gj * G + gj * np.outer(k, kC)
+                h = gj * gj * h + gj * k * km
+                C = gj * C + np.outer(q, v)
+                m = gj * m + q
+                u = q @ S[b, j]
+                o = u @ C - (q @ G if masked else 0.0)
+                if normalize:
+                    o = o / (u @ m - (q @ h if masked else 0.0) + eps)
+                out[b, hh] = o
+                hs["C"][b, hh], hs["G"][b, hh], hs["m"][b, hh], hs["h"][b, hh] = C, G, m, h
+    return S, hs, out

@@ -635,3 +635,67 @@ def test_unmasked_planted_mistakes_are_caught(monkeypatch):
 
     monkeypatch.setattr(O, "combine_unmasked", c_decay_twice)
     assert rel(O.chunked_scan_forward(q, k, v, [0.9], 3, masked=False), truth) > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# Multi-query sharing of S (reading R7)
+# ---------------------------------------------------------------------------
+
+def _mq_run(q, k, v, gam, group, normalize=False, masked=True, S_step=None):
+    """Stream all tokens through the multi-query decode step from the empty state."""
+    N, Hk, n, d = k.shape
+    H, dv = Hk * group, v.shape[-1]
+    S = np.zeros((N, Hk, d, d))
+    heads = {"C": np.zeros((N, H, d, dv)), "G": np.zeros((N, H, d, dv)), "m": np.zeros((N, H, d)),
+             "h": np.zeros((N, H, d))}
+    step = S_step or O.mq_decode_step
+    outs = []
+    for t in range(n):
+        S, heads, o = step(S, heads, q[:, :, t], k[:, :, t], v[:, :, t], gam, group, normalize, 1e-6, masked)
+        outs.append(o)
+    return np.stack(outs, axis=2), S, heads
+
+
+@pytest.mark.parametrize("masked", [True, False])
+@pytest.mark.parametrize("normalize", [False, True])
+def test_mq_decode_equals_heads_with_broadcast_keys(masked, normalize):
+    """A group sharing one key moment gives exactly the outputs of independent heads that
+    all see the group's key and value: against the pair sum on the broadcast inputs."""
+    group, Hk = 3, 2
+    r = np.random.default_rng(70)
+    q = r.standard_normal((2, Hk * group, 7, 4)) / 2
+    k = r.standard_normal((2, Hk, 7, 4)) / 2
+    v = r.standard_normal((2, Hk, 7, 3))
+    if normalize:
+        q, k = np.abs(q) + 0.1, np.abs(k) + 0.1
+    gam = [0.9, 0.97]
+    o, S, heads = _mq_run(q, k, v, gam, group, normalize, masked)
+    kb, vb = np.repeat(k, group, axis=1), np.repeat(v, group, axis=1)
+    gb = np.repeat(gam, group)
+    ref = O.brute_force_forward(q, kb, vb, gb, normalize=normalize, masked=masked)
+    assert rel(o, ref) < 1e-12
+    _, st = O.serial_forward(q, kb, vb, gb, return_state=True)
+    for j in range(Hk):
+        for i in range(group):
+            assert rel(S[:, j], st["S"][:, j * group + i]) < 1e-13
+    for key in ("C", "G", "m", "h"):
+        assert rel(heads[key], st[key]) < 1e-12
+
+
+def test_mq_planted_mistake_is_caught():
+    """Advancing the shared S once per head instead of once per group is caught."""
+    group, Hk = 2, 1
+    r = np.random.default_rng(71)
+    q = r.standard_normal((1, group, 6, 3))
+    k = r.standard_normal((1, Hk, 6, 3))
+    v = r.standard_normal((1, Hk, 6, 2))
+    ref = O.brute_force_forward(q, np.repeat(k, group, axis=1), np.repeat(v, group, axis=1), [0.9, 0.9])
+
+    def per_head_update(S, heads, q_t, k_t, v_t, gamma, group_, normalize, eps, masked):
+        S2 = S
+        for _ in range(group_ - 1):  # the mistake: one extra update per additional head
+            S2 = 0.9 * S2 + np.einsum("nja,njb->njab", k_t, k_t)
+        return O.mq_decode_step(S2, heads, q_t, k_t, v_t, gamma, group_, normalize, eps, masked)
+
+    bad, _, _ = _mq_run(q, k, v, [0.9], group, S_step=per_head_update)
+    assert rel(bad, ref) > 1e-3
