@@ -48,7 +48,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode and training rows measured after the headline")
-    ap.add_argument("--only", choices=("decode", "decode_compact", "decode_unmasked", "train", "ahla", "unmasked"),
+    ap.add_argument("--only", choices=("decode", "decode_compact", "decode_unmasked", "decode_mq", "train", "ahla",
+                                       "unmasked"),
                     default=None,
                     help="measure only this row (for profiler captures; --steps/--warmup apply)")
     ap.add_argument("--decode-seqs", type=int, default=256,
@@ -320,6 +321,50 @@ def measure_decode(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int
                          "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes}}
 
 
+def measure_decode_mq(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5, seqs: int = 256,
+                      group: int = 4):
+    """Multi-query decode row: the decode row's 256 sequences x 32 query heads, d = dv = 128,
+    with the keys and values shared by groups of 4 heads (8 key groups): one S per group
+    and per-head C, G, m, h, updated in place on a resident state that exceeds the L2."""
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = inputs.WORKLOADS["decode_prefill"]
+    N, H, d, dv = seqs, w.H, w.d, w.dv
+    Hk = H // group
+    hsf = hla.mq_head_state_floats(d, dv)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(replica_seed(w.seed, dist.rank))
+    key_state = torch.randn((N, Hk, d * d), generator=gen, device=dev, dtype=torch.float32) * 1e-2
+    head_state = torch.randn((N, H, hsf), generator=gen, device=dev, dtype=torch.float32) * 1e-2
+    gamma = torch.full((Hk,), w.gamma[0], dtype=torch.float32, device=dev)
+    xs = []
+    for i in range(steps):
+        q, _, _ = inputs.decode_step_inputs(i, N, H, d, dv, w.dtype, device=dev)
+        _, k, v = inputs.decode_step_inputs(10000 + i, N, Hk, d, dv, w.dtype, device=dev)
+        xs.append((q, k, v))
+    out = torch.empty((N, H, dv), dtype=w.dtype, device=dev)
+    it = [0]
+
+    def one():
+        q, k, v = xs[it[0] % steps]
+        it[0] += 1
+        hla.decode_step_mq(key_state, head_state, q, k, v, gamma=gamma, out=out)
+
+    ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
+    heads = N * H
+    nbytes = 2 * (N * Hk * d * d + heads * hsf) * 4 + heads * d * 2 + N * Hk * (d + dv) * 2 + heads * dv * 2
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"multi-query decode step: {N} sequences x H={H} query heads in {Hk} key groups, d=dv={d}, "
+                        f"fp32 state (S per group), bf16 q/k/v/out, decay {w.gamma[0]}, masked, unnormalised",
+            "metric": "decode tokens/s (sequences x query heads per second)", "unit": "tokens/s",
+            "value": dist.world * heads / (ms * 1e-3), "us_per_step": ms * 1e3, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes}}
+
+
 def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: int = 10, warmup: int = 3):
     """Training row: B=4 H=16 n=8192 d=dv=128 bf16, decay 0.995, unnormalised; one step =
     forward (keeping the chunk states for the backward) + backward (dq, dk, dv) through the
@@ -442,6 +487,8 @@ def run_only(args, dist: Dist, dev):
     if args.only in ("decode", "decode_compact", "decode_unmasked"):
         row = measure_decode(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs,
                              compact=args.only == "decode_compact", masked=args.only != "decode_unmasked")
+    elif args.only == "decode_mq":
+        row = measure_decode_mq(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs)
     elif args.only == "unmasked":
         row = measure_unmasked(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n,
                                chunk=args.chunk or 64)
@@ -561,6 +608,7 @@ def run_ours(args, dist: Dist):
         secondary = {"decode": measure_decode(dev, dist, hbm_gbs),
                      "decode_compact": measure_decode(dev, dist, hbm_gbs, compact=True),
                      "decode_unmasked": measure_decode(dev, dist, hbm_gbs, masked=False),
+                     "decode_mq": measure_decode_mq(dev, dist, hbm_gbs),
                      "train": measure_train(dev, dist, bf16_tflops, hbm_gbs),
                      "ahla": measure_ahla(dev, dist, hbm_gbs, bf16_tflops),
                      "unmasked": measure_unmasked(dev, dist, hbm_gbs, chunk=64)}

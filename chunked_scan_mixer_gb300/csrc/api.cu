@@ -779,6 +779,34 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
     return succeed();
 }
 
+int hla2_decode_step_mq(float* key_state, float* head_state, const void* q, const void* k, const void* v,
+                        void* out, int N, int Hk, int group, int d, int dv, const float* gamma, int normalize,
+                        hla2_stream_t stream, const hla2_opts* opts) {
+    const int dtype = opts ? opts->dtype : HLA2_BF16;
+    const float eps = opts ? opts->eps : 1e-6f;
+    const int flags = opts ? opts->flags : 0;
+    int rc = check_common(N, Hk, 0, d, dv, dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (group < 1 || group > 8) return fail(HLA2_ERR_INVALID_ARG, "group must be 1 to 8 query heads per key (got %d)", group);
+    if (normalize && !isfinite(eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
+    if (flags & HLA2_FLAG_COMPACT_STATE)
+        return fail(HLA2_ERR_UNSUPPORTED, "the multi-query step keeps the shared S in the packed layout");
+    if (flags & ~HLA2_FLAG_UNMASKED) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_decode_step_mq");
+    if ((long)N * Hk == 0) return succeed();
+    if (!key_state || !head_state || !q || !k || !v || !out)
+        return fail(HLA2_ERR_INVALID_ARG, "state, q, k, v, out must not be NULL");
+    if (!aligned16(key_state) || !aligned16(head_state) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(out))
+        return fail(HLA2_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    cudaGetLastError();
+    if (launch_decode_mq(key_state, head_state, q, k, v, out, N, Hk, group, d, dv, gamma, normalize, eps,
+                         dtype == HLA2_BF16, (flags & HLA2_FLAG_UNMASKED) != 0, reinterpret_cast<cudaStream_t>(stream)))
+        return cuda_fail("multi-query decode step");
+    return succeed();
+}
+
+size_t hla2_mq_head_state_floats(int d, int dv) { return 2 * (size_t)d * dv + 2 * (size_t)d; }
+
 size_t hla2_compact_state_floats(int d, int dv) { return compact_state_floats(d, dv); }
 
 size_t hla2_ahla_state_floats(int d, int dv) { return ahla_state_floats(d, dv); }

@@ -12,6 +12,8 @@
 // The unmasked output (section summary §3: q^T S' C', denominator u . m') needs neither
 // G nor h: that variant skips pass G and the h update and leaves both untouched, so its
 // state traffic is S, C and m only.
+#include <cooperative_groups.h>
+
 #include "kernels.h"
 
 namespace hla2 {
@@ -25,6 +27,7 @@ constexpr int kMaxDim = 128;
 __device__ __forceinline__ float4 ld_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ void st_stream(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
 
+template <int NT = kThreads>
 __device__ __forceinline__ float block_sum(float x, float* red) {
     for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -33,13 +36,14 @@ __device__ __forceinline__ float block_sum(float x, float* red) {
     __syncthreads();
     float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) s += red[w];
+    for (int w = 0; w < NT / 32; ++w) s += red[w];
     return s;
 }
 
 // Column sums of a d x dv pass: each thread holds partial sums for 4 columns
 // (column group tid % (dv/4)); combine threads that share a column group.
-__device__ __forceinline__ void column_reduce(float4 p, int dv, float* red /*[kWarps][kMaxDim]*/,
+template <int NT = kThreads>
+__device__ __forceinline__ void column_reduce(float4 p, int dv, float* red /*[NT / 32][kMaxDim]*/,
                                               float* result /*[dv]*/) {
     const int lpc = dv / 4;  // lanes per row (<= 32, power of two)
     for (int o = lpc; o < 32; o <<= 1) {
@@ -51,10 +55,10 @@ __device__ __forceinline__ void column_reduce(float4 p, int dv, float* red /*[kW
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane < lpc) *reinterpret_cast<float4*>(&red[warp * kMaxDim + lane * 4]) = p;
     __syncthreads();
-    for (int c = threadIdx.x; c < dv; c += kThreads) {
+    for (int c = threadIdx.x; c < dv; c += NT) {
         float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += red[w * kMaxDim + c];
+        for (int w = 0; w < NT / 32; ++w) s += red[w * kMaxDim + c];
         result[c] = s;
     }
     __syncthreads();
@@ -88,6 +92,7 @@ __global__ void __launch_bounds__(kThreads)
     if (!UM) {
         for (int i = tid; i < d; i += kThreads) km += ks[i] * m[i];
         km = block_sum(km, red);
+        __syncthreads();  // every warp has read red before pass S may reuse it
     }
     float mh_dot = 0.f;  // this thread's part of u . m' - q . h', formed after pass S
 
@@ -384,6 +389,177 @@ __global__ void __launch_bounds__(kThreads) state_from_compact_kernel(const floa
     for (size_t i = threadIdx.x; i < tail; i += kThreads) dst[fs + i] = src[cs + i];
 }
 
+// Decode step with multi-query sharing (section summary §5.2: one key moment per group of
+// query heads, state O(d^2 + h d dv) per group).  One CTA per query head; the `group` CTAs
+// of a key group form a thread-block cluster.  Each CTA advances one block of rows of the
+// group's S, so S is streamed once per group:
+//   pass S (rows a of this CTA's block):  S'[a] = g S[a] + k_a k^T,  u_i[a] = S'[a] . q_i
+// for every head i of the group (u = S' q; S' is symmetric).  The row blocks of u are then
+// gathered through distributed shared memory, and each CTA streams its own head's C and G
+// as the single-head step does, with the group's k and v.  With one CTA per head the grid
+// is as large as the single-head step's (8192 CTAs for 256 sequences x 32 heads), which
+// keeps the waves short; one CTA per group (2048) ran 1.7 waves with the last one two-thirds
+// full.  key_state [N*Hk][d*d]; head_state [N*Hk*group][C | G | m | h].
+constexpr int kMaxGroup = 8;
+
+template <typename T, bool UM>
+__global__ void __launch_bounds__(kThreads)
+    decode_mq_kernel(float* __restrict__ key_state, float* __restrict__ head_state, const T* __restrict__ q,
+                     const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ out, int Hk, int group,
+                     int d, int dv, const float* __restrict__ gamma, int normalize, float eps) {
+    __shared__ __align__(16) float qs[kMaxGroup][kMaxDim], us[kMaxGroup][kMaxDim];
+    __shared__ __align__(16) float ks[kMaxDim], vs[kMaxDim], uo[kMaxDim], rs[kMaxDim], ws[kMaxDim], zs[kMaxDim];
+    __shared__ __align__(16) float red[kWarps * kMaxDim];
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x;
+    const int head = blockIdx.x;           // query head (sequence-major)
+    const int grp = head / group;          // its key group
+    const int r = (int)cluster.block_rank();  // == head % group
+    const float g = head_decay(gamma, grp, Hk), g2 = g * g;
+    float* S = key_state + (size_t)grp * d * d;
+
+    for (int i = tid; i < d; i += kThreads) ks[i] = to_f32(k[(size_t)grp * d + i]);
+    for (int i = tid; i < dv; i += kThreads) vs[i] = to_f32(v[(size_t)grp * dv + i]);
+    for (int i = tid; i < group * d; i += kThreads) qs[i / d][i % d] = to_f32(q[(size_t)grp * group * d + i]);
+    __syncthreads();
+
+    // ---- pass S over this CTA's rows [lo, hi) ----------------------------------------------
+    {
+        const int lo = r * d / group, hi = (r + 1) * d / group;
+        const int lpr = d / 4;  // lanes per row; a warp holds 32 / lpr whole rows
+        const int rows_per = kThreads / lpr;
+        const int c4 = (tid % lpr) * 4;
+        const int iters = (hi - lo + rows_per * 4 - 1) / (rows_per * 4);  // the same for every thread
+        for (int it = 0; it < iters; ++it) {
+            const int a0 = lo + it * rows_per * 4 + tid / lpr;
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a < hi) x[u] = ld_stream(S + (size_t)a * d + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                const bool ok = a < hi;
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (ok) {
+                    const float ka = ks[a];
+                    y = x[u];
+                    y.x = g * y.x + ka * ks[c4 + 0];
+                    y.y = g * y.y + ka * ks[c4 + 1];
+                    y.z = g * y.z + ka * ks[c4 + 2];
+                    y.w = g * y.w + ka * ks[c4 + 3];
+                    st_stream(S + (size_t)a * d + c4, y);
+                }
+                for (int i = 0; i < group; ++i) {  // every lane takes part in the shuffles
+                    float part = y.x * qs[i][c4] + y.y * qs[i][c4 + 1] + y.z * qs[i][c4 + 2] + y.w * qs[i][c4 + 3];
+                    for (int o = lpr >> 1; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                    if (ok && (tid % lpr) == 0) us[i][a] = part;
+                }
+            }
+        }
+    }
+    // The other CTAs' row blocks of u are read after the cluster barrier; its arrival is
+    // split from the wait so that the m and h updates fill the gap.
+    auto arrived = cluster.barrier_arrive();
+
+    // ---- this head: m, h, pass C, pass G, output ----------------------------------------------
+    const size_t hsf = 2 * (size_t)d * dv + 2 * (size_t)d;
+    float* C = head_state + (size_t)head * hsf;
+    float* G = C + (size_t)d * dv;
+    float* m = G + (size_t)d * dv;
+    float* hh = m + d;
+    const float* qi = qs[r];
+    float km = 0.f;
+    if (!UM) {
+        for (int a = tid; a < d; a += kThreads) km += ks[a] * m[a];
+        km = block_sum(km, red);
+        __syncthreads();  // every warp has read red before pass C reuses it
+    }
+    float mh_dot = 0.f;  // q . (S' m' - h') = u . m' - q . h'; the u part once u is here
+    for (int a = tid; a < d; a += kThreads) {
+        const float mn = g * m[a] + qi[a];
+        m[a] = mn;
+        if (!UM) {
+            const float hn = g2 * hh[a] + g * ks[a] * km;
+            hh[a] = hn;
+            mh_dot -= qi[a] * hn;
+        }
+    }
+    cluster.barrier_wait(std::move(arrived));
+    for (int a = tid; a < d; a += kThreads) {
+        int owner = 0;
+        while (owner + 1 < group && (owner + 1) * d / group <= a) ++owner;
+        const float* src = cluster.map_shared_rank(&us[0][0], owner);
+        uo[a] = src[r * kMaxDim + a];
+        mh_dot += uo[a] * m[a];  // m[a] was written by this thread above
+    }
+    auto gathered = cluster.barrier_arrive();  // this CTA's reads of the others are done
+    __syncthreads();
+    const int lpc = dv / 4;
+    const int rows_per = kThreads / lpc;
+    const int c4 = (tid % lpc) * 4;
+    {  // pass C
+        float4 pr = make_float4(0.f, 0.f, 0.f, 0.f), pw = pr;
+        for (int a0 = tid / lpc; a0 < d; a0 += rows_per * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a < d) x[u] = ld_stream(C + (size_t)a * dv + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a >= d) continue;
+                const float ka = ks[a], qa = qi[a], ua = uo[a];
+                float4 y = x[u];
+                if (!UM) { pr.x += ka * y.x; pr.y += ka * y.y; pr.z += ka * y.z; pr.w += ka * y.w; }
+                y.x = g * y.x + qa * vs[c4 + 0];
+                y.y = g * y.y + qa * vs[c4 + 1];
+                y.z = g * y.z + qa * vs[c4 + 2];
+                y.w = g * y.w + qa * vs[c4 + 3];
+                pw.x += ua * y.x; pw.y += ua * y.y; pw.z += ua * y.z; pw.w += ua * y.w;
+                st_stream(C + (size_t)a * dv + c4, y);
+            }
+        }
+        if (!UM) column_reduce(pr, dv, red, rs);
+        column_reduce(pw, dv, red, ws);
+    }
+    if (!UM) {  // pass G
+        float4 pz = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 r4 = *reinterpret_cast<const float4*>(&rs[c4]);
+        for (int a0 = tid / lpc; a0 < d; a0 += rows_per * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a < d) x[u] = ld_stream(G + (size_t)a * dv + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a >= d) continue;
+                const float gk = g * ks[a], qa = qi[a];
+                float4 y = x[u];
+                y.x = g2 * y.x + gk * r4.x;
+                y.y = g2 * y.y + gk * r4.y;
+                y.z = g2 * y.z + gk * r4.z;
+                y.w = g2 * y.w + gk * r4.w;
+                pz.x += qa * y.x; pz.y += qa * y.y; pz.z += qa * y.z; pz.w += qa * y.w;
+                st_stream(G + (size_t)a * dv + c4, y);
+            }
+        }
+        column_reduce(pz, dv, red, zs);
+    }
+    float inv = 1.f;
+    if (normalize) inv = 1.f / (block_sum(mh_dot, red) + eps);
+    for (int e = tid; e < dv; e += kThreads) out[(size_t)head * dv + e] = from_f32<T>((UM ? ws[e] : ws[e] - zs[e]) * inv);
+    cluster.barrier_wait(std::move(gathered));  // no CTA leaves while another may still read it
+}
+
 template <bool COMPACT, bool UM>
 void launch_decode_t(float* state, const void* q, const void* k, const void* v, void* out, long heads, int H, int d,
                      int dv, const float* gamma, int normalize, float eps, bool is_bf16, cudaStream_t st) {
@@ -412,6 +588,43 @@ int launch_decode_step(float* state, const void* q, const void* k, const void* v
         launch_decode_t<false, true>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
     else
         launch_decode_t<false, false>(state, q, k, v, out, heads, H, d, dv, gamma, normalize, eps, is_bf16, st);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_decode_mq(float* key_state, float* head_state, const void* q, const void* k, const void* v, void* out,
+                     int N, int Hk, int group, int d, int dv, const float* gamma, int normalize, float eps,
+                     bool is_bf16, bool unmasked, cudaStream_t st) {
+    const long heads = (long)N * Hk * group;
+    if (heads <= 0) return 0;
+    if (group < 1 || group > kMaxGroup) return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)heads);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)group;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+#define HLA2_MQ(T, UMV)                                                                                  \
+    e = cudaLaunchKernelEx(&cfg, decode_mq_kernel<T, UMV>, key_state, head_state, static_cast<const T*>(q), \
+                           static_cast<const T*>(k), static_cast<const T*>(v), static_cast<T*>(out), Hk, group, d, \
+                           dv, gamma, normalize, eps)
+    if (is_bf16 && unmasked) {
+        HLA2_MQ(bf16, true);
+    } else if (is_bf16) {
+        HLA2_MQ(bf16, false);
+    } else if (unmasked) {
+        HLA2_MQ(float, true);
+    } else {
+        HLA2_MQ(float, false);
+    }
+#undef HLA2_MQ
+    if (e != cudaSuccess) return -1;
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -153,6 +153,11 @@ int launch_finalize(const ChunkArgs& a, int d, int dv, float* final_state, cudaS
 int launch_decode_step(float* state, const void* q, const void* k, const void* v, void* out,
                        int N, int H, int d, int dv, const float* gamma, int normalize, float eps,
                        bool is_bf16, bool compact, bool unmasked, cudaStream_t st);
+// Multi-query decode: key_state [N*Hk][d*d], head_state [N*Hk*group][2 d dv + 2 d] (C | G | m | h);
+// q [N*Hk*group][d], k [N*Hk][d], v [N*Hk][dv]; gamma NULL or [Hk]; 1 <= group <= 8.
+int launch_decode_mq(float* key_state, float* head_state, const void* q, const void* k, const void* v, void* out,
+                     int N, int Hk, int group, int d, int dv, const float* gamma, int normalize, float eps,
+                     bool is_bf16, bool unmasked, cudaStream_t st);
 int launch_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
                             int d, int dv, const float* gamma, int normalize, float eps, bool is_bf16,
                             cudaStream_t st);

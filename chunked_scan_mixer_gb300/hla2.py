@@ -107,6 +107,10 @@ def lib():
         L.hla2_ahla_decode_step.restype = I
         L.hla2_compact_state_floats.argtypes = [I, I]
         L.hla2_compact_state_floats.restype = Z
+        L.hla2_mq_head_state_floats.argtypes = [I, I]
+        L.hla2_mq_head_state_floats.restype = Z
+        L.hla2_decode_step_mq.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P, ctypes.POINTER(Opts)]
+        L.hla2_decode_step_mq.restype = I
         for name in ("hla2_state_to_compact", "hla2_state_from_compact"):
             getattr(L, name).argtypes = [P, P, I, I, I, I, P]
             getattr(L, name).restype = I
@@ -119,7 +123,7 @@ EXPORTED_SYMBOLS = (
     "hla2_forward", "hla2_forward_plan", "hla2_workspace_status", "hla2_backward_workspace_bytes",
     "hla2_backward", "hla2_decode_step", "hla2_forward_noalloc", "hla2_compact_state_floats",
     "hla2_state_to_compact", "hla2_state_from_compact", "hla2_ahla_forward_workspace_bytes", "hla2_ahla_forward",
-    "hla2_ahla_state_floats", "hla2_ahla_decode_step",
+    "hla2_ahla_state_floats", "hla2_ahla_decode_step", "hla2_mq_head_state_floats", "hla2_decode_step_mq",
 )
 
 FLAG_COMPACT_STATE = 4
@@ -466,4 +470,54 @@ def decode_step(state, q, k, v, gamma=None, normalize=False, eps=1e-6, out=None,
     rc = L.hla2_decode_step(_ptr(state), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), N, H, d, dv, _ptr(g),
                             int(normalize), _stream_handle(device), ctypes.byref(opts))
     _check("hla2_decode_step", rc)
+    return o
+
+
+def mq_head_state_floats(d, dv):
+    """Floats of one head's part of the multi-query state: C | G | m | h."""
+    return int(lib().hla2_mq_head_state_floats(d, dv))
+
+
+def mq_split_state(state, d, dv, group):
+    """Packed per-head states [N, H, state_floats(d, dv)] whose heads share S within groups of
+    ``group`` (e.g. a forward's final state on keys repeated over each group's heads) ->
+    (key_state [N, H/group, d*d], head_state [N, H, mq_head_state_floats(d, dv)]).  S is
+    taken from each group's first head; a layout copy only (the packed order is
+    S | C | G | m | h, so a head's part is the tail after S)."""
+    N, H, sf = state.shape
+    if sf != state_floats(d, dv) or H % group:
+        raise ValueError("state must be [N, H, state_floats(d, dv)] with H a multiple of group")
+    return state[:, ::group, :d * d].contiguous(), state[:, :, d * d:].contiguous()
+
+
+def mq_merge_state(key_state, head_state, d, dv):
+    """Inverse of mq_split_state: packed per-head states with each group's S repeated."""
+    N, Hk, _ = key_state.shape
+    H = head_state.shape[1]
+    S = key_state.repeat_interleave(H // Hk, dim=1)
+    return torch.cat([S, head_state], dim=-1).contiguous()
+
+
+def decode_step_mq(key_state, head_state, q, k, v, gamma=None, normalize=False, eps=1e-6, out=None, masked=True):
+    """One decode step with one key moment per key group (multi-query sharing).
+    key_state [N,Hk,d*d] and head_state [N,H,mq_head_state_floats(d, dv)] float32 on the GPU
+    are updated in place; q [N,H,d] with H = Hk * group; k [N,Hk,d]; v [N,Hk,dv];
+    gamma None, a scalar or [Hk].  Returns out [N,H,dv]."""
+    L = lib()
+    for t in (key_state, head_state):
+        if t.device.type != "cuda" or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("states must be contiguous float32 CUDA tensors")
+    device = key_state.device
+    N, H, d = q.shape
+    Hk, dv = k.shape[1], v.shape[-1]
+    if H % Hk:
+        raise ValueError("the query heads must be a multiple of the key heads")
+    group = H // Hk
+    qd, kd, vd = (_to_device(t, device) for t in (q, k, v))
+    g = _gamma_tensor(gamma, Hk, device)
+    o = out if out is not None else torch.empty((N, H, dv), dtype=q.dtype, device=device)
+    opts = Opts(_DTYPES[q.dtype], float(eps), None, 0, None, None, None, 0, 0 if masked else FLAG_UNMASKED)
+    rc = L.hla2_decode_step_mq(_ptr(key_state), _ptr(head_state), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), N, Hk,
+                               group, d, dv, _ptr(g), int(normalize), _stream_handle(device), ctypes.byref(opts))
+    _check("hla2_decode_step_mq", rc)
     return o

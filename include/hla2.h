@@ -196,6 +196,27 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
                      int N, int H, int d, int dv, const float* gamma, int normalize,
                      hla2_stream_t stream, const hla2_opts* opts);
 
+/* Floats in one head's part of the multi-query state: C d*dv | G d*dv | m d | h d. */
+size_t hla2_mq_head_state_floats(int d, int dv);
+
+/*
+ * Decode step with multi-query sharing of the key moment (section summary §5.2: sharing
+ * cuts the state from O(h d^2) to O(d^2 + h d dv)).  The `group` query heads of each key
+ * group share the token's key and value, hence one S per group; C, G, m, h stay per head.
+ * key_state [N, Hk] blocks of S (d*d float32, packed), head_state [N, Hk*group] blocks of
+ * hla2_mq_head_state_floats(d, dv) float32 -- both updated in place; q [N, Hk*group, d]
+ * (the heads of key group j are j*group .. j*group+group-1); k [N, Hk, d]; v [N, Hk, dv];
+ * out [N, Hk*group, dv]; gamma NULL or [Hk] (one decay per group, since S carries it).
+ * 1 <= group <= 8.  The result equals hla2_decode_step on heads whose k and v are the
+ * group's and whose S blocks are the group's S.  opts may be NULL; opts->flags may hold
+ * HLA2_FLAG_UNMASKED; HLA2_FLAG_COMPACT_STATE gives HLA2_ERR_UNSUPPORTED.  One CTA per
+ * query head; the CTAs of a key group form a cluster that streams the group's S once (a
+ * block of rows each) and shares u = S' q through distributed shared memory; no workspace.
+ */
+int hla2_decode_step_mq(float* key_state, float* head_state, const void* q, const void* k, const void* v,
+                        void* out, int N, int Hk, int group, int d, int dv, const float* gamma, int normalize,
+                        hla2_stream_t stream, const hla2_opts* opts);
+
 /*
  * Asymmetric HLA (AHLA, technical summary item "2. Asymmetrische Lineare Aufmerksamkeit
  * hoeherer Ordnung"; section summary §6): the masked left-cascaded product

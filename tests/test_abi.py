@@ -133,6 +133,23 @@ def test_unmasked_flag_abi(L):
     assert L.hla2_decode_step(p, p, p, p, p, 0, 1, 16, 16, None, 0, None, ctypes.byref(o)) == -1
 
 
+def test_multi_query_decode_abi(L):
+    """hla2_decode_step_mq: group 1..8, no compact flag, head-state size C | G | m | h."""
+    p = ctypes.c_void_p(16)
+    assert L.hla2_mq_head_state_floats(128, 64) == 2 * 128 * 64 + 2 * 128
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 0)
+    for group in (0, 9):
+        rc = L.hla2_decode_step_mq(p, p, p, p, p, p, 1, 1, group, 16, 16, None, 0, None, ctypes.byref(o))
+        assert rc == -1 and b"group" in L.hla2_last_error()
+    assert L.hla2_decode_step_mq(p, p, p, p, p, p, 0, 4, 4, 16, 16, None, 0, None, ctypes.byref(o)) == 0
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 4)
+    assert L.hla2_decode_step_mq(p, p, p, p, p, p, 1, 1, 2, 16, 16, None, 0, None, ctypes.byref(o)) == -2
+    o = Opts(1, 1e-6, None, 0, None, None, None, 0, 8)
+    assert L.hla2_decode_step_mq(p, p, p, p, p, p, 0, 1, 2, 16, 16, None, 0, None, ctypes.byref(o)) == 0
+    rc = L.hla2_decode_step_mq(None, p, p, p, p, p, 1, 1, 2, 16, 16, None, 0, None, ctypes.byref(o))
+    assert rc == -1
+
+
 def test_compact_state_abi(L):
     from oracle import hla2_oracle as O
 
