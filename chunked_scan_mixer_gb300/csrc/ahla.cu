@@ -339,18 +339,20 @@ __global__ void __launch_bounds__(AhlaCfg<D, W>::NT) ahla_chunk_kernel(const Ahl
 
 constexpr int kScanThreads = 256;
 
-// Carries into segment 0 are zero; clears the status word.
+// Carries into segment 0: the initial state [P | E | m | n] (zero without one); clears the
+// status word.  The scans then seed every later carry from these.
 __global__ void __launch_bounds__(kScanThreads) ahla_init_kernel(const AhlaArgs a, int D) {
     const int bh = blockIdx.x, tid = threadIdx.x;
     if (bh == 0 && tid == 0) *reinterpret_cast<int*>(a.ws) = 0;
     const size_t c0 = (size_t)bh * a.nseg;
+    const float* init = a.init_state ? a.init_state + (size_t)bh * ahla_state_floats(D, D) : nullptr;
     for (int i = tid; i < D * D; i += kScanThreads) {
-        a.ws[a.L.Pin + c0 * D * D + i] = 0.f;
-        a.ws[a.L.Ein + c0 * D * D + i] = 0.f;
+        a.ws[a.L.Pin + c0 * D * D + i] = init ? init[i] : 0.f;
+        a.ws[a.L.Ein + c0 * D * D + i] = init ? init[(size_t)D * D + i] : 0.f;
     }
     for (int i = tid; i < D; i += kScanThreads) {
-        a.ws[a.L.min + c0 * D + i] = 0.f;
-        a.ws[a.L.nin + c0 * D + i] = 0.f;
+        a.ws[a.L.min + c0 * D + i] = init ? init[2 * (size_t)D * D + i] : 0.f;
+        a.ws[a.L.nin + c0 * D + i] = init ? init[2 * (size_t)D * D + D + i] : 0.f;
     }
 }
 

@@ -868,17 +868,21 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
     if (rc != HLA2_OK) return rc;
     if (normalize && !isfinite(opts->eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
     if (opts->flags) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_ahla_forward");
-    if (opts->init_state) return fail(HLA2_ERR_UNSUPPORTED, "the AHLA forward takes no init_state");
     const bool want_final = opts->final_state != nullptr;
+    if (opts->init_state && !aligned16(opts->init_state))
+        return fail(HLA2_ERR_INVALID_ARG, "init_state must be 16-byte aligned");
     if (want_final && chunk == 128)
         return fail(HLA2_ERR_UNSUPPORTED, "the AHLA final state comes from the chunk 32 / 64 kernels");
     if (want_final && !aligned16(opts->final_state))
         return fail(HLA2_ERR_INVALID_ARG, "final_state must be 16-byte aligned");
     const long BH = (long)B * H;
     if (BH == 0) return succeed();
-    if (n == 0) {  // no tokens: the empty state
-        if (want_final && cudaMemsetAsync(opts->final_state, 0, BH * ahla_state_floats(d, dv) * sizeof(float),
-                                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    if (n == 0) {  // no tokens: the final state is the initial one (or the empty state)
+        const size_t bytes = BH * ahla_state_floats(d, dv) * sizeof(float);
+        cudaStream_t s0 = reinterpret_cast<cudaStream_t>(stream);
+        if (want_final && (opts->init_state ? cudaMemcpyAsync(opts->final_state, opts->init_state, bytes,
+                                                              cudaMemcpyDeviceToDevice, s0)
+                                            : cudaMemsetAsync(opts->final_state, 0, bytes, s0)) != cudaSuccess)
             return cuda_fail("final state");
         return succeed();
     }
@@ -912,6 +916,7 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
     a.ws = static_cast<float*>(opts->workspace);
     a.L = L;
     a.final_state = opts->final_state;
+    a.init_state = opts->init_state;
     const bool den_terms = normalize || want_final;  // m, n carried
     auto mark = [&](int i) {
         if (opts->phase_events && i < opts->n_phase_events && opts->phase_events[i] &&

@@ -32,7 +32,7 @@ inline AhlaLayout ahla_layout(const Plan& p) {
 }
 
 // AHLA streaming state of one head: P d*dv | E d*dv | m d | n d.
-inline size_t ahla_state_floats(int d, int dv) { return 2 * (size_t)d * dv + 2 * (size_t)d; }
+__host__ __device__ inline size_t ahla_state_floats(int d, int dv) { return 2 * (size_t)d * dv + 2 * (size_t)d; }
 
 // Arguments of one AHLA chunk-kernel launch.
 struct AhlaArgs {
@@ -47,6 +47,7 @@ struct AhlaArgs {
     float* ws;
     AhlaLayout L;
     float* final_state;  // nullable: [BH][2 d dv + 2 d] = P | E | m | n after token n
+    const float* init_state;  // nullable: the same layout, the state before token 0
 };
 int launch_ahla_chunk(const AhlaArgs& a, int d, int W, bool summary, cudaStream_t st);
 int launch_ahla_init(const AhlaArgs& a, int d, cudaStream_t st);

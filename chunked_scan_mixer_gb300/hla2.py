@@ -361,11 +361,12 @@ def ahla_state_floats(d, dv):
 
 
 def ahla_forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, out=None, phase_events=None,
-                 return_final_state=False):
+                 return_final_state=False, init_state=None):
     """Asymmetric HLA forward (the masked left-cascaded product Q (K^T Q)(K^T V)).
     bf16 q, k, v [B,H,n,d] on the GPU (d == dv); chunk 32 or 64 (or 128 at d = 64,
     unnormalised).  Returns out [B,H,n,d] (and, with return_final_state, the state
-    [B,H,ahla_state_floats] = P | E | m | n after the last token; chunk 32 / 64)."""
+    [B,H,ahla_state_floats] = P | E | m | n after the last token; chunk 32 / 64).
+    init_state: a state in that layout to continue from."""
     L = lib()
     if q.device.type != "cuda" or q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must be bfloat16 CUDA tensors")
@@ -382,8 +383,13 @@ def ahla_forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, out=N
     ws = _workspace(int(nbytes), device, sh)
     fin = torch.empty((B, H, ahla_state_floats(d, dv)), dtype=torch.float32, device=device) \
         if return_final_state else None
-    opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), int(nbytes), None,
-                None if fin is None else fin.data_ptr(), None, 0, 0)
+    init = None
+    if init_state is not None:
+        init = init_state.to(device=device, dtype=torch.float32).contiguous()
+        if init.shape != (B, H, ahla_state_floats(d, dv)):
+            raise ValueError("init_state must be [B, H, ahla_state_floats(d, dv)]")
+    opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), int(nbytes),
+                None if init is None else init.data_ptr(), None if fin is None else fin.data_ptr(), None, 0, 0)
     if phase_events:
         for e in phase_events:
             if not e.cuda_event:

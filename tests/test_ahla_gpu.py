@@ -183,3 +183,31 @@ def test_final_state_with_chunk_128_is_rejected():
     x = inputs.make_custom(1, 1, 64, 64, 64, torch.bfloat16, seed=32)
     with pytest.raises(HLA2Error):
         hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), chunk=128, return_final_state=True)
+
+
+@pytest.mark.parametrize("chunk", [32, 64, 128])
+@pytest.mark.parametrize("normalize", [False, True])
+def test_continuation_from_init_state(chunk, normalize):
+    """A forward over [m, n) from the GPU state after [0, m) equals the oracle run over all
+    of [0, n), on every AHLA kernel (chunk 128 is the tcgen05 one)."""
+    if normalize and chunk == 128:
+        pytest.skip("the tcgen05 kernel is unnormalised")
+    N, H, d, n, m = 2, 4, 64, 900, 333
+    x = inputs.make_custom(N, H, n, d, d, torch.bfloat16, seed=33 + chunk, gamma=(0.99, 0.999),
+                           qk="softplus" if normalize else "gauss", v_scale="unit" if normalize else "gauss_sqrt_d")
+    g = x["gamma"].cuda()
+    q, k, v = (x[key].cuda() for key in ("q", "k", "v"))
+    _, fin = hla.ahla_forward(q[:, :, :m].contiguous(), k[:, :, :m].contiguous(), v[:, :, :m].contiguous(), gamma=g,
+                              chunk=64, normalize=normalize, return_final_state=True)
+    o2 = hla.ahla_forward(q[:, :, m:].contiguous(), k[:, :, m:].contiguous(), v[:, :, m:].contiguous(), gamma=g,
+                          chunk=chunk, normalize=normalize, init_state=fin)
+    ref = A.serial_forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), x["gamma"].double().numpy(), normalize=normalize)
+    assert rel_err(np64(o2.cpu()), ref[:, :, m:]) <= 2e-2
+
+
+def test_empty_sequence_passes_init_state_through():
+    x = inputs.make_custom(1, 2, 0, 32, 32, torch.bfloat16, seed=34)
+    init = torch.randn(1, 2, hla.ahla_state_floats(32, 32), device="cuda")
+    _, fin = hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), chunk=32, init_state=init,
+                              return_final_state=True)
+    assert torch.equal(fin, init)
