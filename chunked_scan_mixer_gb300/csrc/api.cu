@@ -484,7 +484,7 @@ struct BwdLayout {
     size_t total_bytes;
 };
 
-BwdLayout bwd_layout(const Plan& p) {
+BwdLayout bwd_layout(const Plan& p, size_t state_elem = sizeof(bf16)) {
     BwdLayout L;
     L.F = fwd_layout(p, p.nseg);
     const size_t BH = p.BH, ns = p.nseg, dd = (size_t)p.d * p.d, ddv = (size_t)p.d * p.dv;
@@ -494,8 +494,43 @@ BwdLayout bwd_layout(const Plan& p) {
     L.Zh_end = o; o = align64(o + BH * ns * ddv);
     L.Sh_end = o; o = align64(o + BH * ns * dd);
     L.states_bytes_off = o * sizeof(float);
-    L.total_bytes = L.states_bytes_off + BH * (size_t)p.nchunks * (dd + ddv) * sizeof(bf16);
+    L.total_bytes = L.states_bytes_off + BH * (size_t)p.nchunks * (dd + ddv) * state_elem;
     return L;
+}
+
+// The fp32 backward (SIMT kernels) runs at the largest width <= min(chunk, 32) whose forward
+// and reverse kernels fit in shared memory.
+int backward_width_f32(int d, int dv, int chunk, const DevInfo& di) {
+    for (int W = chunk < 32 ? chunk : 32; W >= 16; W /= 2)
+        if (bwd_chunk_simt_smem(d, dv, W) <= (size_t)di.smem_optin &&
+            fwd_chunk_simt_smem(d, dv, W, true) <= (size_t)di.smem_optin)
+            return W;
+    return 0;
+}
+
+int backward_per_sm_f32(int d, int dv, int W, const DevInfo& di) {
+    const int b = blocks_per_sm(bwd_chunk_simt_smem(d, dv, W), 256, 4, di);
+    const int f = blocks_per_sm(fwd_chunk_simt_smem(d, dv, W, false), 256, 4, di);
+    return b < f ? b : f;
+}
+
+// Width, segmentation and workspace of an unnormalised backward call (W = 0: no kernel).
+struct BwdPlan {
+    int W = 0;
+    bool f32 = false;
+    Plan p;
+    BwdLayout L;
+};
+
+BwdPlan backward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, const DevInfo& di) {
+    BwdPlan bp;
+    bp.f32 = dtype == HLA2_F32;
+    bp.W = bp.f32 ? backward_width_f32(d, dv, chunk, di) : backward_width(d, chunk, di);
+    if (!bp.W) return bp;
+    const int per_sm = bp.f32 ? backward_per_sm_f32(d, dv, bp.W, di) : backward_per_sm(d, bp.W, di);
+    bp.p = make_plan(B, H, n, d, dv, bp.W, di.sms, per_sm);
+    bp.L = bwd_layout(bp.p, bp.f32 ? sizeof(float) : sizeof(bf16));
+    return bp;
 }
 
 // Chunk-pass arguments at the backward's width and segmentation.
@@ -560,44 +595,153 @@ int backward_forward_part(const ChunkArgs& a, const Plan& p, const BwdLayout& L,
     return HLA2_OK;
 }
 
+// The same forward pieces for the fp32 backward, on the SIMT kernel: segment summaries, the
+// inter-segment scan, then a pass that exports the fp32 (S, Z) at every chunk start.
+int backward_forward_part_f32(const ChunkArgs& a, const Plan& p, const BwdLayout& L, int d, int dv, cudaStream_t st) {
+    float* ws = a.ws;
+    const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
+    const int seg_tokens = p.seg_chunks * p.W;
+    ChunkArgs c = a;
+    c.seg0 = 0;
+    c.nseg_launch = p.nseg;
+    if (launch_init_carry(a, d, dv, nullptr, st)) return cuda_fail("carry-in initialisation");
+    if (p.nseg > 1) {
+        const int steps = p.nseg - 1;
+        if (launch_fwd_chunk_simt(c, d, dv, p.W, true, true, false, st)) return cuda_fail("segment summaries");
+        if (launch_linear_scan(ws + L.F.SB, ws + L.F.Sin, a.BH, a.H, steps, dd, a.nsum * dd, p.nseg * dd, true,
+                               a.gamma, seg_tokens, 1, st) ||
+            launch_cross(a, d, dv, false, st) ||
+            launch_linear_scan(ws + L.F.ZB, ws + L.F.Zin, a.BH, a.H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true,
+                               a.gamma, seg_tokens, 2, st))
+            return cuda_fail("forward segment scan");
+    }
+    c.out = nullptr;
+    c.chunk_states_f32 = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + L.states_bytes_off);
+    if (launch_fwd_chunk_simt(c, d, dv, p.W, false, false, false, st)) return cuda_fail("forward state export");
+    return HLA2_OK;
+}
+
+// fp32 reverse-mode passes: reverse summaries, the reverse scan with its cross term, gradients.
+int backward_reverse_part_f32(const float* q, const float* k, const float* v, const float* dout, float* dq, float* dk,
+                              float* dvo, int H, const Plan& p, const BwdLayout& L, const float* gamma, float* ws,
+                              int d, int dv, cudaStream_t st) {
+    BwdArgsF b{};
+    b.q = q;
+    b.k = k;
+    b.v = v;
+    b.dout = dout;
+    b.dq = dq;
+    b.dk = dk;
+    b.dv = dvo;
+    b.BH = p.BH;
+    b.H = H;
+    b.n = p.n;
+    b.W = p.W;
+    b.nchunks = p.nchunks;
+    b.seg_chunks = p.seg_chunks;
+    b.nseg = p.nseg;
+    b.gamma = gamma;
+    b.ws = ws;
+    b.ZhB = L.ZhB;
+    b.ShB = L.ShB;
+    b.Zh_end = L.Zh_end;
+    b.Sh_end = L.Sh_end;
+    b.chunk_states = reinterpret_cast<const float*>(reinterpret_cast<const char*>(ws) + L.states_bytes_off);
+    BwdArgs r{};  // what the reverse cross term reads
+    r.BH = p.BH;
+    r.H = H;
+    r.n = p.n;
+    r.W = p.W;
+    r.nchunks = p.nchunks;
+    r.seg_chunks = p.seg_chunks;
+    r.nseg = p.nseg;
+    r.gamma = gamma;
+    r.ws = ws;
+    r.ZhB = L.ZhB;
+    r.ShB = L.ShB;
+    r.Zh_end = L.Zh_end;
+    r.Sh_end = L.Sh_end;
+    const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
+    if (launch_bwd_chunk_simt(b, d, dv, true, st)) return cuda_fail("reverse summaries");
+    if (launch_reverse_scan(ws + L.ZhB, ws + L.Zh_end, p.BH, H, p.nseg, ddv, gamma, p.n, p.W, p.seg_chunks, 2, st) ||
+        launch_reverse_cross(r, ws + L.F.CB, d, dv, st) ||
+        launch_reverse_scan(ws + L.ShB, ws + L.Sh_end, p.BH, H, p.nseg, dd, gamma, p.n, p.W, p.seg_chunks, 1, st))
+        return cuda_fail("reverse segment scan");
+    if (launch_bwd_chunk_simt(b, d, dv, false, st)) return cuda_fail("gradient pass");
+    return HLA2_OK;
+}
+
+
 int check_backward(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
     int rc = check_common(B, H, n, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
     if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
-    if (dtype != HLA2_BF16 || d != dv)
-        return fail(HLA2_ERR_UNSUPPORTED, "the backward needs bf16 tensors and d == dv");
+    if (dtype == HLA2_BF16 && d != dv && !normalize)
+        return fail(HLA2_ERR_UNSUPPORTED, "the bf16 backward needs d == dv (float32 takes any d, dv)");
     return HLA2_OK;
 }
 
-// Workspace of the ratio-normalised backward: one scratch region that the unnormalised
-// forward and backward calls use in turn (stream order keeps them apart), then eight bf16
-// [B, H, n, d] buffers: num, e_0, den output, dL/dnum, dL/dden (column 0), dq2, dk2, dv2.
+// Workspace of the ratio-normalised backward.  Its gradient is the difference of a
+// numerator part and a denominator part that can each be tens of times larger than the
+// result, so the composition runs in float32: one scratch region that the fp32 forward and
+// backward calls use in turn, then fp32 [B, H, n, *] buffers: num (dv), e_0, den and
+// dL/dden (kUnitWidth columns), dL/dnum (dv), dq2, dk2 (d), dv2 (kUnitWidth); for bf16
+// inputs also float32 copies of q, k (d), v, dout (dv) and of the gradients (d, d, dv).
+constexpr int kUnitWidth = 16;  // value width of the denominator pass (only column 0 is 1)
+enum NormBuf { NB_NUM, NB_E0, NB_DEN, NB_DNUM, NB_DDEN, NB_DQ2, NB_DK2, NB_DV2, NB_Q, NB_K, NB_V, NB_DO, NB_DQ, NB_DK,
+               NB_DV, NB_COUNT };
 struct NormBwdLayout {
     size_t sub_bytes = 0;
-    size_t buf[8] = {};
+    size_t buf[NB_COUNT] = {};
     size_t total = 0;
 };
 
-size_t unnormalised_backward_bytes(int B, int H, int n, int d, int dv, int chunk, const DevInfo& di) {
-    const int W = backward_width(d, chunk, di);
-    if (!W) return (size_t)-1;
-    const Plan p = make_plan(B, H, n, d, dv, W, di.sms, backward_per_sm(d, W, di));
-    return p.nseg > 0 ? bwd_layout(p).total_bytes : 0;
+// Chunk width of the normalised backward's float32 forwards: the largest <= chunk whose SIMT
+// kernel fits for both value widths (the result does not depend on the width).
+int normalised_f32_chunk(int d, int dv, int chunk, const DevInfo& di) {
+    for (int W = chunk; W >= 16; W /= 2)
+        if (fwd_chunk_simt_smem(d, dv, W, true) <= (size_t)di.smem_optin &&
+            fwd_chunk_simt_smem(d, kUnitWidth, W, true) <= (size_t)di.smem_optin)
+            return W;
+    return 0;
+}
+
+size_t unnormalised_backward_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype, const DevInfo& di) {
+    const BwdPlan bp = backward_plan(B, H, n, d, dv, chunk, dtype, di);
+    if (!bp.W) return (size_t)-1;
+    return bp.p.nseg > 0 ? bp.L.total_bytes : 0;
 }
 
 NormBwdLayout norm_bwd_layout(int B, int H, int n, int d, int dv, int chunk, int dtype, const DevInfo& di) {
     NormBwdLayout L;
-    const size_t fw = hla2_forward_workspace_bytes(B, H, n, d, dv, chunk, dtype, 0, 0);
-    const size_t bw = unnormalised_backward_bytes(B, H, n, d, dv, chunk, di);
-    if (fw == (size_t)-1 || bw == (size_t)-1) {
+    const int u = kUnitWidth;
+    chunk = normalised_f32_chunk(d, dv, chunk, di);
+    if (!chunk) {
         L.total = (size_t)-1;
         return L;
     }
+    const size_t sizes[4] = {hla2_forward_workspace_bytes(B, H, n, d, dv, chunk, HLA2_F32, 0, 0),
+                             hla2_forward_workspace_bytes(B, H, n, d, u, chunk, HLA2_F32, 0, 0),
+                             unnormalised_backward_bytes(B, H, n, d, dv, chunk, HLA2_F32, di),
+                             unnormalised_backward_bytes(B, H, n, d, u, chunk, HLA2_F32, di)};
+    size_t sub = 0;
+    for (size_t x : sizes) {
+        if (x == (size_t)-1) {
+            L.total = (size_t)-1;
+            return L;
+        }
+        sub = x > sub ? x : sub;
+    }
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    L.sub_bytes = up(fw > bw ? fw : bw);
-    const size_t one = up((size_t)B * H * (size_t)n * (size_t)d * sizeof(bf16));
-    size_t o = L.sub_bytes;
-    for (int i = 0; i < 8; ++i, o += one) L.buf[i] = o;
+    const size_t rows = (size_t)B * H * (size_t)n;
+    const int width[NB_COUNT] = {dv, u, u, dv, u, d, d, u, d, d, dv, dv, d, d, dv};
+    const int count = dtype == HLA2_BF16 ? NB_COUNT : NB_Q;
+    size_t o = up(sub);
+    L.sub_bytes = o;
+    for (int i = 0; i < count; ++i) {
+        L.buf[i] = o;
+        o += up(rows * (size_t)width[i] * sizeof(float));
+    }
     L.total = o;
     return L;
 }
@@ -639,7 +783,7 @@ size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chu
     if (check_backward(B, H, n, d, dv, chunk, dtype, normalize) != HLA2_OK) return (size_t)-1;
     const DevInfo di = dev_info();
     if (normalize) return norm_bwd_layout(B, H, n, d, dv, chunk, dtype, di).total;
-    return unnormalised_backward_bytes(B, H, n, d, dv, chunk, di);
+    return unnormalised_backward_bytes(B, H, n, d, dv, chunk, dtype, di);
 }
 
 int hla2_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
@@ -670,47 +814,77 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
                         opts->workspace ? opts->workspace_bytes : (size_t)0);
         if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
         char* base = static_cast<char*>(opts->workspace);
-        bf16* num = reinterpret_cast<bf16*>(base + N.buf[0]);
-        bf16* e0 = reinterpret_cast<bf16*>(base + N.buf[1]);
-        bf16* den = reinterpret_cast<bf16*>(base + N.buf[2]);
-        bf16* dnum = reinterpret_cast<bf16*>(base + N.buf[3]);
-        bf16* dden = reinterpret_cast<bf16*>(base + N.buf[4]);
-        bf16* dq2 = reinterpret_cast<bf16*>(base + N.buf[5]);
-        bf16* dk2 = reinterpret_cast<bf16*>(base + N.buf[6]);
-        bf16* dv2 = reinterpret_cast<bf16*>(base + N.buf[7]);
+        auto buf = [&](int i) { return reinterpret_cast<float*>(base + N.buf[i]); };
+        const bool bf = opts->dtype == HLA2_BF16;
+        const size_t rows = (size_t)BH * (size_t)n;
+        const int u = kUnitWidth;
+        cudaStream_t s2 = reinterpret_cast<cudaStream_t>(stream);
+        cudaGetLastError();
+        const float* q32 = bf ? buf(NB_Q) : static_cast<const float*>(q);
+        const float* k32 = bf ? buf(NB_K) : static_cast<const float*>(k);
+        const float* v32 = bf ? buf(NB_V) : static_cast<const float*>(v);
+        const float* do32 = bf ? buf(NB_DO) : static_cast<const float*>(dout);
+        float* dq32 = bf ? buf(NB_DQ) : static_cast<float*>(dq);
+        float* dk32 = bf ? buf(NB_DK) : static_cast<float*>(dk);
+        float* dv32 = bf ? buf(NB_DV) : static_cast<float*>(dv_out);
+        if (bf && (launch_convert_bf16_f32(static_cast<const bf16*>(q), buf(NB_Q), rows * d, s2) ||
+                   launch_convert_bf16_f32(static_cast<const bf16*>(k), buf(NB_K), rows * d, s2) ||
+                   launch_convert_bf16_f32(static_cast<const bf16*>(v), buf(NB_V), rows * dv, s2) ||
+                   launch_convert_bf16_f32(static_cast<const bf16*>(dout), buf(NB_DO), rows * dv, s2)))
+            return cuda_fail("float32 copies");
         hla2_opts so{};
-        so.dtype = HLA2_BF16;
+        so.dtype = HLA2_F32;
         so.eps = opts->eps;
         so.workspace = base;
         so.workspace_bytes = N.sub_bytes;
-        cudaStream_t s2 = reinterpret_cast<cudaStream_t>(stream);
-        const size_t rows = (size_t)BH * (size_t)n;
-        cudaGetLastError();
+        const int cf = normalised_f32_chunk(d, dv, chunk, di);
         // num = unnormalised output; den = unnormalised output for the value rows e_0
-        if ((rc = hla2_forward(q, k, v, num, B, H, n, d, dv, gamma, 0, chunk, stream, &so)) != HLA2_OK) return rc;
-        if (launch_unit_first_column(e0, rows, d, s2)) return cuda_fail("unit value rows");
-        if ((rc = hla2_forward(q, k, e0, den, B, H, n, d, d, gamma, 0, chunk, stream, &so)) != HLA2_OK) return rc;
-        if (launch_quotient_rule(static_cast<const bf16*>(dout), num, den, dnum, dden, rows, dv, d, opts->eps, s2))
+        if ((rc = hla2_forward(q32, k32, v32, buf(NB_NUM), B, H, n, d, dv, gamma, 0, cf, stream, &so)) != HLA2_OK)
+            return rc;
+        if (launch_unit_first_column(buf(NB_E0), rows, u, s2)) return cuda_fail("unit value rows");
+        if ((rc = hla2_forward(q32, k32, buf(NB_E0), buf(NB_DEN), B, H, n, d, u, gamma, 0, cf, stream, &so)) !=
+            HLA2_OK)
+            return rc;
+        if (launch_quotient_rule(do32, buf(NB_NUM), buf(NB_DEN), buf(NB_DNUM), buf(NB_DDEN), rows, dv, u, opts->eps, s2))
             return cuda_fail("quotient rule");
-        if ((rc = hla2_backward(q, k, v, dnum, dq, dk, dv_out, B, H, n, d, dv, gamma, 0, chunk, stream, &so)) !=
-            HLA2_OK)
+        if ((rc = hla2_backward(q32, k32, v32, buf(NB_DNUM), dq32, dk32, dv32, B, H, n, d, dv, gamma, 0, cf, stream,
+                                &so)) != HLA2_OK)
             return rc;
-        if ((rc = hla2_backward(q, k, e0, dden, dq2, dk2, dv2, B, H, n, d, d, gamma, 0, chunk, stream, &so)) !=
-            HLA2_OK)
+        if ((rc = hla2_backward(q32, k32, buf(NB_E0), buf(NB_DDEN), buf(NB_DQ2), buf(NB_DK2), buf(NB_DV2), B, H, n, d,
+                                u, gamma, 0, cf, stream, &so)) != HLA2_OK)
             return rc;
-        if (launch_add_into(static_cast<bf16*>(dq), dq2, rows * (size_t)d, s2) ||
-            launch_add_into(static_cast<bf16*>(dk), dk2, rows * (size_t)d, s2))
+        if (launch_add_into(dq32, buf(NB_DQ2), rows * d, s2) || launch_add_into(dk32, buf(NB_DK2), rows * d, s2))
             return cuda_fail("gradient sum");
+        if (bf && (launch_convert_f32_bf16(dq32, static_cast<bf16*>(dq), rows * d, s2) ||
+                   launch_convert_f32_bf16(dk32, static_cast<bf16*>(dk), rows * d, s2) ||
+                   launch_convert_f32_bf16(dv32, static_cast<bf16*>(dv_out), rows * dv, s2)))
+            return cuda_fail("bf16 gradients");
         return succeed();
     }
-    const int W = backward_width(d, chunk, di);
-    if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no backward kernel for d %d, chunk %d", d, chunk);
-    const Plan p = make_plan(B, H, n, d, dv, W, di.sms, backward_per_sm(d, W, di));
-    const BwdLayout L = bwd_layout(p);
-    if (!opts->workspace || opts->workspace_bytes < L.total_bytes)
-        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.total_bytes,
+    const BwdPlan bp = backward_plan(B, H, n, d, dv, chunk, opts->dtype, di);
+    if (!bp.W) return fail(HLA2_ERR_UNSUPPORTED, "no backward kernel for d %d, dv %d, chunk %d", d, dv, chunk);
+    if (bp.f32 && (opts->flags & HLA2_FLAG_STATES_SAVED))
+        return fail(HLA2_ERR_UNSUPPORTED, "saved forward states are kept by the bf16 path only");
+    if (!opts->workspace || opts->workspace_bytes < bp.L.total_bytes)
+        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", bp.L.total_bytes,
                     opts->workspace ? opts->workspace_bytes : (size_t)0);
     if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    if (bp.f32) {
+        cudaStream_t sf = reinterpret_cast<cudaStream_t>(stream);
+        cudaGetLastError();
+        const ChunkArgs a = backward_chunk_args(q, k, v, nullptr, BH, H, n, bp.p, gamma, opts->workspace, bp.L);
+        if ((rc = backward_forward_part_f32(a, bp.p, bp.L, d, dv, sf)) != HLA2_OK) return rc;
+        if ((rc = backward_reverse_part_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                            static_cast<const float*>(v), static_cast<const float*>(dout),
+                                            static_cast<float*>(dq), static_cast<float*>(dk), static_cast<float*>(dv_out),
+                                            H, bp.p, bp.L, gamma, static_cast<float*>(opts->workspace), d, dv, sf)) !=
+            HLA2_OK)
+            return rc;
+        return succeed();
+    }
+    const int W = bp.W;
+    const Plan& p = bp.p;
+    const BwdLayout& L = bp.L;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     float* ws = static_cast<float*>(opts->workspace);
     bf16* states = reinterpret_cast<bf16*>(static_cast<char*>(opts->workspace) + L.states_bytes_off);

@@ -8,8 +8,10 @@
 // Both num and den are unnormalised outputs of the same recurrence: den is the output for
 // the value rows e_0 = (1, 0, ..., 0). So the gradients are those of two unnormalised
 // backward passes: one with (v, dL/dnum), and one with (e_0, dL/dden e_0^T), which adds to
-// dq and dk only. The kernels below build e_0 and the two upstream gradients, and add the
-// second pass's dq, dk into the first's.
+// dq and dk only.  The two parts of dq and dk can each be tens of times larger than their
+// sum, so the composition runs in float32 (bf16 inputs are widened first and the gradients
+// rounded at the end).  The kernels below build e_0 and the two upstream gradients, add the
+// second pass's dq, dk into the first's, and convert between bf16 and float32.
 #include "kernels.h"
 
 namespace hla2 {
@@ -18,76 +20,119 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// rows x d bf16 with column 0 = 1 and every other column 0 (d a multiple of 8).
-__global__ void __launch_bounds__(kThreads) unit_first_column_kernel(bf16* e0, size_t chunks8, int d) {
+// rows x w float32 with column 0 = 1 and every other column 0.
+__global__ void __launch_bounds__(kThreads) unit_first_column_kernel(float* e0, size_t count, int w) {
     const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
-    if (i >= chunks8) return;
-    uint4 z = make_uint4(0u, 0u, 0u, 0u);
-    if ((i * 8) % (size_t)d == 0) z.x = 0x3F80u;  // bf16 1.0 in the low half: element 0
-    reinterpret_cast<uint4*>(e0)[i] = z;
+    if (i < count) e0[i] = (i % (size_t)w) == 0 ? 1.f : 0.f;
 }
 
 // One warp per token row t: den = den_out[t][0], s = dO_t . num_t,
 // dnum[t] = dO_t / (den + eps), dden[t] = (-s / (den + eps)^2, 0, ..., 0).
 __global__ void __launch_bounds__(kThreads)
-    quotient_rule_kernel(const bf16* __restrict__ dout, const bf16* __restrict__ num,
-                         const bf16* __restrict__ den_out, bf16* __restrict__ dnum, bf16* __restrict__ dden,
-                         size_t rows, int dv, int d, float eps) {
+    quotient_rule_kernel(const float* __restrict__ dout, const float* __restrict__ num,
+                         const float* __restrict__ den_out, float* __restrict__ dnum, float* __restrict__ dden,
+                         size_t rows, int dv, int w, float eps) {
     const size_t row = (size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const bf16* o = dout + row * dv;
-    const bf16* x = num + row * dv;
+    const float* o = dout + row * dv;
+    const float* x = num + row * dv;
     float s = 0.f;
-    for (int j = lane; j < dv; j += 32) s += to_f32(o[j]) * to_f32(x[j]);
+    for (int j = lane; j < dv; j += 32) s += o[j] * x[j];
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
-    const float inv = 1.f / (to_f32(den_out[row * d]) + eps);
-    for (int j = lane; j < dv; j += 32) dnum[row * dv + j] = from_f32<bf16>(to_f32(o[j]) * inv);
-    for (int j = lane; j < d; j += 32) dden[row * d + j] = from_f32<bf16>(j == 0 ? -s * inv * inv : 0.f);
+    const float inv = 1.f / (den_out[row * w] + eps);
+    for (int j = lane; j < dv; j += 32) dnum[row * dv + j] = o[j] * inv;
+    for (int j = lane; j < w; j += 32) dden[row * w + j] = j == 0 ? -s * inv * inv : 0.f;
 }
 
-// a += b, bf16, count a multiple of 8.
-__global__ void __launch_bounds__(kThreads) add_into_kernel(bf16* a, const bf16* b, size_t chunks8) {
+// a += b, float32, count a multiple of 4.
+__global__ void __launch_bounds__(kThreads) add_into_kernel(float* a, const float* b, size_t count4) {
     const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
-    if (i >= chunks8) return;
-    uint4 x = reinterpret_cast<uint4*>(a)[i];
-    const uint4 y = reinterpret_cast<const uint4*>(b)[i];
-    uint32_t* xs = reinterpret_cast<uint32_t*>(&x);
-    const uint32_t* ys = reinterpret_cast<const uint32_t*>(&y);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        const float lo = __uint_as_float(xs[w] << 16) + __uint_as_float(ys[w] << 16);
-        const float hi = __uint_as_float(xs[w] & 0xFFFF0000u) + __uint_as_float(ys[w] & 0xFFFF0000u);
-        xs[w] = pack_bf16x2(lo, hi);
-    }
-    reinterpret_cast<uint4*>(a)[i] = x;
+    if (i >= count4) return;
+    float4 x = reinterpret_cast<float4*>(a)[i];
+    const float4 y = reinterpret_cast<const float4*>(b)[i];
+    x.x += y.x;
+    x.y += y.y;
+    x.z += y.z;
+    x.w += y.w;
+    reinterpret_cast<float4*>(a)[i] = x;
+}
+
+// 8 elements per thread; count a multiple of 8.
+__global__ void __launch_bounds__(kThreads) bf16_to_f32_kernel(const bf16* __restrict__ src, float* __restrict__ dst,
+                                                               size_t count8) {
+    const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
+    if (i >= count8) return;
+    const uint4 c = reinterpret_cast<const uint4*>(src)[i];
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    float4 lo, hi;
+    lo.x = __uint_as_float(w[0] << 16);
+    lo.y = __uint_as_float(w[0] & 0xFFFF0000u);
+    lo.z = __uint_as_float(w[1] << 16);
+    lo.w = __uint_as_float(w[1] & 0xFFFF0000u);
+    hi.x = __uint_as_float(w[2] << 16);
+    hi.y = __uint_as_float(w[2] & 0xFFFF0000u);
+    hi.z = __uint_as_float(w[3] << 16);
+    hi.w = __uint_as_float(w[3] & 0xFFFF0000u);
+    reinterpret_cast<float4*>(dst)[2 * i] = lo;
+    reinterpret_cast<float4*>(dst)[2 * i + 1] = hi;
+}
+
+__global__ void __launch_bounds__(kThreads) f32_to_bf16_kernel(const float* __restrict__ src, bf16* __restrict__ dst,
+                                                               size_t count8) {
+    const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
+    if (i >= count8) return;
+    const float4 lo = reinterpret_cast<const float4*>(src)[2 * i];
+    const float4 hi = reinterpret_cast<const float4*>(src)[2 * i + 1];
+    uint4 o;
+    o.x = pack_bf16x2(lo.x, lo.y);
+    o.y = pack_bf16x2(lo.z, lo.w);
+    o.z = pack_bf16x2(hi.x, hi.y);
+    o.w = pack_bf16x2(hi.z, hi.w);
+    reinterpret_cast<uint4*>(dst)[i] = o;
 }
 
 unsigned blocks_for(size_t n, int per_block) { return (unsigned)((n + per_block - 1) / per_block); }
 
+int done() { return cudaPeekAtLastError() == cudaSuccess ? 0 : -1; }
+
 }  // namespace
 
-int launch_unit_first_column(bf16* e0, size_t rows, int d, cudaStream_t st) {
-    const size_t c = rows * (size_t)d / 8;
+int launch_unit_first_column(float* e0, size_t rows, int w, cudaStream_t st) {
+    const size_t c = rows * (size_t)w;
     if (c == 0) return 0;
-    unit_first_column_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(e0, c, d);
-    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+    unit_first_column_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(e0, c, w);
+    return done();
 }
 
-int launch_quotient_rule(const bf16* dout, const bf16* num, const bf16* den_out, bf16* dnum, bf16* dden,
-                         size_t rows, int dv, int d, float eps, cudaStream_t st) {
+int launch_quotient_rule(const float* dout, const float* num, const float* den_out, float* dnum, float* dden,
+                         size_t rows, int dv, int w, float eps, cudaStream_t st) {
     if (rows == 0) return 0;
     quotient_rule_kernel<<<blocks_for(rows, kThreads / 32), kThreads, 0, st>>>(dout, num, den_out, dnum, dden, rows,
-                                                                                dv, d, eps);
-    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+                                                                                dv, w, eps);
+    return done();
 }
 
-int launch_add_into(bf16* a, const bf16* b, size_t count, cudaStream_t st) {
-    const size_t c = count / 8;
+int launch_add_into(float* a, const float* b, size_t count, cudaStream_t st) {
+    const size_t c = count / 4;
     if (c == 0) return 0;
     add_into_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(a, b, c);
-    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+    return done();
+}
+
+int launch_convert_bf16_f32(const bf16* src, float* dst, size_t count, cudaStream_t st) {
+    const size_t c = count / 8;
+    if (c == 0) return 0;
+    bf16_to_f32_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(src, dst, c);
+    return done();
+}
+
+int launch_convert_f32_bf16(const float* src, bf16* dst, size_t count, cudaStream_t st) {
+    const size_t c = count / 8;
+    if (c == 0) return 0;
+    f32_to_bf16_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(src, dst, c);
+    return done();
 }
 
 }  // namespace hla2

@@ -74,6 +74,11 @@ __global__ void __launch_bounds__(kSimtThreads)
         const int row0 = c * W;
         const int Wc = min(W, a.n - row0);
         __syncthreads();
+        if (!summary && a.chunk_states_f32) {  // the state at this chunk start, for the backward
+            float* dst = a.chunk_states_f32 + ((size_t)bh * a.nchunks + c) * (size_t)(D * D + D * DV);
+            for (int i = tid; i < D * D; i += NT) dst[i] = S[i];
+            for (int i = tid; i < D * DV; i += NT) dst[(size_t)D * D + i] = Z[i];
+        }
         for (int i = tid; i < W * D; i += NT) {
             const int r = i / D;
             Qs[i] = r < Wc ? to_f32(q[(size_t)row0 * D + i]) : 0.f;
@@ -110,7 +115,7 @@ __global__ void __launch_bounds__(kSimtThreads)
         }
         __syncthreads();
 
-        if (!summary) {
+        if (!summary && a.out) {
             if (um && a.normalize) {  // unmasked denominator carry g^(r+1) p_r . m0
                 for (int r = tid; r < W; r += NT) {
                     float s = 0.f;

@@ -78,6 +78,9 @@ struct ChunkArgs {
     float* ws;        // forward workspace (floats)
     FwdLayout L;
     bf16* chunk_states;  // state-export pass: bf16 (S | Z) at every chunk start, [BH][nchunks][d*d + d*dv]
+    // fp32 state-export pass of the SIMT kernel: (S | Z) at every chunk start,
+    // [BH][nchunks][d*d + d*dv]; out may then be NULL.
+    float* chunk_states_f32;
     // 1: unmasked output q^T S C (and denominator q^T S m).  The Z and y slots of the
     // summaries, the carries and the raw final state then hold C and m, which decay by
     // g per token, and no cross term enters the inter-segment scan.
@@ -104,6 +107,25 @@ struct BwdArgs {
     const bf16* chunk_states;  // forward (S | Z) bf16 at every chunk start
 };
 
+// Arguments of the fp32 reverse-mode chunk kernel (SIMT, any d, dv; bwd_chunk_simt.cu).
+struct BwdArgsF {
+    const float* q;
+    const float* k;
+    const float* v;
+    const float* dout;
+    float* dq;
+    float* dk;
+    float* dv;
+    int BH, H, n, W, nchunks, seg_chunks, nseg;
+    const float* gamma;
+    float* ws;
+    size_t ZhB, ShB;             // reverse summaries, float offsets, [BH][nseg][...]
+    size_t Zh_end, Sh_end;       // reverse carries at segment ends, [BH][nseg][...]; updated in place
+    const float* chunk_states;   // forward (S | Z) fp32 at every chunk start
+};
+int launch_bwd_chunk_simt(const BwdArgsF& a, int d, int dv, bool rsum, cudaStream_t st);
+size_t bwd_chunk_simt_smem(int d, int dv, int W);
+
 // Reverse-mode chunk kernel: rsum = true stores each segment's reverse summary,
 // false writes dq, dk, dv.  d == dv in {16,32,64,128}; W in {16,32,64} (32 max for d = 128).
 int launch_bwd_chunk_mma(const BwdArgs& a, int d, int W, bool rsum, cudaStream_t st);
@@ -117,10 +139,12 @@ int launch_reverse_scan(const float* src, float* dst, int BH, int H, int nseg, s
 int launch_reverse_cross(const BwdArgs& b, const float* CB, int d, int dv, cudaStream_t st);
 
 // ratio-normalised backward: quotient-rule glue (bwd_normalize.cu)
-int launch_unit_first_column(bf16* e0, size_t rows, int d, cudaStream_t st);
-int launch_quotient_rule(const bf16* dout, const bf16* num, const bf16* den_out, bf16* dnum, bf16* dden,
-                         size_t rows, int dv, int d, float eps, cudaStream_t st);
-int launch_add_into(bf16* a, const bf16* b, size_t count, cudaStream_t st);
+int launch_unit_first_column(float* e0, size_t rows, int w, cudaStream_t st);
+int launch_quotient_rule(const float* dout, const float* num, const float* den_out, float* dnum, float* dden,
+                         size_t rows, int dv, int w, float eps, cudaStream_t st);
+int launch_add_into(float* a, const float* b, size_t count, cudaStream_t st);  // count a multiple of 4
+int launch_convert_bf16_f32(const bf16* src, float* dst, size_t count, cudaStream_t st);  // count % 8 == 0
+int launch_convert_f32_bf16(const float* src, bf16* dst, size_t count, cudaStream_t st);
 
 // Tensor-core (mma.sync bf16) chunk kernel: d == dv in {16,32,64,128}, W in {16,32,64,128}.
 // Returns 0 on success, -1 on a CUDA error, -2 if the shape is not compiled.  With

@@ -99,7 +99,13 @@ def test_normalized_backward_checks_before_launching(L):
     n0 = L.hla2_backward_workspace_bytes(1, 2, 100, 32, 32, 32, 1, 0)
     n1 = L.hla2_backward_workspace_bytes(1, 2, 100, 32, 32, 32, 1, 1)
     assert 0 < n0 < n1 < 2**40
-    assert L.hla2_backward_workspace_bytes(1, 2, 100, 32, 16, 32, 1, 1) == ctypes.c_size_t(-1).value  # d != dv
+    # the bf16 tensor-core backward needs d == dv; float32 (SIMT) and the normalised
+    # backward (which composes float32 passes) take any d, dv
+    assert L.hla2_backward_workspace_bytes(1, 2, 100, 32, 16, 32, 1, 0) == ctypes.c_size_t(-1).value
+    assert 0 < L.hla2_backward_workspace_bytes(1, 2, 100, 32, 16, 32, 1, 1) < 2**40
+    assert 0 < L.hla2_backward_workspace_bytes(1, 2, 100, 32, 16, 32, 0, 0) < 2**40
+    # float32 states: the fp32 backward's workspace is larger than the bf16 one's
+    assert L.hla2_backward_workspace_bytes(1, 2, 100, 32, 32, 32, 0, 0) > n0
 
 
 def test_unknown_flags_rejected(L):

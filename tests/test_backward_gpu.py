@@ -1,6 +1,7 @@
 """GPU reverse-mode chunk scan (dQ, dK, dV) against the float64 oracle's reverse sweep of
 the serial recurrence, through the C ABI.  Bar: max|gpu - oracle| / max|oracle| <= 2e-2
-per gradient (bf16 inputs; the oracle runs on the same bf16-rounded values)."""
+per gradient for bf16 inputs (the oracle runs on the same bf16-rounded values) and <= 1e-4
+for float32 inputs (the SIMT float32 kernels, any d and dv)."""
 import numpy as np
 import pytest
 import torch
@@ -78,9 +79,37 @@ def test_training_workload_full_size_sampled():
 
 
 def test_unsupported_variants_are_reported():
-    x = inputs.make_custom(1, 1, 32, 16, 16, torch.float32, seed=5, with_dout=True)
-    with pytest.raises(HLA2Error):
+    x = inputs.make_custom(1, 1, 32, 16, 32, torch.bfloat16, seed=5, with_dout=True)
+    with pytest.raises(HLA2Error):  # the bf16 tensor-core backward needs d == dv
         run(x, 16)
+
+
+@pytest.mark.parametrize("d, dv", [(16, 16), (32, 64), (64, 32), (64, 64), (128, 128), (16, 128)])
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_fp32_gradients_match_oracle(d, dv, chunk):
+    """float32 inputs: the SIMT reverse-mode kernels, several chunks and a ragged tail."""
+    n = 3 * chunk + 7
+    x = inputs.make_custom(1, 2, n, d, dv, torch.float32, seed=d + 3 * dv + chunk, gamma=(0.9, 0.999), with_dout=True)
+    got = run(x, chunk)
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, oracle(x)):
+        assert rel_err(np64(gg.cpu()), rr) <= 1e-4, name
+
+
+@pytest.mark.parametrize("n", [1, 31, 33, 700, 3000])
+def test_fp32_lengths_and_segments(n):
+    """float32 gradients across many segments (the reverse scan and its cross term at 1e-4)."""
+    x = inputs.make_custom(1, 3, n, 32, 32, torch.float32, seed=n + 11, gamma=(0.99, 0.9999), with_dout=True)
+    got = run(x, 32)
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, oracle(x)):
+        assert rel_err(np64(gg.cpu()), rr) <= 1e-4, (name, n)
+
+
+def test_fp32_no_decay_and_host_tensors():
+    x = inputs.make_custom(2, 1, 300, 16, 32, torch.float32, seed=12, gamma=None, with_dout=True)
+    got = hla.backward(x["q"], x["k"], x["v"], x["dout"], chunk=16)  # CPU tensors in and out
+    assert got[0].device.type == "cpu"
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, oracle(x)):
+        assert rel_err(np64(gg), rr) <= 1e-4, name
 
 
 @pytest.mark.parametrize("B,H,n,d", [(1, 3, 333, 64), (2, 2, 2000, 64), (1, 4, 1000, 128), (4, 16, 300, 32)])
@@ -135,10 +164,9 @@ def test_normalized_gradients_match_oracle(d, chunk, n):
     normalised adjoint on the normalised workload's recipe (positive q, k: den > 0).
 
     dq and dk are a difference of a numerator part and a denominator part that can be many
-    times larger than the result. Four bf16 roundings enter each part: den, the two upstream
-    gradients and the pass's own operands, each within 2^-9 relative. So the bar is
-    max(2e-2, 2^-7 kappa), with kappa the parts' magnitude over the result's (from the
-    oracle, same inputs). dv has no such split."""
+    times larger than the result (kappa, the parts' magnitude over the result's, reaches
+    tens here).  The library therefore runs the composition in float32, and the bf16 bar
+    of 2e-2 holds whatever kappa is."""
     x = inputs.make_custom(2, 2, n, d, d, torch.bfloat16, seed=40 + d + n, qk="softplus", v_scale="unit",
                            gamma=(0.95, 0.999), with_dout=True)
     g = x["gamma"].cuda()
@@ -147,13 +175,24 @@ def test_normalized_gradients_match_oracle(d, chunk, n):
     ref, kappa = _normalized_reference(x, 1e-6)
     for name, gg, rr, kk in zip(("dq", "dk", "dv"), got, ref, kappa):
         assert torch.isfinite(gg.float()).all(), name
-        assert rel_err(np64(gg.cpu()), rr) <= max(2e-2, 2.0 ** -7 * kk), (name, kk)
+        assert rel_err(np64(gg.cpu()), rr) <= 2e-2, (name, kk)
+
+
+@pytest.mark.parametrize("d, dv, chunk", [(32, 32, 32), (64, 16, 64), (16, 64, 16)])
+def test_normalized_gradients_fp32(d, dv, chunk):
+    """float32 inputs: the normalised gradients at the float32 bar, 1e-4."""
+    x = inputs.make_custom(1, 2, 333, d, dv, torch.float32, seed=60 + d + dv, qk="softplus", v_scale="unit",
+                           gamma=(0.95, 0.999), with_dout=True)
+    got = hla.backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), gamma=x["gamma"].cuda(),
+                       chunk=chunk, normalize=True, eps=1e-6)
+    ref, kappa = _normalized_reference(x, 1e-6)
+    for name, gg, rr, kk in zip(("dq", "dk", "dv"), got, ref, kappa):
+        assert rel_err(np64(gg.cpu()), rr) <= 1e-4, (name, kk)
 
 
 @pytest.mark.parametrize("d", [32, 64, 128])
 def test_normalized_gradients_short_memory(d):
-    """Positive q, k scaled by 1/sqrt(d) and a short memory (decay 0.8-0.9), under the same
-    conditioning-aware bar."""
+    """Positive q, k scaled by 1/sqrt(d) and a short memory (decay 0.8-0.9), at 2e-2."""
     x = inputs.make_custom(1, 3, 500, d, d, torch.bfloat16, seed=50 + d, qk="softplus", v_scale="unit",
                            gamma=(0.8, 0.9), with_dout=True)
     x["q"] = (x["q"].float() / d ** 0.5).to(torch.bfloat16)
@@ -162,4 +201,15 @@ def test_normalized_gradients_short_memory(d):
     got = hla.backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), gamma=x["gamma"].cuda(),
                        chunk=64, normalize=True, eps=1e-6)
     for name, gg, rr, kk in zip(("dq", "dk", "dv"), got, ref, kappa):
-        assert rel_err(np64(gg.cpu()), rr) <= max(2e-2, 2.0 ** -7 * kk), (name, kk)
+        assert rel_err(np64(gg.cpu()), rr) <= 2e-2, (name, kk)
+
+
+def test_normalized_gradients_bf16_unequal_dims():
+    """The normalised backward composes float32 passes, so bf16 d != dv works too."""
+    x = inputs.make_custom(1, 2, 260, 64, 32, torch.bfloat16, seed=77, qk="softplus", v_scale="unit",
+                           gamma=(0.95, 0.999), with_dout=True)
+    got = hla.backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), gamma=x["gamma"].cuda(),
+                       chunk=32, normalize=True, eps=1e-6)
+    ref, kappa = _normalized_reference(x, 1e-6)
+    for name, gg, rr, kk in zip(("dq", "dk", "dv"), got, ref, kappa):
+        assert rel_err(np64(gg.cpu()), rr) <= 2e-2, (name, kk)
