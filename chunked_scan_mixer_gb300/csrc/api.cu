@@ -11,6 +11,8 @@
 #include <functional>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kernels.h"
 
 namespace hla2 {
@@ -81,6 +83,35 @@ using namespace hla2;
 namespace {
 
 thread_local std::string g_last_error;
+
+// NVTX ranges for profilers (a no-op unless a tool is attached): one range per C-ABI call,
+// and inside the chunked forwards one range per phase (carry-in, segment summaries,
+// inter-segment scan, output pass, final state).
+struct NvtxScope {
+    int depth = 0;
+    explicit NvtxScope(const char* name) { push(name); }
+    NvtxScope(const NvtxScope&) = delete;
+    NvtxScope& operator=(const NvtxScope&) = delete;
+    void push(const char* name) {
+        nvtxRangePushA(name);
+        ++depth;
+    }
+    void pop() {
+        if (depth > 0) {
+            nvtxRangePop();
+            --depth;
+        }
+    }
+    void phase(const char* name) {  // replace the current phase range
+        if (depth > 1) pop();
+        if (name) push(name);
+    }
+    ~NvtxScope() {
+        while (depth > 0) pop();
+    }
+};
+const char* const kPhaseNames[6] = {"carry-in", "segment summaries", "inter-segment scan", "output pass",
+                                    "final state", nullptr};
 
 int fail(int code, const char* fmt, ...) {
     char buf[512];
@@ -276,6 +307,7 @@ size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chun
 int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
                  int d, int dv, const float* gamma, int normalize, int chunk, hla2_stream_t stream,
                  const hla2_opts* opts) {
+    NvtxScope nvtx("hla2_forward");
     if (!opts) return fail(HLA2_ERR_INVALID_ARG, "opts must not be NULL");
     int rc = check_common(B, H, n, d, dv, opts->dtype, normalize);
     if (rc != HLA2_OK) return rc;
@@ -366,6 +398,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     };
 
     auto mark = [&](int i) {
+        nvtx.phase(kPhaseNames[i]);
         if (opts->phase_events && i < opts->n_phase_events && opts->phase_events[i] &&
             cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[i]), st) != cudaSuccess)
             cudaGetLastError();  // a bad profiling handle must not fail the computation
@@ -431,6 +464,14 @@ int hla2_workspace_status(const void* workspace, hla2_stream_t stream) {
         cudaStreamSynchronize(st) != cudaSuccess)
         return cuda_fail("status read");
     if (code != 0) return fail(HLA2_ERR_TIMEOUT, "a bounded device-side wait gave up (site %d)", code);
+    return succeed();
+}
+
+int hla2_selftest_wait_timeout(void* workspace, hla2_stream_t stream) {
+    if (!workspace || !aligned16(workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    cudaGetLastError();
+    if (launch_wait_timeout_selftest(static_cast<int*>(workspace), reinterpret_cast<cudaStream_t>(stream)))
+        return cuda_fail("wait self-test");
     return succeed();
 }
 
@@ -789,6 +830,7 @@ size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chu
 int hla2_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
                   void* dv_out, int B, int H, int n, int d, int dv, const float* gamma, int normalize,
                   int chunk, hla2_stream_t stream, const hla2_opts* opts) {
+    NvtxScope nvtx("hla2_backward");
     if (!opts) return fail(HLA2_ERR_INVALID_ARG, "opts must not be NULL");
     int rc = check_backward(B, H, n, d, dv, chunk, opts->dtype, normalize);
     if (rc != HLA2_OK) return rc;
@@ -933,6 +975,7 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
 int hla2_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
                      int d, int dv, const float* gamma, int normalize, hla2_stream_t stream,
                      const hla2_opts* opts) {
+    NvtxScope nvtx("hla2_decode_step");
     const int dtype = opts ? opts->dtype : HLA2_BF16;
     const float eps = opts ? opts->eps : 1e-6f;
     const int flags = opts ? opts->flags : 0;
@@ -956,6 +999,7 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
 int hla2_decode_step_mq(float* key_state, float* head_state, const void* q, const void* k, const void* v,
                         void* out, int N, int Hk, int group, int d, int dv, const float* gamma, int normalize,
                         hla2_stream_t stream, const hla2_opts* opts) {
+    NvtxScope nvtx("hla2_decode_step_mq");
     const int dtype = opts ? opts->dtype : HLA2_BF16;
     const float eps = opts ? opts->eps : 1e-6f;
     const int flags = opts ? opts->flags : 0;
@@ -987,6 +1031,7 @@ size_t hla2_ahla_state_floats(int d, int dv) { return ahla_state_floats(d, dv); 
 
 int hla2_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H, int d,
                           int dv, const float* gamma, int normalize, hla2_stream_t stream, const hla2_opts* opts) {
+    NvtxScope nvtx("hla2_ahla_decode_step");
     const int dtype = opts ? opts->dtype : HLA2_BF16;
     const float eps = opts ? opts->eps : 1e-6f;
     int rc = check_common(N, H, 0, d, dv, dtype, normalize);
@@ -1037,6 +1082,7 @@ size_t hla2_ahla_forward_workspace_bytes(int B, int H, int n, int d, int dv, int
 
 int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n, int d, int dv,
                       const float* gamma, int normalize, int chunk, hla2_stream_t stream, const hla2_opts* opts) {
+    NvtxScope nvtx("hla2_ahla_forward");
     if (!opts) return fail(HLA2_ERR_INVALID_ARG, "opts must not be NULL");
     int rc = ahla_check(B, H, n, d, dv, chunk, opts->dtype, normalize);
     if (rc != HLA2_OK) return rc;
@@ -1093,6 +1139,7 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
     a.init_state = opts->init_state;
     const bool den_terms = normalize || want_final;  // m, n carried
     auto mark = [&](int i) {
+        nvtx.phase(kPhaseNames[i]);
         if (opts->phase_events && i < opts->n_phase_events && opts->phase_events[i] &&
             cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[i]), st) != cudaSuccess)
             cudaGetLastError();

@@ -186,6 +186,8 @@ int launch_decode_mq(float* key_state, float* head_state, const void* q, const v
 int launch_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
                             int d, int dv, const float* gamma, int normalize, float eps, bool is_bf16,
                             cudaStream_t st);
+// Bounded-wait self-test: waits on an mbarrier nobody arrives at; records site 90 in *status.
+int launch_wait_timeout_selftest(int* status, cudaStream_t st);
 int launch_state_compact(const float* src, float* dst, long heads, int d, int dv, bool to_compact, cudaStream_t st);
 
 }  // namespace hla2

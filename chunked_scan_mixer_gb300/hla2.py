@@ -107,6 +107,8 @@ def lib():
         L.hla2_ahla_decode_step.restype = I
         L.hla2_compact_state_floats.argtypes = [I, I]
         L.hla2_compact_state_floats.restype = Z
+        L.hla2_selftest_wait_timeout.argtypes = [P, P]
+        L.hla2_selftest_wait_timeout.restype = I
         L.hla2_mq_head_state_floats.argtypes = [I, I]
         L.hla2_mq_head_state_floats.restype = Z
         L.hla2_decode_step_mq.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, I, P, ctypes.POINTER(Opts)]
@@ -124,6 +126,7 @@ EXPORTED_SYMBOLS = (
     "hla2_backward", "hla2_decode_step", "hla2_forward_noalloc", "hla2_compact_state_floats",
     "hla2_state_to_compact", "hla2_state_from_compact", "hla2_ahla_forward_workspace_bytes", "hla2_ahla_forward",
     "hla2_ahla_state_floats", "hla2_ahla_decode_step", "hla2_mq_head_state_floats", "hla2_decode_step_mq",
+    "hla2_selftest_wait_timeout",
 )
 
 FLAG_COMPACT_STATE = 4
@@ -230,6 +233,7 @@ def _to_device(t, device):
 
 
 _side_streams: dict = {}
+HOST_GROUPS = 8  # head groups of the pipelined host-tensor forward
 
 
 def _pipelined_host_forward(q, k, v, gamma, normalize, chunk, eps, out, masked=True):
@@ -240,10 +244,11 @@ def _pipelined_host_forward(q, k, v, gamma, normalize, chunk, eps, out, masked=T
     be cut into at least two groups."""
     B, H, n, d = q.shape
     dv = v.shape[-1]
-    # heads per group: a divisor of H giving about eight groups (the copies then bound the
-    # call to within a group's compute and output copy of the link time), at least two
+    # heads per group: a divisor of H giving at least HOST_GROUPS groups (the copies then
+    # bound the call to within a group's compute and output copy of the link time), at
+    # least two
     divisors = [c for c in range(H, 0, -1) if H % c == 0]
-    gh = next((c for c in divisors if B * H // c >= 8), next((c for c in divisors if B * H // c >= 2), 0))
+    gh = next((c for c in divisors if B * H // c >= HOST_GROUPS), next((c for c in divisors if B * H // c >= 2), 0))
     if gh == 0 or not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         return None
     device = torch.device("cuda", torch.cuda.current_device())

@@ -163,6 +163,15 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
  */
 int hla2_workspace_status(const void* workspace, hla2_stream_t stream);
 
+/*
+ * Self-test of the bounded device-side waits: launches one CTA that waits, with the same
+ * bounded poll the tcgen05 kernels use (over a second), on an mbarrier that nothing
+ * arrives at.  The wait gives up, records site 90 in the status word at the start of
+ * `workspace` (>= 16 bytes, 16-byte aligned) and the kernel returns; hla2_workspace_status
+ * then reports HLA2_ERR_TIMEOUT, and the context stays usable.  Asynchronous on `stream`.
+ */
+int hla2_selftest_wait_timeout(void* workspace, hla2_stream_t stream);
+
 /* Scratch bytes hla2_backward needs; (size_t)-1 for rejected arguments. */
 size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
                                      int normalize);
