@@ -444,9 +444,9 @@ def measure_ahla(dev, dist: Dist, hbm_gbs: float, bf16_tflops: float, steps: int
 
 
 def measure_unmasked(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5, n: int | None = None,
-                     chunk: int = 64):
+                     chunk: int = 128):
     """Unmasked-output row: q^T S C on the long-context shapes (B=1 H=16 n=65536 d=dv=64
-    bf16, decay linspace(0.99, 0.9999), unnormalised) through the mma.sync chunk kernel;
+    bf16, decay linspace(0.99, 0.9999), unnormalised; chunk 128: the tcgen05 kernels);
     1,048,576 tokens per step; inputs + output exceed the L2."""
     import dataclasses
 
@@ -491,7 +491,7 @@ def run_only(args, dist: Dist, dev):
         row = measure_decode_mq(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs)
     elif args.only == "unmasked":
         row = measure_unmasked(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n,
-                               chunk=args.chunk or 64)
+                               chunk=args.chunk or 128)
     elif args.only == "ahla":
         row = measure_ahla(dev, dist, hbm_gbs, bf16_tflops, steps=args.steps, warmup=args.warmup, n=args.n)
     else:
@@ -611,7 +611,7 @@ def run_ours(args, dist: Dist):
                      "decode_mq": measure_decode_mq(dev, dist, hbm_gbs),
                      "train": measure_train(dev, dist, bf16_tflops, hbm_gbs),
                      "ahla": measure_ahla(dev, dist, hbm_gbs, bf16_tflops),
-                     "unmasked": measure_unmasked(dev, dist, hbm_gbs, chunk=64)}
+                     "unmasked": measure_unmasked(dev, dist, hbm_gbs)}
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

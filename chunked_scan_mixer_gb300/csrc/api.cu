@@ -240,8 +240,9 @@ bool tc_disabled() {
 
 Path choose_forward_path(int dtype, int d, int dv, int W, int normalize, bool want_final, const DevInfo& di,
                          bool unmasked = false) {
-    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !normalize && !want_final && !unmasked &&
-        !tc_disabled() && fwd_chunk_tc_smem() <= (size_t)di.smem_optin && fwd_chunk_tc_available())
+    (void)unmasked;  // the tcgen05 kernel has both outputs
+    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !normalize && !want_final && !tc_disabled() &&
+        fwd_chunk_tc_smem() <= (size_t)di.smem_optin && fwd_chunk_tc_available())
         return Path::kTc;
     if (dtype == HLA2_BF16) {
         const size_t s = fwd_chunk_mma_smem(d, dv, W, true);

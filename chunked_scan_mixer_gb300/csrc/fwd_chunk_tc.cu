@@ -19,6 +19,12 @@
 // computes [Q~^T ; P~^T] V -> T1 (dC, dZ; Q~ = diag(g^(Wc-1-j)) Q) and [K~^T ; K~^T] K -> T3
 // (dS twice, so that every thread owns 16 of its columns), accumulating S, C, Z from zero.
 //
+// UM (unmasked output q^T S C = p^T C, section summary §3 and §4.1): MMA3 forms P Q^T and
+// P C0 (C0 in the Z0 slot), EPI3 masks with g^(r-j), out = g^(r+1) P C0 + B~ V, EPI2 writes
+// Q~ = diag(g^(Wc-1-j)) Q in place of P~ so that the state product gives dC, and the
+// summary pass needs no A~ or P: after the scaled copies it forms [Q~^T ; Q~^T] V (dC
+// twice) and [K~^T ; K~^T] K (dS), so C lands in both the C and the Z slots.
+//
 // Roles: warp 0 allocates tensor memory and one of its threads issues the TMA loads and every
 // MMA; warps 1..8 move data between tensor memory, registers and shared memory (warp w reads
 // TMEM lanes 32*(w%4)..+31, i.e. token/feature rows, and half (w-1)/4 of the columns).  Two
@@ -108,10 +114,11 @@ __device__ __forceinline__ void masked_block(uint32_t src, uint32_t dst, int r, 
     tc::tmem_st16(dst, pk);
 }
 
-template <int MODE>
+template <int MODE, bool UM>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_chunk_tc_kernel(const __grid_constant__ TcMaps maps, const ChunkArgs a, int* status) {
     constexpr bool SUMMARY = MODE == kSummary;
+    constexpr bool CHAIN = !(UM && SUMMARY);  // A~ and P are formed
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* gp = reinterpret_cast<float*>(sm + oGP);
@@ -171,29 +178,33 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc::mbar_wait(&bars[FULLKV], ph, abort, status, 2);
                 if (it > 0) tc::mbar_wait(&bars[BS], ph ^ 1, abort, status, 3);
                 tc::fence_after_sync();
-                // MMA1: A = Q K^T -> T0T1
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sK + 32 * ks, 16, 1024),
-                               I_AB, ks > 0);
-                tc::mma_commit(&bars[BA]);
-                tc::mbar_wait(&bars[BAT], ph, abort, status, 4);
-                tc::fence_after_sync();
-                // MMA2: A~ K -> T2;  Q S0 -> T0
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_ts(tmem + T2, tmem + T3 + 8 * ks, tc::smem_desc(sK + 2048 * ks, 16, 1024), I_TS64, ks > 0);
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sS0 + 2048 * ks, 16, 1024),
-                               I_QX, ks > 0);
-                tc::mma_commit(&bars[BP]);
+                if (CHAIN) {
+                    // MMA1: A = Q K^T -> T0T1
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024),
+                                   tc::smem_desc(sK + 32 * ks, 16, 1024), I_AB, ks > 0);
+                    tc::mma_commit(&bars[BA]);
+                    tc::mbar_wait(&bars[BAT], ph, abort, status, 4);
+                    tc::fence_after_sync();
+                    // MMA2: A~ K -> T2;  Q S0 -> T0
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_ts(tmem + T2, tmem + T3 + 8 * ks, tc::smem_desc(sK + 2048 * ks, 16, 1024), I_TS64,
+                                   ks > 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024),
+                                   tc::smem_desc(sS0 + 2048 * ks, 16, 1024), I_QX, ks > 0);
+                    tc::mma_commit(&bars[BP]);
+                }
                 tc::mbar_wait(&bars[BPS], ph, abort, status, 5);
                 tc::fence_after_sync();
                 if (!SUMMARY) {
-                    // MMA3: B = Q P^T -> T0T1;  Q Z0 -> T2
+                    // MMA3: B = Q P^T -> T0T1;  Q Z0 -> T2   (unmasked: P Q^T and P C0)
+                    const uint32_t sL = UM ? sP : sQ, sR = UM ? sQ : sP;
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sP + 32 * ks, 16, 1024),
+                        tc::mma_ss(tmem + T0, tc::smem_desc(sL + 32 * ks, 16, 1024), tc::smem_desc(sR + 32 * ks, 16, 1024),
                                    I_AB, ks > 0);
                     for (int ks = 0; ks < 4; ++ks)
-                        tc::mma_ss(tmem + T2, tc::smem_desc(sQ + 32 * ks, 16, 1024),
+                        tc::mma_ss(tmem + T2, tc::smem_desc(sL + 32 * ks, 16, 1024),
                                    tc::smem_desc(sZ0 + 2048 * ks, 16, 1024), I_QX, ks > 0);
                     tc::mma_commit(&bars[BB]);
                     tc::mbar_wait(&bars[BBT], ph, abort, status, 6);
@@ -211,8 +222,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 } else {
                     if (it + 1 < nit) load_q(c_begin + it + 1);  // Q~ (P slot) is used below, not Q
                     // [Q~^T ; P~^T] V -> T1 (dC, dZ);  [K~^T ; K~^T] K -> T3 (dS twice)
+                    // (unmasked: [Q~^T ; Q~^T] V, dC twice)
                     for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_ss(tmem + T1, tc::smem_desc(sP + 2048 * ks, 2 * kTile, 1024),
+                        tc::mma_ss(tmem + T1, tc::smem_desc(sP + 2048 * ks, UM ? 0 : 2 * kTile, 1024),
                                    tc::smem_desc(sV + 2048 * ks, 16, 1024), I_ST64, ks > 0);
                     for (int ks = 0; ks < 8; ++ks)
                         tc::mma_ss(tmem + T3, tc::smem_desc(sKt + 2048 * ks, 0, 1024),
@@ -287,18 +299,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             // ---- EPI1: A~ -> T3;  K~ (and Q~) -> smem -----------------------------------
             tc::mbar_wait(&bars[FULLQ], ph, abort, status, 11);
             tc::mbar_wait(&bars[FULLKV], ph, abort, status, 12);
-            tc::mbar_wait(&bars[BA], ph, abort, status, 13);
-            tc::fence_after_sync();
+            if (CHAIN) {
+                tc::mbar_wait(&bars[BA], ph, abort, status, 13);
+                tc::fence_after_sync();
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int cb = 64 * h + 32 * p;
-                const float first = r >= cb ? gp[r - cb] : 0.f;
-                masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, ginv);
+                for (int p = 0; p < 2; ++p) {
+                    const int cb = 64 * h + 32 * p;
+                    const float first = r >= cb ? gp[r - cb] : 0.f;
+                    masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, ginv);
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[BAT]);
             }
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[BAT]);
             // K~ (and Q~ in summary mode) rows, features 32h .. 32h+31, while MMA2 runs; they
             // are first read by the MMAs issued after EPI2 / EPI3 (fenced there)
             {
@@ -313,9 +327,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
 
             // ---- EPI2: P = g^(r+1) Q S0 + A~ K;  P, P~ -> smem ---------------------------
-            tc::mbar_wait(&bars[BP], ph, abort, status, 14);
-            tc::fence_after_sync();
-            {
+            // (unmasked: P -> smem and Q~ in the P~ slot; the unmasked summary skips this)
+            if (CHAIN) {
+                tc::mbar_wait(&bars[BP], ph, abort, status, 14);
+                tc::fence_after_sync();
                 const float s1 = gp[r + 1];
                 const float w2 = r < Wc ? gp[2 * (Wc - 1 - r)] : 0.f;
 #pragma unroll
@@ -331,7 +346,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int j = 0; j < 2; ++j) {
                         const uint32_t off = tc::sw128_chunk(r, 4 * h + 2 * half + j);
                         if (!SUMMARY) *reinterpret_cast<uint4*>(sP + off) = pack8(&pv[8 * j], 1.f);
-                        *reinterpret_cast<uint4*>(sPt + off) = pack8(&pv[8 * j], w2);
+                        if (!UM) *reinterpret_cast<uint4*>(sPt + off) = pack8(&pv[8 * j], w2);
+                    }
+                }
+                if (UM) {  // Q~ rows, features 32h .. 32h+31 (S0 in this slot has been read by MMA2)
+                    const float w1 = r < Wc ? gp[Wc - 1 - r] : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t off = tc::sw128_chunk(r, 4 * h + j);
+                        *reinterpret_cast<uint4*>(sPt + off) = scale_chunk(*reinterpret_cast<const uint4*>(sQ + off), w1);
                     }
                 }
             }
@@ -344,11 +367,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 // ---- EPI3: B~ -> T3 ----------------------------------------------------------
                 tc::mbar_wait(&bars[BB], ph, abort, status, 15);
                 tc::fence_after_sync();
+                constexpr int BP2 = UM ? 1 : 2;  // decay power of the second product
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
                     const int cb = 64 * h + 32 * p;
-                    const float first = r >= cb ? gp[2 * (r - cb)] : 0.f;
-                    masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, ginv * ginv);
+                    const float first = r >= cb ? gp[BP2 * (r - cb)] : 0.f;
+                    masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, UM ? ginv : ginv * ginv);
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
@@ -358,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 // ---- EPI4a: out = g^(2(r+1)) Q Z0 + B~ V ---------------------------------------
                 tc::mbar_wait(&bars[BO], ph, abort, status, 16);
                 tc::fence_after_sync();
-                const float s2 = gp[2 * (r + 1)];
+                const float s2 = gp[BP2 * (r + 1)];
                 bf16* out = static_cast<bf16*>(a.out) + ((size_t)bh * a.n + (size_t)c * kW + r) * kD + 32 * h;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
@@ -389,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     // ST rows < 64: dS in ST columns 0..63 (T1); rows >= 64: dZ in columns 64..127 (T3)
                     tc::tmem_ld32(lrow + (r < 64 ? T1 : T3) + 32 * h, v);
                     tc::tmem_wait_ld();
-                    const float decay = r < 64 ? rho : rho2;
+                    const float decay = r < 64 || UM ? rho : rho2;  // unmasked: the Z slot holds C
 #pragma unroll
                     for (int j = 0; j < 32; ++j) st[j] = decay * st[j] + __uint_as_float(v[j]);
                 } else {
@@ -398,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     uint32_t w[16];
                     tc::tmem_ld16(lrow + T3 + 32 * h + 16 * (r >> 6), w);
                     tc::tmem_wait_ld();
-                    const float decay = r < 64 ? rho : rho2;
+                    const float decay = r < 64 || UM ? rho : rho2;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) st[j] = decay * st[j] + __uint_as_float(v[j]);
 #pragma unroll
@@ -474,14 +498,10 @@ int launch_fwd_chunk_tc(const ChunkArgs& a, int mode, int* status, cudaStream_t 
     if (!make_map(&maps.q, a.q, a.BH, a.n) || !make_map(&maps.k, a.k, a.BH, a.n) || !make_map(&maps.v, a.v, a.BH, a.n))
         return -2;
     dim3 grid(a.nseg_launch, a.BH);
-    cudaError_t e;
-    if (mode == kSummary) {
-        e = cudaFuncSetAttribute(fwd_chunk_tc_kernel<kSummary>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e == cudaSuccess) fwd_chunk_tc_kernel<kSummary><<<grid, kThreads, kSmemBytes, st>>>(maps, a, status);
-    } else {
-        e = cudaFuncSetAttribute(fwd_chunk_tc_kernel<kOutput>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e == cudaSuccess) fwd_chunk_tc_kernel<kOutput><<<grid, kThreads, kSmemBytes, st>>>(maps, a, status);
-    }
+    auto kfn = mode == kSummary ? (a.unmasked ? fwd_chunk_tc_kernel<kSummary, true> : fwd_chunk_tc_kernel<kSummary, false>)
+                                : (a.unmasked ? fwd_chunk_tc_kernel<kOutput, true> : fwd_chunk_tc_kernel<kOutput, false>);
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess) kfn<<<grid, kThreads, kSmemBytes, st>>>(maps, a, status);
     if (e != cudaSuccess) return -1;
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

@@ -223,3 +223,40 @@ def test_prefill_then_decode_matches_oracle():
                                     gamma=x["gamma"].cuda(), masked=False))
     o = torch.stack(outs, dim=2).cpu()
     assert rel_err(np64(o), oracle(x)[:, :, n0:]) <= 2e-2
+
+
+# ---- the tcgen05 path (bf16, d = dv = 64, chunk 128, unnormalised) ----------------------------
+
+def _run_kernel(x, kernel=None):
+    import os
+
+    old = os.environ.pop("HLA2_KERNEL", None)
+    if kernel:
+        os.environ["HLA2_KERNEL"] = kernel
+    try:
+        o = run_gpu(x, chunk=128)
+        hla.check_status()
+        return o.cpu()
+    finally:
+        os.environ.pop("HLA2_KERNEL", None)
+        if old is not None:
+            os.environ["HLA2_KERNEL"] = old
+
+
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 1000, 128 * 40, 4096 + 33])
+def test_tcgen05_path_lengths(n):
+    x = inputs.make_custom(1, 3, n, 64, 64, torch.bfloat16, seed=n + 70, gamma=(0.97, 0.9999))
+    o = _run_kernel(x)
+    assert rel_err(np64(o), oracle(x)) <= 2e-2
+
+
+def test_tcgen05_and_mma_paths_agree():
+    """Unmasked output of the tcgen05 kernels and of the mma.sync kernels on the same inputs
+    (many heads, multi-chunk segments)."""
+    x = inputs.make_custom(2, 8, 128 * 24 + 5, 64, 64, torch.bfloat16, seed=71, gamma=(0.99, 0.9999))
+    a = _run_kernel(x)
+    b = _run_kernel(x, "mma")
+    ref = oracle(x)
+    assert rel_err(np64(a), ref) <= 2e-2
+    assert rel_err(np64(b), ref) <= 2e-2
+    assert rel_err(np64(a), np64(b)) <= 2e-2
