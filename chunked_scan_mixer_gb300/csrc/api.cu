@@ -1063,6 +1063,160 @@ static int ahla_check(int B, int H, int n, int d, int dv, int chunk, int dtype, 
 }
 
 // chunk 128 runs the tcgen05 kernel, chunks 32 and 64 the mma.sync one
+// ---- masked third-order output (gamma = 1): first-order pass, then the second-order forward ----
+
+static constexpr int kHla3Unit = 16;  // value width of the denominator passes (column 0 is 1)
+
+static int hla3_la_width(int d, int dv, int chunk, const DevInfo& di) {
+    for (int W = chunk < 64 ? chunk : 64; W >= 16; W /= 2)
+        if (first_order_smem(d, dv, W) <= (size_t)di.smem_optin &&
+            first_order_smem(d, kHla3Unit, W) <= (size_t)di.smem_optin)
+            return W;
+    return 0;
+}
+
+// Chunk width of the third-order output's second-order passes: the largest <= chunk with a
+// forward kernel for both value widths (the result does not depend on the width).
+static int hla3_second_width(int dtype, int d, int dv, int chunk, int normalize, const DevInfo& di) {
+    for (int W = chunk; W >= 16; W /= 2)
+        if (choose_forward_path(dtype, d, dv, W, 0, false, di) != Path::kNone &&
+            (!normalize || choose_forward_path(dtype, d, kHla3Unit, W, 0, false, di) != Path::kNone))
+            return W;
+    return 0;
+}
+
+struct Hla3Layout {
+    int W = 0;
+    int W2 = 0;  // chunk width of the second-order passes
+    Plan p;
+    size_t PB = 0, Pin = 0;  // first-order workspace (floats, in the scratch region)
+    size_t scratch = 0;      // bytes of the scratch region (first-order and second-order calls in turn)
+    size_t u = 0, e0 = 0, u1 = 0, den = 0, total = 0;  // byte offsets
+};
+
+static Hla3Layout hla3_layout(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize,
+                              const DevInfo& di) {
+    Hla3Layout L;
+    L.W = hla3_la_width(d, dv, chunk, di);
+    L.W2 = hla3_second_width(dtype, d, dv, chunk, normalize, di);
+    if (!L.W || !L.W2) {
+        L.W = 0;
+        return L;
+    }
+    chunk = L.W2;
+    L.p = make_plan(B, H, n, d, dv, L.W, di.sms, blocks_per_sm(first_order_smem(d, dv, L.W), 256, 4, di));
+    const size_t BH = (size_t)B * H, ns = L.p.nseg, nsm = ns > 0 ? ns - 1 : 0;
+    const size_t wmax = dv > kHla3Unit ? dv : kHla3Unit;
+    L.PB = kStatusFloats;
+    L.Pin = align64(L.PB + BH * nsm * (size_t)d * wmax);
+    const size_t la = align64(L.Pin + BH * ns * (size_t)d * wmax) * sizeof(float);
+    size_t f1 = hla2_forward_workspace_bytes(B, H, n, d, dv, chunk, dtype, 0, 0);
+    size_t f2 = normalize ? hla2_forward_workspace_bytes(B, H, n, d, kHla3Unit, chunk, dtype, 0, 0) : 0;
+    if (f1 == (size_t)-1 || f2 == (size_t)-1) {
+        L.W = 0;
+        return L;
+    }
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    L.scratch = up(la > f1 ? (la > f2 ? la : f2) : (f1 > f2 ? f1 : f2));
+    const size_t es = dtype == HLA2_BF16 ? 2 : 4, rows = BH * (size_t)n;
+    size_t o = L.scratch;
+    L.u = o;
+    o += up(rows * dv * es);
+    if (normalize) {
+        L.e0 = o;
+        o += up(rows * kHla3Unit * es);
+        L.u1 = o;
+        o += up(rows * kHla3Unit * es);
+        L.den = o;
+        o += up(rows * kHla3Unit * es);
+    }
+    L.total = o;
+    return L;
+}
+
+extern "C" size_t hla2_hla3_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
+                                                    int normalize) {
+    if (check_common(B, H, n, d, dv, dtype, normalize) != HLA2_OK || !dim_ok(chunk)) return (size_t)-1;
+    const Hla3Layout L = hla3_layout(B, H, n, d, dv, chunk, dtype, normalize, dev_info());
+    return L.W ? L.total : (size_t)-1;
+}
+
+// first-order pass u = masked linear attention (q, k, values) into `u`
+static int hla3_first_order(const void* q, const void* k, const void* vals, void* u, int B, int H, int n, int d,
+                            int w, const Hla3Layout& L, void* ws, bool bf, cudaStream_t st) {
+    LaArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = vals;
+    a.u = u;
+    a.BH = B * H;
+    a.H = H;
+    a.n = n;
+    a.d = d;
+    a.dv = w;
+    a.W = L.W;
+    a.nchunks = L.p.nchunks;
+    a.seg_chunks = L.p.seg_chunks;
+    a.nseg = L.p.nseg;
+    a.gamma = nullptr;
+    a.ws = static_cast<float*>(ws);
+    a.PB = L.PB;
+    a.Pin = L.Pin;
+    return launch_first_order_forward(a, bf, st) ? cuda_fail("first-order pass") : HLA2_OK;
+}
+
+extern "C" int hla2_hla3_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n, int d,
+                                 int dv, const float* gamma, int normalize, int chunk, hla2_stream_t stream,
+                                 const hla2_opts* opts) {
+    NvtxScope nvtx("hla2_hla3_forward");
+    if (!opts) return fail(HLA2_ERR_INVALID_ARG, "opts must not be NULL");
+    int rc = check_common(B, H, n, d, dv, opts->dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
+    if (normalize && !isfinite(opts->eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
+    if (opts->flags) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_hla3_forward");
+    if (gamma) return fail(HLA2_ERR_UNSUPPORTED, "the third-order scan is defined for gamma = 1 (pass NULL)");
+    if (opts->init_state || opts->final_state)
+        return fail(HLA2_ERR_UNSUPPORTED, "the third-order forward keeps no state across calls");
+    if ((long)B * H == 0 || n == 0) return succeed();
+    if (!q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must not be NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
+    const DevInfo di = dev_info();
+    const Hla3Layout L = hla3_layout(B, H, n, d, dv, chunk, opts->dtype, normalize, di);
+    if (!L.W) return fail(HLA2_ERR_UNSUPPORTED, "no kernel for d %d, dv %d, chunk %d", d, dv, chunk);
+    if (!opts->workspace || opts->workspace_bytes < L.total)
+        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.total,
+                    opts->workspace ? opts->workspace_bytes : (size_t)0);
+    if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(opts->workspace);
+    const bool bf = opts->dtype == HLA2_BF16;
+    hla2_opts so{};
+    so.dtype = opts->dtype;
+    so.eps = opts->eps;
+    so.workspace = base;
+    so.workspace_bytes = L.scratch;
+    cudaGetLastError();
+    // numerator: the masked second-order output with the first-order outputs as values
+    if ((rc = hla3_first_order(q, k, v, base + L.u, B, H, n, d, dv, L, base, bf, st)) != HLA2_OK) return rc;
+    if ((rc = hla2_forward(q, k, base + L.u, out, B, H, n, d, dv, nullptr, 0, L.W2, stream, &so)) != HLA2_OK)
+        return rc;
+    if (normalize) {  // denominator: the same with v -> 1 (value rows e_0, column 0)
+        const size_t rows = (size_t)B * H * n;
+        if (launch_unit_rows(base + L.e0, rows, kHla3Unit, bf, st)) return cuda_fail("unit value rows");
+        if ((rc = hla3_first_order(q, k, base + L.e0, base + L.u1, B, H, n, d, kHla3Unit, L, base, bf, st)) !=
+            HLA2_OK)
+            return rc;
+        if ((rc = hla2_forward(q, k, base + L.u1, base + L.den, B, H, n, d, kHla3Unit, nullptr, 0, L.W2, stream,
+                               &so)) != HLA2_OK)
+            return rc;
+        if (launch_divide_rows(out, base + L.den, rows, dv, kHla3Unit, opts->eps, bf, st))
+            return cuda_fail("normalisation");
+    }
+    return succeed();
+}
+
 static Plan ahla_plan(int B, int H, int n, int d, int chunk) {
     const DevInfo di = dev_info();
     const int per_sm = chunk == 128 ? blocks_per_sm(ahla_tc_smem(), 288, 2, di)

@@ -186,6 +186,27 @@ int launch_decode_mq(float* key_state, float* head_state, const void* q, const v
 int launch_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
                             int d, int dv, const float* gamma, int normalize, float eps, bool is_bf16,
                             cudaStream_t st);
+// Masked first-order linear attention u_t = sum_{l <= t} g^(t-l) (q_t . k_l) v_l, the inner
+// pass of the third-order output (linattn.cu).  Workspace floats: PB [BH][nseg-1][d*dv],
+// Pin [BH][nseg][d*dv].
+struct LaArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* u;
+    int BH, H, n, d, dv, W, nchunks, seg_chunks, nseg, seg0;
+    const float* gamma;
+    float* ws;
+    size_t PB, Pin;
+};
+int launch_first_order_forward(const LaArgs& a, bool is_bf16, cudaStream_t st);
+size_t first_order_smem(int d, int dv, int W);
+// rows x w with column 0 = 1, in the input type (bf16 or float32)
+int launch_unit_rows(void* e0, size_t rows, int w, bool is_bf16, cudaStream_t st);
+// out[row][:] /= (den[row * w] + eps), in place, bf16 or float32
+int launch_divide_rows(void* out, const void* den, size_t rows, int dv, int w, float eps, bool is_bf16,
+                       cudaStream_t st);
+
 // Bounded-wait self-test: waits on an mbarrier nobody arrives at; records site 90 in *status.
 int launch_wait_timeout_selftest(int* status, cudaStream_t st);
 int launch_state_compact(const float* src, float* dst, long heads, int d, int dv, bool to_compact, cudaStream_t st);

@@ -107,6 +107,10 @@ def lib():
         L.hla2_ahla_decode_step.restype = I
         L.hla2_compact_state_floats.argtypes = [I, I]
         L.hla2_compact_state_floats.restype = Z
+        L.hla2_hla3_forward_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
+        L.hla2_hla3_forward_workspace_bytes.restype = Z
+        L.hla2_hla3_forward.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
+        L.hla2_hla3_forward.restype = I
         L.hla2_selftest_wait_timeout.argtypes = [P, P]
         L.hla2_selftest_wait_timeout.restype = I
         L.hla2_mq_head_state_floats.argtypes = [I, I]
@@ -126,7 +130,7 @@ EXPORTED_SYMBOLS = (
     "hla2_backward", "hla2_decode_step", "hla2_forward_noalloc", "hla2_compact_state_floats",
     "hla2_state_to_compact", "hla2_state_from_compact", "hla2_ahla_forward_workspace_bytes", "hla2_ahla_forward",
     "hla2_ahla_state_floats", "hla2_ahla_decode_step", "hla2_mq_head_state_floats", "hla2_decode_step_mq",
-    "hla2_selftest_wait_timeout",
+    "hla2_selftest_wait_timeout", "hla2_hla3_forward_workspace_bytes", "hla2_hla3_forward",
 )
 
 FLAG_COMPACT_STATE = 4
@@ -531,4 +535,30 @@ def decode_step_mq(key_state, head_state, q, k, v, gamma=None, normalize=False, 
     rc = L.hla2_decode_step_mq(_ptr(key_state), _ptr(head_state), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), N, Hk,
                                group, d, dv, _ptr(g), int(normalize), _stream_handle(device), ctypes.byref(opts))
     _check("hla2_decode_step_mq", rc)
+    return o
+
+
+def hla3_forward(q, k, v, normalize=False, chunk=64, eps=1e-6, out=None):
+    """Masked third-order output at gamma = 1 (every factor of A A^T A and the partial product
+    of the first two causally masked).  q, k [B,H,n,d]; v [B,H,n,dv] on the GPU, float32 or
+    bfloat16.  Returns out [B,H,n,dv]."""
+    L = lib()
+    if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must all be float32 or all bfloat16")
+    if q.device.type != "cuda":
+        raise ValueError("q, k, v must be CUDA tensors")
+    B, H, n, d = q.shape
+    dv = v.shape[-1]
+    device = q.device
+    qd, kd, vd = (t.contiguous() for t in (q, k, v))
+    o = out if out is not None else torch.empty((B, H, n, dv), dtype=q.dtype, device=device)
+    sh = _stream_handle(device)
+    nbytes = L.hla2_hla3_forward_workspace_bytes(B, H, n, d, dv, chunk, _DTYPES[q.dtype], int(normalize))
+    if nbytes == ctypes.c_size_t(-1).value:
+        nbytes = 0
+    ws = _workspace(int(nbytes), device, sh)
+    opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), int(nbytes), None, None, None,
+                0, 0)
+    _check("hla2_hla3_forward", L.hla2_hla3_forward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), B, H, n, d, dv, None,
+                                                    int(normalize), chunk, sh, ctypes.byref(opts)))
     return o

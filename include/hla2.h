@@ -210,6 +210,26 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
                      int N, int H, int d, int dv, const float* gamma, int normalize,
                      hla2_stream_t stream, const hla2_opts* opts);
 
+/*
+ * Masked third-order HLA at gamma = 1 (technical summary item "3. Dritte Ordnung HLA": the
+ * product A A^T A with A = Q K^T, masked so that strict causality holds; section summary:
+ * the chunk scan of this case is exact for gamma = 1).  Every factor and the partial product
+ * of the first two carry the causal mask:
+ *   o_t = sum_{j <= t} sum_{i <= j} sum_{l <= j} (q_t . k_i)(k_i . q_j)(q_j . k_l) v_l,
+ * i.e. the masked second-order output whose values are the first-order outputs
+ * u_j = sum_{l <= j} (q_j . k_l) v_l.  It runs as a chunked first-order pass (SIMT) into the
+ * workspace, then hla2_forward on (q, k, u) -- the tcgen05 kernels for bf16, d = dv = 64,
+ * chunk 128.  normalize != 0 divides by the same sum with v -> 1 (+ opts->eps), computed the
+ * same way with the value rows (1, 0, ..., 0).  gamma must be NULL (HLA2_ERR_UNSUPPORTED
+ * otherwise); no init_state / final_state; opts->flags must be 0.  Tensors as for
+ * hla2_forward; the workspace is hla2_hla3_forward_workspace_bytes.
+ */
+size_t hla2_hla3_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
+                                         int normalize);
+int hla2_hla3_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n, int d,
+                      int dv, const float* gamma, int normalize, int chunk, hla2_stream_t stream,
+                      const hla2_opts* opts);
+
 /* Floats in one head's part of the multi-query state: C d*dv | G d*dv | m d | h d. */
 size_t hla2_mq_head_state_floats(int d, int dv);
 

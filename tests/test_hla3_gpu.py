@@ -1,0 +1,73 @@
+"""GPU masked third-order output (gamma = 1) against the float64 oracle
+(``oracle/hla3_oracle.py``), through the C ABI.  Bars: 1e-4 for float32 inputs, 2e-2 for
+bf16 inputs (the oracle runs on the same bf16-rounded values)."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import chunked_scan_mixer_gb300 as hla
+from chunked_scan_mixer_gb300 import inputs
+from chunked_scan_mixer_gb300.hla2 import Opts
+from oracle import hla3_oracle as O3
+
+from .helpers import np64, rel_err, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def run(x, **kw):
+    return hla.hla3_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), **kw).cpu()
+
+
+def test_tiny_fp32_against_the_triple_sum():
+    x = inputs.make_custom(1, 2, 24, 16, 16, torch.float32, seed=80)
+    ref = O3.brute_force_forward(np64(x["q"]), np64(x["k"]), np64(x["v"]))
+    for chunk in (16, 32):
+        assert rel_err(np64(run(x, chunk=chunk)), ref) <= 1e-4, chunk
+
+
+@pytest.mark.parametrize("d, dv, chunk, n", [(32, 64, 16, 300), (64, 32, 32, 333), (16, 128, 64, 200),
+                                              (128, 128, 32, 150)])
+def test_fp32_shapes_and_segments(d, dv, chunk, n):
+    x = inputs.make_custom(1, 2, n, d, dv, torch.float32, seed=d + dv + n)
+    ref = O3.serial_forward(np64(x["q"]), np64(x["k"]), np64(x["v"]))
+    assert rel_err(np64(run(x, chunk=chunk)), ref) <= 1e-4
+
+
+@pytest.mark.parametrize("chunk, n", [(64, 1000), (128, 1000), (128, 129), (32, 77)])
+def test_bf16(chunk, n):
+    """chunk 128 at d = 64 runs the second pass on the tcgen05 kernels."""
+    x = inputs.make_custom(1, 3, n, 64, 64, torch.bfloat16, seed=81 + n)
+    ref = O3.serial_forward(np64(x["q"]), np64(x["k"]), np64(x["v"]))
+    assert rel_err(np64(run(x, chunk=chunk)), ref) <= 2e-2
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_normalized(dtype):
+    x = inputs.make_custom(2, 2, 260, 32, 32, dtype, seed=82, qk="softplus", v_scale="unit")
+    ref = O3.serial_forward(np64(x["q"]), np64(x["k"]), np64(x["v"]), normalize=True, eps=1e-6)
+    got = run(x, chunk=32, normalize=True, eps=1e-6)
+    assert rel_err(np64(got), ref) <= tol_for(dtype)
+
+
+def test_causality():
+    x = inputs.make_custom(1, 2, 300, 32, 32, torch.float32, seed=83)
+    a = run(x, chunk=32)
+    y = {key: (val.clone() if key in ("q", "k", "v") else val) for key, val in x.items()}
+    y["q"][:, :, 200:] += 1.0
+    y["v"][:, :, 200:] = 0
+    b = run(y, chunk=32)
+    assert torch.equal(a[:, :, :200], b[:, :, :200])
+
+
+def test_decay_is_refused():
+    L = hla.lib()
+    p = ctypes.c_void_p(16)
+    g = torch.full((1,), 0.9, device="cuda")
+    o = Opts(0, 1e-6, None, 0, None, None, None, 0, 0)
+    rc = L.hla2_hla3_forward(p, p, p, p, 1, 1, 16, 16, 16, ctypes.c_void_p(g.data_ptr()), 0, 16, None,
+                             ctypes.byref(o))
+    assert rc == -2 and b"gamma" in L.hla2_last_error()
+    assert np.isfinite(rc)
