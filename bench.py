@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode and training rows measured after the headline")
     ap.add_argument("--only", choices=("decode", "decode_compact", "decode_unmasked", "decode_mq", "train", "ahla",
-                                       "unmasked"),
+                                       "unmasked", "hla3"),
                     default=None,
                     help="measure only this row (for profiler captures; --steps/--warmup apply)")
     ap.add_argument("--decode-seqs", type=int, default=256,
@@ -482,11 +482,47 @@ def measure_unmasked(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: i
                          "frac": achieved / hbm_gbs, "kernel": "output_pass", "algorithmic_bytes_per_launch": nbytes}}
 
 
+def measure_hla3(dev, dist: Dist, hbm_gbs: float, steps: int = 30, warmup: int = 5, n: int | None = None):
+    """Third-order row: the masked third-order output at gamma = 1 on the long-context shapes
+    (B=1 H=16 n=65536 d=dv=64 bf16, unnormalised, chunk 128): the first-order pass on the AHLA
+    tcgen05 kernel in its first-order mode, then the second-order tcgen05 forward."""
+    import dataclasses
+
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = inputs.WORKLOADS["long"]
+    if n is not None:
+        w = dataclasses.replace(w, n=n)
+    x = inputs.make(w, device=dev, seed=replica_seed(w.seed, dist.rank))
+    q, k, v = x["q"], x["k"], x["v"]
+    out = torch.empty_like(v)
+
+    def one():
+        hla.hla3_forward(q, k, v, chunk=w.chunk, out=out)
+
+    ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
+    tokens = w.B * w.H * w.n
+    # two passes over q, k and a value tensor, each reading 3 x 128 B and writing 128 B a token
+    nbytes = 2 * tokens * (2 * w.d + 2 * w.dv) * 2
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"masked third-order HLA forward (gamma = 1): B={w.B} H={w.H} n={w.n} d=dv={w.d} bf16, "
+                        f"unnormalised, chunk {w.chunk}",
+            "metric": "third-order fwd tokens/s", "unit": "tokens/s", "value": dist.world * tokens / (ms * 1e-3),
+            "ms_per_step": ms, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "algorithmic_bytes_per_step": nbytes}}
+
+
 def run_only(args, dist: Dist, dev):
     hbm_gbs, bf16_tflops, _ = peaks()
     if args.only in ("decode", "decode_compact", "decode_unmasked"):
         row = measure_decode(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs,
                              compact=args.only == "decode_compact", masked=args.only != "decode_unmasked")
+    elif args.only == "hla3":
+        row = measure_hla3(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
     elif args.only == "decode_mq":
         row = measure_decode_mq(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs)
     elif args.only == "unmasked":
@@ -611,7 +647,8 @@ def run_ours(args, dist: Dist):
                      "decode_mq": measure_decode_mq(dev, dist, hbm_gbs),
                      "train": measure_train(dev, dist, bf16_tflops, hbm_gbs),
                      "ahla": measure_ahla(dev, dist, hbm_gbs, bf16_tflops),
-                     "unmasked": measure_unmasked(dev, dist, hbm_gbs)}
+                     "unmasked": measure_unmasked(dev, dist, hbm_gbs),
+                     "hla3": measure_hla3(dev, dist, hbm_gbs)}
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

@@ -18,6 +18,11 @@
 // Summary mode keeps MMA1, EPI1, MMA2, EPI2, then computes ST and R = [K^T ; K^T] Q -> T0
 // (undecayed), accumulating P, E, R from zero.
 //
+// FO (first-order mode) serves the third-order output's inner pass, masked first-order linear
+// attention u = Inner: the output pass writes Inner itself and skips MMA3 and EPI3, and the
+// summary pass skips MMA1 to EPI2 and the R product, keeping only the scaled keys and the
+// state product, whose P half is the segment's P (the E and R summaries are then unused).
+//
 // Roles as in the symmetric kernel (fwd_chunk_tc.cu): warp 0 allocates tensor memory and one
 // of its threads issues the TMA loads and every MMA; warps 1..8 move data between tensor
 // memory, registers and shared memory.  Two CTAs share an SM.  Every wait is bounded; on a
@@ -102,9 +107,10 @@ __device__ __forceinline__ void masked_block(uint32_t src, uint32_t dst, int r, 
     tc::tmem_st16(dst, pk);
 }
 
-template <bool SUMMARY>
+template <bool SUMMARY, bool FO>
 __global__ void __launch_bounds__(kThreads, 2)
     ahla_tc_kernel(const __grid_constant__ TcMaps maps, const AhlaArgs a, int* status) {
+    constexpr bool CHAIN = !(FO && SUMMARY);  // A~ and Inner are formed
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* gp = reinterpret_cast<float*>(sm + oGP);
@@ -164,23 +170,32 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc::mbar_wait(&bars[FULLKV], ph, abort, status, 32);
                 if (it > 0) tc::mbar_wait(&bars[BS], ph ^ 1, abort, status, 33);
                 tc::fence_after_sync();
-                // MMA1: A = Q K^T -> T0T1
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sK + 32 * ks, 16, 1024),
-                               I_AB, ks > 0);
-                tc::mma_commit(&bars[BA]);
-                tc::mbar_wait(&bars[BAT], ph, abort, status, 34);
-                tc::fence_after_sync();
-                // MMA2: A~ V -> T2;  Q P0 -> T0
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_ts(tmem + T2, tmem + T3 + 8 * ks, tc::smem_desc(sV + 2048 * ks, 16, 1024), I_TS64, ks > 0);
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sP0 + 2048 * ks, 16, 1024),
-                               I_QX, ks > 0);
-                tc::mma_commit(&bars[BP]);
+                if (CHAIN) {
+                    // MMA1: A = Q K^T -> T0T1
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024),
+                                   tc::smem_desc(sK + 32 * ks, 16, 1024), I_AB, ks > 0);
+                    tc::mma_commit(&bars[BA]);
+                    tc::mbar_wait(&bars[BAT], ph, abort, status, 34);
+                    tc::fence_after_sync();
+                    // MMA2: A~ V -> T2;  Q P0 -> T0
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_ts(tmem + T2, tmem + T3 + 8 * ks, tc::smem_desc(sV + 2048 * ks, 16, 1024), I_TS64,
+                                   ks > 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024),
+                                   tc::smem_desc(sP0 + 2048 * ks, 16, 1024), I_QX, ks > 0);
+                    tc::mma_commit(&bars[BP]);
+                }
                 tc::mbar_wait(&bars[BPS], ph, abort, status, 35);  // Inner and K~ written
                 tc::fence_after_sync();
-                if (!SUMMARY) {
+                if (FO) {
+                    if (it + 1 < nit) load_q(c_begin + it + 1);  // Q is no longer read
+                    // [K~^T ; K~^T] [V | Inner] -> T3T2 (dP; dE is not used)
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_ss(tmem + T3, tc::smem_desc(sKt + 2048 * ks, 0, 1024),
+                                   tc::smem_desc(sV + 2048 * ks, oIn - oV, 1024), I_ST, ks > 0);
+                } else if (!SUMMARY) {
                     // MMA3: A~ Inner -> T0;  Q E0 -> T1
                     for (int ks = 0; ks < 8; ++ks)
                         tc::mma_ts(tmem + T0, tmem + T3 + 8 * ks, tc::smem_desc(sIn + 2048 * ks, 16, 1024), I_TS64,
@@ -207,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc::mma_commit(&bars[BST]);
                 tc::mbar_wait(&bars[BST], ph, abort, status, 37);  // K, V (and Q) free
-                if (SUMMARY && it + 1 < nit) load_q(c_begin + it + 1);
+                if (SUMMARY && !FO && it + 1 < nit) load_q(c_begin + it + 1);
                 if (it + 1 < nit) {
                     load_kv(c_begin + it + 1);
                     ++loads;
@@ -265,18 +280,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int Wc = min(kW, a.n - c * kW);
             // ---- EPI1: A~ -> T3;  K~ -> smem ----------------------------------------------
             tc::mbar_wait(&bars[FULLKV], ph, abort, status, 41);
-            tc::mbar_wait(&bars[BA], ph, abort, status, 42);
-            tc::fence_after_sync();
+            if (CHAIN) {
+                tc::mbar_wait(&bars[BA], ph, abort, status, 42);
+                tc::fence_after_sync();
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int cb = 64 * h + 32 * p;
-                const float first = r >= cb ? gp[r - cb] : 0.f;
-                masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, ginv);
+                for (int p = 0; p < 2; ++p) {
+                    const int cb = 64 * h + 32 * p;
+                    const float first = r >= cb ? gp[r - cb] : 0.f;
+                    masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, ginv);
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[BAT]);
             }
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[BAT]);
             {
                 const float w1 = r < Wc ? gp[Wc - 1 - r] : 0.f;
 #pragma unroll
@@ -286,10 +303,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
 
-            // ---- EPI2: Inner = g^(r+1) Q P0 + A~ V -> smem -----------------------------------
-            tc::mbar_wait(&bars[BP], ph, abort, status, 43);
-            tc::fence_after_sync();
-            {
+            // ---- EPI2: Inner = g^(r+1) Q P0 + A~ V -> smem (first-order mode: also -> out) ----
+            if (CHAIN) {
+                tc::mbar_wait(&bars[BP], ph, abort, status, 43);
+                tc::fence_after_sync();
+                bf16* fo_out = static_cast<bf16*>(a.out) + ((size_t)bh * a.n + (size_t)c * kW + r) * kD + 32 * h;
                 const float s1 = r < Wc ? gp[r + 1] : 0.f;
                 const float keep = r < Wc ? 1.f : 0.f;
 #pragma unroll
@@ -302,8 +320,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) in[j] = s1 * __uint_as_float(qp[j]) + keep * __uint_as_float(av[j]);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        *reinterpret_cast<uint4*>(sIn + tc::sw128_chunk(r, 4 * h + 2 * half + j)) = pack8(&in[8 * j]);
+                    for (int j = 0; j < 2; ++j) {
+                        const uint4 packed = pack8(&in[8 * j]);
+                        *reinterpret_cast<uint4*>(sIn + tc::sw128_chunk(r, 4 * h + 2 * half + j)) = packed;
+                        if (FO && r < Wc) *reinterpret_cast<uint4*>(fo_out + 16 * half + 8 * j) = packed;
+                    }
                 }
             }
             tc::fence_proxy_async();
@@ -311,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[BPS]);
 
-            if (!SUMMARY) {
+            if (!SUMMARY && !FO) {
                 // ---- EPI3: out = g^(r+1) Q E0 + A~ Inner ------------------------------------
                 tc::mbar_wait(&bars[BO], ph, abort, status, 44);
                 tc::fence_after_sync();
@@ -344,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint32_t v[32];
                 // ST rows < 64: dP in columns 0..63 (T3); rows >= 64: dE in columns 64..127 (T2)
                 tc::tmem_ld32(lrow + (r < 64 ? T3 : T2) + 32 * h, v);
-                if (SUMMARY) {
+                if (SUMMARY && !FO) {
                     uint32_t w[16];
                     tc::tmem_ld16(lrow + T0 + 32 * h + 16 * (r >> 6), w);
                     tc::tmem_wait_ld();
@@ -415,20 +436,16 @@ bool ahla_tc_available() { return encode_fn() != nullptr; }
 
 size_t ahla_tc_smem() { return kSmemBytes; }
 
-int launch_ahla_tc(const AhlaArgs& a, bool summary, int* status, cudaStream_t st) {
+int launch_ahla_tc(const AhlaArgs& a, bool summary, int* status, cudaStream_t st, bool first_order) {
     if (a.nseg_launch <= 0 || a.BH <= 0) return 0;
     TcMaps maps;
     if (!make_map(&maps.q, a.q, a.BH, a.n) || !make_map(&maps.k, a.k, a.BH, a.n) || !make_map(&maps.v, a.v, a.BH, a.n))
         return -2;
     dim3 grid(a.nseg_launch, a.BH);
-    cudaError_t e;
-    if (summary) {
-        e = cudaFuncSetAttribute(ahla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e == cudaSuccess) ahla_tc_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(maps, a, status);
-    } else {
-        e = cudaFuncSetAttribute(ahla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e == cudaSuccess) ahla_tc_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(maps, a, status);
-    }
+    auto kfn = summary ? (first_order ? ahla_tc_kernel<true, true> : ahla_tc_kernel<true, false>)
+                       : (first_order ? ahla_tc_kernel<false, true> : ahla_tc_kernel<false, false>);
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess) kfn<<<grid, kThreads, kSmemBytes, st>>>(maps, a, status);
     if (e != cudaSuccess) return -1;
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

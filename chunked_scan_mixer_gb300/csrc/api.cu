@@ -1065,6 +1065,14 @@ static int ahla_check(int B, int H, int n, int d, int dv, int chunk, int dtype, 
 // chunk 128 runs the tcgen05 kernel, chunks 32 and 64 the mma.sync one
 // ---- masked third-order output (gamma = 1): first-order pass, then the second-order forward ----
 
+static Plan ahla_plan(int B, int H, int n, int d, int chunk);
+
+// The first-order pass runs on the AHLA tcgen05 kernel in its first-order mode (Inner is the
+// masked first-order output) for bf16, d = dv = 64; elsewhere on the SIMT kernel.
+static bool hla3_first_order_on_tc(bool bf, int d, int w, const DevInfo& di) {
+    return bf && d == 64 && w == 64 && !tc_disabled() && ahla_tc_available() && ahla_tc_smem() <= (size_t)di.smem_optin;
+}
+
 static constexpr int kHla3Unit = 16;  // value width of the denominator passes (column 0 is 1)
 
 static int hla3_la_width(int d, int dv, int chunk, const DevInfo& di) {
@@ -1109,7 +1117,11 @@ static Hla3Layout hla3_layout(int B, int H, int n, int d, int dv, int chunk, int
     const size_t wmax = dv > kHla3Unit ? dv : kHla3Unit;
     L.PB = kStatusFloats;
     L.Pin = align64(L.PB + BH * nsm * (size_t)d * wmax);
-    const size_t la = align64(L.Pin + BH * ns * (size_t)d * wmax) * sizeof(float);
+    size_t la = align64(L.Pin + BH * ns * (size_t)d * wmax) * sizeof(float);
+    if (hla3_first_order_on_tc(dtype == HLA2_BF16, d, dv, di)) {
+        const size_t t = ahla_layout(ahla_plan(B, H, n, d, 128)).total * sizeof(float);
+        la = la > t ? la : t;
+    }
     size_t f1 = hla2_forward_workspace_bytes(B, H, n, d, dv, chunk, dtype, 0, 0);
     size_t f2 = normalize ? hla2_forward_workspace_bytes(B, H, n, d, kHla3Unit, chunk, dtype, 0, 0) : 0;
     if (f1 == (size_t)-1 || f2 == (size_t)-1) {
@@ -1144,6 +1156,40 @@ extern "C" size_t hla2_hla3_forward_workspace_bytes(int B, int H, int n, int d, 
 // first-order pass u = masked linear attention (q, k, values) into `u`
 static int hla3_first_order(const void* q, const void* k, const void* vals, void* u, int B, int H, int n, int d,
                             int w, const Hla3Layout& L, void* ws, bool bf, cudaStream_t st) {
+    if (hla3_first_order_on_tc(bf, d, w, dev_info())) {
+        const Plan p = ahla_plan(B, H, n, d, 128);
+        AhlaArgs a{};
+        a.q = q;
+        a.k = k;
+        a.v = vals;
+        a.out = u;
+        a.BH = B * H;
+        a.H = H;
+        a.n = n;
+        a.W = 128;
+        a.nchunks = p.nchunks;
+        a.seg_chunks = p.seg_chunks;
+        a.nseg = p.nseg;
+        a.nsum = p.nseg - 1;
+        a.ws = static_cast<float*>(ws);
+        a.L = ahla_layout(p);
+        int* status = static_cast<int*>(ws);
+        if (launch_ahla_init(a, d, st)) return cuda_fail("first-order carry-in");
+        if (p.nseg > 1) {
+            AhlaArgs b = a;
+            b.seg0 = 0;
+            b.nseg_launch = p.nseg - 1;
+            if (launch_ahla_tc(b, true, status, st, true)) return cuda_fail("first-order summaries");
+            const size_t dd = (size_t)d * d;
+            if (launch_linear_scan(a.ws + a.L.PB, a.ws + a.L.Pin, a.BH, H, p.nseg - 1, dd, a.nsum * dd, p.nseg * dd,
+                                   true, nullptr, p.seg_chunks * 128, 1, st))
+                return cuda_fail("first-order scan");
+        }
+        AhlaArgs b = a;
+        b.seg0 = 0;
+        b.nseg_launch = p.nseg;
+        return launch_ahla_tc(b, false, status, st, true) ? cuda_fail("first-order pass") : HLA2_OK;
+    }
     LaArgs a{};
     a.q = q;
     a.k = k;

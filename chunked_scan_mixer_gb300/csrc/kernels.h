@@ -57,7 +57,9 @@ int ahla_chunk_threads(int d);
 // tcgen05 AHLA chunk kernel (d = dv = 64, chunk 128, unnormalised; ahla_tc.cu)
 bool ahla_tc_available();
 size_t ahla_tc_smem();
-int launch_ahla_tc(const AhlaArgs& a, bool summary, int* status, cudaStream_t st);
+// first_order: the pass computes masked first-order linear attention (out = Inner; the
+// summaries keep only P_B), the inner pass of the third-order output.
+int launch_ahla_tc(const AhlaArgs& a, bool summary, int* status, cudaStream_t st, bool first_order = false);
 
 // Arguments of one chunk-kernel launch (summary or output pass of the forward).
 struct ChunkArgs {

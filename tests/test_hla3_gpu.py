@@ -71,3 +71,26 @@ def test_decay_is_refused():
                              ctypes.byref(o))
     assert rc == -2 and b"gamma" in L.hla2_last_error()
     assert np.isfinite(rc)
+
+
+def test_bf16_first_order_paths_agree():
+    """bf16 d = dv = 64 runs the first-order pass on the AHLA tcgen05 kernel in its first-order
+    mode; with the tcgen05 kernels disabled it runs on the SIMT kernel.  Both against the
+    oracle, several segments."""
+    import os
+
+    x = inputs.make_custom(2, 4, 128 * 30 + 7, 64, 64, torch.bfloat16, seed=84)
+    ref = O3.serial_forward(np64(x["q"]), np64(x["k"]), np64(x["v"]))
+    a = run(x, chunk=128)
+    old = os.environ.get("HLA2_KERNEL")
+    os.environ["HLA2_KERNEL"] = "mma"
+    try:
+        b = run(x, chunk=128)
+    finally:
+        if old is None:
+            os.environ.pop("HLA2_KERNEL", None)
+        else:
+            os.environ["HLA2_KERNEL"] = old
+    hla.check_status()
+    assert rel_err(np64(a), ref) <= 2e-2
+    assert rel_err(np64(b), ref) <= 2e-2
