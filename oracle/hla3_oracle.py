@@ -35,7 +35,8 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["brute_force_forward", "serial_forward", "matrix_form_forward", "first_order_forward"]
+__all__ = ["brute_force_forward", "serial_forward", "matrix_form_forward", "first_order_forward", "state_floats",
+           "decode_step"]
 
 
 def _f64(*xs):
@@ -118,4 +119,35 @@ def serial_forward(q, k, v, normalize=False, eps=1e-6):
         if normalize:
             o = o / (np.einsum("bha,bha->bh", qt, y) + eps)[..., None]
         out[:, :, t] = o
+    return out
+
+
+def state_floats(d, dv):
+    """Floats of one head's streaming state [S^K d*d | P^KV d*dv | Y d*dv | m^K d | y d]."""
+    return d * d + 2 * d * dv + 2 * d
+
+
+def decode_step(state, q_t, k_t, v_t, normalize=False, eps=1e-6):
+    """One streaming step of reading T4 on packed states [N, H, state_floats] (float64,
+    updated in place): S^K += k k^T, P^KV += k v^T, m^K += k, then with p = S^K q and
+    u = P^T q: Y += p u^T, y += p (q . m^K), o = q^T Y (/ (q^T y + eps)).  Returns o [N,H,dv]."""
+    q_t, k_t, v_t = _f64(q_t, k_t, v_t)
+    N, H, d = q_t.shape
+    dv = v_t.shape[-1]
+    o = 0
+    S = state[..., o:o + d * d].reshape(N, H, d, d); o += d * d
+    P = state[..., o:o + d * dv].reshape(N, H, d, dv); o += d * dv
+    Y = state[..., o:o + d * dv].reshape(N, H, d, dv); o += d * dv
+    m = state[..., o:o + d]; o += d
+    y = state[..., o:o + d]
+    S += np.einsum("nha,nhc->nhac", k_t, k_t)
+    P += np.einsum("nha,nhe->nhae", k_t, v_t)
+    m += k_t
+    p = np.einsum("nhac,nhc->nha", S, q_t)
+    u = np.einsum("nha,nhae->nhe", q_t, P)
+    Y += np.einsum("nha,nhe->nhae", p, u)
+    y += p * np.einsum("nha,nha->nh", q_t, m)[..., None]
+    out = np.einsum("nha,nhae->nhe", q_t, Y)
+    if normalize:
+        out = out / (np.einsum("nha,nha->nh", q_t, y) + eps)[..., None]
     return out

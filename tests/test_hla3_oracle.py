@@ -93,3 +93,14 @@ def test_planted_mistakes_are_caught():
         Y = Y + np.outer(S @ Q[t], u)
         bad[t] = Q[t] @ Y
     assert rel(bad, ref[0, 0]) > 1e-3
+
+
+@pytest.mark.parametrize("normalize", [False, True])
+def test_decode_from_zero_equals_the_triple_sum(normalize):
+    """Streaming with the packed state [S^K | P^KV | Y | m^K | y] from zero reproduces the
+    triple sum token by token (the masked streaming of the technical summary, item 3)."""
+    q, k, v = rnd(2, 2, 9, 3, 2, seed=9, positive=normalize)
+    ref = O3.brute_force_forward(q, k, v, normalize)
+    state = np.zeros((2, 2, O3.state_floats(3, 2)))
+    outs = [O3.decode_step(state, q[:, :, t], k[:, :, t], v[:, :, t], normalize) for t in range(9)]
+    assert rel(np.stack(outs, axis=2), ref) < 1e-12
