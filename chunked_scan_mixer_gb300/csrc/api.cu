@@ -1026,6 +1026,26 @@ int hla2_decode_step_mq(float* key_state, float* head_state, const void* q, cons
 
 size_t hla2_mq_head_state_floats(int d, int dv) { return 2 * (size_t)d * dv + 2 * (size_t)d; }
 
+int hla2_hla3_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H, int d,
+                          int dv, int normalize, hla2_stream_t stream, const hla2_opts* opts) {
+    NvtxScope nvtx("hla2_hla3_decode_step");
+    const int dtype = opts ? opts->dtype : HLA2_BF16;
+    const float eps = opts ? opts->eps : 1e-6f;
+    int rc = check_common(N, H, 0, d, dv, dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (normalize && !isfinite(eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
+    if (opts && opts->flags) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_hla3_decode_step");
+    if ((long)N * H == 0) return succeed();
+    if (!state || !q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "state, q, k, v, out must not be NULL");
+    if (!aligned16(state) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(HLA2_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    cudaGetLastError();
+    if (launch_hla3_decode_step(state, q, k, v, out, (long)N * H, d, dv, normalize, eps, dtype == HLA2_BF16,
+                                reinterpret_cast<cudaStream_t>(stream)))
+        return cuda_fail("third-order decode step");
+    return succeed();
+}
+
 size_t hla2_compact_state_floats(int d, int dv) { return compact_state_floats(d, dv); }
 
 size_t hla2_ahla_state_floats(int d, int dv) { return ahla_state_floats(d, dv); }

@@ -389,6 +389,138 @@ __global__ void __launch_bounds__(kThreads) state_from_compact_kernel(const floa
     for (size_t i = threadIdx.x; i < tail; i += kThreads) dst[fs + i] = src[cs + i];
 }
 
+// Streaming step of the masked third-order output at gamma = 1 (technical summary item
+// "3. Dritte Ordnung HLA": masked streaming with the prefix moments S^K, P^KV; reading: the
+// output is q^T Y with Y = sum_j (S^K_j q_j)(P_j^T q_j)^T).  One CTA per head, state
+// [S d*d | P d*dv | Y d*dv | m d | y d], each matrix streamed once with 128-bit accesses:
+//   pass S:  S' = S + k k^T,          p = S' q        (row form; S is symmetric)
+//   pass P:  P' = P + k v^T,          u = P'^T q
+//   pass Y:  Y' = Y + p u^T,          o = Y'^T q
+//   m' = m + k,  y' = y + p (q . m'),  den = q . y'
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    hla3_decode_kernel(float* __restrict__ state, const T* __restrict__ q, const T* __restrict__ k,
+                       const T* __restrict__ v, T* __restrict__ out, int d, int dv, int normalize, float eps) {
+    __shared__ __align__(16) float qs[kMaxDim], ks[kMaxDim], vs[kMaxDim], ps[kMaxDim], us[kMaxDim], os[kMaxDim];
+    __shared__ __align__(16) float red[kWarps * kMaxDim];
+    const int head = blockIdx.x, tid = threadIdx.x;
+    float* S = state + (size_t)head * ((size_t)d * d + 2 * (size_t)d * dv + 2 * (size_t)d);
+    float* P = S + (size_t)d * d;
+    float* Y = P + (size_t)d * dv;
+    float* m = Y + (size_t)d * dv;
+    float* y = m + d;
+    for (int i = tid; i < d; i += kThreads) {
+        qs[i] = to_f32(q[(size_t)head * d + i]);
+        ks[i] = to_f32(k[(size_t)head * d + i]);
+    }
+    for (int i = tid; i < dv; i += kThreads) vs[i] = to_f32(v[(size_t)head * dv + i]);
+    __syncthreads();
+
+    // ---- pass S (row form, as the second-order step) ------------------------------------
+    {
+        const int lpr = d / 4, n4 = d * d / 4;
+        for (int base = 0; base < n4; base += kThreads * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = base + u * kThreads + tid;
+                if (i < n4) x[u] = ld_stream(S + (size_t)i * 4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = base + u * kThreads + tid;
+                float part = 0.f;
+                const int a = (i * 4) / d, c = (i * 4) % d;
+                if (i < n4) {
+                    const float ka = ks[a];
+                    float4 z = x[u];
+                    z.x += ka * ks[c + 0];
+                    z.y += ka * ks[c + 1];
+                    z.z += ka * ks[c + 2];
+                    z.w += ka * ks[c + 3];
+                    st_stream(S + (size_t)i * 4, z);
+                    part = z.x * qs[c] + z.y * qs[c + 1] + z.z * qs[c + 2] + z.w * qs[c + 3];
+                }
+                for (int o = lpr >> 1; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+                if (i < n4 && (i % lpr) == 0) ps[a] = part;
+            }
+        }
+    }
+    // m' = m + k and q . m'
+    float qm = 0.f;
+    for (int i = tid; i < d; i += kThreads) {
+        const float mn = m[i] + ks[i];
+        m[i] = mn;
+        qm += qs[i] * mn;
+    }
+    qm = block_sum(qm, red);  // also orders pass S's writes of ps before their reads below
+    __syncthreads();          // every warp has read red before pass P reuses it
+
+    const int lpc = dv / 4, rows_per = kThreads / lpc, c4 = (tid % lpc) * 4;
+    // ---- pass P: P' = P + k v^T, u = P'^T q -------------------------------------------------
+    {
+        float4 pu = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int a0 = tid / lpc; a0 < d; a0 += rows_per * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a < d) x[u] = ld_stream(P + (size_t)a * dv + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a >= d) continue;
+                const float ka = ks[a], qa = qs[a];
+                float4 z = x[u];
+                z.x += ka * vs[c4 + 0];
+                z.y += ka * vs[c4 + 1];
+                z.z += ka * vs[c4 + 2];
+                z.w += ka * vs[c4 + 3];
+                pu.x += qa * z.x; pu.y += qa * z.y; pu.z += qa * z.z; pu.w += qa * z.w;
+                st_stream(P + (size_t)a * dv + c4, z);
+            }
+        }
+        column_reduce(pu, dv, red, us);
+    }
+    // ---- pass Y: Y' = Y + p u^T, o = Y'^T q ---------------------------------------------------
+    {
+        float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 u4 = *reinterpret_cast<const float4*>(&us[c4]);
+        for (int a0 = tid / lpc; a0 < d; a0 += rows_per * 4) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a < d) x[u] = ld_stream(Y + (size_t)a * dv + c4);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int a = a0 + u * rows_per;
+                if (a >= d) continue;
+                const float pa = ps[a], qa = qs[a];
+                float4 z = x[u];
+                z.x += pa * u4.x;
+                z.y += pa * u4.y;
+                z.z += pa * u4.z;
+                z.w += pa * u4.w;
+                po.x += qa * z.x; po.y += qa * z.y; po.z += qa * z.z; po.w += qa * z.w;
+                st_stream(Y + (size_t)a * dv + c4, z);
+            }
+        }
+        column_reduce(po, dv, red, os);
+    }
+    float qy = 0.f;
+    for (int i = tid; i < d; i += kThreads) {
+        const float yn = y[i] + ps[i] * qm;
+        y[i] = yn;
+        qy += qs[i] * yn;
+    }
+    float inv = 1.f;
+    if (normalize) inv = 1.f / (block_sum(qy, red) + eps);
+    for (int e = tid; e < dv; e += kThreads) out[(size_t)head * dv + e] = from_f32<T>(os[e] * inv);
+}
+
 // Decode step with multi-query sharing (section summary §5.2: one key moment per group of
 // query heads, state O(d^2 + h d dv) per group).  One CTA per query head; the `group` CTAs
 // of a key group form a thread-block cluster.  Each CTA advances one block of rows of the
@@ -625,6 +757,20 @@ int launch_decode_mq(float* key_state, float* head_state, const void* q, const v
     }
 #undef HLA2_MQ
     if (e != cudaSuccess) return -1;
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_hla3_decode_step(float* state, const void* q, const void* k, const void* v, void* out, long heads, int d,
+                            int dv, int normalize, float eps, bool is_bf16, cudaStream_t st) {
+    if (heads <= 0) return 0;
+    if (is_bf16)
+        hla3_decode_kernel<bf16><<<(unsigned)heads, kThreads, 0, st>>>(
+            state, static_cast<const bf16*>(q), static_cast<const bf16*>(k), static_cast<const bf16*>(v),
+            static_cast<bf16*>(out), d, dv, normalize, eps);
+    else
+        hla3_decode_kernel<float><<<(unsigned)heads, kThreads, 0, st>>>(
+            state, static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+            static_cast<float*>(out), d, dv, normalize, eps);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -185,6 +185,9 @@ int launch_decode_step(float* state, const void* q, const void* k, const void* v
 int launch_decode_mq(float* key_state, float* head_state, const void* q, const void* k, const void* v, void* out,
                      int N, int Hk, int group, int d, int dv, const float* gamma, int normalize, float eps,
                      bool is_bf16, bool unmasked, cudaStream_t st);
+// Third-order streaming step (gamma = 1): state [heads][d*d + 2 d dv + 2 d] = S | P | Y | m | y.
+int launch_hla3_decode_step(float* state, const void* q, const void* k, const void* v, void* out, long heads, int d,
+                            int dv, int normalize, float eps, bool is_bf16, cudaStream_t st);
 int launch_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
                             int d, int dv, const float* gamma, int normalize, float eps, bool is_bf16,
                             cudaStream_t st);

@@ -111,6 +111,8 @@ def lib():
         L.hla2_hla3_forward_workspace_bytes.restype = Z
         L.hla2_hla3_forward.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
         L.hla2_hla3_forward.restype = I
+        L.hla2_hla3_decode_step.argtypes = [P, P, P, P, P, I, I, I, I, I, P, ctypes.POINTER(Opts)]
+        L.hla2_hla3_decode_step.restype = I
         L.hla2_selftest_wait_timeout.argtypes = [P, P]
         L.hla2_selftest_wait_timeout.restype = I
         L.hla2_mq_head_state_floats.argtypes = [I, I]
@@ -130,7 +132,7 @@ EXPORTED_SYMBOLS = (
     "hla2_backward", "hla2_decode_step", "hla2_forward_noalloc", "hla2_compact_state_floats",
     "hla2_state_to_compact", "hla2_state_from_compact", "hla2_ahla_forward_workspace_bytes", "hla2_ahla_forward",
     "hla2_ahla_state_floats", "hla2_ahla_decode_step", "hla2_mq_head_state_floats", "hla2_decode_step_mq",
-    "hla2_selftest_wait_timeout", "hla2_hla3_forward_workspace_bytes", "hla2_hla3_forward",
+    "hla2_selftest_wait_timeout", "hla2_hla3_forward_workspace_bytes", "hla2_hla3_forward", "hla2_hla3_decode_step",
 )
 
 FLAG_COMPACT_STATE = 4
@@ -561,4 +563,23 @@ def hla3_forward(q, k, v, normalize=False, chunk=64, eps=1e-6, out=None):
                 0, 0)
     _check("hla2_hla3_forward", L.hla2_hla3_forward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), B, H, n, d, dv, None,
                                                     int(normalize), chunk, sh, ctypes.byref(opts)))
+    return o
+
+
+def hla3_decode_step(state, q, k, v, normalize=False, eps=1e-6, out=None):
+    """One third-order streaming step (gamma = 1).  state [N,H,state_floats(d, dv)] float32 on
+    the GPU, laid out S^K | P^KV | Y | m^K | y, updated in place; q, k [N,H,d]; v [N,H,dv].
+    Returns out [N,H,dv]."""
+    L = lib()
+    if state.device.type != "cuda" or state.dtype != torch.float32 or not state.is_contiguous():
+        raise ValueError("state must be a contiguous float32 CUDA tensor")
+    device = state.device
+    N, H, d = q.shape
+    dv = v.shape[-1]
+    qd, kd, vd = (_to_device(t, device) for t in (q, k, v))
+    o = out if out is not None else torch.empty((N, H, dv), dtype=q.dtype, device=device)
+    opts = Opts(_DTYPES[q.dtype], float(eps), None, 0, None, None, None, 0, 0)
+    _check("hla2_hla3_decode_step", L.hla2_hla3_decode_step(_ptr(state), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), N,
+                                                            H, d, dv, int(normalize), _stream_handle(device),
+                                                            ctypes.byref(opts)))
     return o

@@ -230,6 +230,18 @@ int hla2_hla3_forward(const void* q, const void* k, const void* v, void* out, in
                       int dv, const float* gamma, int normalize, int chunk, hla2_stream_t stream,
                       const hla2_opts* opts);
 
+/*
+ * Third-order streaming step (gamma = 1; the masked streaming of technical summary item 3,
+ * under the reading of hla2_hla3_forward).  state [N, H] float32 blocks of
+ * hla2_state_floats(d, dv) floats laid out [S^K d*d | P^KV d*dv | Y d*dv | m^K d | y d],
+ * updated in place: S^K += k k^T, P^KV += k v^T, m^K += k; with p = S^K q and u = P^KV^T q,
+ * Y += p u^T and y += p (q . m^K); out = q^T Y (normalize: / (q^T y + opts->eps)).
+ * q, k [N, H, d]; v, out [N, H, dv].  A zero state is the empty prefix.  opts may be NULL
+ * (dtype bf16, eps 1e-6); opts->flags must be 0.
+ */
+int hla2_hla3_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
+                          int d, int dv, int normalize, hla2_stream_t stream, const hla2_opts* opts);
+
 /* Floats in one head's part of the multi-query state: C d*dv | G d*dv | m d | h d. */
 size_t hla2_mq_head_state_floats(int d, int dv);
 

@@ -94,3 +94,27 @@ def test_bf16_first_order_paths_agree():
     hla.check_status()
     assert rel_err(np64(a), ref) <= 2e-2
     assert rel_err(np64(b), ref) <= 2e-2
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d, dv", [(16, 16), (64, 64), (128, 128), (32, 64)])
+@pytest.mark.parametrize("normalize", [False, True])
+def test_decode_from_zero_equals_forward(dtype, d, dv, normalize):
+    """Streaming steps from the empty state reproduce the oracle's outputs token by token,
+    and agree with the chunked GPU forward on the same tokens."""
+    N, H, n = 2, 3, 21
+    x = inputs.make_custom(N, H, n, d, dv, dtype, seed=d + dv + 90, qk="softplus" if normalize else "gauss",
+                           v_scale="unit" if normalize else "gauss_sqrt_d")
+    state = torch.zeros((N, H, O3.state_floats(d, dv)), device="cuda")
+    outs = [hla.hla3_decode_step(state, x["q"][:, :, t].cuda(), x["k"][:, :, t].cuda(), x["v"][:, :, t].cuda(),
+                                 normalize=normalize, eps=1e-6) for t in range(n)]
+    o = torch.stack(outs, dim=2).cpu()
+    ref = O3.serial_forward(np64(x["q"]), np64(x["k"]), np64(x["v"]), normalize=normalize, eps=1e-6)
+    assert rel_err(np64(o), ref) <= tol_for(dtype)
+    fwd = run(x, chunk=16, normalize=normalize, eps=1e-6)
+    assert rel_err(np64(fwd), ref) <= tol_for(dtype)
+    # and the state after the last step is the oracle's
+    st = np.zeros((N, H, O3.state_floats(d, dv)))
+    for t in range(n):
+        O3.decode_step(st, np64(x["q"][:, :, t]), np64(x["k"][:, :, t]), np64(x["v"][:, :, t]), normalize)
+    assert rel_err(state.cpu().double().numpy(), st) <= 1e-5
