@@ -384,6 +384,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (lane == 0) tc::mbar_arrive(&bars[BS]);
         }
 
+        if (FO && !SUMMARY && a.final_state && seg == a.nseg - 1 && r < 64) {  // P after the last token
+            float* dst = a.final_state + (size_t)bh * kD * kD + (size_t)r * kD + 32 * h;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[j] = st[j];
+        }
         if (SUMMARY) {
             const size_t si = (size_t)bh * a.nsum + seg;
             float* dst = r < 64 ? a.ws + a.L.PB + si * kD * kD + (size_t)r * kD

@@ -1119,14 +1119,17 @@ struct Hla3Layout {
     Plan p;
     size_t PB = 0, Pin = 0;  // first-order workspace (floats, in the scratch region)
     size_t scratch = 0;      // bytes of the scratch region (first-order and second-order calls in turn)
-    size_t u = 0, e0 = 0, u1 = 0, den = 0, total = 0;  // byte offsets
+    size_t u = 0, e0 = 0, u1 = 0, den = 0;  // byte offsets
+    size_t pk_num = 0, pk_den = 0, p_num = 0, p_den = 0;  // final-state pieces (byte offsets)
+    size_t total = 0;
 };
 
 static Hla3Layout hla3_layout(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize,
-                              const DevInfo& di) {
+                              bool want_final, const DevInfo& di) {
     Hla3Layout L;
+    const bool dens = normalize || want_final;  // the unit-value passes run
     L.W = hla3_la_width(d, dv, chunk, di);
-    L.W2 = hla3_second_width(dtype, d, dv, chunk, normalize, di);
+    L.W2 = hla3_second_width(dtype, d, dv, chunk, dens, di);
     if (!L.W || !L.W2) {
         L.W = 0;
         return L;
@@ -1142,8 +1145,8 @@ static Hla3Layout hla3_layout(int B, int H, int n, int d, int dv, int chunk, int
         const size_t t = ahla_layout(ahla_plan(B, H, n, d, 128)).total * sizeof(float);
         la = la > t ? la : t;
     }
-    size_t f1 = hla2_forward_workspace_bytes(B, H, n, d, dv, chunk, dtype, 0, 0);
-    size_t f2 = normalize ? hla2_forward_workspace_bytes(B, H, n, d, kHla3Unit, chunk, dtype, 0, 0) : 0;
+    size_t f1 = hla2_forward_workspace_bytes(B, H, n, d, dv, chunk, dtype, 0, want_final);
+    size_t f2 = dens ? hla2_forward_workspace_bytes(B, H, n, d, kHla3Unit, chunk, dtype, 0, want_final) : 0;
     if (f1 == (size_t)-1 || f2 == (size_t)-1) {
         L.W = 0;
         return L;
@@ -1154,7 +1157,7 @@ static Hla3Layout hla3_layout(int B, int H, int n, int d, int dv, int chunk, int
     size_t o = L.scratch;
     L.u = o;
     o += up(rows * dv * es);
-    if (normalize) {
+    if (dens) {
         L.e0 = o;
         o += up(rows * kHla3Unit * es);
         L.u1 = o;
@@ -1162,20 +1165,31 @@ static Hla3Layout hla3_layout(int B, int H, int n, int d, int dv, int chunk, int
         L.den = o;
         o += up(rows * kHla3Unit * es);
     }
+    if (want_final) {
+        const size_t dd = (size_t)d * d;
+        L.pk_num = o;
+        o += up(BH * (dd + 2 * (size_t)d * dv + 2 * (size_t)d) * sizeof(float));
+        L.pk_den = o;
+        o += up(BH * (dd + 2 * (size_t)d * kHla3Unit + 2 * (size_t)d) * sizeof(float));
+        L.p_num = o;
+        o += up(BH * (size_t)d * dv * sizeof(float));
+        L.p_den = o;
+        o += up(BH * (size_t)d * kHla3Unit * sizeof(float));
+    }
     L.total = o;
     return L;
 }
 
 extern "C" size_t hla2_hla3_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
-                                                    int normalize) {
+                                                    int normalize, int want_final_state) {
     if (check_common(B, H, n, d, dv, dtype, normalize) != HLA2_OK || !dim_ok(chunk)) return (size_t)-1;
-    const Hla3Layout L = hla3_layout(B, H, n, d, dv, chunk, dtype, normalize, dev_info());
+    const Hla3Layout L = hla3_layout(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, dev_info());
     return L.W ? L.total : (size_t)-1;
 }
 
 // first-order pass u = masked linear attention (q, k, values) into `u`
 static int hla3_first_order(const void* q, const void* k, const void* vals, void* u, int B, int H, int n, int d,
-                            int w, const Hla3Layout& L, void* ws, bool bf, cudaStream_t st) {
+                            int w, const Hla3Layout& L, void* ws, bool bf, cudaStream_t st, float* final_P) {
     if (hla3_first_order_on_tc(bf, d, w, dev_info())) {
         const Plan p = ahla_plan(B, H, n, d, 128);
         AhlaArgs a{};
@@ -1193,6 +1207,7 @@ static int hla3_first_order(const void* q, const void* k, const void* vals, void
         a.nsum = p.nseg - 1;
         a.ws = static_cast<float*>(ws);
         a.L = ahla_layout(p);
+        a.final_state = final_P;  // first-order mode: P only, [BH][d*d]
         int* status = static_cast<int*>(ws);
         if (launch_ahla_init(a, d, st)) return cuda_fail("first-order carry-in");
         if (p.nseg > 1) {
@@ -1228,6 +1243,7 @@ static int hla3_first_order(const void* q, const void* k, const void* vals, void
     a.ws = static_cast<float*>(ws);
     a.PB = L.PB;
     a.Pin = L.Pin;
+    a.final_P = final_P;
     return launch_first_order_forward(a, bf, st) ? cuda_fail("first-order pass") : HLA2_OK;
 }
 
@@ -1242,14 +1258,22 @@ extern "C" int hla2_hla3_forward(const void* q, const void* k, const void* v, vo
     if (normalize && !isfinite(opts->eps)) return fail(HLA2_ERR_INVALID_ARG, "eps must be finite");
     if (opts->flags) return fail(HLA2_ERR_INVALID_ARG, "unknown flags for hla2_hla3_forward");
     if (gamma) return fail(HLA2_ERR_UNSUPPORTED, "the third-order scan is defined for gamma = 1 (pass NULL)");
-    if (opts->init_state || opts->final_state)
-        return fail(HLA2_ERR_UNSUPPORTED, "the third-order forward keeps no state across calls");
-    if ((long)B * H == 0 || n == 0) return succeed();
+    if (opts->init_state) return fail(HLA2_ERR_UNSUPPORTED, "the third-order forward starts from the empty prefix");
+    const bool want_final = opts->final_state != nullptr;
+    if (want_final && !aligned16(opts->final_state))
+        return fail(HLA2_ERR_INVALID_ARG, "final_state must be 16-byte aligned");
+    if ((long)B * H == 0) return succeed();
+    if (n == 0) {
+        if (want_final && cudaMemsetAsync(opts->final_state, 0, (size_t)B * H * raw_state_floats(d, dv) * sizeof(float),
+                                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return cuda_fail("final state");
+        return succeed();
+    }
     if (!q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must not be NULL");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
     const DevInfo di = dev_info();
-    const Hla3Layout L = hla3_layout(B, H, n, d, dv, chunk, opts->dtype, normalize, di);
+    const Hla3Layout L = hla3_layout(B, H, n, d, dv, chunk, opts->dtype, normalize, want_final, di);
     if (!L.W) return fail(HLA2_ERR_UNSUPPORTED, "no kernel for d %d, dv %d, chunk %d", d, dv, chunk);
     if (!opts->workspace || opts->workspace_bytes < L.total)
         return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.total,
@@ -1264,22 +1288,29 @@ extern "C" int hla2_hla3_forward(const void* q, const void* k, const void* v, vo
     so.workspace = base;
     so.workspace_bytes = L.scratch;
     cudaGetLastError();
+    auto fbuf = [&](size_t off) { return want_final ? reinterpret_cast<float*>(base + off) : nullptr; };
     // numerator: the masked second-order output with the first-order outputs as values
-    if ((rc = hla3_first_order(q, k, v, base + L.u, B, H, n, d, dv, L, base, bf, st)) != HLA2_OK) return rc;
+    if ((rc = hla3_first_order(q, k, v, base + L.u, B, H, n, d, dv, L, base, bf, st, fbuf(L.p_num))) != HLA2_OK)
+        return rc;
+    so.final_state = fbuf(L.pk_num);
     if ((rc = hla2_forward(q, k, base + L.u, out, B, H, n, d, dv, nullptr, 0, L.W2, stream, &so)) != HLA2_OK)
         return rc;
-    if (normalize) {  // denominator: the same with v -> 1 (value rows e_0, column 0)
+    if (normalize || want_final) {  // the same with v -> 1 (value rows e_0, column 0)
         const size_t rows = (size_t)B * H * n;
         if (launch_unit_rows(base + L.e0, rows, kHla3Unit, bf, st)) return cuda_fail("unit value rows");
-        if ((rc = hla3_first_order(q, k, base + L.e0, base + L.u1, B, H, n, d, kHla3Unit, L, base, bf, st)) !=
-            HLA2_OK)
+        if ((rc = hla3_first_order(q, k, base + L.e0, base + L.u1, B, H, n, d, kHla3Unit, L, base, bf, st,
+                                   fbuf(L.p_den))) != HLA2_OK)
             return rc;
+        so.final_state = fbuf(L.pk_den);
         if ((rc = hla2_forward(q, k, base + L.u1, base + L.den, B, H, n, d, kHla3Unit, nullptr, 0, L.W2, stream,
                                &so)) != HLA2_OK)
             return rc;
-        if (launch_divide_rows(out, base + L.den, rows, dv, kHla3Unit, opts->eps, bf, st))
+        if (normalize && launch_divide_rows(out, base + L.den, rows, dv, kHla3Unit, opts->eps, bf, st))
             return cuda_fail("normalisation");
     }
+    if (want_final && launch_hla3_assemble_state(opts->final_state, fbuf(L.pk_num), fbuf(L.pk_den), fbuf(L.p_num),
+                                                 fbuf(L.p_den), (long)B * H, d, dv, kHla3Unit, st))
+        return cuda_fail("final state");
     return succeed();
 }
 

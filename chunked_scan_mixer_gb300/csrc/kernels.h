@@ -47,6 +47,7 @@ struct AhlaArgs {
     float* ws;
     AhlaLayout L;
     float* final_state;  // nullable: [BH][2 d dv + 2 d] = P | E | m | n after token n
+                         // (first-order mode of the tcgen05 kernel: [BH][d*dv] = P only)
     const float* init_state;  // nullable: the same layout, the state before token 0
 };
 int launch_ahla_chunk(const AhlaArgs& a, int d, int W, bool summary, cudaStream_t st);
@@ -203,8 +204,14 @@ struct LaArgs {
     const float* gamma;
     float* ws;
     size_t PB, Pin;
+    float* final_P;  // nullable: [BH][d*dv], the state P after the last token
 };
 int launch_first_order_forward(const LaArgs& a, bool is_bf16, cudaStream_t st);
+// Third-order streaming state [S | P | Y | m | y] from the passes' final states: the
+// second-order packed states (S, C, G, m, h) on values u (dv wide) and u1 (w wide), and the
+// first-order final P for v (dv wide) and for the unit values (w wide, column 0 = key mass).
+int launch_hla3_assemble_state(float* fin, const float* pk_num, const float* pk_den, const float* p_num,
+                               const float* p_den, long heads, int d, int dv, int w, cudaStream_t st);
 size_t first_order_smem(int d, int dv, int W);
 // rows x w with column 0 = 1, in the input type (bf16 or float32)
 int launch_unit_rows(void* e0, size_t rows, int w, bool is_bf16, cudaStream_t st);

@@ -92,10 +92,40 @@ __global__ void __launch_bounds__(kLaThreads) la_chunk_kernel(const LaArgs a) {
             P[e] = rho * P[e] + s;
         }
     }
-    if (SUMMARY) {
+    if (SUMMARY || (a.final_P && seg == a.nseg - 1)) {
         __syncthreads();
-        float* dst = a.ws + a.PB + ((size_t)bh * (a.nseg - 1) + seg) * ddv;
+        float* dst = SUMMARY ? a.ws + a.PB + ((size_t)bh * (a.nseg - 1) + seg) * ddv : a.final_P + (size_t)bh * ddv;
         for (int i = tid; i < D * DV; i += NT) dst[i] = P[i];
+    }
+}
+
+// One CTA per head: S, P copied; Y = S C - G (the second-order Z on values u); m = the unit
+// pass's P column 0 (sum of keys); y = (S C1 - G1) column 0 (Z on the unit values).
+__global__ void __launch_bounds__(kLaThreads)
+    hla3_assemble_kernel(float* fin, const float* pk_num, const float* pk_den, const float* p_num, const float* p_den,
+                         int d, int dv, int w) {
+    const size_t head = blockIdx.x;
+    const size_t sf = (size_t)d * d + 2 * (size_t)d * dv + 2 * (size_t)d;
+    const size_t sw = (size_t)d * d + 2 * (size_t)d * w + 2 * (size_t)d;
+    float* o = fin + head * sf;
+    const float* S = pk_num + head * sf;
+    const float* C = S + (size_t)d * d;
+    const float* G = C + (size_t)d * dv;
+    const float* C1 = pk_den + head * sw + (size_t)d * d;
+    const float* G1 = C1 + (size_t)d * w;
+    for (int i = threadIdx.x; i < d * d; i += kLaThreads) o[i] = S[i];
+    for (int i = threadIdx.x; i < d * dv; i += kLaThreads) {
+        o[(size_t)d * d + i] = p_num[head * d * dv + i];
+        const int a = i / dv, x = i % dv;
+        float s = 0.f;
+        for (int j = 0; j < d; ++j) s += S[(size_t)a * d + j] * C[(size_t)j * dv + x];
+        o[(size_t)d * d + (size_t)d * dv + i] = s - G[i];
+    }
+    for (int a = threadIdx.x; a < d; a += kLaThreads) {
+        float s = 0.f;
+        for (int j = 0; j < d; ++j) s += S[(size_t)a * d + j] * C1[(size_t)j * w];
+        o[(size_t)d * d + 2 * (size_t)d * dv + a] = p_den[head * d * w + (size_t)a * w];
+        o[(size_t)d * d + 2 * (size_t)d * dv + d + a] = s - G1[(size_t)a * w];
     }
 }
 
@@ -135,6 +165,13 @@ unsigned blocks(size_t n) { return (unsigned)((n + kLaThreads - 1) / kLaThreads)
 }  // namespace
 
 size_t first_order_smem(int d, int dv, int W) { return la_smem(d, dv, W).total * sizeof(float); }
+
+int launch_hla3_assemble_state(float* fin, const float* pk_num, const float* pk_den, const float* p_num,
+                               const float* p_den, long heads, int d, int dv, int w, cudaStream_t st) {
+    if (heads <= 0) return 0;
+    hla3_assemble_kernel<<<(unsigned)heads, kLaThreads, 0, st>>>(fin, pk_num, pk_den, p_num, p_den, d, dv, w);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
 
 int launch_unit_rows(void* e0, size_t rows, int w, bool is_bf16, cudaStream_t st) {
     const size_t c = rows * (size_t)w;

@@ -107,7 +107,7 @@ def lib():
         L.hla2_ahla_decode_step.restype = I
         L.hla2_compact_state_floats.argtypes = [I, I]
         L.hla2_compact_state_floats.restype = Z
-        L.hla2_hla3_forward_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
+        L.hla2_hla3_forward_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I]
         L.hla2_hla3_forward_workspace_bytes.restype = Z
         L.hla2_hla3_forward.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
         L.hla2_hla3_forward.restype = I
@@ -540,10 +540,11 @@ def decode_step_mq(key_state, head_state, q, k, v, gamma=None, normalize=False, 
     return o
 
 
-def hla3_forward(q, k, v, normalize=False, chunk=64, eps=1e-6, out=None):
+def hla3_forward(q, k, v, normalize=False, chunk=64, eps=1e-6, out=None, return_final_state=False):
     """Masked third-order output at gamma = 1 (every factor of A A^T A and the partial product
     of the first two causally masked).  q, k [B,H,n,d]; v [B,H,n,dv] on the GPU, float32 or
-    bfloat16.  Returns out [B,H,n,dv]."""
+    bfloat16.  Returns out [B,H,n,dv] (and with return_final_state the streaming state
+    [B,H,state_floats(d, dv)] after the last token, for hla3_decode_step)."""
     L = lib()
     if q.dtype not in _DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k, v must all be float32 or all bfloat16")
@@ -555,15 +556,17 @@ def hla3_forward(q, k, v, normalize=False, chunk=64, eps=1e-6, out=None):
     qd, kd, vd = (t.contiguous() for t in (q, k, v))
     o = out if out is not None else torch.empty((B, H, n, dv), dtype=q.dtype, device=device)
     sh = _stream_handle(device)
-    nbytes = L.hla2_hla3_forward_workspace_bytes(B, H, n, d, dv, chunk, _DTYPES[q.dtype], int(normalize))
+    nbytes = L.hla2_hla3_forward_workspace_bytes(B, H, n, d, dv, chunk, _DTYPES[q.dtype], int(normalize),
+                                                 int(return_final_state))
     if nbytes == ctypes.c_size_t(-1).value:
         nbytes = 0
     ws = _workspace(int(nbytes), device, sh)
-    opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), int(nbytes), None, None, None,
-                0, 0)
+    fin = torch.empty((B, H, state_floats(d, dv)), dtype=torch.float32, device=device) if return_final_state else None
+    opts = Opts(_DTYPES[q.dtype], float(eps), None if ws is None else ws.data_ptr(), int(nbytes), None,
+                None if fin is None else fin.data_ptr(), None, 0, 0)
     _check("hla2_hla3_forward", L.hla2_hla3_forward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(o), B, H, n, d, dv, None,
                                                     int(normalize), chunk, sh, ctypes.byref(opts)))
-    return o
+    return (o, fin) if return_final_state else o
 
 
 def hla3_decode_step(state, q, k, v, normalize=False, eps=1e-6, out=None):

@@ -221,11 +221,13 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
  * workspace, then hla2_forward on (q, k, u) -- the tcgen05 kernels for bf16, d = dv = 64,
  * chunk 128.  normalize != 0 divides by the same sum with v -> 1 (+ opts->eps), computed the
  * same way with the value rows (1, 0, ..., 0).  gamma must be NULL (HLA2_ERR_UNSUPPORTED
- * otherwise); no init_state / final_state; opts->flags must be 0.  Tensors as for
- * hla2_forward; the workspace is hla2_hla3_forward_workspace_bytes.
+ * otherwise); no init_state; opts->final_state receives the streaming state after token n
+ * in the layout of hla2_hla3_decode_step (prefill; the unit-value passes then run as for
+ * normalize); opts->flags must be 0.  Tensors as for hla2_forward; the workspace is
+ * hla2_hla3_forward_workspace_bytes.
  */
 size_t hla2_hla3_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
-                                         int normalize);
+                                         int normalize, int want_final_state);
 int hla2_hla3_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n, int d,
                       int dv, const float* gamma, int normalize, int chunk, hla2_stream_t stream,
                       const hla2_opts* opts);

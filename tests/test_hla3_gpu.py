@@ -118,3 +118,30 @@ def test_decode_from_zero_equals_forward(dtype, d, dv, normalize):
     for t in range(n):
         O3.decode_step(st, np64(x["q"][:, :, t]), np64(x["k"][:, :, t]), np64(x["v"][:, :, t]), normalize)
     assert rel_err(state.cpu().double().numpy(), st) <= 1e-5
+
+
+@pytest.mark.parametrize("dtype, d, chunk", [(torch.float32, 32, 32), (torch.bfloat16, 64, 128), (torch.bfloat16, 32, 64)])
+@pytest.mark.parametrize("normalize", [False, True])
+def test_prefill_then_decode_matches_the_oracle(dtype, d, chunk, normalize):
+    """The forward's final state (prefill) equals the oracle's streaming state, and decode steps
+    continued from it reproduce the oracle's outputs over prefill + decode tokens."""
+    N, H, n0, steps = 2, 3, 200, 5
+    x = inputs.make_custom(N, H, n0 + steps, d, d, dtype, seed=d + chunk + 95, qk="softplus" if normalize else "gauss",
+                           v_scale="unit" if normalize else "gauss_sqrt_d")
+    q, k, v = (x[key].cuda() for key in ("q", "k", "v"))
+    _, state = hla.hla3_forward(q[:, :, :n0].contiguous(), k[:, :, :n0].contiguous(), v[:, :, :n0].contiguous(),
+                                chunk=chunk, normalize=normalize, eps=1e-6, return_final_state=True)
+    st = np.zeros((N, H, O3.state_floats(d, d)))
+    for t in range(n0):
+        O3.decode_step(st, np64(x["q"][:, :, t]), np64(x["k"][:, :, t]), np64(x["v"][:, :, t]), normalize)
+    tol_state = 1e-4 if dtype == torch.float32 else 2e-2
+    got = state.cpu().double().numpy()
+    sizes = (d * d, d * d, d * d, d, d)  # S, P, Y, m, y
+    off = 0
+    for name, size in zip(("S", "P", "Y", "m", "y"), sizes):
+        assert rel_err(got[..., off:off + size], st[..., off:off + size]) <= tol_state, name
+        off += size
+    ref = O3.serial_forward(np64(x["q"]), np64(x["k"]), np64(x["v"]), normalize=normalize, eps=1e-6)
+    for t in range(n0, n0 + steps):
+        o = hla.hla3_decode_step(state, q[:, :, t], k[:, :, t], v[:, :, t], normalize=normalize, eps=1e-6)
+        assert rel_err(np64(o.cpu()), ref[:, :, t]) <= tol_for(dtype), t
