@@ -44,6 +44,8 @@ __all__ = [
     "identity_element",
     "combine",
     "chunked_scan_forward",
+    "serial_backward",
+    "pairsum_grads",
 ]
 
 
@@ -167,3 +169,69 @@ def chunked_scan_forward(q, k, v, gamma=None, chunk=16, normalize=False, eps=1e-
                     t += 1
                 carry = combine(carry, totals[ci])
     return out
+
+
+def serial_backward(q, k, v, dout, gamma=None):
+    """Hand adjoint of the unnormalised recurrence A3 ([PS] §4.2 states the reverse-mode scan
+    for the second-order case; the same reverse sweep applies here).
+
+    Forward at token t:  P_t = g P + k v^T;  i_t = P_t^T q;  E_t = g E + k i_t^T;  o_t = E_t^T q.
+    Reverse sweep with state adjoints (Eb, Pb) flowing from t+1 to t:
+        Eb = g Eb + q dO^T;        dq += E_t dO;
+        ib = Eb^T k;               dk += Eb i_t;
+        Pb = g Pb + q ib^T;        dq += P_t ib;
+        dk += Pb v;                dv += Pb^T k.
+    Returns (dq, dk, dv) in float64."""
+    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    B, H, n, d = q.shape
+    dv_ = v.shape[-1]
+    g = _gamma(gamma, H)[None, :]
+    Ps, Es, Is = [], [], []
+    P = np.zeros((B, H, d, dv_))
+    E = np.zeros((B, H, d, dv_))
+    for t in range(n):  # forward, keeping the states
+        P = g[..., None, None] * P + np.einsum("bha,bhe->bhae", k[:, :, t], v[:, :, t])
+        inner = np.einsum("bha,bhae->bhe", q[:, :, t], P)
+        E = g[..., None, None] * E + np.einsum("bha,bhe->bhae", k[:, :, t], inner)
+        Ps.append(P)
+        Es.append(E)
+        Is.append(inner)
+    dq, dk, dvv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    Eb = np.zeros((B, H, d, dv_))
+    Pb = np.zeros((B, H, d, dv_))
+    for t in range(n - 1, -1, -1):
+        qt, kt, vt, ot = q[:, :, t], k[:, :, t], v[:, :, t], dout[:, :, t]
+        Eb = g[..., None, None] * Eb + np.einsum("bha,bhe->bhae", qt, ot)
+        dq[:, :, t] += np.einsum("bhae,bhe->bha", Es[t], ot)
+        ib = np.einsum("bhae,bha->bhe", Eb, kt)
+        dk[:, :, t] += np.einsum("bhae,bhe->bha", Eb, Is[t])
+        Pb = g[..., None, None] * Pb + np.einsum("bha,bhe->bhae", qt, ib)
+        dq[:, :, t] += np.einsum("bhae,bhe->bha", Ps[t], ib)
+        dk[:, :, t] += np.einsum("bhae,bhe->bha", Pb, vt)
+        dvv[:, :, t] += np.einsum("bhae,bha->bhe", Pb, kt)
+    return dq, dk, dvv
+
+
+def pairsum_grads(q, k, v, dout, gamma=None):
+    """Gradients of L = sum_t dO_t . o_t with o_t the pair sum A1 (decay A2), differentiated
+    term by term: each term g^(t-i) (q_t.k_j)(q_j.k_i) v_i contributes to q_t, k_j, q_j, k_i
+    and v_i.  O(n^3) per head: tiny n only."""
+    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    B, H, n, d = q.shape
+    g = _gamma(gamma, H)
+    dq, dk, dvv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            Q, K, V, O = q[b, h], k[b, h], v[b, h], dout[b, h]
+            for t in range(n):
+                for j in range(t + 1):
+                    for i in range(j + 1):
+                        w = g[h] ** (t - i)
+                        a, c = Q[t] @ K[j], Q[j] @ K[i]
+                        s = O[t] @ V[i]  # dL/d(weight of the term)
+                        dq[b, h, t] += w * s * c * K[j]
+                        dk[b, h, j] += w * s * c * Q[t]
+                        dq[b, h, j] += w * s * a * K[i]
+                        dk[b, h, i] += w * s * a * Q[j]
+                        dvv[b, h, i] += w * a * c * O[t]
+    return dq, dk, dvv

@@ -113,3 +113,62 @@ def test_planted_mistakes_are_caught(monkeypatch):
     assert rel(pre_update_inner(q, k, v), ref) > 1e-3
     brute_sq = A.brute_force_forward(q, k, v, [0.9 ** 2])  # g^2 per hop instead of g
     assert rel(brute_sq, ref) > 1e-3
+
+
+def test_adjoint_matches_the_pair_sum_gradients():
+    q, k, v = rnd(1, 2, 7, 3, 2, seed=20)
+    dO = np.random.default_rng(21).standard_normal(v.shape)
+    g = [0.9, 1.0]
+    got = A.serial_backward(q, k, v, dO, g)
+    ref = A.pairsum_grads(q, k, v, dO, g)
+    for a, b in zip(got, ref):
+        assert rel(a, b) < 1e-12
+
+
+def test_adjoint_matches_central_differences():
+    q, k, v = rnd(1, 1, 6, 3, 2, seed=22)
+    dO = np.random.default_rng(23).standard_normal(v.shape)
+    g = [0.85]
+    dq, dk, dv = A.serial_backward(q, k, v, dO, g)
+    loss = lambda q_, k_, v_: np.sum(A.serial_forward(q_, k_, v_, g) * dO)  # noqa: E731
+    h = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = {"q": q, "k": k, "v": v}
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (loss(**{"q_": args_p["q"], "k_": args_p["k"], "v_": args_p["v"]})
+                        - loss(**{"q_": args_m["q"], "k_": args_m["k"], "v_": args_m["v"]})) / (2 * h)
+        assert rel(grad, num) < 1e-7, name
+
+
+def test_adjoint_planted_mistake_is_caught():
+    """Reading the inner adjoint from the pre-update E adjoint (dropping the token's own
+    output term) breaks agreement with the pair-sum gradients."""
+    q, k, v = rnd(1, 1, 5, 3, 2, seed=24)
+    dO = np.random.default_rng(25).standard_normal(v.shape)
+    ref = A.pairsum_grads(q, k, v, dO, [0.9])
+    Q, K, V, O = q[0, 0], k[0, 0], v[0, 0], dO[0, 0]
+    g = 0.9
+    Ps, Es, Is = [], [], []
+    P = np.zeros((3, 2))
+    E = np.zeros((3, 2))
+    for t in range(5):
+        P = g * P + np.outer(K[t], V[t])
+        i_t = Q[t] @ P
+        E = g * E + np.outer(K[t], i_t)
+        Ps.append(P); Es.append(E); Is.append(i_t)
+    dk = np.zeros_like(K)
+    Eb = np.zeros((3, 2))
+    Pb = np.zeros((3, 2))
+    for t in range(4, -1, -1):
+        ib = Eb.T @ K[t]                           # mistake: before adding q_t dO_t^T
+        Eb = g * Eb + np.outer(Q[t], O[t])
+        dk[t] += Eb @ Is[t]
+        Pb = g * Pb + np.outer(Q[t], ib)
+        dk[t] += Pb @ V[t]
+    assert rel(dk, ref[1][0, 0]) > 1e-3
