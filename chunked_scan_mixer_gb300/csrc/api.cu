@@ -1314,6 +1314,96 @@ extern "C" int hla2_hla3_forward(const void* q, const void* k, const void* v, vo
     return succeed();
 }
 
+// ---- AHLA reverse mode ----------------------------------------------------------------------
+
+static int ahla_bwd_width(int d, int chunk, const DevInfo& di) {
+    for (int W = chunk < 32 ? chunk : 32; W >= 16; W /= 2)
+        if (ahla_bwd_smem(d, W) <= (size_t)di.smem_optin) return W;
+    return 0;
+}
+
+struct AhlaBwdPlan {
+    int W = 0;
+    Plan p;
+    AhlaBwdLayout L;
+};
+
+static AhlaBwdPlan ahla_bwd_plan(int B, int H, int n, int d, int chunk, const DevInfo& di) {
+    AhlaBwdPlan bp;
+    bp.W = ahla_bwd_width(d, chunk, di);
+    if (!bp.W) return bp;
+    bp.p = make_plan(B, H, n, d, d, bp.W, di.sms, blocks_per_sm(ahla_bwd_smem(d, bp.W), 256, 4, di));
+    bp.L = ahla_bwd_layout(B * H, bp.p.nseg, bp.p.nchunks, d);
+    return bp;
+}
+
+extern "C" size_t hla2_ahla_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
+                                                     int normalize) {
+    if (check_common(B, H, n, d, dv, dtype, normalize) != HLA2_OK || !dim_ok(chunk) || d != dv || normalize)
+        return (size_t)-1;
+    const AhlaBwdPlan bp = ahla_bwd_plan(B, H, n, d, chunk, dev_info());
+    if (!bp.W) return (size_t)-1;
+    return bp.p.nseg > 0 ? bp.L.total * sizeof(float) : 0;
+}
+
+extern "C" int hla2_ahla_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
+                                  void* dv_out, int B, int H, int n, int d, int dv, const float* gamma, int normalize,
+                                  int chunk, hla2_stream_t stream, const hla2_opts* opts) {
+    NvtxScope nvtx("hla2_ahla_backward");
+    if (!opts) return fail(HLA2_ERR_INVALID_ARG, "opts must not be NULL");
+    int rc = check_common(B, H, n, d, dv, opts->dtype, normalize);
+    if (rc != HLA2_OK) return rc;
+    if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
+    if (d != dv) return fail(HLA2_ERR_UNSUPPORTED, "the AHLA backward needs d == dv");
+    if (normalize) return fail(HLA2_ERR_UNSUPPORTED, "the AHLA backward covers the unnormalised output");
+    if (opts->flags || opts->init_state || opts->final_state)
+        return fail(HLA2_ERR_INVALID_ARG, "the AHLA backward takes no flags, init_state or final_state");
+    const long BH = (long)B * H;
+    if (BH == 0 || n == 0) return succeed();
+    if (!q || !k || !v || !dout || !dq || !dk || !dv_out)
+        return fail(HLA2_ERR_INVALID_ARG, "q, k, v, dout, dq, dk, dv must not be NULL");
+    const DevInfo di = dev_info();
+    const AhlaBwdPlan bp = ahla_bwd_plan(B, H, n, d, chunk, di);
+    if (!bp.W) return fail(HLA2_ERR_UNSUPPORTED, "no AHLA backward kernel for d %d", d);
+    const size_t need = bp.L.total * sizeof(float);
+    if (!opts->workspace || opts->workspace_bytes < need)
+        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
+                    opts->workspace ? opts->workspace_bytes : (size_t)0);
+    if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    AhlaBwdArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.dout = dout;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv_out;
+    a.BH = (int)BH;
+    a.H = H;
+    a.n = n;
+    a.d = d;
+    a.W = bp.W;
+    a.nchunks = bp.p.nchunks;
+    a.seg_chunks = bp.p.seg_chunks;
+    a.nseg = bp.p.nseg;
+    a.gamma = gamma;
+    a.ws = static_cast<float*>(opts->workspace);
+    a.PB = bp.L.PB;
+    a.EB = bp.L.EB;
+    a.RB = bp.L.RB;
+    a.Pin = bp.L.Pin;
+    a.Ein = bp.L.Ein;
+    a.EhB = bp.L.EhB;
+    a.PhB = bp.L.PhB;
+    a.Eh_end = bp.L.Eh_end;
+    a.Ph_end = bp.L.Ph_end;
+    a.states = bp.L.states;
+    cudaGetLastError();
+    if (launch_ahla_backward(a, opts->dtype == HLA2_BF16, reinterpret_cast<cudaStream_t>(stream)))
+        return cuda_fail("AHLA backward");
+    return succeed();
+}
+
 static Plan ahla_plan(int B, int H, int n, int d, int chunk) {
     const DevInfo di = dev_info();
     const int per_sm = chunk == 128 ? blocks_per_sm(ahla_tc_smem(), 288, 2, di)

@@ -192,6 +192,28 @@ int launch_hla3_decode_step(float* state, const void* q, const void* k, const vo
 int launch_ahla_decode_step(float* state, const void* q, const void* k, const void* v, void* out, int N, int H,
                             int d, int dv, const float* gamma, int normalize, float eps, bool is_bf16,
                             cudaStream_t st);
+// AHLA reverse mode (ahla_bwd.cu, SIMT float32, d == dv).  Workspace float offsets, each block
+// [BH][nseg][d*d] (states: [BH][nchunks][2 d*d], P then E at every chunk start).
+struct AhlaBwdLayout {
+    size_t PB, EB, RB, Pin, Ein, EhB, PhB, Eh_end, Ph_end, states, total;
+};
+AhlaBwdLayout ahla_bwd_layout(int BH, int nseg, int nchunks, int d);
+struct AhlaBwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* dout;
+    void* dq;
+    void* dk;
+    void* dv;
+    int BH, H, n, d, W, nchunks, seg_chunks, nseg;
+    const float* gamma;
+    float* ws;
+    size_t PB, EB, RB, Pin, Ein, EhB, PhB, Eh_end, Ph_end, states;
+};
+int launch_ahla_backward(const AhlaBwdArgs& a, bool is_bf16, cudaStream_t st);
+size_t ahla_bwd_smem(int d, int W);
+
 // Masked first-order linear attention u_t = sum_{l <= t} g^(t-l) (q_t . k_l) v_l, the inner
 // pass of the third-order output (linattn.cu).  Workspace floats: PB [BH][nseg-1][d*dv],
 // Pin [BH][nseg][d*dv].

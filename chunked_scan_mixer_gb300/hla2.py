@@ -111,6 +111,10 @@ def lib():
         L.hla2_hla3_forward_workspace_bytes.restype = Z
         L.hla2_hla3_forward.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
         L.hla2_hla3_forward.restype = I
+        L.hla2_ahla_backward_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
+        L.hla2_ahla_backward_workspace_bytes.restype = Z
+        L.hla2_ahla_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
+        L.hla2_ahla_backward.restype = I
         L.hla2_hla3_decode_step.argtypes = [P, P, P, P, P, I, I, I, I, I, P, ctypes.POINTER(Opts)]
         L.hla2_hla3_decode_step.restype = I
         L.hla2_selftest_wait_timeout.argtypes = [P, P]
@@ -133,6 +137,7 @@ EXPORTED_SYMBOLS = (
     "hla2_state_to_compact", "hla2_state_from_compact", "hla2_ahla_forward_workspace_bytes", "hla2_ahla_forward",
     "hla2_ahla_state_floats", "hla2_ahla_decode_step", "hla2_mq_head_state_floats", "hla2_decode_step_mq",
     "hla2_selftest_wait_timeout", "hla2_hla3_forward_workspace_bytes", "hla2_hla3_forward", "hla2_hla3_decode_step",
+    "hla2_ahla_backward_workspace_bytes", "hla2_ahla_backward",
 )
 
 FLAG_COMPACT_STATE = 4
@@ -586,3 +591,27 @@ def hla3_decode_step(state, q, k, v, normalize=False, eps=1e-6, out=None):
                                                             H, d, dv, int(normalize), _stream_handle(device),
                                                             ctypes.byref(opts)))
     return o
+
+
+def ahla_backward(q, k, v, dout, gamma=None, chunk=32):
+    """Gradients (dq, dk, dv) of the unnormalised AHLA output for upstream dout.  float32 or
+    bfloat16 CUDA tensors [B,H,n,d] (d == dv)."""
+    L = lib()
+    if q.dtype not in _DTYPES or any(t.dtype != q.dtype for t in (k, v, dout)):
+        raise TypeError("q, k, v, dout must share a dtype (float32 or bfloat16)")
+    B, H, n, d = q.shape
+    dv = v.shape[-1]
+    device = q.device
+    qd, kd, vd, od = (t.contiguous() for t in (q, k, v, dout))
+    g = _gamma_tensor(gamma, H, device)
+    gq, gk, gv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    sh = _stream_handle(device)
+    nbytes = L.hla2_ahla_backward_workspace_bytes(B, H, n, d, dv, chunk, _DTYPES[q.dtype], 0)
+    if nbytes == ctypes.c_size_t(-1).value:
+        nbytes = 0
+    ws = _workspace(int(nbytes), device, sh)
+    opts = Opts(_DTYPES[q.dtype], 1e-6, None if ws is None else ws.data_ptr(), int(nbytes), None, None, None, 0, 0)
+    _check("hla2_ahla_backward", L.hla2_ahla_backward(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(od), _ptr(gq), _ptr(gk),
+                                                      _ptr(gv), B, H, n, d, dv, _ptr(g), 0, chunk, sh,
+                                                      ctypes.byref(opts)))
+    return gq, gk, gv

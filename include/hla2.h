@@ -211,6 +211,22 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
                      hla2_stream_t stream, const hla2_opts* opts);
 
 /*
+ * AHLA reverse mode (section summary §4.2's reverse-mode scan applied to the AHLA
+ * recurrence): given dout = dL/dout of the unnormalised hla2_ahla_forward output, writes dq,
+ * dk, dv.  float32 or bf16 tensors [B, H, n, d], d == dv; float32 arithmetic on SIMT kernels
+ * at a chunk width <= min(chunk, 32).  The passes recompute the forward (segment summaries
+ * P_B, E_B, R_B, the forward scan, the state at every chunk start) and then run the reverse
+ * summaries, the reverse scan (cross term rho R_B^T Eh_end) and the gradient pass.  normalize
+ * must be 0; no flags, init_state or final_state.  Workspace:
+ * hla2_ahla_backward_workspace_bytes.
+ */
+size_t hla2_ahla_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
+                                          int normalize);
+int hla2_ahla_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk,
+                       void* dv_out, int B, int H, int n, int d, int dv, const float* gamma, int normalize,
+                       int chunk, hla2_stream_t stream, const hla2_opts* opts);
+
+/*
  * Masked third-order HLA at gamma = 1 (technical summary item "3. Dritte Ordnung HLA": the
  * product A A^T A with A = Q K^T, masked so that strict causality holds; section summary:
  * the chunk scan of this case is exact for gamma = 1).  Every factor and the partial product

@@ -211,3 +211,36 @@ def test_empty_sequence_passes_init_state_through():
     _, fin = hla.ahla_forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), chunk=32, init_state=init,
                               return_final_state=True)
     assert torch.equal(fin, init)
+
+
+# ---- reverse mode ------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d, chunk, n", [(16, 16, 77), (32, 32, 300), (64, 32, 500), (128, 16, 90), (64, 64, 1000)])
+def test_backward_matches_the_oracle_adjoint(dtype, d, chunk, n):
+    """AHLA gradients against the oracle's reverse sweep of the serial recurrence, across
+    chunks, segments and a ragged tail."""
+    x = inputs.make_custom(1, 2, n, d, d, dtype, seed=d + chunk + n, gamma=(0.95, 0.999), with_dout=True)
+    got = hla.ahla_backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), gamma=x["gamma"].cuda(),
+                            chunk=chunk)
+    ref = A.serial_backward(np32(x["q"]), np32(x["k"]), np32(x["v"]), np32(x["dout"]), x["gamma"].double().numpy())
+    tol = 1e-4 if dtype == torch.float32 else 2e-2
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, ref):
+        assert rel_err(np64(gg.cpu()), rr) <= tol, name
+
+
+def test_backward_tiny_against_the_pair_sum_gradients():
+    x = inputs.make_custom(1, 1, 20, 16, 16, torch.float32, seed=99, gamma=0.9, with_dout=True)
+    got = hla.ahla_backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), gamma=x["gamma"].cuda(),
+                            chunk=16)
+    ref = A.pairsum_grads(np32(x["q"]), np32(x["k"]), np32(x["v"]), np32(x["dout"]), [0.9])
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, ref):
+        assert rel_err(np64(gg.cpu()), rr) <= 1e-4, name
+
+
+def test_backward_many_segments_no_decay():
+    x = inputs.make_custom(2, 2, 2500, 32, 32, torch.float32, seed=98, gamma=None, with_dout=True)
+    got = hla.ahla_backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), chunk=16)
+    ref = A.serial_backward(np32(x["q"]), np32(x["k"]), np32(x["v"]), np32(x["dout"]), None)
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, ref):
+        assert rel_err(np64(gg.cpu()), rr) <= 1e-4, name
