@@ -389,11 +389,18 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     a.unmasked = unmasked ? 1 : 0;
 
     const bool bf = opts->dtype == HLA2_BF16;
+    // Masked tcgen05 path with more than one segment: the summary pass also stores the
+    // segment-local p_t = S_t q_t in out, over every segment, and the output pass starts from it
+    // (kOutputP), so that only Z is carried from chunk to chunk there.
+    const bool stored_p = path == Path::kTc && !unmasked && p.nseg > 1;
     auto chunk_pass = [&](int seg0, int count, bool summary, bool cm) -> int {
         ChunkArgs b = a;
         b.seg0 = seg0;
         b.nseg_launch = count;
-        if (path == Path::kTc) return launch_fwd_chunk_tc(b, summary ? kSummary : kOutput, reinterpret_cast<int*>(a.ws), st);
+        b.store_p = stored_p ? 1 : 0;
+        if (path == Path::kTc)
+            return launch_fwd_chunk_tc(b, summary ? kSummary : (stored_p ? kOutputP : kOutput),
+                                       reinterpret_cast<int*>(a.ws), st);
         if (path == Path::kMma) return launch_fwd_chunk_mma(b, d, dv, chunk, summary ? kSummary : kOutput, cm, st);
         return launch_fwd_chunk_simt(b, d, dv, chunk, summary, cm, bf, st);
     };
@@ -411,7 +418,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     if (p.nseg > 1) {
         const int steps = p.nseg - 1, seg_tokens = p.seg_chunks * chunk;
         const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
-        if (chunk_pass(0, steps, true, true)) return cuda_fail("segment summaries");
+        if (chunk_pass(0, stored_p ? p.nseg : steps, true, true)) return cuda_fail("segment summaries");
         mark(2);
         if (launch_linear_scan(a.ws + L.SB, a.ws + L.Sin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true,
                                gamma, seg_tokens, 1, st))

@@ -362,6 +362,27 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[BPS]);
+            if (SUMMARY && !UM && a.store_p) {
+                // segment-local p for the kOutputP pass, off the chain: while the state product
+                // runs, P is formed again from Q S0 (T0) and A~ K (T2), which stay in place until
+                // the next chunk's MMA1 and MMA2
+                const float s1 = gp[r + 1];
+                bf16* po = static_cast<bf16*>(a.out) + ((size_t)bh * a.n + (size_t)c * kW + r) * kD + 32 * h;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t qs[16], ak[16];
+                    tc::tmem_ld16(lrow + T0 + 32 * h + 16 * half, qs);
+                    tc::tmem_ld16(lrow + T2 + 32 * h + 16 * half, ak);
+                    tc::tmem_wait_ld();
+                    float pv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pv[j] = s1 * __uint_as_float(qs[j]) + __uint_as_float(ak[j]);
+                    if (r < Wc) {
+                        reinterpret_cast<uint4*>(po + 16 * half)[0] = pack8(&pv[0], 1.f);
+                        reinterpret_cast<uint4*>(po + 16 * half)[1] = pack8(&pv[8], 1.f);
+                    }
+                }
+            }
 
             if (!SUMMARY) {
                 // ---- EPI3: B~ -> T3 ----------------------------------------------------------
@@ -436,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (lane == 0) tc::mbar_arrive(&bars[BS]);
         }
 
-        if (SUMMARY) {
+        if (SUMMARY && seg < a.nsum) {  // (a launch that stores p also covers the last segment)
             const size_t si = (size_t)bh * a.nsum + seg;
             float* dst = r < 64 ? a.ws + a.L.CB + si * kD * kD + (size_t)r * kD
                                 : a.ws + a.L.ZB + si * kD * kD + (size_t)(r - 64) * kD;
@@ -449,6 +470,276 @@ __global__ void __launch_bounds__(kThreads, 2)
                 a.ws[a.L.mB + si * kD + r] = 0.f;
                 a.ws[a.L.yB + si * kD + r] = 0.f;
             }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Output pass from the stored segment-local p (masked, unnormalised; kOutputP).
+//
+// The summary pass stores, for every token t of segment s, p^sl_t = S^sl_t q_t, where S^sl is
+// the key moment accumulated from zero at the segment start (bf16, in the output buffer).
+// With the segment's carry-in S_in (section summary §4: the carry enters by one decayed
+// product),
+//     p_t = p^sl_t + g^(t - t0 + 1) S_in q_t,         t0 = the segment's first token,
+// so the key moment leaves the chunk-to-chunk chain: this pass reads q, p^sl and v (no k) and
+// carries only Z from chunk to chunk.  Per chunk (local row r, it = chunk index in the segment):
+//   MMA-a  Q S_in -> T3                                          (no dependence on Z)
+//   EPI-a  P = P^sl + g^(it W + r + 1) Q S_in  (bf16, in place);  P~ = diag(g^(2(Wc-1-r))) P
+//   MMA-b  B = Q P^T -> T0T1;  Q Z0 -> T2
+//   EPI-b  B~ = B * [j <= r] g^(2(r-j))  (bf16)  -> T3
+//   MMA-c  B~ V -> T0;  [P~^T ; P~^T] V -> T1 (dZ, rows 0..63 and again 64..127)
+//   EPI-c  out = g^(2(r+1)) Q Z0 + B~ V  (bf16, over this chunk's p^sl, already consumed);
+//          Z <- g^(2Wc) Z + dZ  (fp32, 16 columns a thread);  bf16 Z0 (smem)
+// MMA-a of the next chunk and the next loads overlap EPI-c.  Same roles, bounded waits and
+// two CTAs per SM as the kernel above.
+namespace outp {
+
+constexpr uint32_t oQ = 0, oP = kTile, oV = 2 * kTile, oPt = 3 * kTile;
+constexpr uint32_t oS = 4 * kTile;        // S_in, [64][64] bf16 (8 KB), B operand of Q S_in
+constexpr uint32_t oZ0 = oS + 8192;       // Z0, [64][64] bf16 (8 KB), B operand of Q Z0
+constexpr uint32_t oGP = oZ0 + 8192;      // decay table g^0 .. g^(2W)
+constexpr uint32_t oBar = oGP + 1088;
+constexpr uint32_t oMisc = oBar + 16 * 8;
+constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
+constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192;
+
+enum Bar { FQP = 0, FV, BA, BAT, BB, BBT, BC, kBarCount };
+
+struct Maps {
+    CUtensorMap q, p, v;
+};
+
+}  // namespace outp
+
+__global__ void __launch_bounds__(kThreads, 2)
+    fwd_out_p_tc_kernel(const __grid_constant__ outp::Maps maps, const ChunkArgs a, int* status) {
+    // this pass's layout (shadows the kernel above)
+    constexpr uint32_t oQ = outp::oQ, oP = outp::oP, oV = outp::oV, oPt = outp::oPt, oS = outp::oS, oZ0 = outp::oZ0;
+    constexpr uint32_t oGP = outp::oGP, oBar = outp::oBar, oMisc = outp::oMisc;
+    constexpr uint32_t T0 = outp::T0, T1 = outp::T1, T2 = outp::T2, T3 = outp::T3;
+    constexpr int FQP = outp::FQP, FV = outp::FV, BA = outp::BA, BAT = outp::BAT, BB = outp::BB, BBT = outp::BBT,
+                  BC = outp::BC, kBarCount = outp::kBarCount;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* gp = reinterpret_cast<float*>(sm + oGP);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + oMisc);
+    volatile int* abort = reinterpret_cast<volatile int*>(sm + oMisc + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seg = a.seg0 + blockIdx.x, bh = blockIdx.y;
+    const int c_begin = seg * a.seg_chunks;
+    const int c_end = min(c_begin + a.seg_chunks, a.nchunks);
+    const float g = head_decay(a.gamma, bh, a.H);
+    const float log2g = log2f(g);
+    const int nit = c_end - c_begin;
+
+    // epilogue thread: TMEM lane / token row r, column half h; Z row zr, columns zc .. zc+15
+    const int q4 = warp & 3, h = (warp - 1) >> 2;
+    const int r = 32 * q4 + lane;
+    const int zr = r & 63, zc = 32 * h + 16 * (r >> 6);
+    float zz[16];
+    auto publish_z = [&]() {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            *reinterpret_cast<uint4*>(sm + oZ0 + tc::sw128_chunk(zr, zc / 8 + j)) = pack8(&zz[8 * j], 1.f);
+    };
+
+    for (int i = tid; i < 2 * kW + 1; i += kThreads) gp[i] = pow_decay(log2g, (float)i);
+    if (tid == 0) {
+        for (int b = 0; b < kBarCount; ++b) tc::mbar_init(&bars[b], (b == BAT || b == BBT) ? 8 : 1);
+        *abort = 0;
+        tc::mbar_fence_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_holder, kTmemCols);
+    } else {
+        // carry-in of the segment: S_in (bf16, smem) and Z_in (fp32 registers, bf16 copy in smem)
+        const size_t sidx = (size_t)bh * a.nseg + seg;
+        if (r < 64) {
+            const float* src = a.ws + a.L.Sin + sidx * kD * kD + (size_t)r * kD + 32 * h;
+            float t[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) t[j] = src[j];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(sm + oS + tc::sw128_chunk(r, 4 * h + j)) = pack8(&t[8 * j], 1.f);
+        }
+        const float* zsrc = a.ws + a.L.Zin + sidx * kD * kD + (size_t)zr * kD + zc;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) zz[j] = zsrc[j];
+        publish_z();
+        tc::fence_proxy_async();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ control thread
+        if (lane == 0 && nit > 0) {
+            const uint32_t sQ = smem_u32(sm + oQ), sP = smem_u32(sm + oP), sV = smem_u32(sm + oV);
+            const uint32_t sPt = smem_u32(sm + oPt), sS = smem_u32(sm + oS), sZ0 = smem_u32(sm + oZ0);
+            auto load_qp = [&](int c) {
+                tc::mbar_arrive_expect_tx(&bars[FQP], 2 * kTile);
+                tc::tma_load_3d(sm + oQ, &maps.q, 0, c * kW, bh, &bars[FQP]);
+                tc::tma_load_3d(sm + oP, &maps.p, 0, c * kW, bh, &bars[FQP]);
+            };
+            auto load_v = [&](int c) {
+                tc::mbar_arrive_expect_tx(&bars[FV], kTile);
+                tc::tma_load_3d(sm + oV, &maps.v, 0, c * kW, bh, &bars[FV]);
+            };
+            constexpr uint32_t I_AB = tc::idesc_bf16(128, 128, 0, 0);   // K-major x K-major, N = 128
+            constexpr uint32_t I_QX = tc::idesc_bf16(128, 64, 0, 1);    // K-major x MN-major, N = 64
+            constexpr uint32_t I_TS64 = tc::idesc_bf16(128, 64, 0, 1);  // A (TMEM) x MN-major B, N = 64
+            constexpr uint32_t I_ST64 = tc::idesc_bf16(128, 64, 1, 1);  // MN-major x MN-major, N = 64
+            load_qp(c_begin);
+            load_v(c_begin);
+            int lqp = 1, lv = 1;
+            for (int it = 0; it < nit; ++it) {
+                const uint32_t ph = it & 1;
+                tc::mbar_wait(&bars[FQP], ph, abort, status, 41);
+                tc::fence_after_sync();
+                // MMA-a: Q S_in -> T3 (T3's B~ of the previous chunk was read: its MMA-c completed)
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_ss(tmem + T3, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sS + 2048 * ks, 16, 1024),
+                               I_QX, ks > 0);
+                tc::mma_commit(&bars[BA]);
+                tc::mbar_wait(&bars[BAT], ph, abort, status, 42);  // P, P~ written; previous EPI-c done
+                tc::fence_after_sync();
+                // MMA-b: B = Q P^T -> T0T1;  Q Z0 -> T2
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sP + 32 * ks, 16, 1024),
+                               I_AB, ks > 0);
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_ss(tmem + T2, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sZ0 + 2048 * ks, 16, 1024),
+                               I_QX, ks > 0);
+                tc::mma_commit(&bars[BB]);
+                tc::mbar_wait(&bars[BB], ph, abort, status, 43);  // Q and P no longer read
+                if (it + 1 < nit) {
+                    load_qp(c_begin + it + 1);
+                    ++lqp;
+                }
+                tc::mbar_wait(&bars[BBT], ph, abort, status, 44);
+                tc::mbar_wait(&bars[FV], ph, abort, status, 45);
+                tc::fence_after_sync();
+                // MMA-c: B~ V -> T0;  [P~^T ; P~^T] V -> T1
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ts(tmem + T0, tmem + T3 + 8 * ks, tc::smem_desc(sV + 2048 * ks, 16, 1024), I_TS64, ks > 0);
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem + T1, tc::smem_desc(sPt + 2048 * ks, 0, 1024), tc::smem_desc(sV + 2048 * ks, 16, 1024),
+                               I_ST64, ks > 0);
+                tc::mma_commit(&bars[BC]);
+                tc::mbar_wait(&bars[BC], ph, abort, status, 46);  // V, P~ and T3 free
+                if (it + 1 < nit) {
+                    load_v(c_begin + it + 1);
+                    ++lv;
+                }
+            }
+            // drain (bounded, ignoring the abort flag) so that nothing is in flight at exit
+            volatile int never = 0;
+            tc::mbar_wait(&bars[BC], (nit - 1) & 1, &never, nullptr, 0);
+            tc::mbar_wait(&bars[FQP], (lqp - 1) & 1, &never, nullptr, 0);
+            tc::mbar_wait(&bars[FV], (lv - 1) & 1, &never, nullptr, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int row0 = 32 * q4;
+        const uint32_t lrow = tmem + ((uint32_t)row0 << 16);
+        unsigned char* sP = sm + oP;
+        unsigned char* sPt = sm + oPt;
+        const float ginv = g > 0.f ? 1.f / g : 0.f;
+        for (int it = 0; it < nit; ++it) {
+            const uint32_t ph = it & 1;
+            const int c = c_begin + it;
+            const int Wc = min(kW, a.n - c * kW);
+            // ---- EPI-a: P = P^sl + g^(it W + r + 1) Q S_in;  P (in place), P~ -> smem ----------
+            tc::mbar_wait(&bars[FQP], ph, abort, status, 51);
+            tc::mbar_wait(&bars[BA], ph, abort, status, 52);
+            tc::fence_after_sync();
+            {
+                const float f = pow_decay(log2g, (float)(it * kW + r + 1));
+                const float w2 = r < Wc ? gp[2 * (Wc - 1 - r)] : 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t qs[16];
+                    tc::tmem_ld16(lrow + T3 + 32 * h + 16 * half, qs);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t off = tc::sw128_chunk(r, 4 * h + 2 * half + j);
+                        const uint4 pl = *reinterpret_cast<const uint4*>(sP + off);
+                        const uint32_t pw[4] = {pl.x, pl.y, pl.z, pl.w};
+                        float pv[8];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            pv[2 * u] = bf_lo(pw[u]) + f * __uint_as_float(qs[8 * j + 2 * u]);
+                            pv[2 * u + 1] = bf_hi(pw[u]) + f * __uint_as_float(qs[8 * j + 2 * u + 1]);
+                        }
+                        *reinterpret_cast<uint4*>(sP + off) = pack8(pv, 1.f);
+                        *reinterpret_cast<uint4*>(sPt + off) = pack8(pv, w2);
+                    }
+                }
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[BAT]);
+
+            // ---- EPI-b: B~ -> T3 ---------------------------------------------------------------
+            tc::mbar_wait(&bars[BB], ph, abort, status, 53);
+            tc::fence_after_sync();
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int cb = 64 * h + 32 * p;
+                const float first = r >= cb ? gp[2 * (r - cb)] : 0.f;
+                masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, ginv * ginv);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[BBT]);
+
+            // ---- EPI-c: out = g^(2(r+1)) Q Z0 + B~ V;  Z <- g^(2Wc) Z + dZ ------------------------
+            tc::mbar_wait(&bars[BC], ph, abort, status, 54);
+            tc::fence_after_sync();
+            {
+                const float s2 = gp[2 * (r + 1)];
+                bf16* out = static_cast<bf16*>(a.out) + ((size_t)bh * a.n + (size_t)c * kW + r) * kD + 32 * h;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t qz[16], bv[16];
+                    tc::tmem_ld16(lrow + T2 + 32 * h + 16 * half, qz);
+                    tc::tmem_ld16(lrow + T0 + 32 * h + 16 * half, bv);
+                    tc::tmem_wait_ld();
+                    if (r < Wc) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            float o[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                o[u] = s2 * __uint_as_float(qz[8 * j + u]) + __uint_as_float(bv[8 * j + u]);
+                            *reinterpret_cast<uint4*>(out + 16 * half + 8 * j) = pack8(o, 1.f);
+                        }
+                    }
+                }
+                uint32_t dz[16];
+                tc::tmem_ld16(lrow + T1 + zc, dz);
+                tc::tmem_wait_ld();
+                const float rho2 = gp[2 * Wc];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) zz[j] = rho2 * zz[j] + __uint_as_float(dz[j]);
+                publish_z();  // read by MMA-b of the next chunk, after its EPI-a arrives
+            }
+            tc::fence_proxy_async();
         }
     }
 
@@ -494,6 +785,16 @@ size_t fwd_chunk_tc_smem() { return kSmemBytes; }
 
 int launch_fwd_chunk_tc(const ChunkArgs& a, int mode, int* status, cudaStream_t st) {
     if (a.nseg_launch <= 0 || a.BH <= 0) return 0;
+    if (mode == kOutputP) {
+        outp::Maps pm;
+        if (!make_map(&pm.q, a.q, a.BH, a.n) || !make_map(&pm.p, a.out, a.BH, a.n) || !make_map(&pm.v, a.v, a.BH, a.n))
+            return -2;
+        cudaError_t e = cudaFuncSetAttribute(fwd_out_p_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             outp::kSmemBytes);
+        if (e != cudaSuccess) return -1;
+        fwd_out_p_tc_kernel<<<dim3(a.nseg_launch, a.BH), kThreads, outp::kSmemBytes, st>>>(pm, a, status);
+        return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+    }
     TcMaps maps;
     if (!make_map(&maps.q, a.q, a.BH, a.n) || !make_map(&maps.k, a.k, a.BH, a.n) || !make_map(&maps.v, a.v, a.BH, a.n))
         return -2;
