@@ -397,9 +397,8 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         ChunkArgs b = a;
         b.seg0 = seg0;
         b.nseg_launch = count;
-        b.store_p = stored_p ? 1 : 0;
         if (path == Path::kTc)
-            return launch_fwd_chunk_tc(b, summary ? kSummary : (stored_p ? kOutputP : kOutput),
+            return launch_fwd_chunk_tc(b, summary ? (stored_p ? kSummaryP : kSummary) : (stored_p ? kOutputP : kOutput),
                                        reinterpret_cast<int*>(a.ws), st);
         if (path == Path::kMma) return launch_fwd_chunk_mma(b, d, dv, chunk, summary ? kSummary : kOutput, cm, st);
         return launch_fwd_chunk_simt(b, d, dv, chunk, summary, cm, bf, st);

@@ -362,28 +362,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[BPS]);
-            if (SUMMARY && !UM && a.store_p) {
-                // segment-local p for the kOutputP pass, off the chain: while the state product
-                // runs, P is formed again from Q S0 (T0) and A~ K (T2), which stay in place until
-                // the next chunk's MMA1 and MMA2
-                const float s1 = gp[r + 1];
-                bf16* po = static_cast<bf16*>(a.out) + ((size_t)bh * a.n + (size_t)c * kW + r) * kD + 32 * h;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t qs[16], ak[16];
-                    tc::tmem_ld16(lrow + T0 + 32 * h + 16 * half, qs);
-                    tc::tmem_ld16(lrow + T2 + 32 * h + 16 * half, ak);
-                    tc::tmem_wait_ld();
-                    float pv[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) pv[j] = s1 * __uint_as_float(qs[j]) + __uint_as_float(ak[j]);
-                    if (r < Wc) {
-                        reinterpret_cast<uint4*>(po + 16 * half)[0] = pack8(&pv[0], 1.f);
-                        reinterpret_cast<uint4*>(po + 16 * half)[1] = pack8(&pv[8], 1.f);
-                    }
-                }
-            }
-
             if (!SUMMARY) {
                 // ---- EPI3: B~ -> T3 ----------------------------------------------------------
                 tc::mbar_wait(&bars[BB], ph, abort, status, 15);
@@ -749,6 +727,292 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Summary pass that also stores the segment-local p (masked, unnormalised; kSummaryP).
+//
+// Same sums as the summary mode above (S, C, Z of the segment from zero), and it writes
+// p^sl_t = S^sl_t q_t (bf16) into the output buffer for the kOutputP pass.  Two changes take
+// work off the chunk-to-chunk chain:
+//   * the key-moment increment is formed as K^T D K = K^_T K^ with K^ = diag(g^((Wc-1-i)/2)) K,
+//     so the raw K slot is free once A~ K has run and the next chunk's Q, K load early;
+//   * the state products land in T2 | T3, so the next chunk's Q K^T (T0T1) is issued while this
+//     chunk's state update still reads them.
+// Per chunk (local row r):
+//   MMA1  A = Q K^T -> T0T1              (issued during the previous chunk's EPI4)
+//   EPI1  A~ = A * [i <= r] g^(r-i) -> T3;  then Q~ = diag(g^(Wc-1-r)) Q, K^ (smem)
+//   MMA2  A~ K -> T2;  Q S0 -> T0
+//   EPI2  P = g^(r+1) Q S0 + A~ K;  P~ = diag(g^(2(Wc-1-r))) P (smem);  then P -> out
+//   ST    [Q~^T ; P~^T] V -> T2 (dC, dZ);  [K^^T ; K^^T] K^ -> T3 (dS twice)
+//   EPI4  S <- g^Wc S + dS,  C <- g^Wc C + dC,  Z <- g^(2Wc) Z + dZ;  bf16 S0 (smem)
+namespace sump {
+
+constexpr uint32_t oQ = 0, oK = kTile, oV = 2 * kTile, oQt = 3 * kTile, oKh = 4 * kTile, oPt = 5 * kTile;
+constexpr uint32_t oS0 = 6 * kTile;   // S0, [64][64] bf16 (8 KB)
+constexpr uint32_t oGP = oS0 + 8192;  // decay table g^0 .. g^(2W)
+constexpr uint32_t oBar = oGP + 1088;
+constexpr uint32_t oMisc = oBar + 16 * 8;
+constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
+constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192;
+
+enum Bar { FQK = 0, FV, BA, BAT, BP, BPS, BST, kBarCount };
+
+struct Maps {
+    CUtensorMap q, k, v, p;  // p: the output buffer, where P is stored
+};
+
+}  // namespace sump
+
+__global__ void __launch_bounds__(kThreads, 2)
+    fwd_sum_p_tc_kernel(const __grid_constant__ sump::Maps maps, const ChunkArgs a, int* status) {
+    // this pass's layout (shadows the first kernel's)
+    constexpr uint32_t oQ = sump::oQ, oK = sump::oK, oV = sump::oV, oQt = sump::oQt, oKh = sump::oKh,
+                       oPt = sump::oPt, oS0 = sump::oS0;
+    constexpr uint32_t oGP = sump::oGP, oBar = sump::oBar, oMisc = sump::oMisc;
+    constexpr uint32_t T0 = sump::T0, T2 = sump::T2, T3 = sump::T3;
+    constexpr int FQK = sump::FQK, FV = sump::FV, BA = sump::BA, BAT = sump::BAT, BP = sump::BP, BPS = sump::BPS,
+                  BST = sump::BST, kBarCount = sump::kBarCount;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* gp = reinterpret_cast<float*>(sm + oGP);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + oMisc);
+    volatile int* abort = reinterpret_cast<volatile int*>(sm + oMisc + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seg = a.seg0 + blockIdx.x, bh = blockIdx.y;
+    const int c_begin = seg * a.seg_chunks;
+    const int c_end = min(c_begin + a.seg_chunks, a.nchunks);
+    const float g = head_decay(a.gamma, bh, a.H);
+    const float log2g = log2f(g);
+    const int nit = c_end - c_begin;
+
+    for (int i = tid; i < 2 * kW + 1; i += kThreads) gp[i] = pow_decay(log2g, (float)i);
+    if (tid == 0) {
+        for (int b = 0; b < kBarCount; ++b) tc::mbar_init(&bars[b], (b == BAT || b == BPS) ? 8 : 1);
+        *abort = 0;
+        tc::mbar_fence_init();
+    }
+    if (warp == 0) tc::tmem_alloc(tmem_holder, kTmemCols);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ control thread
+        if (lane == 0 && nit > 0) {
+            const uint32_t sQ = smem_u32(sm + oQ), sK = smem_u32(sm + oK), sV = smem_u32(sm + oV);
+            const uint32_t sQt = smem_u32(sm + oQt), sKh = smem_u32(sm + oKh), sS0 = smem_u32(sm + oS0);
+            auto load_qk = [&](int c) {
+                tc::mbar_arrive_expect_tx(&bars[FQK], 2 * kTile);
+                tc::tma_load_3d(sm + oQ, &maps.q, 0, c * kW, bh, &bars[FQK]);
+                tc::tma_load_3d(sm + oK, &maps.k, 0, c * kW, bh, &bars[FQK]);
+            };
+            // the next chunk's K at once, its Q once the P tile (staged in the Q slot) is read
+            auto load_k_first = [&](int c) {
+                tc::mbar_arrive_expect_tx(&bars[FQK], 2 * kTile);
+                tc::tma_load_3d(sm + oK, &maps.k, 0, c * kW, bh, &bars[FQK]);
+            };
+            auto load_q_second = [&](int c) { tc::tma_load_3d(sm + oQ, &maps.q, 0, c * kW, bh, &bars[FQK]); };
+            auto load_v = [&](int c) {
+                tc::mbar_arrive_expect_tx(&bars[FV], kTile);
+                tc::tma_load_3d(sm + oV, &maps.v, 0, c * kW, bh, &bars[FV]);
+            };
+            constexpr uint32_t I_AB = tc::idesc_bf16(128, 128, 0, 0);   // K-major x K-major, N = 128
+            constexpr uint32_t I_QX = tc::idesc_bf16(128, 64, 0, 1);    // K-major x MN-major, N = 64
+            constexpr uint32_t I_TS64 = tc::idesc_bf16(128, 64, 0, 1);  // A (TMEM) x MN-major B, N = 64
+            constexpr uint32_t I_ST64 = tc::idesc_bf16(128, 64, 1, 1);  // MN-major x MN-major, N = 64
+            auto mma1 = [&]() {  // A = Q K^T -> T0T1
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sK + 32 * ks, 16, 1024),
+                               I_AB, ks > 0);
+                tc::mma_commit(&bars[BA]);
+            };
+            load_qk(c_begin);
+            load_v(c_begin);
+            int lqk = 1, lv = 1;
+            tc::mbar_wait(&bars[FQK], 0, abort, status, 61);
+            tc::fence_after_sync();
+            mma1();
+            for (int it = 0; it < nit; ++it) {
+                const uint32_t ph = it & 1;
+                if (it + 1 < nit) {  // next chunk's tiles into L2, so that their loads below are short
+                    const int cn = (c_begin + it + 1) * kW;
+                    tc::tma_prefetch_3d(&maps.q, 0, cn, bh);
+                    tc::tma_prefetch_3d(&maps.k, 0, cn, bh);
+                    tc::tma_prefetch_3d(&maps.v, 0, cn, bh);
+                }
+                tc::mbar_wait(&bars[BAT], ph, abort, status, 62);  // A~, and the previous chunk's S0
+                tc::fence_after_sync();
+                // MMA2: A~ K -> T2;  Q S0 -> T0
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ts(tmem + T2, tmem + T3 + 8 * ks, tc::smem_desc(sK + 2048 * ks, 16, 1024), I_TS64, ks > 0);
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sS0 + 2048 * ks, 16, 1024),
+                               I_QX, ks > 0);
+                tc::mma_commit(&bars[BP]);
+                tc::mbar_wait(&bars[BPS], ph, abort, status, 64);  // P (Q slot), P~, Q~, K^ written; T0, T2 read
+                // P -> out (one tile store); raw K is free (MMA2 and EPI1's scaled copy are done)
+                tc::tma_store_3d(&maps.p, sm + oQ, 0, (c_begin + it) * kW, bh);
+                tc::bulk_commit();
+                if (it + 1 < nit) {
+                    load_k_first(c_begin + it + 1);
+                    ++lqk;
+                }
+                tc::mbar_wait(&bars[FV], ph, abort, status, 65);
+                tc::fence_after_sync();
+                // ST: [Q~^T ; P~^T] V -> T2;  [K^^T ; K^^T] K^ -> T3
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem + T2, tc::smem_desc(sQt + 2048 * ks, oPt - oQt, 1024),
+                               tc::smem_desc(sV + 2048 * ks, 16, 1024), I_ST64, ks > 0);
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem + T3, tc::smem_desc(sKh + 2048 * ks, 0, 1024),
+                               tc::smem_desc(sKh + 2048 * ks, 16, 1024), I_ST64, ks > 0);
+                tc::mma_commit(&bars[BST]);
+                tc::bulk_wait_read_all();  // the P tile has left the Q slot
+                if (it + 1 < nit) {
+                    load_q_second(c_begin + it + 1);
+                    // next chunk's Q K^T while this chunk's state update runs
+                    tc::mbar_wait(&bars[FQK], ph ^ 1, abort, status, 66);
+                    tc::fence_after_sync();
+                    mma1();
+                }
+                tc::mbar_wait(&bars[BST], ph, abort, status, 67);  // V, Q~, K^ free
+                if (it + 1 < nit) {
+                    load_v(c_begin + it + 1);
+                    ++lv;
+                }
+            }
+            volatile int never = 0;
+            tc::mbar_wait(&bars[BST], (nit - 1) & 1, &never, nullptr, 0);
+            tc::mbar_wait(&bars[FQK], (lqk - 1) & 1, &never, nullptr, 0);
+            tc::mbar_wait(&bars[FV], (lv - 1) & 1, &never, nullptr, 0);
+            tc::bulk_wait_all();
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int q4 = warp & 3, h = (warp - 1) >> 2;
+        const int r = 32 * q4 + lane;
+        const int row0 = 32 * q4;
+        const uint32_t lrow = tmem + ((uint32_t)row0 << 16);
+        unsigned char* sQ = sm + oQ;  // raw Q, then this chunk's P tile (after MMA2)
+        unsigned char* sK = sm + oK;
+        unsigned char* sQt = sm + oQt;
+        unsigned char* sKh = sm + oKh;
+        unsigned char* sPt = sm + oPt;
+        const float ginv = g > 0.f ? 1.f / g : 0.f;
+        // fp32 sums: C row r (r < 64) or Z row r - 64, columns 32h ..; S row r % 64, columns sc ..
+        const int sc = 32 * h + 16 * (r >> 6);
+        float st[32], ss[16];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) st[j] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ss[j] = 0.f;
+        auto publish_s = [&]() {
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                *reinterpret_cast<uint4*>(sm + oS0 + tc::sw128_chunk(r & 63, sc / 8 + j)) = pack8(&ss[8 * j], 1.f);
+        };
+        publish_s();
+        tc::fence_proxy_async();
+
+        for (int it = 0; it < nit; ++it) {
+            const uint32_t ph = it & 1;
+            const int c = c_begin + it;
+            const int Wc = min(kW, a.n - c * kW);
+            // ---- EPI1: A~ -> T3;  Q~, K^ -> smem ----------------------------------------------
+            tc::mbar_wait(&bars[FQK], ph, abort, status, 71);
+            tc::mbar_wait(&bars[BA], ph, abort, status, 72);
+            tc::fence_after_sync();
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int cb = 64 * h + 32 * p;
+                const float first = r >= cb ? gp[r - cb] : 0.f;
+                masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, ginv);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[BAT]);
+            {  // first read by ST, after EPI2's fence
+                const float w1 = r < Wc ? gp[Wc - 1 - r] : 0.f;
+                const float wh = r < Wc ? pow_decay(log2g, 0.5f * (float)(Wc - 1 - r)) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t off = tc::sw128_chunk(r, 4 * h + j);
+                    *reinterpret_cast<uint4*>(sQt + off) = scale_chunk(*reinterpret_cast<const uint4*>(sQ + off), w1);
+                    *reinterpret_cast<uint4*>(sKh + off) = scale_chunk(*reinterpret_cast<const uint4*>(sK + off), wh);
+                }
+            }
+            // ---- EPI2: P = g^(r+1) Q S0 + A~ K;  P~ -> smem, P -> out ---------------------------
+            tc::mbar_wait(&bars[BP], ph, abort, status, 73);
+            tc::fence_after_sync();
+            {
+                const float s1 = gp[r + 1];
+                const float w2 = r < Wc ? gp[2 * (Wc - 1 - r)] : 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t qs[16], ak[16];
+                    tc::tmem_ld16(lrow + T0 + 32 * h + 16 * half, qs);
+                    tc::tmem_ld16(lrow + T2 + 32 * h + 16 * half, ak);
+                    tc::tmem_wait_ld();
+                    float pv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pv[j] = s1 * __uint_as_float(qs[j]) + __uint_as_float(ak[j]);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t off = tc::sw128_chunk(r, 4 * h + 2 * half + j);
+                        *reinterpret_cast<uint4*>(sPt + off) = pack8(&pv[8 * j], w2);
+                        *reinterpret_cast<uint4*>(sQ + off) = pack8(&pv[8 * j], 1.f);  // rows >= Wc: not stored
+                    }
+                }
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[BPS]);
+            // ---- EPI4: state update --------------------------------------------------------------
+            tc::mbar_wait(&bars[BST], ph, abort, status, 74);
+            tc::fence_after_sync();
+            {
+                const float rho = gp[Wc], rho2 = gp[2 * Wc];
+                uint32_t v[32], w[16];
+                tc::tmem_ld32(lrow + T2 + 32 * h, v);
+                tc::tmem_ld16(lrow + T3 + sc, w);
+                tc::tmem_wait_ld();
+                const float decay = r < 64 ? rho : rho2;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) st[j] = decay * st[j] + __uint_as_float(v[j]);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) ss[j] = rho * ss[j] + __uint_as_float(w[j]);
+                publish_s();  // read by the next chunk's MMA2, after its EPI1 arrives
+            }
+            tc::fence_proxy_async();
+        }
+
+        if (seg < a.nsum) {  // (the launch also covers the last segment, for its p)
+            const size_t si = (size_t)bh * a.nsum + seg;
+            float* dst = r < 64 ? a.ws + a.L.CB + si * kD * kD + (size_t)r * kD
+                                : a.ws + a.L.ZB + si * kD * kD + (size_t)(r - 64) * kD;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[32 * h + j] = st[j];
+            float* ds = a.ws + a.L.SB + si * kD * kD + (size_t)(r & 63) * kD + sc;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ds[j] = ss[j];
+            if (h == 0 && r < 64) {
+                a.ws[a.L.mB + si * kD + r] = 0.f;
+                a.ws[a.L.yB + si * kD + r] = 0.f;
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -798,6 +1062,18 @@ int launch_fwd_chunk_tc(const ChunkArgs& a, int mode, int* status, cudaStream_t 
     TcMaps maps;
     if (!make_map(&maps.q, a.q, a.BH, a.n) || !make_map(&maps.k, a.k, a.BH, a.n) || !make_map(&maps.v, a.v, a.BH, a.n))
         return -2;
+    if (mode == kSummaryP) {
+        sump::Maps sm4;
+        sm4.q = maps.q;
+        sm4.k = maps.k;
+        sm4.v = maps.v;
+        if (!make_map(&sm4.p, a.out, a.BH, a.n)) return -2;
+        cudaError_t e = cudaFuncSetAttribute(fwd_sum_p_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             sump::kSmemBytes);
+        if (e != cudaSuccess) return -1;
+        fwd_sum_p_tc_kernel<<<dim3(a.nseg_launch, a.BH), kThreads, sump::kSmemBytes, st>>>(sm4, a, status);
+        return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+    }
     dim3 grid(a.nseg_launch, a.BH);
     auto kfn = mode == kSummary ? (a.unmasked ? fwd_chunk_tc_kernel<kSummary, true> : fwd_chunk_tc_kernel<kSummary, false>)
                                 : (a.unmasked ? fwd_chunk_tc_kernel<kOutput, true> : fwd_chunk_tc_kernel<kOutput, false>);

@@ -88,15 +88,13 @@ struct ChunkArgs {
     // summaries, the carries and the raw final state then hold C and m, which decay by
     // g per token, and no cross term enters the inter-segment scan.
     int unmasked;
-    // Summary pass of the tcgen05 kernel: also store the segment-local p_t = S_t q_t (bf16,
-    // the key moment accumulated from zero at the segment start) into out, for kOutputP.
-    int store_p;
 };
 
 // Chunk-kernel passes.
-// kOutputP (tcgen05 kernel only): the output pass that starts from the segment-local
-// p_t = S_t q_t which the summary pass stored in `out` (ChunkArgs::store_p).
-enum ChunkMode { kSummary = 0, kOutput = 1, kStates = 2, kOutStates = 3, kOutputP = 4 };
+// tcgen05 kernel only: kSummaryP is the summary pass that also stores the segment-local
+// p_t = S_t q_t (bf16, key moment accumulated from zero at the segment start) in `out`, over
+// every segment; kOutputP is the output pass that starts from it.
+enum ChunkMode { kSummary = 0, kOutput = 1, kStates = 2, kOutStates = 3, kOutputP = 4, kSummaryP = 5 };
 
 // Arguments of the reverse-mode chunk kernel (bf16, d == dv).
 struct BwdArgs {
