@@ -472,14 +472,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 //   MMA-b  B = Q P^T -> T0T1;  Q Z0 -> T2
 //   EPI-b  B~ = B * [j <= r] g^(2(r-j))  (bf16)  -> T3
 //   MMA-c  B~ V -> T0;  [P~^T ; P~^T] V -> T1 (dZ, rows 0..63 and again 64..127)
-//   EPI-c  out = g^(2(r+1)) Q Z0 + B~ V  (bf16, over this chunk's p^sl, already consumed);
-//          Z <- g^(2Wc) Z + dZ  (fp32, 16 columns a thread);  bf16 Z0 (smem)
+//   EPI-c  out = g^(2(r+1)) Q Z0 + B~ V  (bf16 tile in smem; one TMA tile store writes it over
+//          this chunk's p^sl, already consumed);  Z <- g^(2Wc) Z + dZ  (fp32, 16 columns a
+//          thread);  bf16 Z0 (smem)
 // MMA-a of the next chunk and the next loads overlap EPI-c.  Same roles, bounded waits and
 // two CTAs per SM as the kernel above.
 namespace outp {
 
 constexpr uint32_t oQ = 0, oP = kTile, oV = 2 * kTile, oPt = 3 * kTile;
-constexpr uint32_t oS = 4 * kTile;        // S_in, [64][64] bf16 (8 KB), B operand of Q S_in
+constexpr uint32_t oO = 4 * kTile;        // output tile, written by one TMA tile store
+constexpr uint32_t oS = 5 * kTile;        // S_in, [64][64] bf16 (8 KB), B operand of Q S_in
 constexpr uint32_t oZ0 = oS + 8192;       // Z0, [64][64] bf16 (8 KB), B operand of Q Z0
 constexpr uint32_t oGP = oZ0 + 8192;      // decay table g^0 .. g^(2W)
 constexpr uint32_t oBar = oGP + 1088;
@@ -487,7 +489,7 @@ constexpr uint32_t oMisc = oBar + 16 * 8;
 constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
 constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192;
 
-enum Bar { FQP = 0, FV, BA, BAT, BB, BBT, BC, kBarCount };
+enum Bar { FQP = 0, FV, BA, BAT, BB, BBT, BC, BOS, kBarCount };
 
 struct Maps {
     CUtensorMap q, p, v;
@@ -498,11 +500,12 @@ struct Maps {
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_out_p_tc_kernel(const __grid_constant__ outp::Maps maps, const ChunkArgs a, int* status) {
     // this pass's layout (shadows the kernel above)
-    constexpr uint32_t oQ = outp::oQ, oP = outp::oP, oV = outp::oV, oPt = outp::oPt, oS = outp::oS, oZ0 = outp::oZ0;
+    constexpr uint32_t oQ = outp::oQ, oP = outp::oP, oV = outp::oV, oPt = outp::oPt, oO = outp::oO, oS = outp::oS,
+                       oZ0 = outp::oZ0;
     constexpr uint32_t oGP = outp::oGP, oBar = outp::oBar, oMisc = outp::oMisc;
     constexpr uint32_t T0 = outp::T0, T1 = outp::T1, T2 = outp::T2, T3 = outp::T3;
     constexpr int FQP = outp::FQP, FV = outp::FV, BA = outp::BA, BAT = outp::BAT, BB = outp::BB, BBT = outp::BBT,
-                  BC = outp::BC, kBarCount = outp::kBarCount;
+                  BC = outp::BC, BOS = outp::BOS, kBarCount = outp::kBarCount;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* gp = reinterpret_cast<float*>(sm + oGP);
@@ -531,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     for (int i = tid; i < 2 * kW + 1; i += kThreads) gp[i] = pow_decay(log2g, (float)i);
     if (tid == 0) {
-        for (int b = 0; b < kBarCount; ++b) tc::mbar_init(&bars[b], (b == BAT || b == BBT) ? 8 : 1);
+        for (int b = 0; b < kBarCount; ++b) tc::mbar_init(&bars[b], (b == BAT || b == BBT || b == BOS) ? 8 : 1);
         *abort = 0;
         tc::mbar_fence_init();
     }
@@ -592,6 +595,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc::mma_commit(&bars[BA]);
                 tc::mbar_wait(&bars[BAT], ph, abort, status, 42);  // P, P~ written; previous EPI-c done
                 tc::fence_after_sync();
+                if (it > 0) {  // the previous chunk's output tile (staged by its EPI-c) -> out
+                    tc::mbar_wait(&bars[BOS], ph ^ 1, abort, status, 47);
+                    tc::tma_store_3d(&maps.p, sm + oO, 0, (c_begin + it - 1) * kW, bh);
+                    tc::bulk_commit();
+                }
                 // MMA-b: B = Q P^T -> T0T1;  Q Z0 -> T2
                 for (int ks = 0; ks < 4; ++ks)
                     tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sP + 32 * ks, 16, 1024),
@@ -607,6 +615,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc::mbar_wait(&bars[BBT], ph, abort, status, 44);
                 tc::mbar_wait(&bars[FV], ph, abort, status, 45);
+                tc::bulk_wait_read_all();  // the output tile slot is free before this chunk's EPI-c
                 tc::fence_after_sync();
                 // MMA-c: B~ V -> T0;  [P~^T ; P~^T] V -> T1
                 for (int ks = 0; ks < 8; ++ks)
@@ -621,11 +630,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                     ++lv;
                 }
             }
+            tc::mbar_wait(&bars[BOS], (nit - 1) & 1, abort, status, 48);  // the last output tile
+            tc::tma_store_3d(&maps.p, sm + oO, 0, (c_begin + nit - 1) * kW, bh);
+            tc::bulk_commit();
             // drain (bounded, ignoring the abort flag) so that nothing is in flight at exit
             volatile int never = 0;
             tc::mbar_wait(&bars[BC], (nit - 1) & 1, &never, nullptr, 0);
             tc::mbar_wait(&bars[FQP], (lqp - 1) & 1, &never, nullptr, 0);
             tc::mbar_wait(&bars[FV], (lv - 1) & 1, &never, nullptr, 0);
+            tc::bulk_wait_all();
         }
         __syncwarp();
     } else {
@@ -691,22 +704,19 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc::fence_after_sync();
             {
                 const float s2 = gp[2 * (r + 1)];
-                bf16* out = static_cast<bf16*>(a.out) + ((size_t)bh * a.n + (size_t)c * kW + r) * kD + 32 * h;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t qz[16], bv[16];
                     tc::tmem_ld16(lrow + T2 + 32 * h + 16 * half, qz);
                     tc::tmem_ld16(lrow + T0 + 32 * h + 16 * half, bv);
                     tc::tmem_wait_ld();
-                    if (r < Wc) {
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            float o[8];
+                    for (int j = 0; j < 2; ++j) {  // output tile (rows >= Wc fall outside the tensor)
+                        float o[8];
 #pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                o[u] = s2 * __uint_as_float(qz[8 * j + u]) + __uint_as_float(bv[8 * j + u]);
-                            *reinterpret_cast<uint4*>(out + 16 * half + 8 * j) = pack8(o, 1.f);
-                        }
+                        for (int u = 0; u < 8; ++u)
+                            o[u] = s2 * __uint_as_float(qz[8 * j + u]) + __uint_as_float(bv[8 * j + u]);
+                        *reinterpret_cast<uint4*>(sm + oO + tc::sw128_chunk(r, 4 * h + 2 * half + j)) = pack8(o, 1.f);
                     }
                 }
                 uint32_t dz[16];
@@ -718,6 +728,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 publish_z();  // read by MMA-b of the next chunk, after its EPI-a arrives
             }
             tc::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[BOS]);
         }
     }
 
