@@ -138,6 +138,33 @@ __device__ __forceinline__ float head_decay(const float* gamma, int bh, int H) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start while the
+// kernel before it on the stream is still running (once every CTA of that kernel has run
+// pdl_trigger or exited); it must run pdl_wait before it reads or writes memory that an
+// earlier kernel of the stream touches.  pdl_wait returns once the kernels before it have
+// completed and their writes are visible; without the launch attribute it returns at once.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // cp.async (16-byte global -> shared copies)
 // ---------------------------------------------------------------------------
 

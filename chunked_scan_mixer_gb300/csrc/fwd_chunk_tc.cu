@@ -499,6 +499,7 @@ struct Maps {
 
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_out_p_tc_kernel(const __grid_constant__ outp::Maps maps, const ChunkArgs a, int* status) {
+    pdl_trigger();
     // this pass's layout (shadows the kernel above)
     constexpr uint32_t oQ = outp::oQ, oP = outp::oP, oV = outp::oV, oPt = outp::oPt, oO = outp::oO, oS = outp::oS,
                        oZ0 = outp::oZ0;
@@ -538,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         *abort = 0;
         tc::mbar_fence_init();
     }
+    pdl_wait();  // everything below reads what the earlier kernels of the forward wrote
     if (warp == 0) {
         tc::tmem_alloc(tmem_holder, kTmemCols);
     } else {
@@ -776,6 +778,7 @@ struct Maps {
 
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_sum_p_tc_kernel(const __grid_constant__ sump::Maps maps, const ChunkArgs a, int* status) {
+    pdl_trigger();
     // this pass's layout (shadows the first kernel's)
     constexpr uint32_t oQ = sump::oQ, oK = sump::oK, oV = sump::oV, oQt = sump::oQt, oKh = sump::oKh,
                        oPt = sump::oPt, oS0 = sump::oS0;
@@ -808,6 +811,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    pdl_wait();  // the status word and the workspace are written by the kernel before
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
@@ -1068,7 +1072,9 @@ int launch_fwd_chunk_tc(const ChunkArgs& a, int mode, int* status, cudaStream_t 
         cudaError_t e = cudaFuncSetAttribute(fwd_out_p_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              outp::kSmemBytes);
         if (e != cudaSuccess) return -1;
-        fwd_out_p_tc_kernel<<<dim3(a.nseg_launch, a.BH), kThreads, outp::kSmemBytes, st>>>(pm, a, status);
+        if (launch_pdl(fwd_out_p_tc_kernel, dim3(a.nseg_launch, a.BH), dim3(kThreads), outp::kSmemBytes, st, pm, a,
+                       status) != cudaSuccess)
+            return -1;
         return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
     }
     TcMaps maps;
@@ -1083,7 +1089,9 @@ int launch_fwd_chunk_tc(const ChunkArgs& a, int mode, int* status, cudaStream_t 
         cudaError_t e = cudaFuncSetAttribute(fwd_sum_p_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              sump::kSmemBytes);
         if (e != cudaSuccess) return -1;
-        fwd_sum_p_tc_kernel<<<dim3(a.nseg_launch, a.BH), kThreads, sump::kSmemBytes, st>>>(sm4, a, status);
+        if (launch_pdl(fwd_sum_p_tc_kernel, dim3(a.nseg_launch, a.BH), dim3(kThreads), sump::kSmemBytes, st, sm4, a,
+                       status) != cudaSuccess)
+            return -1;
         return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
     }
     dim3 grid(a.nseg_launch, a.BH);

@@ -26,6 +26,7 @@ constexpr int kThreads = 256;
 // output carries C0 and m0 in those slots and ignores G0 and h0.
 __global__ void __launch_bounds__(kThreads)
     init_carry_kernel(const ChunkArgs a, int D, int DV, const float* init) {
+    pdl_trigger();  // the summary pass may start its prologue (it waits before touching memory)
     const int bh = blockIdx.x, tid = threadIdx.x;
     if (bh == 0 && tid == 0) *reinterpret_cast<int*>(a.ws) = 0;  // clear the status word
     const size_t s0 = (size_t)bh * a.nseg;  // segment 0 of this head
@@ -72,6 +73,8 @@ __global__ void __launch_bounds__(kThreads)
     linear_scan_kernel(const float* __restrict__ src, float* __restrict__ dst, int BH, int H,
                        int nsteps, size_t E, size_t src_hs, size_t dst_hs, int store_all,
                        const float* gamma, int step_tokens, int power) {
+    pdl_trigger();
+    pdl_wait();
     const size_t gid = (size_t)blockIdx.x * kThreads + threadIdx.x;
     if (gid >= (size_t)BH * E) return;
     const int bh = (int)(gid / E);
@@ -129,6 +132,8 @@ __global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int 
     float* Ss = sm;            // D x D
     float* Cs = Ss + D * D;    // D x DV
     float* ms = Cs + D * DV;   // D
+    pdl_trigger();
+    pdl_wait();
     const int s = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     const size_t sb = (size_t)bh * a.nsum + s;        // summary index
     const size_t si = (size_t)bh * a.nseg + s;        // carry index
@@ -231,8 +236,9 @@ int launch_linear_scan(const float* src, float* dst, int BH, int H, int nsteps, 
     const size_t total = (size_t)BH * E;
     if (total == 0 || nsteps <= 0) return 0;
     const unsigned blocks = (unsigned)((total + kThreads - 1) / kThreads);
-    linear_scan_kernel<<<blocks, kThreads, 0, st>>>(src, dst, BH, H, nsteps, E, src_hs, dst_hs,
-                                                    store_all ? 1 : 0, gamma, step_tokens, power);
+    if (launch_pdl(linear_scan_kernel, dim3(blocks), dim3(kThreads), 0, st, src, dst, BH, H, nsteps, E, src_hs,
+                   dst_hs, store_all ? 1 : 0, gamma, step_tokens, power) != cudaSuccess)
+        return -1;
     return finish_launch();
 }
 
@@ -243,7 +249,9 @@ int launch_cross_t(const ChunkArgs& a, cudaStream_t st) {
     if (cudaFuncSetAttribute(cross_kernel<TM, TN, WITH_Y>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return -1;
-    cross_kernel<TM, TN, WITH_Y><<<dim3(a.nseg - 1, a.BH), kThreads, smem, st>>>(a, a.seg_chunks * a.W);
+    if (launch_pdl(cross_kernel<TM, TN, WITH_Y>, dim3(a.nseg - 1, a.BH), dim3(kThreads), smem, st, a,
+                   a.seg_chunks * a.W) != cudaSuccess)
+        return -1;
     return finish_launch();
 }
 
