@@ -610,6 +610,14 @@ def run_ours(args, dist: Dist):
     io_mb = tokens * (2 * w.d + 2 * w.dv) * 2 / 1e6
     summary_tokens = w.B * w.H * min(w.n, (nseg - 1) * seg_chunks * w.chunk)
     summ_bytes = summary_tokens * (2 * w.d + w.dv) * 2
+    # The masked bf16 forward at d = dv = 64, chunk 128 with more than one segment takes the
+    # stored-p path: its summary pass covers every token and also writes p = S q (d bf16 per
+    # token) into out, and its output pass reads q, p, v (no k) and writes out (same bytes).
+    stored_p = (w.d == 64 and w.dv == 64 and w.chunk == 128 and not w.normalize and nseg > 1
+                and os.environ.get("HLA2_KERNEL") != "mma")
+    if stored_p:
+        summary_tokens = tokens
+        summ_bytes = tokens * ((2 * w.d + w.dv) * 2 + w.d * 2)
     if ph["output_pass"] >= ph["segment_summaries"]:
         kname, kbytes, kms = "output_pass", out_bytes, ph["output_pass"]
     else:
