@@ -153,6 +153,12 @@ int cuda_fail(const char* what) {
 bool dim_ok(int x) { return x == 16 || x == 32 || x == 64 || x == 128; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// [a, a + na) and [b, b + nb) share a byte
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + nb && y < x + na;
+}
+
 struct DevInfo {
     int sms = 152;                  // GB300 when no device can be queried
     int smem_optin = 232448;        // 227 KB per block
@@ -349,6 +355,14 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     if (!q || !k || !v || !out) return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must not be NULL");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return fail(HLA2_ERR_INVALID_ARG, "q, k, v, out must be 16-byte aligned");
+    {
+        // out is written while q, k, v are still being read (and, on the stored-p path, holds
+        // the summary pass's p until the output pass replaces it)
+        const size_t es = opts->dtype == HLA2_BF16 ? 2 : 4;
+        const size_t rows = (size_t)BH * (size_t)n, nq = rows * d * es, nv = rows * dv * es;
+        if (overlaps(out, nv, q, nq) || overlaps(out, nv, k, nq) || overlaps(out, nv, v, nv))
+            return fail(HLA2_ERR_INVALID_ARG, "out must not overlap q, k or v");
+    }
     if (opts->flags & HLA2_FLAG_SAVE_FOR_BACKWARD)
         return forward_saving_for_backward(q, k, v, out, B, H, n, d, dv, gamma, normalize, chunk, st, opts);
 

@@ -30,8 +30,9 @@ def test_version_and_sizes(L):
 
 
 def _fwd(L, **kw):
-    args = dict(q=ctypes.c_void_p(16), k=ctypes.c_void_p(16), v=ctypes.c_void_p(16),
-                out=ctypes.c_void_p(16), B=1, H=1, n=16, d=16, dv=16, gamma=None, normalize=0,
+    # distinct (never dereferenced) addresses: every check below runs before any launch
+    args = dict(q=ctypes.c_void_p(0x10000), k=ctypes.c_void_p(0x20000), v=ctypes.c_void_p(0x30000),
+                out=ctypes.c_void_p(0x40000), B=1, H=1, n=16, d=16, dv=16, gamma=None, normalize=0,
                 chunk=16, stream=None, opts=Opts(1, 1e-6, None, 0, None, None))
     args.update(kw)
     o = args.pop("opts")
@@ -51,12 +52,21 @@ def _fwd(L, **kw):
     (dict(opts=Opts(7, 1e-6, None, 0, None, None)), -1),
     (dict(q=None), -1),
     (dict(k=ctypes.c_void_p(18)), -1),
+    (dict(out=ctypes.c_void_p(0x10000)), -1),         # out is q
+    (dict(out=ctypes.c_void_p(0x30000 + 256)), -1),   # out overlaps the end of v (16 x 16 bf16)
     (dict(), -3),  # no workspace
 ])
 def test_forward_rejects_bad_arguments(L, kw, code):
     rc, msg = _fwd(L, **kw)
     assert rc == code, msg
     assert msg
+
+
+def test_forward_adjacent_out_is_accepted(L):
+    # out right after v (16 x 16 bf16 = 512 bytes): no overlap, so the call gets as far as the
+    # workspace check
+    rc, msg = _fwd(L, out=ctypes.c_void_p(0x30000 + 512))
+    assert rc == -3, msg
 
 
 def test_forward_empty_is_ok(L):
