@@ -403,10 +403,10 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     a.unmasked = unmasked ? 1 : 0;
 
     const bool bf = opts->dtype == HLA2_BF16;
-    // Masked tcgen05 path with more than one segment: the summary pass also stores the
-    // segment-local p_t = S_t q_t in out, over every segment, and the output pass starts from it
-    // (kOutputP), so that only Z is carried from chunk to chunk there.
-    const bool stored_p = path == Path::kTc && !unmasked && p.nseg > 1;
+    // tcgen05 path with more than one segment: the summary pass also stores the segment-local
+    // p_t = S_t q_t in out, over every segment, and the output pass starts from it (kOutputP),
+    // so that only Z (unmasked: C) is carried from chunk to chunk there.
+    const bool stored_p = path == Path::kTc && p.nseg > 1;
     auto chunk_pass = [&](int seg0, int count, bool summary, bool cm) -> int {
         ChunkArgs b = a;
         b.seg0 = seg0;

@@ -497,6 +497,7 @@ struct Maps {
 
 }  // namespace outp
 
+template <bool UM>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_out_p_tc_kernel(const __grid_constant__ outp::Maps maps, const ChunkArgs a, int* status) {
     pdl_trigger();
@@ -602,15 +603,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tc::tma_store_3d(&maps.p, sm + oO, 0, (c_begin + it - 1) * kW, bh);
                     tc::bulk_commit();
                 }
-                // MMA-b: B = Q P^T -> T0T1;  Q Z0 -> T2
+                // MMA-b: B = Q P^T -> T0T1;  Q Z0 -> T2   (unmasked: P Q^T and P C0)
+                const uint32_t sL = UM ? sP : sQ, sR = UM ? sQ : sP;
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sP + 32 * ks, 16, 1024),
+                    tc::mma_ss(tmem + T0, tc::smem_desc(sL + 32 * ks, 16, 1024), tc::smem_desc(sR + 32 * ks, 16, 1024),
                                I_AB, ks > 0);
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_ss(tmem + T2, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sZ0 + 2048 * ks, 16, 1024),
+                    tc::mma_ss(tmem + T2, tc::smem_desc(sL + 32 * ks, 16, 1024), tc::smem_desc(sZ0 + 2048 * ks, 16, 1024),
                                I_QX, ks > 0);
                 tc::mma_commit(&bars[BB]);
-                tc::mbar_wait(&bars[BB], ph, abort, status, 43);  // Q and P no longer read
+                tc::mbar_wait(&bars[BB], ph, abort, status, 43);  // Q and P no longer read (Q~ was copied)
                 if (it + 1 < nit) {
                     load_qp(c_begin + it + 1);
                     ++lqp;
@@ -661,6 +663,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             {
                 const float f = pow_decay(log2g, (float)(it * kW + r + 1));
                 const float w2 = r < Wc ? gp[2 * (Wc - 1 - r)] : 0.f;
+                if (UM) {  // the state product forms dC = Q~^T V: Q~ = diag(g^(Wc-1-r)) Q in the P~ slot
+                    const float w1 = r < Wc ? gp[Wc - 1 - r] : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t off = tc::sw128_chunk(r, 4 * h + j);
+                        *reinterpret_cast<uint4*>(sPt + off) =
+                            scale_chunk(*reinterpret_cast<const uint4*>(sm + oQ + off), w1);
+                    }
+                }
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t qs[16];
@@ -678,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                             pv[2 * u + 1] = bf_hi(pw[u]) + f * __uint_as_float(qs[8 * j + 2 * u + 1]);
                         }
                         *reinterpret_cast<uint4*>(sP + off) = pack8(pv, 1.f);
-                        *reinterpret_cast<uint4*>(sPt + off) = pack8(pv, w2);
+                        if (!UM) *reinterpret_cast<uint4*>(sPt + off) = pack8(pv, w2);
                     }
                 }
             }
@@ -687,14 +698,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[BAT]);
 
-            // ---- EPI-b: B~ -> T3 ---------------------------------------------------------------
+            // ---- EPI-b: B~ -> T3 (unmasked: decay g^(r-j)) ------------------------------------------
             tc::mbar_wait(&bars[BB], ph, abort, status, 53);
             tc::fence_after_sync();
+            constexpr int BP2 = UM ? 1 : 2;  // decay power of the second product
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
                 const int cb = 64 * h + 32 * p;
-                const float first = r >= cb ? gp[2 * (r - cb)] : 0.f;
-                masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, ginv * ginv);
+                const float first = r >= cb ? gp[BP2 * (r - cb)] : 0.f;
+                masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, UM ? ginv : ginv * ginv);
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
@@ -705,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc::mbar_wait(&bars[BC], ph, abort, status, 54);
             tc::fence_after_sync();
             {
-                const float s2 = gp[2 * (r + 1)];
+                const float s2 = gp[BP2 * (r + 1)];
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t qz[16], bv[16];
@@ -724,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 uint32_t dz[16];
                 tc::tmem_ld16(lrow + T1 + zc, dz);
                 tc::tmem_wait_ld();
-                const float rho2 = gp[2 * Wc];
+                const float rho2 = gp[BP2 * Wc];  // (unmasked: C decays by g per token)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) zz[j] = rho2 * zz[j] + __uint_as_float(dz[j]);
                 publish_z();  // read by MMA-b of the next chunk, after its EPI-a arrives
@@ -776,6 +788,7 @@ struct Maps {
 
 }  // namespace sump
 
+template <bool UM>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_sum_p_tc_kernel(const __grid_constant__ sump::Maps maps, const ChunkArgs a, int* status) {
     pdl_trigger();
@@ -877,9 +890,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc::mbar_wait(&bars[FV], ph, abort, status, 65);
                 tc::fence_after_sync();
-                // ST: [Q~^T ; P~^T] V -> T2;  [K^^T ; K^^T] K^ -> T3
+                // ST: [Q~^T ; P~^T] V -> T2 (unmasked: [Q~^T ; Q~^T] V, dC twice);  [K^^T ; K^^T] K^ -> T3
                 for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_ss(tmem + T2, tc::smem_desc(sQt + 2048 * ks, oPt - oQt, 1024),
+                    tc::mma_ss(tmem + T2, tc::smem_desc(sQt + 2048 * ks, UM ? 0 : oPt - oQt, 1024),
                                tc::smem_desc(sV + 2048 * ks, 16, 1024), I_ST64, ks > 0);
                 for (int ks = 0; ks < 8; ++ks)
                     tc::mma_ss(tmem + T3, tc::smem_desc(sKh + 2048 * ks, 0, 1024),
@@ -979,7 +992,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const uint32_t off = tc::sw128_chunk(r, 4 * h + 2 * half + j);
-                        *reinterpret_cast<uint4*>(sPt + off) = pack8(&pv[8 * j], w2);
+                        if (!UM) *reinterpret_cast<uint4*>(sPt + off) = pack8(&pv[8 * j], w2);
                         *reinterpret_cast<uint4*>(sQ + off) = pack8(&pv[8 * j], 1.f);  // rows >= Wc: not stored
                     }
                 }
@@ -997,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc::tmem_ld32(lrow + T2 + 32 * h, v);
                 tc::tmem_ld16(lrow + T3 + sc, w);
                 tc::tmem_wait_ld();
-                const float decay = r < 64 ? rho : rho2;
+                const float decay = r < 64 || UM ? rho : rho2;  // unmasked: rows >= 64 hold C again
 #pragma unroll
                 for (int j = 0; j < 32; ++j) st[j] = decay * st[j] + __uint_as_float(v[j]);
 #pragma unroll
@@ -1069,11 +1082,11 @@ int launch_fwd_chunk_tc(const ChunkArgs& a, int mode, int* status, cudaStream_t 
         outp::Maps pm;
         if (!make_map(&pm.q, a.q, a.BH, a.n) || !make_map(&pm.p, a.out, a.BH, a.n) || !make_map(&pm.v, a.v, a.BH, a.n))
             return -2;
-        cudaError_t e = cudaFuncSetAttribute(fwd_out_p_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             outp::kSmemBytes);
+        auto kfn = a.unmasked ? fwd_out_p_tc_kernel<true> : fwd_out_p_tc_kernel<false>;
+        cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, outp::kSmemBytes);
         if (e != cudaSuccess) return -1;
-        if (launch_pdl(fwd_out_p_tc_kernel, dim3(a.nseg_launch, a.BH), dim3(kThreads), outp::kSmemBytes, st, pm, a,
-                       status) != cudaSuccess)
+        if (launch_pdl(kfn, dim3(a.nseg_launch, a.BH), dim3(kThreads), outp::kSmemBytes, st, pm, a, status) !=
+            cudaSuccess)
             return -1;
         return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
     }
@@ -1086,11 +1099,11 @@ int launch_fwd_chunk_tc(const ChunkArgs& a, int mode, int* status, cudaStream_t 
         sm4.k = maps.k;
         sm4.v = maps.v;
         if (!make_map(&sm4.p, a.out, a.BH, a.n)) return -2;
-        cudaError_t e = cudaFuncSetAttribute(fwd_sum_p_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             sump::kSmemBytes);
+        auto kfn = a.unmasked ? fwd_sum_p_tc_kernel<true> : fwd_sum_p_tc_kernel<false>;
+        cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, sump::kSmemBytes);
         if (e != cudaSuccess) return -1;
-        if (launch_pdl(fwd_sum_p_tc_kernel, dim3(a.nseg_launch, a.BH), dim3(kThreads), sump::kSmemBytes, st, sm4, a,
-                       status) != cudaSuccess)
+        if (launch_pdl(kfn, dim3(a.nseg_launch, a.BH), dim3(kThreads), sump::kSmemBytes, st, sm4, a, status) !=
+            cudaSuccess)
             return -1;
         return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
     }
