@@ -53,7 +53,7 @@ constexpr uint32_t T0 = 0, T1 = 64, T3 = 128, T2 = 192, kTmemCols = 256;
 enum Bar { FULLQ = 0, FULLKV, BA, BAT, BP, BPS, BO, BST, BS, kBarCount };
 
 struct TcMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k, v, o;  // o: the output buffer (stored Inner, summary pass with store_inner)
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
@@ -189,6 +189,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc::mbar_wait(&bars[BPS], ph, abort, status, 35);  // Inner and K~ written
                 tc::fence_after_sync();
+                if (SUMMARY && !FO && a.store_inner) {  // segment-local Inner -> out (one tile store)
+                    tc::tma_store_3d(&maps.o, sm + oIn, 0, (c_begin + it) * kW, bh);
+                    tc::bulk_commit();
+                }
                 if (FO) {
                     if (it + 1 < nit) load_q(c_begin + it + 1);  // Q is no longer read
                     // [K~^T ; K~^T] [V | Inner] -> T3T2 (dP; dE is not used)
@@ -222,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc::mma_commit(&bars[BST]);
                 tc::mbar_wait(&bars[BST], ph, abort, status, 37);  // K, V (and Q) free
+                if (SUMMARY && !FO && a.store_inner) tc::bulk_wait_read_all();  // Inner slot rewritten next chunk
                 if (SUMMARY && !FO && it + 1 < nit) load_q(c_begin + it + 1);
                 if (it + 1 < nit) {
                     load_kv(c_begin + it + 1);
@@ -232,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc::mbar_wait(&bars[BST], (nit - 1) & 1, &never, nullptr, 0);
             tc::mbar_wait(&bars[FULLKV], (loads - 1) & 1, &never, nullptr, 0);
             tc::mbar_wait(&bars[FULLQ], (loads - 1) & 1, &never, nullptr, 0);
+            tc::bulk_wait_all();
         }
         __syncwarp();
     } else {
@@ -389,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int j = 0; j < 32; ++j) dst[j] = st[j];
         }
-        if (SUMMARY) {
+        if (SUMMARY && seg < a.nsum) {  // (a launch that stores Inner also covers the last segment)
             const size_t si = (size_t)bh * a.nsum + seg;
             float* dst = r < 64 ? a.ws + a.L.PB + si * kD * kD + (size_t)r * kD
                                 : a.ws + a.L.EB + si * kD * kD + (size_t)(r - 64) * kD;
@@ -398,6 +404,271 @@ __global__ void __launch_bounds__(kThreads, 2)
             float* dr = a.ws + a.L.RB + si * kD * kD + (size_t)(r & 63) * kD + 32 * h + 16 * (r >> 6);
 #pragma unroll
             for (int j = 0; j < 16; ++j) dr[j] = rr[j];
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Output pass from the stored segment-local Inner (chunk 128, more than one segment).
+//
+// The summary pass stores, for every token of a segment, Inner^sl_t = P^sl_t^T q_t with the
+// value moment P^sl accumulated from zero at the segment start (bf16, in the output buffer).
+// With the segment's carry P_in,
+//     Inner_t = Inner^sl_t + g^(t - t0 + 1) P_in^T q_t,        t0 = the segment's first token,
+// so P leaves the chunk-to-chunk chain: only E is carried, and this pass reads q, k and
+// Inner^sl (no v).  Per chunk (local row r, it = chunk index in the segment):
+//   MMA1  A = Q K^T -> T0T1;  Q P_in -> T2                       (no dependence on E)
+//   EPI1  A~ = A * [j <= r] g^(r-j) -> T3;  Inner = Inner^sl + g^(it W + r + 1) Q P_in (bf16, in
+//         place);  K~ = diag(g^(Wc-1-i)) K (smem)
+//   MMA2  A~ Inner -> T0;  Q E0 -> T1;  [K~^T ; K~^T] Inner -> T2 (dE, rows 0..63 and 64..127)
+//   EPI2  out = g^(r+1) Q E0 + A~ Inner  (bf16 tile in smem, one TMA tile store over this
+//         chunk's Inner^sl, already consumed);  E <- g^Wc E + dE;  bf16 E0 (smem)
+namespace aout {
+
+constexpr uint32_t oQ = 0, oK = kTile, oI = 2 * kTile, oKt = 3 * kTile, oO = 4 * kTile;
+constexpr uint32_t oPi = 5 * kTile, oE0 = oPi + 8192;  // P_in, E0: [64][64] bf16 each
+constexpr uint32_t oGP = oE0 + 8192;
+constexpr uint32_t oBar = oGP + 1088;
+constexpr uint32_t oMisc = oBar + 16 * 8;
+constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
+constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192;
+
+enum Bar { FQK = 0, FI, BA, BAT, BB, BOS, kBarCount };
+
+struct Maps {
+    CUtensorMap q, k, i;  // i: the output buffer, holding Inner^sl, then out
+};
+
+}  // namespace aout
+
+__global__ void __launch_bounds__(kThreads, 2)
+    ahla_out_i_tc_kernel(const __grid_constant__ aout::Maps maps, const AhlaArgs a, int* status) {
+    // this pass's layout (shadows the kernel above)
+    constexpr uint32_t oQ = aout::oQ, oK = aout::oK, oI = aout::oI, oKt = aout::oKt, oO = aout::oO,
+                       oPi = aout::oPi, oE0 = aout::oE0;
+    constexpr uint32_t oGP = aout::oGP, oBar = aout::oBar, oMisc = aout::oMisc;
+    constexpr uint32_t T0 = aout::T0, T1 = aout::T1, T2 = aout::T2, T3 = aout::T3;
+    constexpr int FQK = aout::FQK, FI = aout::FI, BA = aout::BA, BAT = aout::BAT, BB = aout::BB, BOS = aout::BOS,
+                  kBarCount = aout::kBarCount;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* gp = reinterpret_cast<float*>(sm + oGP);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + oMisc);
+    volatile int* abort = reinterpret_cast<volatile int*>(sm + oMisc + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seg = a.seg0 + blockIdx.x, bh = blockIdx.y;
+    const int c_begin = seg * a.seg_chunks;
+    const int c_end = min(c_begin + a.seg_chunks, a.nchunks);
+    const float g = head_decay(a.gamma, bh, a.H);
+    const float log2g = log2f(g);
+    const int nit = c_end - c_begin;
+
+    // epilogue thread: TMEM lane / token row r, column half h; E row er, columns ec .. ec+15
+    const int q4 = warp & 3, h = (warp - 1) >> 2;
+    const int r = 32 * q4 + lane;
+    const int er = r & 63, ec = 32 * h + 16 * (r >> 6);
+    float ee[16];
+    auto publish_e = [&]() {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            *reinterpret_cast<uint4*>(sm + oE0 + tc::sw128_chunk(er, ec / 8 + j)) = pack8(&ee[8 * j]);
+    };
+
+    for (int i = tid; i < 2 * kW + 1; i += kThreads) gp[i] = pow_decay(log2g, (float)i);
+    if (tid == 0) {
+        for (int b = 0; b < kBarCount; ++b) tc::mbar_init(&bars[b], (b == BAT || b == BOS) ? 8 : 1);
+        *abort = 0;
+        tc::mbar_fence_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_holder, kTmemCols);
+    } else {
+        // carry-in of the segment: P_in (bf16, smem) and E_in (fp32 registers, bf16 copy in smem)
+        const size_t cidx = (size_t)bh * a.nseg + seg;
+        if (r < 64) {
+            const float* src = a.ws + a.L.Pin + cidx * kD * kD + (size_t)r * kD + 32 * h;
+            float t[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) t[j] = src[j];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(sm + oPi + tc::sw128_chunk(r, 4 * h + j)) = pack8(&t[8 * j]);
+        }
+        const float* esrc = a.ws + a.L.Ein + cidx * kD * kD + (size_t)er * kD + ec;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ee[j] = esrc[j];
+        publish_e();
+        tc::fence_proxy_async();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ control thread
+        if (lane == 0 && nit > 0) {
+            const uint32_t sQ = smem_u32(sm + oQ), sK = smem_u32(sm + oK), sI = smem_u32(sm + oI);
+            const uint32_t sKt = smem_u32(sm + oKt), sPi = smem_u32(sm + oPi), sE0 = smem_u32(sm + oE0);
+            auto load_qk = [&](int c) {
+                tc::mbar_arrive_expect_tx(&bars[FQK], 2 * kTile);
+                tc::tma_load_3d(sm + oQ, &maps.q, 0, c * kW, bh, &bars[FQK]);
+                tc::tma_load_3d(sm + oK, &maps.k, 0, c * kW, bh, &bars[FQK]);
+            };
+            auto load_i = [&](int c) {
+                tc::mbar_arrive_expect_tx(&bars[FI], kTile);
+                tc::tma_load_3d(sm + oI, &maps.i, 0, c * kW, bh, &bars[FI]);
+            };
+            constexpr uint32_t I_AB = tc::idesc_bf16(128, 128, 0, 0);   // K-major x K-major, N = 128
+            constexpr uint32_t I_QX = tc::idesc_bf16(128, 64, 0, 1);    // K-major x MN-major, N = 64
+            constexpr uint32_t I_TS64 = tc::idesc_bf16(128, 64, 0, 1);  // A (TMEM) x MN-major B, N = 64
+            constexpr uint32_t I_ST64 = tc::idesc_bf16(128, 64, 1, 1);  // MN-major x MN-major, N = 64
+            load_qk(c_begin);
+            load_i(c_begin);
+            int loads = 1;
+            for (int it = 0; it < nit; ++it) {
+                const uint32_t ph = it & 1;
+                tc::mbar_wait(&bars[FQK], ph, abort, status, 81);
+                if (it > 0) {  // previous chunk's EPI2 done: T0..T2 read, its output tile staged
+                    tc::mbar_wait(&bars[BOS], ph ^ 1, abort, status, 82);
+                    tc::tma_store_3d(&maps.i, sm + oO, 0, (c_begin + it - 1) * kW, bh);
+                    tc::bulk_commit();
+                }
+                tc::fence_after_sync();
+                // MMA1: A = Q K^T -> T0T1;  Q P_in -> T2
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sK + 32 * ks, 16, 1024),
+                               I_AB, ks > 0);
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_ss(tmem + T2, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sPi + 2048 * ks, 16, 1024),
+                               I_QX, ks > 0);
+                tc::mma_commit(&bars[BA]);
+                tc::mbar_wait(&bars[BAT], ph, abort, status, 83);  // A~, Inner, K~ written
+                tc::bulk_wait_read_all();  // the output tile slot is free before this chunk's EPI2
+                tc::fence_after_sync();
+                // MMA2: A~ Inner -> T0;  Q E0 -> T1;  [K~^T ; K~^T] Inner -> T2
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ts(tmem + T0, tmem + T3 + 8 * ks, tc::smem_desc(sI + 2048 * ks, 16, 1024), I_TS64, ks > 0);
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_ss(tmem + T1, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sE0 + 2048 * ks, 16, 1024),
+                               I_QX, ks > 0);
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem + T2, tc::smem_desc(sKt + 2048 * ks, 0, 1024), tc::smem_desc(sI + 2048 * ks, 16, 1024),
+                               I_ST64, ks > 0);
+                tc::mma_commit(&bars[BB]);
+                tc::mbar_wait(&bars[BB], ph, abort, status, 84);  // Q, K, Inner and K~ no longer read
+                if (it + 1 < nit) {
+                    load_qk(c_begin + it + 1);
+                    load_i(c_begin + it + 1);
+                    ++loads;
+                }
+            }
+            tc::mbar_wait(&bars[BOS], (nit - 1) & 1, abort, status, 85);  // the last output tile
+            tc::tma_store_3d(&maps.i, sm + oO, 0, (c_begin + nit - 1) * kW, bh);
+            tc::bulk_commit();
+            volatile int never = 0;
+            tc::mbar_wait(&bars[BB], (nit - 1) & 1, &never, nullptr, 0);
+            tc::mbar_wait(&bars[FQK], (loads - 1) & 1, &never, nullptr, 0);
+            tc::mbar_wait(&bars[FI], (loads - 1) & 1, &never, nullptr, 0);
+            tc::bulk_wait_all();
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int row0 = 32 * q4;
+        const uint32_t lrow = tmem + ((uint32_t)row0 << 16);
+        unsigned char* sK = sm + oK;
+        unsigned char* sI = sm + oI;
+        unsigned char* sKt = sm + oKt;
+        const float ginv = g > 0.f ? 1.f / g : 0.f;
+        for (int it = 0; it < nit; ++it) {
+            const uint32_t ph = it & 1;
+            const int c = c_begin + it;
+            const int Wc = min(kW, a.n - c * kW);
+            // ---- EPI1: A~ -> T3;  Inner (in place);  K~ -----------------------------------------
+            tc::mbar_wait(&bars[FQK], ph, abort, status, 91);
+            tc::mbar_wait(&bars[FI], ph, abort, status, 92);
+            tc::mbar_wait(&bars[BA], ph, abort, status, 93);
+            tc::fence_after_sync();
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int cb = 64 * h + 32 * p;
+                const float first = r >= cb ? gp[r - cb] : 0.f;
+                masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, ginv);
+            }
+            {
+                const float f = pow_decay(log2g, (float)(it * kW + r + 1));
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t qp[16];
+                    tc::tmem_ld16(lrow + T2 + 32 * h + 16 * half, qp);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const uint32_t off = tc::sw128_chunk(r, 4 * h + 2 * half + j);
+                        const uint4 il = *reinterpret_cast<const uint4*>(sI + off);
+                        const uint32_t iw[4] = {il.x, il.y, il.z, il.w};
+                        float in[8];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            in[2 * u] = bf_lo(iw[u]) + f * __uint_as_float(qp[8 * j + 2 * u]);
+                            in[2 * u + 1] = bf_hi(iw[u]) + f * __uint_as_float(qp[8 * j + 2 * u + 1]);
+                        }
+                        *reinterpret_cast<uint4*>(sI + off) = pack8(in);
+                    }
+                }
+                const float w1 = r < Wc ? gp[Wc - 1 - r] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t off = tc::sw128_chunk(r, 4 * h + j);
+                    *reinterpret_cast<uint4*>(sKt + off) = scale_chunk(*reinterpret_cast<const uint4*>(sK + off), w1);
+                }
+            }
+            tc::tmem_wait_st();
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[BAT]);
+
+            // ---- EPI2: out = g^(r+1) Q E0 + A~ Inner;  E <- g^Wc E + dE --------------------------
+            tc::mbar_wait(&bars[BB], ph, abort, status, 94);
+            tc::fence_after_sync();
+            {
+                const float s1 = gp[r + 1];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t qe[16], ai[16];
+                    tc::tmem_ld16(lrow + T1 + 32 * h + 16 * half, qe);
+                    tc::tmem_ld16(lrow + T0 + 32 * h + 16 * half, ai);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {  // output tile (rows >= Wc fall outside the tensor)
+                        float o[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            o[u] = s1 * __uint_as_float(qe[8 * j + u]) + __uint_as_float(ai[8 * j + u]);
+                        *reinterpret_cast<uint4*>(sm + oO + tc::sw128_chunk(r, 4 * h + 2 * half + j)) = pack8(o);
+                    }
+                }
+                uint32_t de[16];
+                tc::tmem_ld16(lrow + T2 + ec, de);
+                tc::tmem_wait_ld();
+                const float rho = gp[Wc];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) ee[j] = rho * ee[j] + __uint_as_float(de[j]);
+                publish_e();  // read by the next chunk's MMA2, after its EPI1 arrives
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[BOS]);
         }
     }
 
@@ -446,12 +717,25 @@ int launch_ahla_tc(const AhlaArgs& a, bool summary, int* status, cudaStream_t st
     TcMaps maps;
     if (!make_map(&maps.q, a.q, a.BH, a.n) || !make_map(&maps.k, a.k, a.BH, a.n) || !make_map(&maps.v, a.v, a.BH, a.n))
         return -2;
+    if (summary && !first_order && a.store_inner && !make_map(&maps.o, a.out, a.BH, a.n)) return -2;
     dim3 grid(a.nseg_launch, a.BH);
     auto kfn = summary ? (first_order ? ahla_tc_kernel<true, true> : ahla_tc_kernel<true, false>)
                        : (first_order ? ahla_tc_kernel<false, true> : ahla_tc_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess) kfn<<<grid, kThreads, kSmemBytes, st>>>(maps, a, status);
     if (e != cudaSuccess) return -1;
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_ahla_tc_out_i(const AhlaArgs& a, int* status, cudaStream_t st) {
+    if (a.nseg_launch <= 0 || a.BH <= 0) return 0;
+    aout::Maps maps;
+    if (!make_map(&maps.q, a.q, a.BH, a.n) || !make_map(&maps.k, a.k, a.BH, a.n) || !make_map(&maps.i, a.out, a.BH, a.n))
+        return -2;
+    cudaError_t e = cudaFuncSetAttribute(ahla_out_i_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         aout::kSmemBytes);
+    if (e != cudaSuccess) return -1;
+    ahla_out_i_tc_kernel<<<dim3(a.nseg_launch, a.BH), kThreads, aout::kSmemBytes, st>>>(maps, a, status);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -1510,12 +1510,16 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
     mark(0);
     if (launch_ahla_init(a, d, st)) return cuda_fail("AHLA carry-in initialisation");
     mark(1);
+    // chunk 128 (tcgen05) with more than one segment: the summary pass also stores the
+    // segment-local Inner in out, over every segment, and the output pass starts from it
+    const bool stored_inner = chunk == 128 && p.nseg > 1;
     if (p.nseg > 1) {
         const int steps = p.nseg - 1, seg_tokens = p.seg_chunks * chunk;
         const size_t dd = (size_t)d * d;
         AhlaArgs b = a;
         b.seg0 = 0;
-        b.nseg_launch = steps;
+        b.nseg_launch = stored_inner ? p.nseg : steps;
+        b.store_inner = stored_inner ? 1 : 0;
         if (ahla_pass(b, d, chunk, true, st)) return cuda_fail("AHLA segment summaries");
         mark(2);
         if (launch_linear_scan(a.ws + L.PB, a.ws + L.Pin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true, gamma,
@@ -1535,7 +1539,8 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
     AhlaArgs o = a;
     o.seg0 = 0;
     o.nseg_launch = p.nseg;
-    if (ahla_pass(o, d, chunk, false, st)) return cuda_fail("AHLA output pass");
+    if (stored_inner ? launch_ahla_tc_out_i(o, reinterpret_cast<int*>(a.ws), st) : ahla_pass(o, d, chunk, false, st))
+        return cuda_fail("AHLA output pass");
     mark(4);
     mark(5);
     return succeed();

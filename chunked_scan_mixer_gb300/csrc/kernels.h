@@ -49,6 +49,10 @@ struct AhlaArgs {
     float* final_state;  // nullable: [BH][2 d dv + 2 d] = P | E | m | n after token n
                          // (first-order mode of the tcgen05 kernel: [BH][d*dv] = P only)
     const float* init_state;  // nullable: the same layout, the state before token 0
+    // tcgen05 summary pass (chunk 128): also store the segment-local Inner (the first-order
+    // output with the value moment accumulated from the segment start, bf16) in out, for the
+    // output pass launch_ahla_tc_out_i; the launch then covers every segment.
+    int store_inner;
 };
 int launch_ahla_chunk(const AhlaArgs& a, int d, int W, bool summary, cudaStream_t st);
 int launch_ahla_init(const AhlaArgs& a, int d, cudaStream_t st);
@@ -61,6 +65,9 @@ size_t ahla_tc_smem();
 // first_order: the pass computes masked first-order linear attention (out = Inner; the
 // summaries keep only P_B), the inner pass of the third-order output.
 int launch_ahla_tc(const AhlaArgs& a, bool summary, int* status, cudaStream_t st, bool first_order = false);
+// Output pass from the stored segment-local Inner (tcgen05, chunk 128): only E is carried
+// from chunk to chunk.
+int launch_ahla_tc_out_i(const AhlaArgs& a, int* status, cudaStream_t st);
 
 // Arguments of one chunk-kernel launch (summary or output pass of the forward).
 struct ChunkArgs {
