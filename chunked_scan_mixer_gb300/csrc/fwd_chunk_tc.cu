@@ -86,9 +86,8 @@ __device__ __forceinline__ uint4 pack8(const float* f, float s) {
 // with base = g (A~) or g^2 (B~), read from src (TMEM, fp32) and written packed (16 columns)
 // to dst.  Blocks entirely above the diagonal of this warp's rows are written as zeros
 // without reading; the factors are stepped multiplicatively from base^(r - cb).
-__device__ __forceinline__ void masked_block(uint32_t src, uint32_t dst, int r, int cb, int warp_row0,
-                                             float first, float step_up) {
-    uint32_t pk[16];
+__device__ __forceinline__ void masked_pack(uint32_t src, int r, int cb, int warp_row0, float first, float step_up,
+                                            uint32_t (&pk)[16]) {
     if (cb > warp_row0 + 31) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = 0u;
@@ -111,6 +110,12 @@ __device__ __forceinline__ void masked_block(uint32_t src, uint32_t dst, int r, 
             pk[j / 2] = pack_bf16x2(a0, a1);
         }
     }
+}
+
+__device__ __forceinline__ void masked_block(uint32_t src, uint32_t dst, int r, int cb, int warp_row0,
+                                             float first, float step_up) {
+    uint32_t pk[16];
+    masked_pack(src, r, cb, warp_row0, first, step_up, pk);
     tc::tmem_st16(dst, pk);
 }
 
@@ -467,11 +472,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 //     p_t = p^sl_t + g^(t - t0 + 1) S_in q_t,         t0 = the segment's first token,
 // so the key moment leaves the chunk-to-chunk chain: this pass reads q, p^sl and v (no k) and
 // carries only Z from chunk to chunk.  Per chunk (local row r, it = chunk index in the segment):
-//   MMA-a  Q S_in -> T3                                          (no dependence on Z)
+//   MMA-a  Q S_in -> T0                                          (no dependence on Z)
 //   EPI-a  P = P^sl + g^(it W + r + 1) Q S_in  (bf16, in place);  P~ = diag(g^(2(Wc-1-r))) P
-//   MMA-b  B = Q P^T -> T0T1;  Q Z0 -> T2
-//   EPI-b  B~ = B * [j <= r] g^(2(r-j))  (bf16)  -> T3
-//   MMA-c  B~ V -> T0;  [P~^T ; P~^T] V -> T1 (dZ, rows 0..63 and again 64..127)
+//   MMA-b  B = Q P^T -> T0T1;  Q Z0 -> T2;  then [P~^T ; P~^T] V -> T3 (dZ, rows 0..63 and again
+//          64..127), which runs while EPI-b masks B
+//   EPI-b  B~ = B * [j <= r] g^(2(r-j))  (bf16, packed in place over T0; the two warps of a lane
+//          quarter order their reads and writes with a named barrier)
+//   MMA-c  B~ V -> T1
 //   EPI-c  out = g^(2(r+1)) Q Z0 + B~ V  (bf16 tile in smem; one TMA tile store writes it over
 //          this chunk's p^sl, already consumed);  Z <- g^(2Wc) Z + dZ  (fp32, 16 columns a
 //          thread);  bf16 Z0 (smem)
@@ -591,18 +598,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t ph = it & 1;
                 tc::mbar_wait(&bars[FQP], ph, abort, status, 41);
                 tc::fence_after_sync();
-                // MMA-a: Q S_in -> T3 (T3's B~ of the previous chunk was read: its MMA-c completed)
+                // MMA-a: Q S_in -> T0 (T0's B~ of the previous chunk was read: its MMA-c completed)
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_ss(tmem + T3, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sS + 2048 * ks, 16, 1024),
+                    tc::mma_ss(tmem + T0, tc::smem_desc(sQ + 32 * ks, 16, 1024), tc::smem_desc(sS + 2048 * ks, 16, 1024),
                                I_QX, ks > 0);
                 tc::mma_commit(&bars[BA]);
                 tc::mbar_wait(&bars[BAT], ph, abort, status, 42);  // P, P~ written; previous EPI-c done
                 tc::fence_after_sync();
-                if (it > 0) {  // the previous chunk's output tile (staged by its EPI-c) -> out
-                    tc::mbar_wait(&bars[BOS], ph ^ 1, abort, status, 47);
-                    tc::tma_store_3d(&maps.p, sm + oO, 0, (c_begin + it - 1) * kW, bh);
-                    tc::bulk_commit();
-                }
                 // MMA-b: B = Q P^T -> T0T1;  Q Z0 -> T2   (unmasked: P Q^T and P C0)
                 const uint32_t sL = UM ? sP : sQ, sR = UM ? sQ : sP;
                 for (int ks = 0; ks < 4; ++ks)
@@ -612,23 +614,30 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tc::mma_ss(tmem + T2, tc::smem_desc(sL + 32 * ks, 16, 1024), tc::smem_desc(sZ0 + 2048 * ks, 16, 1024),
                                I_QX, ks > 0);
                 tc::mma_commit(&bars[BB]);
+                // dZ: [P~^T ; P~^T] V -> T3 (unmasked: [Q~^T ; Q~^T] V), while EPI-b masks B
+                tc::mbar_wait(&bars[FV], ph, abort, status, 45);
+                tc::fence_after_sync();
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem + T3, tc::smem_desc(sPt + 2048 * ks, 0, 1024), tc::smem_desc(sV + 2048 * ks, 16, 1024),
+                               I_ST64, ks > 0);
+                if (it > 0) {  // the previous chunk's output tile (staged by its EPI-c) -> out
+                    tc::mbar_wait(&bars[BOS], ph ^ 1, abort, status, 47);
+                    tc::tma_store_3d(&maps.p, sm + oO, 0, (c_begin + it - 1) * kW, bh);
+                    tc::bulk_commit();
+                }
                 tc::mbar_wait(&bars[BB], ph, abort, status, 43);  // Q and P no longer read (Q~ was copied)
                 if (it + 1 < nit) {
                     load_qp(c_begin + it + 1);
                     ++lqp;
                 }
                 tc::mbar_wait(&bars[BBT], ph, abort, status, 44);
-                tc::mbar_wait(&bars[FV], ph, abort, status, 45);
                 tc::bulk_wait_read_all();  // the output tile slot is free before this chunk's EPI-c
                 tc::fence_after_sync();
-                // MMA-c: B~ V -> T0;  [P~^T ; P~^T] V -> T1
+                // MMA-c: B~ V -> T1 (B~ packed in T0)
                 for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_ts(tmem + T0, tmem + T3 + 8 * ks, tc::smem_desc(sV + 2048 * ks, 16, 1024), I_TS64, ks > 0);
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_ss(tmem + T1, tc::smem_desc(sPt + 2048 * ks, 0, 1024), tc::smem_desc(sV + 2048 * ks, 16, 1024),
-                               I_ST64, ks > 0);
+                    tc::mma_ts(tmem + T1, tmem + T0 + 8 * ks, tc::smem_desc(sV + 2048 * ks, 16, 1024), I_TS64, ks > 0);
                 tc::mma_commit(&bars[BC]);
-                tc::mbar_wait(&bars[BC], ph, abort, status, 46);  // V, P~ and T3 free
+                tc::mbar_wait(&bars[BC], ph, abort, status, 46);  // V, P~ and T0 free
                 if (it + 1 < nit) {
                     load_v(c_begin + it + 1);
                     ++lv;
@@ -675,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t qs[16];
-                    tc::tmem_ld16(lrow + T3 + 32 * h + 16 * half, qs);
+                    tc::tmem_ld16(lrow + T0 + 32 * h + 16 * half, qs);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
@@ -698,15 +707,40 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[BAT]);
 
-            // ---- EPI-b: B~ -> T3 (unmasked: decay g^(r-j)) ------------------------------------------
+            // ---- EPI-b: B~ packed over T0 (unmasked: decay g^(r-j)) -------------------------------
+            // Warp h of a lane quarter reads B's columns 64h .. 64h+63 and writes their packed
+            // pairs to T0 columns 32h .. 32h+31.  Warp h = 1's writes land on columns warp h = 0
+            // reads, so warp h = 0 signals (named barrier 1 + q4) once it has read them.
             tc::mbar_wait(&bars[BB], ph, abort, status, 53);
             tc::fence_after_sync();
             constexpr int BP2 = UM ? 1 : 2;  // decay power of the second product
+            const float step2 = UM ? ginv : ginv * ginv;
+            if (h == 0) {
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int cb = 64 * h + 32 * p;
-                const float first = r >= cb ? gp[BP2 * (r - cb)] : 0.f;
-                masked_block(lrow + T0 + cb, lrow + T3 + cb / 2, r, cb, row0, first, UM ? ginv : ginv * ginv);
+                for (int p = 0; p < 2; ++p) {
+                    const float first = r >= 32 * p ? gp[BP2 * (r - 32 * p)] : 0.f;
+                    masked_block(lrow + T0 + 32 * p, lrow + T0 + 16 * p, r, 32 * p, row0, first, step2);
+                }
+                tc::fence_before_sync();
+                switch (q4) {  // constant barrier ids
+                    case 0: tc::named_arrive(1, 64); break;
+                    case 1: tc::named_arrive(2, 64); break;
+                    case 2: tc::named_arrive(3, 64); break;
+                    default: tc::named_arrive(4, 64); break;
+                }
+            } else {
+                uint32_t pk0[16], pk1[16];
+                masked_pack(lrow + T0 + 64, r, 64, row0, r >= 64 ? gp[BP2 * (r - 64)] : 0.f, step2, pk0);
+                masked_pack(lrow + T0 + 96, r, 96, row0, r >= 96 ? gp[BP2 * (r - 96)] : 0.f, step2, pk1);
+                switch (q4) {
+                    case 0: tc::named_bar(1, 64); break;
+                    case 1: tc::named_bar(2, 64); break;
+                    case 2: tc::named_bar(3, 64); break;
+                    default: tc::named_bar(4, 64); break;
+                }
+                tc::fence_after_sync();
+                tc::tmem_st16(lrow + T0 + 32, pk0);
+                tc::tmem_st16(lrow + T0 + 48, pk1);
             }
             tc::tmem_wait_st();
             tc::fence_before_sync();
@@ -722,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int half = 0; half < 2; ++half) {
                     uint32_t qz[16], bv[16];
                     tc::tmem_ld16(lrow + T2 + 32 * h + 16 * half, qz);
-                    tc::tmem_ld16(lrow + T0 + 32 * h + 16 * half, bv);
+                    tc::tmem_ld16(lrow + T1 + 32 * h + 16 * half, bv);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {  // output tile (rows >= Wc fall outside the tensor)
@@ -734,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
                 uint32_t dz[16];
-                tc::tmem_ld16(lrow + T1 + zc, dz);
+                tc::tmem_ld16(lrow + T3 + zc, dz);
                 tc::tmem_wait_ld();
                 const float rho2 = gp[BP2 * Wc];  // (unmasked: C decays by g per token)
 #pragma unroll

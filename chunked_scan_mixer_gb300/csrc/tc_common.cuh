@@ -183,9 +183,13 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int j) {
     return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
 }
 
-// Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
+// Named barrier over `count` threads (ids 1..15; 0 is __syncthreads): named_bar waits for
+// all `count`, named_arrive counts this warp in without waiting.
 __device__ __forceinline__ void named_bar(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 }  // namespace tc
