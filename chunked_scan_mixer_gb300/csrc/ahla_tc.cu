@@ -19,7 +19,8 @@
 // (undecayed), accumulating P, E, R from zero.
 //
 // FO (first-order mode) serves the third-order output's inner pass, masked first-order linear
-// attention u = Inner: the output pass writes Inner itself and skips MMA3 and EPI3, and the
+// attention u = Inner: the output pass writes Inner itself (one TMA tile store a chunk from the
+// Inner slot) and skips MMA3 and EPI3, and the
 // summary pass skips MMA1 to EPI2 and the R product, keeping only the scaled keys and the
 // state product, whose P half is the segment's P (the E and R summaries are then unused).
 //
@@ -189,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc::mbar_wait(&bars[BPS], ph, abort, status, 35);  // Inner and K~ written
                 tc::fence_after_sync();
-                if (SUMMARY && !FO && a.store_inner) {  // segment-local Inner -> out (one tile store)
+                if ((SUMMARY && !FO && a.store_inner) || (FO && !SUMMARY)) {
+                    // segment-local Inner (first-order mode: the pass's output) -> out, one tile store
                     tc::tma_store_3d(&maps.o, sm + oIn, 0, (c_begin + it) * kW, bh);
                     tc::bulk_commit();
                 }
@@ -226,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc::mma_commit(&bars[BST]);
                 tc::mbar_wait(&bars[BST], ph, abort, status, 37);  // K, V (and Q) free
-                if (SUMMARY && !FO && a.store_inner) tc::bulk_wait_read_all();  // Inner slot rewritten next chunk
+                if ((SUMMARY && !FO && a.store_inner) || (FO && !SUMMARY))
+                    tc::bulk_wait_read_all();  // the Inner slot is rewritten in the next chunk
                 if (SUMMARY && !FO && it + 1 < nit) load_q(c_begin + it + 1);
                 if (it + 1 < nit) {
                     load_kv(c_begin + it + 1);
@@ -309,11 +312,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
 
-            // ---- EPI2: Inner = g^(r+1) Q P0 + A~ V -> smem (first-order mode: also -> out) ----
+            // ---- EPI2: Inner = g^(r+1) Q P0 + A~ V -> smem (first-order mode: the output tile) ----
             if (CHAIN) {
                 tc::mbar_wait(&bars[BP], ph, abort, status, 43);
                 tc::fence_after_sync();
-                bf16* fo_out = static_cast<bf16*>(a.out) + ((size_t)bh * a.n + (size_t)c * kW + r) * kD + 32 * h;
                 const float s1 = r < Wc ? gp[r + 1] : 0.f;
                 const float keep = r < Wc ? 1.f : 0.f;
 #pragma unroll
@@ -326,11 +328,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) in[j] = s1 * __uint_as_float(qp[j]) + keep * __uint_as_float(av[j]);
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const uint4 packed = pack8(&in[8 * j]);
-                        *reinterpret_cast<uint4*>(sIn + tc::sw128_chunk(r, 4 * h + 2 * half + j)) = packed;
-                        if (FO && r < Wc) *reinterpret_cast<uint4*>(fo_out + 16 * half + 8 * j) = packed;
-                    }
+                    for (int j = 0; j < 2; ++j)
+                        *reinterpret_cast<uint4*>(sIn + tc::sw128_chunk(r, 4 * h + 2 * half + j)) = pack8(&in[8 * j]);
                 }
             }
             tc::fence_proxy_async();
@@ -717,7 +716,9 @@ int launch_ahla_tc(const AhlaArgs& a, bool summary, int* status, cudaStream_t st
     TcMaps maps;
     if (!make_map(&maps.q, a.q, a.BH, a.n) || !make_map(&maps.k, a.k, a.BH, a.n) || !make_map(&maps.v, a.v, a.BH, a.n))
         return -2;
-    if (summary && !first_order && a.store_inner && !make_map(&maps.o, a.out, a.BH, a.n)) return -2;
+    if (((summary && !first_order && a.store_inner) || (first_order && !summary)) &&
+        !make_map(&maps.o, a.out, a.BH, a.n))
+        return -2;
     dim3 grid(a.nseg_launch, a.BH);
     auto kfn = summary ? (first_order ? ahla_tc_kernel<true, true> : ahla_tc_kernel<true, false>)
                        : (first_order ? ahla_tc_kernel<false, true> : ahla_tc_kernel<false, false>);
