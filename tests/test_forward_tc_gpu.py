@@ -78,3 +78,17 @@ def test_multi_chunk_segments(B, H, n):
     assert seg_chunks >= 3
     x = inputs.make_custom(B, H, n, 64, 64, torch.bfloat16, seed=n % 1000, gamma=(0.98, 0.9999))
     assert rel_err(np64(run(x)), oracle(x)) <= 2e-2
+
+
+@pytest.mark.parametrize("gamma", [None, (0.5, 0.9)])
+def test_multi_chunk_segments_decay_extremes(gamma):
+    """Segments of several chunks without decay and with strong decay: on the stored-p path
+    the carry enters each chunk as g^(it W + r + 1) S_in q, which underflows to zero within a
+    chunk or two at g = 0.5 (exactly the weight the pair sum gives it)."""
+    B, H, n = 1, 16, 128 * 40 + 9
+    nseg, seg_chunks, _ = hla.forward_plan(B, H, n, 64, 64, 128)
+    assert nseg > 1 and seg_chunks >= 2
+    x = inputs.make_custom(B, H, n, 64, 64, torch.bfloat16, seed=31, gamma=gamma)
+    o = run(x)
+    assert torch.isfinite(o.float()).all()
+    assert rel_err(np64(o), oracle(x)) <= 2e-2

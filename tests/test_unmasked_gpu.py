@@ -260,3 +260,16 @@ def test_tcgen05_and_mma_paths_agree():
     assert rel_err(np64(a), ref) <= 2e-2
     assert rel_err(np64(b), ref) <= 2e-2
     assert rel_err(np64(a), np64(b)) <= 2e-2
+
+
+@pytest.mark.parametrize("gamma", [None, (0.5, 0.9)])
+def test_tcgen05_multi_chunk_segments_decay_extremes(gamma):
+    """The unmasked output on segments of several chunks (the stored-p kernels), without decay
+    and with strong decay, where the carry's share g^(it W + r + 1) underflows to zero."""
+    B, H, n = 1, 16, 128 * 40 + 9
+    nseg, seg_chunks, _ = hla.forward_plan(B, H, n, 64, 64, 128)
+    assert nseg > 1 and seg_chunks >= 2
+    x = inputs.make_custom(B, H, n, 64, 64, torch.bfloat16, seed=32, gamma=gamma)
+    o = _run_kernel(x)
+    assert torch.isfinite(o.float()).all()
+    assert rel_err(np64(o), oracle(x)) <= 2e-2
