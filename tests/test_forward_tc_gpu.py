@@ -92,3 +92,53 @@ def test_multi_chunk_segments_decay_extremes(gamma):
     o = run(x)
     assert torch.isfinite(o.float()).all()
     assert rel_err(np64(o), oracle(x)) <= 2e-2
+
+
+def _device_inputs(seed, B=1, H=16, n=128 * 40 + 9):
+    x = inputs.make_custom(B, H, n, 64, 64, torch.bfloat16, seed=seed, gamma=(0.98, 0.9999))
+    return x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["gamma"].cuda()
+
+
+def test_graph_capture_replays_forward():
+    """The stored-p forward (kernels chained by programmatic dependent launch) captured in a CUDA
+    graph: a replay reproduces the eager output bit for bit, and a replay after new inputs are
+    written into the captured buffers recomputes."""
+    q, k, v, g = _device_inputs(33)
+    ref = hla.forward(q, k, v, gamma=g, chunk=128)
+    out = torch.empty_like(v)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture
+        hla.forward(q, k, v, gamma=g, chunk=128, out=out)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        hla.forward(q, k, v, gamma=g, chunk=128, out=out)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    q2, k2, v2, _ = _device_inputs(34)
+    ref2 = hla.forward(q2, k2, v2, gamma=g, chunk=128)
+    q.copy_(q2)
+    k.copy_(k2)
+    v.copy_(v2)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref2)
+
+
+def test_concurrent_streams():
+    """Two forwards in flight on two streams at once (each stream has its own workspace)."""
+    xs = [_device_inputs(35), _device_inputs(36)]
+    refs = [hla.forward(q, k, v, gamma=g, chunk=128) for q, k, v, g in xs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for (q, k, v, g), s in zip(xs, streams):
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            outs.append(hla.forward(q, k, v, gamma=g, chunk=128))
+    torch.cuda.synchronize()
+    for o, r in zip(outs, refs):
+        assert torch.equal(o, r)
