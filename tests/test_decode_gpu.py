@@ -162,3 +162,37 @@ def test_compact_decode_full_width_sampled():
         ref = cref.decode_step(st, np32(q[n_:n_ + 1, h_:h_ + 1].cpu()), np32(k[n_:n_ + 1, h_:h_ + 1].cpu()),
                                np32(v[n_:n_ + 1, h_:h_ + 1].cpu()), np.full(1, 0.999))
         assert rel_err(np64(o[n_:n_ + 1, h_:h_ + 1].cpu()), ref) <= 2e-2
+
+
+def test_decode_step_captured_in_a_graph():
+    """A serving loop's form of the step: one decode step captured in a CUDA graph and replayed
+    with fresh q, k, v copied into the captured buffers gives, step by step, the eager step's
+    outputs and state (bit for bit) and the oracle's."""
+    N, H, d, dv = 4, 8, 128, 128
+    st, gamma = prefill_state(N, H, d, dv, 40, seed=77, gamma=(0.95, 0.999))
+    g = gamma.cuda()
+    eager = torch.from_numpy(st.astype(np.float32)).cuda()
+    state = eager.clone()
+    state_ref = st.astype(np.float32).astype(np.float64).copy()
+    qb, kb, vb = (torch.empty((N, H, x), dtype=torch.bfloat16, device="cuda") for x in (d, d, dv))
+    out = torch.empty((N, H, dv), dtype=torch.bfloat16, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # warm-up outside the capture, on a scratch copy of the state
+        hla.decode_step(state.clone(), qb.zero_(), kb.zero_(), vb.zero_(), gamma=g, out=out)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        hla.decode_step(state, qb, kb, vb, gamma=g, out=out)
+    for step in range(4):
+        q, k, v = inputs.decode_step_inputs(100 + step, N, H, d, dv, dtype=torch.bfloat16)
+        qb.copy_(q)
+        kb.copy_(k)
+        vb.copy_(v)
+        graph.replay()
+        o_eager = hla.decode_step(eager, q.cuda(), k.cuda(), v.cuda(), gamma=g)
+        torch.cuda.synchronize()
+        assert torch.equal(out, o_eager), step
+        assert torch.equal(state, eager), step
+        ref = cref.decode_step(state_ref, np32(q), np32(k), np32(v), gamma.double().numpy())
+        assert rel_err(np64(out.cpu()), ref) <= tol_for(torch.bfloat16), step
