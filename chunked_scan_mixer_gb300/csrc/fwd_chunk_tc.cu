@@ -812,7 +812,7 @@ constexpr uint32_t oGP = oS0 + 8192;  // decay table g^0 .. g^(2W)
 constexpr uint32_t oBar = oGP + 1088;
 constexpr uint32_t oMisc = oBar + 16 * 8;
 constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
-constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192;
+constexpr uint32_t T0 = 0, T2 = 128, T3 = 192;  // T0 .. T0+127: A = Q K^T (N = 128)
 
 enum Bar { FQK = 0, FV, BA, BAT, BP, BPS, BST, kBarCount };
 
