@@ -142,3 +142,23 @@ def test_concurrent_streams():
     torch.cuda.synchronize()
     for o, r in zip(outs, refs):
         assert torch.equal(o, r)
+
+
+@pytest.mark.parametrize("masked", [True, False])
+def test_stored_p_path_continues_from_init_state(masked):
+    """The stored-p kernels with a carried-in state: a prefill over [0, m) (final state on the
+    mma.sync path), then [m, n) at chunk 128 on multi-chunk segments from that state, equals the
+    oracle over [0, n) on the second part.  Segment 0's carry is then nonzero, so its
+    Q S_in term and Z_in enter as well."""
+    B, H, m, n2 = 1, 16, 300, 128 * 40 + 9
+    nseg, seg_chunks, _ = hla.forward_plan(B, H, n2, 64, 64, 128)
+    assert nseg > 1 and seg_chunks >= 2
+    x = inputs.make_custom(B, H, m + n2, 64, 64, torch.bfloat16, seed=37, gamma=(0.98, 0.9999))
+    g = x["gamma"].cuda()
+    part = lambda lo, hi: [x[t][:, :, lo:hi].contiguous().cuda() for t in ("q", "k", "v")]
+    _, s1 = hla.forward(*part(0, m), gamma=g, chunk=32, return_final_state=True, masked=masked)
+    o2 = hla.forward(*part(m, m + n2), gamma=g, chunk=128, init_state=s1, masked=masked)
+    hla.check_status()
+    gd = x["gamma"].double().numpy()
+    ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), gd, masked=masked)[:, :, m:]
+    assert rel_err(np64(o2.cpu()), ref) <= 2e-2
