@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                                    tc::smem_desc(sK + 32 * ks, 16, 1024), I_AB, ks > 0);
                     tc::mma_commit(&bars[BA]);
                     tc::mbar_wait(&bars[BAT], ph, abort, status, 34);
+                    // the previous chunk's Inner tile store has read the slot before this chunk's
+                    // EPI2 (which follows MMA2) rewrites it
+                    if ((SUMMARY && !FO && a.store_inner) || (FO && !SUMMARY)) tc::bulk_wait_read_all();
                     tc::fence_after_sync();
                     // MMA2: A~ V -> T2;  Q P0 -> T0
                     for (int ks = 0; ks < 8; ++ks)
@@ -228,8 +231,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc::mma_commit(&bars[BST]);
                 tc::mbar_wait(&bars[BST], ph, abort, status, 37);  // K, V (and Q) free
-                if ((SUMMARY && !FO && a.store_inner) || (FO && !SUMMARY))
-                    tc::bulk_wait_read_all();  // the Inner slot is rewritten in the next chunk
                 if (SUMMARY && !FO && it + 1 < nit) load_q(c_begin + it + 1);
                 if (it + 1 < nit) {
                     load_kv(c_begin + it + 1);
