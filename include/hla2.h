@@ -30,7 +30,12 @@
  *   - Packed state of one head (decode layout), float32:
  *       [ S d*d (row-major) | C d*dv | G d*dv | m d | h d ]   (hla2_state_floats)
  *     init_state / final_state / the decode state are [B or N, H] such blocks.
- *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).  The
+ *     compute calls only enqueue work (no host synchronisation, no device allocation);
+ *     hla2_forward and the decode steps can be captured in a CUDA graph.  Within one
+ *     forward, a kernel may start its prologue while the previous kernel of the call
+ *     drains (programmatic dependent launch); it waits for that kernel's results before
+ *     touching memory.
  *     Return value: HLA2_OK or a negative error code; hla2_last_error() describes the
  *     last failure on the calling host thread.  Argument errors are detected on the
  *     host before anything is launched; launch errors map to HLA2_ERR_CUDA.
@@ -236,8 +241,9 @@ int hla2_ahla_backward(const void* q, const void* k, const void* v, const void* 
  * of the first two carry the causal mask:
  *   o_t = sum_{j <= t} sum_{i <= j} sum_{l <= j} (q_t . k_i)(k_i . q_j)(q_j . k_l) v_l,
  * i.e. the masked second-order output whose values are the first-order outputs
- * u_j = sum_{l <= j} (q_j . k_l) v_l.  It runs as a chunked first-order pass (SIMT) into the
- * workspace, then hla2_forward on (q, k, u) -- the tcgen05 kernels for bf16, d = dv = 64,
+ * u_j = sum_{l <= j} (q_j . k_l) v_l.  It runs as a chunked first-order pass into the
+ * workspace (the tcgen05 AHLA kernel in a first-order mode for bf16, d = dv = 64; SIMT
+ * otherwise), then hla2_forward on (q, k, u) -- the tcgen05 kernels for bf16, d = dv = 64,
  * chunk 128.  normalize != 0 divides by the same sum with v -> 1 (+ opts->eps), computed the
  * same way with the value rows (1, 0, ..., 0).  gamma must be NULL (HLA2_ERR_UNSUPPORTED
  * otherwise); no init_state; opts->final_state receives the streaming state after token n
