@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode and training rows measured after the headline")
     ap.add_argument("--only", choices=("decode", "decode_compact", "decode_unmasked", "decode_mq", "train", "ahla",
-                                       "unmasked", "hla3"),
+                                       "unmasked", "hla3", "prefill"),
                     default=None,
                     help="measure only this row (for profiler captures; --steps/--warmup apply)")
     ap.add_argument("--decode-seqs", type=int, default=256,
@@ -490,6 +490,41 @@ def measure_unmasked(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: i
                          "frac": achieved / hbm_gbs, "kernel": kname, "algorithmic_bytes_per_launch": nbytes}}
 
 
+def measure_prefill(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5, n: int | None = None):
+    """Prefill row: the long-context forward (B=1 H=16 n=65536 d=dv=64 bf16, decay
+    linspace(0.99, 0.9999), chunk 128) that also returns the state after the last token (the
+    decode step's starting state); 1,048,576 tokens per step."""
+    import dataclasses
+
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = inputs.WORKLOADS["long"]
+    if n is not None:
+        w = dataclasses.replace(w, n=n)
+    x = inputs.make(w, device=dev, seed=replica_seed(w.seed, dist.rank))
+    q, k, v = x["q"], x["k"], x["v"]
+    gamma = x["gamma"].to(dev)
+    out = torch.empty_like(v)
+
+    def one():
+        hla.forward(q, k, v, gamma=gamma, chunk=w.chunk, out=out, return_final_state=True)
+
+    ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
+    tokens = w.B * w.H * w.n
+    # q, k, v read, out written, plus the state written (about 0.3 % of the bytes)
+    nbytes = tokens * (2 * w.d + 2 * w.dv) * 2 + w.B * w.H * hla.state_floats(w.d, w.dv) * 4
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"prefill: long-context masked forward with the final state, B={w.B} H={w.H} n={w.n} "
+                        f"d=dv={w.d} bf16, decay linspace(0.99,0.9999), unnormalised, chunk {w.chunk}",
+            "metric": "prefill tokens/s", "unit": "tokens/s", "value": dist.world * tokens / (ms * 1e-3),
+            "ms_per_step": ms, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "kernel": "whole step", "algorithmic_bytes_per_step": nbytes}}
+
+
 def measure_hla3(dev, dist: Dist, hbm_gbs: float, steps: int = 30, warmup: int = 5, n: int | None = None):
     """Third-order row: the masked third-order output at gamma = 1 on the long-context shapes
     (B=1 H=16 n=65536 d=dv=64 bf16, unnormalised, chunk 128): the first-order pass on the AHLA
@@ -533,6 +568,8 @@ def run_only(args, dist: Dist, dev):
         row = measure_hla3(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
     elif args.only == "decode_mq":
         row = measure_decode_mq(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, seqs=args.decode_seqs)
+    elif args.only == "prefill":
+        row = measure_prefill(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
     elif args.only == "unmasked":
         row = measure_unmasked(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n,
                                chunk=args.chunk or 128)
@@ -670,7 +707,8 @@ def run_ours(args, dist: Dist):
                      "train": measure_train(dev, dist, bf16_tflops, hbm_gbs),
                      "ahla": measure_ahla(dev, dist, hbm_gbs, bf16_tflops),
                      "unmasked": measure_unmasked(dev, dist, hbm_gbs),
-                     "hla3": measure_hla3(dev, dist, hbm_gbs)}
+                     "hla3": measure_hla3(dev, dist, hbm_gbs),
+                     "prefill": measure_prefill(dev, dist, hbm_gbs)}
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

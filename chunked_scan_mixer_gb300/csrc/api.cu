@@ -246,8 +246,9 @@ bool tc_disabled() {
 
 Path choose_forward_path(int dtype, int d, int dv, int W, int normalize, bool want_final, const DevInfo& di,
                          bool unmasked = false) {
-    (void)unmasked;  // the tcgen05 kernel has both outputs
-    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !normalize && !want_final && !tc_disabled() &&
+    // The tcgen05 kernels have both outputs; the final state they give for the masked one only.
+    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !normalize && !(want_final && unmasked) &&
+        !tc_disabled() &&
         fwd_chunk_tc_smem() <= (size_t)di.smem_optin && fwd_chunk_tc_available())
         return Path::kTc;
     if (dtype == HLA2_BF16) {
@@ -286,7 +287,13 @@ int check_common(int B, int H, int n, int d, int dv, int dtype, int normalize) {
     return HLA2_OK;
 }
 
-size_t forward_ws(const Plan& p) { return p.nseg > 0 ? fwd_layout(p, p.nseg - 1).total * sizeof(float) : 0; }
+// Summaries kept per head: nseg - 1, or nseg with a final state (the tcgen05 path keeps the last
+// segment's summary for the final combine; the other paths use a part of that space).
+int forward_nsum(const Plan& p, bool want_final) { return want_final ? p.nseg : p.nseg - 1; }
+
+size_t forward_ws(const Plan& p, bool want_final) {
+    return p.nseg > 0 ? fwd_layout(p, forward_nsum(p, want_final)).total * sizeof(float) : 0;
+}
 
 }  // namespace
 
@@ -308,7 +315,8 @@ size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chun
                                     int normalize, int want_final_state) {
     if (check_common(B, H, n, d, dv, dtype, normalize) != HLA2_OK || !dim_ok(chunk)) return (size_t)-1;
     const DevInfo di = dev_info();
-    return forward_ws(forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, di));
+    return forward_ws(forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, di),
+                      want_final_state != 0);
 }
 
 int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
@@ -374,12 +382,15 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     // (which has no flags) covers it: it uses a subset of the masked workspace.
     const Plan p = unmasked ? forward_plan(B, H, n, d, dv, chunk, opts->dtype, normalize, want_final, di)
                             : make_plan(B, H, n, d, dv, chunk, di.sms, forward_per_sm(path, d, dv, chunk, di));
-    const FwdLayout L = fwd_layout(p, p.nseg - 1);
+    const FwdLayout L = fwd_layout(p, forward_nsum(p, want_final));
     const size_t need = L.total * sizeof(float);
     if (!opts->workspace || opts->workspace_bytes < need)
         return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
                     opts->workspace ? opts->workspace_bytes : (size_t)0);
     if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    // tcgen05 path with a final state (masked): every segment's summary is kept, and the last
+    // one is combined with the carry into the last segment after the output pass
+    const bool tc_final = path == Path::kTc && want_final;
 
     ChunkArgs a{};
     a.q = q;
@@ -393,7 +404,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     a.nchunks = p.nchunks;
     a.seg_chunks = p.seg_chunks;
     a.nseg = p.nseg;
-    a.nsum = p.nseg - 1;
+    a.nsum = tc_final ? p.nseg : p.nseg - 1;
     a.gamma = gamma;
     a.normalize = normalize;
     a.eps = opts->eps;
@@ -403,10 +414,10 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     a.unmasked = unmasked ? 1 : 0;
 
     const bool bf = opts->dtype == HLA2_BF16;
-    // tcgen05 path with more than one segment: the summary pass also stores the segment-local
-    // p_t = S_t q_t in out, over every segment, and the output pass starts from it (kOutputP),
-    // so that only Z (unmasked: C) is carried from chunk to chunk there.
-    const bool stored_p = path == Path::kTc && p.nseg > 1;
+    // tcgen05 path with more than one segment (or a final state): the summary pass also stores
+    // the segment-local p_t = S_t q_t in out, over every segment, and the output pass starts from
+    // it (kOutputP), so that only Z (unmasked: C) is carried from chunk to chunk there.
+    const bool stored_p = path == Path::kTc && (p.nseg > 1 || tc_final);
     auto chunk_pass = [&](int seg0, int count, bool summary, bool cm) -> int {
         ChunkArgs b = a;
         b.seg0 = seg0;
@@ -428,10 +439,15 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     mark(0);
     if (launch_init_carry(a, d, dv, opts->init_state, st)) return cuda_fail("carry-in initialisation");
     mark(1);
-    if (p.nseg > 1) {
+    if (tc_final && p.nseg == 1) {  // one segment: its summary and moments for the final combine
+        if (chunk_pass(0, 1, true, true)) return cuda_fail("segment summaries");
+        if (launch_seg_moments64(a, st)) return cuda_fail("segment moments");
+        mark(2);
+    } else if (p.nseg > 1) {
         const int steps = p.nseg - 1, seg_tokens = p.seg_chunks * chunk;
         const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
         if (chunk_pass(0, stored_p ? p.nseg : steps, true, true)) return cuda_fail("segment summaries");
+        if (tc_final && launch_seg_moments64(a, st)) return cuda_fail("segment moments");
         mark(2);
         if (launch_linear_scan(a.ws + L.SB, a.ws + L.Sin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true,
                                gamma, seg_tokens, 1, st))
@@ -465,14 +481,18 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         mark(2);
     }
     mark(3);
-    if (want_final && p.nseg > 1 && !unmasked) {
+    if (want_final && p.nseg > 1 && !unmasked && !tc_final) {
         if (chunk_pass(0, p.nseg - 1, false, false) || chunk_pass(p.nseg - 1, 1, false, true))
             return cuda_fail("output pass");
     } else {
         if (chunk_pass(0, p.nseg, false, want_final)) return cuda_fail("output pass");
     }
     mark(4);
-    if (want_final && launch_finalize(a, d, dv, opts->final_state, st)) return cuda_fail("final state");
+    if (tc_final) {
+        if (launch_final_combine64(a, opts->final_state, st)) return cuda_fail("final state");
+    } else if (want_final && launch_finalize(a, d, dv, opts->final_state, st)) {
+        return cuda_fail("final state");
+    }
     mark(5);
     return succeed();
 }
@@ -501,9 +521,15 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     int rc = check_common(B, H, n, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
     if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
-    const Plan p = forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, dev_info());
+    const DevInfo di = dev_info();
+    const Plan p = forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, di);
     int l = 0;
-    if (p.nseg > 0) {
+    if (p.nseg > 0 && want_final_state &&
+        choose_forward_path(dtype, d, dv, chunk, normalize, true, di) == Path::kTc) {
+        // carry-in, summary, segment moments, output, final combine; S, C, m scans, cross terms,
+        // Z and y scans
+        l = 5 + (p.nseg > 1 ? 6 : 0);
+    } else if (p.nseg > 0) {
         l = 2;                                                   // carry-in, output pass
         if (p.nseg > 1)                                          // summary, S/Z scans, cross; y, C, m scans
             l += 4 + (normalize || want_final_state ? 1 : 0) + (want_final_state ? 2 : 0);

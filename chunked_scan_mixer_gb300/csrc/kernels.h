@@ -185,6 +185,11 @@ int launch_linear_scan(const float* src, float* dst, int BH, int H, int nsteps, 
                        size_t src_head_stride, size_t dst_head_stride, bool store_all,
                        const float* gamma, int step_tokens, int power, cudaStream_t st);
 int launch_cross(const ChunkArgs& a, int d, int dv, bool with_y, cudaStream_t st);
+// Final state on the stored-p path (bf16, d = dv = 64): every segment's query and p moments
+// (m_B, y_B, from q and the p stored in out), then the carry into the last segment combined with
+// its summary and converted to the packed public state (final_state).
+int launch_seg_moments64(const ChunkArgs& a, cudaStream_t st);
+int launch_final_combine64(const ChunkArgs& a, float* final_state, cudaStream_t st);
 int launch_finalize(const ChunkArgs& a, int d, int dv, float* final_state, cudaStream_t st);
 
 // Decode step.

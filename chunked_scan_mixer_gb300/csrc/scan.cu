@@ -184,6 +184,156 @@ __global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int 
     }
 }
 
+// Query and p moments of every segment for the final state of the stored-p path (d = 64, bf16):
+//   m_B[s] = sum_t g^(L-1-t) q_t,   y_B[s] = sum_t g^(2(L-1-t)) p^sl_t,
+// t the token's place in segment s of L tokens, p^sl the segment-local p that the summary pass
+// stored in out (read here before the output pass replaces it).  The tcgen05 summary pass
+// forms S_B, C_B and Z_B but not these two vectors.  One CTA per (segment, head, half of the
+// features); thread (row, j) sums features 32 z + 8j .. +7 over tokens row, row + 64, ...
+__global__ void __launch_bounds__(kThreads) seg_moments64_kernel(const ChunkArgs a) {
+    constexpr int D = 64, HALF = 32, ROWS = kThreads / 4;
+    __shared__ float red_m[ROWS][HALF + 1], red_y[ROWS][HALF + 1];
+    pdl_trigger();
+    pdl_wait();
+    const int s = blockIdx.x, bh = blockIdx.y, z = blockIdx.z, tid = threadIdx.x;
+    const int row = tid / 4, j = tid % 4;
+    const int t0 = s * a.seg_chunks * a.W, t1 = min(t0 + a.seg_chunks * a.W, a.n);
+    const float log2g = log2f(head_decay(a.gamma, bh, a.H));
+    const int f0 = HALF * z + 8 * j;
+    const bf16* q = static_cast<const bf16*>(a.q) + (size_t)bh * a.n * D + f0;
+    const bf16* pp = static_cast<const bf16*>(a.out) + (size_t)bh * a.n * D + f0;
+    float am[8], ay[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) am[u] = ay[u] = 0.f;
+    constexpr int U = 4;  // tokens a thread has in flight (loads issued before use)
+    for (int t = t0 + row; t < t1; t += ROWS * U) {
+        uint4 qv[U], pv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int tu = t + ROWS * u;
+            if (tu < t1) {
+                qv[u] = *reinterpret_cast<const uint4*>(q + (size_t)tu * D);
+                pv[u] = *reinterpret_cast<const uint4*>(pp + (size_t)tu * D);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int tu = t + ROWS * u;
+            if (tu < t1) {
+                const float w = pow_decay(log2g, (float)(t1 - 1 - tu)), w2 = w * w;
+                const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+                const uint32_t pw[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    am[2 * e] += w * __uint_as_float(qw[e] << 16);
+                    am[2 * e + 1] += w * __uint_as_float(qw[e] & 0xFFFF0000u);
+                    ay[2 * e] += w2 * __uint_as_float(pw[e] << 16);
+                    ay[2 * e + 1] += w2 * __uint_as_float(pw[e] & 0xFFFF0000u);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        red_m[row][8 * j + u] = am[u];
+        red_y[row][8 * j + u] = ay[u];
+    }
+    __syncthreads();
+    if (tid < 2 * HALF) {
+        const int f = tid % HALF;
+        float (*red)[HALF + 1] = tid < HALF ? red_m : red_y;
+        float acc = 0.f;
+        for (int r = 0; r < ROWS; ++r) acc += red[r][f];
+        const size_t sb = (size_t)bh * a.nsum + s;
+        a.ws[(tid < HALF ? a.L.mB : a.L.yB) + sb * D + HALF * z + f] = acc;
+    }
+}
+
+// Final state of the stored-p path (d = dv = 64): the carry into the last segment combined with
+// that segment's summary by the masked combine (rho = g^L of the last segment),
+//   S = rho S_in + S_B,  C = rho C_in + C_B,  m = rho m_in + m_B,
+//   Z = rho^2 Z_in + Z_B + rho S_in C_B,  y = rho^2 y_in + y_B + rho S_in m_B,
+// then G = S C - Z and h = S m - y, written as the packed public state.  Four CTAs a head, CTA
+// rb forming rows 16 rb .. 16 rb + 15 of every part; the products run from shared-memory
+// copies (its 16 rows of S_in, then of S, and all of C_B, then of C), thread (r, c) forming
+// row r and columns 4c .. 4c + 3.
+__global__ void __launch_bounds__(kThreads) final_combine64_kernel(const ChunkArgs a, float* final_state) {
+    constexpr int D = 64, RB = 16;
+    __shared__ __align__(16) float Ss[RB * D];
+    __shared__ __align__(16) float Cs[D * D];
+    __shared__ float ms[D], ys[RB];
+    pdl_trigger();
+    pdl_wait();
+    const int rb = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+    const int r0 = RB * rb;
+    const int last = a.nseg - 1;
+    const int L = a.n - last * a.seg_chunks * a.W;
+    const float rho = pow_decay(log2f(head_decay(a.gamma, bh, a.H)), (float)L), rho2 = rho * rho;
+    const size_t ci = (size_t)bh * a.nseg + last, sb = (size_t)bh * a.nsum + last;
+    const float* Sin = a.ws + a.L.Sin + ci * D * D;
+    const float* Zin = a.ws + a.L.Zin + ci * D * D;
+    const float* yin = a.ws + a.L.yin + ci * D;
+    const float* Cin = a.ws + a.L.Clast + (size_t)bh * D * D;
+    const float* min_ = a.ws + a.L.mlast + (size_t)bh * D;
+    const float *SB = a.ws + a.L.SB + sb * D * D, *CB = a.ws + a.L.CB + sb * D * D, *ZB = a.ws + a.L.ZB + sb * D * D;
+    const float *mB = a.ws + a.L.mB + sb * D, *yB = a.ws + a.L.yB + sb * D;
+    float* o = final_state + (size_t)bh * raw_state_floats(D, D);
+    const PackOff po = pack_off(D, D);
+    const int r = tid / 16, c4 = (tid % 16) * 4;  // row r0 + r, columns c4 .. c4 + 3
+    auto product = [&](float (&acc)[4]) {          // acc = (Ss Cs)[r][c4 ..]
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll 8
+        for (int x = 0; x < D; ++x) {
+            const float av = Ss[r * D + x];
+            const float4 bv = *reinterpret_cast<const float4*>(&Cs[x * D + c4]);
+            acc[0] += av * bv.x;
+            acc[1] += av * bv.y;
+            acc[2] += av * bv.z;
+            acc[3] += av * bv.w;
+        }
+    };
+    // Z and y rows from the carry S_in and the last summary's C_B, m_B
+    copy_to_smem<RB * D>(Ss, Sin + (size_t)r0 * D, tid);
+    copy_to_smem<D * D>(Cs, CB, tid);
+    for (int i = tid; i < D; i += kThreads) ms[i] = mB[i];
+    __syncthreads();
+    float zt[4], acc[4];
+    product(acc);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const size_t e = (size_t)(r0 + r) * D + c4 + u;
+        zt[u] = rho2 * Zin[e] + ZB[e] + rho * acc[u];
+    }
+    if (tid < RB) {
+        float t = 0.f;
+        for (int x = 0; x < D; ++x) t += Ss[tid * D + x] * ms[x];
+        ys[tid] = rho2 * yin[r0 + tid] + yB[r0 + tid] + rho * t;
+    }
+    __syncthreads();  // every product of S_in is done
+    // S rows, all of C, and m after the last token (in place); this CTA writes its rows
+    for (int i = tid; i < RB * D; i += kThreads) {
+        Ss[i] = rho * Ss[i] + SB[(size_t)r0 * D + i];
+        o[po.S + (size_t)r0 * D + i] = Ss[i];
+    }
+    for (int i = tid; i < D * D; i += kThreads) {
+        Cs[i] = rho * Cin[i] + Cs[i];
+        if (i >= r0 * D && i < (r0 + RB) * D) o[po.C + i] = Cs[i];
+    }
+    for (int i = tid; i < D; i += kThreads) {
+        ms[i] = rho * min_[i] + ms[i];
+        if (i >= r0 && i < r0 + RB) o[po.m + i] = ms[i];
+    }
+    __syncthreads();
+    product(acc);  // G = S C - Z
+#pragma unroll
+    for (int u = 0; u < 4; ++u) o[po.G + (size_t)(r0 + r) * D + c4 + u] = acc[u] - zt[u];
+    if (tid < RB) {  // h = S m - y
+        float t = 0.f;
+        for (int x = 0; x < D; ++x) t += Ss[tid * D + x] * ms[x];
+        o[po.h + r0 + tid] = t - ys[tid];
+    }
+}
+
 // Raw final (S, C, m, Z, y) -> packed public state (S, C, G = S C - Z, m, h = S m - y).
 __global__ void __launch_bounds__(kThreads)
     finalize_kernel(const ChunkArgs a, int D, int DV, float* final_state) {
@@ -271,6 +421,19 @@ int launch_cross(const ChunkArgs& a, int d, int dv, bool with_y, cudaStream_t st
     HLA2_CROSS(128, 16) HLA2_CROSS(128, 32) HLA2_CROSS(128, 64) HLA2_CROSS(128, 128)
 #undef HLA2_CROSS
     return -1;
+}
+
+int launch_seg_moments64(const ChunkArgs& a, cudaStream_t st) {
+    if (a.nseg <= 0 || a.BH <= 0) return 0;
+    if (launch_pdl(seg_moments64_kernel, dim3(a.nseg, a.BH, 2), dim3(kThreads), 0, st, a) != cudaSuccess) return -1;
+    return finish_launch();
+}
+
+int launch_final_combine64(const ChunkArgs& a, float* final_state, cudaStream_t st) {
+    if (a.nseg <= 0 || a.BH <= 0) return 0;
+    if (launch_pdl(final_combine64_kernel, dim3(4, a.BH), dim3(kThreads), 0, st, a, final_state) != cudaSuccess)
+        return -1;
+    return finish_launch();
 }
 
 int launch_finalize(const ChunkArgs& a, int d, int dv, float* final_state, cudaStream_t st) {

@@ -162,3 +162,64 @@ def test_stored_p_path_continues_from_init_state(masked):
     gd = x["gamma"].double().numpy()
     ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), gd, masked=masked)[:, :, m:]
     assert rel_err(np64(o2.cpu()), ref) <= 2e-2
+
+
+def _unpack(state, d=64):
+    from oracle import hla2_oracle as O
+    return O.unpack_state(np64(state.cpu()), d, d)
+
+
+@pytest.mark.parametrize("B,H,n", [(1, 16, 128 * 40 + 9), (1, 8, 128 * 100 + 1), (2, 8, 100)])
+def test_final_state_on_the_stored_p_path(B, H, n):
+    """The state after the last token from the tcgen05 path (summaries of every segment, their
+    q and p moments, the carry into the last segment combined with its summary): every part
+    (S, C, m, G, h) and the output against the oracle, on multi-segment and one-segment calls."""
+    x = inputs.make_custom(B, H, n, 64, 64, torch.bfloat16, seed=41 + H, gamma=(0.97, 0.9999))
+    g = x["gamma"].cuda()
+    o, fin = hla.forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), gamma=g, chunk=128, return_final_state=True)
+    hla.check_status()
+    gd = x["gamma"].double().numpy()
+    ref, ref_state = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), gd, return_state=True)
+    assert rel_err(np64(o.cpu()), ref) <= 2e-2
+    from oracle import hla2_oracle as O
+    got, want = _unpack(fin), O.unpack_state(ref_state, 64, 64)
+    for key in ("S", "C", "m", "G", "h"):
+        assert rel_err(got[key], want[key]) <= 2e-2, key
+
+
+def test_final_state_with_init_state_and_decode_after():
+    """Prefill at chunk 128 from a carried-in state, with the final state; the decode steps that
+    follow match the oracle run over the whole sequence."""
+    B, H, m, n2, steps = 1, 16, 300, 128 * 40 + 9, 3
+    x = inputs.make_custom(B, H, m + n2 + steps, 64, 64, torch.bfloat16, seed=43, gamma=(0.98, 0.9999))
+    g = x["gamma"].cuda()
+    part = lambda lo, hi: [x[t][:, :, lo:hi].contiguous().cuda() for t in ("q", "k", "v")]
+    _, s1 = hla.forward(*part(0, m), gamma=g, chunk=32, return_final_state=True)
+    o2, s2 = hla.forward(*part(m, m + n2), gamma=g, chunk=128, init_state=s1, return_final_state=True)
+    hla.check_status()
+    gd = x["gamma"].double().numpy()
+    ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), gd)
+    assert rel_err(np64(o2.cpu()), ref[:, :, m:m + n2]) <= 2e-2
+    for t in range(m + n2, m + n2 + steps):
+        q, k, v = part(t, t + 1)
+        o = hla.decode_step(s2, q[:, :, 0], k[:, :, 0], v[:, :, 0], gamma=g)
+        assert rel_err(np64(o.cpu()), ref[:, :, t]) <= 2e-2, t
+
+
+def test_final_state_paths_agree():
+    """tcgen05 and mma.sync final states on the same inputs."""
+    x = inputs.make_custom(2, 8, 128 * 24 + 5, 64, 64, torch.bfloat16, seed=45, gamma=(0.99, 0.9999))
+    g = x["gamma"].cuda()
+    args = (x["q"].cuda(), x["k"].cuda(), x["v"].cuda())
+    _, a = hla.forward(*args, gamma=g, chunk=128, return_final_state=True)
+    old = os.environ.pop("HLA2_KERNEL", None)
+    os.environ["HLA2_KERNEL"] = "mma"
+    try:
+        _, b = hla.forward(*args, gamma=g, chunk=128, return_final_state=True)
+    finally:
+        os.environ.pop("HLA2_KERNEL", None)
+        if old is not None:
+            os.environ["HLA2_KERNEL"] = old
+    ga, gb = _unpack(a), _unpack(b)
+    for key in ("S", "C", "m", "G", "h"):
+        assert rel_err(ga[key], gb[key]) <= 2e-2, key
