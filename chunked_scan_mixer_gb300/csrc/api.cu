@@ -246,9 +246,9 @@ bool tc_disabled() {
 
 Path choose_forward_path(int dtype, int d, int dv, int W, int normalize, bool want_final, const DevInfo& di,
                          bool unmasked = false) {
-    // The tcgen05 kernels have both outputs; the final state they give for the masked one only.
-    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !normalize && !(want_final && unmasked) &&
-        !tc_disabled() &&
+    (void)want_final;
+    (void)unmasked;  // the tcgen05 kernels have both outputs, with or without the final state
+    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !normalize && !tc_disabled() &&
         fwd_chunk_tc_smem() <= (size_t)di.smem_optin && fwd_chunk_tc_available())
         return Path::kTc;
     if (dtype == HLA2_BF16) {

@@ -188,7 +188,8 @@ __global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int 
 //   m_B[s] = sum_t g^(L-1-t) q_t,   y_B[s] = sum_t g^(2(L-1-t)) p^sl_t,
 // t the token's place in segment s of L tokens, p^sl the segment-local p that the summary pass
 // stored in out (read here before the output pass replaces it).  The tcgen05 summary pass
-// forms S_B, C_B and Z_B but not these two vectors.  One CTA per (segment, head, half of the
+// forms S_B, C_B and Z_B but not these two vectors.  The unmasked output carries m in the y
+// slot, so there y_B = m_B and p is not read.  One CTA per (segment, head, half of the
 // features); thread (row, j) sums features 32 z + 8j .. +7 over tokens row, row + 64, ...
 __global__ void __launch_bounds__(kThreads) seg_moments64_kernel(const ChunkArgs a) {
     constexpr int D = 64, HALF = 32, ROWS = kThreads / 4;
@@ -213,16 +214,17 @@ __global__ void __launch_bounds__(kThreads) seg_moments64_kernel(const ChunkArgs
             const int tu = t + ROWS * u;
             if (tu < t1) {
                 qv[u] = *reinterpret_cast<const uint4*>(q + (size_t)tu * D);
-                pv[u] = *reinterpret_cast<const uint4*>(pp + (size_t)tu * D);
+                if (!a.unmasked) pv[u] = *reinterpret_cast<const uint4*>(pp + (size_t)tu * D);
             }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int tu = t + ROWS * u;
             if (tu < t1) {
-                const float w = pow_decay(log2g, (float)(t1 - 1 - tu)), w2 = w * w;
+                const float w = pow_decay(log2g, (float)(t1 - 1 - tu)), w2 = a.unmasked ? w : w * w;
                 const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
-                const uint32_t pw[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
+                const uint32_t pw[4] = {a.unmasked ? qv[u].x : pv[u].x, a.unmasked ? qv[u].y : pv[u].y,
+                                        a.unmasked ? qv[u].z : pv[u].z, a.unmasked ? qv[u].w : pv[u].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     am[2 * e] += w * __uint_as_float(qw[e] << 16);
@@ -250,7 +252,8 @@ __global__ void __launch_bounds__(kThreads) seg_moments64_kernel(const ChunkArgs
 }
 
 // Final state of the stored-p path (d = dv = 64): the carry into the last segment combined with
-// that segment's summary by the masked combine (rho = g^L of the last segment),
+// that segment's summary by the masked combine (rho = g^L of the last segment; the unmasked
+// output adds S, C and m without cross terms),
 //   S = rho S_in + S_B,  C = rho C_in + C_B,  m = rho m_in + m_B,
 //   Z = rho^2 Z_in + Z_B + rho S_in C_B,  y = rho^2 y_in + y_B + rho S_in m_B,
 // then G = S C - Z and h = S m - y, written as the packed public state.  Four CTAs a head, CTA
@@ -279,6 +282,21 @@ __global__ void __launch_bounds__(kThreads) final_combine64_kernel(const ChunkAr
     const float *mB = a.ws + a.L.mB + sb * D, *yB = a.ws + a.L.yB + sb * D;
     float* o = final_state + (size_t)bh * raw_state_floats(D, D);
     const PackOff po = pack_off(D, D);
+    if (a.unmasked) {
+        // unmasked output: S, C (in the Z slots) and m (in the y slots) add up decayed, without
+        // cross terms; G and h are not tracked and are written as 0
+        for (int i = tid; i < RB * D; i += kThreads) {
+            const size_t e = (size_t)r0 * D + i;
+            o[po.S + e] = rho * Sin[e] + SB[e];
+            o[po.C + e] = rho * Zin[e] + ZB[e];
+            o[po.G + e] = 0.f;
+        }
+        for (int i = tid; i < RB; i += kThreads) {
+            o[po.m + r0 + i] = rho * yin[r0 + i] + yB[r0 + i];
+            o[po.h + r0 + i] = 0.f;
+        }
+        return;
+    }
     const int r = tid / 16, c4 = (tid % 16) * 4;  // row r0 + r, columns c4 .. c4 + 3
     auto product = [&](float (&acc)[4]) {          // acc = (Ss Cs)[r][c4 ..]
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;

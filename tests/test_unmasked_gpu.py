@@ -273,3 +273,38 @@ def test_tcgen05_multi_chunk_segments_decay_extremes(gamma):
     o = _run_kernel(x)
     assert torch.isfinite(o.float()).all()
     assert rel_err(np64(o), oracle(x)) <= 2e-2
+
+
+@pytest.mark.parametrize("B,H,n", [(1, 16, 128 * 40 + 9), (2, 8, 100)])
+def test_tcgen05_final_state(B, H, n):
+    """The unmasked final state from the tcgen05 path (chunk 128): S, C, m against the oracle on
+    multi-segment and one-segment calls; G and h are not tracked and come back as 0."""
+    x = inputs.make_custom(B, H, n, 64, 64, torch.bfloat16, seed=55 + H, gamma=(0.97, 0.9999))
+    o, fin = run_gpu(x, chunk=128, return_final_state=True)
+    hla.check_status()
+    ref, ref_state = oracle(x, return_state=True)
+    assert rel_err(np64(o.cpu()), ref) <= 2e-2
+    got = O.unpack_state(np64(fin.cpu()), 64, 64)
+    want = O.unpack_state(ref_state, 64, 64)
+    for key in ("S", "C", "m"):
+        assert rel_err(got[key], want[key]) <= 2e-2, key
+    assert not got["G"].any() and not got["h"].any()
+
+
+def test_tcgen05_prefill_from_state_then_decode():
+    """Unmasked prefill at chunk 128 from a carried-in state, then decode steps, against the
+    oracle over the whole sequence."""
+    B, H, m, n2, steps = 1, 16, 300, 128 * 40 + 9, 3
+    x = inputs.make_custom(B, H, m + n2 + steps, 64, 64, torch.bfloat16, seed=57, gamma=(0.98, 0.9999))
+    g = x["gamma"].cuda()
+    part = lambda lo, hi: [x[t][:, :, lo:hi].contiguous().cuda() for t in ("q", "k", "v")]
+    _, s1 = hla.forward(*part(0, m), gamma=g, chunk=32, return_final_state=True, masked=False)
+    o2, s2 = hla.forward(*part(m, m + n2), gamma=g, chunk=128, init_state=s1, return_final_state=True,
+                         masked=False)
+    hla.check_status()
+    ref = oracle(x)
+    assert rel_err(np64(o2.cpu()), ref[:, :, m:m + n2]) <= 2e-2
+    for t in range(m + n2, m + n2 + steps):
+        q, k, v = part(t, t + 1)
+        o = hla.decode_step(s2, q[:, :, 0], k[:, :, 0], v[:, :, 0], gamma=g, masked=False)
+        assert rel_err(np64(o.cpu()), ref[:, :, t]) <= 2e-2, t
