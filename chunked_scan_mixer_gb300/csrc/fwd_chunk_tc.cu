@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ---------------------------------------------------------------------------------------------
-// Output pass from the stored segment-local p (masked, unnormalised; kOutputP).
+// Output pass from the stored segment-local p (unnormalised; kOutputP; UM = unmasked).
 //
 // The summary pass stores, for every token t of segment s, p^sl_t = S^sl_t q_t, where S^sl is
 // the key moment accumulated from zero at the segment start (bf16, in the output buffer).
@@ -482,8 +482,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 //   EPI-c  out = g^(2(r+1)) Q Z0 + B~ V  (bf16 tile in smem; one TMA tile store writes it over
 //          this chunk's p^sl, already consumed);  Z <- g^(2Wc) Z + dZ  (fp32, 16 columns a
 //          thread);  bf16 Z0 (smem)
-// MMA-a of the next chunk and the next loads overlap EPI-c.  Same roles, bounded waits and
-// two CTAs per SM as the kernel above.
+// MMA-a of the next chunk and the next loads overlap EPI-c.  The unmasked output (UM) forms
+// P Q^T and P C0 instead (C0 in the Z0 slot), masks with g^(r-j), scales by g^(r+1), carries
+// C (decay g^Wc) and takes dC = [Q~^T ; Q~^T] V with Q~ = diag(g^(Wc-1-r)) Q in the P~ slot.
+// Same roles, bounded waits and two CTAs per SM as the kernel above.
 namespace outp {
 
 constexpr uint32_t oQ = 0, oP = kTile, oV = 2 * kTile, oPt = 3 * kTile;
@@ -788,21 +790,25 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ---------------------------------------------------------------------------------------------
-// Summary pass that also stores the segment-local p (masked, unnormalised; kSummaryP).
+// Summary pass that also stores the segment-local p (unnormalised; kSummaryP; UM = unmasked).
 //
 // Same sums as the summary mode above (S, C, Z of the segment from zero), and it writes
-// p^sl_t = S^sl_t q_t (bf16) into the output buffer for the kOutputP pass.  Two changes take
-// work off the chunk-to-chunk chain:
-//   * the key-moment increment is formed as K^T D K = K^_T K^ with K^ = diag(g^((Wc-1-i)/2)) K,
-//     so the raw K slot is free once A~ K has run and the next chunk's Q, K load early;
+// p^sl_t = S^sl_t q_t (bf16) into the output buffer for the kOutputP pass.  The launch covers
+// every segment (the last one for its p, and for the final combine when a final state is
+// wanted).  Work taken off the chunk-to-chunk chain:
+//   * the key-moment increment is formed as K^T D K = K^^T K^ with K^ = diag(g^((Wc-1-i)/2)) K,
+//     so the raw K slot is free once A~ K has run and the next chunk's K loads early;
+//   * P is staged in the raw Q slot (free after A~ K and Q S0) and written by one TMA tile
+//     store; the next chunk's Q loads once that store has read the slot;
 //   * the state products land in T2 | T3, so the next chunk's Q K^T (T0T1) is issued while this
 //     chunk's state update still reads them.
 // Per chunk (local row r):
 //   MMA1  A = Q K^T -> T0T1              (issued during the previous chunk's EPI4)
 //   EPI1  A~ = A * [i <= r] g^(r-i) -> T3;  then Q~ = diag(g^(Wc-1-r)) Q, K^ (smem)
 //   MMA2  A~ K -> T2;  Q S0 -> T0
-//   EPI2  P = g^(r+1) Q S0 + A~ K;  P~ = diag(g^(2(Wc-1-r))) P (smem);  then P -> out
-//   ST    [Q~^T ; P~^T] V -> T2 (dC, dZ);  [K^^T ; K^^T] K^ -> T3 (dS twice)
+//   EPI2  P = g^(r+1) Q S0 + A~ K;  P~ = diag(g^(2(Wc-1-r))) P and P (smem);  P -> out (TMA)
+//   ST    [Q~^T ; P~^T] V -> T2 (dC, dZ; unmasked: [Q~^T ; Q~^T] V, dC twice);
+//         [K^^T ; K^^T] K^ -> T3 (dS twice)
 //   EPI4  S <- g^Wc S + dS,  C <- g^Wc C + dC,  Z <- g^(2Wc) Z + dZ;  bf16 S0 (smem)
 namespace sump {
 
