@@ -239,11 +239,17 @@ def run_reference(args, dist: Dist):
 # ---------------------------------------------------------------------------------
 
 def kernel_source_sha():
+    """Hash of the forward tcgen05 kernel sources with // comments and blank lines left out, so
+    that an edit of comments alone keeps a recorded traffic capture valid."""
     h = hashlib.sha256()
     for rel in ("chunked_scan_mixer_gb300/csrc/fwd_chunk_tc.cu", "chunked_scan_mixer_gb300/csrc/tc_common.cuh",
                 "chunked_scan_mixer_gb300/csrc/common.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            for line in f:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode())
+                    h.update(b"\n")
     return h.hexdigest()[:16]
 
 
