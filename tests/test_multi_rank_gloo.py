@@ -89,3 +89,33 @@ def test_torchrun_reference_arm_prints_once():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_record_survives_comment_edits(tmp_path, monkeypatch):
+    """The recorded DRAM traffic stays valid through an edit of comments or blank lines in
+    the kernel sources and turns null on an edit of code."""
+    import shutil
+    import bench
+
+    rels = ("chunked_scan_mixer_gb300/csrc/fwd_chunk_tc.cu", "chunked_scan_mixer_gb300/csrc/tc_common.cuh",
+            "chunked_scan_mixer_gb300/csrc/common.cuh")
+    for rel in rels + ("profiles/traffic.json",):
+        (tmp_path / rel).parent.mkdir(parents=True, exist_ok=True)
+        shutil.copy(os.path.join(bench.ROOT, rel), tmp_path / rel)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.kernel_source_sha()
+    rec = json.loads((tmp_path / "profiles/traffic.json").read_text())
+    rec["segment_summaries"]["source_sha"] = sha
+    (tmp_path / "profiles/traffic.json").write_text(json.dumps(rec))
+    want = rec["segment_summaries"]["bytes_per_launch"]
+    assert bench.recorded_traffic("segment_summaries") == want
+
+    src = tmp_path / rels[0]
+    text = src.read_text()
+    src.write_text("// an added comment line\n\n" + text.replace("\n", "   // trailing note\n", 3))
+    assert bench.kernel_source_sha() == sha
+    assert bench.recorded_traffic("segment_summaries") == want
+
+    src.write_text(text + "\nstatic int added_code_line = 0;\n")
+    assert bench.kernel_source_sha() != sha
+    assert bench.recorded_traffic("segment_summaries") is None
