@@ -82,8 +82,8 @@ def test_many_segments_long_sequence_fp32():
 
 
 def test_long_context_shapes_bf16():
-    """B=1 H=16 n=65536 d=dv=64 at chunk 128 (the tensor-core mma path; the tcgen05 kernel is
-    the masked output's), every output compared, per head."""
+    """B=1 H=16 n=65536 d=dv=64 at chunk 128 (the tcgen05 stored-p kernels, unmasked variant),
+    every output compared, per head."""
     x = inputs.make("long")
     o = run_gpu(x, chunk=x["chunk"]).cpu()
     ref = oracle(x)
