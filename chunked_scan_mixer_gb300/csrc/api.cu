@@ -277,6 +277,14 @@ Plan forward_plan(int B, int H, int n, int d, int dv, int W, int dtype, int norm
     return make_plan(B, H, n, d, dv, W, di.sms, forward_per_sm(path, d, dv, W, di));
 }
 
+// Chunk width a forward call runs at: the widest one <= chunk with a forward kernel for these
+// sizes (the output does not depend on the width, only the rounding order does); 0 if none.
+int forward_width(int dtype, int d, int dv, int chunk, int normalize, const DevInfo& di) {
+    for (int W = chunk; W >= 16; W /= 2)
+        if (choose_forward_path(dtype, d, dv, W, normalize, false, di) != Path::kNone) return W;
+    return 0;
+}
+
 int check_common(int B, int H, int n, int d, int dv, int dtype, int normalize) {
     if (B < 0 || H < 0 || n < 0) return fail(HLA2_ERR_INVALID_ARG, "B, H, n must be >= 0 (got %d, %d, %d)", B, H, n);
     if ((long)B * H > (1L << 30)) return fail(HLA2_ERR_INVALID_ARG, "B*H too large");
@@ -315,7 +323,8 @@ size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chun
                                     int normalize, int want_final_state) {
     if (check_common(B, H, n, d, dv, dtype, normalize) != HLA2_OK || !dim_ok(chunk)) return (size_t)-1;
     const DevInfo di = dev_info();
-    return forward_ws(forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, di),
+    const int W = forward_width(dtype, d, dv, chunk, normalize, di);
+    return forward_ws(forward_plan(B, H, n, d, dv, W ? W : chunk, dtype, normalize, want_final_state != 0, di),
                       want_final_state != 0);
 }
 
@@ -375,9 +384,12 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         return forward_saving_for_backward(q, k, v, out, B, H, n, d, dv, gamma, normalize, chunk, st, opts);
 
     const DevInfo di = dev_info();
+    {
+        const int W = forward_width(opts->dtype, d, dv, chunk, normalize, di);
+        if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no kernel for dtype %d, d %d, dv %d, chunk %d", opts->dtype, d, dv, chunk);
+        chunk = W;  // everything below runs at the width the kernels cover
+    }
     const Path path = choose_forward_path(opts->dtype, d, dv, chunk, normalize, want_final, di, unmasked);
-    if (path == Path::kNone)
-        return fail(HLA2_ERR_UNSUPPORTED, "no kernel for dtype %d, d %d, dv %d, chunk %d", opts->dtype, d, dv, chunk);
     // The unmasked output keeps the masked call's segmentation, so the workspace query
     // (which has no flags) covers it: it uses a subset of the masked workspace.
     const Plan p = unmasked ? forward_plan(B, H, n, d, dv, chunk, opts->dtype, normalize, want_final, di)
@@ -522,6 +534,7 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     if (rc != HLA2_OK) return rc;
     if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
     const DevInfo di = dev_info();
+    if (const int W = forward_width(dtype, d, dv, chunk, normalize, di)) chunk = W;
     const Plan p = forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, di);
     int l = 0;
     if (p.nseg > 0 && want_final_state &&

@@ -42,7 +42,10 @@
  *   - Supported sizes: d, dv in {16, 32, 64, 128}; chunk in {16, 32, 64, 128};
  *     any n >= 0 (the last chunk may be partial); B, H >= 0.  Pointers must be
  *     16-byte aligned.  A combination the kernels do not cover returns
- *     HLA2_ERR_UNSUPPORTED.
+ *     HLA2_ERR_UNSUPPORTED.  For hla2_forward (and its workspace and plan queries)
+ *     chunk is the widest width used: where no kernel covers (dtype, d, dv) at that
+ *     width, the call runs at the widest smaller one that has a kernel, since the output
+ *     does not depend on the width (only the floating-point summation order does).
  */
 #ifndef HLA2_H_
 #define HLA2_H_

@@ -62,8 +62,8 @@ def test_long_context_full_size():
 @pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("chunk", [16, 32, 64, 128])
 def test_bf16_shapes_and_chunks(d, chunk):
-    if d == 128 and chunk == 128:
-        pytest.skip("not compiled for the tensor-core kernel (shared memory)")
+    # d = 128 at chunk 128 has no kernel (its tiles exceed one CTA's shared memory) and runs
+    # at the widest narrower width that has one
     n = 3 * chunk + 5  # several chunks and a ragged tail
     x = inputs.make_custom(2, 3, n, d, d, torch.bfloat16, seed=d + chunk, gamma=(0.9, 1.0))
     o = run_gpu(x, chunk=chunk).cpu()
@@ -113,6 +113,36 @@ def test_chunk_width_independence_on_gpu():
         assert rel_err(o, ref) <= 2e-2
     for o in outs[1:]:
         assert rel_err(o, outs[0]) <= 2e-2
+
+
+@pytest.mark.parametrize("dtype, d, dv", [(torch.bfloat16, 128, 128), (torch.bfloat16, 128, 32),
+                                           (torch.float32, 128, 128), (torch.float32, 64, 64)])
+def test_chunk_wider_than_the_kernels_runs_narrower(dtype, d, dv):
+    """A chunk width with no forward kernel for these sizes runs at the widest narrower width
+    that has one: the same plan, workspace and output, bit for bit, as asking for that width.
+    (The final state is compared to rounding only: on the legacy tensor-core path its y
+    moment sums row-block partials with shared-memory atomic adds, in no fixed order.)"""
+    x = inputs.make_custom(1, 3, 1000, d, dv, dtype, seed=18, gamma=(0.97, 0.999))
+    got, fin = run_gpu(x, chunk=128, return_final_state=True)
+    # widths round the sums differently, so only the width the call ran at matches bit for bit
+    same = []
+    for W in (64, 32, 16):
+        o, f = run_gpu(x, chunk=W, return_final_state=True)
+        if torch.equal(o, got):
+            same.append((W, f))
+    assert same, "the call at chunk 128 matches no narrower width"
+    W, f = same[0]
+    got_f, want_f = O.unpack_state(np64(fin.cpu()), d, dv), O.unpack_state(np64(f.cpu()), d, dv)
+    for key in ("S", "C", "m", "G", "h"):
+        assert rel_err(got_f[key], want_f[key]) <= 1e-4, key
+    assert hla.forward_plan(1, 3, 1000, d, dv, 128, dtype) == hla.forward_plan(1, 3, 1000, d, dv, W, dtype)
+    assert hla.forward_workspace_bytes(1, 3, 1000, d, dv, 128, dtype) == \
+        hla.forward_workspace_bytes(1, 3, 1000, d, dv, W, dtype)
+    ref, ref_state = oracle(x, return_state=True)
+    assert rel_err(np64(got.cpu()), ref) <= tol_for(dtype)
+    got_s, want_s = O.unpack_state(np64(fin.cpu()), d, dv), O.unpack_state(ref_state, d, dv)
+    for key in ("S", "C", "m", "G", "h"):
+        assert rel_err(got_s[key], want_s[key]) <= tol_for(dtype), key
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])

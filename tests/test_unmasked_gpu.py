@@ -44,8 +44,8 @@ def test_tiny_fp32_against_brute_force():
 @pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("chunk", [16, 32, 64, 128])
 def test_bf16_shapes_and_chunks(d, chunk):
-    if d == 128 and chunk == 128:
-        pytest.skip("not compiled for the tensor-core kernel (shared memory)")
+    # d = 128 at chunk 128 has no kernel (its tiles exceed one CTA's shared memory) and runs
+    # at the widest narrower width that has one
     n = 3 * chunk + 5  # several chunks and a ragged tail
     x = inputs.make_custom(2, 3, n, d, d, torch.bfloat16, seed=d + chunk + 1, gamma=(0.9, 1.0))
     o = run_gpu(x, chunk=chunk).cpu()
