@@ -125,7 +125,7 @@ def backward_case(i):
     dtype = torch.bfloat16 if rng.random() < 0.6 else torch.float32
     d = rng.choice(DIMS)
     dv = d if dtype == torch.bfloat16 or rng.random() < 0.5 else rng.choice(DIMS)
-    chunk = rng.choice((16, 32, 64))
+    chunk = rng.choice(CHUNKS)  # the backward runs at the widest width <= chunk with a kernel
     B, H = rng.choice((1, 2)), rng.choice((1, 2, 3))
     n = max(1, min(_length(rng, chunk), 8000 // (B * H)))
     normalize = rng.random() < 0.3
