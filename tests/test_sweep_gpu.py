@@ -162,3 +162,53 @@ def test_backward_sweep(i):
     for name, gg, rr in zip(("dq", "dk", "dv"), got, ref):
         assert torch.isfinite(gg.float()).all(), (name, c)
         assert rel_err(np64(gg.cpu()), rr) <= tol_for(c["dtype"]), (name, c)
+
+
+def ahla_case(i):
+    rng = random.Random(3000 + i)
+    d = rng.choice(DIMS)
+    normalize = rng.random() < 0.3
+    final = rng.random() < 0.4
+    tc_ok = d == 64 and not normalize and not final  # the tcgen05 AHLA kernel (chunk 128)
+    chunk = rng.choice((32, 64, 128, 128) if tc_ok else (32, 64))
+    B, H = rng.choice((1, 2)), rng.choice((1, 2, 3, 16))
+    n = max(1, min(_length(rng, chunk), 12000 // (B * H)))
+    return dict(d=d, chunk=chunk, B=B, H=H, n=n, normalize=normalize, final=final, gamma=_gamma(rng),
+                prefix=rng.choice((0, 0, rng.randint(1, 200))), seed=11000 + i)
+
+
+def _ahla_state_flat(st):
+    B, H = st["P"].shape[:2]
+    return np.concatenate([st["P"].reshape(B, H, -1), st["E"].reshape(B, H, -1), st["m"], st["n"]], axis=-1)
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_ahla_forward_sweep(i):
+    """The AHLA forward (bf16, d == dv) with the same kind of draws; a carried-in state comes
+    from a GPU prefix call (chunk 64) and the oracle runs over prefix and sequence together."""
+    from oracle import ahla_oracle as A
+
+    c = ahla_case(i)
+    d, m = c["d"], c["prefix"]
+    kw = dict(qk="softplus", v_scale="unit") if c["normalize"] else {}
+    x = inputs.make_custom(c["B"], c["H"], m + c["n"], d, d, torch.bfloat16, seed=c["seed"], gamma=c["gamma"], **kw)
+    g = None if x["gamma"] is None else x["gamma"].cuda()
+    q, k, v = (x[key].cuda() for key in ("q", "k", "v"))
+    init = None
+    if m:
+        _, init = hla.ahla_forward(q[:, :, :m].contiguous(), k[:, :, :m].contiguous(), v[:, :, :m].contiguous(),
+                                   gamma=g, chunk=64, normalize=c["normalize"], return_final_state=True)
+    res = hla.ahla_forward(q[:, :, m:].contiguous(), k[:, :, m:].contiguous(), v[:, :, m:].contiguous(), gamma=g,
+                           chunk=c["chunk"], normalize=c["normalize"], init_state=init,
+                           return_final_state=c["final"])
+    hla.check_status()
+    o, fin = res if c["final"] else (res, None)
+    g64 = None if x["gamma"] is None else x["gamma"].double().numpy()
+    ref_o, st = A.serial_forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), g64, normalize=c["normalize"],
+                                 return_state=True)
+    assert torch.isfinite(o.float()).all(), c
+    assert rel_err(np64(o.cpu()), ref_o[:, :, m:]) <= 2e-2, c
+    if c["final"]:
+        got, ref = np64(fin.cpu()), _ahla_state_flat(st)
+        for lo, hi in ((0, d * d), (d * d, 2 * d * d), (2 * d * d, 2 * d * d + d), (2 * d * d + d, 2 * d * d + 2 * d)):
+            assert rel_err(got[..., lo:hi], ref[..., lo:hi]) <= 2e-2, (lo, c)
