@@ -3,6 +3,7 @@ header declares, and rejects bad arguments on the host before any launch."""
 import ctypes
 
 import pytest
+import torch
 
 import chunked_scan_mixer_gb300 as hla
 from chunked_scan_mixer_gb300.hla2 import EXPORTED_SYMBOLS, Opts
@@ -81,6 +82,19 @@ def test_workspace_query(L):
     assert hla.forward_workspace_bytes(1, 1, 0, 64, 64) == 0
     with pytest.raises(ValueError):
         hla.forward_workspace_bytes(1, 1, 16, 40, 64)
+
+
+@pytest.mark.parametrize("dtype, d, dv", [(torch.bfloat16, 128, 128), (torch.float32, 128, 128),
+                                           (torch.float32, 64, 64)])
+def test_wide_chunk_queries_agree_with_a_narrower_width(L, dtype, d, dv):
+    """A chunk width whose tiles no kernel holds: the workspace and plan queries report the
+    narrower width the call runs at (the same width for both), never an error."""
+    plan128 = hla.forward_plan(2, 3, 1000, d, dv, 128, dtype, want_final_state=True)
+    ws128 = hla.forward_workspace_bytes(2, 3, 1000, d, dv, 128, dtype, want_final_state=True)
+    same = [W for W in (64, 32, 16)
+            if hla.forward_plan(2, 3, 1000, d, dv, W, dtype, want_final_state=True) == plan128
+            and hla.forward_workspace_bytes(2, 3, 1000, d, dv, W, dtype, want_final_state=True) == ws128]
+    assert same and ws128 > 0
 
 
 def test_decode_rejects_bad_arguments(L):
