@@ -324,7 +324,8 @@ size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chun
     if (check_common(B, H, n, d, dv, dtype, normalize) != HLA2_OK || !dim_ok(chunk)) return (size_t)-1;
     const DevInfo di = dev_info();
     const int W = forward_width(dtype, d, dv, chunk, normalize, di);
-    return forward_ws(forward_plan(B, H, n, d, dv, W ? W : chunk, dtype, normalize, want_final_state != 0, di),
+    if (!W) return (size_t)-1;  // hla2_forward rejects these sizes (HLA2_ERR_UNSUPPORTED)
+    return forward_ws(forward_plan(B, H, n, d, dv, W, dtype, normalize, want_final_state != 0, di),
                       want_final_state != 0);
 }
 
@@ -534,7 +535,9 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     if (rc != HLA2_OK) return rc;
     if (!dim_ok(chunk)) return fail(HLA2_ERR_INVALID_ARG, "chunk must be 16, 32, 64 or 128 (got %d)", chunk);
     const DevInfo di = dev_info();
-    if (const int W = forward_width(dtype, d, dv, chunk, normalize, di)) chunk = W;
+    const int W = forward_width(dtype, d, dv, chunk, normalize, di);
+    if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no forward kernel for d %d, dv %d at chunk <= %d", d, dv, chunk);
+    chunk = W;
     const Plan p = forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, di);
     int l = 0;
     if (p.nseg > 0 && want_final_state &&

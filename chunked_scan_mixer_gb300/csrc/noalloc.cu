@@ -15,6 +15,9 @@ namespace hla2 {
 int set_last_error(int code, const char* fmt, ...);
 }
 
+extern "C" int hla2_workspace_status(const void* workspace, hla2_stream_t stream);
+extern "C" int hla2_selftest_wait_timeout(void* workspace, hla2_stream_t stream);
+
 namespace {
 
 constexpr size_t kScratchBytes = 32u << 20;  // 32 MiB
@@ -69,4 +72,21 @@ extern "C" int hla2_forward_noalloc(const void* q, const void* k, const void* v,
     o.workspace = scratch;
     o.workspace_bytes = scratch ? kScratchBytes : 0;
     return hla2_forward(q, k, v, out, B, H, n, d, dv, gamma, normalize, chunk, stream, &o);
+}
+
+// The scratch array starts with the same status word as a caller's workspace; a caller of
+// this entry point has no address for it, so these two read it and run the wait self-test
+// on it for them.
+extern "C" int hla2_noalloc_status(hla2_stream_t stream) {
+    void* scratch = nullptr;
+    const int rc = scratch_pointer(&scratch);
+    if (rc != HLA2_OK) return rc;
+    return hla2_workspace_status(scratch, stream);
+}
+
+extern "C" int hla2_noalloc_selftest_wait_timeout(hla2_stream_t stream) {
+    void* scratch = nullptr;
+    const int rc = scratch_pointer(&scratch);
+    if (rc != HLA2_OK) return rc;
+    return hla2_selftest_wait_timeout(scratch, stream);
 }

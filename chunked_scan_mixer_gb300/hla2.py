@@ -97,6 +97,10 @@ def lib():
         L.hla2_decode_step.restype = I
         L.hla2_forward_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, I, F, P]
         L.hla2_forward_noalloc.restype = I
+        L.hla2_noalloc_status.argtypes = [P]
+        L.hla2_noalloc_status.restype = I
+        L.hla2_noalloc_selftest_wait_timeout.argtypes = [P]
+        L.hla2_noalloc_selftest_wait_timeout.restype = I
         L.hla2_ahla_forward_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
         L.hla2_ahla_forward_workspace_bytes.restype = Z
         L.hla2_ahla_forward.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
@@ -137,7 +141,8 @@ EXPORTED_SYMBOLS = (
     "hla2_state_to_compact", "hla2_state_from_compact", "hla2_ahla_forward_workspace_bytes", "hla2_ahla_forward",
     "hla2_ahla_state_floats", "hla2_ahla_decode_step", "hla2_mq_head_state_floats", "hla2_decode_step_mq",
     "hla2_selftest_wait_timeout", "hla2_hla3_forward_workspace_bytes", "hla2_hla3_forward", "hla2_hla3_decode_step",
-    "hla2_ahla_backward_workspace_bytes", "hla2_ahla_backward",
+    "hla2_ahla_backward_workspace_bytes", "hla2_ahla_backward", "hla2_noalloc_status",
+    "hla2_noalloc_selftest_wait_timeout",
 )
 
 FLAG_COMPACT_STATE = 4

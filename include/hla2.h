@@ -159,7 +159,8 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
  * The segmentation hla2_forward will use for these arguments on the current device:
  * *nseg segments of *seg_chunks chunks per head, and *launches kernel launches per
  * call (normalize and want_final_state as passed to hla2_forward).  Any output pointer
- * may be NULL.  Returns HLA2_OK or HLA2_ERR_INVALID_ARG.  The segmentation is the same
+ * may be NULL.  Returns HLA2_OK, HLA2_ERR_INVALID_ARG, or HLA2_ERR_UNSUPPORTED where no
+ * kernel covers the sizes at any width <= chunk (as hla2_forward).  The segmentation is the same
  * with HLA2_FLAG_UNMASKED; the launch count is the masked output's (the unmasked one
  * needs fewer).
  */
@@ -371,6 +372,25 @@ int hla2_state_from_compact(const float* compact, float* state, int N, int H, in
 int hla2_forward_noalloc(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
                          int d, int dv, const float* gamma, int normalize, int chunk, int dtype,
                          float eps, hla2_stream_t stream);
+
+/*
+ * The status word of the allocation-free entry point's scratch array on the current device
+ * (no counterpart in the paper either).  Its kernels report a bounded device-side wait that
+ * gave up in the first word of their scratch, as hla2_forward does in its workspace; the
+ * caller of hla2_forward_noalloc has no address for that array, so this reads it:
+ * HLA2_OK, or HLA2_ERR_TIMEOUT when a wait of the last hla2_forward_noalloc call on this
+ * device gave up (its output is then not valid).  The next call clears the word, so read
+ * it after a call and before the next one.  Synchronises `stream`.
+ */
+int hla2_noalloc_status(hla2_stream_t stream);
+
+/*
+ * hla2_selftest_wait_timeout run on the allocation-free entry point's scratch array: a
+ * wait that nothing ends gives up and records site 90 there, after which
+ * hla2_noalloc_status reports HLA2_ERR_TIMEOUT until the next hla2_forward_noalloc call.
+ * Asynchronous on `stream`; no fault, and the context stays usable.
+ */
+int hla2_noalloc_selftest_wait_timeout(hla2_stream_t stream);
 
 #ifdef __cplusplus
 }

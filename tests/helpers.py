@@ -40,3 +40,20 @@ def header_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(hla2_[a-z0-9_]+)\s*\(", src)))
+
+
+def state_part_errs(got, want, d, dv):
+    """rel_err of each part (S, C, m, G, h) of packed states [..., d*d + 2*d*dv + 2*d]: a
+    part's error is measured against its own scale, so an error in the small parts (m, h)
+    is not hidden by the large ones."""
+    from oracle import hla2_oracle as O
+
+    g = O.unpack_state(np.asarray(got, dtype=np.float64), d, dv)
+    w = O.unpack_state(np.asarray(want, dtype=np.float64), d, dv)
+    return {key: rel_err(g[key], w[key]) for key in ("S", "C", "m", "G", "h")}
+
+
+def assert_state_parts(got, want, d, dv, tol, what=""):
+    errs = state_part_errs(got, want, d, dv)
+    bad = {k: e for k, e in errs.items() if not e <= tol}
+    assert not bad, f"{what} state parts over {tol}: {bad}"

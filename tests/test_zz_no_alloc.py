@@ -2,9 +2,11 @@
 
 It serves callers that cannot allocate device memory (graph captures, hosts that pass a
 kernel only its inputs and outputs): its scratch is a fixed array inside the library.  Its
-output must match hla2_forward's (which takes a caller-provided workspace) within the bf16
-parity tolerance, on two calls in a row (the array keeps the previous call's contents).
-This file is collected last so that a stop-at-first-failure run has run everything else.
+output must match hla2_forward's (which takes a caller-provided workspace) and the float64
+oracle's within the bf16 parity tolerance, on two calls in a row (the array keeps the
+previous call's contents).  A bounded wait that gives up is reported through the array's
+status word (hla2_noalloc_status).  This file is collected last so that a
+stop-at-first-failure run has run everything else.
 """
 import ctypes
 
@@ -14,12 +16,15 @@ import torch
 import chunked_scan_mixer_gb300 as hla
 from chunked_scan_mixer_gb300 import inputs
 
-from .helpers import np64, rel_err
+from oracle import cref
+
+from .helpers import np32, np64, rel_err
 
 pytestmark = pytest.mark.gpu
 
 HLA2_BF16 = 1
 HLA2_ERR_WORKSPACE = -3
+HLA2_ERR_TIMEOUT = -5
 
 
 def noalloc(q, k, v, gamma, chunk, normalize=False):
@@ -44,6 +49,29 @@ def test_matches_workspace_entry_point_on_two_calls(chunk, normalize):
     second = np64(noalloc(q, k, v, g, chunk, normalize).cpu())
     assert rel_err(first, ref) <= 2e-2
     assert rel_err(second, ref) <= 2e-2
+    oracle = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), x["gamma"].double().numpy(),
+                          normalize=normalize, eps=1e-6)
+    assert rel_err(first, oracle) <= 2e-2
+    assert rel_err(second, oracle) <= 2e-2
+    assert hla.lib().hla2_noalloc_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+
+
+def test_timed_out_wait_in_its_scratch_is_reported():
+    """The bounded-wait self-test run on the library's scratch array: the status query reports
+    the timeout; the next call clears it and is correct again."""
+    L = hla.lib()
+    sh = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    x = inputs.make_custom(1, 2, 700, 64, 64, torch.bfloat16, seed=32, gamma=(0.97, 0.999))
+    q, k, v, g = (x[n].cuda() for n in ("q", "k", "v", "gamma"))
+    noalloc(q, k, v, g, 128)
+    assert L.hla2_noalloc_status(sh) == 0
+    assert L.hla2_noalloc_selftest_wait_timeout(sh) == 0
+    assert L.hla2_noalloc_status(sh) == HLA2_ERR_TIMEOUT  # synchronises: the wait has given up
+    assert b"site 90" in L.hla2_last_error()
+    o = np64(noalloc(q, k, v, g, 128).cpu())
+    assert L.hla2_noalloc_status(sh) == 0
+    ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), x["gamma"].double().numpy())
+    assert rel_err(o, ref) <= 2e-2
 
 
 def test_rejects_sizes_beyond_its_scratch():
