@@ -776,6 +776,155 @@ int backward_reverse_part_f32(const float* q, const float* k, const float* v, co
 }
 
 
+// ---- d = dv = 128 training path on the tcgen05 first-order scan kernel (fo_tc.cu) -----------
+//
+// With LA_g(x, k, v)_t = sum_{i <= t} g^(t-i) (x_t . k_i) v_i (a first-order scan; RLA_g: the
+// reverse one, sum over i >= t), the masked output is two chained scans (section summary §4.2,
+// technical summary item 1): p = LA_g(q, k, k) = S_t q_t and o = LA_{g^2}(q, p, v) = q_t^T Z_t.
+// Its reverse mode is six more:
+//   dp = RLA_{g^2}(v, dO, q)   (= Zh_t v_t,  Zh = sum q dO^T)
+//   dv = RLA_{g^2}(p, q, dO)   (= Zh_t^T p_t)
+//   dk = RLA_g(k, dp, q) + RLA_g(k, q, dp)   (= (Sh_t + Sh_t^T) k_t,  Sh = sum dp q^T)
+//   dq = LA_{g^2}(dO, v, p) + LA_g(dp, k, k)  (= Z_t dO_t + S_t dp_t)
+// Each launch runs every segment of every head with a carry from the other segments.  The
+// carry of a scan whose keys are an earlier launch's output comes from summaries that launch
+// forms over its own output, so every inter-segment scan is a plain decayed prefix.
+// Passes: forward F1 (S summaries), F2 (p, stored, with Z summaries), F3 (o); reverse B1 (Zh
+// summaries), B2 (dp, stored, with Sh summaries), B3 (dv), B4 (dk), B5a (Z dO, stored), B5b (dq).
+
+bool fo_path(int dtype, int d, int dv, int chunk, int normalize, const DevInfo& di) {
+    return dtype == HLA2_BF16 && d == 128 && dv == 128 && chunk >= 128 && !normalize && !tc_disabled() &&
+           fo_tc_available() && fo_tc_max_smem() <= (size_t)di.smem_optin;
+}
+
+Plan fo_plan(int B, int H, int n, const DevInfo& di) { return make_plan(B, H, n, 128, 128, 128, di.sms, 1); }
+
+struct FoLayout {
+    size_t SB, Sin, ZB, Zin, ZhB, Zhend, ShB, Shend;  // byte offsets, fp32 [BH][nseg][128][128]
+    size_t P, dP, dqa;                                // byte offsets, bf16 [BH][n][128]
+    size_t fwd_total, total;                          // bytes kept by the forward; by the backward
+};
+
+FoLayout fo_layout(const Plan& p) {
+    FoLayout L;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t sum = (size_t)p.BH * p.nseg * 128 * 128 * sizeof(float);
+    const size_t tok = (size_t)p.BH * p.n * 128 * sizeof(bf16);
+    size_t o = 256;  // status word
+    L.SB = o;    o = up(o + sum);
+    L.Sin = o;   o = up(o + sum);
+    L.ZB = o;    o = up(o + sum);
+    L.Zin = o;   o = up(o + sum);
+    L.P = o;     o = up(o + tok);
+    L.fwd_total = o;
+    L.ZhB = o;   o = up(o + sum);
+    L.Zhend = o; o = up(o + sum);
+    L.ShB = o;   o = up(o + sum);
+    L.Shend = o; o = up(o + sum);
+    L.dP = o;    o = up(o + tok);
+    L.dqa = o;   o = up(o + tok);
+    L.total = o;
+    return L;
+}
+
+FoArgs fo_args(const Plan& p, const float* gamma, char* ws) {
+    FoArgs a{};
+    a.BH = p.BH;
+    a.H = p.H;
+    a.n = p.n;
+    a.nchunks = p.nchunks;
+    a.seg_chunks = p.seg_chunks;
+    a.nseg = p.nseg;
+    a.gamma = gamma;
+    a.status = reinterpret_cast<int*>(ws);
+    return a;
+}
+
+// Forward scans up to the stored p: S summaries, S carries, p with the Z summaries, Z carries.
+int fo_forward_part(const void* q, const void* k, const void* v, const Plan& p, const float* gamma, char* ws,
+                    const FoLayout& L, cudaStream_t st) {
+    auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+    const size_t E = 128 * 128;
+    const int seg_tokens = p.seg_chunks * p.W;
+    FoArgs a = fo_args(p, gamma, ws);
+    a.pow = 1;
+    a.summary = f(L.SB);
+    if (launch_fo_tc_summary(a, k, nullptr, false, st)) return cuda_fail("key moment summaries");
+    if (launch_fo_zero_first(f(L.Sin), p.BH, p.nseg, a.status, st) ||
+        (p.nseg > 1 && launch_linear_scan(f(L.SB), f(L.Sin), p.BH, p.H, p.nseg - 1, E, p.nseg * E, p.nseg * E, true,
+                                          gamma, seg_tokens, 1, st)))
+        return cuda_fail("key moment scan");
+    a.pow = 1;
+    a.pow_next = 2;
+    a.carry = f(L.Sin);
+    a.carry_mode = 0;
+    a.summary = f(L.ZB);
+    if (launch_fo_tc_out(a, q, k, nullptr, false, 2, v, nullptr, ws + L.P, false, st)) return cuda_fail("p pass");
+    if (launch_fo_zero_first(f(L.Zin), p.BH, p.nseg, nullptr, st) ||
+        (p.nseg > 1 && launch_linear_scan(f(L.ZB), f(L.Zin), p.BH, p.H, p.nseg - 1, E, p.nseg * E, p.nseg * E, true,
+                                          gamma, seg_tokens, 2, st)))
+        return cuda_fail("Z scan");
+    return HLA2_OK;
+}
+
+// F3: o = LA_{g^2}(q, p, v) from the stored p and the Z carries.
+int fo_output_pass(const void* q, const void* v, void* out, const Plan& p, const float* gamma, char* ws,
+                   const FoLayout& L, cudaStream_t st) {
+    FoArgs a = fo_args(p, gamma, ws);
+    a.pow = 2;
+    a.carry = reinterpret_cast<const float*>(ws + L.Zin);
+    a.carry_mode = 0;
+    if (launch_fo_tc_out(a, q, ws + L.P, v, false, 0, nullptr, nullptr, out, false, st)) return cuda_fail("output pass");
+    return HLA2_OK;
+}
+
+// B1 .. B5b from the stored p and the forward carries.
+int fo_reverse_part(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dvv,
+                    const Plan& p, const float* gamma, char* ws, const FoLayout& L, cudaStream_t st) {
+    auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+    const size_t E = 128 * 128;
+    void* P = ws + L.P;
+    void* dP = ws + L.dP;
+    void* dqa = ws + L.dqa;
+    FoArgs a = fo_args(p, gamma, ws);
+    // B1: Zh^T summaries (keys dO, values q), reverse, g^2; then the reverse scan
+    a.pow = 2;
+    a.summary = f(L.ZhB);
+    if (launch_fo_tc_summary(a, dout, q, true, st)) return cuda_fail("Zh summaries");
+    if (launch_reverse_scan(f(L.ZhB), f(L.Zhend), p.BH, p.H, p.nseg, E, gamma, p.n, p.W, p.seg_chunks, 2, st))
+        return cuda_fail("Zh scan");
+    // B2: dp = RLA_{g^2}(v, dO, q), stored; Sh summaries over (dp, q) with g
+    a.pow = 2;
+    a.pow_next = 1;
+    a.carry = f(L.Zhend);
+    a.carry_mode = 0;
+    a.summary = f(L.ShB);
+    if (launch_fo_tc_out(a, v, dout, q, false, 1, nullptr, nullptr, dP, true, st)) return cuda_fail("dp pass");
+    if (launch_reverse_scan(f(L.ShB), f(L.Shend), p.BH, p.H, p.nseg, E, gamma, p.n, p.W, p.seg_chunks, 1, st))
+        return cuda_fail("Sh scan");
+    a.summary = nullptr;
+    // B3: dv = RLA_{g^2}(p, q, dO), carry Zh (the transposed Zh^T)
+    a.pow = 2;
+    a.carry = f(L.Zhend);
+    a.carry_mode = 1;
+    if (launch_fo_tc_out(a, P, q, dout, false, 0, nullptr, nullptr, dvv, true, st)) return cuda_fail("dv pass");
+    // B4: dk = RLA_g(k, dp, q) + RLA_g(k, q, dp), carry Sh + Sh^T
+    a.pow = 1;
+    a.carry = f(L.Shend);
+    a.carry_mode = 2;
+    if (launch_fo_tc_out(a, k, dP, q, true, 0, nullptr, nullptr, dk, true, st)) return cuda_fail("dk pass");
+    // B5a: Z dO = LA_{g^2}(dO, v, p), carry Z^T;  B5b: dq = LA_g(dp, k, k) + that, carry S
+    a.pow = 2;
+    a.carry = f(L.Zin);
+    a.carry_mode = 1;
+    if (launch_fo_tc_out(a, dout, v, P, false, 0, nullptr, nullptr, dqa, false, st)) return cuda_fail("dq pass (Z dO)");
+    a.pow = 1;
+    a.carry = f(L.Sin);
+    a.carry_mode = 0;
+    if (launch_fo_tc_out(a, dP, k, nullptr, false, 0, nullptr, dqa, dq, false, st)) return cuda_fail("dq pass");
+    return HLA2_OK;
+}
+
 int check_backward(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
     int rc = check_common(B, H, n, d, dv, dtype, normalize);
     if (rc != HLA2_OK) return rc;
@@ -811,6 +960,10 @@ int normalised_f32_chunk(int d, int dv, int chunk, const DevInfo& di) {
 }
 
 size_t unnormalised_backward_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype, const DevInfo& di) {
+    if (fo_path(dtype, d, dv, chunk, 0, di)) {
+        const Plan p = fo_plan(B, H, n, di);
+        return p.nseg > 0 ? fo_layout(p).total : 0;
+    }
     const BwdPlan bp = backward_plan(B, H, n, d, dv, chunk, dtype, di);
     if (!bp.W) return (size_t)-1;
     return bp.p.nseg > 0 ? bp.L.total_bytes : 0;
@@ -857,6 +1010,19 @@ int forward_saving_for_backward(const void* q, const void* k, const void* v, voi
         return fail(HLA2_ERR_UNSUPPORTED,
                     "saving for the backward needs bf16, d == dv, normalize == 0 and no init_state / final_state");
     const DevInfo di = dev_info();
+    if (fo_path(opts->dtype, d, dv, chunk, normalize, di)) {
+        const Plan p = fo_plan(B, H, n, di);
+        const FoLayout L = fo_layout(p);
+        if (!opts->workspace || opts->workspace_bytes < L.total)
+            return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required to save for the backward (got %zu)",
+                        L.total, opts->workspace ? opts->workspace_bytes : (size_t)0);
+        if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+        char* ws = static_cast<char*>(opts->workspace);
+        cudaGetLastError();
+        int rc = fo_forward_part(q, k, v, p, gamma, ws, L, st);
+        if (rc == HLA2_OK) rc = fo_output_pass(q, v, out, p, gamma, ws, L, st);
+        return rc == HLA2_OK ? succeed() : rc;
+    }
     const int W = backward_width(d, chunk, di);
     if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no backward kernel for d %d, chunk %d", d, chunk);
     const Plan p = make_plan(B, H, n, d, dv, W, di.sms, backward_per_sm(d, W, di));
@@ -965,6 +1131,24 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
                    launch_convert_f32_bf16(dv32, static_cast<bf16*>(dv_out), rows * dv, s2)))
             return cuda_fail("bf16 gradients");
         return succeed();
+    }
+    if (fo_path(opts->dtype, d, dv, chunk, 0, di)) {
+        const Plan p = fo_plan(B, H, n, di);
+        const FoLayout L = fo_layout(p);
+        if (!opts->workspace || opts->workspace_bytes < L.total)
+            return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.total,
+                        opts->workspace ? opts->workspace_bytes : (size_t)0);
+        if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+        char* ws = static_cast<char*>(opts->workspace);
+        cudaStream_t sf = reinterpret_cast<cudaStream_t>(stream);
+        cudaGetLastError();
+        if (opts->flags & HLA2_FLAG_STATES_SAVED) {
+            if (cudaMemsetAsync(ws, 0, sizeof(int), sf) != cudaSuccess) return cuda_fail("status word");
+        } else if ((rc = fo_forward_part(q, k, v, p, gamma, ws, L, sf)) != HLA2_OK) {
+            return rc;
+        }
+        rc = fo_reverse_part(q, k, v, dout, dq, dk, dv_out, p, gamma, ws, L, sf);
+        return rc == HLA2_OK ? succeed() : rc;
     }
     const BwdPlan bp = backward_plan(B, H, n, d, dv, chunk, opts->dtype, di);
     if (!bp.W) return fail(HLA2_ERR_UNSUPPORTED, "no backward kernel for d %d, dv %d, chunk %d", d, dv, chunk);

@@ -1,0 +1,760 @@
+// First-order chunked linear attention on the 5th-generation tensor cores, d = dv = 128,
+// chunk width 128 (bf16 tiles, fp32 state).  It is the building block of the d = 128
+// training path: the masked HLA-2 output is two chained first-order scans, and so is its
+// reverse mode (page "Higher-order Linear Attention", section summary §4.2: the reverse-mode
+// scan gives the serial recurrence's gradients).
+//
+// With decay g (= gamma or gamma^2 of the head), one launch computes over every segment of
+// every head
+//   forward:  Y_t = sum_{i <= t} g^(t-i) (x_t . k_i) v_i   (+ g^(t-t0+1) x_t^T Sig_in)
+//   reverse:  Y_t = sum_{i >= t} g^(i-t) (x_t . k_i) v_i   (+ g^(t1-t) x_t^T Sig_in)
+// with Sig = sum_i k_i v_i^T decayed to the segment's start (forward) or end (reverse);
+// Sig_in is the carry from the other segments.  Per chunk of W = 128 rows r (Wc valid):
+//   MMA-G  G = X K^T                                     (128 x 128 fp32, tensor memory)
+//   EPI-1  G~ = mask(G) (forward [i <= r] g^(r-i), reverse [i >= r] g^(i-r)), bf16 packed
+//          in tensor memory beside fX = diag(f_r) X (forward f = g^(r+1), reverse
+//          g^(Wc-r)): the A operand of the next product;  K~ = diag(w_i) K in shared memory
+//          (forward w = g^(Wc-1-i), reverse g^i)
+//   MMA-Y  Y = [G~ | fX] [V ; Sig0]                       (one accumulation, K = 256)
+//   MMA-S  dSig = K~^T V
+//   EPI-S  Sig <- g^Wc Sig + dSig  (fp32 registers, 64 a thread), bf16 Sig0 for the next chunk
+//   EPI-Y  Y (+ a partial sum read from global) -> bf16 tile -> one TMA tile store
+// Optional parts, chosen per launch:
+//   * a second key/value pair with the values and keys swapped, (K2, V2) = (V, K), sharing
+//     X and the state: Y = G~1 V + G~2 K + fX Sig0, Sig = sum_i (k_i v_i^T + v_i k_i^T)
+//     (the symmetric pair of the key-gradient scan);
+//   * the next summary: Sig'_B = sum_t w'_t y_t u_t^T over the segment, keys = this launch's
+//     own (bf16) output and values u = one of its inputs or an extra tile, decayed with g'
+//     to the segment's end (forward) or start (reverse) -- the segment summary of the scan
+//     that takes Y as its keys, so that scan needs no cross term;
+//   * a partial output (bf16, same layout) added before the store.
+// The carry Sig_in is read as stored, transposed, or symmetrised (Sig + Sig^T).
+//
+// A second kernel forms segment summaries only: Sig_B = sum_i w_i k_i v_i^T with no chain,
+// the keys scaled in shared memory and the products accumulated in tensor memory.
+//
+// Roles: warp 0 allocates tensor memory and one of its threads issues the TMA loads and every
+// MMA; warps 1..8 move data between tensor memory, registers and shared memory (warp w holds
+// TMEM lanes 32 (w % 4) .. +31 = token / feature rows, and half (w - 1) / 4 of the columns).
+// One CTA per SM (up to 192 KB of shared memory, all 512 tensor-memory columns).  Every
+// wait is bounded; on a timeout the kernel records the site in the status word, drains and
+// exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+#include "tc_common.cuh"
+
+namespace hla2 {
+
+namespace {
+
+namespace la {
+
+constexpr int kW = 128, kD = 128;
+constexpr int kThreads = 288;          // 1 control warp + 8 epilogue warps
+constexpr uint32_t kBlk = 128 * 128;   // one [128 rows][64 bf16] SW128 column block (16 KB)
+constexpr uint32_t kTile = 2 * kBlk;   // a [128][128] bf16 tile: column blocks 0 (cols 0..63) and 1
+constexpr uint32_t kTmemCols = 512;
+
+// Shared-memory plan of the output kernel (byte offsets of 32 KB slots from the 1024-aligned base).
+template <bool R2, bool KVS, bool XVS, bool ADD>
+struct OutLayout {
+    static constexpr uint32_t oQ = 0;
+    static constexpr uint32_t oK = kTile;
+    static constexpr uint32_t oV = KVS ? oK : oK + kTile;
+    static constexpr uint32_t oXV = XVS ? oV + kTile : oV;                    // next summary's values
+    static constexpr uint32_t oAD = (XVS ? oXV : oV) + kTile;                 // partial (ADD)
+    static constexpr uint32_t oKt = ADD ? oAD + kTile : oAD;                  // K~ (and V~ for R2)
+    static constexpr uint32_t oKt2 = oKt + kTile;
+    static constexpr uint32_t oS0 = R2 ? oKt2 + kTile : oKt + kTile;         // bf16 Sig0
+    static constexpr bool kStageInQ = R2;                                     // no room for a stage slot
+    static constexpr uint32_t oST = kStageInQ ? oQ : oS0 + kTile;             // output tile
+    static constexpr uint32_t oGP = (kStageInQ ? oS0 : oST) + kTile;          // g^0 .. g^(2W)
+    static constexpr uint32_t oBar = oGP + 1088;
+    static constexpr uint32_t oMisc = oBar + 16 * 8;
+    static constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;  // + alignment slack
+};
+
+// Tensor-memory columns.  R = 1: G / Y [0,128), A operands [128,256) (G~ | fX), dSig
+// [256,384), next summary [384,512).  R = 2: G1 [0,128), G2 [128,256); after EPI-1 Y [0,128)
+// and dSig [128,256); A operands [256,448) (G~1 | G~2 | fX).
+template <bool R2>
+struct Cols {
+    static constexpr uint32_t TG = 0, TY = 0;
+    static constexpr uint32_t TA = R2 ? 256 : 128;
+    static constexpr uint32_t TX = TA + (R2 ? 128 : 64);  // fX
+    static constexpr uint32_t TS = R2 ? 128 : 256;
+    static constexpr uint32_t TN = 384;
+};
+
+enum Bar { FQ = 0, FK, FV, BG, BGT, BY, BSU, BS, BYT, BN, BSF, kBarCount };
+
+struct Maps {
+    CUtensorMap x, k, v, xv, ad, out;
+};
+
+}  // namespace la
+
+__device__ __forceinline__ float la_bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float la_bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint4 la_scale_chunk(uint4 c, float s) {
+    uint4 o;
+    o.x = pack_bf16x2(s * la_bf_lo(c.x), s * la_bf_hi(c.x));
+    o.y = pack_bf16x2(s * la_bf_lo(c.y), s * la_bf_hi(c.y));
+    o.z = pack_bf16x2(s * la_bf_lo(c.z), s * la_bf_hi(c.z));
+    o.w = pack_bf16x2(s * la_bf_lo(c.w), s * la_bf_hi(c.w));
+    return o;
+}
+
+__device__ __forceinline__ uint4 la_pack8(const float* f) {
+    uint4 o;
+    o.x = pack_bf16x2(f[0], f[1]);
+    o.y = pack_bf16x2(f[2], f[3]);
+    o.z = pack_bf16x2(f[4], f[5]);
+    o.w = pack_bf16x2(f[6], f[7]);
+    return o;
+}
+
+// Byte offset of 16-byte chunk j (0..7) of row r in column block b of a [128][128] tile.
+__device__ __forceinline__ uint32_t la_off(int b, int r, int j) { return (uint32_t)b * la::kBlk + tc::sw128_chunk(r, j); }
+
+// Masked, decayed 32-column block [cb, cb + 32) of Gram row r (fp32 at src in tensor memory),
+// packed to 16 bf16 pairs.  Forward keeps i <= r with g^(r - i); reverse keeps i >= r with
+// g^(i - r).  cb and the warp's first row row0 are multiples of 32, so a block is entirely
+// kept, entirely dropped (written as zeros without reading) or the diagonal block.
+template <bool REV>
+__device__ __forceinline__ void la_masked_pack(uint32_t src, int r, int cb, int row0, float log2g, float g,
+                                               float ginv, uint32_t (&pk)[16]) {
+    const bool dropped = REV ? cb < row0 : cb > row0;
+    if (dropped) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = 0u;
+        return;
+    }
+    uint32_t v[32];
+    tc::tmem_ld32(src, v);
+    tc::tmem_wait_ld();
+    const bool diag = cb == row0;
+    float f = pow_decay(log2g, (float)(REV ? cb - r : r - cb));  // factor at column cb
+    const float step = REV ? g : ginv;
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        float a0 = f * __uint_as_float(v[j]);
+        f *= step;
+        float a1 = f * __uint_as_float(v[j + 1]);
+        f *= step;
+        if (diag) {
+            const int i0 = cb + j, i1 = cb + j + 1;
+            a0 = (REV ? i0 >= r : i0 <= r) ? a0 : 0.f;
+            a1 = (REV ? i1 >= r : i1 <= r) ? a1 : 0.f;
+        }
+        pk[j / 2] = pack_bf16x2(a0, a1);
+    }
+}
+
+// Segment geometry of a CTA.
+struct FoSeg {
+    int c_begin, c_end, nit, t0, L;
+};
+__device__ __forceinline__ FoSeg la_seg(const FoArgs& a, int seg) {
+    FoSeg s;
+    s.c_begin = seg * a.seg_chunks;
+    s.c_end = min(s.c_begin + a.seg_chunks, a.nchunks);
+    s.nit = s.c_end - s.c_begin;
+    s.t0 = s.c_begin * la::kW;
+    s.L = min(s.c_end * la::kW, a.n) - s.t0;
+    return s;
+}
+
+// ----------------------------------------------------------------------------------------
+// Output kernel.  REV: reverse direction.  NSUM: next summary of the output.  R2: the swapped
+// second pair.  KVS: keys and values are the same tensor (one tile).  XVS: the next
+// summary's values are a separate tensor (else the value tile).  ADD: partial added.
+template <bool REV, bool NSUM, bool R2, bool KVS, bool XVS, bool ADD>
+__global__ void __launch_bounds__(la::kThreads, 1)
+    fo_out_tc_kernel(const __grid_constant__ la::Maps maps, const FoArgs a) {
+    using Lay = la::OutLayout<R2, KVS, XVS, ADD>;
+    using C = la::Cols<R2>;
+    constexpr int kW = la::kW;
+    pdl_trigger();
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* gp = reinterpret_cast<float*>(sm + Lay::oGP);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + Lay::oMisc);
+    volatile int* abort = reinterpret_cast<volatile int*>(sm + Lay::oMisc + 4);
+    int* status = a.status;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seg = blockIdx.x, bh = blockIdx.y;
+    const FoSeg sg = la_seg(a, seg);
+    const int nit = sg.nit;
+    const float gam = head_decay(a.gamma, bh, a.H);
+    const float log2g = (float)a.pow * log2f(gam);
+    const float log2gn = (float)a.pow_next * log2f(gam);
+    const float g = exp2f(log2g);
+
+    for (int i = tid; i < 2 * kW + 1; i += la::kThreads) gp[i] = pow_decay(log2g, (float)i);
+    if (tid == 0) {
+        for (int b = 0; b < la::kBarCount; ++b) {
+            const bool from_epilogue = (b == la::BGT || b == la::BS || b == la::BYT);
+            tc::mbar_init(&bars[b], from_epilogue ? 8 : 1);
+        }
+        *abort = 0;
+        tc::mbar_fence_init();
+    }
+    pdl_wait();  // everything below reads what earlier kernels of the stream wrote
+
+    // epilogue thread: TMEM lane / row r, column half h (columns 64h .. 64h+63)
+    const int q4 = warp & 3, h = (warp - 1) >> 2;
+    const int r = 32 * q4 + lane;
+    float sig[64];  // Sig row r, columns 64h ..
+    auto publish_sig = [&]() {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(sm + Lay::oS0 + la_off(h, r, j)) = la_pack8(&sig[8 * j]);
+    };
+
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_holder, la::kTmemCols);
+    } else {
+        // carry-in of the segment (zero without one), as stored, transposed or symmetrised
+        if (a.carry) {
+            const float* src = a.carry + ((size_t)bh * a.nseg + seg) * la::kD * la::kD;
+            if (a.carry_mode == 0) {
+#pragma unroll
+                for (int j = 0; j < 64; j += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(src + (size_t)r * la::kD + 64 * h + j);
+                    sig[j] = x.x, sig[j + 1] = x.y, sig[j + 2] = x.z, sig[j + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) sig[j] = src[(size_t)(64 * h + j) * la::kD + r];
+                if (a.carry_mode == 2) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) sig[j] += src[(size_t)r * la::kD + 64 * h + j];
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) sig[j] = 0.f;
+        }
+        publish_sig();
+        tc::fence_proxy_async();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    auto chunk_of = [&](int it) { return REV ? sg.c_end - 1 - it : sg.c_begin + it; };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ control thread
+        if (lane == 0 && nit > 0) {
+            auto load2 = [&](uint32_t slot, const CUtensorMap* m, int c, uint64_t* bar) {
+                tc::tma_load_3d(sm + slot, m, 0, c * kW, bh, bar);
+                tc::tma_load_3d(sm + slot + la::kBlk, m, 64, c * kW, bh, bar);
+            };
+            auto load_x = [&](int c) {
+                tc::mbar_arrive_expect_tx(&bars[la::FQ], la::kTile);
+                load2(Lay::oQ, &maps.x, c, &bars[la::FQ]);
+            };
+            auto load_k = [&](int c) {
+                tc::mbar_arrive_expect_tx(&bars[la::FK], la::kTile);
+                load2(Lay::oK, &maps.k, c, &bars[la::FK]);
+            };
+            constexpr int kVTiles = (KVS ? 0 : 1) + (XVS ? 1 : 0) + (ADD ? 1 : 0);
+            auto load_v = [&](int c) {
+                if (kVTiles == 0) return;
+                tc::mbar_arrive_expect_tx(&bars[la::FV], kVTiles * la::kTile);
+                if (!KVS) load2(Lay::oV, &maps.v, c, &bars[la::FV]);
+                if (XVS) load2(Lay::oXV, &maps.xv, c, &bars[la::FV]);
+                if (ADD) load2(Lay::oAD, &maps.ad, c, &bars[la::FV]);
+            };
+            const uint32_t sX = smem_u32(sm + Lay::oQ), sK = smem_u32(sm + Lay::oK), sV = smem_u32(sm + Lay::oV);
+            const uint32_t sKt = smem_u32(sm + Lay::oKt), sKt2 = smem_u32(sm + Lay::oKt2);
+            const uint32_t sS0 = smem_u32(sm + Lay::oS0), sST = smem_u32(sm + Lay::oST);
+            const uint32_t sXV = smem_u32(sm + Lay::oXV);
+            constexpr uint32_t I_KK = tc::idesc_bf16(128, 128, 0, 0);  // K-major x K-major
+            constexpr uint32_t I_TM = tc::idesc_bf16(128, 128, 0, 1);  // A (TMEM, K-major) x MN-major B
+            constexpr uint32_t I_MM = tc::idesc_bf16(128, 128, 1, 1);  // MN-major x MN-major
+            // K-major operand, K = 128 features in two column blocks; MN-major, K = 128 tokens
+            auto kdesc = [](uint32_t base, int ks) {
+                return tc::smem_desc(base + (uint32_t)(ks >> 2) * la::kBlk + (uint32_t)(ks & 3) * 32, 16, 1024);
+            };
+            auto mdesc = [](uint32_t base, int ks) { return tc::smem_desc(base + 2048u * ks, la::kBlk, 1024); };
+
+            load_x(chunk_of(0));
+            load_k(chunk_of(0));
+            load_v(chunk_of(0));
+            int lx = 1, lk = 1, lv = 1;
+            for (int it = 0; it < nit; ++it) {
+                const uint32_t ph = it & 1;
+                tc::mbar_wait(&bars[la::FQ], ph, abort, status, 101);
+                tc::mbar_wait(&bars[la::FK], ph, abort, status, 102);
+                if (kVTiles > 0 && R2) tc::mbar_wait(&bars[la::FV], ph, abort, status, 103);
+                tc::fence_after_sync();
+                // MMA-G: G = X K^T (R2: and X V^T)
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem + C::TG, kdesc(sX, ks), kdesc(sK, ks), I_KK, ks > 0);
+                if (R2)
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_ss(tmem + C::TG + 128, kdesc(sX, ks), kdesc(sV, ks), I_KK, ks > 0);
+                tc::mma_commit(&bars[la::BG]);
+                tc::mbar_wait(&bars[la::BGT], ph, abort, status, 104);  // G read; G~, fX, K~ written
+                if (!Lay::kStageInQ && it + 1 < nit) {  // X no longer read
+                    load_x(chunk_of(it + 1));
+                    ++lx;
+                }
+                if (!KVS && !R2) tc::mbar_wait(&bars[la::FV], ph, abort, status, 105);  // the value tile
+                if (it > 0) tc::mbar_wait(&bars[la::BS], ph ^ 1, abort, status, 106);  // Sig0 of this chunk
+                tc::fence_after_sync();
+                // MMA-Y: Y = [G~ | (G~2) | fX] [V ; (K) ; Sig0]
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ts(tmem + C::TY, tmem + C::TA + 8 * ks, mdesc(sV, ks), I_TM, ks > 0);
+                if (R2)
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_ts(tmem + C::TY, tmem + C::TA + 64 + 8 * ks, mdesc(sK, ks), I_TM, 1);
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ts(tmem + C::TY, tmem + C::TX + 8 * ks, mdesc(sS0, ks), I_TM, 1);
+                tc::mma_commit(&bars[la::BY]);
+                // MMA-S: dSig = K~^T V (R2: + V~^T K)
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem + C::TS, mdesc(sKt, ks), mdesc(sV, ks), I_MM, ks > 0);
+                if (R2)
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_ss(tmem + C::TS, mdesc(sKt2, ks), mdesc(sK, ks), I_MM, 1);
+                tc::mma_commit(&bars[la::BSU]);
+                tc::mbar_wait(&bars[la::BSU], ph, abort, status, 107);  // K, V, K~, Sig0 no longer read
+                if (it + 1 < nit) {
+                    load_k(chunk_of(it + 1));
+                    ++lk;
+                }
+                const bool v_late = NSUM || ADD;  // the value group is still read after MMA-S
+                if (!v_late && it + 1 < nit && kVTiles > 0) {
+                    load_v(chunk_of(it + 1));
+                    ++lv;
+                }
+                tc::mbar_wait(&bars[la::BYT], ph, abort, status, 108);  // output tile staged
+                tc::fence_after_sync();
+                const int c = chunk_of(it);
+                tc::tma_store_3d(&maps.out, sm + Lay::oST, 0, c * kW, bh);
+                tc::tma_store_3d(&maps.out, sm + Lay::oST + la::kBlk, 64, c * kW, bh);
+                tc::bulk_commit();
+                if (NSUM) {  // next summary: T_N += Y^T (w' U)
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_ss(tmem + C::TN, mdesc(sST, ks), mdesc(sXV, ks), I_MM, (it > 0 || ks > 0) ? 1u : 0u);
+                    tc::mma_commit(&bars[la::BN]);
+                    tc::mbar_wait(&bars[la::BN], ph, abort, status, 109);
+                }
+                if (v_late && it + 1 < nit && kVTiles > 0) {
+                    load_v(chunk_of(it + 1));
+                    ++lv;
+                }
+                tc::bulk_wait_read_all();  // the output tile has been read
+                if (Lay::kStageInQ && it + 1 < nit) {
+                    load_x(chunk_of(it + 1));
+                    ++lx;
+                }
+                tc::mbar_arrive(&bars[la::BSF]);
+            }
+            // drain (bounded, ignoring the abort flag) so that nothing is in flight at exit
+            volatile int never = 0;
+            tc::mbar_wait(&bars[la::BSU], (nit - 1) & 1, &never, nullptr, 0);
+            if (NSUM) tc::mbar_wait(&bars[la::BN], (nit - 1) & 1, &never, nullptr, 0);
+            tc::mbar_wait(&bars[la::FQ], (lx - 1) & 1, &never, nullptr, 0);
+            tc::mbar_wait(&bars[la::FK], (lk - 1) & 1, &never, nullptr, 0);
+            if (kVTiles > 0) tc::mbar_wait(&bars[la::FV], (lv - 1) & 1, &never, nullptr, 0);
+            tc::bulk_wait_all();
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue warps
+        const int row0 = 32 * q4;
+        const uint32_t lrow = tmem + ((uint32_t)row0 << 16);
+        const float ginv = g > 0.f ? 1.f / g : 0.f;
+        unsigned char* sX = sm + Lay::oQ;
+        unsigned char* sK = sm + Lay::oK;
+        unsigned char* sV = sm + Lay::oV;
+        for (int it = 0; it < nit; ++it) {
+            const uint32_t ph = it & 1;
+            const int c = chunk_of(it);
+            const int Wc = min(kW, a.n - c * kW);
+            const bool live = r < Wc;
+            // ---- EPI-1: G~ (and G~2), fX -> tensor memory;  K~ (and V~) -> shared memory -------------
+            tc::mbar_wait(&bars[la::FQ], ph, abort, status, 111);
+            tc::mbar_wait(&bars[la::FK], ph, abort, status, 112);
+            if (R2) tc::mbar_wait(&bars[la::FV], ph, abort, status, 113);
+            tc::mbar_wait(&bars[la::BG], ph, abort, status, 114);
+            tc::fence_after_sync();
+#pragma unroll
+            for (int gi = 0; gi < (R2 ? 2 : 1); ++gi) {
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int cb = 64 * h + 32 * p;
+                    uint32_t pk[16];
+                    la_masked_pack<REV>(lrow + C::TG + 128 * gi + cb, r, cb, row0, log2g, g, ginv, pk);
+                    tc::tmem_st16(lrow + C::TA + 64 * gi + cb / 2, pk);
+                }
+            }
+            {
+                const float f = live ? (REV ? gp[Wc - r] : gp[r + 1]) : 0.f;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 x =
+                            la_scale_chunk(*reinterpret_cast<const uint4*>(sX + la_off(h, r, 4 * half + j)), f);
+                        pk[4 * j] = x.x, pk[4 * j + 1] = x.y, pk[4 * j + 2] = x.z, pk[4 * j + 3] = x.w;
+                    }
+                    tc::tmem_st16(lrow + C::TX + 32 * h + 16 * half, pk);
+                }
+                const float w = live ? (REV ? gp[r] : gp[Wc - 1 - r]) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t off = la_off(h, r, j);
+                    *reinterpret_cast<uint4*>(sm + Lay::oKt + off) =
+                        la_scale_chunk(*reinterpret_cast<const uint4*>(sK + off), w);
+                    if (R2)
+                        *reinterpret_cast<uint4*>(sm + Lay::oKt2 + off) =
+                            la_scale_chunk(*reinterpret_cast<const uint4*>(sV + off), w);
+                }
+            }
+            tc::tmem_wait_st();
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[la::BGT]);
+
+            // ---- EPI-S: Sig <- g^Wc Sig + dSig;  bf16 Sig0 for the next chunk ------------------------
+            tc::mbar_wait(&bars[la::BSU], ph, abort, status, 115);
+            tc::fence_after_sync();
+            {
+                const float rho = gp[Wc];
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lrow + C::TS + 64 * h + 32 * p, v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sig[32 * p + j] = rho * sig[32 * p + j] + __uint_as_float(v[j]);
+                }
+                if (it + 1 < nit) publish_sig();  // MMA-Y of this chunk has completed (commit order)
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[la::BS]);
+
+            // ---- EPI-Y: Y (+ partial) -> bf16 output tile;  next summary's values scaled ----------------
+            if (it > 0) tc::mbar_wait(&bars[la::BSF], ph ^ 1, abort, status, 116);  // previous tile read
+            if (ADD || (NSUM && XVS)) tc::mbar_wait(&bars[la::FV], ph, abort, status, 117);
+            tc::fence_after_sync();
+            {
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lrow + C::TY + 64 * h + 32 * p, v);
+                    tc::tmem_wait_ld();
+                    float y[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[j]);
+                    if (ADD) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 x = *reinterpret_cast<const uint4*>(sm + Lay::oAD + la_off(h, r, 4 * p + j));
+                            const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                y[8 * j + 2 * u] += la_bf_lo(xw[u]);
+                                y[8 * j + 2 * u + 1] += la_bf_hi(xw[u]);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(sm + Lay::oST + la_off(h, r, 4 * p + j)) = la_pack8(&y[8 * j]);
+                }
+                if (NSUM) {
+                    const int pos = (c - sg.c_begin) * kW + r;  // token position in the segment
+                    const float wn = live ? pow_decay(log2gn, (float)(REV ? pos : sg.L - 1 - pos)) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t off = la_off(h, r, j);
+                        *reinterpret_cast<uint4*>(sm + Lay::oXV + off) =
+                            la_scale_chunk(*reinterpret_cast<const uint4*>(sm + Lay::oXV + off), wn);
+                    }
+                }
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[la::BYT]);
+        }
+        if (NSUM && nit > 0) {  // the segment's next summary -> global (fp32)
+            tc::mbar_wait(&bars[la::BN], (nit - 1) & 1, abort, status, 118);
+            tc::fence_after_sync();
+            float* dst = a.summary + ((size_t)bh * a.nseg + seg) * la::kD * la::kD + (size_t)r * la::kD + 64 * h;
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                uint32_t v[32];
+                tc::tmem_ld32(lrow + C::TN + 64 * h + 32 * p, v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(dst + 32 * p + j) =
+                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                    __uint_as_float(v[j + 3]));
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, la::kTmemCols);
+}
+
+// ----------------------------------------------------------------------------------------
+// Summary kernel: Sig_B[s] = sum_{i in s} w_i k_i v_i^T, w_i = g^(t1-1-i) (forward, decayed
+// to the segment's end) or g^(i-t0) (reverse, to its start).  Two stages of tiles; per chunk
+// the epilogue scales K into K~ and the control thread accumulates K~^T V in tensor memory.
+namespace las {
+template <bool KVS>
+struct Layout {
+    static constexpr uint32_t oK = 0;                                 // 2 stages
+    static constexpr uint32_t oV = KVS ? oK : oK + 2 * la::kTile;     // 2 stages
+    static constexpr uint32_t oKt = (KVS ? oK : oV) + 2 * la::kTile;  // 2 stages
+    static constexpr uint32_t oBar = oKt + 2 * la::kTile;
+    static constexpr uint32_t oMisc = oBar + 16 * 8;
+    static constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
+};
+enum Bar { F0 = 0, F1, T0, T1, N0, N1, kBarCount };
+}  // namespace las
+
+template <bool REV, bool KVS>
+__global__ void __launch_bounds__(la::kThreads, 1)
+    fo_sum_tc_kernel(const __grid_constant__ la::Maps maps, const FoArgs a) {
+    using Lay = las::Layout<KVS>;
+    constexpr int kW = la::kW;
+    pdl_trigger();
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Lay::oBar);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + Lay::oMisc);
+    volatile int* abort = reinterpret_cast<volatile int*>(sm + Lay::oMisc + 4);
+    int* status = a.status;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seg = blockIdx.x, bh = blockIdx.y;
+    const FoSeg sg = la_seg(a, seg);
+    const int nit = sg.nit;
+    const float log2g = (float)a.pow * log2f(head_decay(a.gamma, bh, a.H));
+
+    if (tid == 0) {
+        for (int b = 0; b < las::kBarCount; ++b) tc::mbar_init(&bars[b], (b == las::T0 || b == las::T1) ? 8 : 1);
+        *abort = 0;
+        tc::mbar_fence_init();
+    }
+    pdl_wait();
+    if (warp == 0) tc::tmem_alloc(tmem_holder, 128);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+    auto chunk_of = [&](int it) { return REV ? sg.c_end - 1 - it : sg.c_begin + it; };
+
+    if (warp == 0) {
+        if (lane == 0 && nit > 0) {
+            auto load = [&](int it) {
+                const int s = it & 1, c = chunk_of(it);
+                uint64_t* bar = &bars[las::F0 + s];
+                tc::mbar_arrive_expect_tx(bar, (KVS ? 1 : 2) * la::kTile);
+                const uint32_t ok = Lay::oK + s * la::kTile, ov = Lay::oV + s * la::kTile;
+                tc::tma_load_3d(sm + ok, &maps.k, 0, c * kW, bh, bar);
+                tc::tma_load_3d(sm + ok + la::kBlk, &maps.k, 64, c * kW, bh, bar);
+                if (!KVS) {
+                    tc::tma_load_3d(sm + ov, &maps.v, 0, c * kW, bh, bar);
+                    tc::tma_load_3d(sm + ov + la::kBlk, &maps.v, 64, c * kW, bh, bar);
+                }
+            };
+            constexpr uint32_t I_MM = tc::idesc_bf16(128, 128, 1, 1);
+            auto mdesc = [](uint32_t base, int ks) { return tc::smem_desc(base + 2048u * ks, la::kBlk, 1024); };
+            load(0);
+            if (nit > 1) load(1);
+            for (int it = 0; it < nit; ++it) {
+                const int s = it & 1;
+                const uint32_t ph = (it >> 1) & 1;
+                tc::mbar_wait(&bars[las::T0 + s], ph, abort, status, 121);  // K~ of this chunk written
+                tc::fence_after_sync();
+                const uint32_t sKt = smem_u32(sm + Lay::oKt + s * la::kTile);
+                const uint32_t sV = smem_u32(sm + Lay::oV + s * la::kTile);
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem, mdesc(sKt, ks), mdesc(sV, ks), I_MM, (it > 0 || ks > 0) ? 1u : 0u);
+                tc::mma_commit(&bars[las::N0 + s]);
+                if (it + 2 < nit) {  // this stage's tiles are free once its product has run
+                    tc::mbar_wait(&bars[las::N0 + s], ph, abort, status, 122);
+                    load(it + 2);
+                }
+            }
+            volatile int never = 0;
+            tc::mbar_wait(&bars[las::N0 + ((nit - 1) & 1)], ((nit - 1) >> 1) & 1, &never, nullptr, 0);
+            if (nit > 1) tc::mbar_wait(&bars[las::N0 + ((nit - 2) & 1)], ((nit - 2) >> 1) & 1, &never, nullptr, 0);
+        }
+        __syncwarp();
+    } else {
+        const int q4 = warp & 3, h = (warp - 1) >> 2;
+        const int r = 32 * q4 + lane;
+        const uint32_t lrow = tmem + ((uint32_t)(32 * q4) << 16);
+        for (int it = 0; it < nit; ++it) {
+            const int s = it & 1;
+            const uint32_t ph = (it >> 1) & 1;
+            const int c = chunk_of(it);
+            const int Wc = min(kW, a.n - c * kW);
+            tc::mbar_wait(&bars[las::F0 + s], ph, abort, status, 123);
+            const int pos = (c - sg.c_begin) * kW + r;
+            const float w = r < Wc ? pow_decay(log2g, (float)(REV ? pos : sg.L - 1 - pos)) : 0.f;
+            unsigned char* sK = sm + Lay::oK + s * la::kTile;
+            unsigned char* sKt = sm + Lay::oKt + s * la::kTile;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t off = la_off(h, r, j);
+                *reinterpret_cast<uint4*>(sKt + off) = la_scale_chunk(*reinterpret_cast<const uint4*>(sK + off), w);
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[las::T0 + s]);
+        }
+        if (nit > 0) {
+            tc::mbar_wait(&bars[las::N0 + ((nit - 1) & 1)], ((nit - 1) >> 1) & 1, abort, status, 124);
+            tc::fence_after_sync();
+            float* dst = a.summary + ((size_t)bh * a.nseg + seg) * la::kD * la::kD + (size_t)r * la::kD + 64 * h;
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                uint32_t v[32];
+                tc::tmem_ld32(lrow + 64 * h + 32 * p, v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(dst + 32 * p + j) =
+                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                    __uint_as_float(v[j + 3]));
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+}
+
+// Zeroes the carry into segment 0 of every head ([BH][nseg][d*d], segment 0) and clears the
+// status word, before a forward linear scan fills the other segments.
+__global__ void fo_zero_first_kernel(float* carry, int nseg, int* status) {
+    pdl_trigger();
+    pdl_wait();
+    const int bh = blockIdx.x;
+    float4* dst = reinterpret_cast<float4*>(carry + (size_t)bh * nseg * la::kD * la::kD);
+    for (int i = threadIdx.x; i < la::kD * la::kD / 4; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (bh == 0 && threadIdx.x == 0 && status) *status = 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 la_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// [BH][n][128] bf16, box [1][128][64] (128-byte rows), 128-byte swizzle; rows past n read as
+// zero and are not written by stores.
+bool la_map(CUtensorMap* m, const void* ptr, int BH, int n) {
+    auto fn = la_encode_fn();
+    if (!fn || !ptr) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)la::kD, (cuuint64_t)n, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)la::kD * 2, (cuuint64_t)n * la::kD * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)la::kW, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename K>
+int la_launch(K kfn, uint32_t smem, const la::Maps& maps, const FoArgs& a, cudaStream_t st) {
+    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return -1;
+    if (launch_pdl(kfn, dim3(a.nseg, a.BH), dim3(la::kThreads), smem, st, maps, a) != cudaSuccess) return -1;
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+bool fo_tc_available() { return la_encode_fn() != nullptr; }
+
+size_t fo_tc_max_smem() {
+    return la::OutLayout<true, false, false, false>::kSmemBytes > la::OutLayout<false, false, true, true>::kSmemBytes
+               ? la::OutLayout<true, false, false, false>::kSmemBytes
+               : la::OutLayout<false, false, true, true>::kSmemBytes;
+}
+
+int launch_fo_zero_first(float* carry, int BH, int nseg, int* status, cudaStream_t st) {
+    if (BH <= 0) return 0;
+    if (launch_pdl(fo_zero_first_kernel, dim3(BH), dim3(256), 0, st, carry, nseg, status) != cudaSuccess) return -1;
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_fo_tc_summary(const FoArgs& a, const void* k, const void* v, bool reverse, cudaStream_t st) {
+    if (a.BH <= 0 || a.nseg <= 0) return 0;
+    la::Maps m{};
+    if (!la_map(&m.k, k, a.BH, a.n) || !la_map(&m.v, v ? v : k, a.BH, a.n)) return -2;
+    const bool kvs = !v || v == k;
+    if (kvs)
+        return reverse ? la_launch(fo_sum_tc_kernel<true, true>, las::Layout<true>::kSmemBytes, m, a, st)
+                       : la_launch(fo_sum_tc_kernel<false, true>, las::Layout<true>::kSmemBytes, m, a, st);
+    return reverse ? la_launch(fo_sum_tc_kernel<true, false>, las::Layout<false>::kSmemBytes, m, a, st)
+                   : la_launch(fo_sum_tc_kernel<false, false>, las::Layout<false>::kSmemBytes, m, a, st);
+}
+
+// Output launch.  x, k, v: queries, keys, values ([BH][n][128] bf16); v == nullptr: the values
+// are the key tile.  r2: the swapped second pair.  next_sum: 0 none, 1 over (out, the value
+// tile), 2 over (out, xv).  add: partial added to the output (nullptr: none).
+int launch_fo_tc_out(const FoArgs& a, const void* x, const void* k, const void* v, bool r2, int next_sum,
+                     const void* xv, const void* add, void* out, bool reverse, cudaStream_t st) {
+    if (a.BH <= 0 || a.nseg <= 0) return 0;
+    la::Maps m{};
+    const bool kvs = v == nullptr, nsum = next_sum != 0, xvs = next_sum == 2, addp = add != nullptr;
+    if (!la_map(&m.x, x, a.BH, a.n) || !la_map(&m.k, k, a.BH, a.n) || !la_map(&m.v, kvs ? k : v, a.BH, a.n) ||
+        !la_map(&m.out, out, a.BH, a.n))
+        return -2;
+    if (xvs && !la_map(&m.xv, xv, a.BH, a.n)) return -2;
+    if (addp && !la_map(&m.ad, add, a.BH, a.n)) return -2;
+    if (nsum && !a.summary) return -2;
+#define HLA2_LA(REV, NSUM, R2, KVS, XVS, ADD)                                                               \
+    if (reverse == REV && nsum == NSUM && r2 == R2 && kvs == KVS && xvs == XVS && addp == ADD)             \
+        return la_launch(fo_out_tc_kernel<REV, NSUM, R2, KVS, XVS, ADD>,                                      \
+                         la::OutLayout<R2, KVS, XVS, ADD>::kSmemBytes, m, a, st);
+    // the passes of the d = 128 training path
+    HLA2_LA(false, true, false, true, true, false)    // p = LA(q, k, k), next summary over (p, v)
+    HLA2_LA(false, false, false, false, false, false) // o = LA(q, p, v);  dq_a = LA(dO, v, p)
+    HLA2_LA(true, true, false, false, false, false)   // dp = RLA(v, dO, q), next summary over (dp, q)
+    HLA2_LA(true, false, false, false, false, false)  // dv = RLA(p, q, dO)
+    HLA2_LA(true, false, true, false, false, false)   // dk = RLA(k, dp, q) + RLA(k, q, dp)
+    HLA2_LA(false, false, false, true, false, true)   // dq = LA(dp, k, k) + dq_a
+#undef HLA2_LA
+    return -3;  // combination not instantiated
+}
+
+}  // namespace hla2

@@ -256,6 +256,29 @@ int launch_unit_rows(void* e0, size_t rows, int w, bool is_bf16, cudaStream_t st
 int launch_divide_rows(void* out, const void* den, size_t rows, int dv, int w, float eps, bool is_bf16,
                        cudaStream_t st);
 
+// tcgen05 first-order chunked scan, d = dv = 128, chunk 128 (fo_tc.cu): the building block of
+// the d = 128 training path.  One launch runs every segment of every head ([BH] x [nseg] CTAs).
+struct FoArgs {
+    int BH, H, n, nchunks, seg_chunks, nseg;
+    const float* gamma;   // per head [H] (NULL: 1); the scan's decay is gamma^pow
+    int pow, pow_next;    // decay powers of the scan and of its next summary
+    const float* carry;   // [BH][nseg][128*128] carry into each segment (NULL: zero)
+    int carry_mode;       // 0 as stored, 1 transposed, 2 symmetrised (carry + carry^T)
+    float* summary;       // [BH][nseg][128*128] segment summaries written (summary launch / next summary)
+    int* status;          // bounded-wait status word
+};
+bool fo_tc_available();
+size_t fo_tc_max_smem();
+// carry[bh][0] = 0 for every head (and *status = 0)
+int launch_fo_zero_first(float* carry, int BH, int nseg, int* status, cudaStream_t st);
+// summary[s] = sum_{i in s} g^(distance to the segment's end (forward) / start (reverse)) k_i v_i^T
+int launch_fo_tc_summary(const FoArgs& a, const void* k, const void* v, bool reverse, cudaStream_t st);
+// out = (R)LA(x, k, v) with the carry (v == NULL: the values are the keys); r2 adds the swapped
+// pair (v, k); next_sum 1 / 2 also writes the next summary over (out, the values) / (out, xv);
+// add != NULL adds that partial.
+int launch_fo_tc_out(const FoArgs& a, const void* x, const void* k, const void* v, bool r2, int next_sum,
+                     const void* xv, const void* add, void* out, bool reverse, cudaStream_t st);
+
 // Bounded-wait self-test: waits on an mbarrier nobody arrives at; records site 90 in *status.
 int launch_wait_timeout_selftest(int* status, cudaStream_t st);
 int launch_state_compact(const float* src, float* dst, long heads, int d, int dv, bool to_compact, cudaStream_t st);

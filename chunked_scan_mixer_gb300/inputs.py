@@ -19,7 +19,7 @@ Workloads (sizes and distributions of the benchmark configurations):
   decode    256 sequences x H=32, d=dv=128; 4096-token bf16 prefill, N(0,1)/sqrt(d),
             decay 0.999; then single-token steps with fresh draws (seed 4000 + step)
   train     B=4 H=16 n=8192  d=dv=128 bf16; q,k,v ~ N(0,1)/sqrt(d); dO ~ N(0,1);
-            decay 0.995; unnormalised; forward + backward
+            decay 0.995; unnormalised; forward + backward; chunk 128
 """
 from __future__ import annotations
 
@@ -62,7 +62,7 @@ WORKLOADS = {
     "decode_prefill": Workload("decode_prefill", 256, 32, 4096, 128, 128, torch.bfloat16, 4,
                                "gauss", "gauss_sqrt_d", (0.999,), False, 1e-6, 64),
     "train": Workload("train", 4, 16, 8192, 128, 128, torch.bfloat16, 5, "gauss",
-                      "gauss_sqrt_d", (0.995,), False, 1e-6, 64, True),
+                      "gauss_sqrt_d", (0.995,), False, 1e-6, 128, True),
 }
 
 DECODE_STEPS = 1024

@@ -1,0 +1,96 @@
+"""The d = dv = 128 bf16 training path on the tcgen05 first-order scan kernel (chunk 128),
+through the C ABI, against the float64 oracle.
+
+The masked output is two chained first-order scans (p = S q, then o = q^T Z) and its reverse
+mode six more; every pass runs segment-parallel on the same kernel.  Bar: max|gpu - oracle| /
+max|oracle| <= 2e-2 per gradient and for the output (bf16 inputs; the oracle runs on the same
+bf16-rounded values).  Sizes span one and many segments, multi-chunk segments, ragged tails
+(the last chunk partial), a sequence shorter than a chunk, one token, and no decay.
+"""
+import numpy as np
+import pytest
+import torch
+
+import chunked_scan_mixer_gb300 as hla
+from chunked_scan_mixer_gb300 import inputs
+from oracle import cref
+
+from .helpers import np32, np64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+def _gamma_np(x):
+    return None if x["gamma"] is None else x["gamma"].double().numpy()
+
+
+def _dev(x):
+    g = None if x["gamma"] is None else x["gamma"].cuda()
+    return x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), g
+
+
+def _check_grads(got, x, what=""):
+    ref = cref.backward(np32(x["q"]), np32(x["k"]), np32(x["v"]), np32(x["dout"]), _gamma_np(x))
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, ref):
+        assert torch.isfinite(gg.float()).all(), (name, what)
+        err = rel_err(np64(gg.cpu()), rr)
+        assert err <= 2e-2, (name, what, err)
+
+
+@pytest.mark.parametrize("B, H, n", [(1, 2, 1000), (2, 8, 4000), (1, 3, 128), (1, 2, 127), (1, 2, 129),
+                                     (1, 1, 1), (3, 1, 2500)])
+@pytest.mark.parametrize("gamma", [None, (0.9, 0.999)])
+def test_backward_matches_oracle(B, H, n, gamma):
+    x = inputs.make_custom(B, H, n, D, D, torch.bfloat16, seed=B * 1000 + H * 100 + n % 97, gamma=gamma,
+                           with_dout=True)
+    q, k, v, do, g = _dev(x)
+    _check_grads(hla.backward(q, k, v, do, gamma=g, chunk=128), x, (B, H, n, gamma))
+
+
+@pytest.mark.parametrize("n", [300, 3000])
+def test_forward_saved_then_backward(n):
+    """The forward that keeps p for the backward gives the oracle's output; the backward from
+    the saved p and carries equals, bit for bit, the one that recomputes them, and the oracle."""
+    x = inputs.make_custom(2, 3, n, D, D, torch.bfloat16, seed=n, gamma=(0.97, 0.999), with_dout=True)
+    q, k, v, do, g = _dev(x)
+    o, saved = hla.forward(q, k, v, gamma=g, chunk=128, save_for_backward=True)
+    ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), _gamma_np(x))
+    assert rel_err(np64(o.cpu()), ref) <= 2e-2
+    plain = hla.forward(q, k, v, gamma=g, chunk=128)
+    assert rel_err(np64(o.cpu()), np64(plain.cpu())) <= 2e-2
+    a = hla.backward(q, k, v, do, gamma=g, chunk=128, saved=saved)
+    b = hla.backward(q, k, v, do, gamma=g, chunk=128)
+    for u, w in zip(a, b):
+        assert torch.equal(u, w)
+    _check_grads(a, x, "saved")
+
+
+def test_steep_and_flat_decay_per_head():
+    """Decays from 0.5 (a pair weight that underflows within a chunk) to 1 across heads."""
+    x = inputs.make_custom(1, 4, 700, D, D, torch.bfloat16, seed=77, gamma=None, with_dout=True)
+    x["gamma"] = torch.tensor([0.5, 0.9, 0.999, 1.0], dtype=torch.float32)
+    q, k, v, do, g = _dev(x)
+    _check_grads(hla.backward(q, k, v, do, gamma=g, chunk=128), x)
+
+
+def test_training_workload_all_heads():
+    """B=4, H=16, n=8192, d=dv=128, decay 0.995: forward keeping p, then the backward from it;
+    the output and all 64 heads' gradients against the oracle."""
+    w = inputs.WORKLOADS["train"]
+    assert w.chunk == 128
+    x = inputs.make(w)
+    q, k, v, do, g = _dev(x)
+    o, saved = hla.forward(q, k, v, gamma=g, chunk=w.chunk, save_for_backward=True)
+    grads = hla.backward(q, k, v, do, gamma=g, chunk=w.chunk, saved=saved)
+    torch.cuda.synchronize()
+    ref_o = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), _gamma_np(x))
+    assert rel_err(np64(o.cpu()), ref_o) <= 2e-2
+    del ref_o
+    ref = cref.backward(np32(x["q"]), np32(x["k"]), np32(x["v"]), np32(x["dout"]), _gamma_np(x))
+    for name, gg, rr in zip(("dq", "dk", "dv"), grads, ref):
+        got = np64(gg.cpu())
+        assert rel_err(got, rr) <= 2e-2, name
+        per_head = [rel_err(got[b, h], rr[b, h]) for b in range(w.B) for h in range(w.H)]
+        assert max(per_head) <= 2e-2, (name, int(np.argmax(per_head)))
