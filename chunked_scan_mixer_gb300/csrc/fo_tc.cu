@@ -57,14 +57,17 @@ constexpr uint32_t kBlk = 128 * 128;   // one [128 rows][64 bf16] SW128 column b
 constexpr uint32_t kTile = 2 * kBlk;   // a [128][128] bf16 tile: column blocks 0 (cols 0..63) and 1
 constexpr uint32_t kTmemCols = 512;
 
-// Shared-memory plan of the output kernel (byte offsets of 32 KB slots from the 1024-aligned base).
+// Shared-memory plan of the output kernel (byte offsets of 32 KB slots from the 1024-aligned
+// base).  Two key slots (chunk j in slot j % 2) let the next chunk's keys load while this
+// chunk's products still read its own; with KVS the key slot also serves as the value tile.
 template <bool R2, bool KVS, bool XVS, bool ADD>
 struct OutLayout {
     static constexpr uint32_t oQ = 0;
-    static constexpr uint32_t oK = kTile;
-    static constexpr uint32_t oV = KVS ? oK : oK + kTile;
-    static constexpr uint32_t oXV = XVS ? oV + kTile : oV;                    // next summary's values
-    static constexpr uint32_t oAD = (XVS ? oXV : oV) + kTile;                 // partial (ADD)
+    static constexpr uint32_t oK = kTile;                                     // slots oK, oK + kTile
+    static constexpr uint32_t oV = KVS ? oK : oK + 2 * kTile;                 // KVS: the key slot
+    static constexpr uint32_t oEnd0 = KVS ? oK + 2 * kTile : oV + kTile;
+    static constexpr uint32_t oXV = XVS ? oEnd0 : oV;                         // next summary's values
+    static constexpr uint32_t oAD = XVS ? oXV + kTile : oEnd0;                // partial (ADD)
     static constexpr uint32_t oKt = ADD ? oAD + kTile : oAD;                  // K~ (and V~ for R2)
     static constexpr uint32_t oKt2 = oKt + kTile;
     static constexpr uint32_t oS0 = R2 ? oKt2 + kTile : oKt + kTile;         // bf16 Sig0
@@ -74,21 +77,25 @@ struct OutLayout {
     static constexpr uint32_t oBar = oGP + 1088;
     static constexpr uint32_t oMisc = oBar + 16 * 8;
     static constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;  // + alignment slack
+    __host__ __device__ static constexpr uint32_t key(int j) { return oK + (uint32_t)(j & 1) * kTile; }
+    __host__ __device__ static constexpr uint32_t val(int j) { return KVS ? key(j) : oV; }
 };
 
-// Tensor-memory columns.  R = 1: G / Y [0,128), A operands [128,256) (G~ | fX), dSig
-// [256,384), next summary [384,512).  R = 2: G1 [0,128), G2 [128,256); after EPI-1 Y [0,128)
-// and dSig [128,256); A operands [256,448) (G~1 | G~2 | fX).
-template <bool R2>
+// Tensor-memory columns.  R = 1: G / Y of chunk j in [0,128) or, without a next summary,
+// alternately [384,512); A operands [128,256) (G~ | fX); dSig [256,384); next summary
+// [384,512).  R = 2: G1 [0,128), G2 [128,256); after EPI-1 Y [0,128) and dSig [128,256);
+// A operands [256,448) (G~1 | G~2 | fX).
+template <bool R2, bool NSUM>
 struct Cols {
-    static constexpr uint32_t TG = 0, TY = 0;
+    static constexpr bool kTwoG = !R2 && !NSUM;  // G / Y double-buffered
     static constexpr uint32_t TA = R2 ? 256 : 128;
     static constexpr uint32_t TX = TA + (R2 ? 128 : 64);  // fX
     static constexpr uint32_t TS = R2 ? 128 : 256;
     static constexpr uint32_t TN = 384;
+    __device__ static constexpr uint32_t TG(int j) { return kTwoG && (j & 1) ? 384u : 0u; }
 };
 
-enum Bar { FQ = 0, FK, FV, BG, BGT, BY, BSU, BS, BYT, BN, BSF, kBarCount };
+enum Bar { FQ = 0, FK0, FK1, FV, BG, BGT, BSU, BS, BYT, BN, BSF, kBarCount };
 
 struct Maps {
     CUtensorMap x, k, v, xv, ad, out;
@@ -133,24 +140,27 @@ __device__ __forceinline__ void la_masked_pack(uint32_t src, int r, int cb, int 
         for (int j = 0; j < 16; ++j) pk[j] = 0u;
         return;
     }
-    uint32_t v[32];
-    tc::tmem_ld32(src, v);
-    tc::tmem_wait_ld();
     const bool diag = cb == row0;
     float f = pow_decay(log2g, (float)(REV ? cb - r : r - cb));  // factor at column cb
     const float step = REV ? g : ginv;
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-        float a0 = f * __uint_as_float(v[j]);
-        f *= step;
-        float a1 = f * __uint_as_float(v[j + 1]);
-        f *= step;
-        if (diag) {
-            const int i0 = cb + j, i1 = cb + j + 1;
-            a0 = (REV ? i0 >= r : i0 <= r) ? a0 : 0.f;
-            a1 = (REV ? i1 >= r : i1 <= r) ? a1 : 0.f;
+    for (int half = 0; half < 2; ++half) {  // 16 columns at a time (register pressure)
+        uint32_t v[16];
+        tc::tmem_ld16(src + 16 * half, v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+            float a0 = f * __uint_as_float(v[j]);
+            f *= step;
+            float a1 = f * __uint_as_float(v[j + 1]);
+            f *= step;
+            if (diag) {
+                const int i0 = cb + 16 * half + j, i1 = i0 + 1;
+                a0 = (REV ? i0 >= r : i0 <= r) ? a0 : 0.f;
+                a1 = (REV ? i1 >= r : i1 <= r) ? a1 : 0.f;
+            }
+            pk[8 * half + j / 2] = pack_bf16x2(a0, a1);
         }
-        pk[j / 2] = pack_bf16x2(a0, a1);
     }
 }
 
@@ -172,11 +182,18 @@ __device__ __forceinline__ FoSeg la_seg(const FoArgs& a, int seg) {
 // Output kernel.  REV: reverse direction.  NSUM: next summary of the output.  R2: the swapped
 // second pair.  KVS: keys and values are the same tensor (one tile).  XVS: the next
 // summary's values are a separate tensor (else the value tile).  ADD: partial added.
+//
+// Schedule per chunk j (control thread / epilogue warps):
+//   MMA-G(j) -> EPI-1(j) -> MMA-Y(j), MMA-S(j) (one commit) -> EPI-S(j) -> ...
+// With G / Y double-buffered (no next summary, one pair) the epilogue runs EPI-S(j), EPI-1(j+1),
+// EPI-Y(j): MMA-G(j+1) is issued as soon as chunk j's products are, and MMA-Y(j+1) runs while
+// chunk j's output is staged.  Otherwise the order is EPI-S(j), EPI-Y(j), EPI-1(j+1).
 template <bool REV, bool NSUM, bool R2, bool KVS, bool XVS, bool ADD>
 __global__ void __launch_bounds__(la::kThreads, 1)
     fo_out_tc_kernel(const __grid_constant__ la::Maps maps, const FoArgs a) {
     using Lay = la::OutLayout<R2, KVS, XVS, ADD>;
-    using C = la::Cols<R2>;
+    using C = la::Cols<R2, NSUM>;
+    constexpr bool kTwoG = C::kTwoG;
     constexpr int kW = la::kW;
     pdl_trigger();
     extern __shared__ unsigned char smem_raw[];
@@ -250,6 +267,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
     const uint32_t tmem = *tmem_holder;
 
     auto chunk_of = [&](int it) { return REV ? sg.c_end - 1 - it : sg.c_begin + it; };
+    auto fk = [&](int j) { return &bars[(j & 1) ? la::FK1 : la::FK0]; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ control thread
@@ -258,23 +276,24 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                 tc::tma_load_3d(sm + slot, m, 0, c * kW, bh, bar);
                 tc::tma_load_3d(sm + slot + la::kBlk, m, 64, c * kW, bh, bar);
             };
-            auto load_x = [&](int c) {
+            auto load_x = [&](int j) {
                 tc::mbar_arrive_expect_tx(&bars[la::FQ], la::kTile);
-                load2(Lay::oQ, &maps.x, c, &bars[la::FQ]);
+                load2(Lay::oQ, &maps.x, chunk_of(j), &bars[la::FQ]);
             };
-            auto load_k = [&](int c) {
-                tc::mbar_arrive_expect_tx(&bars[la::FK], la::kTile);
-                load2(Lay::oK, &maps.k, c, &bars[la::FK]);
+            auto load_k = [&](int j) {
+                tc::mbar_arrive_expect_tx(fk(j), la::kTile);
+                load2(Lay::key(j), &maps.k, chunk_of(j), fk(j));
             };
             constexpr int kVTiles = (KVS ? 0 : 1) + (XVS ? 1 : 0) + (ADD ? 1 : 0);
-            auto load_v = [&](int c) {
+            auto load_v = [&](int j) {
                 if (kVTiles == 0) return;
                 tc::mbar_arrive_expect_tx(&bars[la::FV], kVTiles * la::kTile);
-                if (!KVS) load2(Lay::oV, &maps.v, c, &bars[la::FV]);
-                if (XVS) load2(Lay::oXV, &maps.xv, c, &bars[la::FV]);
-                if (ADD) load2(Lay::oAD, &maps.ad, c, &bars[la::FV]);
+                if (!KVS) load2(Lay::oV, &maps.v, chunk_of(j), &bars[la::FV]);
+                if (XVS) load2(Lay::oXV, &maps.xv, chunk_of(j), &bars[la::FV]);
+                if (ADD) load2(Lay::oAD, &maps.ad, chunk_of(j), &bars[la::FV]);
             };
-            const uint32_t sX = smem_u32(sm + Lay::oQ), sK = smem_u32(sm + Lay::oK), sV = smem_u32(sm + Lay::oV);
+            constexpr bool v_late = NSUM || ADD;  // the value group is still read after the products
+            const uint32_t sX = smem_u32(sm + Lay::oQ), sV = smem_u32(sm + Lay::oV);
             const uint32_t sKt = smem_u32(sm + Lay::oKt), sKt2 = smem_u32(sm + Lay::oKt2);
             const uint32_t sS0 = smem_u32(sm + Lay::oS0), sST = smem_u32(sm + Lay::oST);
             const uint32_t sXV = smem_u32(sm + Lay::oXV);
@@ -286,88 +305,128 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                 return tc::smem_desc(base + (uint32_t)(ks >> 2) * la::kBlk + (uint32_t)(ks & 3) * 32, 16, 1024);
             };
             auto mdesc = [](uint32_t base, int ks) { return tc::smem_desc(base + 2048u * ks, la::kBlk, 1024); };
-
-            load_x(chunk_of(0));
-            load_k(chunk_of(0));
-            load_v(chunk_of(0));
-            int lx = 1, lk = 1, lv = 1;
-            for (int it = 0; it < nit; ++it) {
-                const uint32_t ph = it & 1;
-                tc::mbar_wait(&bars[la::FQ], ph, abort, status, 101);
-                tc::mbar_wait(&bars[la::FK], ph, abort, status, 102);
-                if (kVTiles > 0 && R2) tc::mbar_wait(&bars[la::FV], ph, abort, status, 103);
-                tc::fence_after_sync();
-                // MMA-G: G = X K^T (R2: and X V^T)
+            int lx = 0, lk = 0, lv = 0;
+            // MMA-G: G = X K^T (R2: and X V^T), chunk j
+            auto mma_g = [&](int j) {
+                const uint32_t sK = smem_u32(sm + Lay::key(j));
                 for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_ss(tmem + C::TG, kdesc(sX, ks), kdesc(sK, ks), I_KK, ks > 0);
+                    tc::mma_ss(tmem + C::TG(j), kdesc(sX, ks), kdesc(sK, ks), I_KK, ks > 0);
                 if (R2)
                     for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_ss(tmem + C::TG + 128, kdesc(sX, ks), kdesc(sV, ks), I_KK, ks > 0);
+                        tc::mma_ss(tmem + C::TG(j) + 128, kdesc(sX, ks), kdesc(sV, ks), I_KK, ks > 0);
                 tc::mma_commit(&bars[la::BG]);
-                tc::mbar_wait(&bars[la::BGT], ph, abort, status, 104);  // G read; G~, fX, K~ written
-                if (!Lay::kStageInQ && it + 1 < nit) {  // X no longer read
-                    load_x(chunk_of(it + 1));
-                    ++lx;
-                }
-                if (!KVS && !R2) tc::mbar_wait(&bars[la::FV], ph, abort, status, 105);  // the value tile
-                if (it > 0) tc::mbar_wait(&bars[la::BS], ph ^ 1, abort, status, 106);  // Sig0 of this chunk
+            };
+            auto wait_g_inputs = [&](int j) {
+                tc::mbar_wait(&bars[la::FQ], j & 1, abort, status, 101);
+                tc::mbar_wait(fk(j), (j >> 1) & 1, abort, status, 102);
+                if (R2) tc::mbar_wait(&bars[la::FV], j & 1, abort, status, 103);
                 tc::fence_after_sync();
-                // MMA-Y: Y = [G~ | (G~2) | fX] [V ; (K) ; Sig0]
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_ts(tmem + C::TY, tmem + C::TA + 8 * ks, mdesc(sV, ks), I_TM, ks > 0);
-                if (R2)
-                    for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_ts(tmem + C::TY, tmem + C::TA + 64 + 8 * ks, mdesc(sK, ks), I_TM, 1);
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_ts(tmem + C::TY, tmem + C::TX + 8 * ks, mdesc(sS0, ks), I_TM, 1);
-                tc::mma_commit(&bars[la::BY]);
-                // MMA-S: dSig = K~^T V (R2: + V~^T K)
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_ss(tmem + C::TS, mdesc(sKt, ks), mdesc(sV, ks), I_MM, ks > 0);
-                if (R2)
-                    for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_ss(tmem + C::TS, mdesc(sKt2, ks), mdesc(sK, ks), I_MM, 1);
-                tc::mma_commit(&bars[la::BSU]);
-                tc::mbar_wait(&bars[la::BSU], ph, abort, status, 107);  // K, V, K~, Sig0 no longer read
-                if (it + 1 < nit) {
-                    load_k(chunk_of(it + 1));
-                    ++lk;
-                }
-                const bool v_late = NSUM || ADD;  // the value group is still read after MMA-S
-                if (!v_late && it + 1 < nit && kVTiles > 0) {
-                    load_v(chunk_of(it + 1));
-                    ++lv;
-                }
-                tc::mbar_wait(&bars[la::BYT], ph, abort, status, 108);  // output tile staged
+            };
+            // after EPI-Y(j): the tile store, the next summary, late loads, the stage freed
+            auto finish = [&](int j) {
+                tc::mbar_wait(&bars[la::BYT], j & 1, abort, status, 108);
                 tc::fence_after_sync();
-                const int c = chunk_of(it);
+                const int c = chunk_of(j);
                 tc::tma_store_3d(&maps.out, sm + Lay::oST, 0, c * kW, bh);
                 tc::tma_store_3d(&maps.out, sm + Lay::oST + la::kBlk, 64, c * kW, bh);
                 tc::bulk_commit();
                 if (NSUM) {  // next summary: T_N += Y^T (w' U)
                     for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_ss(tmem + C::TN, mdesc(sST, ks), mdesc(sXV, ks), I_MM, (it > 0 || ks > 0) ? 1u : 0u);
+                        tc::mma_ss(tmem + C::TN, mdesc(sST, ks), mdesc(sXV, ks), I_MM, (j > 0 || ks > 0) ? 1u : 0u);
                     tc::mma_commit(&bars[la::BN]);
-                    tc::mbar_wait(&bars[la::BN], ph, abort, status, 109);
+                    tc::mbar_wait(&bars[la::BN], j & 1, abort, status, 109);
                 }
-                if (v_late && it + 1 < nit && kVTiles > 0) {
-                    load_v(chunk_of(it + 1));
+                if (v_late && j + 1 < nit && kVTiles > 0) {
+                    load_v(j + 1);
                     ++lv;
                 }
                 tc::bulk_wait_read_all();  // the output tile has been read
-                if (Lay::kStageInQ && it + 1 < nit) {
-                    load_x(chunk_of(it + 1));
+                if (Lay::kStageInQ && j + 1 < nit) {
+                    load_x(j + 1);
                     ++lx;
                 }
                 tc::mbar_arrive(&bars[la::BSF]);
+            };
+
+            load_x(0);
+            ++lx;
+            load_k(0);
+            ++lk;
+            if (kVTiles > 0) {
+                load_v(0);
+                ++lv;
             }
+            if (nit > 1) {
+                load_k(1);
+                ++lk;
+            }
+            wait_g_inputs(0);
+            mma_g(0);
+            for (int j = 0; j < nit; ++j) {
+                tc::mbar_wait(&bars[la::BGT], j & 1, abort, status, 104);  // G read; G~, fX, K~ written
+                if (j > 0) tc::mbar_wait(&bars[la::BS], (j - 1) & 1, abort, status, 106);  // Sig0 of chunk j
+                if (!Lay::kStageInQ && j + 1 < nit) {  // X no longer read
+                    load_x(j + 1);
+                    ++lx;
+                }
+                if (!KVS) tc::mbar_wait(&bars[la::FV], j & 1, abort, status, 105);  // the value tile
+                tc::fence_after_sync();
+                const uint32_t sK = smem_u32(sm + Lay::key(j)), sVj = smem_u32(sm + Lay::val(j));
+                // MMA-Y: Y = [G~ | (G~2) | fX] [V ; (K) ; Sig0]
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ts(tmem + C::TG(j), tmem + C::TA + 8 * ks, mdesc(sVj, ks), I_TM, ks > 0);
+                if (R2)
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_ts(tmem + C::TG(j), tmem + C::TA + 64 + 8 * ks, mdesc(sK, ks), I_TM, 1);
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ts(tmem + C::TG(j), tmem + C::TX + 8 * ks, mdesc(sS0, ks), I_TM, 1);
+                // MMA-S: dSig = K~^T V (R2: + V~^T K)
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem + C::TS, mdesc(sKt, ks), mdesc(sVj, ks), I_MM, ks > 0);
+                if (R2)
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_ss(tmem + C::TS, mdesc(sKt2, ks), mdesc(sK, ks), I_MM, 1);
+                tc::mma_commit(&bars[la::BSU]);
+                if (kTwoG) {
+                    if (j > 0) finish(j - 1);  // also frees G / Y region (j+1) % 2
+                    if (j + 1 < nit) {
+                        wait_g_inputs(j + 1);
+                        mma_g(j + 1);
+                    }
+                    tc::mbar_wait(&bars[la::BSU], j & 1, abort, status, 107);  // chunk j's products done
+                    if (j + 2 < nit) {
+                        load_k(j + 2);
+                        ++lk;
+                    }
+                    if (!v_late && !KVS && j + 1 < nit) {
+                        load_v(j + 1);
+                        ++lv;
+                    }
+                } else {
+                    finish(j);  // after EPI-Y(j), so chunk j's products are done
+                    if (j + 2 < nit) {
+                        load_k(j + 2);
+                        ++lk;
+                    }
+                    if (!v_late && !KVS && j + 1 < nit) {
+                        load_v(j + 1);
+                        ++lv;
+                    }
+                    if (j + 1 < nit) {
+                        wait_g_inputs(j + 1);
+                        mma_g(j + 1);
+                    }
+                }
+            }
+            if (kTwoG) finish(nit - 1);
             // drain (bounded, ignoring the abort flag) so that nothing is in flight at exit
             volatile int never = 0;
             tc::mbar_wait(&bars[la::BSU], (nit - 1) & 1, &never, nullptr, 0);
             if (NSUM) tc::mbar_wait(&bars[la::BN], (nit - 1) & 1, &never, nullptr, 0);
             tc::mbar_wait(&bars[la::FQ], (lx - 1) & 1, &never, nullptr, 0);
-            tc::mbar_wait(&bars[la::FK], (lk - 1) & 1, &never, nullptr, 0);
-            if (kVTiles > 0) tc::mbar_wait(&bars[la::FV], (lv - 1) & 1, &never, nullptr, 0);
+            tc::mbar_wait(&bars[la::FK0], ((lk + 1) / 2 - 1) & 1, &never, nullptr, 0);
+            if (lk > 1) tc::mbar_wait(&bars[la::FK1], (lk / 2 - 1) & 1, &never, nullptr, 0);
+            if (lv > 0) tc::mbar_wait(&bars[la::FV], (lv - 1) & 1, &never, nullptr, 0);
             tc::bulk_wait_all();
         }
         __syncwarp();
@@ -377,18 +436,18 @@ __global__ void __launch_bounds__(la::kThreads, 1)
         const uint32_t lrow = tmem + ((uint32_t)row0 << 16);
         const float ginv = g > 0.f ? 1.f / g : 0.f;
         unsigned char* sX = sm + Lay::oQ;
-        unsigned char* sK = sm + Lay::oK;
         unsigned char* sV = sm + Lay::oV;
-        for (int it = 0; it < nit; ++it) {
-            const uint32_t ph = it & 1;
-            const int c = chunk_of(it);
+
+        // ---- EPI-1(j): G~ (and G~2), fX -> tensor memory;  K~ (and V~) -> shared memory ------------
+        auto epi1 = [&](int j) {
+            const int c = chunk_of(j);
             const int Wc = min(kW, a.n - c * kW);
             const bool live = r < Wc;
-            // ---- EPI-1: G~ (and G~2), fX -> tensor memory;  K~ (and V~) -> shared memory -------------
-            tc::mbar_wait(&bars[la::FQ], ph, abort, status, 111);
-            tc::mbar_wait(&bars[la::FK], ph, abort, status, 112);
-            if (R2) tc::mbar_wait(&bars[la::FV], ph, abort, status, 113);
-            tc::mbar_wait(&bars[la::BG], ph, abort, status, 114);
+            unsigned char* sK = sm + Lay::key(j);
+            tc::mbar_wait(&bars[la::FQ], j & 1, abort, status, 111);
+            tc::mbar_wait(fk(j), (j >> 1) & 1, abort, status, 112);
+            if (R2) tc::mbar_wait(&bars[la::FV], j & 1, abort, status, 113);
+            tc::mbar_wait(&bars[la::BG], j & 1, abort, status, 114);
             tc::fence_after_sync();
 #pragma unroll
             for (int gi = 0; gi < (R2 ? 2 : 1); ++gi) {
@@ -396,104 +455,116 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                 for (int p = 0; p < 2; ++p) {
                     const int cb = 64 * h + 32 * p;
                     uint32_t pk[16];
-                    la_masked_pack<REV>(lrow + C::TG + 128 * gi + cb, r, cb, row0, log2g, g, ginv, pk);
+                    la_masked_pack<REV>(lrow + C::TG(j) + 128 * gi + cb, r, cb, row0, log2g, g, ginv, pk);
                     tc::tmem_st16(lrow + C::TA + 64 * gi + cb / 2, pk);
                 }
             }
-            {
-                const float f = live ? (REV ? gp[Wc - r] : gp[r + 1]) : 0.f;
+            const float f = live ? (REV ? gp[Wc - r] : gp[r + 1]) : 0.f;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[16];
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[16];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint4 x =
-                            la_scale_chunk(*reinterpret_cast<const uint4*>(sX + la_off(h, r, 4 * half + j)), f);
-                        pk[4 * j] = x.x, pk[4 * j + 1] = x.y, pk[4 * j + 2] = x.z, pk[4 * j + 3] = x.w;
-                    }
-                    tc::tmem_st16(lrow + C::TX + 32 * h + 16 * half, pk);
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 x = la_scale_chunk(*reinterpret_cast<const uint4*>(sX + la_off(h, r, 4 * half + i)), f);
+                    pk[4 * i] = x.x, pk[4 * i + 1] = x.y, pk[4 * i + 2] = x.z, pk[4 * i + 3] = x.w;
                 }
-                const float w = live ? (REV ? gp[r] : gp[Wc - 1 - r]) : 0.f;
+                tc::tmem_st16(lrow + C::TX + 32 * h + 16 * half, pk);
+            }
+            const float w = live ? (REV ? gp[r] : gp[Wc - 1 - r]) : 0.f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t off = la_off(h, r, j);
-                    *reinterpret_cast<uint4*>(sm + Lay::oKt + off) =
-                        la_scale_chunk(*reinterpret_cast<const uint4*>(sK + off), w);
-                    if (R2)
-                        *reinterpret_cast<uint4*>(sm + Lay::oKt2 + off) =
-                            la_scale_chunk(*reinterpret_cast<const uint4*>(sV + off), w);
-                }
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t off = la_off(h, r, i);
+                *reinterpret_cast<uint4*>(sm + Lay::oKt + off) = la_scale_chunk(*reinterpret_cast<const uint4*>(sK + off), w);
+                if (R2)
+                    *reinterpret_cast<uint4*>(sm + Lay::oKt2 + off) =
+                        la_scale_chunk(*reinterpret_cast<const uint4*>(sV + off), w);
             }
             tc::tmem_wait_st();
             tc::fence_proxy_async();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[la::BGT]);
+        };
 
-            // ---- EPI-S: Sig <- g^Wc Sig + dSig;  bf16 Sig0 for the next chunk ------------------------
-            tc::mbar_wait(&bars[la::BSU], ph, abort, status, 115);
+        // ---- EPI-S(j): Sig <- g^Wc Sig + dSig;  bf16 Sig0 for chunk j + 1 ---------------------------
+        auto epis = [&](int j) {
+            const int c = chunk_of(j);
+            const int Wc = min(kW, a.n - c * kW);
+            tc::mbar_wait(&bars[la::BSU], j & 1, abort, status, 115);  // chunk j's products are done
             tc::fence_after_sync();
-            {
-                const float rho = gp[Wc];
+            const float rho = gp[Wc];
 #pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    uint32_t v[32];
-                    tc::tmem_ld32(lrow + C::TS + 64 * h + 32 * p, v);
-                    tc::tmem_wait_ld();
+            for (int p = 0; p < 4; ++p) {
+                uint32_t v[16];
+                tc::tmem_ld16(lrow + C::TS + 64 * h + 16 * p, v);
+                tc::tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) sig[32 * p + j] = rho * sig[32 * p + j] + __uint_as_float(v[j]);
-                }
-                if (it + 1 < nit) publish_sig();  // MMA-Y of this chunk has completed (commit order)
+                for (int i = 0; i < 16; ++i) sig[16 * p + i] = rho * sig[16 * p + i] + __uint_as_float(v[i]);
             }
+            if (j + 1 < nit) publish_sig();
             tc::fence_proxy_async();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[la::BS]);
+        };
 
-            // ---- EPI-Y: Y (+ partial) -> bf16 output tile;  next summary's values scaled ----------------
-            if (it > 0) tc::mbar_wait(&bars[la::BSF], ph ^ 1, abort, status, 116);  // previous tile read
-            if (ADD || (NSUM && XVS)) tc::mbar_wait(&bars[la::FV], ph, abort, status, 117);
+        // ---- EPI-Y(j): Y (+ partial) -> bf16 output tile;  next summary's values scaled -------------
+        auto epiy = [&](int j) {
+            const int c = chunk_of(j);
+            const int Wc = min(kW, a.n - c * kW);
+            const bool live = r < Wc;
+            if (j > 0) tc::mbar_wait(&bars[la::BSF], (j - 1) & 1, abort, status, 116);  // previous tile read
+            if (ADD || (NSUM && XVS)) tc::mbar_wait(&bars[la::FV], j & 1, abort, status, 117);
             tc::fence_after_sync();
-            {
 #pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    uint32_t v[32];
-                    tc::tmem_ld32(lrow + C::TY + 64 * h + 32 * p, v);
-                    tc::tmem_wait_ld();
-                    float y[32];
+            for (int p = 0; p < 4; ++p) {  // 16 columns = 2 chunks of the tile at a time
+                uint32_t v[16];
+                tc::tmem_ld16(lrow + C::TG(j) + 64 * h + 16 * p, v);
+                tc::tmem_wait_ld();
+                float y[16];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(v[j]);
-                    if (ADD) {
+                for (int i = 0; i < 16; ++i) y[i] = __uint_as_float(v[i]);
+                if (ADD) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint4 x = *reinterpret_cast<const uint4*>(sm + Lay::oAD + la_off(h, r, 4 * p + j));
-                            const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                y[8 * j + 2 * u] += la_bf_lo(xw[u]);
-                                y[8 * j + 2 * u + 1] += la_bf_hi(xw[u]);
-                            }
-                        }
+                    for (int i = 0; i < 2; ++i) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(sm + Lay::oAD + la_off(h, r, 2 * p + i));
+                        y[8 * i + 0] += la_bf_lo(x.x), y[8 * i + 1] += la_bf_hi(x.x);
+                        y[8 * i + 2] += la_bf_lo(x.y), y[8 * i + 3] += la_bf_hi(x.y);
+                        y[8 * i + 4] += la_bf_lo(x.z), y[8 * i + 5] += la_bf_hi(x.z);
+                        y[8 * i + 6] += la_bf_lo(x.w), y[8 * i + 7] += la_bf_hi(x.w);
                     }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<uint4*>(sm + Lay::oST + la_off(h, r, 4 * p + j)) = la_pack8(&y[8 * j]);
                 }
-                if (NSUM) {
-                    const int pos = (c - sg.c_begin) * kW + r;  // token position in the segment
-                    const float wn = live ? pow_decay(log2gn, (float)(REV ? pos : sg.L - 1 - pos)) : 0.f;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t off = la_off(h, r, j);
-                        *reinterpret_cast<uint4*>(sm + Lay::oXV + off) =
-                            la_scale_chunk(*reinterpret_cast<const uint4*>(sm + Lay::oXV + off), wn);
-                    }
+                for (int i = 0; i < 2; ++i)
+                    *reinterpret_cast<uint4*>(sm + Lay::oST + la_off(h, r, 2 * p + i)) = la_pack8(&y[8 * i]);
+            }
+            if (NSUM) {
+                const int pos = (c - sg.c_begin) * kW + r;  // token position in the segment
+                const float wn = live ? pow_decay(log2gn, (float)(REV ? pos : sg.L - 1 - pos)) : 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t off = la_off(h, r, i);
+                    *reinterpret_cast<uint4*>(sm + Lay::oXV + off) =
+                        la_scale_chunk(*reinterpret_cast<const uint4*>(sm + Lay::oXV + off), wn);
                 }
             }
+            tc::tmem_wait_ld();
             tc::fence_proxy_async();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[la::BYT]);
+        };
+
+        if (nit > 0) epi1(0);
+        for (int j = 0; j < nit; ++j) {
+            epis(j);
+            if (kTwoG) {
+                if (j + 1 < nit) epi1(j + 1);
+                epiy(j);
+            } else {
+                epiy(j);
+                if (j + 1 < nit) epi1(j + 1);
+            }
         }
         if (NSUM && nit > 0) {  // the segment's next summary -> global (fp32)
             tc::mbar_wait(&bars[la::BN], (nit - 1) & 1, abort, status, 118);
@@ -505,10 +576,10 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                 tc::tmem_ld32(lrow + C::TN + 64 * h + 32 * p, v);
                 tc::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(dst + 32 * p + j) =
-                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                                    __uint_as_float(v[j + 3]));
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4*>(dst + 32 * p + i) =
+                        make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                                    __uint_as_float(v[i + 3]));
             }
         }
     }
@@ -704,10 +775,16 @@ int la_launch(K kfn, uint32_t smem, const la::Maps& maps, const FoArgs& a, cudaS
 
 bool fo_tc_available() { return la_encode_fn() != nullptr; }
 
+// The largest shared-memory plan among the instantiated output kernels (and the summary kernels).
 size_t fo_tc_max_smem() {
-    return la::OutLayout<true, false, false, false>::kSmemBytes > la::OutLayout<false, false, true, true>::kSmemBytes
-               ? la::OutLayout<true, false, false, false>::kSmemBytes
-               : la::OutLayout<false, false, true, true>::kSmemBytes;
+    const uint32_t sizes[] = {la::OutLayout<false, true, true, false>::kSmemBytes,    // p
+                              la::OutLayout<false, false, false, false>::kSmemBytes,  // o, Z dO, dv
+                              la::OutLayout<true, false, false, false>::kSmemBytes,   // dk
+                              la::OutLayout<false, true, false, true>::kSmemBytes,    // dq
+                              las::Layout<false>::kSmemBytes, las::Layout<true>::kSmemBytes};
+    uint32_t m = 0;
+    for (uint32_t x : sizes) m = x > m ? x : m;
+    return m;
 }
 
 int launch_fo_zero_first(float* carry, int BH, int nseg, int* status, cudaStream_t st) {

@@ -7,6 +7,8 @@ max|oracle| <= 2e-2 per gradient and for the output (bf16 inputs; the oracle run
 bf16-rounded values).  Sizes span one and many segments, multi-chunk segments, ragged tails
 (the last chunk partial), a sequence shorter than a chunk, one token, and no decay.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -94,3 +96,24 @@ def test_training_workload_all_heads():
         assert rel_err(got, rr) <= 2e-2, name
         per_head = [rel_err(got[b, h], rr[b, h]) for b in range(w.B) for h in range(w.H)]
         assert max(per_head) <= 2e-2, (name, int(np.argmax(per_head)))
+
+
+def test_distinct_from_the_legacy_path():
+    """HLA2_KERNEL=mma selects the mma.sync kernels: both paths match the oracle, and their
+    gradients are not bit for bit equal (different kernels, different rounding order), so the
+    default call does run the first-order scan kernels."""
+    x = inputs.make_custom(1, 2, 600, D, D, torch.bfloat16, seed=5, gamma=(0.98, 0.999), with_dout=True)
+    q, k, v, do, g = _dev(x)
+    tc = hla.backward(q, k, v, do, gamma=g, chunk=128)
+    old = os.environ.get("HLA2_KERNEL")
+    os.environ["HLA2_KERNEL"] = "mma"
+    try:
+        legacy = hla.backward(q, k, v, do, gamma=g, chunk=128)
+    finally:
+        if old is None:
+            os.environ.pop("HLA2_KERNEL", None)
+        else:
+            os.environ["HLA2_KERNEL"] = old
+    _check_grads(tc, x, "tcgen05")
+    _check_grads(legacy, x, "mma.sync")
+    assert not all(torch.equal(a, b) for a, b in zip(tc, legacy))
