@@ -372,9 +372,9 @@ def measure_decode_mq(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: 
 
 
 def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: int = 10, warmup: int = 3):
-    """Training row: B=4 H=16 n=8192 d=dv=128 bf16, decay 0.995, unnormalised; one step =
-    forward (keeping the chunk states for the backward) + backward (dq, dk, dv) through the
-    public calls, inputs resident."""
+    """Training row: B=4 H=16 n=8192 d=dv=128 bf16, decay 0.995, unnormalised, chunk 128 (the
+    tcgen05 first-order scan passes); one step = forward (keeping p and the carries for the
+    backward) + backward (dq, dk, dv) through the public calls, inputs resident."""
     import torch
 
     import chunked_scan_mixer_gb300 as hla
