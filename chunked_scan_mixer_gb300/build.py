@@ -1,9 +1,12 @@
 """Builds the HLA-2 CUDA library (libhla2.so) in-tree for sm_103a.
 
 Every translation unit is compiled by nvcc in parallel, then linked into
-``chunked_scan_mixer_gb300/_build/libhla2.so``.  Nothing is installed.
+``chunked_scan_mixer_gb300/_build/libhla2.so``.  Nothing is installed.  ``--debug`` builds
+the bounds-checking variant (HLA2_DEBUG: global-memory indices checked against the buffer
+extents, a failed check recorded and the access skipped; see hla2_debug_status) into
+``chunked_scan_mixer_gb300/_build_debug/libhla2.so``.
 
-    python -m chunked_scan_mixer_gb300.build [--force] [--ptxas-v]
+    python -m chunked_scan_mixer_gb300.build [--force] [--ptxas-v] [--debug]
 """
 from __future__ import annotations
 
@@ -20,6 +23,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libhla2.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libhla2.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -49,9 +54,11 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None) -> str:
+def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = None, debug: bool = False) -> str:
     nvcc = _nvcc()
-    objdir = os.path.join(BUILD, "obj")
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    flags = NVCC_FLAGS + (["-DHLA2_DEBUG"] if debug else [])
+    objdir = os.path.join(build_dir, "obj")
     os.makedirs(objdir, exist_ok=True)
     hdrs = _headers()
     srcs = sources()
@@ -65,7 +72,7 @@ def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = N
 
     def compile_one(so):
         s, o = so
-        cmd = [nvcc] + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_verbose else []) + ["-c", s, "-o", o]
+        cmd = [nvcc] + flags + (["-Xptxas", "-v"] if ptxas_verbose else []) + ["-c", s, "-o", o]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(s)}:\n{r.stderr}")
@@ -76,22 +83,23 @@ def build(force: bool = False, ptxas_verbose: bool = False, jobs: int | None = N
             for log in ex.map(compile_one, todo):
                 if ptxas_verbose and log:
                     sys.stderr.write(log)
-    if force or todo or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    if force or todo or _stale(lib, objs):
+        tmp = lib + f".{os.getpid()}.tmp"
         cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--ptxas-v", action="store_true")
+    ap.add_argument("--debug", action="store_true", help="the bounds-checking build (HLA2_DEBUG)")
     args = ap.parse_args()
-    print(build(force=args.force, ptxas_verbose=args.ptxas_v))
+    print(build(force=args.force, ptxas_verbose=args.ptxas_v, debug=args.debug))
 
 
 if __name__ == "__main__":

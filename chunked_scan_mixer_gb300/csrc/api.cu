@@ -521,6 +521,39 @@ int hla2_workspace_status(const void* workspace, hla2_stream_t stream) {
     return succeed();
 }
 
+int hla2_debug_status(int clear) {
+#ifdef HLA2_DEBUG
+    int (*const readers[])(bool) = {dbg_read_fwd_simt,    dbg_read_decode,      dbg_read_fwd_mma_d16,
+                                    dbg_read_fwd_mma_d32, dbg_read_fwd_mma_d64, dbg_read_fwd_mma_d128,
+                                    dbg_read_bwd_mma_d16, dbg_read_bwd_mma_d32, dbg_read_bwd_mma_d64,
+                                    dbg_read_bwd_mma_d128, dbg_read_bwd_simt,   dbg_read_scan,
+                                    dbg_read_fo_tc,       dbg_read_selftest};
+    if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail("debug status");
+    int site = 0;
+    for (auto rd : readers) {
+        const int v = rd(clear != 0);
+        if (v < 0) return cuda_fail("debug status read");
+        if (!site) site = v;
+    }
+    succeed();
+    return site;
+#else
+    (void)clear;
+    return fail(HLA2_ERR_UNSUPPORTED, "not a debug build (compile with HLA2_DEBUG)");
+#endif
+}
+
+int hla2_debug_selftest(hla2_stream_t stream) {
+#ifdef HLA2_DEBUG
+    cudaGetLastError();
+    if (launch_debug_check_selftest(reinterpret_cast<cudaStream_t>(stream))) return cuda_fail("debug self-test");
+    return succeed();
+#else
+    (void)stream;
+    return fail(HLA2_ERR_UNSUPPORTED, "not a debug build (compile with HLA2_DEBUG)");
+#endif
+}
+
 int hla2_selftest_wait_timeout(void* workspace, hla2_stream_t stream) {
     if (!workspace || !aligned16(workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     cudaGetLastError();

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, W>::NT) bwd_chunk_mma_kernel(con
         const int cpr = width / 8;
         for (int i = tid; i < W * cpr; i += NT) {
             const int r = i / cpr, p = (i % cpr) * 8;
-            if (r < Wc)
+            if (r < Wc && HLA2_IN(row0 + r < a.n, 501))
                 cp_async16(&dst[r * ld + p], src + (size_t)(row0 + r) * width + p);
             else
                 *reinterpret_cast<uint4*>(&dst[r * ld + p]) = make_uint4(0, 0, 0, 0);
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, W>::NT) bwd_chunk_mma_kernel(con
         load_rows(Qs, LD, a.q + hq * D, D, row0, Wc);
         load_rows(Vs, LDV, a.v + hq * DV, DV, row0, Wc);
         load_rows(Os, LDV, a.dout + hq * DV, DV, row0, Wc);
-        if (!RSUM) {
+        if (!RSUM && HLA2_IN(bh < a.BH && c < a.nchunks, 502)) {
             load_rows(Ks, LD, a.k + hq * D, D, row0, Wc);
             const bf16* st = a.chunk_states + ((size_t)bh * a.nchunks + c) * (size_t)(D * D + D * DV);
             for (int i = tid; i < D * D / 8; i += NT) {
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, W>::NT) bwd_chunk_mma_kernel(con
 #pragma unroll
                     for (int i = 0; i < 4; i += 2) {
                         const int r = acc_row(rb * 16, i), col = acc_col(cb * 16, h, i);
-                        if (r < Wc)
+                        if (r < Wc && HLA2_IN(row0 + r < a.n, 503))
                             *reinterpret_cast<uint32_t*>(&dst[(size_t)r * ldo + col]) = pack_bf16x2(acc[h][i], acc[h][i + 1]);
                     }
             }
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, W>::NT) bwd_chunk_mma_kernel(con
         if (c > c_begin) load_chunk(c - 1);
     }
 
-    if (RSUM) {
+    if (RSUM && HLA2_IN(bh < a.BH && seg < a.nseg, 504)) {
         float* dZ = a.ws + a.ZhB + sidx * D * DV;
         float* dS = a.ws + a.ShB + sidx * D * D;
 #pragma unroll

@@ -79,13 +79,15 @@ __global__ void __launch_bounds__(kBsThreads) bwd_chunk_simt_kernel(const BwdArg
         __syncthreads();  // the previous chunk's readers of the tiles and carries are done
         for (int i = tid; i < W * D; i += NT) {
             const int r = i / D;
-            Qs[i] = r < Wc ? a.q[(hq + row0) * D + i] : 0.f;
-            if (!RSUM) Ks[i] = r < Wc ? a.k[(hq + row0) * D + i] : 0.f;
+            const bool in = r < Wc && HLA2_IN(row0 + r < a.n, 601);
+            Qs[i] = in ? a.q[(hq + row0) * D + i] : 0.f;
+            if (!RSUM) Ks[i] = in ? a.k[(hq + row0) * D + i] : 0.f;
         }
         for (int i = tid; i < W * DV; i += NT) {
             const int r = i / DV;
-            Vs[i] = r < Wc ? a.v[(hq + row0) * DV + i] : 0.f;
-            Os[i] = r < Wc ? a.dout[(hq + row0) * DV + i] : 0.f;
+            const bool in = r < Wc && HLA2_IN(row0 + r < a.n, 602);
+            Vs[i] = in ? a.v[(hq + row0) * DV + i] : 0.f;
+            Os[i] = in ? a.dout[(hq + row0) * DV + i] : 0.f;
         }
         const float* S0 = RSUM ? nullptr : a.chunk_states + ((size_t)bh * a.nchunks + c) * (size_t)(D * D + D * DV);
         const float* Z0 = RSUM ? nullptr : S0 + (size_t)D * D;
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(kBsThreads) bwd_chunk_simt_kernel(const BwdArg
                 float s0 = 0.f, s1 = 0.f;
                 for (int f = 0; f < D; ++f) s0 += Ps[j * D + f] * Zh[(size_t)f * DV + x];
                 for (int r = j; r < Wc; ++r) s1 += Bt[r * W + j] * Os[r * DV + x];
-                a.dv[(hq + row0) * DV + e] = gp[2 * (Wc - 1 - j)] * s0 + s1;
+                if (HLA2_IN(row0 + j < a.n, 603)) a.dv[(hq + row0) * DV + e] = gp[2 * (Wc - 1 - j)] * s0 + s1;
             }
             for (int e = tid; e < Wc * D; e += NT) {
                 const int r = e / D, f = e % D;
@@ -151,14 +153,14 @@ __global__ void __launch_bounds__(kBsThreads) bwd_chunk_simt_kernel(const BwdArg
                 for (int x = 0; x < DV; ++x) sz += Os[r * DV + x] * Z0[(size_t)f * DV + x];
                 for (int x = 0; x < D; ++x) ss += dPs[r * D + x] * S0[(size_t)x * D + f];
                 for (int j = 0; j <= r; ++j) sp += Dt[r * W + j] * Ps[j * D + f] + dAt[r * W + j] * Ks[j * D + f];
-                a.dq[(hq + row0) * D + e] = gp[r + 1] * (gp[r + 1] * sz + ss) + sp;
+                if (HLA2_IN(row0 + r < a.n, 604)) a.dq[(hq + row0) * D + e] = gp[r + 1] * (gp[r + 1] * sz + ss) + sp;
             }
             for (int e = tid; e < Wc * D; e += NT) {
                 const int i = e / D, f = e % D;
                 float sh = 0.f, sr = 0.f;
                 for (int x = 0; x < D; ++x) sh += Ks[i * D + x] * (Sh[(size_t)x * D + f] + Sh[(size_t)f * D + x]);
                 for (int r = i; r < Wc; ++r) sr += At[r * W + i] * dPs[r * D + f] + dAt[r * W + i] * Qs[r * D + f];
-                a.dk[(hq + row0) * D + e] = gp[Wc - 1 - i] * sh + sr;
+                if (HLA2_IN(row0 + i < a.n, 605)) a.dk[(hq + row0) * D + e] = gp[Wc - 1 - i] * sh + sr;
             }
             __syncthreads();  // every read of the carries is done before they move
         }
@@ -195,3 +197,5 @@ int launch_bwd_chunk_simt(const BwdArgsF& a, int d, int dv, bool rsum, cudaStrea
 }
 
 }  // namespace hla2
+
+HLA2_DEBUG_READER(bwd_simt)

@@ -20,3 +20,5 @@ size_t bwd_chunk_mma_smem_d128(int W) {
 }
 
 }  // namespace hla2
+
+HLA2_DEBUG_READER(bwd_mma_d128)

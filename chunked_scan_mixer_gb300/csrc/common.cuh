@@ -116,6 +116,37 @@ __host__ __device__ inline PackOff compact_off(int d, int dv) {
 }
 
 // ---------------------------------------------------------------------------
+// Debug build (compiled with -DHLA2_DEBUG).  HLA2_IN(cond, site) evaluates to cond; a
+// false cond records `site` in this translation unit's debug word (the first site wins), and
+// the caller skips the access it guards.  Nothing traps.  In the normal build HLA2_IN is
+// `true` and costs nothing.  HLA2_DEBUG_READER(name) defines, at the end of a file that uses
+// HLA2_IN, the host function that reads (and optionally clears) that file's word.
+// ---------------------------------------------------------------------------
+#ifdef HLA2_DEBUG
+static __device__ int hla2_dbg_word;
+__device__ __forceinline__ bool hla2_dbg_in(bool ok, int site) {
+    if (!ok) atomicCAS(&hla2_dbg_word, 0, site);
+    return ok;
+}
+#define HLA2_IN(cond, site) hla2_dbg_in((cond), (site))
+#define HLA2_DEBUG_READER(name)                                                            \
+    namespace hla2 {                                                                       \
+    int dbg_read_##name(bool clear) {                                                      \
+        int v = 0;                                                                         \
+        if (cudaMemcpyFromSymbol(&v, hla2_dbg_word, sizeof(int)) != cudaSuccess) return -1; \
+        if (clear) {                                                                       \
+            const int z = 0;                                                               \
+            if (cudaMemcpyToSymbol(hla2_dbg_word, &z, sizeof(int)) != cudaSuccess) return -1; \
+        }                                                                                  \
+        return v;                                                                          \
+    }                                                                                      \
+    }
+#else
+#define HLA2_IN(cond, site) true
+#define HLA2_DEBUG_READER(name)
+#endif
+
+// ---------------------------------------------------------------------------
 // Element access
 // ---------------------------------------------------------------------------
 

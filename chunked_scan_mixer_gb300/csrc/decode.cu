@@ -24,8 +24,19 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxDim = 128;
 
-__device__ __forceinline__ float4 ld_stream(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
-__device__ __forceinline__ void st_stream(float* p, float4 v) { __stcs(reinterpret_cast<float4*>(p), v); }
+// 128-bit streaming state accesses.  Win is the state block the access must stay in: the
+// debug build checks it (HLA2_IN) and skips an access outside it; the normal build ignores it.
+struct Win {
+    const float* lo;
+    const float* hi;
+};
+__device__ __forceinline__ float4 ld_stream(const float* p, const Win& w) {
+    if (!HLA2_IN(p >= w.lo && p + 4 <= w.hi, 301)) return make_float4(0.f, 0.f, 0.f, 0.f);
+    return __ldcs(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ void st_stream(float* p, float4 v, const Win& w) {
+    if (HLA2_IN(p >= w.lo && p + 4 <= w.hi, 302)) __stcs(reinterpret_cast<float4*>(p), v);
+}
 
 template <int NT = kThreads>
 __device__ __forceinline__ float block_sum(float x, float* red) {
@@ -76,7 +87,9 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ __align__(16) float red[kWarps * kMaxDim];
     const int head = blockIdx.x, tid = threadIdx.x;
     const float g = head_decay(gamma, head, H), g2 = g * g;
-    float* S = state + (size_t)head * (COMPACT ? compact_state_floats(d, dv) : raw_state_floats(d, dv));
+    const size_t sf = COMPACT ? compact_state_floats(d, dv) : raw_state_floats(d, dv);
+    float* S = state + (size_t)head * sf;
+    const Win win{S, S + sf};
     const PackOff po = COMPACT ? compact_off(d, dv) : pack_off(d, dv);
     float *C = S + po.C, *G = S + po.G, *m = S + po.m, *hh = S + po.h;
 
@@ -113,7 +126,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int a = a0 + u * rows_per;
-                if (a < d && l >= (a >> 2)) x[u] = ld_stream(S + compact_row(a, d) + (size_t)(c - 4 * (a >> 2)));
+                if (a < d && l >= (a >> 2)) x[u] = ld_stream(S + compact_row(a, d) + (size_t)(c - 4 * (a >> 2)), win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -126,7 +139,7 @@ __global__ void __launch_bounds__(kThreads)
                     y.y = g * y.y + ka * ks[c + 1];
                     y.z = g * y.z + ka * ks[c + 2];
                     y.w = g * y.w + ka * ks[c + 3];
-                    st_stream(S + compact_row(a, d) + (size_t)(c - 4 * (a >> 2)), y);
+                    st_stream(S + compact_row(a, d) + (size_t)(c - 4 * (a >> 2)), y, win);
                     part = y.x * qs[c] + y.y * qs[c + 1] + y.z * qs[c + 2] + y.w * qs[c + 3];
                     if (l > (a >> 2)) {
                         const float qa = qs[a];
@@ -150,7 +163,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int i = base + u * kThreads + tid;
-                if (i < n4) x[u] = ld_stream(S + (size_t)i * 4);
+                if (i < n4) x[u] = ld_stream(S + (size_t)i * 4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -164,7 +177,7 @@ __global__ void __launch_bounds__(kThreads)
                     y.y = g * y.y + ka * ks[c + 1];
                     y.z = g * y.z + ka * ks[c + 2];
                     y.w = g * y.w + ka * ks[c + 3];
-                    st_stream(S + (size_t)i * 4, y);
+                    st_stream(S + (size_t)i * 4, y, win);
                     part = y.x * qs[c] + y.y * qs[c + 1] + y.z * qs[c + 2] + y.w * qs[c + 3];
                 }
                 // all lanes of a row group take part (rows are aligned to lpr lanes)
@@ -198,7 +211,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int a = a0 + u * rows_per;
-                if (a < d) x[u] = ld_stream(C + (size_t)a * dv + c4);
+                if (a < d) x[u] = ld_stream(C + (size_t)a * dv + c4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -212,7 +225,7 @@ __global__ void __launch_bounds__(kThreads)
                 y.z = g * y.z + qa * vs[c4 + 2];
                 y.w = g * y.w + qa * vs[c4 + 3];
                 pw.x += ua * y.x; pw.y += ua * y.y; pw.z += ua * y.z; pw.w += ua * y.w;
-                st_stream(C + (size_t)a * dv + c4, y);
+                st_stream(C + (size_t)a * dv + c4, y, win);
             }
         }
         if (!UM) column_reduce(pr, dv, red, rs);
@@ -231,7 +244,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int a = a0 + u * rows_per;
-                if (a < d) x[u] = ld_stream(G + (size_t)a * dv + c4);
+                if (a < d) x[u] = ld_stream(G + (size_t)a * dv + c4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -244,7 +257,7 @@ __global__ void __launch_bounds__(kThreads)
                 y.z = g2 * y.z + gk * r4.z;
                 y.w = g2 * y.w + gk * r4.w;
                 pz.x += qa * y.x; pz.y += qa * y.y; pz.z += qa * y.z; pz.w += qa * y.w;
-                st_stream(G + (size_t)a * dv + c4, y);
+                st_stream(G + (size_t)a * dv + c4, y, win);
             }
         }
         column_reduce(pz, dv, red, zs);
@@ -275,6 +288,7 @@ __global__ void __launch_bounds__(kThreads)
     const int head = blockIdx.x, tid = threadIdx.x;
     const float g = head_decay(gamma, head, H);
     float* P = state + (size_t)head * (2 * (size_t)d * dv + 2 * (size_t)d);
+    const Win win{P, P + 2 * (size_t)d * dv + 2 * (size_t)d};
     float* E = P + (size_t)d * dv;
     float* m = E + (size_t)d * dv;
     float* nn = m + d;
@@ -294,7 +308,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int a = a0 + u * rows_per;
-                if (a < d) x[u] = ld_stream(P + (size_t)a * dv + c4);
+                if (a < d) x[u] = ld_stream(P + (size_t)a * dv + c4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -307,7 +321,7 @@ __global__ void __launch_bounds__(kThreads)
                 y.z = g * y.z + ka * vs[c4 + 2];
                 y.w = g * y.w + ka * vs[c4 + 3];
                 pi.x += qa * y.x; pi.y += qa * y.y; pi.z += qa * y.z; pi.w += qa * y.w;
-                st_stream(P + (size_t)a * dv + c4, y);
+                st_stream(P + (size_t)a * dv + c4, y, win);
             }
         }
         column_reduce(pi, dv, red, is);
@@ -321,7 +335,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int a = a0 + u * rows_per;
-                if (a < d) x[u] = ld_stream(E + (size_t)a * dv + c4);
+                if (a < d) x[u] = ld_stream(E + (size_t)a * dv + c4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -334,7 +348,7 @@ __global__ void __launch_bounds__(kThreads)
                 y.z = g * y.z + ka * i4.z;
                 y.w = g * y.w + ka * i4.w;
                 po.x += qa * y.x; po.y += qa * y.y; po.z += qa * y.z; po.w += qa * y.w;
-                st_stream(E + (size_t)a * dv + c4, y);
+                st_stream(E + (size_t)a * dv + c4, y, win);
             }
         }
         column_reduce(po, dv, red, os);
@@ -405,6 +419,7 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ __align__(16) float red[kWarps * kMaxDim];
     const int head = blockIdx.x, tid = threadIdx.x;
     float* S = state + (size_t)head * ((size_t)d * d + 2 * (size_t)d * dv + 2 * (size_t)d);
+    const Win win{S, S + (size_t)d * d + 2 * (size_t)d * dv + 2 * (size_t)d};
     float* P = S + (size_t)d * d;
     float* Y = P + (size_t)d * dv;
     float* m = Y + (size_t)d * dv;
@@ -424,7 +439,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int i = base + u * kThreads + tid;
-                if (i < n4) x[u] = ld_stream(S + (size_t)i * 4);
+                if (i < n4) x[u] = ld_stream(S + (size_t)i * 4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -438,7 +453,7 @@ __global__ void __launch_bounds__(kThreads)
                     z.y += ka * ks[c + 1];
                     z.z += ka * ks[c + 2];
                     z.w += ka * ks[c + 3];
-                    st_stream(S + (size_t)i * 4, z);
+                    st_stream(S + (size_t)i * 4, z, win);
                     part = z.x * qs[c] + z.y * qs[c + 1] + z.z * qs[c + 2] + z.w * qs[c + 3];
                 }
                 for (int o = lpr >> 1; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
@@ -465,7 +480,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int a = a0 + u * rows_per;
-                if (a < d) x[u] = ld_stream(P + (size_t)a * dv + c4);
+                if (a < d) x[u] = ld_stream(P + (size_t)a * dv + c4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -478,7 +493,7 @@ __global__ void __launch_bounds__(kThreads)
                 z.z += ka * vs[c4 + 2];
                 z.w += ka * vs[c4 + 3];
                 pu.x += qa * z.x; pu.y += qa * z.y; pu.z += qa * z.z; pu.w += qa * z.w;
-                st_stream(P + (size_t)a * dv + c4, z);
+                st_stream(P + (size_t)a * dv + c4, z, win);
             }
         }
         column_reduce(pu, dv, red, us);
@@ -492,7 +507,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int a = a0 + u * rows_per;
-                if (a < d) x[u] = ld_stream(Y + (size_t)a * dv + c4);
+                if (a < d) x[u] = ld_stream(Y + (size_t)a * dv + c4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -505,7 +520,7 @@ __global__ void __launch_bounds__(kThreads)
                 z.z += pa * u4.z;
                 z.w += pa * u4.w;
                 po.x += qa * z.x; po.y += qa * z.y; po.z += qa * z.z; po.w += qa * z.w;
-                st_stream(Y + (size_t)a * dv + c4, z);
+                st_stream(Y + (size_t)a * dv + c4, z, win);
             }
         }
         column_reduce(po, dv, red, os);
@@ -550,6 +565,7 @@ __global__ void __launch_bounds__(kThreads)
     const int r = (int)cluster.block_rank();  // == head % group
     const float g = head_decay(gamma, grp, Hk), g2 = g * g;
     float* S = key_state + (size_t)grp * d * d;
+    Win win{S, S + (size_t)d * d};  // the key group's S; the head's block from pass C on
 
     for (int i = tid; i < d; i += kThreads) ks[i] = to_f32(k[(size_t)grp * d + i]);
     for (int i = tid; i < dv; i += kThreads) vs[i] = to_f32(v[(size_t)grp * dv + i]);
@@ -569,7 +585,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int a = a0 + u * rows_per;
-                if (a < hi) x[u] = ld_stream(S + (size_t)a * d + c4);
+                if (a < hi) x[u] = ld_stream(S + (size_t)a * d + c4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -583,7 +599,7 @@ __global__ void __launch_bounds__(kThreads)
                     y.y = g * y.y + ka * ks[c4 + 1];
                     y.z = g * y.z + ka * ks[c4 + 2];
                     y.w = g * y.w + ka * ks[c4 + 3];
-                    st_stream(S + (size_t)a * d + c4, y);
+                    st_stream(S + (size_t)a * d + c4, y, win);
                 }
                 for (int i = 0; i < group; ++i) {  // every lane takes part in the shuffles
                     float part = y.x * qs[i][c4] + y.y * qs[i][c4 + 1] + y.z * qs[i][c4 + 2] + y.w * qs[i][c4 + 3];
@@ -600,6 +616,7 @@ __global__ void __launch_bounds__(kThreads)
     // ---- this head: m, h, pass C, pass G, output ----------------------------------------------
     const size_t hsf = 2 * (size_t)d * dv + 2 * (size_t)d;
     float* C = head_state + (size_t)head * hsf;
+    win = Win{C, C + hsf};
     float* G = C + (size_t)d * dv;
     float* m = G + (size_t)d * dv;
     float* hh = m + d;
@@ -640,7 +657,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int a = a0 + u * rows_per;
-                if (a < d) x[u] = ld_stream(C + (size_t)a * dv + c4);
+                if (a < d) x[u] = ld_stream(C + (size_t)a * dv + c4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -654,7 +671,7 @@ __global__ void __launch_bounds__(kThreads)
                 y.z = g * y.z + qa * vs[c4 + 2];
                 y.w = g * y.w + qa * vs[c4 + 3];
                 pw.x += ua * y.x; pw.y += ua * y.y; pw.z += ua * y.z; pw.w += ua * y.w;
-                st_stream(C + (size_t)a * dv + c4, y);
+                st_stream(C + (size_t)a * dv + c4, y, win);
             }
         }
         if (!UM) column_reduce(pr, dv, red, rs);
@@ -668,7 +685,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int a = a0 + u * rows_per;
-                if (a < d) x[u] = ld_stream(G + (size_t)a * dv + c4);
+                if (a < d) x[u] = ld_stream(G + (size_t)a * dv + c4, win);
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -681,7 +698,7 @@ __global__ void __launch_bounds__(kThreads)
                 y.z = g2 * y.z + gk * r4.z;
                 y.w = g2 * y.w + gk * r4.w;
                 pz.x += qa * y.x; pz.y += qa * y.y; pz.z += qa * y.z; pz.w += qa * y.w;
-                st_stream(G + (size_t)a * dv + c4, y);
+                st_stream(G + (size_t)a * dv + c4, y, win);
             }
         }
         column_reduce(pz, dv, red, zs);
@@ -800,3 +817,5 @@ int launch_state_compact(const float* src, float* dst, long heads, int d, int dv
 }
 
 }  // namespace hla2
+
+HLA2_DEBUG_READER(decode)

@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
         tc::tmem_alloc(tmem_holder, la::kTmemCols);
     } else {
         // carry-in of the segment (zero without one), as stored, transposed or symmetrised
-        if (a.carry) {
+        if (a.carry && HLA2_IN(bh < a.BH && seg < a.nseg, 801)) {
             const float* src = a.carry + ((size_t)bh * a.nseg + seg) * la::kD * la::kD;
             if (a.carry_mode == 0) {
 #pragma unroll
@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                 if (j + 1 < nit) epi1(j + 1);
             }
         }
-        if (NSUM && nit > 0) {  // the segment's next summary -> global (fp32)
+        if (NSUM && nit > 0 && HLA2_IN(bh < a.BH && seg < a.nseg, 802)) {  // the segment's next summary (fp32)
             tc::mbar_wait(&bars[la::BN], (nit - 1) & 1, abort, status, 118);
             tc::fence_after_sync();
             float* dst = a.summary + ((size_t)bh * a.nseg + seg) * la::kD * la::kD + (size_t)r * la::kD + 64 * h;
@@ -701,7 +701,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[las::T0 + s]);
         }
-        if (nit > 0) {
+        if (nit > 0 && HLA2_IN(bh < a.BH && seg < a.nseg, 803)) {
             tc::mbar_wait(&bars[las::N0 + ((nit - 1) & 1)], ((nit - 1) >> 1) & 1, abort, status, 124);
             tc::fence_after_sync();
             float* dst = a.summary + ((size_t)bh * a.nseg + seg) * la::kD * la::kD + (size_t)r * la::kD + 64 * h;
@@ -835,3 +835,5 @@ int launch_fo_tc_out(const FoArgs& a, const void* x, const void* k, const void* 
 }
 
 }  // namespace hla2
+
+HLA2_DEBUG_READER(fo_tc)

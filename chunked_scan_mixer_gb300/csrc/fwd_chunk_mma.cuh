@@ -113,9 +113,13 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
     const float* Cinit = nullptr;
     if (!SUMMARY) {
         const size_t sidx = (size_t)bh * nseg + seg;
-        Sinit = a.ws + a.L.Sin + sidx * D * D;
-        Zinit = a.ws + a.L.Zin + sidx * D * DV;
-        if (CM) Cinit = a.ws + a.L.Clast + (size_t)bh * D * DV;
+        if (HLA2_IN(a.L.Sin + (sidx + 1) * D * D <= a.L.total && a.L.Zin + (sidx + 1) * D * DV <= a.L.total &&
+                        a.L.Clast + (size_t)(bh + 1) * D * DV <= a.L.total,
+                    401)) {
+            Sinit = a.ws + a.L.Sin + sidx * D * D;
+            Zinit = a.ws + a.L.Zin + sidx * D * DV;
+            if (CM) Cinit = a.ws + a.L.Clast + (size_t)bh * D * DV;
+        }
     }
 #pragma unroll
     for (int s = 0; s < Cfg::S_PER; ++s) {
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         constexpr int CPR = D / 8, CPRV = DV / 8;  // 16-byte pieces per row
         for (int i = tid; i < W * CPR; i += NT) {
             const int r = i / CPR, p = (i % CPR) * 8;
-            if (r < Wc) {
+            if (r < Wc && HLA2_IN(row0 + r < a.n, 402)) {
                 cp_async16(&Qs[r * LD + p], q + (size_t)(row0 + r) * D + p);
                 cp_async16(&Ks[r * LD + p], k + (size_t)(row0 + r) * D + p);
             } else {
@@ -195,7 +199,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         }
         for (int i = tid; i < W * CPRV; i += NT) {
             const int r = i / CPRV, p = (i % CPRV) * 8;
-            if (r < Wc)
+            if (r < Wc && HLA2_IN(row0 + r < a.n, 403))
                 cp_async16(&Vs[r * LDV + p], v + (size_t)(row0 + r) * DV + p);
             else
                 *reinterpret_cast<uint4*>(&Vs[r * LDV + p]) = make_uint4(0, 0, 0, 0);
@@ -209,7 +213,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         cp_async_wait_all();
         __syncthreads();
 
-        if (EXPORT) {  // export the state at this chunk start
+        if (EXPORT && HLA2_IN(bh < a.BH && c < a.nchunks, 404)) {  // export the state at this chunk start
             bf16* dst = a.chunk_states + ((size_t)bh * a.nchunks + c) * (size_t)(D * D + D * DV);
             for (int i = tid; i < D * D / 8; i += NT) {
                 const int r = (i * 8) / D, f = (i * 8) % D;
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
 #pragma unroll
                     for (int i = 0; i < 4; i += 2) {
                         const int r = acc_row(rb * 16, i), col = acc_col(eb * 16, h, i);
-                        if (r >= Wc) continue;
+                        if (r >= Wc || !HLA2_IN(c * W + r < a.n, 405)) continue;
                         float o0 = acc[h][i], o1 = acc[h][i + 1];
                         if (a.normalize) {
                             const float inv = 1.f / (den[r] + a.eps);
@@ -444,7 +448,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
         dm = base + ro.m;
         dy = base + ro.y;
     }
-    if (dS) {
+    if (dS && HLA2_IN(dS >= a.ws && (size_t)(dy + D - a.ws) <= a.L.total, 406)) {
 #pragma unroll
         for (int s = 0; s < Cfg::S_PER; ++s) {
             const int t = warp + s * NW;

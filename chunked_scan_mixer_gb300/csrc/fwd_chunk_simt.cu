@@ -60,14 +60,15 @@ __global__ void __launch_bounds__(kSimtThreads)
 
     // initial state: zero (summary) or the segment's carry-in
     const size_t sidx = (size_t)bh * nseg + seg;
-    for (int i = tid; i < D * D; i += NT) S[i] = summary ? 0.f : a.ws[a.L.Sin + sidx * D * D + i];
+    auto wsr = [&](size_t idx, int site) { return HLA2_IN(idx < a.L.total, site) ? a.ws[idx] : 0.f; };
+    for (int i = tid; i < D * D; i += NT) S[i] = summary ? 0.f : wsr(a.L.Sin + sidx * D * D + i, 201);
     for (int i = tid; i < D * DV; i += NT) {
-        Z[i] = summary ? 0.f : a.ws[a.L.Zin + sidx * D * DV + i];
-        if (cm) C[i] = summary ? 0.f : a.ws[a.L.Clast + (size_t)bh * D * DV + i];
+        Z[i] = summary ? 0.f : wsr(a.L.Zin + sidx * D * DV + i, 202);
+        if (cm) C[i] = summary ? 0.f : wsr(a.L.Clast + (size_t)bh * D * DV + i, 203);
     }
     for (int i = tid; i < D; i += NT) {
-        y[i] = summary ? 0.f : a.ws[a.L.yin + sidx * D + i];
-        m[i] = (cm && !summary) ? a.ws[a.L.mlast + (size_t)bh * D + i] : 0.f;
+        y[i] = summary ? 0.f : wsr(a.L.yin + sidx * D + i, 204);
+        m[i] = (cm && !summary) ? wsr(a.L.mlast + (size_t)bh * D + i, 205) : 0.f;
     }
 
     for (int c = c_begin; c < c_end; ++c) {
@@ -75,17 +76,21 @@ __global__ void __launch_bounds__(kSimtThreads)
         const int Wc = min(W, a.n - row0);
         __syncthreads();
         if (!summary && a.chunk_states_f32) {  // the state at this chunk start, for the backward
-            float* dst = a.chunk_states_f32 + ((size_t)bh * a.nchunks + c) * (size_t)(D * D + D * DV);
-            for (int i = tid; i < D * D; i += NT) dst[i] = S[i];
-            for (int i = tid; i < D * DV; i += NT) dst[(size_t)D * D + i] = Z[i];
+            const size_t cs = (size_t)(D * D + D * DV), base = ((size_t)bh * a.nchunks + c) * cs;
+            float* dst = a.chunk_states_f32 + base;
+            const bool ok = HLA2_IN(bh < a.BH && c < a.nchunks && base + cs <= (size_t)a.BH * a.nchunks * cs, 206);
+            for (int i = tid; ok && i < D * D; i += NT) dst[i] = S[i];
+            for (int i = tid; ok && i < D * DV; i += NT) dst[(size_t)D * D + i] = Z[i];
         }
         for (int i = tid; i < W * D; i += NT) {
             const int r = i / D;
-            Qs[i] = r < Wc ? to_f32(q[(size_t)row0 * D + i]) : 0.f;
-            Ks[i] = r < Wc ? to_f32(k[(size_t)row0 * D + i]) : 0.f;
+            const bool in = r < Wc && HLA2_IN((size_t)row0 * D + i < (size_t)a.n * D, 207);
+            Qs[i] = in ? to_f32(q[(size_t)row0 * D + i]) : 0.f;
+            Ks[i] = in ? to_f32(k[(size_t)row0 * D + i]) : 0.f;
         }
         for (int i = tid; i < W * DV; i += NT)
-            Vs[i] = (i / DV) < Wc ? to_f32(v[(size_t)row0 * DV + i]) : 0.f;
+            Vs[i] = ((i / DV) < Wc && HLA2_IN((size_t)row0 * DV + i < (size_t)a.n * DV, 208))
+                        ? to_f32(v[(size_t)row0 * DV + i]) : 0.f;
         __syncthreads();
 
         // A~[r, i] = [i <= r] g^(r-i) q_r . k_i ; den carry term
@@ -153,7 +158,7 @@ __global__ void __launch_bounds__(kSimtThreads)
                 for (int j = 0; j <= r; ++j) s1 += AB[r * W + j] * Vs[j * DV + x];
                 float o = gp[bp * (r + 1)] * s0 + s1;
                 if (a.normalize) o /= (den[r] + a.eps);
-                out[e] = from_f32<T>(o);
+                if (HLA2_IN(row0 + r < a.n && bh < a.BH, 209)) out[e] = from_f32<T>(o);
             }
             __syncthreads();
         }
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(kSimtThreads)
         dm = base + ro.m;
         dy = base + ro.y;
     }
-    if (dS) {
+    if (dS && HLA2_IN((size_t)(dy + D - a.ws) <= a.L.total && dS >= a.ws, 210)) {
         for (int i = tid; i < D * D; i += NT) dS[i] = S[i];
         for (int i = tid; i < D * DV; i += NT) {
             dZ[i] = Z[i];
@@ -247,3 +252,5 @@ int launch_fwd_chunk_simt(const ChunkArgs& a, int d, int dv, int W, bool summary
 }
 
 }  // namespace hla2
+
+HLA2_DEBUG_READER(fwd_simt)

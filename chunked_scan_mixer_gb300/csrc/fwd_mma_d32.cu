@@ -24,3 +24,5 @@ size_t fwd_chunk_mma_smem_d32(int W, bool cm) {
 }
 
 }  // namespace hla2
+
+HLA2_DEBUG_READER(fwd_mma_d32)

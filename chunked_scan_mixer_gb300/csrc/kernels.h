@@ -281,6 +281,26 @@ int launch_fo_tc_out(const FoArgs& a, const void* x, const void* k, const void* 
 
 // Bounded-wait self-test: waits on an mbarrier nobody arrives at; records site 90 in *status.
 int launch_wait_timeout_selftest(int* status, cudaStream_t st);
+// Debug build: one failing bounds check (site 1) that guards no access.
+int launch_debug_check_selftest(cudaStream_t st);
+#ifdef HLA2_DEBUG
+// Debug words of the files with bounds checks (HLA2_DEBUG_READER): the recorded site or 0;
+// clear resets the word.
+int dbg_read_fwd_simt(bool clear);
+int dbg_read_decode(bool clear);
+int dbg_read_fwd_mma_d16(bool clear);
+int dbg_read_fwd_mma_d32(bool clear);
+int dbg_read_fwd_mma_d64(bool clear);
+int dbg_read_fwd_mma_d128(bool clear);
+int dbg_read_bwd_mma_d16(bool clear);
+int dbg_read_bwd_mma_d32(bool clear);
+int dbg_read_bwd_mma_d64(bool clear);
+int dbg_read_bwd_mma_d128(bool clear);
+int dbg_read_bwd_simt(bool clear);
+int dbg_read_scan(bool clear);
+int dbg_read_fo_tc(bool clear);
+int dbg_read_selftest(bool clear);
+#endif
 int launch_state_compact(const float* src, float* dst, long heads, int d, int dv, bool to_compact, cudaStream_t st);
 
 }  // namespace hla2

@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(kThreads)
     const float rho = pow_decay(log2f(head_decay(gamma, bh, H)), (float)step_tokens * (float)power);
     const float* s = src + (size_t)bh * src_hs + e;
     float* d = dst + (size_t)bh * dst_hs + e;
+    // every access below stays in head bh's part of src and dst (debug build: checked once)
+    if (!HLA2_IN(e < E && (size_t)nsteps * E <= src_hs && (size_t)(store_all ? nsteps : 0) * E < dst_hs, 701)) return;
     float acc = d[0];
     constexpr int U = 8;
     int t = 0;
@@ -485,6 +487,7 @@ __global__ void __launch_bounds__(kThreads)
     const float log2g = log2f(head_decay(gamma, bh, H));
     const float* s_ = src + (size_t)bh * nseg * E + e;
     float* d_ = dst + (size_t)bh * nseg * E + e;
+    if (!HLA2_IN(e < E && nseg >= 1, 702)) return;
     float acc = 0.f;
     d_[(size_t)(nseg - 1) * E] = 0.f;
     for (int s = nseg - 1; s >= 1; --s) {
@@ -595,3 +598,5 @@ int launch_reverse_cross(const BwdArgs& b, const float* CB, int d, int dv, cudaS
 }
 
 }  // namespace hla2
+
+HLA2_DEBUG_READER(scan)

@@ -28,6 +28,14 @@ __global__ void __launch_bounds__(32) wait_timeout_kernel(int* status) {
     __syncthreads();
 }
 
+// Debug build only: one failing bounds check that guards no access, so that the recording of
+// a check's site can be tested without an out-of-bounds access anywhere.
+constexpr int kDebugSelfTestSite = 1;
+__global__ void debug_check_kernel(int* sink) {
+    if (!HLA2_IN(threadIdx.x > 0, kDebugSelfTestSite)) return;  // thread 0 records the site
+    (void)sink;
+}
+
 }  // namespace
 
 int launch_wait_timeout_selftest(int* status, cudaStream_t st) {
@@ -35,4 +43,11 @@ int launch_wait_timeout_selftest(int* status, cudaStream_t st) {
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
+int launch_debug_check_selftest(cudaStream_t st) {
+    debug_check_kernel<<<1, 32, 0, st>>>(nullptr);
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
 }  // namespace hla2
+
+HLA2_DEBUG_READER(selftest)

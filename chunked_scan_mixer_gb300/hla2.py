@@ -101,6 +101,10 @@ def lib():
         L.hla2_noalloc_status.restype = I
         L.hla2_noalloc_selftest_wait_timeout.argtypes = [P]
         L.hla2_noalloc_selftest_wait_timeout.restype = I
+        L.hla2_debug_status.argtypes = [I]
+        L.hla2_debug_status.restype = I
+        L.hla2_debug_selftest.argtypes = [P]
+        L.hla2_debug_selftest.restype = I
         L.hla2_ahla_forward_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I]
         L.hla2_ahla_forward_workspace_bytes.restype = Z
         L.hla2_ahla_forward.argtypes = [P, P, P, P, I, I, I, I, I, P, I, I, P, ctypes.POINTER(Opts)]
@@ -142,7 +146,7 @@ EXPORTED_SYMBOLS = (
     "hla2_ahla_state_floats", "hla2_ahla_decode_step", "hla2_mq_head_state_floats", "hla2_decode_step_mq",
     "hla2_selftest_wait_timeout", "hla2_hla3_forward_workspace_bytes", "hla2_hla3_forward", "hla2_hla3_decode_step",
     "hla2_ahla_backward_workspace_bytes", "hla2_ahla_backward", "hla2_noalloc_status",
-    "hla2_noalloc_selftest_wait_timeout",
+    "hla2_noalloc_selftest_wait_timeout", "hla2_debug_status", "hla2_debug_selftest",
 )
 
 FLAG_COMPACT_STATE = 4

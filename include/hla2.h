@@ -184,6 +184,22 @@ int hla2_workspace_status(const void* workspace, hla2_stream_t stream);
  */
 int hla2_selftest_wait_timeout(void* workspace, hla2_stream_t stream);
 
+/*
+ * Debug build (the library compiled with HLA2_DEBUG, as `python -m chunked_scan_mixer_gb300.build
+ * --debug` makes it in chunked_scan_mixer_gb300/_build_debug/): the kernels of the float32 and
+ * mma.sync chunk paths, the forward and backward inter-segment scans, the decode steps and the
+ * tcgen05 first-order scans check the indices of their global-memory accesses against the
+ * buffers' extents.  A failed check records a site code (positive) in a device word, skips
+ * the access and lets the kernel finish: nothing traps.
+ * hla2_debug_status synchronises the device and returns the first recorded site, 0 when every
+ * check passed since the last clear (clear != 0 resets the words), or HLA2_ERR_UNSUPPORTED in
+ * the normal build.  hla2_debug_selftest launches one kernel whose only check fails without
+ * guarding any access, so that hla2_debug_status then reports site 1 (HLA2_ERR_UNSUPPORTED in
+ * the normal build).
+ */
+int hla2_debug_status(int clear);
+int hla2_debug_selftest(hla2_stream_t stream);
+
 /* Scratch bytes hla2_backward needs; (size_t)-1 for rejected arguments. */
 size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
                                      int normalize);

@@ -193,3 +193,12 @@ def test_compact_state_abi(L):
     assert L.hla2_state_to_compact(p, p, 1, 1, 20, 16, None) == -1      # bad d
     assert L.hla2_state_to_compact(None, None, 0, 4, 16, 16, None) == 0  # nothing to do
     assert L.hla2_state_from_compact(p, p, 1, 1, 16, 16, None) == -1     # overlapping buffers
+
+
+def test_debug_queries_report_a_normal_build():
+    """The normal build has no bounds checks: both debug entry points answer
+    HLA2_ERR_UNSUPPORTED (without touching a device)."""
+    L = hla.lib()
+    assert L.hla2_debug_status(0) == -2
+    assert b"debug build" in L.hla2_last_error()
+    assert L.hla2_debug_selftest(None) == -2
