@@ -309,6 +309,12 @@ namespace {
 int forward_saving_for_backward(const void* q, const void* k, const void* v, void* out, int B, int H, int n, int d,
                                 int dv, const float* gamma, int normalize, int chunk, cudaStream_t st,
                                 const hla2_opts* opts);
+// Plain forward on the tcgen05 first-order scans (bf16, d = dv = 128, chunk >= 128, masked,
+// unnormalised, no state in or out): its workspace bytes (0: not this path), and the call.
+size_t fo_forward_ws(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize);
+int fo_forward_call(const void* q, const void* k, const void* v, void* out, int B, int H, int n, const float* gamma,
+                    cudaStream_t st, const hla2_opts* opts);
+Plan fo_plan(int B, int H, int n, const DevInfo& di);
 }  // namespace
 
 extern "C" {
@@ -325,8 +331,12 @@ size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chun
     const DevInfo di = dev_info();
     const int W = forward_width(dtype, d, dv, chunk, normalize, di);
     if (!W) return (size_t)-1;  // hla2_forward rejects these sizes (HLA2_ERR_UNSUPPORTED)
-    return forward_ws(forward_plan(B, H, n, d, dv, W, dtype, normalize, want_final_state != 0, di),
-                      want_final_state != 0);
+    const size_t ws = forward_ws(forward_plan(B, H, n, d, dv, W, dtype, normalize, want_final_state != 0, di),
+                                 want_final_state != 0);
+    // masked calls without a state run on the first-order scans; the unmasked output and
+    // calls with init_state keep the chunk kernels (flags the query does not see): the larger
+    const size_t fo = want_final_state ? 0 : fo_forward_ws(B, H, n, d, dv, chunk, dtype, normalize);
+    return fo > ws ? fo : ws;
 }
 
 int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
@@ -385,6 +395,8 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         return forward_saving_for_backward(q, k, v, out, B, H, n, d, dv, gamma, normalize, chunk, st, opts);
 
     const DevInfo di = dev_info();
+    if (!unmasked && !want_final && !opts->init_state && fo_forward_ws(B, H, n, d, dv, chunk, opts->dtype, normalize))
+        return fo_forward_call(q, k, v, out, B, H, n, gamma, st, opts);  // (at the width asked for)
     {
         const int W = forward_width(opts->dtype, d, dv, chunk, normalize, di);
         if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no kernel for dtype %d, d %d, dv %d, chunk %d", opts->dtype, d, dv, chunk);
@@ -570,6 +582,14 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     const DevInfo di = dev_info();
     const int W = forward_width(dtype, d, dv, chunk, normalize, di);
     if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no forward kernel for d %d, dv %d at chunk <= %d", d, dv, chunk);
+    if (!want_final_state && fo_forward_ws(B, H, n, d, dv, chunk, dtype, normalize)) {
+        // first-order scans: S summaries, zero + scan, p pass, zero + scan, output pass
+        const Plan p = fo_plan(B, H, n, di);
+        if (nseg) *nseg = p.nseg;
+        if (seg_chunks) *seg_chunks = p.seg_chunks;
+        if (launches) *launches = p.nseg > 0 ? 7 : 0;
+        return succeed();
+    }
     chunk = W;
     const Plan p = forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, di);
     int l = 0;
@@ -956,6 +976,38 @@ int fo_reverse_part(const void* q, const void* k, const void* v, const void* dou
     a.carry_mode = 0;
     if (launch_fo_tc_out(a, dP, k, nullptr, false, 0, nullptr, dqa, dq, false, st)) return cuda_fail("dq pass");
     return HLA2_OK;
+}
+
+size_t fo_forward_ws(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
+    const DevInfo di = dev_info();
+    if (!fo_path(dtype, d, dv, chunk, normalize, di)) return 0;
+    const Plan p = fo_plan(B, H, n, di);
+    return p.nseg > 0 ? fo_layout(p).fwd_total : 0;
+}
+
+int fo_forward_call(const void* q, const void* k, const void* v, void* out, int B, int H, int n, const float* gamma,
+                    cudaStream_t st, const hla2_opts* opts) {
+    const DevInfo di = dev_info();
+    const Plan p = fo_plan(B, H, n, di);
+    const FoLayout L = fo_layout(p);
+    if (!opts->workspace || opts->workspace_bytes < L.fwd_total)
+        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.fwd_total,
+                    opts->workspace ? opts->workspace_bytes : (size_t)0);
+    if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    char* ws = static_cast<char*>(opts->workspace);
+    auto mark = [&](int i) {
+        if (opts->phase_events && i < opts->n_phase_events && opts->phase_events[i] &&
+            cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[i]), st) != cudaSuccess)
+            cudaGetLastError();
+    };
+    cudaGetLastError();
+    mark(0);
+    int rc = fo_forward_part(q, k, v, p, gamma, ws, L, st);
+    mark(3);
+    if (rc == HLA2_OK) rc = fo_output_pass(q, v, out, p, gamma, ws, L, st);
+    mark(4);
+    mark(5);
+    return rc == HLA2_OK ? succeed() : rc;
 }
 
 int check_backward(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {

@@ -135,9 +135,11 @@ def test_chunk_wider_than_the_kernels_runs_narrower(dtype, d, dv):
     got_f, want_f = O.unpack_state(np64(fin.cpu()), d, dv), O.unpack_state(np64(f.cpu()), d, dv)
     for key in ("S", "C", "m", "G", "h"):
         assert rel_err(got_f[key], want_f[key]) <= 1e-4, key
-    assert hla.forward_plan(1, 3, 1000, d, dv, 128, dtype) == hla.forward_plan(1, 3, 1000, d, dv, W, dtype)
-    assert hla.forward_workspace_bytes(1, 3, 1000, d, dv, 128, dtype) == \
-        hla.forward_workspace_bytes(1, 3, 1000, d, dv, W, dtype)
+    # the queries for the same call (with a final state) as the one compared above
+    assert hla.forward_plan(1, 3, 1000, d, dv, 128, dtype, want_final_state=True) == \
+        hla.forward_plan(1, 3, 1000, d, dv, W, dtype, want_final_state=True)
+    assert hla.forward_workspace_bytes(1, 3, 1000, d, dv, 128, dtype, want_final_state=True) == \
+        hla.forward_workspace_bytes(1, 3, 1000, d, dv, W, dtype, want_final_state=True)
     ref, ref_state = oracle(x, return_state=True)
     assert rel_err(np64(got.cpu()), ref) <= tol_for(dtype)
     got_s, want_s = O.unpack_state(np64(fin.cpu()), d, dv), O.unpack_state(ref_state, d, dv)

@@ -1,5 +1,5 @@
 """The d = dv = 128 bf16 training path on the tcgen05 first-order scan kernel (chunk 128),
-through the C ABI, against the float64 oracle.
+and the plain forward on the same passes, through the C ABI, against the float64 oracle.
 
 The masked output is two chained first-order scans (p = S q, then o = q^T Z) and its reverse
 mode six more; every pass runs segment-parallel on the same kernel.  Bar: max|gpu - oracle| /
@@ -117,3 +117,34 @@ def test_distinct_from_the_legacy_path():
     _check_grads(tc, x, "tcgen05")
     _check_grads(legacy, x, "mma.sync")
     assert not all(torch.equal(a, b) for a, b in zip(tc, legacy))
+
+
+@pytest.mark.parametrize("B, H, n", [(1, 2, 1000), (2, 3, 129), (1, 1, 1), (1, 4, 3000)])
+@pytest.mark.parametrize("gamma", [None, (0.9, 0.999)])
+def test_forward_matches_oracle(B, H, n, gamma):
+    """The plain forward (no state in or out) runs the same first-order passes."""
+    x = inputs.make_custom(B, H, n, D, D, torch.bfloat16, seed=7 * n + H, gamma=gamma)
+    g = None if x["gamma"] is None else x["gamma"].cuda()
+    o = hla.forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), gamma=g, chunk=128)
+    ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), _gamma_np(x))
+    assert rel_err(np64(o.cpu()), ref) <= 2e-2
+    nseg, seg_chunks, launches = hla.forward_plan(B, H, n, D, D, 128)
+    assert launches == 7 and nseg * seg_chunks * 128 >= n
+
+
+def test_forward_distinct_from_the_legacy_path():
+    x = inputs.make_custom(1, 2, 700, D, D, torch.bfloat16, seed=9, gamma=(0.98, 0.999))
+    q, k, v, g = x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["gamma"].cuda()
+    tc = hla.forward(q, k, v, gamma=g, chunk=128)
+    old = os.environ.get("HLA2_KERNEL")
+    os.environ["HLA2_KERNEL"] = "mma"
+    try:
+        legacy = hla.forward(q, k, v, gamma=g, chunk=128)
+    finally:
+        if old is None:
+            os.environ.pop("HLA2_KERNEL", None)
+        else:
+            os.environ["HLA2_KERNEL"] = old
+    ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), _gamma_np(x))
+    assert rel_err(np64(tc.cpu()), ref) <= 2e-2 and rel_err(np64(legacy.cpu()), ref) <= 2e-2
+    assert not torch.equal(tc, legacy)
