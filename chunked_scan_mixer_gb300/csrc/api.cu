@@ -314,7 +314,7 @@ int forward_saving_for_backward(const void* q, const void* k, const void* v, voi
 size_t fo_forward_ws(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize);
 int fo_forward_call(const void* q, const void* k, const void* v, void* out, int B, int H, int n, const float* gamma,
                     cudaStream_t st, const hla2_opts* opts);
-Plan fo_plan(int B, int H, int n, const DevInfo& di);
+Plan fo_plan(int B, int H, int n, int d, const DevInfo& di);
 }  // namespace
 
 extern "C" {
@@ -539,7 +539,7 @@ int hla2_debug_status(int clear) {
                                     dbg_read_fwd_mma_d32, dbg_read_fwd_mma_d64, dbg_read_fwd_mma_d128,
                                     dbg_read_bwd_mma_d16, dbg_read_bwd_mma_d32, dbg_read_bwd_mma_d64,
                                     dbg_read_bwd_mma_d128, dbg_read_bwd_simt,   dbg_read_scan,
-                                    dbg_read_fo_tc,       dbg_read_selftest};
+                                    dbg_read_fo_tc,       dbg_read_fo64_tc,     dbg_read_selftest};
     if (cudaDeviceSynchronize() != cudaSuccess) return cuda_fail("debug status");
     int site = 0;
     for (auto rd : readers) {
@@ -584,7 +584,7 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no forward kernel for d %d, dv %d at chunk <= %d", d, dv, chunk);
     if (!want_final_state && fo_forward_ws(B, H, n, d, dv, chunk, dtype, normalize)) {
         // first-order scans: S summaries, zero + scan, p pass, zero + scan, output pass
-        const Plan p = fo_plan(B, H, n, di);
+        const Plan p = fo_plan(B, H, n, d, di);
         if (nseg) *nseg = p.nseg;
         if (seg_chunks) *seg_chunks = p.seg_chunks;
         if (launches) *launches = p.nseg > 0 ? 7 : 0;
@@ -845,24 +845,36 @@ int backward_reverse_part_f32(const float* q, const float* k, const float* v, co
 // Passes: forward F1 (S summaries), F2 (p, stored, with Z summaries), F3 (o); reverse B1 (Zh
 // summaries), B2 (dp, stored, with Sh summaries), B3 (dv), B4 (dk), B5a (Z dO, stored), B5b (dq).
 
+// bf16, d == dv in {64, 128}, chunk >= 128, unnormalised, and the kernels fit this device.
 bool fo_path(int dtype, int d, int dv, int chunk, int normalize, const DevInfo& di) {
-    return dtype == HLA2_BF16 && d == 128 && dv == 128 && chunk >= 128 && !normalize && !tc_disabled() &&
-           fo_tc_available() && fo_tc_max_smem() <= (size_t)di.smem_optin;
+    if (dtype != HLA2_BF16 || d != dv || (d != 64 && d != 128) || chunk < 128 || normalize || tc_disabled() ||
+        !fo_tc_available())
+        return false;
+    return (d == 128 ? fo_tc_max_smem() : fo64_tc_max_smem()) <= (size_t)di.smem_optin;
 }
 
-Plan fo_plan(int B, int H, int n, const DevInfo& di) { return make_plan(B, H, n, 128, 128, 128, di.sms, 1); }
+Plan fo_plan(int B, int H, int n, int d, const DevInfo& di) { return make_plan(B, H, n, d, d, 128, di.sms, 1); }
+
+int fo_summary(const FoArgs& a, int d, const void* k, const void* v, bool reverse, cudaStream_t st) {
+    return d == 64 ? launch_fo64_tc_summary(a, k, v, reverse, st) : launch_fo_tc_summary(a, k, v, reverse, st);
+}
+int fo_out(const FoArgs& a, int d, const void* x, const void* k, const void* v, bool r2, int next_sum, const void* xv,
+           const void* add, void* out, bool reverse, cudaStream_t st) {
+    return d == 64 ? launch_fo64_tc_out(a, x, k, v, r2, next_sum, xv, add, out, reverse, st)
+                   : launch_fo_tc_out(a, x, k, v, r2, next_sum, xv, add, out, reverse, st);
+}
 
 struct FoLayout {
-    size_t SB, Sin, ZB, Zin, ZhB, Zhend, ShB, Shend;  // byte offsets, fp32 [BH][nseg][128][128]
-    size_t P, dP, dqa;                                // byte offsets, bf16 [BH][n][128]
+    size_t SB, Sin, ZB, Zin, ZhB, Zhend, ShB, Shend;  // byte offsets, fp32 [BH][nseg][d][d]
+    size_t P, dP, dqa;                                // byte offsets, bf16 [BH][n][d]
     size_t fwd_total, total;                          // bytes kept by the forward; by the backward
 };
 
 FoLayout fo_layout(const Plan& p) {
     FoLayout L;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-    const size_t sum = (size_t)p.BH * p.nseg * 128 * 128 * sizeof(float);
-    const size_t tok = (size_t)p.BH * p.n * 128 * sizeof(bf16);
+    const size_t sum = (size_t)p.BH * p.nseg * p.d * p.d * sizeof(float);
+    const size_t tok = (size_t)p.BH * p.n * p.d * sizeof(bf16);
     size_t o = 256;  // status word
     L.SB = o;    o = up(o + sum);
     L.Sin = o;   o = up(o + sum);
@@ -897,13 +909,13 @@ FoArgs fo_args(const Plan& p, const float* gamma, char* ws) {
 int fo_forward_part(const void* q, const void* k, const void* v, const Plan& p, const float* gamma, char* ws,
                     const FoLayout& L, cudaStream_t st) {
     auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
-    const size_t E = 128 * 128;
+    const size_t E = (size_t)p.d * p.d;
     const int seg_tokens = p.seg_chunks * p.W;
     FoArgs a = fo_args(p, gamma, ws);
     a.pow = 1;
     a.summary = f(L.SB);
-    if (launch_fo_tc_summary(a, k, nullptr, false, st)) return cuda_fail("key moment summaries");
-    if (launch_fo_zero_first(f(L.Sin), p.BH, p.nseg, a.status, st) ||
+    if (fo_summary(a, p.d, k, nullptr, false, st)) return cuda_fail("key moment summaries");
+    if (launch_fo_zero_first(f(L.Sin), p.BH, p.nseg, (int)E, a.status, st) ||
         (p.nseg > 1 && launch_linear_scan(f(L.SB), f(L.Sin), p.BH, p.H, p.nseg - 1, E, p.nseg * E, p.nseg * E, true,
                                           gamma, seg_tokens, 1, st)))
         return cuda_fail("key moment scan");
@@ -912,8 +924,8 @@ int fo_forward_part(const void* q, const void* k, const void* v, const Plan& p, 
     a.carry = f(L.Sin);
     a.carry_mode = 0;
     a.summary = f(L.ZB);
-    if (launch_fo_tc_out(a, q, k, nullptr, false, 2, v, nullptr, ws + L.P, false, st)) return cuda_fail("p pass");
-    if (launch_fo_zero_first(f(L.Zin), p.BH, p.nseg, nullptr, st) ||
+    if (fo_out(a, p.d, q, k, nullptr, false, 2, v, nullptr, ws + L.P, false, st)) return cuda_fail("p pass");
+    if (launch_fo_zero_first(f(L.Zin), p.BH, p.nseg, (int)E, nullptr, st) ||
         (p.nseg > 1 && launch_linear_scan(f(L.ZB), f(L.Zin), p.BH, p.H, p.nseg - 1, E, p.nseg * E, p.nseg * E, true,
                                           gamma, seg_tokens, 2, st)))
         return cuda_fail("Z scan");
@@ -927,7 +939,7 @@ int fo_output_pass(const void* q, const void* v, void* out, const Plan& p, const
     a.pow = 2;
     a.carry = reinterpret_cast<const float*>(ws + L.Zin);
     a.carry_mode = 0;
-    if (launch_fo_tc_out(a, q, ws + L.P, v, false, 0, nullptr, nullptr, out, false, st)) return cuda_fail("output pass");
+    if (fo_out(a, p.d, q, ws + L.P, v, false, 0, nullptr, nullptr, out, false, st)) return cuda_fail("output pass");
     return HLA2_OK;
 }
 
@@ -935,7 +947,7 @@ int fo_output_pass(const void* q, const void* v, void* out, const Plan& p, const
 int fo_reverse_part(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dvv,
                     const Plan& p, const float* gamma, char* ws, const FoLayout& L, cudaStream_t st) {
     auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
-    const size_t E = 128 * 128;
+    const size_t E = (size_t)p.d * p.d;
     void* P = ws + L.P;
     void* dP = ws + L.dP;
     void* dqa = ws + L.dqa;
@@ -943,7 +955,7 @@ int fo_reverse_part(const void* q, const void* k, const void* v, const void* dou
     // B1: Zh^T summaries (keys dO, values q), reverse, g^2; then the reverse scan
     a.pow = 2;
     a.summary = f(L.ZhB);
-    if (launch_fo_tc_summary(a, dout, q, true, st)) return cuda_fail("Zh summaries");
+    if (fo_summary(a, p.d, dout, q, true, st)) return cuda_fail("Zh summaries");
     if (launch_reverse_scan(f(L.ZhB), f(L.Zhend), p.BH, p.H, p.nseg, E, gamma, p.n, p.W, p.seg_chunks, 2, st))
         return cuda_fail("Zh scan");
     // B2: dp = RLA_{g^2}(v, dO, q), stored; Sh summaries over (dp, q) with g
@@ -952,7 +964,7 @@ int fo_reverse_part(const void* q, const void* k, const void* v, const void* dou
     a.carry = f(L.Zhend);
     a.carry_mode = 0;
     a.summary = f(L.ShB);
-    if (launch_fo_tc_out(a, v, dout, q, false, 1, nullptr, nullptr, dP, true, st)) return cuda_fail("dp pass");
+    if (fo_out(a, p.d, v, dout, q, false, 1, nullptr, nullptr, dP, true, st)) return cuda_fail("dp pass");
     if (launch_reverse_scan(f(L.ShB), f(L.Shend), p.BH, p.H, p.nseg, E, gamma, p.n, p.W, p.seg_chunks, 1, st))
         return cuda_fail("Sh scan");
     a.summary = nullptr;
@@ -960,35 +972,35 @@ int fo_reverse_part(const void* q, const void* k, const void* v, const void* dou
     a.pow = 2;
     a.carry = f(L.Zhend);
     a.carry_mode = 1;
-    if (launch_fo_tc_out(a, P, q, dout, false, 0, nullptr, nullptr, dvv, true, st)) return cuda_fail("dv pass");
+    if (fo_out(a, p.d, P, q, dout, false, 0, nullptr, nullptr, dvv, true, st)) return cuda_fail("dv pass");
     // B4: dk = RLA_g(k, dp, q) + RLA_g(k, q, dp), carry Sh + Sh^T
     a.pow = 1;
     a.carry = f(L.Shend);
     a.carry_mode = 2;
-    if (launch_fo_tc_out(a, k, dP, q, true, 0, nullptr, nullptr, dk, true, st)) return cuda_fail("dk pass");
+    if (fo_out(a, p.d, k, dP, q, true, 0, nullptr, nullptr, dk, true, st)) return cuda_fail("dk pass");
     // B5a: Z dO = LA_{g^2}(dO, v, p), carry Z^T;  B5b: dq = LA_g(dp, k, k) + that, carry S
     a.pow = 2;
     a.carry = f(L.Zin);
     a.carry_mode = 1;
-    if (launch_fo_tc_out(a, dout, v, P, false, 0, nullptr, nullptr, dqa, false, st)) return cuda_fail("dq pass (Z dO)");
+    if (fo_out(a, p.d, dout, v, P, false, 0, nullptr, nullptr, dqa, false, st)) return cuda_fail("dq pass (Z dO)");
     a.pow = 1;
     a.carry = f(L.Sin);
     a.carry_mode = 0;
-    if (launch_fo_tc_out(a, dP, k, nullptr, false, 0, nullptr, dqa, dq, false, st)) return cuda_fail("dq pass");
+    if (fo_out(a, p.d, dP, k, nullptr, false, 0, nullptr, dqa, dq, false, st)) return cuda_fail("dq pass");
     return HLA2_OK;
 }
 
 size_t fo_forward_ws(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
     const DevInfo di = dev_info();
-    if (!fo_path(dtype, d, dv, chunk, normalize, di)) return 0;
-    const Plan p = fo_plan(B, H, n, di);
+    if (d != 128 || !fo_path(dtype, d, dv, chunk, normalize, di)) return 0;  // d = 64: the stored-p kernels
+    const Plan p = fo_plan(B, H, n, d, di);
     return p.nseg > 0 ? fo_layout(p).fwd_total : 0;
 }
 
 int fo_forward_call(const void* q, const void* k, const void* v, void* out, int B, int H, int n, const float* gamma,
                     cudaStream_t st, const hla2_opts* opts) {
     const DevInfo di = dev_info();
-    const Plan p = fo_plan(B, H, n, di);
+    const Plan p = fo_plan(B, H, n, 128, di);
     const FoLayout L = fo_layout(p);
     if (!opts->workspace || opts->workspace_bytes < L.fwd_total)
         return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.fwd_total,
@@ -1046,7 +1058,7 @@ int normalised_f32_chunk(int d, int dv, int chunk, const DevInfo& di) {
 
 size_t unnormalised_backward_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype, const DevInfo& di) {
     if (fo_path(dtype, d, dv, chunk, 0, di)) {
-        const Plan p = fo_plan(B, H, n, di);
+        const Plan p = fo_plan(B, H, n, d, di);
         return p.nseg > 0 ? fo_layout(p).total : 0;
     }
     const BwdPlan bp = backward_plan(B, H, n, d, dv, chunk, dtype, di);
@@ -1096,7 +1108,7 @@ int forward_saving_for_backward(const void* q, const void* k, const void* v, voi
                     "saving for the backward needs bf16, d == dv, normalize == 0 and no init_state / final_state");
     const DevInfo di = dev_info();
     if (fo_path(opts->dtype, d, dv, chunk, normalize, di)) {
-        const Plan p = fo_plan(B, H, n, di);
+        const Plan p = fo_plan(B, H, n, d, di);
         const FoLayout L = fo_layout(p);
         if (!opts->workspace || opts->workspace_bytes < L.total)
             return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required to save for the backward (got %zu)",
@@ -1218,7 +1230,7 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
         return succeed();
     }
     if (fo_path(opts->dtype, d, dv, chunk, 0, di)) {
-        const Plan p = fo_plan(B, H, n, di);
+        const Plan p = fo_plan(B, H, n, d, di);
         const FoLayout L = fo_layout(p);
         if (!opts->workspace || opts->workspace_bytes < L.total)
             return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.total,

@@ -39,11 +39,7 @@
 // One CTA per SM (up to 192 KB of shared memory, all 512 tensor-memory columns).  Every
 // wait is bounded; on a timeout the kernel records the site in the status word, drains and
 // exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "kernels.h"
-#include "tc_common.cuh"
+#include "fo_common.cuh"
 
 namespace hla2 {
 
@@ -102,81 +98,6 @@ struct Maps {
 };
 
 }  // namespace la
-
-__device__ __forceinline__ float la_bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float la_bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
-
-__device__ __forceinline__ uint4 la_scale_chunk(uint4 c, float s) {
-    uint4 o;
-    o.x = pack_bf16x2(s * la_bf_lo(c.x), s * la_bf_hi(c.x));
-    o.y = pack_bf16x2(s * la_bf_lo(c.y), s * la_bf_hi(c.y));
-    o.z = pack_bf16x2(s * la_bf_lo(c.z), s * la_bf_hi(c.z));
-    o.w = pack_bf16x2(s * la_bf_lo(c.w), s * la_bf_hi(c.w));
-    return o;
-}
-
-__device__ __forceinline__ uint4 la_pack8(const float* f) {
-    uint4 o;
-    o.x = pack_bf16x2(f[0], f[1]);
-    o.y = pack_bf16x2(f[2], f[3]);
-    o.z = pack_bf16x2(f[4], f[5]);
-    o.w = pack_bf16x2(f[6], f[7]);
-    return o;
-}
-
-// Byte offset of 16-byte chunk j (0..7) of row r in column block b of a [128][128] tile.
-__device__ __forceinline__ uint32_t la_off(int b, int r, int j) { return (uint32_t)b * la::kBlk + tc::sw128_chunk(r, j); }
-
-// Masked, decayed 32-column block [cb, cb + 32) of Gram row r (fp32 at src in tensor memory),
-// packed to 16 bf16 pairs.  Forward keeps i <= r with g^(r - i); reverse keeps i >= r with
-// g^(i - r).  cb and the warp's first row row0 are multiples of 32, so a block is entirely
-// kept, entirely dropped (written as zeros without reading) or the diagonal block.
-template <bool REV>
-__device__ __forceinline__ void la_masked_pack(uint32_t src, int r, int cb, int row0, float log2g, float g,
-                                               float ginv, uint32_t (&pk)[16]) {
-    const bool dropped = REV ? cb < row0 : cb > row0;
-    if (dropped) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) pk[j] = 0u;
-        return;
-    }
-    const bool diag = cb == row0;
-    float f = pow_decay(log2g, (float)(REV ? cb - r : r - cb));  // factor at column cb
-    const float step = REV ? g : ginv;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {  // 16 columns at a time (register pressure)
-        uint32_t v[16];
-        tc::tmem_ld16(src + 16 * half, v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-            float a0 = f * __uint_as_float(v[j]);
-            f *= step;
-            float a1 = f * __uint_as_float(v[j + 1]);
-            f *= step;
-            if (diag) {
-                const int i0 = cb + 16 * half + j, i1 = i0 + 1;
-                a0 = (REV ? i0 >= r : i0 <= r) ? a0 : 0.f;
-                a1 = (REV ? i1 >= r : i1 <= r) ? a1 : 0.f;
-            }
-            pk[8 * half + j / 2] = pack_bf16x2(a0, a1);
-        }
-    }
-}
-
-// Segment geometry of a CTA.
-struct FoSeg {
-    int c_begin, c_end, nit, t0, L;
-};
-__device__ __forceinline__ FoSeg la_seg(const FoArgs& a, int seg) {
-    FoSeg s;
-    s.c_begin = seg * a.seg_chunks;
-    s.c_end = min(s.c_begin + a.seg_chunks, a.nchunks);
-    s.nit = s.c_end - s.c_begin;
-    s.t0 = s.c_begin * la::kW;
-    s.L = min(s.c_end * la::kW, a.n) - s.t0;
-    return s;
-}
 
 // ----------------------------------------------------------------------------------------
 // Output kernel.  REV: reverse direction.  NSUM: next summary of the output.  R2: the swapped
@@ -724,44 +645,16 @@ __global__ void __launch_bounds__(la::kThreads, 1)
     if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
-// Zeroes the carry into segment 0 of every head ([BH][nseg][d*d], segment 0) and clears the
-// status word, before a forward linear scan fills the other segments.
-__global__ void fo_zero_first_kernel(float* carry, int nseg, int* status) {
+// Zeroes the carry into segment 0 of every head ([BH][nseg][E], segment 0; E = d * d) and
+// clears the status word, before a forward linear scan fills the other segments.
+__global__ void fo_zero_first_kernel(float* carry, int nseg, int E, int BH, int* status) {
     pdl_trigger();
     pdl_wait();
     const int bh = blockIdx.x;
-    float4* dst = reinterpret_cast<float4*>(carry + (size_t)bh * nseg * la::kD * la::kD);
-    for (int i = threadIdx.x; i < la::kD * la::kD / 4; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!HLA2_IN(bh < BH && E % 4 == 0, 804)) return;
+    float4* dst = reinterpret_cast<float4*>(carry + (size_t)bh * nseg * E);
+    for (int i = threadIdx.x; i < E / 4; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (bh == 0 && threadIdx.x == 0 && status) *status = 0;
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 la_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        else
-            cudaGetLastError();
-    }
-    return fn;
-}
-
-// [BH][n][128] bf16, box [1][128][64] (128-byte rows), 128-byte swizzle; rows past n read as
-// zero and are not written by stores.
-bool la_map(CUtensorMap* m, const void* ptr, int BH, int n) {
-    auto fn = la_encode_fn();
-    if (!fn || !ptr) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)la::kD, (cuuint64_t)n, (cuuint64_t)BH};
-    cuuint64_t strides[2] = {(cuuint64_t)la::kD * 2, (cuuint64_t)n * la::kD * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)la::kW, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename K>
@@ -787,9 +680,10 @@ size_t fo_tc_max_smem() {
     return m;
 }
 
-int launch_fo_zero_first(float* carry, int BH, int nseg, int* status, cudaStream_t st) {
+int launch_fo_zero_first(float* carry, int BH, int nseg, int E, int* status, cudaStream_t st) {
     if (BH <= 0) return 0;
-    if (launch_pdl(fo_zero_first_kernel, dim3(BH), dim3(256), 0, st, carry, nseg, status) != cudaSuccess) return -1;
+    if (launch_pdl(fo_zero_first_kernel, dim3(BH), dim3(256), 0, st, carry, nseg, E, BH, status) != cudaSuccess)
+        return -1;
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -269,8 +269,8 @@ struct FoArgs {
 };
 bool fo_tc_available();
 size_t fo_tc_max_smem();
-// carry[bh][0] = 0 for every head (and *status = 0)
-int launch_fo_zero_first(float* carry, int BH, int nseg, int* status, cudaStream_t st);
+// carry[bh][0][0 .. E) = 0 for every head of a [BH][nseg][E] array (and *status = 0)
+int launch_fo_zero_first(float* carry, int BH, int nseg, int E, int* status, cudaStream_t st);
 // summary[s] = sum_{i in s} g^(distance to the segment's end (forward) / start (reverse)) k_i v_i^T
 int launch_fo_tc_summary(const FoArgs& a, const void* k, const void* v, bool reverse, cudaStream_t st);
 // out = (R)LA(x, k, v) with the carry (v == NULL: the values are the keys); r2 adds the swapped
@@ -278,6 +278,11 @@ int launch_fo_tc_summary(const FoArgs& a, const void* k, const void* v, bool rev
 // add != NULL adds that partial.
 int launch_fo_tc_out(const FoArgs& a, const void* x, const void* k, const void* v, bool r2, int next_sum,
                      const void* xv, const void* add, void* out, bool reverse, cudaStream_t st);
+// The same two launches for d = dv = 64 (fo64_tc.cu; [BH][nseg][64*64] summaries and carries).
+size_t fo64_tc_max_smem();
+int launch_fo64_tc_summary(const FoArgs& a, const void* k, const void* v, bool reverse, cudaStream_t st);
+int launch_fo64_tc_out(const FoArgs& a, const void* x, const void* k, const void* v, bool r2, int next_sum,
+                       const void* xv, const void* add, void* out, bool reverse, cudaStream_t st);
 
 // Bounded-wait self-test: waits on an mbarrier nobody arrives at; records site 90 in *status.
 int launch_wait_timeout_selftest(int* status, cudaStream_t st);
@@ -299,6 +304,7 @@ int dbg_read_bwd_mma_d128(bool clear);
 int dbg_read_bwd_simt(bool clear);
 int dbg_read_scan(bool clear);
 int dbg_read_fo_tc(bool clear);
+int dbg_read_fo64_tc(bool clear);
 int dbg_read_selftest(bool clear);
 #endif
 int launch_state_compact(const float* src, float* dst, long heads, int d, int dv, bool to_compact, cudaStream_t st);

@@ -1,5 +1,6 @@
-"""The d = dv = 128 bf16 training path on the tcgen05 first-order scan kernel (chunk 128),
-and the plain forward on the same passes, through the C ABI, against the float64 oracle.
+"""The bf16 training path (d = dv = 128 and 64) on the tcgen05 first-order scan kernels (chunk
+128), and the plain d = 128 forward on the same passes, through the C ABI, against the float64
+oracle.
 
 The masked output is two chained first-order scans (p = S q, then o = q^T Z) and its reverse
 mode six more; every pass runs segment-parallel on the same kernel.  Bar: max|gpu - oracle| /
@@ -41,21 +42,23 @@ def _check_grads(got, x, what=""):
         assert err <= 2e-2, (name, what, err)
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("B, H, n", [(1, 2, 1000), (2, 8, 4000), (1, 3, 128), (1, 2, 127), (1, 2, 129),
                                      (1, 1, 1), (3, 1, 2500)])
 @pytest.mark.parametrize("gamma", [None, (0.9, 0.999)])
-def test_backward_matches_oracle(B, H, n, gamma):
-    x = inputs.make_custom(B, H, n, D, D, torch.bfloat16, seed=B * 1000 + H * 100 + n % 97, gamma=gamma,
+def test_backward_matches_oracle(d, B, H, n, gamma):
+    x = inputs.make_custom(B, H, n, d, d, torch.bfloat16, seed=B * 1000 + H * 100 + n % 97 + d, gamma=gamma,
                            with_dout=True)
     q, k, v, do, g = _dev(x)
     _check_grads(hla.backward(q, k, v, do, gamma=g, chunk=128), x, (B, H, n, gamma))
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("n", [300, 3000])
-def test_forward_saved_then_backward(n):
+def test_forward_saved_then_backward(d, n):
     """The forward that keeps p for the backward gives the oracle's output; the backward from
     the saved p and carries equals, bit for bit, the one that recomputes them, and the oracle."""
-    x = inputs.make_custom(2, 3, n, D, D, torch.bfloat16, seed=n, gamma=(0.97, 0.999), with_dout=True)
+    x = inputs.make_custom(2, 3, n, d, d, torch.bfloat16, seed=n + d, gamma=(0.97, 0.999), with_dout=True)
     q, k, v, do, g = _dev(x)
     o, saved = hla.forward(q, k, v, gamma=g, chunk=128, save_for_backward=True)
     ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), _gamma_np(x))
@@ -69,9 +72,10 @@ def test_forward_saved_then_backward(n):
     _check_grads(a, x, "saved")
 
 
-def test_steep_and_flat_decay_per_head():
+@pytest.mark.parametrize("d", [128, 64])
+def test_steep_and_flat_decay_per_head(d):
     """Decays from 0.5 (a pair weight that underflows within a chunk) to 1 across heads."""
-    x = inputs.make_custom(1, 4, 700, D, D, torch.bfloat16, seed=77, gamma=None, with_dout=True)
+    x = inputs.make_custom(1, 4, 700, d, d, torch.bfloat16, seed=77, gamma=None, with_dout=True)
     x["gamma"] = torch.tensor([0.5, 0.9, 0.999, 1.0], dtype=torch.float32)
     q, k, v, do, g = _dev(x)
     _check_grads(hla.backward(q, k, v, do, gamma=g, chunk=128), x)
@@ -98,11 +102,12 @@ def test_training_workload_all_heads():
         assert max(per_head) <= 2e-2, (name, int(np.argmax(per_head)))
 
 
-def test_distinct_from_the_legacy_path():
+@pytest.mark.parametrize("d", [128, 64])
+def test_distinct_from_the_legacy_path(d):
     """HLA2_KERNEL=mma selects the mma.sync kernels: both paths match the oracle, and their
     gradients are not bit for bit equal (different kernels, different rounding order), so the
     default call does run the first-order scan kernels."""
-    x = inputs.make_custom(1, 2, 600, D, D, torch.bfloat16, seed=5, gamma=(0.98, 0.999), with_dout=True)
+    x = inputs.make_custom(1, 2, 600, d, d, torch.bfloat16, seed=5 + d, gamma=(0.98, 0.999), with_dout=True)
     q, k, v, do, g = _dev(x)
     tc = hla.backward(q, k, v, do, gamma=g, chunk=128)
     old = os.environ.get("HLA2_KERNEL")
@@ -148,3 +153,20 @@ def test_forward_distinct_from_the_legacy_path():
     ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), _gamma_np(x))
     assert rel_err(np64(tc.cpu()), ref) <= 2e-2 and rel_err(np64(legacy.cpu()), ref) <= 2e-2
     assert not torch.equal(tc, legacy)
+
+
+def test_d64_training_shapes_all_heads():
+    """The training workload's batch and length at d = dv = 64 (B=4, H=16, n=8192): forward
+    keeping p, backward from it; output and all 64 heads' gradients against the oracle."""
+    w = inputs.WORKLOADS["train"]
+    x = inputs.make_custom(w.B, w.H, w.n, 64, 64, torch.bfloat16, seed=55, gamma=0.995, with_dout=True)
+    q, k, v, do, g = _dev(x)
+    o, saved = hla.forward(q, k, v, gamma=g, chunk=128, save_for_backward=True)
+    grads = hla.backward(q, k, v, do, gamma=g, chunk=128, saved=saved)
+    torch.cuda.synchronize()
+    assert rel_err(np64(o.cpu()), cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), _gamma_np(x))) <= 2e-2
+    ref = cref.backward(np32(x["q"]), np32(x["k"]), np32(x["v"]), np32(x["dout"]), _gamma_np(x))
+    for name, gg, rr in zip(("dq", "dk", "dv"), grads, ref):
+        got = np64(gg.cpu())
+        per_head = [rel_err(got[b, h], rr[b, h]) for b in range(w.B) for h in range(w.H)]
+        assert max(per_head) <= 2e-2, (name, int(np.argmax(per_head)))
