@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode and training rows measured after the headline")
     ap.add_argument("--only", choices=("decode", "decode_compact", "decode_unmasked", "decode_mq", "train", "ahla",
-                                       "unmasked", "hla3", "prefill"),
+                                       "unmasked", "hla3", "prefill", "train_d64", "ahla_backward"),
                     default=None,
                     help="measure only this row (for profiler captures; --steps/--warmup apply)")
     ap.add_argument("--decode-seqs", type=int, default=256,
@@ -371,16 +371,22 @@ def measure_decode_mq(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: 
                          "frac": achieved / hbm_gbs, "algorithmic_bytes_per_launch": nbytes}}
 
 
-def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: int = 10, warmup: int = 3):
+def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: int = 10, warmup: int = 3,
+                  d: int | None = None):
     """Training row: B=4 H=16 n=8192 d=dv=128 bf16, decay 0.995, unnormalised, chunk 128 (the
     tcgen05 first-order scan passes); one step = forward (keeping p and the carries for the
-    backward) + backward (dq, dk, dv) through the public calls, inputs resident."""
+    backward) + backward (dq, dk, dv) through the public calls, inputs resident.  d overrides
+    the head width (the train_d64 row: d = dv = 64, same batch and length)."""
+    import dataclasses
+
     import torch
 
     import chunked_scan_mixer_gb300 as hla
     from chunked_scan_mixer_gb300 import inputs
 
     w = inputs.WORKLOADS["train"]
+    if d is not None:
+        w = dataclasses.replace(w, d=d, dv=d)
     x = inputs.make(w, device=dev, seed=replica_seed(w.seed, dist.rank))
     q, k, v, do = x["q"], x["k"], x["v"], x["dout"]
     gamma = x["gamma"].to(dev)
@@ -393,7 +399,7 @@ def measure_train(dev, dist: Dist, bf16_tflops: float, hbm_gbs: float, steps: in
 
     ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
     tokens = w.B * w.H * w.n
-    flops = 3 * tokens * 368640  # forward F(64) + backward 2 F(64) at d = dv = 128
+    flops = 3 * tokens * (368640 if w.d == 128 else 98304)  # forward F(64) + backward 2 F(64)
     nbytes = tokens * ((2 * w.d + w.dv) * 2 + w.dv * 2)  # forward
     nbytes += tokens * ((2 * w.d + 2 * w.dv) * 2 + (2 * w.d + w.dv) * 2)  # backward reads, writes
     achieved = flops / (ms * 1e-3) / 1e12
@@ -447,6 +453,40 @@ def measure_ahla(dev, dist: Dist, hbm_gbs: float, bf16_tflops: float, steps: int
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
                          "frac": achieved / hbm_gbs, "kernel": "output_pass", "algorithmic_bytes_per_launch": nbytes,
                          "step_tensor_frac": flops / (ms * 1e-3) / 1e12 / bf16_tflops}}
+
+
+def measure_ahla_backward(dev, dist: Dist, hbm_gbs: float, steps: int = 20, warmup: int = 3, n: int | None = None):
+    """AHLA reverse-mode row: dq, dk, dv of the unnormalised AHLA output on the long-context
+    shapes (B=1 H=16 n=65536 d=dv=64 bf16, decay linspace(0.99, 0.9999), chunk 128: the tcgen05
+    first-order scans), upstream dO ~ N(0, 1); HBM roofline of the whole call over its
+    algorithmic bytes (q, k, v, dO read, dq, dk, dv written)."""
+    import dataclasses
+
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = dataclasses.replace(inputs.WORKLOADS["long"], with_dout=True)
+    if n is not None:
+        w = dataclasses.replace(w, n=n)
+    x = inputs.make(w, device=dev, seed=replica_seed(w.seed, dist.rank))
+    q, k, v, do = x["q"], x["k"], x["v"], x["dout"]
+    gamma = x["gamma"].to(dev)
+
+    def one():
+        hla.ahla_backward(q, k, v, do, gamma=gamma, chunk=w.chunk)
+
+    ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
+    tokens = w.B * w.H * w.n
+    nbytes = tokens * (4 * w.d + 3 * w.dv) * 2
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"AHLA backward: B={w.B} H={w.H} n={w.n} d=dv={w.d} bf16, decay linspace(0.99,0.9999), "
+                        f"unnormalised, chunk {w.chunk}",
+            "metric": "AHLA bwd tokens/s", "unit": "tokens/s", "value": dist.world * tokens / (ms * 1e-3),
+            "ms_per_step": ms, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "kernel": "whole call", "algorithmic_bytes_per_step": nbytes}}
 
 
 def measure_unmasked(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5, n: int | None = None,
@@ -581,6 +621,10 @@ def run_only(args, dist: Dist, dev):
                                chunk=args.chunk or 128)
     elif args.only == "ahla":
         row = measure_ahla(dev, dist, hbm_gbs, bf16_tflops, steps=args.steps, warmup=args.warmup, n=args.n)
+    elif args.only == "ahla_backward":
+        row = measure_ahla_backward(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
+    elif args.only == "train_d64":
+        row = measure_train(dev, dist, bf16_tflops, hbm_gbs, steps=args.steps, warmup=args.warmup, d=64)
     else:
         row = measure_train(dev, dist, bf16_tflops, hbm_gbs, steps=args.steps, warmup=args.warmup)
     if dist.rank == 0:
@@ -711,7 +755,9 @@ def run_ours(args, dist: Dist):
                      "decode_unmasked": measure_decode(dev, dist, hbm_gbs, masked=False),
                      "decode_mq": measure_decode_mq(dev, dist, hbm_gbs),
                      "train": measure_train(dev, dist, bf16_tflops, hbm_gbs),
+                     "train_d64": measure_train(dev, dist, bf16_tflops, hbm_gbs, d=64),
                      "ahla": measure_ahla(dev, dist, hbm_gbs, bf16_tflops),
+                     "ahla_backward": measure_ahla_backward(dev, dist, hbm_gbs),
                      "unmasked": measure_unmasked(dev, dist, hbm_gbs),
                      "hla3": measure_hla3(dev, dist, hbm_gbs),
                      "prefill": measure_prefill(dev, dist, hbm_gbs)}

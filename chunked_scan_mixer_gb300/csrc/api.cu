@@ -1680,10 +1680,113 @@ static AhlaBwdPlan ahla_bwd_plan(int B, int H, int n, int d, int chunk, const De
     return bp;
 }
 
+// ---- AHLA reverse mode on the tcgen05 first-order scans (bf16, d = dv = 64, chunk >= 128) ------
+// AHLA is two chained first-order scans with the same queries and keys, u = LA_g(q, k, v) and
+// o = LA_g(q, k, u).  Its reverse mode:
+//   du = RLA_g(k, q, dO),  dv = RLA_g(k, q, du),
+//   dk = RLA_g(u, dO, q) + RLA_g(v, du, q),  dq = LA_g(dO, u, k) + LA_g(du, v, k),
+// whose carries are four summaries (some read transposed): KV = sum k v^T (F1, forward),
+// UK = sum u k^T (over the u pass's own output), QD = sum q dO^T (B1, reverse) and DQ =
+// sum du q^T (over the du pass's own output).
+struct AhlaFoLayout {
+    size_t KVB, KVin, UKB, UKin, QDB, QDend, DQB, DQend;  // byte offsets, fp32 [BH][nseg][d][d]
+    size_t U, DU, DKA, DQA;                               // byte offsets, bf16 [BH][n][d]
+    size_t total;
+};
+
+AhlaFoLayout ahla_fo_layout(const Plan& p) {
+    AhlaFoLayout L;
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t sum = (size_t)p.BH * p.nseg * p.d * p.d * sizeof(float);
+    const size_t tok = (size_t)p.BH * p.n * p.d * sizeof(bf16);
+    size_t o = 256;  // status word
+    size_t* sums[] = {&L.KVB, &L.KVin, &L.UKB, &L.UKin, &L.QDB, &L.QDend, &L.DQB, &L.DQend};
+    for (size_t* x : sums) {
+        *x = o;
+        o = up(o + sum);
+    }
+    size_t* toks[] = {&L.U, &L.DU, &L.DKA, &L.DQA};
+    for (size_t* x : toks) {
+        *x = o;
+        o = up(o + tok);
+    }
+    L.total = o;
+    return L;
+}
+
+bool ahla_fo_path(int dtype, int d, int dv, int chunk, const DevInfo& di) {
+    return d == 64 && fo_path(dtype, d, dv, chunk, 0, di);
+}
+
+int ahla_fo_backward(const void* q, const void* k, const void* v, const void* dout, void* dq, void* dk, void* dvv,
+                     const Plan& p, const float* gamma, char* ws, const AhlaFoLayout& L, cudaStream_t st) {
+    auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+    const size_t E = (size_t)p.d * p.d;
+    const int seg_tokens = p.seg_chunks * p.W;
+    void* U = ws + L.U;
+    void* DU = ws + L.DU;
+    FoArgs a = fo_args(p, gamma, ws);
+    a.pow = 1;
+    a.pow_next = 1;
+    // F1: KV summaries and the forward scan
+    a.summary = f(L.KVB);
+    if (fo_summary(a, p.d, k, v, false, st)) return cuda_fail("AHLA key-value summaries");
+    if (launch_fo_zero_first(f(L.KVin), p.BH, p.nseg, (int)E, a.status, st) ||
+        (p.nseg > 1 && launch_linear_scan(f(L.KVB), f(L.KVin), p.BH, p.H, p.nseg - 1, E, p.nseg * E, p.nseg * E, true,
+                                          gamma, seg_tokens, 1, st)))
+        return cuda_fail("AHLA key-value scan");
+    // F2: u = LA(q, k, v), UK summaries over (u, k)
+    a.carry = f(L.KVin);
+    a.carry_mode = 0;
+    a.summary = f(L.UKB);
+    if (fo_out(a, p.d, q, k, v, false, 2, k, nullptr, U, false, st)) return cuda_fail("AHLA u pass");
+    if (launch_fo_zero_first(f(L.UKin), p.BH, p.nseg, (int)E, nullptr, st) ||
+        (p.nseg > 1 && launch_linear_scan(f(L.UKB), f(L.UKin), p.BH, p.H, p.nseg - 1, E, p.nseg * E, p.nseg * E, true,
+                                          gamma, seg_tokens, 1, st)))
+        return cuda_fail("AHLA u-key scan");
+    // B1: QD summaries (reverse) and the reverse scan
+    a.carry = nullptr;
+    a.summary = f(L.QDB);
+    if (fo_summary(a, p.d, q, dout, true, st)) return cuda_fail("AHLA query-gradient summaries");
+    if (launch_reverse_scan(f(L.QDB), f(L.QDend), p.BH, p.H, p.nseg, E, gamma, p.n, p.W, p.seg_chunks, 1, st))
+        return cuda_fail("AHLA query-gradient scan");
+    // B2: du = RLA(k, q, dO), DQ summaries over (du, q)
+    a.carry = f(L.QDend);
+    a.carry_mode = 0;
+    a.summary = f(L.DQB);
+    if (fo_out(a, p.d, k, q, dout, false, 2, q, nullptr, DU, true, st)) return cuda_fail("AHLA du pass");
+    if (launch_reverse_scan(f(L.DQB), f(L.DQend), p.BH, p.H, p.nseg, E, gamma, p.n, p.W, p.seg_chunks, 1, st))
+        return cuda_fail("AHLA du-query scan");
+    a.summary = nullptr;
+    // B3: dv = RLA(k, q, du), carry sum q du^T
+    a.carry = f(L.DQend);
+    a.carry_mode = 1;
+    if (fo_out(a, p.d, k, q, DU, false, 0, nullptr, nullptr, dvv, true, st)) return cuda_fail("AHLA dv pass");
+    // B4: dk = RLA(u, dO, q) [carry sum dO q^T] + RLA(v, du, q) [carry sum du q^T]
+    a.carry = f(L.QDend);
+    a.carry_mode = 1;
+    if (fo_out(a, p.d, U, dout, q, false, 0, nullptr, nullptr, ws + L.DKA, true, st)) return cuda_fail("AHLA dk pass");
+    a.carry = f(L.DQend);
+    a.carry_mode = 0;
+    if (fo_out(a, p.d, v, DU, q, false, 0, nullptr, ws + L.DKA, dk, true, st)) return cuda_fail("AHLA dk pass");
+    // B5: dq = LA(dO, u, k) [carry sum u k^T] + LA(du, v, k) [carry sum v k^T]
+    a.carry = f(L.UKin);
+    a.carry_mode = 0;
+    if (fo_out(a, p.d, dout, U, k, false, 0, nullptr, nullptr, ws + L.DQA, false, st)) return cuda_fail("AHLA dq pass");
+    a.carry = f(L.KVin);
+    a.carry_mode = 1;
+    if (fo_out(a, p.d, DU, v, k, false, 0, nullptr, ws + L.DQA, dq, false, st)) return cuda_fail("AHLA dq pass");
+    return HLA2_OK;
+}
+
 extern "C" size_t hla2_ahla_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
                                                      int normalize) {
     if (check_common(B, H, n, d, dv, dtype, normalize) != HLA2_OK || !dim_ok(chunk) || d != dv || normalize)
         return (size_t)-1;
+    if (ahla_fo_path(dtype, d, dv, chunk, dev_info())) {
+        const Plan p = fo_plan(B, H, n, d, dev_info());
+        return p.nseg > 0 ? ahla_fo_layout(p).total : 0;
+    }
     const AhlaBwdPlan bp = ahla_bwd_plan(B, H, n, d, chunk, dev_info());
     if (!bp.W) return (size_t)-1;
     return bp.p.nseg > 0 ? bp.L.total * sizeof(float) : 0;
@@ -1706,6 +1809,21 @@ extern "C" int hla2_ahla_backward(const void* q, const void* k, const void* v, c
     if (!q || !k || !v || !dout || !dq || !dk || !dv_out)
         return fail(HLA2_ERR_INVALID_ARG, "q, k, v, dout, dq, dk, dv must not be NULL");
     const DevInfo di = dev_info();
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv_out))
+        return fail(HLA2_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    if (ahla_fo_path(opts->dtype, d, dv, chunk, di)) {
+        const Plan p = fo_plan(B, H, n, d, di);
+        const AhlaFoLayout L = ahla_fo_layout(p);
+        if (!opts->workspace || opts->workspace_bytes < L.total)
+            return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.total,
+                        opts->workspace ? opts->workspace_bytes : (size_t)0);
+        if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+        cudaGetLastError();
+        rc = ahla_fo_backward(q, k, v, dout, dq, dk, dv_out, p, gamma, static_cast<char*>(opts->workspace), L,
+                              reinterpret_cast<cudaStream_t>(stream));
+        return rc == HLA2_OK ? succeed() : rc;
+    }
     const AhlaBwdPlan bp = ahla_bwd_plan(B, H, n, d, chunk, di);
     if (!bp.W) return fail(HLA2_ERR_UNSUPPORTED, "no AHLA backward kernel for d %d", d);
     const size_t need = bp.L.total * sizeof(float);

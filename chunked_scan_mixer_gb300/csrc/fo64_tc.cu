@@ -584,6 +584,7 @@ size_t fo64_tc_max_smem() {
                               f64::OutLayout<true, false, false, false>::kSmemBytes,
                               f64::OutLayout<false, true, false, true>::kSmemBytes,
                               f64::OutLayout<false, false, false, true>::kSmemBytes,
+                              f64::OutLayout<false, false, true, false>::kSmemBytes,
                               f64s::Layout<false>::kSmemBytes, f64s::Layout<true>::kSmemBytes};
     uint32_t m = 0;
     for (uint32_t x : sizes) m = x > m ? x : m;
@@ -624,6 +625,11 @@ int launch_fo64_tc_out(const FoArgs& a, const void* x, const void* k, const void
     HLA2_F64(true, false, false, false, false, false)  // dv = RLA(p, q, dO)
     HLA2_F64(true, false, true, false, false, false)   // dk = RLA(k, dp, q) + RLA(k, q, dp)
     HLA2_F64(false, false, false, true, false, true)   // dq = LA(dp, k, k) + Z dO
+    // the AHLA reverse mode (u = LA(q, k, v), o = LA(q, k, u))
+    HLA2_F64(false, true, false, false, true, false)   // u = LA(q, k, v), next summary over (u, k)
+    HLA2_F64(true, true, false, false, true, false)    // du = RLA(k, q, dO), next summary over (du, q)
+    HLA2_F64(true, false, false, false, false, true)   // dk = RLA(v, du, q) + RLA(u, dO, q)
+    HLA2_F64(false, false, false, false, false, true)  // dq = LA(du, v, k) + LA(dO, u, k)
 #undef HLA2_F64
     return -3;
 }

@@ -241,12 +241,15 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
 /*
  * AHLA reverse mode (section summary §4.2's reverse-mode scan applied to the AHLA
  * recurrence): given dout = dL/dout of the unnormalised hla2_ahla_forward output, writes dq,
- * dk, dv.  float32 or bf16 tensors [B, H, n, d], d == dv; float32 arithmetic on SIMT kernels
- * at a chunk width <= min(chunk, 32).  The passes recompute the forward (segment summaries
- * P_B, E_B, R_B, the forward scan, the state at every chunk start) and then run the reverse
- * summaries, the reverse scan (cross term rho R_B^T Eh_end) and the gradient pass.  normalize
- * must be 0; no flags, init_state or final_state.  Workspace:
- * hla2_ahla_backward_workspace_bytes.
+ * dk, dv.  float32 or bf16 tensors [B, H, n, d], d == dv.  bf16 with d = dv = 64 and
+ * chunk >= 128: tcgen05 first-order chunked scans at width 128 (the output is two chained
+ * first-order scans with the same queries and keys, u = LA(q, k, v) and o = LA(q, k, u), and
+ * its gradients six more, fp32 state, bf16 u and du between the passes).  Otherwise float32
+ * arithmetic on SIMT kernels at a chunk width <= min(chunk, 32): the passes recompute the
+ * forward (segment summaries P_B, E_B, R_B, the forward scan, the state at every chunk start)
+ * and then run the reverse summaries, the reverse scan (cross term rho R_B^T Eh_end) and the
+ * gradient pass.  normalize must be 0; no flags, init_state or final_state.  Tensor pointers
+ * must be 16-byte aligned.  Workspace: hla2_ahla_backward_workspace_bytes.
  */
 size_t hla2_ahla_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype,
                                           int normalize);

@@ -16,6 +16,7 @@ import torch
 
 import chunked_scan_mixer_gb300 as hla
 from chunked_scan_mixer_gb300 import inputs
+from oracle import ahla_oracle as A
 from oracle import cref
 
 from .helpers import np32, np64, rel_err
@@ -170,3 +171,42 @@ def test_d64_training_shapes_all_heads():
         got = np64(gg.cpu())
         per_head = [rel_err(got[b, h], rr[b, h]) for b in range(w.B) for h in range(w.H)]
         assert max(per_head) <= 2e-2, (name, int(np.argmax(per_head)))
+
+
+# ---- AHLA reverse mode (d = dv = 64, chunk 128) on the same kernel -----------------------------
+
+def _ahla_grads(x, chunk=128):
+    g = None if x["gamma"] is None else x["gamma"].cuda()
+    return hla.ahla_backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), gamma=g, chunk=chunk)
+
+
+@pytest.mark.parametrize("B, H, n", [(1, 2, 1000), (2, 3, 129), (1, 1, 1), (1, 2, 127), (2, 8, 3000)])
+@pytest.mark.parametrize("gamma", [None, (0.9, 0.999)])
+def test_ahla_backward_matches_oracle(B, H, n, gamma):
+    """AHLA gradients (u = LA(q, k, v), o = LA(q, k, u) and six reverse-mode scans) against the
+    oracle's reverse sweep of the AHLA streaming recurrence."""
+    x = inputs.make_custom(B, H, n, 64, 64, torch.bfloat16, seed=11 * n + H, gamma=gamma, with_dout=True)
+    got = _ahla_grads(x)
+    ref = A.serial_backward(np32(x["q"]), np32(x["k"]), np32(x["v"]), np32(x["dout"]), _gamma_np(x))
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, ref):
+        assert torch.isfinite(gg.float()).all(), name
+        assert rel_err(np64(gg.cpu()), rr) <= 2e-2, (name, B, H, n, gamma)
+
+
+def test_ahla_backward_distinct_from_the_simt_path():
+    x = inputs.make_custom(1, 2, 600, 64, 64, torch.bfloat16, seed=12, gamma=(0.97, 0.999), with_dout=True)
+    tc = _ahla_grads(x)
+    old = os.environ.get("HLA2_KERNEL")
+    os.environ["HLA2_KERNEL"] = "mma"
+    try:
+        simt = _ahla_grads(x)
+    finally:
+        if old is None:
+            os.environ.pop("HLA2_KERNEL", None)
+        else:
+            os.environ["HLA2_KERNEL"] = old
+    ref = A.serial_backward(np32(x["q"]), np32(x["k"]), np32(x["v"]), np32(x["dout"]), _gamma_np(x))
+    for gg in (tc, simt):
+        for name, g1, rr in zip(("dq", "dk", "dv"), gg, ref):
+            assert rel_err(np64(g1.cpu()), rr) <= 2e-2, name
+    assert not all(torch.equal(a, b) for a, b in zip(tc, simt))
