@@ -57,8 +57,10 @@ struct MmaCfg {
     static constexpr size_t oS = oAB + (size_t)W * LW * 2;
     static constexpr size_t oZ = oS + (size_t)D * LD * 2;
     static constexpr size_t oF = oZ + (size_t)D * LDV * 2;  // float region
-    // floats: gp[2W+2] den[W] yadd[D] y[D] m[D]
-    static constexpr size_t nF = (2 * W + 2) + W + 3 * D;
+    // floats: gp[2W+2] den[W] denpart[TW][W] ypart[TW][D] y[D] m[D]; the per-tile partial
+    // sums of the denominator rows and the y increment are added in a fixed order, so that
+    // the result does not depend on the order in which warps finish
+    static constexpr size_t nF = (2 * W + 2) + W + (size_t)TW * W + (size_t)TW * D + 2 * D;
     static constexpr size_t oQt = oF + ((nF * 4 + 15) / 16) * 16;
     static constexpr size_t bytes(bool cm) { return oQt + (cm ? ROWS_D : 0); }
 };
@@ -85,8 +87,9 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
     bf16* Zst = reinterpret_cast<bf16*>(smem + Cfg::oZ);
     float* gp = reinterpret_cast<float*>(smem + Cfg::oF);
     float* den = gp + 2 * W + 2;
-    float* yadd = den + W;
-    float* ys = yadd + D;
+    float* denpart = den + W;          // [TW][W]: row sums of B~ over column block jb
+    float* ypart = denpart + TW * W;   // [TW][D]: column sums of P~ over row block rb
+    float* ys = ypart + TW * D;
     float* ms = ys + D;
     bf16* Qt = reinterpret_cast<bf16*>(smem + Cfg::oQt);
 
@@ -150,8 +153,8 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
     for (int f = tid; f < D; f += NT) {
         ys[f] = SUMMARY ? 0.f : a.ws[a.L.yin + ((size_t)bh * nseg + seg) * D + f];
         ms[f] = (CM && !SUMMARY) ? a.ws[a.L.mlast + (size_t)bh * D + f] : 0.f;
-        yadd[f] = 0.f;
     }
+    for (int i = tid; i < TW * D; i += NT) ypart[i] = 0.f;
 
     // bf16 copies of S and Z: the B operands of Q S0 and Q Z0
     auto publish_state = [&]() {
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
             for (int f = tid; f < D; f += NT) {
                 float s = 0.f;
                 for (int r = 0; r < Wc; ++r) s += gp[Wc - 1 - r] * to_f32(Qs[r * LD + f]);
-                yadd[f] = s;
+                ypart[f] = s;
             }
         }
         if (OUTPUT && a.normalize && !UM) {
@@ -311,7 +314,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
                     s += __shfl_xor_sync(0xffffffffu, s, 4);
                     s += __shfl_xor_sync(0xffffffffu, s, 8);
                     s += __shfl_xor_sync(0xffffffffu, s, 16);
-                    if (lane < 4) atomicAdd(&yadd[fb * 16 + h * 8 + lane * 2 + j], s);
+                    if (lane < 4) ypart[rb * D + fb * 16 + h * 8 + lane * 2 + j] = s;
                 }
         }
         __syncthreads();
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
                         float s = rs[j];
                         s += __shfl_xor_sync(0xffffffffu, s, 1);
                         s += __shfl_xor_sync(0xffffffffu, s, 2);
-                        if ((lane & 3) == 0) atomicAdd(&den[rb * 16 + (lane >> 2) + j * 8], s);
+                        if ((lane & 3) == 0) denpart[jb * W + rb * 16 + (lane >> 2) + j * 8] = s;
                     }
                 }
             }
@@ -380,7 +383,9 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
                         if (r >= Wc || !HLA2_IN(c * W + r < a.n, 405)) continue;
                         float o0 = acc[h][i], o1 = acc[h][i + 1];
                         if (a.normalize) {
-                            const float inv = 1.f / (den[r] + a.eps);
+                            float dr = den[r];
+                            for (int jb = 0; jb <= r / 16; ++jb) dr += denpart[jb * W + r];
+                            const float inv = 1.f / (dr + a.eps);
                             o0 *= inv;
                             o1 *= inv;
                         }
@@ -423,8 +428,12 @@ __global__ void __launch_bounds__(MmaCfg<D, DV, W>::NT)
 
         publish_state();
         for (int f = tid; f < D; f += NT) {
-            ys[f] = rho2 * ys[f] + yadd[f];
-            yadd[f] = 0.f;
+            float inc = 0.f;
+            for (int rb = 0; rb < TW; ++rb) {
+                inc += ypart[rb * D + f];
+                ypart[rb * D + f] = 0.f;
+            }
+            ys[f] = rho2 * ys[f] + inc;
         }
         if (c + 1 < c_end) load_chunk(c + 1);
     }

@@ -45,6 +45,25 @@ def test_normed_bf16_workload():
     assert rel_err(np64(o), ref) <= 2e-2
 
 
+def test_mma_forward_is_reproducible():
+    """The mma.sync forward adds the per-tile partial sums of the denominator rows and of the
+    y moment in a fixed order: two runs of the normalised workload, and two runs of a call
+    whose final state reads the y moment, give the same bits."""
+    x = inputs.make("normed")
+    a = run_gpu(x, chunk=64, normalize=True, eps=x["eps"])
+    b = run_gpu(x, chunk=64, normalize=True, eps=x["eps"])
+    assert torch.equal(a, b)
+    y = inputs.make_custom(2, 4, 700, 64, 64, torch.bfloat16, seed=21, gamma=(0.97, 0.999))
+    o1, s1 = run_gpu(y, chunk=64, return_final_state=True)
+    o2, s2 = run_gpu(y, chunk=64, return_final_state=True)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    ref, ref_state = oracle(y, return_state=True)
+    assert rel_err(np64(o1.cpu()), ref) <= 2e-2
+    got, want = O.unpack_state(np64(s1.cpu()), 64, 64), O.unpack_state(ref_state, 64, 64)
+    for key in ("S", "C", "m", "G", "h"):
+        assert rel_err(got[key], want[key]) <= 2e-2, key
+
+
 def test_long_context_full_size():
     """n = 65536, 16 heads, d = dv = 64: the benchmarked launch, every output compared."""
     x = inputs.make("long")
