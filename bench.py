@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode and training rows measured after the headline")
     ap.add_argument("--only", choices=("decode", "decode_compact", "decode_unmasked", "decode_mq", "train", "ahla",
-                                       "unmasked", "hla3", "prefill", "train_d64", "ahla_backward"),
+                                       "unmasked", "hla3", "prefill", "train_d64", "ahla_backward", "normed"),
                     default=None,
                     help="measure only this row (for profiler captures; --steps/--warmup apply)")
     ap.add_argument("--decode-seqs", type=int, default=256,
@@ -455,6 +455,47 @@ def measure_ahla(dev, dist: Dist, hbm_gbs: float, bf16_tflops: float, steps: int
                          "step_tensor_frac": flops / (ms * 1e-3) / 1e12 / bf16_tflops}}
 
 
+def measure_normed(dev, dist: Dist, hbm_gbs: float, steps: int = 200, warmup: int = 10, n: int | None = None):
+    """Ratio-normalised rows: the normalised workload (B=2 H=8 n=2048 d=dv=64 bf16, softplus
+    q and k, unit-variance v, decay linspace(0.95, 0.999), eps 1e-6) at chunk 128, where the
+    tcgen05 stored-p kernels run (the output pass forms the denominator in its epilogue), and
+    at its stated chunk 64 on the mma.sync kernels; then the same recipe at the long-context
+    length (B=1 H=16 n=65536) at chunk 128.  HBM roofline of the whole call over q, k, v read
+    and out written."""
+    import dataclasses
+
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = inputs.WORKLOADS["normed"]
+    rows = {}
+    for name, ww, chunk in (("normed_chunk128", w, 128), ("normed_chunk64", w, 64),
+                            ("normed_long", dataclasses.replace(w, B=1, H=16, n=n or 65536), 128)):
+        x = inputs.make(ww, device=dev, seed=replica_seed(ww.seed, dist.rank))
+        q, k, v = x["q"], x["k"], x["v"]
+        gamma = x["gamma"].to(dev)
+        out = torch.empty_like(v)
+
+        def one():
+            hla.forward(q, k, v, gamma=gamma, chunk=chunk, normalize=True, eps=ww.eps, out=out)
+
+        long = name == "normed_long"
+        ms = dist.max(_device_ms(one, steps // 4 if long else steps, warmup, torch.cuda.synchronize))
+        tokens = ww.B * ww.H * ww.n
+        nbytes = tokens * (2 * ww.d + 2 * ww.dv) * 2
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        rows[name] = {"workload": f"normalised forward: B={ww.B} H={ww.H} n={ww.n} d=dv={ww.d} bf16, softplus q/k, "
+                                  f"decay linspace{tuple(ww.gamma)}, eps {ww.eps}, chunk {chunk}",
+                      "metric": "normalised fwd tokens/s", "unit": "tokens/s",
+                      "value": dist.world * tokens / (ms * 1e-3), "ms_per_step": ms,
+                      "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                                   "frac": achieved / hbm_gbs, "kernel": "whole call",
+                                   "algorithmic_bytes_per_step": nbytes}}
+    return rows
+
+
 def measure_ahla_backward(dev, dist: Dist, hbm_gbs: float, steps: int = 20, warmup: int = 3, n: int | None = None):
     """AHLA reverse-mode row: dq, dk, dv of the unnormalised AHLA output on the long-context
     shapes (B=1 H=16 n=65536 d=dv=64 bf16, decay linspace(0.99, 0.9999), chunk 128: the tcgen05
@@ -623,6 +664,8 @@ def run_only(args, dist: Dist, dev):
         row = measure_ahla(dev, dist, hbm_gbs, bf16_tflops, steps=args.steps, warmup=args.warmup, n=args.n)
     elif args.only == "ahla_backward":
         row = measure_ahla_backward(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
+    elif args.only == "normed":
+        row = measure_normed(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
     elif args.only == "train_d64":
         row = measure_train(dev, dist, bf16_tflops, hbm_gbs, steps=args.steps, warmup=args.warmup, d=64)
     else:
@@ -761,6 +804,7 @@ def run_ours(args, dist: Dist):
                      "unmasked": measure_unmasked(dev, dist, hbm_gbs),
                      "hla3": measure_hla3(dev, dist, hbm_gbs),
                      "prefill": measure_prefill(dev, dist, hbm_gbs)}
+        secondary.update(measure_normed(dev, dist, hbm_gbs))
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

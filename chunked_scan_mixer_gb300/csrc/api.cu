@@ -246,9 +246,9 @@ bool tc_disabled() {
 
 Path choose_forward_path(int dtype, int d, int dv, int W, int normalize, bool want_final, const DevInfo& di,
                          bool unmasked = false) {
-    (void)want_final;
-    (void)unmasked;  // the tcgen05 kernels have both outputs, with or without the final state
-    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !normalize && !tc_disabled() &&
+    (void)want_final;  // the tcgen05 kernels have both outputs, with or without the final state,
+                       // and the masked one also ratio-normalised
+    if (dtype == HLA2_BF16 && d == 64 && dv == 64 && W == 128 && !(normalize && unmasked) && !tc_disabled() &&
         fwd_chunk_tc_smem() <= (size_t)di.smem_optin && fwd_chunk_tc_available())
         return Path::kTc;
     if (dtype == HLA2_BF16) {
@@ -439,10 +439,13 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     a.unmasked = unmasked ? 1 : 0;
 
     const bool bf = opts->dtype == HLA2_BF16;
-    // tcgen05 path with more than one segment (or a final state): the summary pass also stores
-    // the segment-local p_t = S_t q_t in out, over every segment, and the output pass starts from
-    // it (kOutputP), so that only Z (unmasked: C) is carried from chunk to chunk there.
-    const bool stored_p = path == Path::kTc && (p.nseg > 1 || tc_final);
+    // tcgen05 path with more than one segment (or a final state, or normalised): the summary
+    // pass also stores the segment-local p_t = S_t q_t in out, over every segment, and the
+    // output pass starts from it (kOutputP), so that only Z (unmasked: C) is carried from chunk
+    // to chunk there.  Its q and p moments per segment (the y carry of the denominator and of
+    // the final state) come from the moments kernel.
+    const bool stored_p = path == Path::kTc && (p.nseg > 1 || tc_final || normalize);
+    const bool tc_moments = path == Path::kTc && (tc_final || normalize);
     auto chunk_pass = [&](int seg0, int count, bool summary, bool cm) -> int {
         ChunkArgs b = a;
         b.seg0 = seg0;
@@ -464,15 +467,15 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     mark(0);
     if (launch_init_carry(a, d, dv, opts->init_state, st)) return cuda_fail("carry-in initialisation");
     mark(1);
-    if (tc_final && p.nseg == 1) {  // one segment: its summary and moments for the final combine
+    if (stored_p && p.nseg == 1) {  // one segment: its p (a final state: its summary and moments)
         if (chunk_pass(0, 1, true, true)) return cuda_fail("segment summaries");
-        if (launch_seg_moments64(a, st)) return cuda_fail("segment moments");
+        if (tc_final && launch_seg_moments64(a, st)) return cuda_fail("segment moments");
         mark(2);
     } else if (p.nseg > 1) {
         const int steps = p.nseg - 1, seg_tokens = p.seg_chunks * chunk;
         const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
         if (chunk_pass(0, stored_p ? p.nseg : steps, true, true)) return cuda_fail("segment summaries");
-        if (tc_final && launch_seg_moments64(a, st)) return cuda_fail("segment moments");
+        if (tc_moments && launch_seg_moments64(a, st)) return cuda_fail("segment moments");
         mark(2);
         if (launch_linear_scan(a.ws + L.SB, a.ws + L.Sin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true,
                                gamma, seg_tokens, 1, st))
@@ -593,11 +596,15 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     chunk = W;
     const Plan p = forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, di);
     int l = 0;
-    if (p.nseg > 0 && want_final_state &&
-        choose_forward_path(dtype, d, dv, chunk, normalize, true, di) == Path::kTc) {
+    const bool tc = choose_forward_path(dtype, d, dv, chunk, normalize, want_final_state != 0, di) == Path::kTc;
+    if (p.nseg > 0 && want_final_state && tc) {
         // carry-in, summary, segment moments, output, final combine; S, C, m scans, cross terms,
         // Z and y scans
         l = 5 + (p.nseg > 1 ? 6 : 0);
+    } else if (p.nseg > 0 && normalize && tc) {
+        // carry-in, summary (it stores p), output; segment moments, S scan, cross terms, Z and
+        // y scans
+        l = 3 + (p.nseg > 1 ? 5 : 0);
     } else if (p.nseg > 0) {
         l = 2;                                                   // carry-in, output pass
         if (p.nseg > 1)                                          // summary, S/Z scans, cross; y, C, m scans

@@ -85,9 +85,10 @@ __device__ __forceinline__ uint4 pack8(const float* f, float s) {
 //   out[i] = [i <= r] base^(r - i) * in[i],  i = cb .. cb + 31,
 // with base = g (A~) or g^2 (B~), read from src (TMEM, fp32) and written packed (16 columns)
 // to dst.  Blocks entirely above the diagonal of this warp's rows are written as zeros
-// without reading; the factors are stepped multiplicatively from base^(r - cb).
+// without reading; the factors are stepped multiplicatively from base^(r - cb).  rs, when
+// given, accumulates the block's fp32 row sum (the normalised output's denominator).
 __device__ __forceinline__ void masked_pack(uint32_t src, int r, int cb, int warp_row0, float first, float step_up,
-                                            uint32_t (&pk)[16]) {
+                                            uint32_t (&pk)[16], float* rs = nullptr) {
     if (cb > warp_row0 + 31) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = 0u;
@@ -107,15 +108,16 @@ __device__ __forceinline__ void masked_pack(uint32_t src, int r, int cb, int war
                 a0 = cb + j <= r ? a0 : 0.f;
                 a1 = cb + j + 1 <= r ? a1 : 0.f;
             }
+            if (rs) *rs += a0 + a1;
             pk[j / 2] = pack_bf16x2(a0, a1);
         }
     }
 }
 
 __device__ __forceinline__ void masked_block(uint32_t src, uint32_t dst, int r, int cb, int warp_row0,
-                                             float first, float step_up) {
+                                             float first, float step_up, float* rs = nullptr) {
     uint32_t pk[16];
-    masked_pack(src, r, cb, warp_row0, first, step_up, pk);
+    masked_pack(src, r, cb, warp_row0, first, step_up, pk, rs);
     tc::tmem_st16(dst, pk);
 }
 
@@ -463,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ---------------------------------------------------------------------------------------------
-// Output pass from the stored segment-local p (unnormalised; kOutputP; UM = unmasked).
+// Output pass from the stored segment-local p (kOutputP; UM = unmasked, NORM = ratio-normalised).
 //
 // The summary pass stores, for every token t of segment s, p^sl_t = S^sl_t q_t, where S^sl is
 // the key moment accumulated from zero at the segment start (bf16, in the output buffer).
@@ -485,6 +487,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 // MMA-a of the next chunk and the next loads overlap EPI-c.  The unmasked output (UM) forms
 // P Q^T and P C0 instead (C0 in the Z0 slot), masks with g^(r-j), scales by g^(r+1), carries
 // C (decay g^Wc) and takes dC = [Q~^T ; Q~^T] V with Q~ = diag(g^(Wc-1-r)) Q in the P~ slot.
+//
+// NORM (masked; section summary §3: the denominator is the same recurrence with every value
+// row replaced by 1) divides each output row by den + eps, with
+//     den_r = g^(2(r+1)) q_r . y0 + sum_j B~[r][j],     y <- g^(2Wc) y0 + sum_r P~[r],
+// y0 the p moment at the chunk start (the segment's carry-in y_in, then updated chunk by
+// chunk).  All of it is epilogue arithmetic in fp32: q_r . y0 and the column sums of P~ in
+// EPI-a (the column sums by a shuffle reduction over the warp's 32 rows, then per lane
+// quarter in shared memory), the row sums of B~ in EPI-b, the division and the y update in
+// EPI-c.  The partial sums are added in a fixed order (results reproducible bit for bit).
 // Same roles, bounded waits and two CTAs per SM as the kernel above.
 namespace outp {
 
@@ -495,7 +506,10 @@ constexpr uint32_t oZ0 = oS + 8192;       // Z0, [64][64] bf16 (8 KB), B operand
 constexpr uint32_t oGP = oZ0 + 8192;      // decay table g^0 .. g^(2W)
 constexpr uint32_t oBar = oGP + 1088;
 constexpr uint32_t oMisc = oBar + 16 * 8;
-constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
+constexpr uint32_t oY = oMisc + 16;       // NORM: y0 [64] fp32
+constexpr uint32_t oYP = oY + 256;        // NORM: column sums of P~ per lane quarter [4][64]
+constexpr uint32_t oDP = oYP + 1024;      // NORM: denominator partials per column half [2][128]
+constexpr uint32_t kSmemBytes = oDP + 1024 + 1024;
 constexpr uint32_t T0 = 0, T1 = 64, T2 = 128, T3 = 192;
 
 enum Bar { FQP = 0, FV, BA, BAT, BB, BBT, BC, BOS, kBarCount };
@@ -506,9 +520,10 @@ struct Maps {
 
 }  // namespace outp
 
-template <bool UM>
+template <bool UM, bool NORM>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_out_p_tc_kernel(const __grid_constant__ outp::Maps maps, const ChunkArgs a, int* status) {
+    static_assert(!(UM && NORM), "the unmasked normalised output runs on the other kernels");
     pdl_trigger();
     // this pass's layout (shadows the kernel above)
     constexpr uint32_t oQ = outp::oQ, oP = outp::oP, oV = outp::oV, oPt = outp::oPt, oO = outp::oO, oS = outp::oS,
@@ -523,6 +538,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + oMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(sm + oMisc + 4);
+    float* y0 = reinterpret_cast<float*>(sm + outp::oY);
+    float* ypart = reinterpret_cast<float*>(sm + outp::oYP);
+    float* dpart = reinterpret_cast<float*>(sm + outp::oDP);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = a.seg0 + blockIdx.x, bh = blockIdx.y;
@@ -568,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int j = 0; j < 16; ++j) zz[j] = zsrc[j];
         publish_z();
+        if (NORM && h == 0 && r < 64) y0[r] = a.ws[a.L.yin + sidx * kD + r];
         tc::fence_proxy_async();
     }
     tc::fence_before_sync();
@@ -671,9 +690,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc::mbar_wait(&bars[FQP], ph, abort, status, 51);
             tc::mbar_wait(&bars[BA], ph, abort, status, 52);
             tc::fence_after_sync();
+            float qy = 0.f;  // NORM: q_r . y0 over this thread's 32 columns
             {
                 const float f = pow_decay(log2g, (float)(it * kW + r + 1));
                 const float w2 = r < Wc ? gp[2 * (Wc - 1 - r)] : 0.f;
+                if (NORM) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 qc = *reinterpret_cast<const uint4*>(sm + oQ + tc::sw128_chunk(r, 4 * h + j));
+                        const uint32_t qw[4] = {qc.x, qc.y, qc.z, qc.w};
+                        const float* yy = y0 + 32 * h + 8 * j;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) qy += bf_lo(qw[u]) * yy[2 * u] + bf_hi(qw[u]) * yy[2 * u + 1];
+                    }
+                }
                 if (UM) {  // the state product forms dC = Q~^T V: Q~ = diag(g^(Wc-1-r)) Q in the P~ slot
                     const float w1 = r < Wc ? gp[Wc - 1 - r] : 0.f;
 #pragma unroll
@@ -688,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     uint32_t qs[16];
                     tc::tmem_ld16(lrow + T0 + 32 * h + 16 * half, qs);
                     tc::tmem_wait_ld();
+                    float cs[16];  // NORM: this row's P~ over the half's 16 columns
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const uint32_t off = tc::sw128_chunk(r, 4 * h + 2 * half + j);
@@ -701,6 +732,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                         }
                         *reinterpret_cast<uint4*>(sP + off) = pack8(pv, 1.f);
                         if (!UM) *reinterpret_cast<uint4*>(sPt + off) = pack8(pv, w2);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) cs[8 * j + u] = w2 * pv[u];
+                    }
+                    if (NORM) {
+                        // column sums over the warp's 32 rows: after the halving steps lane l holds
+                        // column l & 15 summed over the 16 lanes that share bit 4, then over all 32
+#pragma unroll
+                        for (int off = 8; off >= 1; off >>= 1) {
+                            const bool up = (lane & off) != 0;
+#pragma unroll
+                            for (int i = 0; i < off; ++i) {
+                                const float send = up ? cs[i] : cs[i + off];
+                                const float keep = up ? cs[i + off] : cs[i];
+                                cs[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                            }
+                        }
+                        cs[0] += __shfl_xor_sync(0xffffffffu, cs[0], 16);
+                        if (lane < 16) ypart[64 * q4 + 32 * h + 16 * half + lane] = cs[0];
                     }
                 }
             }
@@ -717,11 +766,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc::fence_after_sync();
             constexpr int BP2 = UM ? 1 : 2;  // decay power of the second product
             const float step2 = UM ? ginv : ginv * ginv;
+            float rs = 0.f;  // NORM: row sum of B~ over this warp's 64 columns
             if (h == 0) {
 #pragma unroll
                 for (int p = 0; p < 2; ++p) {
                     const float first = r >= 32 * p ? gp[BP2 * (r - 32 * p)] : 0.f;
-                    masked_block(lrow + T0 + 32 * p, lrow + T0 + 16 * p, r, 32 * p, row0, first, step2);
+                    masked_block(lrow + T0 + 32 * p, lrow + T0 + 16 * p, r, 32 * p, row0, first, step2,
+                                 NORM ? &rs : nullptr);
                 }
                 tc::fence_before_sync();
                 switch (q4) {  // constant barrier ids
@@ -732,8 +783,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             } else {
                 uint32_t pk0[16], pk1[16];
-                masked_pack(lrow + T0 + 64, r, 64, row0, r >= 64 ? gp[BP2 * (r - 64)] : 0.f, step2, pk0);
-                masked_pack(lrow + T0 + 96, r, 96, row0, r >= 96 ? gp[BP2 * (r - 96)] : 0.f, step2, pk1);
+                masked_pack(lrow + T0 + 64, r, 64, row0, r >= 64 ? gp[BP2 * (r - 64)] : 0.f, step2, pk0,
+                            NORM ? &rs : nullptr);
+                masked_pack(lrow + T0 + 96, r, 96, row0, r >= 96 ? gp[BP2 * (r - 96)] : 0.f, step2, pk1,
+                            NORM ? &rs : nullptr);
                 switch (q4) {
                     case 0: tc::named_bar(1, 64); break;
                     case 1: tc::named_bar(2, 64); break;
@@ -745,6 +798,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 tc::tmem_st16(lrow + T0 + 48, pk1);
             }
             tc::tmem_wait_st();
+            if (NORM) dpart[128 * h + r] = gp[2 * (r + 1)] * qy + rs;
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&bars[BBT]);
@@ -752,6 +806,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             // ---- EPI-c: out = g^(2(r+1)) Q Z0 + B~ V;  Z <- g^(2Wc) Z + dZ ------------------------
             tc::mbar_wait(&bars[BC], ph, abort, status, 54);
             tc::fence_after_sync();
+            float inv = 1.f;
+            if (NORM) {  // every epilogue warp's partials of this chunk are written, and y0 read
+                tc::named_bar(5, 256);
+                inv = 1.f / ((dpart[r] + dpart[128 + r]) + a.eps);
+            }
             {
                 const float s2 = gp[BP2 * (r + 1)];
 #pragma unroll
@@ -766,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
                             o[u] = s2 * __uint_as_float(qz[8 * j + u]) + __uint_as_float(bv[8 * j + u]);
-                        *reinterpret_cast<uint4*>(sm + oO + tc::sw128_chunk(r, 4 * h + 2 * half + j)) = pack8(o, 1.f);
+                        *reinterpret_cast<uint4*>(sm + oO + tc::sw128_chunk(r, 4 * h + 2 * half + j)) = pack8(o, inv);
                     }
                 }
                 uint32_t dz[16];
@@ -776,6 +835,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) zz[j] = rho2 * zz[j] + __uint_as_float(dz[j]);
                 publish_z();  // read by MMA-b of the next chunk, after its EPI-a arrives
+                if (NORM) {  // y0 for the next chunk, then every warp sees it before its EPI-a
+                    if (q4 == 0) {
+                        const int cy = 32 * h + lane;
+                        y0[cy] = rho2 * y0[cy] + (((ypart[cy] + ypart[64 + cy]) + ypart[128 + cy]) + ypart[192 + cy]);
+                    }
+                    tc::named_bar(6, 256);
+                }
             }
             tc::fence_proxy_async();
             __syncwarp();
@@ -1122,7 +1188,8 @@ int launch_fwd_chunk_tc(const ChunkArgs& a, int mode, int* status, cudaStream_t 
         outp::Maps pm;
         if (!make_map(&pm.q, a.q, a.BH, a.n) || !make_map(&pm.p, a.out, a.BH, a.n) || !make_map(&pm.v, a.v, a.BH, a.n))
             return -2;
-        auto kfn = a.unmasked ? fwd_out_p_tc_kernel<true> : fwd_out_p_tc_kernel<false>;
+        auto kfn = a.unmasked ? fwd_out_p_tc_kernel<true, false>
+                              : (a.normalize ? fwd_out_p_tc_kernel<false, true> : fwd_out_p_tc_kernel<false, false>);
         cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, outp::kSmemBytes);
         if (e != cudaSuccess) return -1;
         if (launch_pdl(kfn, dim3(a.nseg_launch, a.BH), dim3(kThreads), outp::kSmemBytes, st, pm, a, status) !=

@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(kThreads) cross_kernel(const ChunkArgs a, int 
     }
 }
 
-// Query and p moments of every segment for the final state of the stored-p path (d = 64, bf16):
+// Query and p moments of every kept segment summary for the final state and the normalised
+// output of the stored-p path (d = 64, bf16):
 //   m_B[s] = sum_t g^(L-1-t) q_t,   y_B[s] = sum_t g^(2(L-1-t)) p^sl_t,
 // t the token's place in segment s of L tokens, p^sl the segment-local p that the summary pass
 // stored in out (read here before the output pass replaces it).  The tcgen05 summary pass
@@ -444,8 +445,8 @@ int launch_cross(const ChunkArgs& a, int d, int dv, bool with_y, cudaStream_t st
 }
 
 int launch_seg_moments64(const ChunkArgs& a, cudaStream_t st) {
-    if (a.nseg <= 0 || a.BH <= 0) return 0;
-    if (launch_pdl(seg_moments64_kernel, dim3(a.nseg, a.BH, 2), dim3(kThreads), 0, st, a) != cudaSuccess) return -1;
+    if (a.nsum <= 0 || a.BH <= 0) return 0;  // the summaries kept: every segment but the last, or all
+    if (launch_pdl(seg_moments64_kernel, dim3(a.nsum, a.BH, 2), dim3(kThreads), 0, st, a) != cudaSuccess) return -1;
     return finish_launch();
 }
 

@@ -142,14 +142,16 @@ size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chun
  * grouped into segments; per-segment summaries are combined by an exclusive scan
  * with the masked semidirect product (cross term S_B C_A) to give each segment
  * its carry-in; every token's output is then formed from its inclusive state.
- * normalize != 0 divides by the masked denominator (+ opts->eps).
+ * normalize != 0 divides by the masked denominator (+ opts->eps); on the tcgen05 path (bf16,
+ * d = dv = 64, chunk 128, masked) the denominator is formed in the output pass's epilogue.
  * opts must be non-NULL (dtype and workspace).  init_state continues a previous
  * sequence; final_state receives the state after the last token (prefill for
  * hla2_decode_step).  opts->flags may hold HLA2_FLAG_SAVE_FOR_BACKWARD or
  * HLA2_FLAG_UNMASKED (the unmasked output, with the same workspace size).
  * out must not overlap q, k or v: on the masked bf16 path at d = dv = 64, chunk 128 with
- * more than one segment, the summary pass first stores p_t = S_t q_t (the key moment
- * accumulated from the segment start) in out, and the output pass overwrites it.
+ * more than one segment, a final state or normalize != 0, the summary pass first stores
+ * p_t = S_t q_t (the key moment accumulated from the segment start) in out, and the output
+ * pass overwrites it.
  */
 int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n,
                  int d, int dv, const float* gamma, int normalize, int chunk,
