@@ -445,7 +445,8 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     // to chunk there.  Its q and p moments per segment (the y carry of the denominator and of
     // the final state) come from the moments kernel.
     const bool stored_p = path == Path::kTc && (p.nseg > 1 || tc_final || normalize);
-    const bool tc_moments = path == Path::kTc && (tc_final || normalize);
+    // (the masked summary pass forms them itself; the unmasked final state runs the kernel)
+    const bool tc_moments = path == Path::kTc && unmasked && tc_final;
     auto chunk_pass = [&](int seg0, int count, bool summary, bool cm) -> int {
         ChunkArgs b = a;
         b.seg0 = seg0;
@@ -469,7 +470,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
     mark(1);
     if (stored_p && p.nseg == 1) {  // one segment: its p (a final state: its summary and moments)
         if (chunk_pass(0, 1, true, true)) return cuda_fail("segment summaries");
-        if (tc_final && launch_seg_moments64(a, st)) return cuda_fail("segment moments");
+        if (tc_moments && launch_seg_moments64(a, st)) return cuda_fail("segment moments");
         mark(2);
     } else if (p.nseg > 1) {
         const int steps = p.nseg - 1, seg_tokens = p.seg_chunks * chunk;
@@ -598,13 +599,13 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     int l = 0;
     const bool tc = choose_forward_path(dtype, d, dv, chunk, normalize, want_final_state != 0, di) == Path::kTc;
     if (p.nseg > 0 && want_final_state && tc) {
-        // carry-in, summary, segment moments, output, final combine; S, C, m scans, cross terms,
-        // Z and y scans
-        l = 5 + (p.nseg > 1 ? 6 : 0);
+        // carry-in, summary (with the segment moments), output, final combine; S, C, m scans,
+        // cross terms, Z and y scans (the launch count of the masked output)
+        l = 4 + (p.nseg > 1 ? 6 : 0);
     } else if (p.nseg > 0 && normalize && tc) {
-        // carry-in, summary (it stores p), output; segment moments, S scan, cross terms, Z and
-        // y scans
-        l = 3 + (p.nseg > 1 ? 5 : 0);
+        // carry-in, summary (it stores p and forms the moments), output; S scan, cross terms,
+        // Z and y scans
+        l = 3 + (p.nseg > 1 ? 4 : 0);
     } else if (p.nseg > 0) {
         l = 2;                                                   // carry-in, output pass
         if (p.nseg > 1)                                          // summary, S/Z scans, cross; y, C, m scans

@@ -114,6 +114,23 @@ __device__ __forceinline__ void masked_pack(uint32_t src, int r, int cb, int war
     }
 }
 
+// Sums over a warp's 32 rows of a 16-column block held one row per lane (cs[c], column c):
+// halving steps leave lane l with column l & 15 summed over the 16 lanes that share bit 4, the
+// last step adds the other 16.  Every lane returns the sum of column l & 15.
+__device__ __forceinline__ float warp_colsum16(float (&cs)[16], int lane) {
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) {
+        const bool up = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = up ? cs[i] : cs[i + off];
+            const float keep = up ? cs[i + off] : cs[i];
+            cs[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return cs[0] + __shfl_xor_sync(0xffffffffu, cs[0], 16);
+}
+
 __device__ __forceinline__ void masked_block(uint32_t src, uint32_t dst, int r, int cb, int warp_row0,
                                              float first, float step_up, float* rs = nullptr) {
     uint32_t pk[16];
@@ -735,21 +752,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                         for (int u = 0; u < 8; ++u) cs[8 * j + u] = w2 * pv[u];
                     }
-                    if (NORM) {
-                        // column sums over the warp's 32 rows: after the halving steps lane l holds
-                        // column l & 15 summed over the 16 lanes that share bit 4, then over all 32
-#pragma unroll
-                        for (int off = 8; off >= 1; off >>= 1) {
-                            const bool up = (lane & off) != 0;
-#pragma unroll
-                            for (int i = 0; i < off; ++i) {
-                                const float send = up ? cs[i] : cs[i + off];
-                                const float keep = up ? cs[i + off] : cs[i];
-                                cs[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                            }
-                        }
-                        cs[0] += __shfl_xor_sync(0xffffffffu, cs[0], 16);
-                        if (lane < 16) ypart[64 * q4 + 32 * h + 16 * half + lane] = cs[0];
+                    if (NORM) {  // column sums over the warp's 32 rows
+                        const float t = warp_colsum16(cs, lane);
+                        if (lane < 16) ypart[64 * q4 + 32 * h + 16 * half + lane] = t;
                     }
                 }
             }
@@ -876,6 +881,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 //   ST    [Q~^T ; P~^T] V -> T2 (dC, dZ; unmasked: [Q~^T ; Q~^T] V, dC twice);
 //         [K^^T ; K^^T] K^ -> T3 (dS twice)
 //   EPI4  S <- g^Wc S + dS,  C <- g^Wc C + dC,  Z <- g^(2Wc) Z + dZ;  bf16 S0 (smem)
+// MOM (masked; a final state or the normalised output) also forms the segment's query and p
+// moments, m_B = sum_t g^(L-1-t) q_t and y_B = sum_t g^(2(L-1-t)) p^sl_t: per chunk the column
+// sums of Q~ (EPI1) and P~ (EPI2), each reduced over a warp's 32 rows by shuffles into lane l's
+// running sum of column 32h + l (decayed by g^Wc and g^(2Wc) like C and Z), and at the end
+// summed over the four lane quarters in a fixed order.
 namespace sump {
 
 constexpr uint32_t oQ = 0, oK = kTile, oV = 2 * kTile, oQt = 3 * kTile, oKh = 4 * kTile, oPt = 5 * kTile;
@@ -883,7 +893,8 @@ constexpr uint32_t oS0 = 6 * kTile;   // S0, [64][64] bf16 (8 KB)
 constexpr uint32_t oGP = oS0 + 8192;  // decay table g^0 .. g^(2W)
 constexpr uint32_t oBar = oGP + 1088;
 constexpr uint32_t oMisc = oBar + 16 * 8;
-constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
+constexpr uint32_t oMom = oMisc + 16;  // MOM: m and y partials per lane quarter [2][4][64] fp32
+constexpr uint32_t kSmemBytes = oMom + 2048 + 1024;
 constexpr uint32_t T0 = 0, T2 = 128, T3 = 192;  // T0 .. T0+127: A = Q K^T (N = 128)
 
 enum Bar { FQK = 0, FV, BA, BAT, BP, BPS, BST, kBarCount };
@@ -894,9 +905,10 @@ struct Maps {
 
 }  // namespace sump
 
-template <bool UM>
+template <bool UM, bool MOM>
 __global__ void __launch_bounds__(kThreads, 2)
     fwd_sum_p_tc_kernel(const __grid_constant__ sump::Maps maps, const ChunkArgs a, int* status) {
+    static_assert(!(UM && MOM), "the unmasked moments come from the moments kernel");
     pdl_trigger();
     // this pass's layout (shadows the first kernel's)
     constexpr uint32_t oQ = sump::oQ, oK = sump::oK, oV = sump::oV, oQt = sump::oQt, oKh = sump::oKh,
@@ -1051,6 +1063,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         };
         publish_s();
         tc::fence_proxy_async();
+        float mw = 0.f, yw = 0.f;  // MOM: this warp's rows' moments of column 32h + lane
 
         for (int it = 0; it < nit; ++it) {
             const uint32_t ph = it & 1;
@@ -1073,12 +1086,28 @@ __global__ void __launch_bounds__(kThreads, 2)
             {  // first read by ST, after EPI2's fence
                 const float w1 = r < Wc ? gp[Wc - 1 - r] : 0.f;
                 const float wh = r < Wc ? pow_decay(log2g, 0.5f * (float)(Wc - 1 - r)) : 0.f;
+                float cs[16];  // MOM: this row's w1 q over a 16-column half
+                float dm = 0.f;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint32_t off = tc::sw128_chunk(r, 4 * h + j);
-                    *reinterpret_cast<uint4*>(sQt + off) = scale_chunk(*reinterpret_cast<const uint4*>(sQ + off), w1);
+                    const uint4 qc = *reinterpret_cast<const uint4*>(sQ + off);
+                    *reinterpret_cast<uint4*>(sQt + off) = scale_chunk(qc, w1);
                     *reinterpret_cast<uint4*>(sKh + off) = scale_chunk(*reinterpret_cast<const uint4*>(sK + off), wh);
+                    if (MOM) {
+                        const uint32_t qw[4] = {qc.x, qc.y, qc.z, qc.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            cs[8 * (j & 1) + 2 * u] = w1 * bf_lo(qw[u]);
+                            cs[8 * (j & 1) + 2 * u + 1] = w1 * bf_hi(qw[u]);
+                        }
+                        if (j & 1) {
+                            const float t = warp_colsum16(cs, lane);
+                            if ((lane >> 4) == (j >> 1)) dm = t;  // lane l keeps column 32h + l
+                        }
+                    }
                 }
+                if (MOM) mw = gp[Wc] * mw + dm;
             }
             // ---- EPI2: P = g^(r+1) Q S0 + A~ K;  P~ -> smem, P -> out ---------------------------
             tc::mbar_wait(&bars[BP], ph, abort, status, 73);
@@ -1086,6 +1115,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             {
                 const float s1 = gp[r + 1];
                 const float w2 = r < Wc ? gp[2 * (Wc - 1 - r)] : 0.f;
+                float dy = 0.f;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     uint32_t qs[16], ak[16];
@@ -1095,6 +1125,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                     float pv[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) pv[j] = s1 * __uint_as_float(qs[j]) + __uint_as_float(ak[j]);
+                    if (MOM) {  // P~ column sums (P as stored: rounded to bf16 first, as the output pass reads it)
+                        float cs[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) cs[j] = w2 * __bfloat162float(__float2bfloat16(pv[j]));
+                        const float t = warp_colsum16(cs, lane);
+                        if ((lane >> 4) == half) dy = t;
+                    }
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const uint32_t off = tc::sw128_chunk(r, 4 * h + 2 * half + j);
@@ -1102,6 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         *reinterpret_cast<uint4*>(sQ + off) = pack8(&pv[8 * j], 1.f);  // rows >= Wc: not stored
                     }
                 }
+                if (MOM) yw = gp[2 * Wc] * yw + dy;
             }
             tc::fence_proxy_async();
             tc::fence_before_sync();
@@ -1135,7 +1173,17 @@ __global__ void __launch_bounds__(kThreads, 2)
             float* ds = a.ws + a.L.SB + si * kD * kD + (size_t)(r & 63) * kD + sc;
 #pragma unroll
             for (int j = 0; j < 16; ++j) ds[j] = ss[j];
-            if (h == 0 && r < 64) {
+            if (MOM) {  // the four lane quarters' moments, added in a fixed order
+                float* mom = reinterpret_cast<float*>(sm + sump::oMom);
+                mom[64 * q4 + 32 * h + lane] = mw;
+                mom[256 + 64 * q4 + 32 * h + lane] = yw;
+                tc::named_bar(5, 256);
+                if (q4 == 0) {
+                    const int c = 32 * h + lane;
+                    a.ws[a.L.mB + si * kD + c] = ((mom[c] + mom[64 + c]) + mom[128 + c]) + mom[192 + c];
+                    a.ws[a.L.yB + si * kD + c] = ((mom[256 + c] + mom[320 + c]) + mom[384 + c]) + mom[448 + c];
+                }
+            } else if (h == 0 && r < 64) {
                 a.ws[a.L.mB + si * kD + r] = 0.f;
                 a.ws[a.L.yB + si * kD + r] = 0.f;
             }
@@ -1206,7 +1254,10 @@ int launch_fwd_chunk_tc(const ChunkArgs& a, int mode, int* status, cudaStream_t 
         sm4.k = maps.k;
         sm4.v = maps.v;
         if (!make_map(&sm4.p, a.out, a.BH, a.n)) return -2;
-        auto kfn = a.unmasked ? fwd_sum_p_tc_kernel<true> : fwd_sum_p_tc_kernel<false>;
+        // masked with a final state or normalised: the segment moments come from this pass
+        auto kfn = a.unmasked ? fwd_sum_p_tc_kernel<true, false>
+                              : (a.want_final || a.normalize ? fwd_sum_p_tc_kernel<false, true>
+                                                             : fwd_sum_p_tc_kernel<false, false>);
         cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, sump::kSmemBytes);
         if (e != cudaSuccess) return -1;
         if (launch_pdl(kfn, dim3(a.nseg_launch, a.BH), dim3(kThreads), sump::kSmemBytes, st, sm4, a, status) !=
