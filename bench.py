@@ -482,7 +482,7 @@ def measure_normed(dev, dist: Dist, hbm_gbs: float, steps: int = 200, warmup: in
             hla.forward(q, k, v, gamma=gamma, chunk=chunk, normalize=True, eps=ww.eps, out=out)
 
         long = name == "normed_long"
-        ms = dist.max(_device_ms(one, steps // 4 if long else steps, warmup, torch.cuda.synchronize))
+        ms = dist.max(_device_ms(one, max(1, steps // 4) if long else steps, warmup, torch.cuda.synchronize))
         tokens = ww.B * ww.H * ww.n
         nbytes = tokens * (2 * ww.d + 2 * ww.dv) * 2
         achieved = nbytes / (ms * 1e-3) / 1e9
