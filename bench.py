@@ -49,7 +49,8 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the decode and training rows measured after the headline")
     ap.add_argument("--only", choices=("decode", "decode_compact", "decode_unmasked", "decode_mq", "train", "ahla",
-                                       "unmasked", "hla3", "prefill", "train_d64", "ahla_backward", "normed"),
+                                       "unmasked", "hla3", "prefill", "train_d64", "ahla_backward", "normed",
+                                       "prefill_d128"),
                     default=None,
                     help="measure only this row (for profiler captures; --steps/--warmup apply)")
     ap.add_argument("--decode-seqs", type=int, default=256,
@@ -455,6 +456,52 @@ def measure_ahla(dev, dist: Dist, hbm_gbs: float, bf16_tflops: float, steps: int
                          "step_tensor_frac": flops / (ms * 1e-3) / 1e12 / bf16_tflops}}
 
 
+def measure_prefill_d128(dev, dist: Dist, hbm_gbs: float, steps: int = 3, warmup: int = 1, n: int | None = None):
+    """Decode-workload prefill row: the 4096-token prefill that starts the streaming decode
+    (B=256 sequences x H=32, d=dv=128 bf16, decay 0.999, masked, unnormalised) with the state
+    after the last token, at chunk 128 on the first-order scans (33.5M tokens a call); the same
+    call on the mma.sync chunk kernels beside it (HLA2_KERNEL=mma).  HBM roofline of the whole
+    call over q, k, v read, out and the state written."""
+    import dataclasses
+    import os
+
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = inputs.WORKLOADS["decode_prefill"]
+    if n is not None:
+        w = dataclasses.replace(w, n=n)
+    x = inputs.make(w, device=dev, seed=replica_seed(w.seed, dist.rank))
+    q, k, v = x["q"], x["k"], x["v"]
+    gamma = x["gamma"].to(dev)
+    out = torch.empty_like(v)
+
+    def one():
+        hla.forward(q, k, v, gamma=gamma, chunk=128, out=out, return_final_state=True)
+
+    ms = dist.max(_device_ms(one, steps, warmup, torch.cuda.synchronize))
+    old = os.environ.get("HLA2_KERNEL")
+    os.environ["HLA2_KERNEL"] = "mma"
+    try:
+        legacy_ms = dist.max(_device_ms(one, max(1, steps - 1), 1, torch.cuda.synchronize))
+    finally:
+        if old is None:
+            os.environ.pop("HLA2_KERNEL", None)
+        else:
+            os.environ["HLA2_KERNEL"] = old
+    tokens = w.B * w.H * w.n
+    nbytes = tokens * (2 * w.d + 2 * w.dv) * 2 + w.B * w.H * hla.state_floats(w.d, w.dv) * 4
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"decode-workload prefill with the final state: B={w.B} H={w.H} n={w.n} d=dv={w.d} bf16, "
+                        f"decay {w.gamma[0]}, unnormalised, chunk 128",
+            "metric": "prefill tokens/s", "unit": "tokens/s", "value": dist.world * tokens / (ms * 1e-3),
+            "ms_per_step": ms, "steps": steps, "legacy_mma_ms": legacy_ms,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs, "kernel": "whole call", "algorithmic_bytes_per_step": nbytes}}
+
+
 def measure_normed(dev, dist: Dist, hbm_gbs: float, steps: int = 200, warmup: int = 10, n: int | None = None):
     """Ratio-normalised rows: the normalised workload (B=2 H=8 n=2048 d=dv=64 bf16, softplus
     q and k, unit-variance v, decay linspace(0.95, 0.999), eps 1e-6) at chunk 128, where the
@@ -666,6 +713,8 @@ def run_only(args, dist: Dist, dev):
         row = measure_ahla_backward(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
     elif args.only == "normed":
         row = measure_normed(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
+    elif args.only == "prefill_d128":
+        row = measure_prefill_d128(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
     elif args.only == "train_d64":
         row = measure_train(dev, dist, bf16_tflops, hbm_gbs, steps=args.steps, warmup=args.warmup, d=64)
     else:
@@ -805,6 +854,7 @@ def run_ours(args, dist: Dist):
                      "hla3": measure_hla3(dev, dist, hbm_gbs),
                      "prefill": measure_prefill(dev, dist, hbm_gbs)}
         secondary.update(measure_normed(dev, dist, hbm_gbs))
+        secondary["prefill_d128"] = measure_prefill_d128(dev, dist, hbm_gbs)
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

@@ -311,7 +311,7 @@ int forward_saving_for_backward(const void* q, const void* k, const void* v, voi
                                 const hla2_opts* opts);
 // Plain forward on the tcgen05 first-order scans (bf16, d = dv = 128, chunk >= 128, masked,
 // unnormalised, no state in or out): its workspace bytes (0: not this path), and the call.
-size_t fo_forward_ws(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize);
+size_t fo_forward_ws(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize, bool want_final);
 int fo_forward_call(const void* q, const void* k, const void* v, void* out, int B, int H, int n, const float* gamma,
                     cudaStream_t st, const hla2_opts* opts);
 Plan fo_plan(int B, int H, int n, int d, const DevInfo& di);
@@ -333,9 +333,9 @@ size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chun
     if (!W) return (size_t)-1;  // hla2_forward rejects these sizes (HLA2_ERR_UNSUPPORTED)
     const size_t ws = forward_ws(forward_plan(B, H, n, d, dv, W, dtype, normalize, want_final_state != 0, di),
                                  want_final_state != 0);
-    // masked calls without a state run on the first-order scans; the unmasked output and
-    // calls with init_state keep the chunk kernels (flags the query does not see): the larger
-    const size_t fo = want_final_state ? 0 : fo_forward_ws(B, H, n, d, dv, chunk, dtype, normalize);
+    // masked calls without init_state run on the first-order scans; the unmasked output and
+    // calls with init_state keep the chunk kernels (what the query does not see): the larger
+    const size_t fo = fo_forward_ws(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0);
     return fo > ws ? fo : ws;
 }
 
@@ -395,7 +395,7 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         return forward_saving_for_backward(q, k, v, out, B, H, n, d, dv, gamma, normalize, chunk, st, opts);
 
     const DevInfo di = dev_info();
-    if (!unmasked && !want_final && !opts->init_state && fo_forward_ws(B, H, n, d, dv, chunk, opts->dtype, normalize))
+    if (!unmasked && !opts->init_state && fo_forward_ws(B, H, n, d, dv, chunk, opts->dtype, normalize, want_final))
         return fo_forward_call(q, k, v, out, B, H, n, gamma, st, opts);  // (at the width asked for)
     {
         const int W = forward_width(opts->dtype, d, dv, chunk, normalize, di);
@@ -586,12 +586,13 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     const DevInfo di = dev_info();
     const int W = forward_width(dtype, d, dv, chunk, normalize, di);
     if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no forward kernel for d %d, dv %d at chunk <= %d", d, dv, chunk);
-    if (!want_final_state && fo_forward_ws(B, H, n, d, dv, chunk, dtype, normalize)) {
-        // first-order scans: S summaries, zero + scan, p pass, zero + scan, output pass
+    if (fo_forward_ws(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0)) {
+        // first-order scans: S summaries, zero + scan, p pass, zero + scan, output pass; with a
+        // final state also the (q, v) summaries, the moments, three scans and the final combine
         const Plan p = fo_plan(B, H, n, d, di);
         if (nseg) *nseg = p.nseg;
         if (seg_chunks) *seg_chunks = p.seg_chunks;
-        if (launches) *launches = p.nseg > 0 ? 7 : 0;
+        if (launches) *launches = p.nseg > 0 ? 7 + (want_final_state ? 3 + (p.nseg > 1 ? 3 : 0) : 0) : 0;
         return succeed();
     }
     chunk = W;
@@ -875,7 +876,11 @@ int fo_out(const FoArgs& a, int d, const void* x, const void* k, const void* v, 
 struct FoLayout {
     size_t SB, Sin, ZB, Zin, ZhB, Zhend, ShB, Shend;  // byte offsets, fp32 [BH][nseg][d][d]
     size_t P, dP, dqa;                                // byte offsets, bf16 [BH][n][d]
-    size_t fwd_total, total;                          // bytes kept by the forward; by the backward
+    // a forward with a final state (not with the backward's parts): C summaries [BH][nseg][d][d],
+    // m and y moments [BH][nseg][d], the carries of C, m, y into the last segment [BH][d][d],
+    // [BH][d] (contiguous, zeroed together)
+    size_t CB, mB, yB, Cl, ml, yl, carries_bytes;
+    size_t fwd_total, final_total, total;             // bytes kept by the forward; with a final state; by the backward
 };
 
 FoLayout fo_layout(const Plan& p) {
@@ -890,6 +895,18 @@ FoLayout fo_layout(const Plan& p) {
     L.Zin = o;   o = up(o + sum);
     L.P = o;     o = up(o + tok);
     L.fwd_total = o;
+    {
+        const size_t vec = (size_t)p.BH * p.nseg * p.d * sizeof(float);
+        size_t f = o;
+        L.CB = f;  f = up(f + sum);
+        L.mB = f;  f = up(f + vec);
+        L.yB = f;  f = up(f + vec);
+        L.Cl = f;  f += (size_t)p.BH * p.d * p.d * sizeof(float);
+        L.ml = f;  f += (size_t)p.BH * p.d * sizeof(float);
+        L.yl = f;  f += (size_t)p.BH * p.d * sizeof(float);
+        L.carries_bytes = f - L.Cl;
+        L.final_total = up(f);
+    }
     L.ZhB = o;   o = up(o + sum);
     L.Zhend = o; o = up(o + sum);
     L.ShB = o;   o = up(o + sum);
@@ -998,11 +1015,58 @@ int fo_reverse_part(const void* q, const void* k, const void* v, const void* dou
     return HLA2_OK;
 }
 
-size_t fo_forward_ws(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
+size_t fo_forward_ws(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize, bool want_final) {
     const DevInfo di = dev_info();
     if (d != 128 || !fo_path(dtype, d, dv, chunk, normalize, di)) return 0;  // d = 64: the stored-p kernels
     const Plan p = fo_plan(B, H, n, d, di);
-    return p.nseg > 0 ? fo_layout(p).fwd_total : 0;
+    if (p.nseg <= 0) return 0;
+    const FoLayout L = fo_layout(p);
+    return want_final ? L.final_total : L.fwd_total;
+}
+
+// The state after the last token from the first-order scans: the (q, v) summaries, the m and y
+// moments (y from the stored full p), the carries of C, m, y into the last segment, and the
+// last segment's combine with G = S C - Z and h = S m - y.
+int fo_final_state(const void* q, const void* v, const Plan& p, const float* gamma, char* ws, const FoLayout& L,
+                   float* final_state, cudaStream_t st) {
+    auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+    const size_t E = (size_t)p.d * p.d;
+    const int seg_tokens = p.seg_chunks * p.W;
+    FoArgs a = fo_args(p, gamma, ws);
+    a.pow = 1;
+    a.summary = f(L.CB);
+    if (fo_summary(a, p.d, q, v, false, st)) return cuda_fail("query-value summaries");
+    if (launch_fo_moments(q, ws + L.P, f(L.mB), f(L.yB), p.BH, p.H, p.n, p.d, p.nseg, seg_tokens, gamma, st))
+        return cuda_fail("segment moments");
+    if (cudaMemsetAsync(ws + L.Cl, 0, L.carries_bytes, st) != cudaSuccess) return cuda_fail("carry reset");
+    if (p.nseg > 1 &&
+        (launch_linear_scan(f(L.CB), f(L.Cl), p.BH, p.H, p.nseg - 1, E, p.nseg * E, E, false, gamma, seg_tokens, 1,
+                            st) ||
+         launch_linear_scan(f(L.mB), f(L.ml), p.BH, p.H, p.nseg - 1, p.d, p.nseg * (size_t)p.d, p.d, false, gamma,
+                            seg_tokens, 1, st) ||
+         launch_linear_scan(f(L.yB), f(L.yl), p.BH, p.H, p.nseg - 1, p.d, p.nseg * (size_t)p.d, p.d, false, gamma,
+                            seg_tokens, 2, st)))
+        return cuda_fail("last-segment carries");
+    FoFinal fin{};
+    fin.SB = f(L.SB);
+    fin.Sin = f(L.Sin);
+    fin.ZB = f(L.ZB);
+    fin.Zin = f(L.Zin);
+    fin.CB = f(L.CB);
+    fin.Cl = f(L.Cl);
+    fin.ml = f(L.ml);
+    fin.yl = f(L.yl);
+    fin.mB = f(L.mB);
+    fin.yB = f(L.yB);
+    fin.BH = p.BH;
+    fin.H = p.H;
+    fin.n = p.n;
+    fin.d = p.d;
+    fin.nseg = p.nseg;
+    fin.seg_tokens = seg_tokens;
+    fin.gamma = gamma;
+    if (launch_fo_final_state(fin, final_state, st)) return cuda_fail("final state");
+    return HLA2_OK;
 }
 
 int fo_forward_call(const void* q, const void* k, const void* v, void* out, int B, int H, int n, const float* gamma,
@@ -1010,8 +1074,10 @@ int fo_forward_call(const void* q, const void* k, const void* v, void* out, int 
     const DevInfo di = dev_info();
     const Plan p = fo_plan(B, H, n, 128, di);
     const FoLayout L = fo_layout(p);
-    if (!opts->workspace || opts->workspace_bytes < L.fwd_total)
-        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", L.fwd_total,
+    const bool want_final = opts->final_state != nullptr;
+    const size_t need = want_final ? L.final_total : L.fwd_total;
+    if (!opts->workspace || opts->workspace_bytes < need)
+        return fail(HLA2_ERR_WORKSPACE, "workspace of %zu bytes required (got %zu)", need,
                     opts->workspace ? opts->workspace_bytes : (size_t)0);
     if (!aligned16(opts->workspace)) return fail(HLA2_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
     char* ws = static_cast<char*>(opts->workspace);
@@ -1026,6 +1092,7 @@ int fo_forward_call(const void* q, const void* k, const void* v, void* out, int 
     mark(3);
     if (rc == HLA2_OK) rc = fo_output_pass(q, v, out, p, gamma, ws, L, st);
     mark(4);
+    if (rc == HLA2_OK && want_final) rc = fo_final_state(q, v, p, gamma, ws, L, opts->final_state, st);
     mark(5);
     return rc == HLA2_OK ? succeed() : rc;
 }

@@ -278,6 +278,22 @@ int launch_fo_tc_summary(const FoArgs& a, const void* k, const void* v, bool rev
 // add != NULL adds that partial.
 int launch_fo_tc_out(const FoArgs& a, const void* x, const void* k, const void* v, bool r2, int next_sum,
                      const void* xv, const void* add, void* out, bool reverse, cudaStream_t st);
+// Final state of the first-order-scan forward (d = dv = 64 or 128).  Per segment s of head bh:
+//   mB[bh][s] = sum_t g^(L-1-t) q_t,  yB[bh][s] = sum_t g^(2(L-1-t)) p_t  (p the full p),
+// t the token's place in the segment of L tokens (seg_tokens, the last one shorter).
+int launch_fo_moments(const void* q, const void* p, float* mB, float* yB, int BH, int H, int n, int d, int nseg,
+                      int seg_tokens, const float* gamma, cudaStream_t st);
+struct FoFinal {
+    const float *SB, *Sin, *ZB, *Zin, *CB;  // [BH][nseg][d][d]: summaries and carries (S, Z); C summaries
+    const float *Cl, *ml, *yl;              // [BH][d][d], [BH][d]: carries of C, m, y into the last segment
+    const float *mB, *yB;                   // [BH][nseg][d]
+    int BH, H, n, d, nseg, seg_tokens;
+    const float* gamma;
+};
+// The carry into the last segment combined with its summaries (rho = g^L, L its tokens),
+//   S = rho S_in + S_B, C = rho C_in + C_B, m = rho m_in + m_B, Z = rho^2 Z_in + Z_B,
+//   y = rho^2 y_in + y_B, written as the packed state (S, C, G = S C - Z, m, h = S m - y).
+int launch_fo_final_state(const FoFinal& f, float* final_state, cudaStream_t st);
 // The same two launches for d = dv = 64 (fo64_tc.cu; [BH][nseg][64*64] summaries and carries).
 size_t fo64_tc_max_smem();
 int launch_fo64_tc_summary(const FoArgs& a, const void* k, const void* v, bool reverse, cudaStream_t st);

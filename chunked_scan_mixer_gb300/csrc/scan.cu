@@ -355,6 +355,114 @@ __global__ void __launch_bounds__(kThreads) final_combine64_kernel(const ChunkAr
     }
 }
 
+// Segment moments of the first-order-scan forward: one CTA per (segment, head, 32 features);
+// thread (row, j) sums features 32 z + 8j .. +7 over tokens row, row + 64, ... of the segment,
+// then the 64 row partials are added in a fixed order.
+template <int D>
+__global__ void __launch_bounds__(kThreads) fo_moments_kernel(const bf16* __restrict__ q, const bf16* __restrict__ p,
+                                                              float* mB, float* yB, int H, int n, int nseg,
+                                                              int seg_tokens, const float* gamma) {
+    constexpr int HALF = 32, ROWS = kThreads / 4;
+    __shared__ float red_m[ROWS][HALF + 1], red_y[ROWS][HALF + 1];
+    pdl_trigger();
+    pdl_wait();
+    const int s = blockIdx.x, bh = blockIdx.y, z = blockIdx.z, tid = threadIdx.x;
+    const int row = tid / 4, j = tid % 4;
+    const int t0 = s * seg_tokens, t1 = min(t0 + seg_tokens, n);
+    const float log2g = log2f(head_decay(gamma, bh, H));
+    const int f0 = HALF * z + 8 * j;
+    const bf16* qh = q + (size_t)bh * n * D + f0;
+    const bf16* ph = p + (size_t)bh * n * D + f0;
+    float am[8], ay[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) am[u] = ay[u] = 0.f;
+    for (int t = t0 + row; t < t1; t += ROWS) {
+        const uint4 qv = *reinterpret_cast<const uint4*>(qh + (size_t)t * D);
+        const uint4 pv = *reinterpret_cast<const uint4*>(ph + (size_t)t * D);
+        const float w = pow_decay(log2g, (float)(t1 - 1 - t)), w2 = w * w;
+        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            am[2 * e] += w * __uint_as_float(qw[e] << 16);
+            am[2 * e + 1] += w * __uint_as_float(qw[e] & 0xFFFF0000u);
+            ay[2 * e] += w2 * __uint_as_float(pw[e] << 16);
+            ay[2 * e + 1] += w2 * __uint_as_float(pw[e] & 0xFFFF0000u);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        red_m[row][8 * j + u] = am[u];
+        red_y[row][8 * j + u] = ay[u];
+    }
+    __syncthreads();
+    if (tid < 2 * HALF) {
+        const int f = tid % HALF;
+        float (*red)[HALF + 1] = tid < HALF ? red_m : red_y;
+        float acc = 0.f;
+        for (int r = 0; r < ROWS; ++r) acc += red[r][f];
+        (tid < HALF ? mB : yB)[((size_t)bh * nseg + s) * D + HALF * z + f] = acc;
+    }
+}
+
+// Final state of the first-order-scan forward: CTA (rb, bh) forms rows 16 rb .. 16 rb + 15 of
+// every part from shared-memory copies of the combined C (all of it), its 16 rows of S, and m;
+// thread (r, c) forms row r and columns D/16 * c .. of G.
+template <int D>
+__global__ void __launch_bounds__(kThreads) fo_final_state_kernel(const FoFinal f, float* final_state) {
+    constexpr int RB = 16, CPT = D / 16;
+    extern __shared__ __align__(16) float fsm[];
+    float* Cs = fsm;             // [D][D]
+    float* Ss = Cs + D * D;      // [RB][D]
+    float* ms = Ss + RB * D;     // [D]
+    float* ys = ms + D;          // [RB]
+    pdl_trigger();
+    pdl_wait();
+    const int rb = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+    const int r0 = RB * rb, last = f.nseg - 1;
+    const int L = f.n - last * f.seg_tokens;
+    const float rho = pow_decay(log2f(head_decay(f.gamma, bh, f.H)), (float)L), rho2 = rho * rho;
+    const size_t si = (size_t)bh * f.nseg + last, DD = (size_t)D * D;
+    const float *SB = f.SB + si * DD, *Sin = f.Sin + si * DD, *ZB = f.ZB + si * DD, *Zin = f.Zin + si * DD;
+    const float *CB = f.CB + si * DD, *Cl = f.Cl + (size_t)bh * DD;
+    const float *mB = f.mB + si * D, *yB = f.yB + si * D, *ml = f.ml + (size_t)bh * D, *yl = f.yl + (size_t)bh * D;
+    float* o = final_state + (size_t)bh * raw_state_floats(D, D);
+    const PackOff po = pack_off(D, D);
+    for (int i = tid; i < (int)DD; i += kThreads) {
+        Cs[i] = rho * Cl[i] + CB[i];
+        if (i >= r0 * D && i < (r0 + RB) * D) o[po.C + i] = Cs[i];
+    }
+    for (int i = tid; i < RB * D; i += kThreads) {
+        const size_t e = (size_t)r0 * D + i;
+        Ss[i] = rho * Sin[e] + SB[e];
+        o[po.S + e] = Ss[i];
+    }
+    for (int i = tid; i < D; i += kThreads) {
+        ms[i] = rho * ml[i] + mB[i];
+        if (i >= r0 && i < r0 + RB) o[po.m + i] = ms[i];
+    }
+    for (int i = tid; i < RB; i += kThreads) ys[i] = rho2 * yl[r0 + i] + yB[r0 + i];
+    __syncthreads();
+    const int r = tid / 16, c0 = (tid % 16) * CPT;
+    float acc[CPT];
+#pragma unroll
+    for (int u = 0; u < CPT; ++u) acc[u] = 0.f;
+    for (int x = 0; x < D; ++x) {
+        const float a = Ss[r * D + x];
+#pragma unroll
+        for (int u = 0; u < CPT; ++u) acc[u] += a * Cs[x * D + c0 + u];
+    }
+#pragma unroll
+    for (int u = 0; u < CPT; ++u) {
+        const size_t e = (size_t)(r0 + r) * D + c0 + u;
+        o[po.G + e] = acc[u] - (rho2 * Zin[e] + ZB[e]);
+    }
+    if (tid < RB) {  // h = S m - y
+        float t = 0.f;
+        for (int x = 0; x < D; ++x) t += Ss[tid * D + x] * ms[x];
+        o[po.h + r0 + tid] = t - ys[tid];
+    }
+}
+
 // Raw final (S, C, m, Z, y) -> packed public state (S, C, G = S C - Z, m, h = S m - y).
 __global__ void __launch_bounds__(kThreads)
     finalize_kernel(const ChunkArgs a, int D, int DV, float* final_state) {
@@ -448,6 +556,37 @@ int launch_seg_moments64(const ChunkArgs& a, cudaStream_t st) {
     if (a.nsum <= 0 || a.BH <= 0) return 0;  // the summaries kept: every segment but the last, or all
     if (launch_pdl(seg_moments64_kernel, dim3(a.nsum, a.BH, 2), dim3(kThreads), 0, st, a) != cudaSuccess) return -1;
     return finish_launch();
+}
+
+int launch_fo_moments(const void* q, const void* p, float* mB, float* yB, int BH, int H, int n, int d, int nseg,
+                      int seg_tokens, const float* gamma, cudaStream_t st) {
+    if (nseg <= 0 || BH <= 0) return 0;
+    const dim3 grid(nseg, BH, d / 32);
+    const bf16 *qq = static_cast<const bf16*>(q), *pp = static_cast<const bf16*>(p);
+    cudaError_t e = d == 64 ? launch_pdl(fo_moments_kernel<64>, grid, dim3(kThreads), 0, st, qq, pp, mB, yB, H, n, nseg,
+                                         seg_tokens, gamma)
+                  : d == 128 ? launch_pdl(fo_moments_kernel<128>, grid, dim3(kThreads), 0, st, qq, pp, mB, yB, H, n,
+                                          nseg, seg_tokens, gamma)
+                             : cudaErrorInvalidValue;
+    return e == cudaSuccess ? finish_launch() : -1;
+}
+
+int launch_fo_final_state(const FoFinal& f, float* final_state, cudaStream_t st) {
+    if (f.nseg <= 0 || f.BH <= 0) return 0;
+    const size_t smem = ((size_t)f.d * f.d + 16 * (size_t)f.d + f.d + 16) * sizeof(float);
+    cudaError_t e;
+    if (f.d == 128) {
+        e = cudaFuncSetAttribute(fo_final_state_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = launch_pdl(fo_final_state_kernel<128>, dim3(f.d / 16, f.BH), dim3(kThreads), smem, st, f, final_state);
+    } else if (f.d == 64) {
+        e = cudaFuncSetAttribute(fo_final_state_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = launch_pdl(fo_final_state_kernel<64>, dim3(f.d / 16, f.BH), dim3(kThreads), smem, st, f, final_state);
+    } else {
+        e = cudaErrorInvalidValue;
+    }
+    return e == cudaSuccess ? finish_launch() : -1;
 }
 
 int launch_final_combine64(const ChunkArgs& a, float* final_state, cudaStream_t st) {

@@ -144,6 +144,8 @@ size_t hla2_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chun
  * its carry-in; every token's output is then formed from its inclusive state.
  * normalize != 0 divides by the masked denominator (+ opts->eps); on the tcgen05 path (bf16,
  * d = dv = 64, chunk 128, masked) the denominator is formed in the output pass's epilogue.
+ * bf16 at d = dv = 128, chunk 128, masked and unnormalised without init_state runs on the
+ * tcgen05 first-order scans, with or without final_state.
  * opts must be non-NULL (dtype and workspace).  init_state continues a previous
  * sequence; final_state receives the state after the last token (prefill for
  * hla2_decode_step).  opts->flags may hold HLA2_FLAG_SAVE_FOR_BACKWARD or

@@ -1,6 +1,6 @@
 """The bf16 training path (d = dv = 128 and 64) on the tcgen05 first-order scan kernels (chunk
-128), and the plain d = 128 forward on the same passes, through the C ABI, against the float64
-oracle.
+128), and the d = 128 forward (plain, or with the final state) on the same passes, through the
+C ABI, against the float64 oracle.
 
 The masked output is two chained first-order scans (p = S q, then o = q^T Z) and its reverse
 mode six more; every pass runs segment-parallel on the same kernel.  Bar: max|gpu - oracle| /
@@ -154,6 +154,54 @@ def test_forward_distinct_from_the_legacy_path():
     ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), _gamma_np(x))
     assert rel_err(np64(tc.cpu()), ref) <= 2e-2 and rel_err(np64(legacy.cpu()), ref) <= 2e-2
     assert not torch.equal(tc, legacy)
+
+
+@pytest.mark.parametrize("B, H, n", [(1, 2, 1000), (2, 3, 129), (1, 1, 1), (1, 4, 3000), (2, 64, 700)])
+@pytest.mark.parametrize("gamma", [None, (0.9, 0.999)])
+def test_forward_final_state_matches_oracle(B, H, n, gamma):
+    """The d = 128 forward with the state after the last token, on the first-order scans: the
+    (q, v) summaries, the m and y moments (y from the stored full p), the carries into the last
+    segment, and its combine.  Every part (S, C, m, G, h) and the output against the oracle, on
+    one and many segments per head (B H = 128: one each), ragged tails, one token."""
+    x = inputs.make_custom(B, H, n, D, D, torch.bfloat16, seed=11 * n + H, gamma=gamma)
+    g = None if x["gamma"] is None else x["gamma"].cuda()
+    o, fin = hla.forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), gamma=g, chunk=128, return_final_state=True)
+    hla.check_status()
+    ref, ref_state = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), _gamma_np(x), return_state=True)
+    assert rel_err(np64(o.cpu()), ref) <= 2e-2
+    from oracle import hla2_oracle as O
+    got, want = O.unpack_state(np64(fin.cpu()), D, D), O.unpack_state(ref_state, D, D)
+    for key in ("S", "C", "m", "G", "h"):
+        assert rel_err(got[key], want[key]) <= 2e-2, key
+    nseg, seg_chunks, launches = hla.forward_plan(B, H, n, D, D, 128, want_final_state=True)
+    assert launches == 10 + (3 if nseg > 1 else 0)
+
+
+def test_final_state_then_decode_and_distinct_from_the_legacy_path():
+    """A d = 128 prefill on the first-order scans, then decode steps from its state, against the
+    oracle over the whole sequence; the same prefill on the mma.sync kernels meets the bar with
+    other bits."""
+    B, H, n, steps = 2, 4, 128 * 12 + 37, 3
+    x = inputs.make_custom(B, H, n + steps, D, D, torch.bfloat16, seed=61, gamma=(0.99, 0.9995))
+    g = x["gamma"].cuda()
+    part = lambda lo, hi: [x[t][:, :, lo:hi].contiguous().cuda() for t in ("q", "k", "v")]
+    o, fin = hla.forward(*part(0, n), gamma=g, chunk=128, return_final_state=True)
+    old = os.environ.get("HLA2_KERNEL")
+    os.environ["HLA2_KERNEL"] = "mma"
+    try:
+        o2, fin2 = hla.forward(*part(0, n), gamma=g, chunk=128, return_final_state=True)
+    finally:
+        if old is None:
+            os.environ.pop("HLA2_KERNEL", None)
+        else:
+            os.environ["HLA2_KERNEL"] = old
+    assert not torch.equal(fin, fin2)
+    ref = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), _gamma_np(x))
+    assert rel_err(np64(o.cpu()), ref[:, :, :n]) <= 2e-2 and rel_err(np64(o2.cpu()), ref[:, :, :n]) <= 2e-2
+    for t in range(n, n + steps):
+        q, k, v = part(t, t + 1)
+        y = hla.decode_step(fin, q[:, :, 0], k[:, :, 0], v[:, :, 0], gamma=g)
+        assert rel_err(np64(y.cpu()), ref[:, :, t]) <= 2e-2, t
 
 
 def test_d64_training_shapes_all_heads():
