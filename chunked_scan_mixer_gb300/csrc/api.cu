@@ -1955,7 +1955,13 @@ static int ahla_pass(const AhlaArgs& a, int d, int chunk, bool summary, cudaStre
 size_t hla2_ahla_forward_workspace_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype, int normalize) {
     if (ahla_check(B, H, n, d, dv, chunk, dtype, normalize) != HLA2_OK) return (size_t)-1;
     const Plan p = ahla_plan(B, H, n, d, chunk);
-    return p.nseg > 0 ? ahla_layout(p).total * sizeof(float) : 0;
+    size_t bytes = p.nseg > 0 ? ahla_layout(p).total * sizeof(float) : 0;
+    if (chunk == 128) {  // a call with a final state (which the query does not see) runs at width 64
+        const Plan p64 = ahla_plan(B, H, n, d, 64);
+        const size_t b64 = p64.nseg > 0 ? ahla_layout(p64).total * sizeof(float) : 0;
+        bytes = b64 > bytes ? b64 : bytes;
+    }
+    return bytes;
 }
 
 int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int n, int d, int dv,
@@ -1969,8 +1975,9 @@ int hla2_ahla_forward(const void* q, const void* k, const void* v, void* out, in
     const bool want_final = opts->final_state != nullptr;
     if (opts->init_state && !aligned16(opts->init_state))
         return fail(HLA2_ERR_INVALID_ARG, "init_state must be 16-byte aligned");
-    if (want_final && chunk == 128)
-        return fail(HLA2_ERR_UNSUPPORTED, "the AHLA final state comes from the chunk 32 / 64 kernels");
+    // the tcgen05 kernel keeps no final state: such calls run at width 64 (the result does not
+    // depend on the width; the workspace query covers both widths)
+    if (want_final && chunk == 128) chunk = 64;
     if (want_final && !aligned16(opts->final_state))
         return fail(HLA2_ERR_INVALID_ARG, "final_state must be 16-byte aligned");
     const long BH = (long)B * H;

@@ -390,7 +390,8 @@ def ahla_forward(q, k, v, gamma=None, normalize=False, chunk=64, eps=1e-6, out=N
     """Asymmetric HLA forward (the masked left-cascaded product Q (K^T Q)(K^T V)).
     bf16 q, k, v [B,H,n,d] on the GPU (d == dv); chunk 32 or 64 (or 128 at d = 64,
     unnormalised).  Returns out [B,H,n,d] (and, with return_final_state, the state
-    [B,H,ahla_state_floats] = P | E | m | n after the last token; chunk 32 / 64).
+    [B,H,ahla_state_floats] = P | E | m | n after the last token; a chunk-128 call with a final
+    state runs at width 64).
     init_state: a state in that layout to continue from."""
     L = lib()
     if q.device.type != "cuda" or q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype:

@@ -327,9 +327,10 @@ int hla2_decode_step_mq(float* key_state, float* head_state, const void* q, cons
  * exclusive scan of segment summaries (P, E, m, n, R = sum k q^T) (section summary §6.2).
  * bf16 q, k, v, out [B, H, n, d], d == dv in {16, 32, 64, 128}, chunk 32 or 64 (legacy
  * tensor cores), or chunk 128 for d = dv = 64 unnormalised (tcgen05).
- * opts->final_state (chunk 32 / 64 only) receives the AHLA state after token n, [B, H]
- * blocks of hla2_ahla_state_floats = [P d*dv | E d*dv | m d | n d]; opts->init_state (any
- * chunk) in the same layout continues from that state; opts->flags must be 0.
+ * opts->final_state receives the AHLA state after token n, [B, H] blocks of
+ * hla2_ahla_state_floats = [P d*dv | E d*dv | m d | n d] (a call at chunk 128 with a final
+ * state runs at width 64: the tcgen05 kernel keeps none); opts->init_state (any chunk) in the
+ * same layout continues from that state; opts->flags must be 0.
  * Workspace as for hla2_forward; a timed-out device-side wait of the tcgen05 kernel is
  * reported by hla2_workspace_status.
  */
