@@ -203,7 +203,9 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                 if (R2) tc::mbar_wait(fv(j), (j >> 1) & 1, abort, status, 133);
                 tc::fence_after_sync();
             };
-            auto finish = [&](int j) {
+            // after EPI-Y(j): the tile store and the next summary's products (finish_store), then,
+            // once the next Gram is issued, the late loads and the stage freed (finish_release)
+            auto finish_store = [&](int j) {
                 tc::mbar_wait(&bars[f64::BYT], j & 1, abort, status, 138);
                 tc::fence_after_sync();
                 tc::tma_store_3d(&maps.out, sm + Lay::oST, 0, chunk_of(j) * kW, bh);
@@ -213,14 +215,20 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                     for (int ks = 0; ks < 8; ++ks)
                         tc::mma_ss(tmem + C::TN, mdesc(sST, ks), mdesc(sXV, ks), I_S, (j > 0 || ks > 0) ? 1u : 0u);
                     tc::mma_commit(&bars[f64::BN]);
-                    tc::mbar_wait(&bars[f64::BN], j & 1, abort, status, 139);
                 }
+            };
+            auto finish_release = [&](int j) {
+                if (NSUM) tc::mbar_wait(&bars[f64::BN], j & 1, abort, status, 139);
                 if (v_late && j + 2 < nit && kVTiles > 0) {  // slot j % 2 of the value group is free
                     load_v(j + 2);
                     ++lv;
                 }
                 tc::bulk_wait_read_all();
                 tc::mbar_arrive(&bars[f64::BSF]);
+            };
+            auto finish = [&](int j) {
+                finish_store(j);
+                finish_release(j);
             };
 
             // prologue: chunks 0 and 1 in flight
@@ -260,11 +268,14 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                     for (int ks = 0; ks < 8; ++ks) tc::mma_ss(tmem + C::TS, mdesc(sKt2, ks), mdesc(sK, ks), I_S, 1);
                 tc::mma_commit(&bars[f64::BSU]);
                 if (kTwoG) {
-                    if (j > 0) finish(j - 1);  // also frees G / Y region (j + 1) % 2
+                    // EPI-Y(j - 1) has read G / Y region (j + 1) % 2: the next Gram goes before the
+                    // wait for the previous tile store to leave the stage
+                    if (j > 0) finish_store(j - 1);
                     if (j + 1 < nit) {
                         wait_g_inputs(j + 1);
                         mma_g(j + 1);
                     }
+                    if (j > 0) finish_release(j - 1);
                     tc::mbar_wait(&bars[f64::BSU], j & 1, abort, status, 137);  // chunk j's products done
                 } else {
                     finish(j);  // after EPI-Y(j): chunk j's products are done

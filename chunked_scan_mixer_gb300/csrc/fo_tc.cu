@@ -243,8 +243,10 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                 if (R2) tc::mbar_wait(&bars[la::FV], j & 1, abort, status, 103);
                 tc::fence_after_sync();
             };
-            // after EPI-Y(j): the tile store, the next summary, late loads, the stage freed
-            auto finish = [&](int j) {
+            // after EPI-Y(j): the tile store and the next summary's products (finish_store); then
+            // the late loads and the stage freed (finish_release), which the two-region order
+            // runs after the next Gram is issued
+            auto finish_store = [&](int j) {
                 tc::mbar_wait(&bars[la::BYT], j & 1, abort, status, 108);
                 tc::fence_after_sync();
                 const int c = chunk_of(j);
@@ -255,8 +257,10 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                     for (int ks = 0; ks < 8; ++ks)
                         tc::mma_ss(tmem + C::TN, mdesc(sST, ks), mdesc(sXV, ks), I_MM, (j > 0 || ks > 0) ? 1u : 0u);
                     tc::mma_commit(&bars[la::BN]);
-                    tc::mbar_wait(&bars[la::BN], j & 1, abort, status, 109);
                 }
+            };
+            auto finish_release = [&](int j) {
+                if (NSUM) tc::mbar_wait(&bars[la::BN], j & 1, abort, status, 109);
                 if (v_late && j + 1 < nit && kVTiles > 0) {
                     load_v(j + 1);
                     ++lv;
@@ -267,6 +271,10 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                     ++lx;
                 }
                 tc::mbar_arrive(&bars[la::BSF]);
+            };
+            auto finish = [&](int j) {
+                finish_store(j);
+                finish_release(j);
             };
 
             load_x(0);
@@ -309,11 +317,14 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                         tc::mma_ss(tmem + C::TS, mdesc(sKt2, ks), mdesc(sK, ks), I_MM, 1);
                 tc::mma_commit(&bars[la::BSU]);
                 if (kTwoG) {
-                    if (j > 0) finish(j - 1);  // also frees G / Y region (j+1) % 2
+                    // EPI-Y(j - 1) has read G / Y region (j + 1) % 2: the next Gram goes before the
+                    // wait for the previous tile store to leave the stage
+                    if (j > 0) finish_store(j - 1);
                     if (j + 1 < nit) {
                         wait_g_inputs(j + 1);
                         mma_g(j + 1);
                     }
+                    if (j > 0) finish_release(j - 1);
                     tc::mbar_wait(&bars[la::BSU], j & 1, abort, status, 107);  // chunk j's products done
                     if (j + 2 < nit) {
                         load_k(j + 2);
