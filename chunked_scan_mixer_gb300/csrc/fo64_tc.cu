@@ -247,9 +247,13 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
             for (int j = 0; j < nit; ++j) {
                 tc::mbar_wait(&bars[f64::BGT], j & 1, abort, status, 134);  // G read; G~, fX, K~ written
                 if (j > 0) tc::mbar_wait(&bars[f64::BS], (j - 1) & 1, abort, status, 136);  // Sig0 of chunk j
-                if (j + 2 < nit) {  // X slot j % 2 is free
+                if (j + 2 < nit) {  // X slot j % 2 is free (and key slot j % 2, unless MMA-Y reads it)
                     load_x(j + 2);
                     ++lx;
+                    if (!R2 && !KVS) {
+                        load_k(j + 2);
+                        ++lk;
+                    }
                 }
                 if (!KVS) tc::mbar_wait(fv(j), (j >> 1) & 1, abort, status, 135);
                 tc::fence_after_sync();
@@ -281,8 +285,10 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                     finish(j);  // after EPI-Y(j): chunk j's products are done
                 }
                 if (j + 2 < nit) {  // key slot j % 2 is free (and the value slot, without late reads)
-                    load_k(j + 2);
-                    ++lk;
+                    if (R2 || KVS) {  // MMA-Y reads the raw keys (the swapped pair, or keys as values)
+                        load_k(j + 2);
+                        ++lk;
+                    }
                     if (!v_late && !KVS) {
                         load_v(j + 2);
                         ++lv;

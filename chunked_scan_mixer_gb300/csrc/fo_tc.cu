@@ -298,6 +298,10 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                     load_x(j + 1);
                     ++lx;
                 }
+                if (!R2 && !KVS && j + 2 < nit) {  // key slot j % 2 no longer read (unless MMA-Y reads it:
+                    load_k(j + 2);                    // the swapped pair, or keys as values)
+                    ++lk;
+                }
                 if (!KVS) tc::mbar_wait(&bars[la::FV], j & 1, abort, status, 105);  // the value tile
                 tc::fence_after_sync();
                 const uint32_t sK = smem_u32(sm + Lay::key(j)), sVj = smem_u32(sm + Lay::val(j));
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                     }
                     if (j > 0) finish_release(j - 1);
                     tc::mbar_wait(&bars[la::BSU], j & 1, abort, status, 107);  // chunk j's products done
-                    if (j + 2 < nit) {
+                    if ((R2 || KVS) && j + 2 < nit) {
                         load_k(j + 2);
                         ++lk;
                     }
@@ -336,7 +340,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                     }
                 } else {
                     finish(j);  // after EPI-Y(j), so chunk j's products are done
-                    if (j + 2 < nit) {
+                    if ((R2 || KVS) && j + 2 < nit) {
                         load_k(j + 2);
                         ++lk;
                     }
