@@ -31,11 +31,15 @@ namespace f64 {
 
 constexpr int kW = 128, kD = 64;
 constexpr int kThreads = 288;
+// the output kernel: warp 0 issues the MMAs (and, except in the two-operand-slot order, the tile
+// loads and stores), warps 1..8 are the epilogue, warp 9 issues the loads and stores in that order
+constexpr int kThreadsOut = 320, kLoadWarp = 9;
 constexpr uint32_t kTile = 128 * 128;  // a [128][64] bf16 tile: one SW128 block (16 KB)
 constexpr uint32_t kSig = 64 * 128;    // the [64][64] bf16 state (8 KB)
 constexpr uint32_t kTmemCols = 512;
 
-template <bool R2, bool KVS, bool XVS, bool ADD>
+// TWOA: the scaled keys K~ and the bf16 state Sig0 have two slots as well (by chunk parity).
+template <bool R2, bool KVS, bool XVS, bool ADD, bool TWOA = false>
 struct OutLayout {
     static constexpr uint32_t oX = 0;                                   // 2 slots
     static constexpr uint32_t oK = oX + 2 * kTile;                      // 2 slots
@@ -43,36 +47,46 @@ struct OutLayout {
     static constexpr uint32_t oE0 = (KVS ? oK : oV) + 2 * kTile;
     static constexpr uint32_t oXV = XVS ? oE0 : oV;                     // 2 slots
     static constexpr uint32_t oAD = XVS ? oXV + 2 * kTile : oE0;        // 2 slots
-    static constexpr uint32_t oKt = ADD ? oAD + 2 * kTile : oAD;        // K~ (and V~ for R2)
+    static constexpr uint32_t oKt = ADD ? oAD + 2 * kTile : oAD;        // K~ (TWOA: 2 slots; V~ next for R2)
     static constexpr uint32_t oKt2 = oKt + kTile;
-    static constexpr uint32_t oST = (R2 ? oKt2 : oKt) + kTile;          // output tile
-    static constexpr uint32_t oS0 = oST + kTile;                        // bf16 Sig0
-    static constexpr uint32_t oGP = oS0 + kSig;                         // g^0 .. g^(2W)
+    static constexpr uint32_t oST = R2 ? oKt2 + kTile : oKt + (TWOA ? 2 : 1) * kTile;  // output tile
+    static constexpr bool kTwoST = TWOA && !ADD;                        // (2 slots where they fit)
+    static constexpr uint32_t oS0 = oST + (kTwoST ? 2 : 1) * kTile;     // bf16 Sig0 (TWOA: 2 slots)
+    static constexpr uint32_t oGP = oS0 + (TWOA ? 2 : 1) * kSig;        // g^0 .. g^(2W)
     static constexpr uint32_t oBar = oGP + 1088;
-    static constexpr uint32_t oMisc = oBar + 16 * 8;
+    static constexpr uint32_t oMisc = oBar + 24 * 8;
     static constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
     __host__ __device__ static constexpr uint32_t x(int j) { return oX + (uint32_t)(j & 1) * kTile; }
     __host__ __device__ static constexpr uint32_t key(int j) { return oK + (uint32_t)(j & 1) * kTile; }
     __host__ __device__ static constexpr uint32_t val(int j) { return KVS ? key(j) : oV + (uint32_t)(j & 1) * kTile; }
     __host__ __device__ static constexpr uint32_t xv(int j) { return XVS ? oXV + (uint32_t)(j & 1) * kTile : val(j); }
     __host__ __device__ static constexpr uint32_t ad(int j) { return oAD + (uint32_t)(j & 1) * kTile; }
+    __host__ __device__ static constexpr uint32_t kt(int j) { return oKt + (TWOA ? (uint32_t)(j & 1) * kTile : 0u); }
+    __host__ __device__ static constexpr uint32_t s0(int j) { return oS0 + (TWOA ? (uint32_t)(j & 1) * kSig : 0u); }
+    __host__ __device__ static constexpr uint32_t st(int j) { return oST + (kTwoST ? (uint32_t)(j & 1) * kTile : 0u); }
 };
 
-// Tensor-memory columns.  One pair: G / Y of chunk j in [0,128) or [128,256) (Y: the first 64);
-// A operands [256,352) (G~ 64 | fX 32); dSig [384,448); next summary [448,512).  Swapped pair:
+// Tensor-memory columns.  One pair with a next summary: G / Y of chunk j in [0,128) or
+// [128,256) (Y: the first 64); A operands [256,352) (G~ 64 | fX 32); dSig [384,448); next
+// summary [448,512).  One pair without (kTwoA): G [0,128); Y of chunk j in [128,192) or
+// [192,256); A operands of chunk j in [256,352) or [352,448); dSig [448,512).  Swapped pair:
 // G1 [0,128), G2 [128,256); after EPI-1 Y [0,64) and dSig [128,192); A operands [256,416)
 // (G~1 | G~2 | fX).
-template <bool R2>
+template <bool R2, bool NSUM>
 struct Cols {
     static constexpr bool kTwoG = !R2;
-    static constexpr uint32_t TA = 256;
-    static constexpr uint32_t TX = TA + (R2 ? 128 : 64);
-    static constexpr uint32_t TS = R2 ? 128 : 384;
+    static constexpr bool kTwoA = !R2 && !NSUM;
+    static constexpr uint32_t TS = R2 ? 128 : (kTwoA ? 448 : 384);
     static constexpr uint32_t TN = 448;
-    __device__ static constexpr uint32_t TG(int j) { return kTwoG && (j & 1) ? 128u : 0u; }
+    __device__ static constexpr uint32_t TG(int j) { return !kTwoA && kTwoG && (j & 1) ? 128u : 0u; }
+    __device__ static constexpr uint32_t TY(int j) { return kTwoA ? 128u + 64u * (uint32_t)(j & 1) : TG(j); }
+    __device__ static constexpr uint32_t TA(int j) { return kTwoA && (j & 1) ? 352u : 256u; }
+    __device__ static constexpr uint32_t TX(int j) { return TA(j) + (R2 ? 128u : 64u); }
 };
 
-enum Bar { FX0 = 0, FX1, FK0, FK1, FV0, FV1, BG, BGT, BSU, BS, BYT, BN, BSF, kBarCount };
+// BYT1 / BSF1: with two output stage slots, BYT / BSF serve even chunks and these odd ones;
+// BGT1 / BSU1 likewise in the two-operand-slot order, where two threads wait on them
+enum Bar { FX0 = 0, FX1, FK0, FK1, FV0, FV1, BG, BGT, BSU, BS, BYT, BN, BSF, BSF1, BYT1, BGT1, BSU1, kBarCount };
 
 struct Maps {
     CUtensorMap x, k, v, xv, ad, out;
@@ -82,11 +96,11 @@ struct Maps {
 
 // ----------------------------------------------------------------------------------------
 template <bool REV, bool NSUM, bool R2, bool KVS, bool XVS, bool ADD>
-__global__ void __launch_bounds__(f64::kThreads, 1)
+__global__ void __launch_bounds__(f64::kThreadsOut, 1)
     fo64_out_tc_kernel(const __grid_constant__ f64::Maps maps, const FoArgs a) {
-    using Lay = f64::OutLayout<R2, KVS, XVS, ADD>;
-    using C = f64::Cols<R2>;
-    constexpr bool kTwoG = C::kTwoG;
+    using C = f64::Cols<R2, NSUM>;
+    constexpr bool kTwoG = C::kTwoG, kTwoA = C::kTwoA;
+    using Lay = f64::OutLayout<R2, KVS, XVS, ADD, kTwoA>;
     constexpr int kW = f64::kW, kD = f64::kD;
     pdl_trigger();
     extern __shared__ unsigned char smem_raw[];
@@ -106,10 +120,10 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
     const float log2gn = (float)a.pow_next * log2f(gam);
     const float g = exp2f(log2g);
 
-    for (int i = tid; i < 2 * kW + 1; i += f64::kThreads) gp[i] = pow_decay(log2g, (float)i);
+    for (int i = tid; i < 2 * kW + 1; i += f64::kThreadsOut) gp[i] = pow_decay(log2g, (float)i);
     if (tid == 0) {
         for (int b = 0; b < f64::kBarCount; ++b) {
-            const bool from_epilogue = (b == f64::BGT || b == f64::BS || b == f64::BYT);
+            const bool from_epilogue = b == f64::BGT || b == f64::BGT1 || b == f64::BS || b == f64::BYT || b == f64::BYT1;
             tc::mbar_init(&bars[b], from_epilogue ? 8 : 1);
         }
         *abort = 0;
@@ -123,15 +137,15 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
     const int r = 32 * q4 + lane;
     const int sr = r & 63, sc = 32 * h + 16 * (r >> 6);
     float sig[16];
-    auto publish_sig = [&]() {
+    auto publish_sig = [&](int jn) {  // Sig0 of chunk jn
 #pragma unroll
         for (int j = 0; j < 2; ++j)
-            *reinterpret_cast<uint4*>(sm + Lay::oS0 + tc::sw128_chunk(sr, sc / 8 + j)) = la_pack8(&sig[8 * j]);
+            *reinterpret_cast<uint4*>(sm + Lay::s0(jn) + tc::sw128_chunk(sr, sc / 8 + j)) = la_pack8(&sig[8 * j]);
     };
 
     if (warp == 0) {
         tc::tmem_alloc(tmem_holder, f64::kTmemCols);
-    } else {
+    } else if (warp <= 8) {
         if (a.carry && HLA2_IN(bh < a.BH && seg < a.nseg, 851)) {
             const float* src = a.carry + ((size_t)bh * a.nseg + seg) * kD * kD;
 #pragma unroll
@@ -143,7 +157,7 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) sig[j] = 0.f;
         }
-        publish_sig();
+        publish_sig(0);
         tc::fence_proxy_async();
     }
     tc::fence_before_sync();
@@ -157,9 +171,16 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
     auto fv = [&](int j) { return &bars[(j & 1) ? f64::FV1 : f64::FV0]; };
     constexpr int kVTiles = (KVS ? 0 : 1) + (XVS ? 1 : 0) + (ADD ? 1 : 0);
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ control thread
-        if (lane == 0 && nit > 0) {
+    // the barriers that complete once per chunk and have two waiters in the two-operand-slot
+    // order come in pairs by chunk parity, so that no wait can see a later phase
+    auto bgt = [&](int j) { return &bars[kTwoA && (j & 1) ? f64::BGT1 : f64::BGT]; };
+    auto bsu = [&](int j) { return &bars[kTwoA && (j & 1) ? f64::BSU1 : f64::BSU]; };
+    auto par = [&](int j) { return (uint32_t)(kTwoA ? (j >> 1) & 1 : j & 1); };
+
+    if (warp == 0 || warp == f64::kLoadWarp) {
+        // ------------------------------------------------------------ control threads
+        const bool mma_role = warp == 0;
+        if (lane == 0 && nit > 0 && (kTwoA || mma_role)) {
             auto load1 = [&](uint32_t slot, const CUtensorMap* m, int c, uint64_t* bar) {
                 tc::tma_load_3d(sm + slot, m, 0, c * kW, bh, bar);
             };
@@ -179,8 +200,7 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                 if (ADD) load1(Lay::ad(j), &maps.ad, chunk_of(j), fv(j));
             };
             constexpr bool v_late = NSUM || ADD;  // the value group is still read after the products
-            const uint32_t sKt = smem_u32(sm + Lay::oKt), sKt2 = smem_u32(sm + Lay::oKt2);
-            const uint32_t sS0 = smem_u32(sm + Lay::oS0), sST = smem_u32(sm + Lay::oST);
+            const uint32_t sKt2 = smem_u32(sm + Lay::oKt2), sST = smem_u32(sm + Lay::oST);
             constexpr uint32_t I_G = tc::idesc_bf16(128, 128, 0, 0);   // X K^T, K = 64 features
             constexpr uint32_t I_Y = tc::idesc_bf16(128, 64, 0, 1);    // A (TMEM) x MN-major B, N = 64
             constexpr uint32_t I_S = tc::idesc_bf16(128, 64, 1, 1);    // [A^T ; A^T] B, N = 64
@@ -206,9 +226,12 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
             // after EPI-Y(j): the tile store and the next summary's products (finish_store), then,
             // once the next Gram is issued, the late loads and the stage freed (finish_release)
             auto finish_store = [&](int j) {
-                tc::mbar_wait(&bars[f64::BYT], j & 1, abort, status, 138);
+                if (Lay::kTwoST)
+                    tc::mbar_wait(&bars[(j & 1) ? f64::BYT1 : f64::BYT], (j >> 1) & 1, abort, status, 138);
+                else
+                    tc::mbar_wait(&bars[f64::BYT], j & 1, abort, status, 138);
                 tc::fence_after_sync();
-                tc::tma_store_3d(&maps.out, sm + Lay::oST, 0, chunk_of(j) * kW, bh);
+                tc::tma_store_3d(&maps.out, sm + Lay::st(j), 0, chunk_of(j) * kW, bh);
                 tc::bulk_commit();
                 if (NSUM) {  // next summary: T_N += [Y^T ; Y^T] (w' U)
                     const uint32_t sXV = smem_u32(sm + Lay::xv(j));
@@ -223,25 +246,100 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                     load_v(j + 2);
                     ++lv;
                 }
-                tc::bulk_wait_read_all();
-                tc::mbar_arrive(&bars[f64::BSF]);
+                if (Lay::kTwoST) {  // two stage slots: chunk j - 1's store has read its slot
+                    tc::bulk_wait_read_but_last();
+                    if (j > 0) tc::mbar_arrive(&bars[(j & 1) ? f64::BSF : f64::BSF1]);
+                } else {
+                    tc::bulk_wait_read_all();
+                    tc::mbar_arrive(&bars[f64::BSF]);
+                }
             };
             auto finish = [&](int j) {
                 finish_store(j);
                 finish_release(j);
             };
 
-            // prologue: chunks 0 and 1 in flight
-            for (int j = 0; j < 2 && j < nit; ++j) {
-                load_x(j);
-                load_k(j);
-                ++lx;
-                ++lk;
-                if (kVTiles > 0) {
-                    load_v(j);
-                    ++lv;
+            auto prologue_loads = [&]() {  // chunks 0 and 1 in flight
+                for (int j = 0; j < 2 && j < nit; ++j) {
+                    load_x(j);
+                    load_k(j);
+                    ++lx;
+                    ++lk;
+                    if (kVTiles > 0) {
+                        load_v(j);
+                        ++lv;
+                    }
                 }
-            }
+            };
+            if constexpr (kTwoA) {
+                // G in one region, read by EPI-1(j) before the next Gram; Y, the A operands, K~ and
+                // Sig0 by chunk parity.  The epilogue runs EPI-1(j+1), EPI-S(j), EPI-Y(j): every
+                // product of chunk j is issued as soon as EPI-1(j) and EPI-S(j-1) have arrived.
+                // Warp 0 issues the MMAs, warp 9 the loads (the tiles three chunks ahead are
+                // brought into L2 first, so that the loads two ahead are short) and the stores.
+                if (mma_role) {
+                    wait_g_inputs(0);
+                    mma_g(0);
+                    for (int j = 0; j < nit; ++j) {
+                        tc::mbar_wait(bgt(j), par(j), abort, status, 134);  // G read; G~, fX, K~ written
+                        if (j + 1 < nit) {
+                            wait_g_inputs(j + 1);
+                            mma_g(j + 1);
+                        }
+                        if (j > 0) tc::mbar_wait(&bars[f64::BS], (j - 1) & 1, abort, status, 136);  // Sig0 of chunk j
+                        if (!KVS) tc::mbar_wait(fv(j), (j >> 1) & 1, abort, status, 135);
+                        tc::fence_after_sync();
+                        const uint32_t sV = smem_u32(sm + Lay::val(j));
+                        const uint32_t sKt = smem_u32(sm + Lay::kt(j)), sS0 = smem_u32(sm + Lay::s0(j));
+                        // MMA-Y: Y = [G~ | fX] [V ; Sig0];  MMA-S: dSig = [K~^T ; K~^T] V
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_ts(tmem + C::TY(j), tmem + C::TA(j) + 8 * ks, mdesc(sV, ks), I_Y, ks > 0);
+                        for (int ks = 0; ks < 4; ++ks)
+                            tc::mma_ts(tmem + C::TY(j), tmem + C::TX(j) + 8 * ks, mdesc(sS0, ks), I_Y, 1);
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_ss(tmem + C::TS, mdesc(sKt, ks), mdesc(sV, ks), I_S, ks > 0);
+                        tc::mma_commit(bsu(j));
+                    }
+                    volatile int never = 0;  // drain (bounded, ignoring the abort flag)
+                    tc::mbar_wait(bsu(nit - 1), par(nit - 1), &never, nullptr, 0);
+                } else {
+                    auto prefetch = [&](int j) {
+                        const int c = chunk_of(j) * kW;
+                        tc::tma_prefetch_3d(&maps.x, 0, c, bh);
+                        tc::tma_prefetch_3d(&maps.k, 0, c, bh);
+                        if (!KVS) tc::tma_prefetch_3d(&maps.v, 0, c, bh);
+                        if (ADD) tc::tma_prefetch_3d(&maps.ad, 0, c, bh);
+                    };
+                    prologue_loads();
+                    if (nit > 2) prefetch(2);
+                    for (int j = 0; j < nit; ++j) {
+                        tc::mbar_wait(bgt(j), par(j), abort, status, 139);  // MMA-G(j) and EPI-1(j) done
+                        if (j + 3 < nit) prefetch(j + 3);
+                        if (j + 2 < nit) {  // X and key slots j % 2 are free
+                            load_x(j + 2);
+                            ++lx;
+                            if (!KVS) {
+                                load_k(j + 2);
+                                ++lk;
+                            }
+                        }
+                        if (j > 0) finish(j - 1);  // after EPI-Y(j - 1)
+                        tc::mbar_wait(bsu(j), par(j), abort, status, 137);  // chunk j's products done
+                        if (j + 2 < nit) {  // the value slot j % 2 is free (keys as values: the key slot)
+                            if (KVS) {
+                                load_k(j + 2);
+                                ++lk;
+                            }
+                            if (!v_late && !KVS) {
+                                load_v(j + 2);
+                                ++lv;
+                            }
+                        }
+                    }
+                    finish(nit - 1);
+                }
+            } else {
+            prologue_loads();
             wait_g_inputs(0);
             mma_g(0);
             for (int j = 0; j < nit; ++j) {
@@ -258,14 +356,15 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                 if (!KVS) tc::mbar_wait(fv(j), (j >> 1) & 1, abort, status, 135);
                 tc::fence_after_sync();
                 const uint32_t sK = smem_u32(sm + Lay::key(j)), sV = smem_u32(sm + Lay::val(j));
+                const uint32_t sKt = smem_u32(sm + Lay::kt(j)), sS0 = smem_u32(sm + Lay::s0(j));
                 // MMA-Y: Y = [G~ | (G~2) | fX] [V ; (K) ; Sig0]
                 for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_ts(tmem + C::TG(j), tmem + C::TA + 8 * ks, mdesc(sV, ks), I_Y, ks > 0);
+                    tc::mma_ts(tmem + C::TY(j), tmem + C::TA(j) + 8 * ks, mdesc(sV, ks), I_Y, ks > 0);
                 if (R2)
                     for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_ts(tmem + C::TG(j), tmem + C::TA + 64 + 8 * ks, mdesc(sK, ks), I_Y, 1);
+                        tc::mma_ts(tmem + C::TY(j), tmem + C::TA(j) + 64 + 8 * ks, mdesc(sK, ks), I_Y, 1);
                 for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_ts(tmem + C::TG(j), tmem + C::TX + 8 * ks, mdesc(sS0, ks), I_Y, 1);
+                    tc::mma_ts(tmem + C::TY(j), tmem + C::TX(j) + 8 * ks, mdesc(sS0, ks), I_Y, 1);
                 // MMA-S: dSig = [K~^T ; K~^T] V (R2: + [V~^T ; V~^T] K)
                 for (int ks = 0; ks < 8; ++ks) tc::mma_ss(tmem + C::TS, mdesc(sKt, ks), mdesc(sV, ks), I_S, ks > 0);
                 if (R2)
@@ -300,8 +399,9 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                 }
             }
             if (kTwoG) finish(nit - 1);
+            }
             volatile int never = 0;
-            tc::mbar_wait(&bars[f64::BSU], (nit - 1) & 1, &never, nullptr, 0);
+            if (!kTwoA) tc::mbar_wait(&bars[f64::BSU], (nit - 1) & 1, &never, nullptr, 0);
             if (NSUM) tc::mbar_wait(&bars[f64::BN], (nit - 1) & 1, &never, nullptr, 0);
             // every load group's last phase, per slot
             auto drain = [&](int count, uint64_t* b0, uint64_t* b1) {
@@ -339,7 +439,7 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                     const int cb = 64 * h + 32 * p;
                     uint32_t pk[16];
                     la_masked_pack<REV>(lrow + C::TG(j) + 128 * gi + cb, r, cb, row0, log2g, g, ginv, pk);
-                    tc::tmem_st16(lrow + C::TA + 64 * gi + cb / 2, pk);
+                    tc::tmem_st16(lrow + C::TA(j) + 64 * gi + cb / 2, pk);
                 }
             }
             {  // fX: this thread's 32 features of row r -> 16 packed columns
@@ -350,13 +450,13 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                     const uint4 x = la_scale_chunk(*reinterpret_cast<const uint4*>(sX + tc::sw128_chunk(r, 4 * h + i)), f);
                     pk[4 * i] = x.x, pk[4 * i + 1] = x.y, pk[4 * i + 2] = x.z, pk[4 * i + 3] = x.w;
                 }
-                tc::tmem_st16(lrow + C::TX + 16 * h, pk);
+                tc::tmem_st16(lrow + C::TX(j) + 16 * h, pk);
             }
             const float w = live ? (REV ? gp[r] : gp[Wc - 1 - r]) : 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t off = tc::sw128_chunk(r, 4 * h + i);
-                *reinterpret_cast<uint4*>(sm + Lay::oKt + off) = la_scale_chunk(*reinterpret_cast<const uint4*>(sK + off), w);
+                *reinterpret_cast<uint4*>(sm + Lay::kt(j) + off) = la_scale_chunk(*reinterpret_cast<const uint4*>(sK + off), w);
                 if (R2)
                     *reinterpret_cast<uint4*>(sm + Lay::oKt2 + off) =
                         la_scale_chunk(*reinterpret_cast<const uint4*>(sV + off), w);
@@ -365,13 +465,13 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
             tc::fence_proxy_async();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[f64::BGT]);
+            if (lane == 0) tc::mbar_arrive(bgt(j));
         };
 
         auto epis = [&](int j) {
             const int c = chunk_of(j);
             const int Wc = min(kW, a.n - c * kW);
-            tc::mbar_wait(&bars[f64::BSU], j & 1, abort, status, 145);
+            tc::mbar_wait(bsu(j), par(j), abort, status, 145);
             tc::fence_after_sync();
             const float rho = gp[Wc];
             uint32_t v[16];
@@ -379,7 +479,7 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
             tc::tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) sig[i] = rho * sig[i] + __uint_as_float(v[i]);
-            if (j + 1 < nit) publish_sig();  // MMA-Y of chunk j has completed (commit order)
+            if (j + 1 < nit) publish_sig(j + 1);  // the products that read this slot last have completed
             tc::fence_proxy_async();
             tc::fence_before_sync();
             __syncwarp();
@@ -390,13 +490,18 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
             const int c = chunk_of(j);
             const int Wc = min(kW, a.n - c * kW);
             const bool live = r < Wc;
-            if (j > 0) tc::mbar_wait(&bars[f64::BSF], (j - 1) & 1, abort, status, 146);
+            if (Lay::kTwoST) {  // the stage slot j % 2 was last stored from by chunk j - 2 (released
+                                // once chunk j - 1's store is issued)
+                if (j > 1) tc::mbar_wait(&bars[(j & 1) ? f64::BSF1 : f64::BSF], ((j >> 1) - 1) & 1, abort, status, 146);
+            } else if (j > 0) {
+                tc::mbar_wait(&bars[f64::BSF], (j - 1) & 1, abort, status, 146);
+            }
             if (ADD || (NSUM && XVS)) tc::mbar_wait(fv(j), (j >> 1) & 1, abort, status, 147);
             tc::fence_after_sync();
 #pragma unroll
             for (int p = 0; p < 2; ++p) {
                 uint32_t v[16];
-                tc::tmem_ld16(lrow + C::TG(j) + 32 * h + 16 * p, v);
+                tc::tmem_ld16(lrow + C::TY(j) + 32 * h + 16 * p, v);
                 tc::tmem_wait_ld();
                 float y[16];
 #pragma unroll
@@ -413,7 +518,7 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
                 }
 #pragma unroll
                 for (int i = 0; i < 2; ++i)
-                    *reinterpret_cast<uint4*>(sm + Lay::oST + tc::sw128_chunk(r, 4 * h + 2 * p + i)) = la_pack8(&y[8 * i]);
+                    *reinterpret_cast<uint4*>(sm + Lay::st(j) + tc::sw128_chunk(r, 4 * h + 2 * p + i)) = la_pack8(&y[8 * i]);
             }
             if (NSUM) {
                 const int pos = (c - sg.c_begin) * kW + r;
@@ -427,16 +532,21 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
             tc::fence_proxy_async();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&bars[f64::BYT]);
+            if (lane == 0) tc::mbar_arrive(&bars[Lay::kTwoST && (j & 1) ? f64::BYT1 : f64::BYT]);
         };
 
         if (nit > 0) epi1(0);
         for (int j = 0; j < nit; ++j) {
-            epis(j);
-            if (kTwoG) {
+            if (kTwoA) {
+                if (j + 1 < nit) epi1(j + 1);
+                epis(j);
+                epiy(j);
+            } else if (kTwoG) {
+                epis(j);
                 if (j + 1 < nit) epi1(j + 1);
                 epiy(j);
             } else {
+                epis(j);
                 epiy(j);
                 if (j + 1 < nit) epi1(j + 1);
             }
@@ -587,20 +697,25 @@ __global__ void __launch_bounds__(f64::kThreads, 1)
 }
 
 template <typename K>
-int f64_launch(K kfn, uint32_t smem, const f64::Maps& maps, const FoArgs& a, cudaStream_t st) {
+int f64_launch(K kfn, uint32_t smem, const f64::Maps& maps, const FoArgs& a, cudaStream_t st,
+               int threads = f64::kThreads) {
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return -1;
-    if (launch_pdl(kfn, dim3(a.nseg, a.BH), dim3(f64::kThreads), smem, st, maps, a) != cudaSuccess) return -1;
+    if (launch_pdl(kfn, dim3(a.nseg, a.BH), dim3(threads), smem, st, maps, a) != cudaSuccess) return -1;
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace
 
 size_t fo64_tc_max_smem() {
+    // the instantiated layouts: next summary over an extra tile (NSUM), plain (two slots for the
+    // A-side operands), swapped pair, partial added (keys as values or not), next summary over
+    // the values (NSUM)
     const uint32_t sizes[] = {f64::OutLayout<false, true, true, false>::kSmemBytes,
+                              f64::OutLayout<false, false, false, false, true>::kSmemBytes,
                               f64::OutLayout<false, false, false, false>::kSmemBytes,
                               f64::OutLayout<true, false, false, false>::kSmemBytes,
-                              f64::OutLayout<false, true, false, true>::kSmemBytes,
-                              f64::OutLayout<false, false, false, true>::kSmemBytes,
+                              f64::OutLayout<false, true, false, true, true>::kSmemBytes,
+                              f64::OutLayout<false, false, false, true, true>::kSmemBytes,
                               f64::OutLayout<false, false, true, false>::kSmemBytes,
                               f64s::Layout<false>::kSmemBytes, f64s::Layout<true>::kSmemBytes};
     uint32_t m = 0;
@@ -635,7 +750,8 @@ int launch_fo64_tc_out(const FoArgs& a, const void* x, const void* k, const void
 #define HLA2_F64(REV, NSUM, R2, KVS, XVS, ADD)                                                               \
     if (reverse == REV && nsum == NSUM && r2 == R2 && kvs == KVS && xvs == XVS && addp == ADD)              \
         return f64_launch(fo64_out_tc_kernel<REV, NSUM, R2, KVS, XVS, ADD>,                                    \
-                          f64::OutLayout<R2, KVS, XVS, ADD>::kSmemBytes, m, a, st);
+                          f64::OutLayout<R2, KVS, XVS, ADD, f64::Cols<R2, NSUM>::kTwoA>::kSmemBytes, m, a, st, \
+                          f64::kThreadsOut);
     HLA2_F64(false, true, false, true, true, false)    // p = LA(q, k, k), next summary over (p, v)
     HLA2_F64(false, false, false, false, false, false) // o = LA(q, p, v);  Z dO = LA(dO, v, p)
     HLA2_F64(true, true, false, false, false, false)   // dp = RLA(v, dO, q), next summary over (dp, q)
