@@ -207,9 +207,14 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
             auto kdesc = [](uint32_t base, int ks) { return tc::smem_desc(base + 32u * ks, 16, 1024); };
             auto mdesc = [](uint32_t base, int ks) { return tc::smem_desc(base + 2048u * ks, 0, 1024); };
             int lx = 0, lk = 0, lv = 0;
+            // a descriptor's address field counts 16-byte units: a K step of 32 bytes (K-major) is
+            // +2, one of 2048 bytes (MN-major, 8 K-rows of a SW128 tile) is +128
             auto mma_g = [&](int j) {
                 const uint32_t sX = smem_u32(sm + Lay::x(j)), sK = smem_u32(sm + Lay::key(j));
-                for (int ks = 0; ks < 4; ++ks) tc::mma_ss(tmem + C::TG(j), kdesc(sX, ks), kdesc(sK, ks), I_G, ks > 0);
+                const uint64_t dX = kdesc(sX, 0), dK = kdesc(sK, 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_ss(tmem + C::TG(j), dX + 2u * ks, dK + 2u * ks, I_G, ks > 0);
                 if (R2) {
                     const uint32_t sV = smem_u32(sm + Lay::val(j));
                     for (int ks = 0; ks < 4; ++ks)
@@ -289,15 +294,18 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
                         if (j > 0) tc::mbar_wait(&bars[f64::BS], (j - 1) & 1, abort, status, 136);  // Sig0 of chunk j
                         if (!KVS) tc::mbar_wait(fv(j), (j >> 1) & 1, abort, status, 135);
                         tc::fence_after_sync();
-                        const uint32_t sV = smem_u32(sm + Lay::val(j));
-                        const uint32_t sKt = smem_u32(sm + Lay::kt(j)), sS0 = smem_u32(sm + Lay::s0(j));
+                        const uint64_t dV = mdesc(smem_u32(sm + Lay::val(j)), 0);
+                        const uint64_t dKt = mdesc(smem_u32(sm + Lay::kt(j)), 0);
+                        const uint64_t dS0 = mdesc(smem_u32(sm + Lay::s0(j)), 0);
+                        const uint32_t tY = tmem + C::TY(j), tA = tmem + C::TA(j), tX = tmem + C::TX(j);
                         // MMA-Y: Y = [G~ | fX] [V ; Sig0];  MMA-S: dSig = [K~^T ; K~^T] V
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) tc::mma_ts(tY, tA + 8 * ks, dV + 128u * ks, I_Y, ks > 0);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) tc::mma_ts(tY, tX + 8 * ks, dS0 + 128u * ks, I_Y, 1);
+#pragma unroll
                         for (int ks = 0; ks < 8; ++ks)
-                            tc::mma_ts(tmem + C::TY(j), tmem + C::TA(j) + 8 * ks, mdesc(sV, ks), I_Y, ks > 0);
-                        for (int ks = 0; ks < 4; ++ks)
-                            tc::mma_ts(tmem + C::TY(j), tmem + C::TX(j) + 8 * ks, mdesc(sS0, ks), I_Y, 1);
-                        for (int ks = 0; ks < 8; ++ks)
-                            tc::mma_ss(tmem + C::TS, mdesc(sKt, ks), mdesc(sV, ks), I_S, ks > 0);
+                            tc::mma_ss(tmem + C::TS, dKt + 128u * ks, dV + 128u * ks, I_S, ks > 0);
                         tc::mma_commit(bsu(j));
                     }
                     volatile int never = 0;  // drain (bounded, ignoring the abort flag)
