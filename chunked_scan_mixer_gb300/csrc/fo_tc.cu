@@ -49,6 +49,9 @@ namespace la {
 
 constexpr int kW = 128, kD = 128;
 constexpr int kThreads = 288;          // 1 control warp + 8 epilogue warps
+// the output kernel adds warp 9: with G / Y double-buffered it issues the tile loads and stores
+// while warp 0 issues only the MMAs
+constexpr int kThreadsOut = 320, kLoadWarp = 9;
 constexpr uint32_t kBlk = 128 * 128;   // one [128 rows][64 bf16] SW128 column block (16 KB)
 constexpr uint32_t kTile = 2 * kBlk;   // a [128][128] bf16 tile: column blocks 0 (cols 0..63) and 1
 constexpr uint32_t kTmemCols = 512;
@@ -91,7 +94,8 @@ struct Cols {
     __device__ static constexpr uint32_t TG(int j) { return kTwoG && (j & 1) ? 384u : 0u; }
 };
 
-enum Bar { FQ = 0, FK0, FK1, FV, BG, BGT, BSU, BS, BYT, BN, BSF, kBarCount };
+// BSU1: with G / Y double-buffered BSU serves even chunks and BSU1 odd ones (two waiters)
+enum Bar { FQ = 0, FK0, FK1, FV, BG, BGT, BSU, BS, BYT, BN, BSF, BSU1, kBarCount };
 
 struct Maps {
     CUtensorMap x, k, v, xv, ad, out;
@@ -110,7 +114,7 @@ struct Maps {
 // EPI-Y(j): MMA-G(j+1) is issued as soon as chunk j's products are, and MMA-Y(j+1) runs while
 // chunk j's output is staged.  Otherwise the order is EPI-S(j), EPI-Y(j), EPI-1(j+1).
 template <bool REV, bool NSUM, bool R2, bool KVS, bool XVS, bool ADD>
-__global__ void __launch_bounds__(la::kThreads, 1)
+__global__ void __launch_bounds__(la::kThreadsOut, 1)
     fo_out_tc_kernel(const __grid_constant__ la::Maps maps, const FoArgs a) {
     using Lay = la::OutLayout<R2, KVS, XVS, ADD>;
     using C = la::Cols<R2, NSUM>;
@@ -134,7 +138,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
     const float log2gn = (float)a.pow_next * log2f(gam);
     const float g = exp2f(log2g);
 
-    for (int i = tid; i < 2 * kW + 1; i += la::kThreads) gp[i] = pow_decay(log2g, (float)i);
+    for (int i = tid; i < 2 * kW + 1; i += la::kThreadsOut) gp[i] = pow_decay(log2g, (float)i);
     if (tid == 0) {
         for (int b = 0; b < la::kBarCount; ++b) {
             const bool from_epilogue = (b == la::BGT || b == la::BS || b == la::BYT);
@@ -157,7 +161,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
 
     if (warp == 0) {
         tc::tmem_alloc(tmem_holder, la::kTmemCols);
-    } else {
+    } else if (warp <= 8) {
         // carry-in of the segment (zero without one), as stored, transposed or symmetrised
         if (a.carry && HLA2_IN(bh < a.BH && seg < a.nseg, 801)) {
             const float* src = a.carry + ((size_t)bh * a.nseg + seg) * la::kD * la::kD;
@@ -189,10 +193,15 @@ __global__ void __launch_bounds__(la::kThreads, 1)
 
     auto chunk_of = [&](int it) { return REV ? sg.c_end - 1 - it : sg.c_begin + it; };
     auto fk = [&](int j) { return &bars[(j & 1) ? la::FK1 : la::FK0]; };
+    // the products' barrier: with G / Y double-buffered a pair by chunk parity (the epilogue and
+    // the load thread wait on it, and neither may see a later phase)
+    auto bsu = [&](int j) { return &bars[kTwoG && (j & 1) ? la::BSU1 : la::BSU]; };
+    auto bsu_par = [&](int j) { return (uint32_t)(kTwoG ? (j >> 1) & 1 : j & 1); };
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ control thread
-        if (lane == 0 && nit > 0) {
+    if (warp == 0 || warp == la::kLoadWarp) {
+        // ------------------------------------------------------------ control threads
+        const bool mma_role = warp == 0;
+        if (lane == 0 && nit > 0 && (kTwoG || mma_role)) {
             auto load2 = [&](uint32_t slot, const CUtensorMap* m, int c, uint64_t* bar) {
                 tc::tma_load_3d(sm + slot, m, 0, c * kW, bh, bar);
                 tc::tma_load_3d(sm + slot + la::kBlk, m, 64, c * kW, bh, bar);
@@ -277,18 +286,80 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                 finish_release(j);
             };
 
-            load_x(0);
-            ++lx;
-            load_k(0);
-            ++lk;
-            if (kVTiles > 0) {
-                load_v(0);
-                ++lv;
-            }
-            if (nit > 1) {
-                load_k(1);
+            auto prologue_loads = [&]() {
+                load_x(0);
+                ++lx;
+                load_k(0);
                 ++lk;
-            }
+                if (kVTiles > 0) {
+                    load_v(0);
+                    ++lv;
+                }
+                if (nit > 1) {
+                    load_k(1);
+                    ++lk;
+                }
+            };
+            if constexpr (kTwoG) {
+                // warp 0 issues the MMAs; warp 9 the loads and the tile stores
+                if (mma_role) {
+                    wait_g_inputs(0);
+                    mma_g(0);
+                    for (int j = 0; j < nit; ++j) {
+                        tc::mbar_wait(&bars[la::BGT], j & 1, abort, status, 104);  // G read; G~, fX, K~ written
+                        if (j > 0) tc::mbar_wait(&bars[la::BS], (j - 1) & 1, abort, status, 106);  // Sig0 of chunk j
+                        if (!KVS) tc::mbar_wait(&bars[la::FV], j & 1, abort, status, 105);  // the value tile
+                        tc::fence_after_sync();
+                        const uint32_t sVj = smem_u32(sm + Lay::val(j));
+                        // MMA-Y: Y = [G~ | fX] [V ; Sig0];  MMA-S: dSig = K~^T V
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_ts(tmem + C::TG(j), tmem + C::TA + 8 * ks, mdesc(sVj, ks), I_TM, ks > 0);
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_ts(tmem + C::TG(j), tmem + C::TX + 8 * ks, mdesc(sS0, ks), I_TM, 1);
+                        for (int ks = 0; ks < 8; ++ks)
+                            tc::mma_ss(tmem + C::TS, mdesc(sKt, ks), mdesc(sVj, ks), I_MM, ks > 0);
+                        tc::mma_commit(bsu(j));
+                        if (j + 1 < nit) {  // G / Y region (j + 1) % 2: EPI-Y(j - 1) has read it
+                            if (j > 0) tc::mbar_wait(&bars[la::BYT], (j - 1) & 1, abort, status, 110);
+                            wait_g_inputs(j + 1);
+                            mma_g(j + 1);
+                        }
+                    }
+                    volatile int never = 0;  // drain (bounded, ignoring the abort flag)
+                    tc::mbar_wait(bsu(nit - 1), bsu_par(nit - 1), &never, nullptr, 0);
+                } else {
+                    prologue_loads();
+                    for (int j = 0; j < nit; ++j) {
+                        tc::mbar_wait(&bars[la::BGT], j & 1, abort, status, 111);  // X and key slot j % 2 read
+                        if (j + 1 < nit) {
+                            load_x(j + 1);
+                            ++lx;
+                        }
+                        if (!KVS && j + 2 < nit) {
+                            load_k(j + 2);
+                            ++lk;
+                        }
+                        if (j > 0) finish(j - 1);  // after EPI-Y(j - 1)
+                        tc::mbar_wait(bsu(j), bsu_par(j), abort, status, 107);  // chunk j's products done
+                        if (KVS && j + 2 < nit) {
+                            load_k(j + 2);
+                            ++lk;
+                        }
+                        if (!v_late && !KVS && j + 1 < nit) {
+                            load_v(j + 1);
+                            ++lv;
+                        }
+                    }
+                    finish(nit - 1);
+                    volatile int never = 0;  // drain (bounded, ignoring the abort flag)
+                    tc::mbar_wait(&bars[la::FQ], (lx - 1) & 1, &never, nullptr, 0);
+                    tc::mbar_wait(&bars[la::FK0], ((lk + 1) / 2 - 1) & 1, &never, nullptr, 0);
+                    if (lk > 1) tc::mbar_wait(&bars[la::FK1], (lk / 2 - 1) & 1, &never, nullptr, 0);
+                    if (lv > 0) tc::mbar_wait(&bars[la::FV], (lv - 1) & 1, &never, nullptr, 0);
+                    tc::bulk_wait_all();
+                }
+            } else {
+            prologue_loads();
             wait_g_inputs(0);
             mma_g(0);
             for (int j = 0; j < nit; ++j) {
@@ -354,7 +425,6 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                     }
                 }
             }
-            if (kTwoG) finish(nit - 1);
             // drain (bounded, ignoring the abort flag) so that nothing is in flight at exit
             volatile int never = 0;
             tc::mbar_wait(&bars[la::BSU], (nit - 1) & 1, &never, nullptr, 0);
@@ -364,6 +434,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
             if (lk > 1) tc::mbar_wait(&bars[la::FK1], (lk / 2 - 1) & 1, &never, nullptr, 0);
             if (lv > 0) tc::mbar_wait(&bars[la::FV], (lv - 1) & 1, &never, nullptr, 0);
             tc::bulk_wait_all();
+            }
         }
         __syncwarp();
     } else {
@@ -426,7 +497,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
         auto epis = [&](int j) {
             const int c = chunk_of(j);
             const int Wc = min(kW, a.n - c * kW);
-            tc::mbar_wait(&bars[la::BSU], j & 1, abort, status, 115);  // chunk j's products are done
+            tc::mbar_wait(bsu(j), bsu_par(j), abort, status, 115);  // chunk j's products are done
             tc::fence_after_sync();
             const float rho = gp[Wc];
 #pragma unroll
@@ -673,9 +744,10 @@ __global__ void fo_zero_first_kernel(float* carry, int nseg, int E, int BH, int*
 }
 
 template <typename K>
-int la_launch(K kfn, uint32_t smem, const la::Maps& maps, const FoArgs& a, cudaStream_t st) {
+int la_launch(K kfn, uint32_t smem, const la::Maps& maps, const FoArgs& a, cudaStream_t st,
+              int threads = la::kThreads) {
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return -1;
-    if (launch_pdl(kfn, dim3(a.nseg, a.BH), dim3(la::kThreads), smem, st, maps, a) != cudaSuccess) return -1;
+    if (launch_pdl(kfn, dim3(a.nseg, a.BH), dim3(threads), smem, st, maps, a) != cudaSuccess) return -1;
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
@@ -731,7 +803,7 @@ int launch_fo_tc_out(const FoArgs& a, const void* x, const void* k, const void* 
 #define HLA2_LA(REV, NSUM, R2, KVS, XVS, ADD)                                                               \
     if (reverse == REV && nsum == NSUM && r2 == R2 && kvs == KVS && xvs == XVS && addp == ADD)             \
         return la_launch(fo_out_tc_kernel<REV, NSUM, R2, KVS, XVS, ADD>,                                      \
-                         la::OutLayout<R2, KVS, XVS, ADD>::kSmemBytes, m, a, st);
+                         la::OutLayout<R2, KVS, XVS, ADD>::kSmemBytes, m, a, st, la::kThreadsOut);
     // the passes of the d = 128 training path
     HLA2_LA(false, true, false, true, true, false)    // p = LA(q, k, k), next summary over (p, v)
     HLA2_LA(false, false, false, false, false, false) // o = LA(q, p, v);  dq_a = LA(dO, v, p)
