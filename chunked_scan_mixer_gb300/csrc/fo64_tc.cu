@@ -66,20 +66,20 @@ struct OutLayout {
     __host__ __device__ static constexpr uint32_t st(int j) { return oST + (kTwoST ? (uint32_t)(j & 1) * kTile : 0u); }
 };
 
-// Tensor-memory columns.  One pair with a next summary: G / Y of chunk j in [0,128) or
-// [128,256) (Y: the first 64); A operands [256,352) (G~ 64 | fX 32); dSig [384,448); next
-// summary [448,512).  One pair without (kTwoA): G [0,128); Y of chunk j in [128,192) or
-// [192,256); A operands of chunk j in [256,352) or [352,448); dSig [448,512).  Swapped pair:
-// G1 [0,128), G2 [128,256); after EPI-1 Y [0,64) and dSig [128,192); A operands [256,416)
+// Tensor-memory columns.  One pair (kTwoA, the two-slot order): G [0,128); Y of chunk j in
+// [128,192) or [192,256) (with a next summary: Y [128,192), the summary [192,256)); A operands
+// of chunk j in [256,352) or [352,448) (G~ 64 | fX 32); dSig [448,512).  Swapped pair: G1
+// [0,128), G2 [128,256); after EPI-1 Y [0,64) and dSig [128,192); A operands [256,416)
 // (G~1 | G~2 | fX).
 template <bool R2, bool NSUM>
 struct Cols {
     static constexpr bool kTwoG = !R2;
-    static constexpr bool kTwoA = !R2 && !NSUM;
-    static constexpr uint32_t TS = R2 ? 128 : (kTwoA ? 448 : 384);
-    static constexpr uint32_t TN = 448;
-    __device__ static constexpr uint32_t TG(int j) { return !kTwoA && kTwoG && (j & 1) ? 128u : 0u; }
-    __device__ static constexpr uint32_t TY(int j) { return kTwoA ? 128u + 64u * (uint32_t)(j & 1) : TG(j); }
+    static constexpr bool kTwoA = !R2;
+    static constexpr bool kTwoY = kTwoA && !NSUM;
+    static constexpr uint32_t TS = R2 ? 128 : 448;
+    static constexpr uint32_t TN = 192;
+    __device__ static constexpr uint32_t TG(int j) { return 0u; }
+    __device__ static constexpr uint32_t TY(int j) { return kTwoA ? 128u + (kTwoY ? 64u * (uint32_t)(j & 1) : 0u) : 0u; }
     __device__ static constexpr uint32_t TA(int j) { return kTwoA && (j & 1) ? 352u : 256u; }
     __device__ static constexpr uint32_t TX(int j) { return TA(j) + (R2 ? 128u : 64u); }
 };
@@ -239,9 +239,9 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
                 tc::tma_store_3d(&maps.out, sm + Lay::st(j), 0, chunk_of(j) * kW, bh);
                 tc::bulk_commit();
                 if (NSUM) {  // next summary: T_N += [Y^T ; Y^T] (w' U)
-                    const uint32_t sXV = smem_u32(sm + Lay::xv(j));
+                    const uint32_t sXV = smem_u32(sm + Lay::xv(j)), sSTj = smem_u32(sm + Lay::st(j));
                     for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_ss(tmem + C::TN, mdesc(sST, ks), mdesc(sXV, ks), I_S, (j > 0 || ks > 0) ? 1u : 0u);
+                        tc::mma_ss(tmem + C::TN, mdesc(sSTj, ks), mdesc(sXV, ks), I_S, (j > 0 || ks > 0) ? 1u : 0u);
                     tc::mma_commit(&bars[f64::BN]);
                 }
             };
@@ -293,6 +293,8 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
                         }
                         if (j > 0) tc::mbar_wait(&bars[f64::BS], (j - 1) & 1, abort, status, 136);  // Sig0 of chunk j
                         if (!KVS) tc::mbar_wait(fv(j), (j >> 1) & 1, abort, status, 135);
+                        if (!C::kTwoY && j > 0)  // one Y region: EPI-Y(j - 1) has read it
+                            tc::mbar_wait(&bars[(j & 1) ? f64::BYT : f64::BYT1], ((j - 1) >> 1) & 1, abort, status, 130);
                         tc::fence_after_sync();
                         const uint64_t dV = mdesc(smem_u32(sm + Lay::val(j)), 0);
                         const uint64_t dKt = mdesc(smem_u32(sm + Lay::kt(j)), 0);
@@ -316,6 +318,7 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
                         tc::tma_prefetch_3d(&maps.x, 0, c, bh);
                         tc::tma_prefetch_3d(&maps.k, 0, c, bh);
                         if (!KVS) tc::tma_prefetch_3d(&maps.v, 0, c, bh);
+                        if (XVS) tc::tma_prefetch_3d(&maps.xv, 0, c, bh);
                         if (ADD) tc::tma_prefetch_3d(&maps.ad, 0, c, bh);
                     };
                     prologue_loads();
@@ -718,13 +721,12 @@ size_t fo64_tc_max_smem() {
     // the instantiated layouts: next summary over an extra tile (NSUM), plain (two slots for the
     // A-side operands), swapped pair, partial added (keys as values or not), next summary over
     // the values (NSUM)
-    const uint32_t sizes[] = {f64::OutLayout<false, true, true, false>::kSmemBytes,
+    const uint32_t sizes[] = {f64::OutLayout<false, true, true, false, true>::kSmemBytes,
                               f64::OutLayout<false, false, false, false, true>::kSmemBytes,
-                              f64::OutLayout<false, false, false, false>::kSmemBytes,
                               f64::OutLayout<true, false, false, false>::kSmemBytes,
                               f64::OutLayout<false, true, false, true, true>::kSmemBytes,
                               f64::OutLayout<false, false, false, true, true>::kSmemBytes,
-                              f64::OutLayout<false, false, true, false>::kSmemBytes,
+                              f64::OutLayout<false, false, true, false, true>::kSmemBytes,
                               f64s::Layout<false>::kSmemBytes, f64s::Layout<true>::kSmemBytes};
     uint32_t m = 0;
     for (uint32_t x : sizes) m = x > m ? x : m;
