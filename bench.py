@@ -50,7 +50,7 @@ def parse():
                     help="skip the decode and training rows measured after the headline")
     ap.add_argument("--only", choices=("decode", "decode_compact", "decode_unmasked", "decode_mq", "train", "ahla",
                                        "unmasked", "hla3", "prefill", "train_d64", "ahla_backward", "normed",
-                                       "prefill_d128"),
+                                       "prefill_d128", "normed_backward"),
                     default=None,
                     help="measure only this row (for profiler captures; --steps/--warmup apply)")
     ap.add_argument("--decode-seqs", type=int, default=256,
@@ -543,6 +543,48 @@ def measure_normed(dev, dist: Dist, hbm_gbs: float, steps: int = 200, warmup: in
     return rows
 
 
+def measure_normed_backward(dev, dist: Dist, hbm_gbs: float, steps: int = 50, warmup: int = 5,
+                            n: int | None = None):
+    """Ratio-normalised reverse-mode rows: dq, dk, dv of o / (den + eps) on the normalised
+    workload (B=2 H=8 n=2048 d=dv=64 bf16, softplus q and k, decay linspace(0.95, 0.999),
+    eps 1e-6, chunk 64), upstream dO ~ N(0, 1), and on the same recipe at B=1 H=16 n=16384.
+    The call widens the inputs to float32 and composes float32 passes (two forwards, the
+    quotient rule, two backwards).  HBM roofline of the whole call over q, k, v, dO read and
+    dq, dk, dv written (bf16)."""
+    import dataclasses
+
+    import torch
+
+    import chunked_scan_mixer_gb300 as hla
+    from chunked_scan_mixer_gb300 import inputs
+
+    w = dataclasses.replace(inputs.WORKLOADS["normed"], with_dout=True)
+    rows = {}
+    for name, ww in (("normed_backward", w),
+                     ("normed_backward_long", dataclasses.replace(w, B=1, H=16, n=n or 16384))):
+        x = inputs.make(ww, device=dev, seed=replica_seed(ww.seed, dist.rank))
+        q, k, v, do = x["q"], x["k"], x["v"], x["dout"]
+        gamma = x["gamma"].to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def one():
+            hla.backward(q, k, v, do, gamma=gamma, chunk=ww.chunk, normalize=True, eps=ww.eps, dq=dq, dk=dk, dv=dv)
+
+        long = name == "normed_backward_long"
+        ms = dist.max(_device_ms(one, max(1, steps // 5) if long else steps, warmup, torch.cuda.synchronize))
+        tokens = ww.B * ww.H * ww.n
+        nbytes = tokens * (4 * ww.d + 3 * ww.dv) * 2
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        rows[name] = {"workload": f"normalised backward: B={ww.B} H={ww.H} n={ww.n} d=dv={ww.d} bf16, softplus q/k, "
+                                  f"decay linspace{tuple(ww.gamma)}, eps {ww.eps}, chunk {ww.chunk}, float32 passes",
+                      "metric": "normalised bwd tokens/s", "unit": "tokens/s",
+                      "value": dist.world * tokens / (ms * 1e-3), "ms_per_step": ms,
+                      "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                                   "frac": achieved / hbm_gbs, "kernel": "whole call",
+                                   "algorithmic_bytes_per_step": nbytes}}
+    return rows
+
+
 def measure_ahla_backward(dev, dist: Dist, hbm_gbs: float, steps: int = 20, warmup: int = 3, n: int | None = None):
     """AHLA reverse-mode row: dq, dk, dv of the unnormalised AHLA output on the long-context
     shapes (B=1 H=16 n=65536 d=dv=64 bf16, decay linspace(0.99, 0.9999), chunk 128: the tcgen05
@@ -713,6 +755,8 @@ def run_only(args, dist: Dist, dev):
         row = measure_ahla_backward(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
     elif args.only == "normed":
         row = measure_normed(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
+    elif args.only == "normed_backward":
+        row = measure_normed_backward(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
     elif args.only == "prefill_d128":
         row = measure_prefill_d128(dev, dist, hbm_gbs, steps=args.steps, warmup=args.warmup, n=args.n)
     elif args.only == "train_d64":
@@ -854,6 +898,7 @@ def run_ours(args, dist: Dist):
                      "hla3": measure_hla3(dev, dist, hbm_gbs),
                      "prefill": measure_prefill(dev, dist, hbm_gbs)}
         secondary.update(measure_normed(dev, dist, hbm_gbs))
+        secondary.update(measure_normed_backward(dev, dist, hbm_gbs))
         secondary["prefill_d128"] = measure_prefill_d128(dev, dist, hbm_gbs)
 
     cpu = None

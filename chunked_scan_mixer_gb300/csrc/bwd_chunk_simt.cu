@@ -1,10 +1,9 @@
-// fp32 reverse-mode chunk kernel of the masked HLA-2 backward (SIMT): the same per-chunk
-// algebra as the bf16 tensor-core kernel (bwd_chunk_mma.cuh), written as plain loops in
-// float32 for float32 inputs of any d, dv in {16, 32, 64, 128}.  Gradients of the
-// unnormalised output, equal to those of the serial recurrence (page "Higher-order Linear
-// Attention", section summary §4.2: a reverse-mode scan reproduces the serial recurrence's
-// gradients).  With p_t = S_t q_t, Z_t = g^2 Z_{t-1} + p_t v_t^T, o_t = q_t^T Z_t the
-// adjoint is
+// float32 reverse-mode chunk kernel of the masked HLA-2 backward (SIMT): the same per-chunk
+// algebra as the bf16 tensor-core kernel (bwd_chunk_mma.cuh), in float32 for float32 inputs
+// of any d, dv in {16, 32, 64, 128}.  Gradients of the unnormalised output, equal to those of
+// the serial recurrence (page "Higher-order Linear Attention", section summary §4.2: a
+// reverse-mode scan reproduces the serial recurrence's gradients).  With p_t = S_t q_t,
+// Z_t = g^2 Z_{t-1} + p_t v_t^T, o_t = q_t^T Z_t the adjoint is
 //     Zh_t = q_t dO_t^T + g^2 Zh_{t+1},   dp_t = Zh_t v_t,   Sh_t = dp_t q_t^T + g Sh_{t+1}
 //     dq_t = Z_t dO_t + S_t dp_t,   dv_t = Zh_t^T p_t,   dk_t = (Sh_t + Sh_t^T) k_t
 // and per chunk (rows r < Wc, forward state S0, Z0 at the chunk start, reverse carries Zh,
@@ -17,168 +16,299 @@
 //   dQ[r]   = g^(r+1) (g^(r+1) Z0 dO_r + S0^T dP_r) + sum_j D~[r,j] p_j + sum_i dA~[r,i] k_i
 //   dK[i]   = g^(Wc-1-i) (Sh + Sh^T) k_i + sum_{r >= i} (A~[r,i] dP_r + dA~[r,i] q_r)
 //   Zh <- g^(2Wc) Zh + sum_r g^(2(r+1)) q_r dO_r^T,   Sh <- g^Wc Sh + sum_j g^(j+1) dP_j q_j^T
-// One CTA walks one segment's chunks from the last to the first.  The reverse carries live
-// in the workspace (the segment's slot, updated in place); the forward states S0, Z0 come
-// from the float32 state-export pass of the forward kernel.  RSUM mode starts from zero
-// carries and keeps only what the reverse scan needs (D~, dP and the carry updates).
+// One CTA walks one segment's chunks from the last to the first.  RSUM mode starts from zero
+// carries, keeps only what the reverse scan needs (D~, dP and the carry updates) and stores
+// the segment's (Zh, Sh).  The gradient pass starts from the carries at the segment end and
+// only ever needs Sh + Sh^T, so it carries that symmetric sum (its update is the symmetric
+// part of the one above, doubled).  The forward states S0, Z0 come from the float32
+// state-export pass of the forward kernel.  Every product runs through the register-tiled
+// helpers of simt_tile.cuh.
 #include "kernels.h"
+#include "simt_tile.cuh"
 
 namespace hla2 {
 
 namespace {
 
-constexpr int kBsThreads = 256;
+using simt::kThreads;
 
+// Shared-memory tiles (floats): the chunk's Q, K, V, dO, P, dP row-major with padded rows;
+// K^T, V^T, P^T, dP^T; the four W x W matrices; Z0^T; and, while they fit, the carries Zh
+// (row-major [D][DV]) and Sh (the symmetric sum in the gradient pass), else those stay in
+// their workspace slots.
 struct BsLayout {
-    size_t Q, K, V, O, P, dP, At, Dt, Bt, dAt, gp, total;
+    int ldD, ldV, ldW;
+    bool st_smem;
+    size_t Q, K, V, O, P, dP, Kt, Vt, Pt, dPt, At, Dt, Bt, dAt, Z0t, Zh, Sh, gp, total;
 };
 
 __host__ __device__ inline BsLayout bs_layout(int D, int DV, int W) {
     BsLayout L;
+    L.ldD = simt::pad(D);
+    L.ldV = simt::pad(DV);
+    L.ldW = simt::pad(W);
+    L.st_smem = (size_t)D * D <= 4096 && (size_t)D * DV <= 4096;
     size_t o = 0;
-    L.Q = o;   o += (size_t)W * D;
-    L.K = o;   o += (size_t)W * D;
-    L.V = o;   o += (size_t)W * DV;
-    L.O = o;   o += (size_t)W * DV;
-    L.P = o;   o += (size_t)W * D;
-    L.dP = o;  o += (size_t)W * D;
-    L.At = o;  o += (size_t)W * W;
-    L.Dt = o;  o += (size_t)W * W;
-    L.Bt = o;  o += (size_t)W * W;
-    L.dAt = o; o += (size_t)W * W;
+    L.Q = o;   o += (size_t)W * L.ldD;
+    L.K = o;   o += (size_t)W * L.ldD;
+    L.V = o;   o += (size_t)W * L.ldV;
+    L.O = o;   o += (size_t)W * L.ldV;
+    L.P = o;   o += (size_t)W * L.ldD;
+    L.dP = o;  o += (size_t)W * L.ldD;
+    L.Kt = o;  o += (size_t)D * L.ldW;
+    L.Vt = o;  o += (size_t)DV * L.ldW;
+    L.Pt = o;  o += (size_t)D * L.ldW;
+    L.dPt = o; o += (size_t)D * L.ldW;
+    L.At = o;  o += (size_t)W * L.ldW;
+    L.Dt = o;  o += (size_t)W * L.ldW;
+    L.Bt = o;  o += (size_t)W * L.ldW;
+    L.dAt = o; o += (size_t)W * L.ldW;
+    L.Z0t = o; o += (size_t)DV * L.ldD;
+    L.Zh = o;  o += L.st_smem ? (size_t)D * DV : 0;
+    L.Sh = o;  o += L.st_smem ? (size_t)D * D : 0;
     L.gp = o;  o += 2 * (size_t)W + 2;
     L.total = o;
     return L;
 }
 
+// M x M lower-triangular product into T: T[r][c] = [c <= r] gp[pw (r - c)] sum_k A(r, k) B(k, c)
+// with A row-major (lda) and B row-major over c (ldb).
+__device__ __forceinline__ void tri_gram(float* T, int ldt, const float* A, int lda, const float* B, int ldb, int M,
+                                         int K, const float* gp, int pw) {
+    simt::with_rm(M, M, [&](auto t) {
+        constexpr int RM = decltype(t)::value;
+        simt::for_blocks<RM>(M, M, [&](int m0, int n0) {
+            simt::Acc<RM> acc;
+            simt::zero(acc);
+            if (n0 < m0 + RM) simt::mac<RM>(acc, A + m0 * lda, lda, 1, B + n0, ldb, 0, K);
+#pragma unroll
+            for (int i = 0; i < RM; ++i) {
+                const int r = m0 + i;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[i][b] = n0 + b <= r ? gp[pw * (r - n0 - b)] * acc[i][b] : 0.f;
+                simt::st4(T + r * ldt + n0, acc[i]);
+            }
+        });
+    });
+}
+
 template <bool RSUM>
-__global__ void __launch_bounds__(kBsThreads) bwd_chunk_simt_kernel(const BwdArgsF a, int D, int DV) {
+__global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdArgsF a, int D, int DV) {
     extern __shared__ __align__(16) float sm[];
     const int W = a.W;
     const BsLayout L = bs_layout(D, DV, W);
+    const int ldD = L.ldD, ldV = L.ldV, ldW = L.ldW;
     float *Qs = sm + L.Q, *Ks = sm + L.K, *Vs = sm + L.V, *Os = sm + L.O, *Ps = sm + L.P, *dPs = sm + L.dP;
-    float *At = sm + L.At, *Dt = sm + L.Dt, *Bt = sm + L.Bt, *dAt = sm + L.dAt, *gp = sm + L.gp;
-    const int tid = threadIdx.x, NT = blockDim.x;
+    float *Kt = sm + L.Kt, *Vt = sm + L.Vt, *Pt = sm + L.Pt, *dPt = sm + L.dPt;
+    float *At = sm + L.At, *Dt = sm + L.Dt, *Bt = sm + L.Bt, *dAt = sm + L.dAt, *Z0t = sm + L.Z0t, *gp = sm + L.gp;
+    const int tid = threadIdx.x;
     const int seg = blockIdx.x, bh = blockIdx.y;
     const int c_begin = seg * a.seg_chunks;
     const int c_end = min(c_begin + a.seg_chunks, a.nchunks);
     const size_t hq = (size_t)bh * a.n;
     const float log2g = log2f(head_decay(a.gamma, bh, a.H));
-    for (int i = tid; i < 2 * W + 2; i += NT) gp[i] = pow_decay(log2g, (float)i);
+    for (int i = tid; i < 2 * W + 2; i += kThreads) gp[i] = pow_decay(log2g, (float)i);
 
+    // reverse carries: the segment's workspace slot, or shared memory while it fits
     const size_t sidx = (size_t)bh * a.nseg + seg;
-    float* Zh = a.ws + (RSUM ? a.ZhB : a.Zh_end) + sidx * D * DV;  // [D][DV], updated in place
-    float* Sh = a.ws + (RSUM ? a.ShB : a.Sh_end) + sidx * D * D;    // [D][D]
+    float* Zg = a.ws + (RSUM ? a.ZhB : a.Zh_end) + sidx * D * DV;  // [D][DV]
+    float* Sg = a.ws + (RSUM ? a.ShB : a.Sh_end) + sidx * D * D;    // [D][D]
+    float* Zh = L.st_smem ? sm + L.Zh : Zg;
+    float* Sh = L.st_smem ? sm + L.Sh : Sg;
     if (RSUM) {
-        for (int i = tid; i < D * DV; i += NT) Zh[i] = 0.f;
-        for (int i = tid; i < D * D; i += NT) Sh[i] = 0.f;
+        for (int i = tid; i < D * DV; i += kThreads) Zh[i] = 0.f;
+        for (int i = tid; i < D * D; i += kThreads) Sh[i] = 0.f;
+    } else {
+        if (L.st_smem)
+            for (int i = tid; i < D * DV; i += kThreads) Zh[i] = Zg[i];
+        // Sh + Sh^T, one thread per unordered pair (in place when it stays in the workspace)
+        for (int e = tid; e < D * D; e += kThreads) {
+            const int x = e / D, f = e - x * D;
+            if (f < x) continue;
+            const float s = Sg[x * D + f] + Sg[f * D + x];
+            Sh[x * D + f] = s;
+            Sh[f * D + x] = s;
+        }
     }
 
     for (int c = c_end - 1; c >= c_begin; --c) {
         const int row0 = c * W, Wc = min(W, a.n - row0);
         __syncthreads();  // the previous chunk's readers of the tiles and carries are done
-        for (int i = tid; i < W * D; i += NT) {
-            const int r = i / D;
+        for (int i = tid; i < W * D; i += kThreads) {
+            const int r = i / D, f = i - r * D;
             const bool in = r < Wc && HLA2_IN(row0 + r < a.n, 601);
-            Qs[i] = in ? a.q[(hq + row0) * D + i] : 0.f;
-            if (!RSUM) Ks[i] = in ? a.k[(hq + row0) * D + i] : 0.f;
+            Qs[r * ldD + f] = in ? a.q[(hq + row0) * D + i] : 0.f;
+            if (!RSUM) {
+                const float kx = in ? a.k[(hq + row0) * D + i] : 0.f;
+                Ks[r * ldD + f] = kx;
+                Kt[f * ldW + r] = kx;
+            }
         }
-        for (int i = tid; i < W * DV; i += NT) {
-            const int r = i / DV;
+        for (int i = tid; i < W * DV; i += kThreads) {
+            const int r = i / DV, x = i - r * DV;
             const bool in = r < Wc && HLA2_IN(row0 + r < a.n, 602);
-            Vs[i] = in ? a.v[(hq + row0) * DV + i] : 0.f;
-            Os[i] = in ? a.dout[(hq + row0) * DV + i] : 0.f;
+            const float vx = in ? a.v[(hq + row0) * DV + i] : 0.f;
+            Vt[x * ldW + r] = vx;
+            if (!RSUM) Vs[r * ldV + x] = vx;
+            Os[r * ldV + x] = in ? a.dout[(hq + row0) * DV + i] : 0.f;
         }
         const float* S0 = RSUM ? nullptr : a.chunk_states + ((size_t)bh * a.nchunks + c) * (size_t)(D * D + D * DV);
-        const float* Z0 = RSUM ? nullptr : S0 + (size_t)D * D;
-        __syncthreads();
-
-        // ---- phase 1: D~ (and A~) ---------------------------------------------------------
-        for (int e = tid; e < W * W; e += NT) {
-            const int r = e / W, j = e % W;
-            float sd = 0.f, sa = 0.f;
-            if (j <= r) {
-                for (int x = 0; x < DV; ++x) sd += Os[r * DV + x] * Vs[j * DV + x];
-                if (!RSUM)
-                    for (int x = 0; x < D; ++x) sa += Qs[r * D + x] * Ks[j * D + x];
+        if (!RSUM) {  // Z0^T (the forward exports Z0 row-major [D][DV])
+            const float* Z0 = S0 + (size_t)D * D;
+            for (int i = tid; i < D * DV; i += kThreads) {
+                const int x = i / D, f = i - x * D;
+                Z0t[x * ldD + f] = Z0[(size_t)f * DV + x];
             }
-            Dt[e] = j <= r ? gp[2 * (r - j)] * sd : 0.f;
-            if (!RSUM) At[e] = j <= r ? gp[r - j] * sa : 0.f;
         }
         __syncthreads();
 
-        // ---- phase 2: dP (and P) -------------------------------------------------------------
-        for (int e = tid; e < W * D; e += NT) {
-            const int j = e / D, f = e % D;
-            float s0 = 0.f, s1 = 0.f;
-            if (j < Wc)
-                for (int x = 0; x < DV; ++x) s0 += Vs[j * DV + x] * Zh[(size_t)f * DV + x];
-            for (int r = j; r < W; ++r) s1 += Dt[r * W + j] * Qs[r * D + f];
-            dPs[e] = (j < Wc ? gp[2 * (Wc - 1 - j)] * s0 : 0.f) + s1;
-            if (!RSUM) {
-                float p0 = 0.f, p1 = 0.f;
-                for (int x = 0; x < D; ++x) p0 += Qs[j * D + x] * S0[(size_t)x * D + f];
-                for (int i = 0; i <= j; ++i) p1 += At[j * W + i] * Ks[i * D + f];
-                Ps[e] = gp[j + 1] * p0 + p1;
-            }
+        // ---- D~ (and A~) -----------------------------------------------------------------
+        tri_gram(Dt, ldW, Os, ldV, Vt, ldW, W, DV, gp, 2);
+        if (!RSUM) tri_gram(At, ldW, Qs, ldD, Kt, ldW, W, D, gp, 1);
+        __syncthreads();
+
+        // ---- dP^T[f][j] = g^(2(Wc-1-j)) (Zh V^T)[f][j] + sum_{r >= j} q_r[f] D~[r][j] ---------
+        simt::with_rm(D, W, [&](auto t) {
+            constexpr int RM = decltype(t)::value;
+            simt::for_blocks<RM>(D, W, [&](int m0, int n0) {
+                simt::Acc<RM> acc;
+                simt::zero(acc);
+                simt::mac<RM>(acc, Zh + m0 * DV, DV, 1, Vt + n0, ldW, 0, DV);
+                float cw[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) cw[b] = n0 + b < Wc ? gp[2 * (Wc - 1 - n0 - b)] : 0.f;
+#pragma unroll
+                for (int i = 0; i < RM; ++i)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[i][b] *= cw[b];
+                simt::mac<RM>(acc, Qs + m0, 1, ldD, Dt + n0, ldW, n0, W);
+#pragma unroll
+                for (int i = 0; i < RM; ++i) {
+                    simt::st4(dPt + (m0 + i) * ldW + n0, acc[i]);
+                    if (!RSUM) {
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) dPs[(n0 + b) * ldD + m0 + i] = acc[i][b];
+                    }
+                }
+            });
+        });
+        // ---- P = diag(g^(j+1)) Q S0 + A~ K -------------------------------------------------
+        if (!RSUM) {
+            simt::with_rm(W, D, [&](auto t) {
+                constexpr int RM = decltype(t)::value;
+                simt::for_blocks<RM>(W, D, [&](int m0, int n0) {
+                    simt::Acc<RM> acc;
+                    simt::zero(acc);
+                    simt::mac<RM>(acc, Qs + m0 * ldD, ldD, 1, S0 + n0, D, 0, D);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) simt::scale_row(acc, i, gp[m0 + i + 1]);
+                    simt::mac<RM>(acc, At + m0 * ldW, ldW, 1, Ks + n0, ldD, 0, min(W, m0 + RM));
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) {
+                        simt::st4(Ps + (m0 + i) * ldD + n0, acc[i]);
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) Pt[(n0 + b) * ldW + m0 + i] = acc[i][b];
+                    }
+                });
+            });
         }
         __syncthreads();
 
         if (!RSUM) {
-            // ---- phase 3: B~, dA~ ----------------------------------------------------------------
-            for (int e = tid; e < W * W; e += NT) {
-                const int r = e / W, j = e % W;
-                float sb = 0.f, sa = 0.f;
-                if (j <= r)
-                    for (int x = 0; x < D; ++x) {
-                        sb += Qs[r * D + x] * Ps[j * D + x];
-                        sa += dPs[r * D + x] * Ks[j * D + x];
-                    }
-                Bt[e] = j <= r ? gp[2 * (r - j)] * sb : 0.f;
-                dAt[e] = j <= r ? gp[r - j] * sa : 0.f;
-            }
+            // ---- B~, dA~ ---------------------------------------------------------------------
+            tri_gram(Bt, ldW, Qs, ldD, Pt, ldW, W, D, gp, 2);
+            tri_gram(dAt, ldW, dPs, ldD, Kt, ldW, W, D, gp, 1);
             __syncthreads();
 
-            // ---- phase 4: dV, dQ, dK -> global ---------------------------------------------------
-            for (int e = tid; e < Wc * DV; e += NT) {
-                const int j = e / DV, x = e % DV;
-                float s0 = 0.f, s1 = 0.f;
-                for (int f = 0; f < D; ++f) s0 += Ps[j * D + f] * Zh[(size_t)f * DV + x];
-                for (int r = j; r < Wc; ++r) s1 += Bt[r * W + j] * Os[r * DV + x];
-                if (HLA2_IN(row0 + j < a.n, 603)) a.dv[(hq + row0) * DV + e] = gp[2 * (Wc - 1 - j)] * s0 + s1;
-            }
-            for (int e = tid; e < Wc * D; e += NT) {
-                const int r = e / D, f = e % D;
-                float sz = 0.f, ss = 0.f, sp = 0.f;
-                for (int x = 0; x < DV; ++x) sz += Os[r * DV + x] * Z0[(size_t)f * DV + x];
-                for (int x = 0; x < D; ++x) ss += dPs[r * D + x] * S0[(size_t)x * D + f];
-                for (int j = 0; j <= r; ++j) sp += Dt[r * W + j] * Ps[j * D + f] + dAt[r * W + j] * Ks[j * D + f];
-                if (HLA2_IN(row0 + r < a.n, 604)) a.dq[(hq + row0) * D + e] = gp[r + 1] * (gp[r + 1] * sz + ss) + sp;
-            }
-            for (int e = tid; e < Wc * D; e += NT) {
-                const int i = e / D, f = e % D;
-                float sh = 0.f, sr = 0.f;
-                for (int x = 0; x < D; ++x) sh += Ks[i * D + x] * (Sh[(size_t)x * D + f] + Sh[(size_t)f * D + x]);
-                for (int r = i; r < Wc; ++r) sr += At[r * W + i] * dPs[r * D + f] + dAt[r * W + i] * Qs[r * D + f];
-                if (HLA2_IN(row0 + i < a.n, 605)) a.dk[(hq + row0) * D + e] = gp[Wc - 1 - i] * sh + sr;
-            }
+            // ---- dV, dQ, dK -> global ----------------------------------------------------------
+            simt::with_rm(W, DV, [&](auto t) {
+                constexpr int RM = decltype(t)::value;
+                simt::for_blocks<RM>(W, DV, [&](int m0, int n0) {
+                    if (m0 >= Wc) return;
+                    simt::Acc<RM> acc;
+                    simt::zero(acc);
+                    simt::mac<RM>(acc, Ps + m0 * ldD, ldD, 1, Zh + n0, DV, 0, D);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i)
+                        simt::scale_row(acc, i, m0 + i < Wc ? gp[2 * (Wc - 1 - m0 - i)] : 0.f);
+                    simt::mac<RM>(acc, Bt + m0, 1, ldW, Os + n0, ldV, m0, W);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i)
+                        if (m0 + i < Wc && HLA2_IN(row0 + m0 + i < a.n, 603))
+                            simt::st4(a.dv + (hq + row0 + m0 + i) * DV + n0, acc[i]);
+                });
+            });
+            simt::with_rm(W, D, [&](auto t) {
+                constexpr int RM = decltype(t)::value;
+                simt::for_blocks<RM>(W, D, [&](int m0, int n0) {
+                    if (m0 >= Wc) return;
+                    const int kr = min(W, m0 + RM);
+                    simt::Acc<RM> acc;
+                    simt::zero(acc);
+                    simt::mac<RM>(acc, Os + m0 * ldV, ldV, 1, Z0t + n0, ldD, 0, DV);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) simt::scale_row(acc, i, gp[m0 + i + 1]);
+                    simt::mac<RM>(acc, dPs + m0 * ldD, ldD, 1, S0 + n0, D, 0, D);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) simt::scale_row(acc, i, gp[m0 + i + 1]);
+                    simt::mac<RM>(acc, Dt + m0 * ldW, ldW, 1, Ps + n0, ldD, 0, kr);
+                    simt::mac<RM>(acc, dAt + m0 * ldW, ldW, 1, Ks + n0, ldD, 0, kr);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i)
+                        if (m0 + i < Wc && HLA2_IN(row0 + m0 + i < a.n, 604))
+                            simt::st4(a.dq + (hq + row0 + m0 + i) * D + n0, acc[i]);
+                });
+            });
+            simt::with_rm(W, D, [&](auto t) {
+                constexpr int RM = decltype(t)::value;
+                simt::for_blocks<RM>(W, D, [&](int m0, int n0) {
+                    if (m0 >= Wc) return;
+                    simt::Acc<RM> acc;
+                    simt::zero(acc);
+                    simt::mac<RM>(acc, Ks + m0 * ldD, ldD, 1, Sh + n0, D, 0, D);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i)
+                        simt::scale_row(acc, i, m0 + i < Wc ? gp[Wc - 1 - m0 - i] : 0.f);
+                    simt::mac<RM>(acc, At + m0, 1, ldW, dPs + n0, ldD, m0, W);
+                    simt::mac<RM>(acc, dAt + m0, 1, ldW, Qs + n0, ldD, m0, W);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i)
+                        if (m0 + i < Wc && HLA2_IN(row0 + m0 + i < a.n, 605))
+                            simt::st4(a.dk + (hq + row0 + m0 + i) * D + n0, acc[i]);
+                });
+            });
             __syncthreads();  // every read of the carries is done before they move
         }
 
-        // ---- carries to the chunk start (each element owned by one thread) -----------------
+        // ---- carries to the chunk start (each block owned by one thread) ---------------------
         const float rho = gp[Wc], rho2 = gp[2 * Wc];
-        for (int e = tid; e < D * DV; e += NT) {
-            const int f = e / DV, x = e % DV;
-            float s = 0.f;
-            for (int r = 0; r < Wc; ++r) s += gp[2 * (r + 1)] * Qs[r * D + f] * Os[r * DV + x];
-            Zh[e] = rho2 * Zh[e] + s;
-        }
-        for (int e = tid; e < D * D; e += NT) {
-            const int f = e / D, x = e % D;
-            float s = 0.f;
-            for (int j = 0; j < Wc; ++j) s += gp[j + 1] * dPs[j * D + f] * Qs[j * D + x];
-            Sh[e] = rho * Sh[e] + s;
-        }
+        simt::with_rm(D, DV, [&](auto t) {
+            constexpr int RM = decltype(t)::value;
+            simt::for_blocks<RM>(D, DV, [&](int m0, int n0) {
+                simt::Acc<RM> acc;
+                simt::zero(acc);
+                simt::mac_w<RM>(acc, Qs + m0, 1, ldD, Os + n0, ldV, 0, Wc, [&](int r) { return gp[2 * (r + 1)]; });
+#pragma unroll
+                for (int i = 0; i < RM; ++i) simt::decay_add4(Zh + (m0 + i) * DV + n0, rho2, acc[i]);
+            });
+        });
+        simt::with_rm(D, D, [&](auto t) {
+            constexpr int RM = decltype(t)::value;
+            simt::for_blocks<RM>(D, D, [&](int m0, int n0) {
+                simt::Acc<RM> acc;
+                simt::zero(acc);
+                auto wj = [&](int j) { return gp[j + 1]; };
+                simt::mac_w<RM>(acc, dPt + m0 * ldW, ldW, 1, Qs + n0, ldD, 0, Wc, wj);
+                if (!RSUM) simt::mac_w<RM>(acc, Qs + m0, 1, ldD, dPs + n0, ldD, 0, Wc, wj);
+#pragma unroll
+                for (int i = 0; i < RM; ++i) simt::decay_add4(Sh + (m0 + i) * D + n0, rho, acc[i]);
+            });
+        });
+    }
+    if (RSUM && L.st_smem) {
+        __syncthreads();
+        for (int i = tid; i < D * DV; i += kThreads) Zg[i] = Zh[i];
+        for (int i = tid; i < D * D; i += kThreads) Sg[i] = Sh[i];
     }
 }
 
@@ -188,11 +318,12 @@ size_t bwd_chunk_simt_smem(int d, int dv, int W) { return bs_layout(d, dv, W).to
 
 int launch_bwd_chunk_simt(const BwdArgsF& a, int d, int dv, bool rsum, cudaStream_t st) {
     if (a.nseg <= 0 || a.BH <= 0) return 0;
+    if ((d & 15) || (dv & 15) || (a.W & 15)) return -1;
     const size_t smem = bwd_chunk_simt_smem(d, dv, a.W);
     auto kfn = rsum ? bwd_chunk_simt_kernel<true> : bwd_chunk_simt_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return -1;
-    kfn<<<dim3(a.nseg, a.BH), kBsThreads, smem, st>>>(a, d, dv);
+    kfn<<<dim3(a.nseg, a.BH), kThreads, smem, st>>>(a, d, dv);
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

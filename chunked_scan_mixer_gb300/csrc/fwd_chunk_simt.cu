@@ -1,50 +1,94 @@
-// SIMT chunk kernel of the masked HLA-2 forward: fp32 arithmetic on shared-memory
-// tiles, runtime shapes.  Same per-chunk algebra as the tensor-core kernel
-// (fwd_chunk_mma.cuh), written as plain loops; it serves float32 inputs (where bf16
-// tensor-core operands would not meet a 1e-4 relative error) and bf16 shapes the
-// tensor-core kernel does not cover.  With a.unmasked it computes the unmasked output
-// q^T S C (section summary §3, §4.1): Z and y then hold C and m, the second product is
-// (P Q^T) * [j <= r] g^(r-j), and the carry term is g^(r+1) P C0.
+// SIMT chunk kernel of the masked HLA-2 forward: float32 arithmetic on shared-memory
+// tiles, runtime shapes.  Same per-chunk algebra as the tensor-core kernels
+// (fwd_chunk_mma.cuh); it serves float32 inputs (where bf16 tensor-core operands would not
+// meet a 1e-4 relative error) and bf16 shapes the tensor-core kernels do not cover.  With
+// a.unmasked it computes the unmasked output q^T S C (section summary §3, §4.1): Z and y
+// then hold C and m, the second product is (P Q^T) * [j <= r] g^(r-j), and the carry term
+// is g^(r+1) P C0.
+//
+// Per chunk of width W (rows r < Wc, state S0, Z0, y0 at the chunk start, g the decay):
+//   A~[r, i] = [i <= r] g^(r-i) q_r . k_i
+//   P        = diag(g^(r+1)) Q S0 + A~ K                       (p_r = S_r q_r)
+//   B~[r, j] = [j <= r] g^(2(r-j)) q_r . p_j
+//   O        = diag(g^(2(r+1))) Q Z0 + B~ V                    (o_r = Z_r^T q_r)
+//   den_r    = g^(2(r+1)) q_r . y0 + sum_j B~[r, j]           (normalised: o_r / (den_r + eps))
+//   S <- g^Wc S0 + K~^T K,  Z <- g^(2Wc) Z0 + P~^T V,  y <- g^(2Wc) y0 + sum_j g^(2(Wc-1-j)) p_j
+// with K~, P~ the rows scaled by their decay to the chunk end; C and m (summaries and the
+// final state) take q v^T and q with decay g.  Every product runs through the register-tiled
+// helpers of simt_tile.cuh: a thread owns an RM x 4 block of the output.
 #include "kernels.h"
+#include "simt_tile.cuh"
 
 namespace hla2 {
 
 namespace {
 
+using simt::kThreads;
+
+// Shared-memory tiles (floats).  Q, K, V, P row-major with padded rows; T holds K^T for the
+// key Gram, then P^T (masked) or Q^T (unmasked) for the second Gram; AB holds A~, then B~.
+// S and Z (and C for small states) are row-major without padding: they are read only as the
+// B operand of a product, or updated by the thread that owns a block.
 struct SimtLayout {
-    size_t Q, K, V, AB, P, S, Z, C, y, m, gp, den, total;
+    int ldD, ldV, ldW;
+    bool c_smem;
+    size_t Q, K, T, V, AB, P, S, Z, C, y, m, den, gp, total;
 };
 
 __host__ __device__ inline SimtLayout simt_layout(int D, int DV, int W, bool cm) {
     SimtLayout L;
+    L.ldD = simt::pad(D);
+    L.ldV = simt::pad(DV);
+    L.ldW = simt::pad(W);
+    L.c_smem = cm && (size_t)D * DV <= 4096;
     size_t o = 0;
-    L.Q = o; o += (size_t)W * D;
-    L.K = o; o += (size_t)W * D;
-    L.V = o; o += (size_t)W * DV;
-    L.AB = o; o += (size_t)W * W;
-    L.P = o; o += (size_t)W * D;
-    L.S = o; o += (size_t)D * D;
-    L.Z = o; o += (size_t)D * DV;
-    L.C = o; o += cm ? (size_t)D * DV : 0;
-    L.y = o; o += D;
-    L.m = o; o += D;
-    L.gp = o; o += 2 * (size_t)W + 2;
+    L.Q = o;   o += (size_t)W * L.ldD;
+    L.K = o;   o += (size_t)W * L.ldD;
+    L.T = o;   o += (size_t)D * L.ldW;
+    L.V = o;   o += (size_t)W * L.ldV;
+    L.AB = o;  o += (size_t)W * L.ldW;
+    L.P = o;   o += (size_t)W * L.ldD;
+    L.S = o;   o += (size_t)D * D;
+    L.Z = o;   o += (size_t)D * DV;
+    L.C = o;   o += L.c_smem ? (size_t)D * DV : 0;
+    L.y = o;   o += D;
+    L.m = o;   o += D;
     L.den = o; o += W;
+    L.gp = o;  o += 2 * (size_t)W + 2;
     L.total = o;
     return L;
 }
 
-constexpr int kSimtThreads = 256;
+template <typename T>
+__device__ __forceinline__ void load4(const T* p, float (&r)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&r)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    r[0] = v.x;
+    r[1] = v.y;
+    r[2] = v.z;
+    r[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void load4<bf16>(const bf16* p, float (&r)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+    r[0] = __low2float(a);
+    r[1] = __high2float(a);
+    r[2] = __low2float(b);
+    r[3] = __high2float(b);
+}
 
 template <typename T>
-__global__ void __launch_bounds__(kSimtThreads)
+__global__ void __launch_bounds__(kThreads)
     fwd_chunk_simt_kernel(const ChunkArgs a, int D, int DV, int W, int summary, int cm) {
     extern __shared__ __align__(16) float sm[];
     const SimtLayout L = simt_layout(D, DV, W, cm != 0);
-    float *Qs = sm + L.Q, *Ks = sm + L.K, *Vs = sm + L.V, *AB = sm + L.AB, *Ps = sm + L.P;
-    float *S = sm + L.S, *Z = sm + L.Z, *C = sm + L.C, *y = sm + L.y, *m = sm + L.m;
-    float *gp = sm + L.gp, *den = sm + L.den;
-    const int tid = threadIdx.x, NT = blockDim.x;
+    const int ldD = L.ldD, ldV = L.ldV, ldW = L.ldW;
+    float *Qs = sm + L.Q, *Ks = sm + L.K, *Ts = sm + L.T, *Vs = sm + L.V, *AB = sm + L.AB, *Ps = sm + L.P;
+    float *S = sm + L.S, *Z = sm + L.Z, *y = sm + L.y, *m = sm + L.m, *den = sm + L.den, *gp = sm + L.gp;
+    const int tid = threadIdx.x;
     const int seg = a.seg0 + blockIdx.x, bh = blockIdx.y, nseg = a.nseg;
     const int c_begin = seg * a.seg_chunks;
     const int c_end = min(c_begin + a.seg_chunks, a.nchunks);
@@ -52,149 +96,19 @@ __global__ void __launch_bounds__(kSimtThreads)
     const T* k = static_cast<const T*>(a.k) + (size_t)bh * a.n * D;
     const T* v = static_cast<const T*>(a.v) + (size_t)bh * a.n * DV;
     const bool um = a.unmasked != 0;
-    const bool need_p = !(summary && um);  // the unmasked summary needs no p
-    const int bp = um ? 1 : 2;             // decay power of the second scan
+    const bool need_p = !(summary && um);          // the unmasked summary needs no p
+    const bool out_pass = !summary && a.out != nullptr;
+    const bool norm = out_pass && a.normalize;
+    const int bp = um ? 1 : 2;                     // decay power of the second scan
+    // The final raw state is written by the last segment of an output pass that wants it.
+    const bool final_seg = !summary && (cm || um) && seg == nseg - 1 && a.want_final;
+    // C (masked only) is kept where it is written: summaries and the final state.
+    const bool keep_c = cm && (summary || final_seg);
 
     const float log2g = log2f(head_decay(a.gamma, bh, a.H));
-    for (int i = tid; i < 2 * W + 2; i += NT) gp[i] = pow_decay(log2g, (float)i);
+    for (int i = tid; i < 2 * W + 2; i += kThreads) gp[i] = pow_decay(log2g, (float)i);
 
-    // initial state: zero (summary) or the segment's carry-in
-    const size_t sidx = (size_t)bh * nseg + seg;
-    auto wsr = [&](size_t idx, int site) { return HLA2_IN(idx < a.L.total, site) ? a.ws[idx] : 0.f; };
-    for (int i = tid; i < D * D; i += NT) S[i] = summary ? 0.f : wsr(a.L.Sin + sidx * D * D + i, 201);
-    for (int i = tid; i < D * DV; i += NT) {
-        Z[i] = summary ? 0.f : wsr(a.L.Zin + sidx * D * DV + i, 202);
-        if (cm) C[i] = summary ? 0.f : wsr(a.L.Clast + (size_t)bh * D * DV + i, 203);
-    }
-    for (int i = tid; i < D; i += NT) {
-        y[i] = summary ? 0.f : wsr(a.L.yin + sidx * D + i, 204);
-        m[i] = (cm && !summary) ? wsr(a.L.mlast + (size_t)bh * D + i, 205) : 0.f;
-    }
-
-    for (int c = c_begin; c < c_end; ++c) {
-        const int row0 = c * W;
-        const int Wc = min(W, a.n - row0);
-        __syncthreads();
-        if (!summary && a.chunk_states_f32) {  // the state at this chunk start, for the backward
-            const size_t cs = (size_t)(D * D + D * DV), base = ((size_t)bh * a.nchunks + c) * cs;
-            float* dst = a.chunk_states_f32 + base;
-            const bool ok = HLA2_IN(bh < a.BH && c < a.nchunks && base + cs <= (size_t)a.BH * a.nchunks * cs, 206);
-            for (int i = tid; ok && i < D * D; i += NT) dst[i] = S[i];
-            for (int i = tid; ok && i < D * DV; i += NT) dst[(size_t)D * D + i] = Z[i];
-        }
-        for (int i = tid; i < W * D; i += NT) {
-            const int r = i / D;
-            const bool in = r < Wc && HLA2_IN((size_t)row0 * D + i < (size_t)a.n * D, 207);
-            Qs[i] = in ? to_f32(q[(size_t)row0 * D + i]) : 0.f;
-            Ks[i] = in ? to_f32(k[(size_t)row0 * D + i]) : 0.f;
-        }
-        for (int i = tid; i < W * DV; i += NT)
-            Vs[i] = ((i / DV) < Wc && HLA2_IN((size_t)row0 * DV + i < (size_t)a.n * DV, 208))
-                        ? to_f32(v[(size_t)row0 * DV + i]) : 0.f;
-        __syncthreads();
-
-        // A~[r, i] = [i <= r] g^(r-i) q_r . k_i ; den carry term
-        for (int e = tid; need_p && e < W * W; e += NT) {
-            const int r = e / W, i = e % W;
-            float s = 0.f;
-            if (i <= r)
-                for (int f = 0; f < D; ++f) s += Qs[r * D + f] * Ks[i * D + f];
-            AB[e] = i <= r ? gp[r - i] * s : 0.f;
-        }
-        if (!summary && a.normalize && !um) {
-            for (int r = tid; r < W; r += NT) {
-                float s = 0.f;
-                for (int f = 0; f < D; ++f) s += Qs[r * D + f] * y[f];
-                den[r] = gp[2 * (r + 1)] * s;
-            }
-        }
-        __syncthreads();
-
-        // P = diag(g^(r+1)) Q S0 + A~ K
-        for (int e = tid; need_p && e < W * D; e += NT) {
-            const int r = e / D, f = e % D;
-            float s0 = 0.f, s1 = 0.f;
-            for (int x = 0; x < D; ++x) s0 += Qs[r * D + x] * S[x * D + f];
-            for (int i = 0; i <= r; ++i) s1 += AB[r * W + i] * Ks[i * D + f];
-            Ps[e] = gp[r + 1] * s0 + s1;
-        }
-        __syncthreads();
-
-        if (!summary && a.out) {
-            if (um && a.normalize) {  // unmasked denominator carry g^(r+1) p_r . m0
-                for (int r = tid; r < W; r += NT) {
-                    float s = 0.f;
-                    for (int f = 0; f < D; ++f) s += Ps[r * D + f] * y[f];
-                    den[r] = gp[r + 1] * s;
-                }
-            }
-            // B~[r, j] = [j <= r] g^(2(r-j)) q_r . p_j   (unmasked: g^(r-j) p_r . q_j)
-            for (int e = tid; e < W * W; e += NT) {
-                const int r = e / W, j = e % W;
-                float s = 0.f;
-                if (j <= r) {
-                    const float* x0 = um ? Ps + r * D : Qs + r * D;
-                    const float* x1 = um ? Qs + j * D : Ps + j * D;
-                    for (int f = 0; f < D; ++f) s += x0[f] * x1[f];
-                }
-                AB[e] = j <= r ? gp[bp * (r - j)] * s : 0.f;
-            }
-            __syncthreads();
-            if (a.normalize) {
-                for (int r = tid; r < W; r += NT) {
-                    float s = 0.f;
-                    for (int j = 0; j <= r; ++j) s += AB[r * W + j];
-                    den[r] += s;
-                }
-                __syncthreads();
-            }
-            // O = diag(g^(2(r+1))) Q Z0 + B~ V   (unmasked: diag(g^(r+1)) P C0 + B~ V)
-            T* out = static_cast<T*>(a.out) + ((size_t)bh * a.n + row0) * DV;
-            const float* lhs = um ? Ps : Qs;
-            for (int e = tid; e < Wc * DV; e += NT) {
-                const int r = e / DV, x = e % DV;
-                float s0 = 0.f, s1 = 0.f;
-                for (int f = 0; f < D; ++f) s0 += lhs[r * D + f] * Z[f * DV + x];
-                for (int j = 0; j <= r; ++j) s1 += AB[r * W + j] * Vs[j * DV + x];
-                float o = gp[bp * (r + 1)] * s0 + s1;
-                if (a.normalize) o /= (den[r] + a.eps);
-                if (HLA2_IN(row0 + r < a.n && bh < a.BH, 209)) out[e] = from_f32<T>(o);
-            }
-            __syncthreads();
-        }
-
-        // state updates (each element owned by one thread); unmasked, Z and y take the
-        // query-value and query-mass increments with decay g
-        const float rho = gp[Wc], rho2 = gp[bp * Wc];
-        const float* zl = um ? Qs : Ps;  // left factor of the Z and y increments
-        for (int e = tid; e < D * D; e += NT) {
-            const int x = e / D, f = e % D;
-            float s = 0.f;
-            for (int i = 0; i < Wc; ++i) s += gp[Wc - 1 - i] * Ks[i * D + x] * Ks[i * D + f];
-            S[e] = rho * S[e] + s;
-        }
-        for (int e = tid; e < D * DV; e += NT) {
-            const int x = e / DV, f = e % DV;
-            float s = 0.f, sc = 0.f;
-            for (int j = 0; j < Wc; ++j) {
-                s += gp[bp * (Wc - 1 - j)] * zl[j * D + x] * Vs[j * DV + f];
-                if (cm) sc += gp[Wc - 1 - j] * Qs[j * D + x] * Vs[j * DV + f];
-            }
-            Z[e] = rho2 * Z[e] + s;
-            if (cm) C[e] = rho * C[e] + sc;
-        }
-        for (int x = tid; x < D; x += NT) {
-            float s = 0.f, sm_ = 0.f;
-            for (int j = 0; j < Wc; ++j) {
-                s += gp[bp * (Wc - 1 - j)] * zl[j * D + x];
-                sm_ += gp[Wc - 1 - j] * Qs[j * D + x];
-            }
-            y[x] = rho2 * y[x] + s;
-            m[x] = rho * m[x] + sm_;
-        }
-    }
-    __syncthreads();
-
+    // destination of the summaries or of the final state (also where a large C accumulates)
     float *dS = nullptr, *dC = nullptr, *dZ = nullptr, *dm = nullptr, *dy = nullptr;
     if (summary) {
         const size_t si = (size_t)bh * a.nsum + seg;
@@ -203,7 +117,7 @@ __global__ void __launch_bounds__(kSimtThreads)
         dZ = a.ws + a.L.ZB + si * D * DV;
         dm = a.ws + a.L.mB + si * D;
         dy = a.ws + a.L.yB + si * D;
-    } else if ((cm || um) && seg == nseg - 1 && a.want_final) {
+    } else if (final_seg) {
         const RawOff ro = raw_off(D, DV);
         float* base = a.ws + a.L.fin + (size_t)bh * raw_state_floats(D, DV);
         dS = base + ro.S;
@@ -212,13 +126,240 @@ __global__ void __launch_bounds__(kSimtThreads)
         dm = base + ro.m;
         dy = base + ro.y;
     }
-    if (dS && HLA2_IN((size_t)(dy + D - a.ws) <= a.L.total && dS >= a.ws, 210)) {
-        for (int i = tid; i < D * D; i += NT) dS[i] = S[i];
-        for (int i = tid; i < D * DV; i += NT) {
-            dZ[i] = Z[i];
-            if (cm) dC[i] = C[i];
+    const bool dst_ok = dS && HLA2_IN((size_t)(dy + D - a.ws) <= a.L.total && dS >= a.ws, 210);
+    float* C = L.c_smem ? sm + L.C : dC;  // row-major [D][DV]
+    const bool track_c = keep_c && (L.c_smem || dst_ok);
+
+    // initial state: zero (summary) or the segment's carry-in
+    const size_t sidx = (size_t)bh * nseg + seg;
+    auto wsr = [&](size_t idx, int site) { return HLA2_IN(idx < a.L.total, site) ? a.ws[idx] : 0.f; };
+    for (int i = tid; i < D * D; i += kThreads) S[i] = summary ? 0.f : wsr(a.L.Sin + sidx * D * D + i, 201);
+    for (int i = tid; i < D * DV; i += kThreads) {
+        Z[i] = summary ? 0.f : wsr(a.L.Zin + sidx * D * DV + i, 202);
+        if (track_c) C[i] = summary ? 0.f : wsr(a.L.Clast + (size_t)bh * D * DV + i, 203);
+    }
+    for (int i = tid; i < D; i += kThreads) {
+        y[i] = summary ? 0.f : wsr(a.L.yin + sidx * D + i, 204);
+        m[i] = (!summary && keep_c) ? wsr(a.L.mlast + (size_t)bh * D + i, 205) : 0.f;
+    }
+
+    for (int c = c_begin; c < c_end; ++c) {
+        const int row0 = c * W;
+        const int Wc = min(W, a.n - row0);
+        __syncthreads();  // the previous chunk's state updates are done
+        if (!summary && a.chunk_states_f32) {  // the state at this chunk start, for the backward
+            const size_t cs = (size_t)(D * D + D * DV), base = ((size_t)bh * a.nchunks + c) * cs;
+            float* dst = a.chunk_states_f32 + base;
+            if (HLA2_IN(bh < a.BH && c < a.nchunks && base + cs <= (size_t)a.BH * a.nchunks * cs, 206)) {
+                for (int i = tid; i < (D * D) / 4; i += kThreads)
+                    reinterpret_cast<float4*>(dst)[i] = reinterpret_cast<const float4*>(S)[i];
+                for (int i = tid; i < (D * DV) / 4; i += kThreads)
+                    reinterpret_cast<float4*>(dst + (size_t)D * D)[i] = reinterpret_cast<const float4*>(Z)[i];
+            }
         }
-        for (int i = tid; i < D; i += NT) {
+        // tiles of this chunk (rows past the end are zero); K^T beside K for the key Gram
+        for (int i = tid; i < W * D; i += kThreads) {
+            const int r = i / D, f = i - r * D;
+            const bool in = r < Wc && HLA2_IN((size_t)row0 * D + i < (size_t)a.n * D, 207);
+            const float qx = in ? to_f32(q[(size_t)row0 * D + i]) : 0.f;
+            const float kx = in ? to_f32(k[(size_t)row0 * D + i]) : 0.f;
+            Qs[r * ldD + f] = qx;
+            Ks[r * ldD + f] = kx;
+            if (need_p) Ts[f * ldW + r] = kx;
+        }
+        for (int i = tid; i < (W * DV) / 4; i += kThreads) {
+            const int r = (4 * i) / DV, x = 4 * i - r * DV;
+            float t[4] = {0.f, 0.f, 0.f, 0.f};
+            if (r < Wc && HLA2_IN((size_t)row0 * DV + 4 * i + 4 <= (size_t)a.n * DV, 208))
+                load4<T>(v + (size_t)row0 * DV + 4 * i, t);
+            simt::st4(Vs + r * ldV + x, t);
+        }
+        __syncthreads();
+
+        // A~ = (Q K^T) * [i <= r] g^(r-i); masked denominator carry g^(2(r+1)) q_r . y0
+        if (need_p) {
+            simt::with_rm(W, W, [&](auto t) {
+                constexpr int RM = decltype(t)::value;
+                simt::for_blocks<RM>(W, W, [&](int m0, int n0) {
+                    simt::Acc<RM> acc;
+                    simt::zero(acc);
+                    if (n0 < m0 + RM) simt::mac<RM>(acc, Qs + m0 * ldD, ldD, 1, Ts + n0, ldW, 0, D);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) {
+                        const int r = m0 + i;
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) acc[i][b] = n0 + b <= r ? gp[r - n0 - b] * acc[i][b] : 0.f;
+                        simt::st4(AB + r * ldW + n0, acc[i]);
+                    }
+                });
+            });
+        }
+        if (norm && !um) {
+            for (int r = tid; r < W; r += kThreads) {
+                float s = 0.f;
+                for (int f = 0; f < D; ++f) s = fmaf(Qs[r * ldD + f], y[f], s);
+                den[r] = gp[2 * (r + 1)] * s;
+            }
+        }
+        __syncthreads();
+
+        // P = diag(g^(r+1)) Q S0 + A~ K; P^T (masked output pass) or Q^T (unmasked) into T
+        if (need_p) {
+            simt::with_rm(W, D, [&](auto t) {
+                constexpr int RM = decltype(t)::value;
+                simt::for_blocks<RM>(W, D, [&](int m0, int n0) {
+                    simt::Acc<RM> acc;
+                    simt::zero(acc);
+                    simt::mac<RM>(acc, Qs + m0 * ldD, ldD, 1, S + n0, D, 0, D);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) simt::scale_row(acc, i, gp[m0 + i + 1]);
+                    simt::mac<RM>(acc, AB + m0 * ldW, ldW, 1, Ks + n0, ldD, 0, min(W, m0 + RM));
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) {
+                        simt::st4(Ps + (m0 + i) * ldD + n0, acc[i]);
+                        if (out_pass && !um) {
+#pragma unroll
+                            for (int b = 0; b < 4; ++b) Ts[(n0 + b) * ldW + m0 + i] = acc[i][b];
+                        }
+                    }
+                });
+            });
+        }
+        if (out_pass && um)
+            for (int i = tid; i < W * D; i += kThreads) {
+                const int r = i / D, f = i - r * D;
+                Ts[f * ldW + r] = Qs[r * ldD + f];
+            }
+        __syncthreads();
+
+        if (out_pass) {
+            if (norm && um) {  // unmasked denominator carry g^(r+1) p_r . m0
+                for (int r = tid; r < W; r += kThreads) {
+                    float s = 0.f;
+                    for (int f = 0; f < D; ++f) s = fmaf(Ps[r * ldD + f], y[f], s);
+                    den[r] = gp[r + 1] * s;
+                }
+            }
+            // B~[r, j] = [j <= r] g^(2(r-j)) q_r . p_j   (unmasked: g^(r-j) p_r . q_j)
+            const float* X0 = um ? Ps : Qs;
+            simt::with_rm(W, W, [&](auto t) {
+                constexpr int RM = decltype(t)::value;
+                simt::for_blocks<RM>(W, W, [&](int m0, int n0) {
+                    simt::Acc<RM> acc;
+                    simt::zero(acc);
+                    if (n0 < m0 + RM) simt::mac<RM>(acc, X0 + m0 * ldD, ldD, 1, Ts + n0, ldW, 0, D);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) {
+                        const int r = m0 + i;
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            acc[i][b] = n0 + b <= r ? gp[bp * (r - n0 - b)] * acc[i][b] : 0.f;
+                        simt::st4(AB + r * ldW + n0, acc[i]);
+                    }
+                });
+            });
+            __syncthreads();
+
+            // O = diag(g^(2(r+1))) Q Z0 + B~ V   (unmasked: diag(g^(r+1)) P C0 + B~ V)
+            T* out = static_cast<T*>(a.out) + ((size_t)bh * a.n + row0) * DV;
+            simt::with_rm(W, DV, [&](auto t) {
+                constexpr int RM = decltype(t)::value;
+                simt::for_blocks<RM>(W, DV, [&](int m0, int n0) {
+                    if (m0 >= Wc) return;
+                    simt::Acc<RM> acc;
+                    simt::zero(acc);
+                    simt::mac<RM>(acc, X0 + m0 * ldD, ldD, 1, Z + n0, DV, 0, D);
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) simt::scale_row(acc, i, gp[bp * (m0 + i + 1)]);
+                    simt::mac<RM>(acc, AB + m0 * ldW, ldW, 1, Vs + n0, ldV, 0, min(W, m0 + RM));
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) {
+                        const int r = m0 + i;
+                        if (r >= Wc) break;
+                        if (norm) {
+                            float dn = den[r];
+                            for (int j = 0; j <= r; ++j) dn += AB[r * ldW + j];
+                            const float dd = dn + a.eps;
+#pragma unroll
+                            for (int b = 0; b < 4; ++b) acc[i][b] /= dd;
+                        }
+                        if (HLA2_IN(row0 + r < a.n && bh < a.BH, 209)) simt::store4(out + (size_t)r * DV + n0, acc[i]);
+                    }
+                });
+            });
+            __syncthreads();  // S0 and Z0 are read above
+        }
+
+        // the state to the chunk end (the output pass skips it after its last chunk unless the
+        // final state is written); each block owned by one thread
+        if (!summary && c + 1 == c_end && !final_seg) continue;
+        const float rho = gp[Wc], rho2 = gp[bp * Wc];
+        simt::with_rm(D, D, [&](auto t) {  // S <- g^Wc S0 + K~^T K
+            constexpr int RM = decltype(t)::value;
+            simt::for_blocks<RM>(D, D, [&](int m0, int n0) {
+                simt::Acc<RM> acc;
+                simt::zero(acc);
+                simt::mac_w<RM>(acc, Ks + m0, 1, ldD, Ks + n0, ldD, 0, Wc, [&](int i) { return gp[Wc - 1 - i]; });
+#pragma unroll
+                for (int i = 0; i < RM; ++i) simt::decay_add4(S + (m0 + i) * D + n0, rho, acc[i]);
+            });
+        });
+        // Z (masked: P~^T V with g^2; unmasked: Q~^T V with g) and C = Q~^T V with g
+        const float* ZL = um ? Qs : Ps;
+        simt::with_rm(D, DV, [&](auto t) {
+            constexpr int RM = decltype(t)::value;
+            simt::for_blocks<RM>(D, DV, [&](int m0, int n0) {
+                simt::Acc<RM> az;
+                simt::zero(az);
+                if (track_c) {
+                    simt::Acc<RM> ac;
+                    simt::zero(ac);
+#pragma unroll 2
+                    for (int j = 0; j < Wc; ++j) {
+                        const float4 b = *reinterpret_cast<const float4*>(Vs + j * ldV + n0);
+                        const float wz = gp[bp * (Wc - 1 - j)], wc = gp[Wc - 1 - j];
+#pragma unroll
+                        for (int i = 0; i < RM; ++i) {
+                            const float xz = ZL[j * ldD + m0 + i] * wz, xc = Qs[j * ldD + m0 + i] * wc;
+                            az[i][0] = fmaf(xz, b.x, az[i][0]);
+                            az[i][1] = fmaf(xz, b.y, az[i][1]);
+                            az[i][2] = fmaf(xz, b.z, az[i][2]);
+                            az[i][3] = fmaf(xz, b.w, az[i][3]);
+                            ac[i][0] = fmaf(xc, b.x, ac[i][0]);
+                            ac[i][1] = fmaf(xc, b.y, ac[i][1]);
+                            ac[i][2] = fmaf(xc, b.z, ac[i][2]);
+                            ac[i][3] = fmaf(xc, b.w, ac[i][3]);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < RM; ++i) simt::decay_add4(C + (m0 + i) * DV + n0, rho, ac[i]);
+                } else {
+                    simt::mac_w<RM>(az, ZL + m0, 1, ldD, Vs + n0, ldV, 0, Wc,
+                                    [&](int j) { return gp[bp * (Wc - 1 - j)]; });
+                }
+#pragma unroll
+                for (int i = 0; i < RM; ++i) simt::decay_add4(Z + (m0 + i) * DV + n0, rho2, az[i]);
+            });
+        });
+        for (int x = tid; x < D; x += kThreads) {
+            float s = 0.f, sq = 0.f;
+            for (int j = 0; j < Wc; ++j) {
+                s = fmaf(gp[bp * (Wc - 1 - j)], ZL[j * ldD + x], s);
+                sq = fmaf(gp[Wc - 1 - j], Qs[j * ldD + x], sq);
+            }
+            y[x] = rho2 * y[x] + s;
+            if (keep_c || um) m[x] = rho * m[x] + sq;
+        }
+    }
+    __syncthreads();
+
+    if (dst_ok) {
+        for (int i = tid; i < D * D; i += kThreads) dS[i] = S[i];
+        for (int i = tid; i < D * DV; i += kThreads) {
+            dZ[i] = Z[i];
+            if (cm && L.c_smem) dC[i] = C[i];
+        }
+        for (int i = tid; i < D; i += kThreads) {
             dm[i] = m[i];
             dy[i] = y[i];
         }
@@ -234,9 +375,10 @@ size_t fwd_chunk_simt_smem(int d, int dv, int W, bool track_cm) {
 int launch_fwd_chunk_simt(const ChunkArgs& a, int d, int dv, int W, bool summary, bool track_cm,
                           bool is_bf16, cudaStream_t st) {
     if (a.nseg_launch <= 0 || a.BH <= 0) return 0;
+    if ((d & 15) || (dv & 15) || (W & 15)) return -1;
     const bool cm = !a.unmasked && (summary || track_cm);
     const size_t smem = fwd_chunk_simt_smem(d, dv, W, cm);
-    dim3 grid(a.nseg_launch, a.BH), block(kSimtThreads);
+    dim3 grid(a.nseg_launch, a.BH), block(kThreads);
     cudaError_t e;
     if (is_bf16) {
         auto kfn = fwd_chunk_simt_kernel<bf16>;
