@@ -266,7 +266,7 @@ int forward_per_sm(Path path, int d, int dv, int W, const DevInfo& di) {
     switch (path) {
         case Path::kTc: return blocks_per_sm(fwd_chunk_tc_smem(), 288, 2, di);
         case Path::kMma: return blocks_per_sm(fwd_chunk_mma_smem(d, dv, W, false), mma_threads(d), 4, di);
-        case Path::kSimt: return blocks_per_sm(fwd_chunk_simt_smem(d, dv, W, false), 256, 4, di);
+        case Path::kSimt: return blocks_per_sm(fwd_chunk_simt_smem(d, dv, W, false), 256, kSimtFwdCtas, di);
         default: return 2;
     }
 }
@@ -675,8 +675,8 @@ int backward_width_f32(int d, int dv, int chunk, const DevInfo& di) {
 }
 
 int backward_per_sm_f32(int d, int dv, int W, const DevInfo& di) {
-    const int b = blocks_per_sm(bwd_chunk_simt_smem(d, dv, W), 256, 4, di);
-    const int f = blocks_per_sm(fwd_chunk_simt_smem(d, dv, W, false), 256, 4, di);
+    const int b = blocks_per_sm(bwd_chunk_simt_smem(d, dv, W), 256, kSimtBwdCtas, di);
+    const int f = blocks_per_sm(fwd_chunk_simt_smem(d, dv, W, false), 256, kSimtFwdCtas, di);
     return b < f ? b : f;
 }
 
@@ -762,8 +762,10 @@ int backward_forward_part(const ChunkArgs& a, const Plan& p, const BwdLayout& L,
 }
 
 // The same forward pieces for the fp32 backward, on the SIMT kernel: segment summaries, the
-// inter-segment scan, then a pass that exports the fp32 (S, Z) at every chunk start.
-int backward_forward_part_f32(const ChunkArgs& a, const Plan& p, const BwdLayout& L, int d, int dv, cudaStream_t st) {
+// inter-segment scan, then a pass that exports the fp32 (S, Z) at every chunk start (and, with
+// out, also writes the unnormalised output there).
+int backward_forward_part_f32(const ChunkArgs& a, const Plan& p, const BwdLayout& L, int d, int dv, cudaStream_t st,
+                              float* out = nullptr) {
     float* ws = a.ws;
     const size_t dd = (size_t)d * d, ddv = (size_t)d * dv;
     const int seg_tokens = p.seg_chunks * p.W;
@@ -781,7 +783,7 @@ int backward_forward_part_f32(const ChunkArgs& a, const Plan& p, const BwdLayout
                                a.gamma, seg_tokens, 2, st))
             return cuda_fail("forward segment scan");
     }
-    c.out = nullptr;
+    c.out = out;
     c.chunk_states_f32 = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + L.states_bytes_off);
     if (launch_fwd_chunk_simt(c, d, dv, p.W, false, false, false, st)) return cuda_fail("forward state export");
     return HLA2_OK;
@@ -1106,30 +1108,22 @@ int check_backward(int B, int H, int n, int d, int dv, int chunk, int dtype, int
     return HLA2_OK;
 }
 
-// Workspace of the ratio-normalised backward.  Its gradient is the difference of a
-// numerator part and a denominator part that can each be tens of times larger than the
-// result, so the composition runs in float32: one scratch region that the fp32 forward and
-// backward calls use in turn, then fp32 [B, H, n, *] buffers: num (dv), e_0, den and
-// dL/dden (kUnitWidth columns), dL/dnum (dv), dq2, dk2 (d), dv2 (kUnitWidth); for bf16
-// inputs also float32 copies of q, k (d), v, dout (dv) and of the gradients (d, d, dv).
-constexpr int kUnitWidth = 16;  // value width of the denominator pass (only column 0 is 1)
-enum NormBuf { NB_NUM, NB_E0, NB_DEN, NB_DNUM, NB_DDEN, NB_DQ2, NB_DK2, NB_DV2, NB_Q, NB_K, NB_V, NB_DO, NB_DQ, NB_DK,
-               NB_DV, NB_COUNT };
+// Workspace of the ratio-normalised backward.  num and den are the unnormalised outputs of
+// one recurrence for the widened value rows [v | e_0] (dv + kUnitWidth columns, column dv
+// the unit), so one float32 unnormalised backward at that width covers both: its forward part
+// writes [num | den], the quotient rule forms the upstream gradient [dL/dnum | dL/dden], and its
+// reverse part gives dq, dk and [dv | .].  Its gradient is the difference of a numerator part
+// and a denominator part that can each be tens of times larger than the result, hence float32.
+// Layout: that backward's workspace, then float32 [B, H, n, *] buffers: the widened values,
+// [num | den], the upstream gradient and [dv | .] (dv + kUnitWidth wide); for bf16 inputs
+// also float32 copies of q, k and the float32 dq, dk (d wide).
+constexpr int kUnitWidth = 16;
+enum NormBuf { NB_VE, NB_ND, NB_DND, NB_DVE, NB_Q, NB_K, NB_DQ, NB_DK, NB_COUNT };
 struct NormBwdLayout {
-    size_t sub_bytes = 0;
+    BwdPlan bp;
     size_t buf[NB_COUNT] = {};
     size_t total = 0;
 };
-
-// Chunk width of the normalised backward's float32 forwards: the largest <= chunk whose SIMT
-// kernel fits for both value widths (the result does not depend on the width).
-int normalised_f32_chunk(int d, int dv, int chunk, const DevInfo& di) {
-    for (int W = chunk; W >= 16; W /= 2)
-        if (fwd_chunk_simt_smem(d, dv, W, true) <= (size_t)di.smem_optin &&
-            fwd_chunk_simt_smem(d, kUnitWidth, W, true) <= (size_t)di.smem_optin)
-            return W;
-    return 0;
-}
 
 size_t unnormalised_backward_bytes(int B, int H, int n, int d, int dv, int chunk, int dtype, const DevInfo& di) {
     if (fo_path(dtype, d, dv, chunk, 0, di)) {
@@ -1143,30 +1137,17 @@ size_t unnormalised_backward_bytes(int B, int H, int n, int d, int dv, int chunk
 
 NormBwdLayout norm_bwd_layout(int B, int H, int n, int d, int dv, int chunk, int dtype, const DevInfo& di) {
     NormBwdLayout L;
-    const int u = kUnitWidth;
-    chunk = normalised_f32_chunk(d, dv, chunk, di);
-    if (!chunk) {
+    const int w = dv + kUnitWidth;
+    L.bp = backward_plan(B, H, n, d, w, chunk, HLA2_F32, di);
+    if (!L.bp.W) {
         L.total = (size_t)-1;
         return L;
     }
-    const size_t sizes[4] = {hla2_forward_workspace_bytes(B, H, n, d, dv, chunk, HLA2_F32, 0, 0),
-                             hla2_forward_workspace_bytes(B, H, n, d, u, chunk, HLA2_F32, 0, 0),
-                             unnormalised_backward_bytes(B, H, n, d, dv, chunk, HLA2_F32, di),
-                             unnormalised_backward_bytes(B, H, n, d, u, chunk, HLA2_F32, di)};
-    size_t sub = 0;
-    for (size_t x : sizes) {
-        if (x == (size_t)-1) {
-            L.total = (size_t)-1;
-            return L;
-        }
-        sub = x > sub ? x : sub;
-    }
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t rows = (size_t)B * H * (size_t)n;
-    const int width[NB_COUNT] = {dv, u, u, dv, u, d, d, u, d, d, dv, dv, d, d, dv};
+    const int width[NB_COUNT] = {w, w, w, w, d, d, d, d};
     const int count = dtype == HLA2_BF16 ? NB_COUNT : NB_Q;
-    size_t o = up(sub);
-    L.sub_bytes = o;
+    size_t o = up(L.bp.p.nseg > 0 ? L.bp.L.total_bytes : 0);
     for (int i = 0; i < count; ++i) {
         L.buf[i] = o;
         o += up(rows * (size_t)width[i] * sizeof(float));
@@ -1260,47 +1241,29 @@ int hla2_backward(const void* q, const void* k, const void* v, const void* dout,
         auto buf = [&](int i) { return reinterpret_cast<float*>(base + N.buf[i]); };
         const bool bf = opts->dtype == HLA2_BF16;
         const size_t rows = (size_t)BH * (size_t)n;
-        const int u = kUnitWidth;
+        const int w = dv + kUnitWidth;
+        const BwdPlan& bp = N.bp;
         cudaStream_t s2 = reinterpret_cast<cudaStream_t>(stream);
         cudaGetLastError();
         const float* q32 = bf ? buf(NB_Q) : static_cast<const float*>(q);
         const float* k32 = bf ? buf(NB_K) : static_cast<const float*>(k);
-        const float* v32 = bf ? buf(NB_V) : static_cast<const float*>(v);
-        const float* do32 = bf ? buf(NB_DO) : static_cast<const float*>(dout);
         float* dq32 = bf ? buf(NB_DQ) : static_cast<float*>(dq);
         float* dk32 = bf ? buf(NB_DK) : static_cast<float*>(dk);
-        float* dv32 = bf ? buf(NB_DV) : static_cast<float*>(dv_out);
         if (bf && (launch_convert_bf16_f32(static_cast<const bf16*>(q), buf(NB_Q), rows * d, s2) ||
-                   launch_convert_bf16_f32(static_cast<const bf16*>(k), buf(NB_K), rows * d, s2) ||
-                   launch_convert_bf16_f32(static_cast<const bf16*>(v), buf(NB_V), rows * dv, s2) ||
-                   launch_convert_bf16_f32(static_cast<const bf16*>(dout), buf(NB_DO), rows * dv, s2)))
+                   launch_convert_bf16_f32(static_cast<const bf16*>(k), buf(NB_K), rows * d, s2)))
             return cuda_fail("float32 copies");
-        hla2_opts so{};
-        so.dtype = HLA2_F32;
-        so.eps = opts->eps;
-        so.workspace = base;
-        so.workspace_bytes = N.sub_bytes;
-        const int cf = normalised_f32_chunk(d, dv, chunk, di);
-        // num = unnormalised output; den = unnormalised output for the value rows e_0
-        if ((rc = hla2_forward(q32, k32, v32, buf(NB_NUM), B, H, n, d, dv, gamma, 0, cf, stream, &so)) != HLA2_OK)
-            return rc;
-        if (launch_unit_first_column(buf(NB_E0), rows, u, s2)) return cuda_fail("unit value rows");
-        if ((rc = hla2_forward(q32, k32, buf(NB_E0), buf(NB_DEN), B, H, n, d, u, gamma, 0, cf, stream, &so)) !=
-            HLA2_OK)
-            return rc;
-        if (launch_quotient_rule(do32, buf(NB_NUM), buf(NB_DEN), buf(NB_DNUM), buf(NB_DDEN), rows, dv, u, opts->eps, s2))
+        if (launch_widen_values(v, buf(NB_VE), rows, dv, w, bf, s2)) return cuda_fail("widened values");
+        // [num | den] and the states the reverse passes read
+        const ChunkArgs a = backward_chunk_args(q32, k32, buf(NB_VE), nullptr, BH, H, n, bp.p, gamma, base, bp.L);
+        if ((rc = backward_forward_part_f32(a, bp.p, bp.L, d, w, s2, buf(NB_ND))) != HLA2_OK) return rc;
+        if (launch_quotient_rule(dout, buf(NB_ND), buf(NB_DND), rows, dv, w, opts->eps, bf, s2))
             return cuda_fail("quotient rule");
-        if ((rc = hla2_backward(q32, k32, v32, buf(NB_DNUM), dq32, dk32, dv32, B, H, n, d, dv, gamma, 0, cf, stream,
-                                &so)) != HLA2_OK)
+        if ((rc = backward_reverse_part_f32(q32, k32, buf(NB_VE), buf(NB_DND), dq32, dk32, buf(NB_DVE), H, bp.p, bp.L,
+                                            gamma, reinterpret_cast<float*>(base), d, w, s2)) != HLA2_OK)
             return rc;
-        if ((rc = hla2_backward(q32, k32, buf(NB_E0), buf(NB_DDEN), buf(NB_DQ2), buf(NB_DK2), buf(NB_DV2), B, H, n, d,
-                                u, gamma, 0, cf, stream, &so)) != HLA2_OK)
-            return rc;
-        if (launch_add_into(dq32, buf(NB_DQ2), rows * d, s2) || launch_add_into(dk32, buf(NB_DK2), rows * d, s2))
-            return cuda_fail("gradient sum");
+        if (launch_narrow_values(buf(NB_DVE), dv_out, rows, dv, w, bf, s2)) return cuda_fail("value gradient");
         if (bf && (launch_convert_f32_bf16(dq32, static_cast<bf16*>(dq), rows * d, s2) ||
-                   launch_convert_f32_bf16(dk32, static_cast<bf16*>(dk), rows * d, s2) ||
-                   launch_convert_f32_bf16(dv32, static_cast<bf16*>(dv_out), rows * dv, s2)))
+                   launch_convert_f32_bf16(dk32, static_cast<bf16*>(dk), rows * d, s2)))
             return cuda_fail("bf16 gradients");
         return succeed();
     }

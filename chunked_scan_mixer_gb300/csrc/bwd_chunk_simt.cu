@@ -33,13 +33,15 @@ namespace {
 using simt::kThreads;
 
 // Shared-memory tiles (floats): the chunk's Q, K, V, dO, P, dP row-major with padded rows;
-// K^T, V^T, P^T, dP^T; the four W x W matrices; Z0^T; and, while they fit, the carries Zh
-// (row-major [D][DV]) and Sh (the symmetric sum in the gradient pass), else those stay in
-// their workspace slots.
+// K^T, V^T, P^T, dP^T; the four W x W matrices; Z0^T; and, while they fit without lowering
+// the CTAs an SM holds, S0 (else read from the exported states) and the carries Zh (row-major [D][DV], padded rows: it is also read as an
+// A operand) and Sh (the symmetric sum in the gradient pass), else those stay in their
+// workspace slots.
 struct BsLayout {
     int ldD, ldV, ldW;
     bool st_smem;
-    size_t Q, K, V, O, P, dP, Kt, Vt, Pt, dPt, At, Dt, Bt, dAt, Z0t, Zh, Sh, gp, total;
+    bool s0_smem;
+    size_t Q, K, V, O, P, dP, Kt, Vt, Pt, dPt, At, Dt, Bt, dAt, Z0t, S0, Zh, Sh, gp, total;
 };
 
 __host__ __device__ inline BsLayout bs_layout(int D, int DV, int W) {
@@ -47,7 +49,6 @@ __host__ __device__ inline BsLayout bs_layout(int D, int DV, int W) {
     L.ldD = simt::pad(D);
     L.ldV = simt::pad(DV);
     L.ldW = simt::pad(W);
-    L.st_smem = (size_t)D * D <= 4096 && (size_t)D * DV <= 4096;
     size_t o = 0;
     L.Q = o;   o += (size_t)W * L.ldD;
     L.K = o;   o += (size_t)W * L.ldD;
@@ -64,9 +65,13 @@ __host__ __device__ inline BsLayout bs_layout(int D, int DV, int W) {
     L.Bt = o;  o += (size_t)W * L.ldW;
     L.dAt = o; o += (size_t)W * L.ldW;
     L.Z0t = o; o += (size_t)DV * L.ldD;
-    L.Zh = o;  o += L.st_smem ? (size_t)D * DV : 0;
-    L.Sh = o;  o += L.st_smem ? (size_t)D * D : 0;
     L.gp = o;  o += 2 * (size_t)W + 2;
+    o = (o + 3) & ~(size_t)3;
+    L.s0_smem = simt::fits_beside(o, (size_t)D * D, kSimtBwdCtas);
+    L.S0 = o;  o += L.s0_smem ? (size_t)D * D : 0;
+    L.st_smem = simt::fits_beside(o, (size_t)D * L.ldV + (size_t)D * D, kSimtBwdCtas);
+    L.Zh = o;  o += L.st_smem ? (size_t)D * L.ldV : 0;
+    L.Sh = o;  o += L.st_smem ? (size_t)D * D : 0;
     L.total = o;
     return L;
 }
@@ -80,7 +85,7 @@ __device__ __forceinline__ void tri_gram(float* T, int ldt, const float* A, int 
         simt::for_blocks<RM>(M, M, [&](int m0, int n0) {
             simt::Acc<RM> acc;
             simt::zero(acc);
-            if (n0 < m0 + RM) simt::mac<RM>(acc, A + m0 * lda, lda, 1, B + n0, ldb, 0, K);
+            if (n0 < m0 + RM) simt::mac_r<RM>(acc, A + m0 * lda, lda, B + n0, ldb, K);
 #pragma unroll
             for (int i = 0; i < RM; ++i) {
                 const int r = m0 + i;
@@ -93,7 +98,7 @@ __device__ __forceinline__ void tri_gram(float* T, int ldt, const float* A, int 
 }
 
 template <bool RSUM>
-__global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdArgsF a, int D, int DV) {
+__global__ void __launch_bounds__(kThreads, kSimtBwdCtas) bwd_chunk_simt_kernel(const BwdArgsF a, int D, int DV) {
     extern __shared__ __align__(16) float sm[];
     const int W = a.W;
     const BsLayout L = bs_layout(D, DV, W);
@@ -115,12 +120,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
     float* Sg = a.ws + (RSUM ? a.ShB : a.Sh_end) + sidx * D * D;    // [D][D]
     float* Zh = L.st_smem ? sm + L.Zh : Zg;
     float* Sh = L.st_smem ? sm + L.Sh : Sg;
+    const int ldZ = L.st_smem ? ldV : DV;  // Zh rows: padded in shared memory
     if (RSUM) {
-        for (int i = tid; i < D * DV; i += kThreads) Zh[i] = 0.f;
+        for (int i = tid; i < D * DV; i += kThreads) Zh[(i / DV) * ldZ + i % DV] = 0.f;
         for (int i = tid; i < D * D; i += kThreads) Sh[i] = 0.f;
     } else {
         if (L.st_smem)
-            for (int i = tid; i < D * DV; i += kThreads) Zh[i] = Zg[i];
+            for (int i = tid; i < D * DV; i += kThreads) Zh[(i / DV) * ldZ + i % DV] = Zg[i];
         // Sh + Sh^T, one thread per unordered pair (in place when it stays in the workspace)
         for (int e = tid; e < D * D; e += kThreads) {
             const int x = e / D, f = e - x * D;
@@ -152,9 +158,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
             if (!RSUM) Vs[r * ldV + x] = vx;
             Os[r * ldV + x] = in ? a.dout[(hq + row0) * DV + i] : 0.f;
         }
-        const float* S0 = RSUM ? nullptr : a.chunk_states + ((size_t)bh * a.nchunks + c) * (size_t)(D * D + D * DV);
-        if (!RSUM) {  // Z0^T (the forward exports Z0 row-major [D][DV])
-            const float* Z0 = S0 + (size_t)D * D;
+        const float* S0g = RSUM ? nullptr : a.chunk_states + ((size_t)bh * a.nchunks + c) * (size_t)(D * D + D * DV);
+        const float* S0 = L.s0_smem ? sm + L.S0 : S0g;
+        if (!RSUM) {  // S0 and Z0^T (the forward exports S0 [D][D] and Z0 [D][DV], row-major)
+            if (L.s0_smem)
+                for (int i = tid; i < (D * D) / 4; i += kThreads)
+                    reinterpret_cast<float4*>(sm + L.S0)[i] = reinterpret_cast<const float4*>(S0g)[i];
+            const float* Z0 = S0g + (size_t)D * D;
             for (int i = tid; i < D * DV; i += kThreads) {
                 const int x = i / D, f = i - x * D;
                 Z0t[x * ldD + f] = Z0[(size_t)f * DV + x];
@@ -173,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
             simt::for_blocks<RM>(D, W, [&](int m0, int n0) {
                 simt::Acc<RM> acc;
                 simt::zero(acc);
-                simt::mac<RM>(acc, Zh + m0 * DV, DV, 1, Vt + n0, ldW, 0, DV);
+                simt::mac_r<RM>(acc, Zh + m0 * ldZ, ldZ, Vt + n0, ldW, DV);
                 float cw[4];
 #pragma unroll
                 for (int b = 0; b < 4; ++b) cw[b] = n0 + b < Wc ? gp[2 * (Wc - 1 - n0 - b)] : 0.f;
@@ -181,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
                 for (int i = 0; i < RM; ++i)
 #pragma unroll
                     for (int b = 0; b < 4; ++b) acc[i][b] *= cw[b];
-                simt::mac<RM>(acc, Qs + m0, 1, ldD, Dt + n0, ldW, n0, W);
+                simt::mac_c<RM>(acc, Qs + m0, ldD, Dt + n0, ldW, n0, W);
 #pragma unroll
                 for (int i = 0; i < RM; ++i) {
                     simt::st4(dPt + (m0 + i) * ldW + n0, acc[i]);
@@ -199,10 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
                 simt::for_blocks<RM>(W, D, [&](int m0, int n0) {
                     simt::Acc<RM> acc;
                     simt::zero(acc);
-                    simt::mac<RM>(acc, Qs + m0 * ldD, ldD, 1, S0 + n0, D, 0, D);
+                    simt::mac_r<RM>(acc, Qs + m0 * ldD, ldD, S0 + n0, D, D);
 #pragma unroll
                     for (int i = 0; i < RM; ++i) simt::scale_row(acc, i, gp[m0 + i + 1]);
-                    simt::mac<RM>(acc, At + m0 * ldW, ldW, 1, Ks + n0, ldD, 0, min(W, m0 + RM));
+                    simt::mac_r<RM>(acc, At + m0 * ldW, ldW, Ks + n0, ldD, min(W, m0 + RM));
 #pragma unroll
                     for (int i = 0; i < RM; ++i) {
                         simt::st4(Ps + (m0 + i) * ldD + n0, acc[i]);
@@ -227,11 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
                     if (m0 >= Wc) return;
                     simt::Acc<RM> acc;
                     simt::zero(acc);
-                    simt::mac<RM>(acc, Ps + m0 * ldD, ldD, 1, Zh + n0, DV, 0, D);
+                    simt::mac_r<RM>(acc, Ps + m0 * ldD, ldD, Zh + n0, ldZ, D);
 #pragma unroll
                     for (int i = 0; i < RM; ++i)
                         simt::scale_row(acc, i, m0 + i < Wc ? gp[2 * (Wc - 1 - m0 - i)] : 0.f);
-                    simt::mac<RM>(acc, Bt + m0, 1, ldW, Os + n0, ldV, m0, W);
+                    simt::mac_c<RM>(acc, Bt + m0, ldW, Os + n0, ldV, m0, W);
 #pragma unroll
                     for (int i = 0; i < RM; ++i)
                         if (m0 + i < Wc && HLA2_IN(row0 + m0 + i < a.n, 603))
@@ -245,14 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
                     const int kr = min(W, m0 + RM);
                     simt::Acc<RM> acc;
                     simt::zero(acc);
-                    simt::mac<RM>(acc, Os + m0 * ldV, ldV, 1, Z0t + n0, ldD, 0, DV);
+                    simt::mac_r<RM>(acc, Os + m0 * ldV, ldV, Z0t + n0, ldD, DV);
 #pragma unroll
                     for (int i = 0; i < RM; ++i) simt::scale_row(acc, i, gp[m0 + i + 1]);
-                    simt::mac<RM>(acc, dPs + m0 * ldD, ldD, 1, S0 + n0, D, 0, D);
+                    simt::mac_r<RM>(acc, dPs + m0 * ldD, ldD, S0 + n0, D, D);
 #pragma unroll
                     for (int i = 0; i < RM; ++i) simt::scale_row(acc, i, gp[m0 + i + 1]);
-                    simt::mac<RM>(acc, Dt + m0 * ldW, ldW, 1, Ps + n0, ldD, 0, kr);
-                    simt::mac<RM>(acc, dAt + m0 * ldW, ldW, 1, Ks + n0, ldD, 0, kr);
+                    simt::mac_r<RM>(acc, Dt + m0 * ldW, ldW, Ps + n0, ldD, kr);
+                    simt::mac_r<RM>(acc, dAt + m0 * ldW, ldW, Ks + n0, ldD, kr);
 #pragma unroll
                     for (int i = 0; i < RM; ++i)
                         if (m0 + i < Wc && HLA2_IN(row0 + m0 + i < a.n, 604))
@@ -265,12 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
                     if (m0 >= Wc) return;
                     simt::Acc<RM> acc;
                     simt::zero(acc);
-                    simt::mac<RM>(acc, Ks + m0 * ldD, ldD, 1, Sh + n0, D, 0, D);
+                    simt::mac_r<RM>(acc, Ks + m0 * ldD, ldD, Sh + n0, D, D);
 #pragma unroll
                     for (int i = 0; i < RM; ++i)
                         simt::scale_row(acc, i, m0 + i < Wc ? gp[Wc - 1 - m0 - i] : 0.f);
-                    simt::mac<RM>(acc, At + m0, 1, ldW, dPs + n0, ldD, m0, W);
-                    simt::mac<RM>(acc, dAt + m0, 1, ldW, Qs + n0, ldD, m0, W);
+                    simt::mac_c<RM>(acc, At + m0, ldW, dPs + n0, ldD, m0, W);
+                    simt::mac_c<RM>(acc, dAt + m0, ldW, Qs + n0, ldD, m0, W);
 #pragma unroll
                     for (int i = 0; i < RM; ++i)
                         if (m0 + i < Wc && HLA2_IN(row0 + m0 + i < a.n, 605))
@@ -287,9 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
             simt::for_blocks<RM>(D, DV, [&](int m0, int n0) {
                 simt::Acc<RM> acc;
                 simt::zero(acc);
-                simt::mac_w<RM>(acc, Qs + m0, 1, ldD, Os + n0, ldV, 0, Wc, [&](int r) { return gp[2 * (r + 1)]; });
+                simt::mac_c<RM>(acc, Qs + m0, ldD, Os + n0, ldV, 0, Wc, [&](int r) { return gp[2 * (r + 1)]; });
 #pragma unroll
-                for (int i = 0; i < RM; ++i) simt::decay_add4(Zh + (m0 + i) * DV + n0, rho2, acc[i]);
+                for (int i = 0; i < RM; ++i) simt::decay_add4(Zh + (m0 + i) * ldZ + n0, rho2, acc[i]);
             });
         });
         simt::with_rm(D, D, [&](auto t) {
@@ -298,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
                 simt::Acc<RM> acc;
                 simt::zero(acc);
                 auto wj = [&](int j) { return gp[j + 1]; };
-                simt::mac_w<RM>(acc, dPt + m0 * ldW, ldW, 1, Qs + n0, ldD, 0, Wc, wj);
-                if (!RSUM) simt::mac_w<RM>(acc, Qs + m0, 1, ldD, dPs + n0, ldD, 0, Wc, wj);
+                simt::mac_r<RM>(acc, dPt + m0 * ldW, ldW, Qs + n0, ldD, Wc, wj);
+                if (!RSUM) simt::mac_c<RM>(acc, Qs + m0, ldD, dPs + n0, ldD, 0, Wc, wj);
 #pragma unroll
                 for (int i = 0; i < RM; ++i) simt::decay_add4(Sh + (m0 + i) * D + n0, rho, acc[i]);
             });
@@ -307,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chunk_simt_kernel(const BwdAr
     }
     if (RSUM && L.st_smem) {
         __syncthreads();
-        for (int i = tid; i < D * DV; i += kThreads) Zg[i] = Zh[i];
+        for (int i = tid; i < D * DV; i += kThreads) Zg[i] = Zh[(i / DV) * ldZ + i % DV];
         for (int i = tid; i < D * D; i += kThreads) Sg[i] = Sh[i];
     }
 }

@@ -5,13 +5,14 @@
 // With o_t = num_t / (den_t + eps), num the unnormalised output and den the same pair sum
 // with every v_j replaced by 1, the quotient rule gives
 //     dL/dnum_t = dO_t / (den_t + eps),   dL/dden_t = -(dO_t . num_t) / (den_t + eps)^2.
-// Both num and den are unnormalised outputs of the same recurrence: den is the output for
-// the value rows e_0 = (1, 0, ..., 0). So the gradients are those of two unnormalised
-// backward passes: one with (v, dL/dnum), and one with (e_0, dL/dden e_0^T), which adds to
-// dq and dk only.  The two parts of dq and dk can each be tens of times larger than their
-// sum, so the composition runs in float32 (bf16 inputs are widened first and the gradients
-// rounded at the end).  The kernels below build e_0 and the two upstream gradients, add the
-// second pass's dq, dk into the first's, and convert between bf16 and float32.
+// num and den are the unnormalised outputs of one recurrence for the widened value rows
+// [v_j | 1 | 0 ...] (dv + w0 columns, column dv the unit), so one unnormalised forward gives
+// [num | den] and one unnormalised backward with the upstream gradient [dL/dnum | dL/dden]
+// gives dq, dk and [dv | .].  dq and dk are then the difference of a numerator part and a
+// denominator part that can each be tens of times larger than their sum, so the composition
+// runs in float32 (bf16 inputs are widened first and the gradients rounded at the end).
+// The kernels below widen the values, apply the quotient rule, narrow the value gradient
+// and convert between bf16 and float32.
 #include "kernels.h"
 
 namespace hla2 {
@@ -20,43 +21,50 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// rows x w float32 with column 0 = 1 and every other column 0.
-__global__ void __launch_bounds__(kThreads) unit_first_column_kernel(float* e0, size_t count, int w) {
+__device__ __forceinline__ float ld_f32(const float* p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ld_f32(const bf16* p, size_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ void st_val(float* p, size_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_val(bf16* p, size_t i, float x) { p[i] = __float2bfloat16_rn(x); }
+
+// ve[t] = [v_t | 1 | 0 ...]: rows x w float32 from rows x dv values (w > dv).
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    widen_values_kernel(const T* __restrict__ v, float* __restrict__ ve, size_t count, int dv, int w) {
     const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
-    if (i < count) e0[i] = (i % (size_t)w) == 0 ? 1.f : 0.f;
+    if (i >= count) return;
+    const size_t t = i / (size_t)w;
+    const int j = (int)(i - t * (size_t)w);
+    ve[i] = j < dv ? ld_f32(v, t * dv + j) : (j == dv ? 1.f : 0.f);
 }
 
-// One warp per token row t: den = den_out[t][0], s = dO_t . num_t,
-// dnum[t] = dO_t / (den + eps), dden[t] = (-s / (den + eps)^2, 0, ..., 0).
+// One warp per token row t of nd = [num | den | .] (w wide): den = nd[t][dv],
+// s = dO_t . num_t, dnd[t] = [dO_t / (den + eps) | -s / (den + eps)^2 | 0 ...].
+template <typename T>
 __global__ void __launch_bounds__(kThreads)
-    quotient_rule_kernel(const float* __restrict__ dout, const float* __restrict__ num,
-                         const float* __restrict__ den_out, float* __restrict__ dnum, float* __restrict__ dden,
+    quotient_rule_kernel(const T* __restrict__ dout, const float* __restrict__ nd, float* __restrict__ dnd,
                          size_t rows, int dv, int w, float eps) {
     const size_t row = (size_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const float* o = dout + row * dv;
-    const float* x = num + row * dv;
+    const float* x = nd + row * w;
     float s = 0.f;
-    for (int j = lane; j < dv; j += 32) s += o[j] * x[j];
+    for (int j = lane; j < dv; j += 32) s += ld_f32(dout, row * dv + j) * x[j];
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
-    const float inv = 1.f / (den_out[row * w] + eps);
-    for (int j = lane; j < dv; j += 32) dnum[row * dv + j] = o[j] * inv;
-    for (int j = lane; j < w; j += 32) dden[row * w + j] = j == 0 ? -s * inv * inv : 0.f;
+    const float inv = 1.f / (x[dv] + eps);
+    for (int j = lane; j < w; j += 32)
+        dnd[row * w + j] = j < dv ? ld_f32(dout, row * dv + j) * inv : (j == dv ? -s * inv * inv : 0.f);
 }
 
-// a += b, float32, count a multiple of 4.
-__global__ void __launch_bounds__(kThreads) add_into_kernel(float* a, const float* b, size_t count4) {
+// out[t][j] = dve[t][j] for j < dv (the value gradient out of [dv | .], w wide).
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    narrow_values_kernel(const float* __restrict__ dve, T* __restrict__ out, size_t count, int dv, int w) {
     const size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x;
-    if (i >= count4) return;
-    float4 x = reinterpret_cast<float4*>(a)[i];
-    const float4 y = reinterpret_cast<const float4*>(b)[i];
-    x.x += y.x;
-    x.y += y.y;
-    x.z += y.z;
-    x.w += y.w;
-    reinterpret_cast<float4*>(a)[i] = x;
+    if (i >= count) return;
+    const size_t t = i / (size_t)dv;
+    const int j = (int)(i - t * (size_t)dv);
+    st_val(out, i, dve[t * w + j]);
 }
 
 // 8 elements per thread; count a multiple of 8.
@@ -99,25 +107,34 @@ int done() { return cudaPeekAtLastError() == cudaSuccess ? 0 : -1; }
 
 }  // namespace
 
-int launch_unit_first_column(float* e0, size_t rows, int w, cudaStream_t st) {
+int launch_widen_values(const void* v, float* ve, size_t rows, int dv, int w, bool is_bf16, cudaStream_t st) {
     const size_t c = rows * (size_t)w;
     if (c == 0) return 0;
-    unit_first_column_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(e0, c, w);
+    if (is_bf16)
+        widen_values_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(static_cast<const bf16*>(v), ve, c, dv, w);
+    else
+        widen_values_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(static_cast<const float*>(v), ve, c, dv, w);
     return done();
 }
 
-int launch_quotient_rule(const float* dout, const float* num, const float* den_out, float* dnum, float* dden,
-                         size_t rows, int dv, int w, float eps, cudaStream_t st) {
+int launch_quotient_rule(const void* dout, const float* nd, float* dnd, size_t rows, int dv, int w, float eps,
+                         bool is_bf16, cudaStream_t st) {
     if (rows == 0) return 0;
-    quotient_rule_kernel<<<blocks_for(rows, kThreads / 32), kThreads, 0, st>>>(dout, num, den_out, dnum, dden, rows,
-                                                                                dv, w, eps);
+    const unsigned g = blocks_for(rows, kThreads / 32);
+    if (is_bf16)
+        quotient_rule_kernel<<<g, kThreads, 0, st>>>(static_cast<const bf16*>(dout), nd, dnd, rows, dv, w, eps);
+    else
+        quotient_rule_kernel<<<g, kThreads, 0, st>>>(static_cast<const float*>(dout), nd, dnd, rows, dv, w, eps);
     return done();
 }
 
-int launch_add_into(float* a, const float* b, size_t count, cudaStream_t st) {
-    const size_t c = count / 4;
+int launch_narrow_values(const float* dve, void* out, size_t rows, int dv, int w, bool is_bf16, cudaStream_t st) {
+    const size_t c = rows * (size_t)dv;
     if (c == 0) return 0;
-    add_into_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(a, b, c);
+    if (is_bf16)
+        narrow_values_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(dve, static_cast<bf16*>(out), c, dv, w);
+    else
+        narrow_values_kernel<<<blocks_for(c, kThreads), kThreads, 0, st>>>(dve, static_cast<float*>(out), c, dv, w);
     return done();
 }
 

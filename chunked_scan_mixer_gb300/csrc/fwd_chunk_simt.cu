@@ -27,8 +27,9 @@ using simt::kThreads;
 
 // Shared-memory tiles (floats).  Q, K, V, P row-major with padded rows; T holds K^T for the
 // key Gram, then P^T (masked) or Q^T (unmasked) for the second Gram; AB holds A~, then B~.
-// S and Z (and C for small states) are row-major without padding: they are read only as the
-// B operand of a product, or updated by the thread that owns a block.
+// S and Z (and C while it fits without lowering the CTAs an SM holds; else C accumulates in the
+// slot it is written to) are row-major without padding: they are read only as the B operand of
+// a product, or updated by the thread that owns a block.
 struct SimtLayout {
     int ldD, ldV, ldW;
     bool c_smem;
@@ -40,7 +41,6 @@ __host__ __device__ inline SimtLayout simt_layout(int D, int DV, int W, bool cm)
     L.ldD = simt::pad(D);
     L.ldV = simt::pad(DV);
     L.ldW = simt::pad(W);
-    L.c_smem = cm && (size_t)D * DV <= 4096;
     size_t o = 0;
     L.Q = o;   o += (size_t)W * L.ldD;
     L.K = o;   o += (size_t)W * L.ldD;
@@ -50,11 +50,13 @@ __host__ __device__ inline SimtLayout simt_layout(int D, int DV, int W, bool cm)
     L.P = o;   o += (size_t)W * L.ldD;
     L.S = o;   o += (size_t)D * D;
     L.Z = o;   o += (size_t)D * DV;
-    L.C = o;   o += L.c_smem ? (size_t)D * DV : 0;
     L.y = o;   o += D;
     L.m = o;   o += D;
     L.den = o; o += W;
     L.gp = o;  o += 2 * (size_t)W + 2;
+    o = (o + 3) & ~(size_t)3;
+    L.c_smem = cm && simt::fits_beside(o, (size_t)D * DV, kSimtFwdCtas);
+    L.C = o;   o += L.c_smem ? (size_t)D * DV : 0;
     L.total = o;
     return L;
 }
@@ -81,7 +83,7 @@ __device__ __forceinline__ void load4<bf16>(const bf16* p, float (&r)[4]) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kSimtFwdCtas)
     fwd_chunk_simt_kernel(const ChunkArgs a, int D, int DV, int W, int summary, int cm) {
     extern __shared__ __align__(16) float sm[];
     const SimtLayout L = simt_layout(D, DV, W, cm != 0);
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kThreads)
                 simt::for_blocks<RM>(W, W, [&](int m0, int n0) {
                     simt::Acc<RM> acc;
                     simt::zero(acc);
-                    if (n0 < m0 + RM) simt::mac<RM>(acc, Qs + m0 * ldD, ldD, 1, Ts + n0, ldW, 0, D);
+                    if (n0 < m0 + RM) simt::mac_r<RM>(acc, Qs + m0 * ldD, ldD, Ts + n0, ldW, D);
 #pragma unroll
                     for (int i = 0; i < RM; ++i) {
                         const int r = m0 + i;
@@ -210,10 +212,10 @@ __global__ void __launch_bounds__(kThreads)
                 simt::for_blocks<RM>(W, D, [&](int m0, int n0) {
                     simt::Acc<RM> acc;
                     simt::zero(acc);
-                    simt::mac<RM>(acc, Qs + m0 * ldD, ldD, 1, S + n0, D, 0, D);
+                    simt::mac_r<RM>(acc, Qs + m0 * ldD, ldD, S + n0, D, D);
 #pragma unroll
                     for (int i = 0; i < RM; ++i) simt::scale_row(acc, i, gp[m0 + i + 1]);
-                    simt::mac<RM>(acc, AB + m0 * ldW, ldW, 1, Ks + n0, ldD, 0, min(W, m0 + RM));
+                    simt::mac_r<RM>(acc, AB + m0 * ldW, ldW, Ks + n0, ldD, min(W, m0 + RM));
 #pragma unroll
                     for (int i = 0; i < RM; ++i) {
                         simt::st4(Ps + (m0 + i) * ldD + n0, acc[i]);
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThreads)
                 simt::for_blocks<RM>(W, W, [&](int m0, int n0) {
                     simt::Acc<RM> acc;
                     simt::zero(acc);
-                    if (n0 < m0 + RM) simt::mac<RM>(acc, X0 + m0 * ldD, ldD, 1, Ts + n0, ldW, 0, D);
+                    if (n0 < m0 + RM) simt::mac_r<RM>(acc, X0 + m0 * ldD, ldD, Ts + n0, ldW, D);
 #pragma unroll
                     for (int i = 0; i < RM; ++i) {
                         const int r = m0 + i;
@@ -268,10 +270,10 @@ __global__ void __launch_bounds__(kThreads)
                     if (m0 >= Wc) return;
                     simt::Acc<RM> acc;
                     simt::zero(acc);
-                    simt::mac<RM>(acc, X0 + m0 * ldD, ldD, 1, Z + n0, DV, 0, D);
+                    simt::mac_r<RM>(acc, X0 + m0 * ldD, ldD, Z + n0, DV, D);
 #pragma unroll
                     for (int i = 0; i < RM; ++i) simt::scale_row(acc, i, gp[bp * (m0 + i + 1)]);
-                    simt::mac<RM>(acc, AB + m0 * ldW, ldW, 1, Vs + n0, ldV, 0, min(W, m0 + RM));
+                    simt::mac_r<RM>(acc, AB + m0 * ldW, ldW, Vs + n0, ldV, min(W, m0 + RM));
 #pragma unroll
                     for (int i = 0; i < RM; ++i) {
                         const int r = m0 + i;
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kThreads)
             simt::for_blocks<RM>(D, D, [&](int m0, int n0) {
                 simt::Acc<RM> acc;
                 simt::zero(acc);
-                simt::mac_w<RM>(acc, Ks + m0, 1, ldD, Ks + n0, ldD, 0, Wc, [&](int i) { return gp[Wc - 1 - i]; });
+                simt::mac_c<RM>(acc, Ks + m0, ldD, Ks + n0, ldD, 0, Wc, [&](int i) { return gp[Wc - 1 - i]; });
 #pragma unroll
                 for (int i = 0; i < RM; ++i) simt::decay_add4(S + (m0 + i) * D + n0, rho, acc[i]);
             });
@@ -316,25 +318,17 @@ __global__ void __launch_bounds__(kThreads)
                     simt::zero(ac);
 #pragma unroll 2
                     for (int j = 0; j < Wc; ++j) {
-                        const float4 b = *reinterpret_cast<const float4*>(Vs + j * ldV + n0);
-                        const float wz = gp[bp * (Wc - 1 - j)], wc = gp[Wc - 1 - j];
-#pragma unroll
-                        for (int i = 0; i < RM; ++i) {
-                            const float xz = ZL[j * ldD + m0 + i] * wz, xc = Qs[j * ldD + m0 + i] * wc;
-                            az[i][0] = fmaf(xz, b.x, az[i][0]);
-                            az[i][1] = fmaf(xz, b.y, az[i][1]);
-                            az[i][2] = fmaf(xz, b.z, az[i][2]);
-                            az[i][3] = fmaf(xz, b.w, az[i][3]);
-                            ac[i][0] = fmaf(xc, b.x, ac[i][0]);
-                            ac[i][1] = fmaf(xc, b.y, ac[i][1]);
-                            ac[i][2] = fmaf(xc, b.z, ac[i][2]);
-                            ac[i][3] = fmaf(xc, b.w, ac[i][3]);
-                        }
+                        const float4 b = simt::ldb4(Vs + n0, ldV, j);
+                        float xz[RM], xc[RM];
+                        simt::ldv<RM>(xz, ZL + j * ldD + m0);
+                        simt::ldv<RM>(xc, Qs + j * ldD + m0);
+                        simt::fma_row<RM>(az, xz, simt::scale4(b, gp[bp * (Wc - 1 - j)]));
+                        simt::fma_row<RM>(ac, xc, simt::scale4(b, gp[Wc - 1 - j]));
                     }
 #pragma unroll
                     for (int i = 0; i < RM; ++i) simt::decay_add4(C + (m0 + i) * DV + n0, rho, ac[i]);
                 } else {
-                    simt::mac_w<RM>(az, ZL + m0, 1, ldD, Vs + n0, ldV, 0, Wc,
+                    simt::mac_c<RM>(az, ZL + m0, ldD, Vs + n0, ldV, 0, Wc,
                                     [&](int j) { return gp[bp * (Wc - 1 - j)]; });
                 }
 #pragma unroll

@@ -136,6 +136,9 @@ struct BwdArgsF {
     size_t Zh_end, Sh_end;       // reverse carries at segment ends, [BH][nseg][...]; updated in place
     const float* chunk_states;   // forward (S | Z) fp32 at every chunk start
 };
+// Resident CTAs per SM of the SIMT chunk kernels as their registers allow (their launch
+// bounds): two of the forward kernel, one of the reverse-mode kernel.
+constexpr int kSimtFwdCtas = 2, kSimtBwdCtas = 1;
 int launch_bwd_chunk_simt(const BwdArgsF& a, int d, int dv, bool rsum, cudaStream_t st);
 size_t bwd_chunk_simt_smem(int d, int dv, int W);
 
@@ -152,10 +155,13 @@ int launch_reverse_scan(const float* src, float* dst, int BH, int H, int nseg, s
 int launch_reverse_cross(const BwdArgs& b, const float* CB, int d, int dv, cudaStream_t st);
 
 // ratio-normalised backward: quotient-rule glue (bwd_normalize.cu)
-int launch_unit_first_column(float* e0, size_t rows, int w, cudaStream_t st);
-int launch_quotient_rule(const float* dout, const float* num, const float* den_out, float* dnum, float* dden,
-                         size_t rows, int dv, int w, float eps, cudaStream_t st);
-int launch_add_into(float* a, const float* b, size_t count, cudaStream_t st);  // count a multiple of 4
+// [v | 1 | 0 ...] (w columns) from v (dv columns, bf16 or float32)
+int launch_widen_values(const void* v, float* ve, size_t rows, int dv, int w, bool is_bf16, cudaStream_t st);
+// [dL/dnum | dL/dden | 0 ...] from dout (dv columns) and [num | den | .] (w columns)
+int launch_quotient_rule(const void* dout, const float* nd, float* dnd, size_t rows, int dv, int w, float eps,
+                         bool is_bf16, cudaStream_t st);
+// the first dv columns of [dv | .] (w columns), as bf16 or float32
+int launch_narrow_values(const float* dve, void* out, size_t rows, int dv, int w, bool is_bf16, cudaStream_t st);
 int launch_convert_bf16_f32(const bf16* src, float* dst, size_t count, cudaStream_t st);  // count % 8 == 0
 int launch_convert_f32_bf16(const float* src, bf16* dst, size_t count, cudaStream_t st);
 

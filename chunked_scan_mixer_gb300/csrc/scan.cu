@@ -534,7 +534,8 @@ int launch_cross_t(const ChunkArgs& a, cudaStream_t st) {
     return finish_launch();
 }
 
-// d, dv in {16, 32, 64, 128}; the largest (128 x 128) needs 128 KB of shared memory.
+// d in {16, 32, 64, 128}, dv in {16, 32, 48, 64, 80, 128, 144}; the largest (128 x 144) needs
+// 137 KB of shared memory.
 // with_y adds the denominator moment's cross term (needed by the normalised output and the
 // final state only).
 int launch_cross(const ChunkArgs& a, int d, int dv, bool with_y, cudaStream_t st) {
@@ -548,6 +549,11 @@ int launch_cross(const ChunkArgs& a, int d, int dv, bool with_y, cudaStream_t st
     HLA2_CROSS(32, 16) HLA2_CROSS(32, 32) HLA2_CROSS(32, 64) HLA2_CROSS(32, 128)
     HLA2_CROSS(64, 16) HLA2_CROSS(64, 32) HLA2_CROSS(64, 64) HLA2_CROSS(64, 128)
     HLA2_CROSS(128, 16) HLA2_CROSS(128, 32) HLA2_CROSS(128, 64) HLA2_CROSS(128, 128)
+    // value widths dv + 16 of the normalised backward's widened values [v | e_0]
+    HLA2_CROSS(16, 48) HLA2_CROSS(16, 80) HLA2_CROSS(16, 144)
+    HLA2_CROSS(32, 48) HLA2_CROSS(32, 80) HLA2_CROSS(32, 144)
+    HLA2_CROSS(64, 48) HLA2_CROSS(64, 80) HLA2_CROSS(64, 144)
+    HLA2_CROSS(128, 48) HLA2_CROSS(128, 80) HLA2_CROSS(128, 144)
 #undef HLA2_CROSS
     return -1;
 }
@@ -733,6 +739,10 @@ int launch_reverse_cross(const BwdArgs& b, const float* CB, int d, int dv, cudaS
     HLA2_RCROSS(32, 16) HLA2_RCROSS(32, 32) HLA2_RCROSS(32, 64) HLA2_RCROSS(32, 128)
     HLA2_RCROSS(64, 16) HLA2_RCROSS(64, 32) HLA2_RCROSS(64, 64) HLA2_RCROSS(64, 128)
     HLA2_RCROSS(128, 16) HLA2_RCROSS(128, 32) HLA2_RCROSS(128, 64) HLA2_RCROSS(128, 128)
+    HLA2_RCROSS(16, 48) HLA2_RCROSS(16, 80) HLA2_RCROSS(16, 144)
+    HLA2_RCROSS(32, 48) HLA2_RCROSS(32, 80) HLA2_RCROSS(32, 144)
+    HLA2_RCROSS(64, 48) HLA2_RCROSS(64, 80) HLA2_RCROSS(64, 144)
+    HLA2_RCROSS(128, 48) HLA2_RCROSS(128, 80) HLA2_RCROSS(128, 144)
 #undef HLA2_RCROSS
     return -1;
 }

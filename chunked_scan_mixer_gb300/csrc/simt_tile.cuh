@@ -4,7 +4,8 @@
 // A thread owns an RM x 4 block of an M x N output: four consecutive columns n0 .. n0 + 3
 // and RM consecutive rows m0 ..  Every step k of a product reads one float4 of B's row k
 // (B row-major over the output's columns, leading dimension a multiple of 4, 16-byte
-// aligned) and RM values of A through two strides, so A may sit in either orientation.
+// aligned) and the block's RM values of A: from a row-major A one float4 per row serves
+// four steps (mac_r), from a column-major A one vector of RM floats serves a step (mac_c).
 // Consecutive threads take consecutive column groups, so the lanes of a warp read one
 // contiguous run of B (shared by the row groups of the warp: a broadcast) and the few A
 // values of their row groups.  Tiles that are read as A with their rows spread over a warp
@@ -23,47 +24,116 @@ constexpr int kThreads = 256;
 
 __host__ __device__ constexpr int pad(int x) { return x + 4; }
 
+// Shared memory of an SM (228 KB) and the most one CTA may take (227 KB); the runtime keeps
+// 1 KB per resident CTA.
+constexpr size_t kSmemPerSm = 233472, kSmemPerCta = 232448, kSmemReserved = 1024;
+
+// CTAs of `bytes` dynamic shared memory that fit on one SM (shared memory only).
+__host__ __device__ constexpr int ctas_per_sm(size_t bytes) {
+    return bytes > kSmemPerCta ? 0 : (int)(kSmemPerSm / (bytes + kSmemReserved));
+}
+
+// Whether `extra` more floats of shared memory beside `floats` are free for a kernel of at most
+// `max_ctas` resident CTAs per SM: they fit, and as many CTAs stay resident.
+__host__ __device__ constexpr int min_ctas(int a, int b) { return a < b ? a : b; }
+__host__ __device__ constexpr bool fits_beside(size_t floats, size_t extra, int max_ctas) {
+    return ctas_per_sm((floats + extra) * 4) >= 1 &&
+           min_ctas(ctas_per_sm((floats + extra) * 4), max_ctas) >= min_ctas(ctas_per_sm(floats * 4), max_ctas);
+}
+
 template <int RM>
 using Acc = float[RM][4];
 
-// acc += sum_{k0 <= k < k1} A(i, k) B(k, 0..3),  A(i, k) = A[i * sam + k * sak]
+// RM values a[0 .. RM) from 16-byte aligned consecutive floats
 template <int RM>
-__device__ __forceinline__ void mac(Acc<RM>& acc, const float* A, int sam, int sak, const float* B, int ldb, int k0,
-                                    int k1) {
-#pragma unroll 4
-    for (int k = k0; k < k1; ++k) {
-        const float4 b = *reinterpret_cast<const float4*>(B + (size_t)k * ldb);
-#pragma unroll
-        for (int i = 0; i < RM; ++i) {
-            const float x = A[i * sam + k * sak];
-            acc[i][0] = fmaf(x, b.x, acc[i][0]);
-            acc[i][1] = fmaf(x, b.y, acc[i][1]);
-            acc[i][2] = fmaf(x, b.z, acc[i][2]);
-            acc[i][3] = fmaf(x, b.w, acc[i][3]);
-        }
+__device__ __forceinline__ void ldv(float (&a)[RM], const float* p) {
+    if constexpr (RM == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(p);
+        a[0] = t.x;
+        a[1] = t.y;
+        a[2] = t.z;
+        a[3] = t.w;
+    } else if constexpr (RM == 2) {
+        const float2 t = *reinterpret_cast<const float2*>(p);
+        a[0] = t.x;
+        a[1] = t.y;
+    } else {
+        a[0] = p[0];
     }
 }
 
-// The same with a weight w(k) on every B row.
-template <int RM, class Wk>
-__device__ __forceinline__ void mac_w(Acc<RM>& acc, const float* A, int sam, int sak, const float* B, int ldb, int k0,
-                                      int k1, Wk w) {
+template <int RM>
+__device__ __forceinline__ void fma_row(Acc<RM>& acc, const float (&a)[RM], const float4& b) {
+#pragma unroll
+    for (int i = 0; i < RM; ++i) {
+        acc[i][0] = fmaf(a[i], b.x, acc[i][0]);
+        acc[i][1] = fmaf(a[i], b.y, acc[i][1]);
+        acc[i][2] = fmaf(a[i], b.z, acc[i][2]);
+        acc[i][3] = fmaf(a[i], b.w, acc[i][3]);
+    }
+}
+
+__device__ __forceinline__ float4 ldb4(const float* B, int ldb, int k) {
+    return *reinterpret_cast<const float4*>(B + (size_t)k * ldb);
+}
+
+__device__ __forceinline__ float4 scale4(float4 b, float s) {
+    b.x *= s;
+    b.y *= s;
+    b.z *= s;
+    b.w *= s;
+    return b;
+}
+
+struct NoWeight {
+    __device__ __forceinline__ float operator()(int) const { return 1.f; }
+};
+
+// acc += sum_{0 <= k < k1} A[i][k] w(k) B(k, 0..3) with A row-major (lda, 16-byte aligned
+// rows): four k at a time, one float4 of every A row.
+template <int RM, class Wk = NoWeight>
+__device__ __forceinline__ void mac_r(Acc<RM>& acc, const float* A, int lda, const float* B, int ldb, int k1,
+                                      Wk w = Wk{}) {
+    constexpr bool kW = !std::is_same<Wk, NoWeight>::value;
+    const int k4 = k1 & ~3;
+#pragma unroll 2
+    for (int k = 0; k < k4; k += 4) {
+        float4 a[RM];
+#pragma unroll
+        for (int i = 0; i < RM; ++i) a[i] = *reinterpret_cast<const float4*>(A + i * lda + k);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float4 b = ldb4(B, ldb, k + u);
+            if (kW) b = scale4(b, w(k + u));
+            float x[RM];
+#pragma unroll
+            for (int i = 0; i < RM; ++i) x[i] = u == 0 ? a[i].x : u == 1 ? a[i].y : u == 2 ? a[i].z : a[i].w;
+            fma_row<RM>(acc, x, b);
+        }
+    }
+    for (int k = k4; k < k1; ++k) {
+        float4 b = ldb4(B, ldb, k);
+        if (kW) b = scale4(b, w(k));
+        float x[RM];
+#pragma unroll
+        for (int i = 0; i < RM; ++i) x[i] = A[i * lda + k];
+        fma_row<RM>(acc, x, b);
+    }
+}
+
+// acc += sum_{k0 <= k < k1} A[k][i] w(k) B(k, 0..3) with A column-major (row k of A holds the
+// RM values of this block contiguously, 4 * RM-byte aligned): one vector load of A per k.
+template <int RM, class Wk = NoWeight>
+__device__ __forceinline__ void mac_c(Acc<RM>& acc, const float* A, int lda, const float* B, int ldb, int k0, int k1,
+                                      Wk w = Wk{}) {
+    constexpr bool kW = !std::is_same<Wk, NoWeight>::value;
 #pragma unroll 4
     for (int k = k0; k < k1; ++k) {
-        float4 b = *reinterpret_cast<const float4*>(B + (size_t)k * ldb);
-        const float s = w(k);
-        b.x *= s;
-        b.y *= s;
-        b.z *= s;
-        b.w *= s;
-#pragma unroll
-        for (int i = 0; i < RM; ++i) {
-            const float x = A[i * sam + k * sak];
-            acc[i][0] = fmaf(x, b.x, acc[i][0]);
-            acc[i][1] = fmaf(x, b.y, acc[i][1]);
-            acc[i][2] = fmaf(x, b.z, acc[i][2]);
-            acc[i][3] = fmaf(x, b.w, acc[i][3]);
-        }
+        float4 b = ldb4(B, ldb, k);
+        if (kW) b = scale4(b, w(k));
+        float x[RM];
+        ldv<RM>(x, A + (size_t)k * lda);
+        fma_row<RM>(acc, x, b);
     }
 }
 
