@@ -946,12 +946,16 @@ int fo_forward_part(const void* q, const void* k, const void* v, const Plan& p, 
         (p.nseg > 1 && launch_linear_scan(f(L.SB), f(L.Sin), p.BH, p.H, p.nseg - 1, E, p.nseg * E, p.nseg * E, true,
                                           gamma, seg_tokens, 1, st)))
         return cuda_fail("key moment scan");
+    // p = LA_g(q, k, k) in the pipelined order of the passes without a next summary, then the
+    // (p, v) summaries at decay g^2 in a summary pass of their own
     a.pow = 1;
-    a.pow_next = 2;
     a.carry = f(L.Sin);
     a.carry_mode = 0;
+    if (fo_out(a, p.d, q, k, nullptr, false, 0, nullptr, nullptr, ws + L.P, false, st)) return cuda_fail("p pass");
+    a.pow = 2;
+    a.carry = nullptr;
     a.summary = f(L.ZB);
-    if (fo_out(a, p.d, q, k, nullptr, false, 2, v, nullptr, ws + L.P, false, st)) return cuda_fail("p pass");
+    if (fo_summary(a, p.d, ws + L.P, v, false, st)) return cuda_fail("Z summaries");
     if (launch_fo_zero_first(f(L.Zin), p.BH, p.nseg, (int)E, nullptr, st) ||
         (p.nseg > 1 && launch_linear_scan(f(L.ZB), f(L.Zin), p.BH, p.H, p.nseg - 1, E, p.nseg * E, p.nseg * E, true,
                                           gamma, seg_tokens, 2, st)))
@@ -1040,7 +1044,8 @@ int fo_final_state(const void* q, const void* v, const Plan& p, const float* gam
     if (fo_summary(a, p.d, q, v, false, st)) return cuda_fail("query-value summaries");
     if (launch_fo_moments(q, ws + L.P, f(L.mB), f(L.yB), p.BH, p.H, p.n, p.d, p.nseg, seg_tokens, gamma, st))
         return cuda_fail("segment moments");
-    if (cudaMemsetAsync(ws + L.Cl, 0, L.carries_bytes, st) != cudaSuccess) return cuda_fail("carry reset");
+    // (one segment: the final-state kernel reads no carries)
+    if (p.nseg > 1 && cudaMemsetAsync(ws + L.Cl, 0, L.carries_bytes, st) != cudaSuccess) return cuda_fail("carry reset");
     if (p.nseg > 1 &&
         (launch_linear_scan(f(L.CB), f(L.Cl), p.BH, p.H, p.nseg - 1, E, p.nseg * E, E, false, gamma, seg_tokens, 1,
                             st) ||

@@ -763,6 +763,7 @@ int launch_fo64_tc_out(const FoArgs& a, const void* x, const void* k, const void
                           f64::OutLayout<R2, KVS, XVS, ADD, f64::Cols<R2, NSUM>::kTwoA>::kSmemBytes, m, a, st, \
                           f64::kThreadsOut);
     HLA2_F64(false, true, false, true, true, false)    // p = LA(q, k, k), next summary over (p, v)
+    HLA2_F64(false, false, false, true, false, false)   // p = LA(q, k, k) (the summary over (p, v) apart)
     HLA2_F64(false, false, false, false, false, false) // o = LA(q, p, v);  Z dO = LA(dO, v, p)
     HLA2_F64(true, true, false, false, false, false)   // dp = RLA(v, dO, q), next summary over (dp, q)
     HLA2_F64(true, false, false, false, false, false)  // dv = RLA(p, q, dO)

@@ -806,6 +806,7 @@ int launch_fo_tc_out(const FoArgs& a, const void* x, const void* k, const void* 
                          la::OutLayout<R2, KVS, XVS, ADD>::kSmemBytes, m, a, st, la::kThreadsOut);
     // the passes of the d = 128 training path
     HLA2_LA(false, true, false, true, true, false)    // p = LA(q, k, k), next summary over (p, v)
+    HLA2_LA(false, false, false, true, false, false)   // p = LA(q, k, k) (the summary over (p, v) apart)
     HLA2_LA(false, false, false, false, false, false) // o = LA(q, p, v);  dq_a = LA(dO, v, p)
     HLA2_LA(true, true, false, false, false, false)   // dp = RLA(v, dO, q), next summary over (dp, q)
     HLA2_LA(true, false, false, false, false, false)  // dv = RLA(p, q, dO)

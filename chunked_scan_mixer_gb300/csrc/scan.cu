@@ -14,6 +14,7 @@
 //   2. independent products X_s = Z_B[s] + rho S_in[s] C_B[s] (cross_kernel),
 //   3. a decayed (rho^2) prefix sum of X (linear_scan_kernel again).
 #include "kernels.h"
+#include "simt_tile.cuh"
 
 namespace hla2 {
 
@@ -366,7 +367,8 @@ __global__ void __launch_bounds__(kThreads) fo_moments_kernel(const bf16* __rest
     __shared__ float red_m[ROWS][HALF + 1], red_y[ROWS][HALF + 1];
     pdl_trigger();
     pdl_wait();
-    const int s = blockIdx.x, bh = blockIdx.y, z = blockIdx.z, tid = threadIdx.x;
+    // the column quarters of a segment run next to each other, so that they read whole rows
+    const int z = blockIdx.x % (D / HALF), s = blockIdx.x / (D / HALF), bh = blockIdx.y, tid = threadIdx.x;
     const int row = tid / 4, j = tid % 4;
     const int t0 = s * seg_tokens, t1 = min(t0 + seg_tokens, n);
     const float log2g = log2f(head_decay(gamma, bh, H));
@@ -376,17 +378,27 @@ __global__ void __launch_bounds__(kThreads) fo_moments_kernel(const bf16* __rest
     float am[8], ay[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) am[u] = ay[u] = 0.f;
-    for (int t = t0 + row; t < t1; t += ROWS) {
-        const uint4 qv = *reinterpret_cast<const uint4*>(qh + (size_t)t * D);
-        const uint4 pv = *reinterpret_cast<const uint4*>(ph + (size_t)t * D);
-        const float w = pow_decay(log2g, (float)(t1 - 1 - t)), w2 = w * w;
-        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, pw[4] = {pv.x, pv.y, pv.z, pv.w};
+    constexpr int U = 4;  // rows of a thread whose loads are issued together
+    for (int tb = t0 + row; tb < t1; tb += U * ROWS) {
+        uint4 qv[U], pv[U];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            am[2 * e] += w * __uint_as_float(qw[e] << 16);
-            am[2 * e + 1] += w * __uint_as_float(qw[e] & 0xFFFF0000u);
-            ay[2 * e] += w2 * __uint_as_float(pw[e] << 16);
-            ay[2 * e + 1] += w2 * __uint_as_float(pw[e] & 0xFFFF0000u);
+        for (int u = 0; u < U; ++u) {
+            const int t = tb + u * ROWS;
+            qv[u] = t < t1 ? *reinterpret_cast<const uint4*>(qh + (size_t)t * D) : make_uint4(0, 0, 0, 0);
+            pv[u] = t < t1 ? *reinterpret_cast<const uint4*>(ph + (size_t)t * D) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = tb + u * ROWS;
+            const float w = t < t1 ? pow_decay(log2g, (float)(t1 - 1 - t)) : 0.f, w2 = w * w;
+            const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w}, pw[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                am[2 * e] += w * __uint_as_float(qw[e] << 16);
+                am[2 * e + 1] += w * __uint_as_float(qw[e] & 0xFFFF0000u);
+                ay[2 * e] += w2 * __uint_as_float(pw[e] << 16);
+                ay[2 * e + 1] += w2 * __uint_as_float(pw[e] & 0xFFFF0000u);
+            }
         }
     }
 #pragma unroll
@@ -404,21 +416,24 @@ __global__ void __launch_bounds__(kThreads) fo_moments_kernel(const bf16* __rest
     }
 }
 
-// Final state of the first-order-scan forward: CTA (rb, bh) forms rows 16 rb .. 16 rb + 15 of
-// every part from shared-memory copies of the combined C (all of it), its 16 rows of S, and m;
-// thread (r, c) forms row r and columns D/16 * c .. of G.
+// Final state of the first-order-scan forward: CTA (rb, bh) forms rows 32 rb .. 32 rb + 31 of
+// every part.  The combined C (all D rows) and the CTA's rows of S sit in shared memory; the
+// rows of G = S C come from the register-tiled products of simt_tile.cuh.  Loads are float4 and
+// issued together; with a single segment the carries into it are zero and are not read.
 template <int D>
 __global__ void __launch_bounds__(kThreads) fo_final_state_kernel(const FoFinal f, float* final_state) {
-    constexpr int RB = 16, CPT = D / 16;
+    constexpr int RB = 32, LDS = simt::pad(D), NC4 = D * D / 4 / kThreads, NS4 = RB * D / 4 / kThreads;
+    static_assert(NC4 * 4 * kThreads == D * D && NS4 * 4 * kThreads == RB * D, "whole float4 per thread");
     extern __shared__ __align__(16) float fsm[];
-    float* Cs = fsm;             // [D][D]
-    float* Ss = Cs + D * D;      // [RB][D]
-    float* ms = Ss + RB * D;     // [D]
-    float* ys = ms + D;          // [RB]
+    float* Cs = fsm;                // [D][D]
+    float* Ss = Cs + D * D;         // [RB][LDS]
+    float* ms = Ss + RB * LDS;      // [D]
+    float* ys = ms + D;             // [RB]
     pdl_trigger();
     pdl_wait();
     const int rb = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     const int r0 = RB * rb, last = f.nseg - 1;
+    const bool carry = f.nseg > 1;
     const int L = f.n - last * f.seg_tokens;
     const float rho = pow_decay(log2f(head_decay(f.gamma, bh, f.H)), (float)L), rho2 = rho * rho;
     const size_t si = (size_t)bh * f.nseg + last, DD = (size_t)D * D;
@@ -427,38 +442,64 @@ __global__ void __launch_bounds__(kThreads) fo_final_state_kernel(const FoFinal 
     const float *mB = f.mB + si * D, *yB = f.yB + si * D, *ml = f.ml + (size_t)bh * D, *yl = f.yl + (size_t)bh * D;
     float* o = final_state + (size_t)bh * raw_state_floats(D, D);
     const PackOff po = pack_off(D, D);
-    for (int i = tid; i < (int)DD; i += kThreads) {
-        Cs[i] = rho * Cl[i] + CB[i];
-        if (i >= r0 * D && i < (r0 + RB) * D) o[po.C + i] = Cs[i];
+    auto ld4 = [](const float* p) { return *reinterpret_cast<const float4*>(p); };
+    auto comb = [](float r, float4 a, float4 b) {  // r a + b
+        return make_float4(fmaf(r, a.x, b.x), fmaf(r, a.y, b.y), fmaf(r, a.z, b.z), fmaf(r, a.w, b.w));
+    };
+    {  // C = rho C_in + C_B, all rows; this CTA's rows to the state
+        float4 c[NC4];
+#pragma unroll
+        for (int k = 0; k < NC4; ++k) c[k] = ld4(CB + 4 * (tid + kThreads * k));
+        if (carry)
+#pragma unroll
+            for (int k = 0; k < NC4; ++k) c[k] = comb(rho, ld4(Cl + 4 * (tid + kThreads * k)), c[k]);
+#pragma unroll
+        for (int k = 0; k < NC4; ++k) {
+            const int e = 4 * (tid + kThreads * k);
+            *reinterpret_cast<float4*>(Cs + e) = c[k];
+            if (e >= r0 * D && e < (r0 + RB) * D) *reinterpret_cast<float4*>(o + po.C + e) = c[k];
+        }
     }
-    for (int i = tid; i < RB * D; i += kThreads) {
-        const size_t e = (size_t)r0 * D + i;
-        Ss[i] = rho * Sin[e] + SB[e];
-        o[po.S + e] = Ss[i];
+    {  // S = rho S_in + S_B, this CTA's rows
+        float4 sv[NS4];
+#pragma unroll
+        for (int k = 0; k < NS4; ++k) sv[k] = ld4(SB + (size_t)r0 * D + 4 * (tid + kThreads * k));
+        if (carry)
+#pragma unroll
+            for (int k = 0; k < NS4; ++k) sv[k] = comb(rho, ld4(Sin + (size_t)r0 * D + 4 * (tid + kThreads * k)), sv[k]);
+#pragma unroll
+        for (int k = 0; k < NS4; ++k) {
+            const int e = 4 * (tid + kThreads * k), r = e / D, c = e - r * D;
+            *reinterpret_cast<float4*>(Ss + r * LDS + c) = sv[k];
+            *reinterpret_cast<float4*>(o + po.S + (size_t)r0 * D + e) = sv[k];
+        }
     }
     for (int i = tid; i < D; i += kThreads) {
-        ms[i] = rho * ml[i] + mB[i];
+        ms[i] = carry ? fmaf(rho, ml[i], mB[i]) : mB[i];
         if (i >= r0 && i < r0 + RB) o[po.m + i] = ms[i];
     }
-    for (int i = tid; i < RB; i += kThreads) ys[i] = rho2 * yl[r0 + i] + yB[r0 + i];
+    for (int i = tid; i < RB; i += kThreads) ys[i] = carry ? fmaf(rho2, yl[r0 + i], yB[r0 + i]) : yB[r0 + i];
     __syncthreads();
-    const int r = tid / 16, c0 = (tid % 16) * CPT;
-    float acc[CPT];
+    // G = S C - (rho^2 Z_in + Z_B), this CTA's rows
+    simt::with_rm(RB, D, [&](auto t) {
+        constexpr int RM = decltype(t)::value;
+        simt::for_blocks<RM>(RB, D, [&](int m0, int n0) {
+            simt::Acc<RM> acc;
+            simt::zero(acc);
+            simt::mac_r<RM>(acc, Ss + m0 * LDS, LDS, Cs + n0, D, D);
 #pragma unroll
-    for (int u = 0; u < CPT; ++u) acc[u] = 0.f;
-    for (int x = 0; x < D; ++x) {
-        const float a = Ss[r * D + x];
-#pragma unroll
-        for (int u = 0; u < CPT; ++u) acc[u] += a * Cs[x * D + c0 + u];
-    }
-#pragma unroll
-    for (int u = 0; u < CPT; ++u) {
-        const size_t e = (size_t)(r0 + r) * D + c0 + u;
-        o[po.G + e] = acc[u] - (rho2 * Zin[e] + ZB[e]);
-    }
+            for (int i = 0; i < RM; ++i) {
+                const size_t e = (size_t)(r0 + m0 + i) * D + n0;
+                float4 z = ld4(ZB + e);
+                if (carry) z = comb(rho2, ld4(Zin + e), z);
+                const float g[4] = {acc[i][0] - z.x, acc[i][1] - z.y, acc[i][2] - z.z, acc[i][3] - z.w};
+                simt::st4(o + po.G + e, g);
+            }
+        });
+    });
     if (tid < RB) {  // h = S m - y
         float t = 0.f;
-        for (int x = 0; x < D; ++x) t += Ss[tid * D + x] * ms[x];
+        for (int x = 0; x < D; ++x) t = fmaf(Ss[tid * LDS + x], ms[x], t);
         o[po.h + r0 + tid] = t - ys[tid];
     }
 }
@@ -567,7 +608,7 @@ int launch_seg_moments64(const ChunkArgs& a, cudaStream_t st) {
 int launch_fo_moments(const void* q, const void* p, float* mB, float* yB, int BH, int H, int n, int d, int nseg,
                       int seg_tokens, const float* gamma, cudaStream_t st) {
     if (nseg <= 0 || BH <= 0) return 0;
-    const dim3 grid(nseg, BH, d / 32);
+    const dim3 grid(nseg * (d / 32), BH);
     const bf16 *qq = static_cast<const bf16*>(q), *pp = static_cast<const bf16*>(p);
     cudaError_t e = d == 64 ? launch_pdl(fo_moments_kernel<64>, grid, dim3(kThreads), 0, st, qq, pp, mB, yB, H, n, nseg,
                                          seg_tokens, gamma)
@@ -579,16 +620,16 @@ int launch_fo_moments(const void* q, const void* p, float* mB, float* yB, int BH
 
 int launch_fo_final_state(const FoFinal& f, float* final_state, cudaStream_t st) {
     if (f.nseg <= 0 || f.BH <= 0) return 0;
-    const size_t smem = ((size_t)f.d * f.d + 16 * (size_t)f.d + f.d + 16) * sizeof(float);
+    const size_t smem = ((size_t)f.d * f.d + 32 * (size_t)simt::pad(f.d) + f.d + 32) * sizeof(float);
     cudaError_t e;
     if (f.d == 128) {
         e = cudaFuncSetAttribute(fo_final_state_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            e = launch_pdl(fo_final_state_kernel<128>, dim3(f.d / 16, f.BH), dim3(kThreads), smem, st, f, final_state);
+            e = launch_pdl(fo_final_state_kernel<128>, dim3(f.d / 32, f.BH), dim3(kThreads), smem, st, f, final_state);
     } else if (f.d == 64) {
         e = cudaFuncSetAttribute(fo_final_state_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            e = launch_pdl(fo_final_state_kernel<64>, dim3(f.d / 16, f.BH), dim3(kThreads), smem, st, f, final_state);
+            e = launch_pdl(fo_final_state_kernel<64>, dim3(f.d / 32, f.BH), dim3(kThreads), smem, st, f, final_state);
     } else {
         e = cudaErrorInvalidValue;
     }
