@@ -478,33 +478,34 @@ int hla2_forward(const void* q, const void* k, const void* v, void* out, int B, 
         if (chunk_pass(0, stored_p ? p.nseg : steps, true, true)) return cuda_fail("segment summaries");
         if (tc_moments && launch_seg_moments64(a, st)) return cuda_fail("segment moments");
         mark(2);
-        if (launch_linear_scan(a.ws + L.SB, a.ws + L.Sin, a.BH, H, steps, dd, a.nsum * dd, p.nseg * dd, true,
-                               gamma, seg_tokens, 1, st))
-            return cuda_fail("key-moment scan");
+        // independent decayed prefixes share a launch (one alone keeps the plain scan kernel)
+        auto scans = [&](const ScanJob* jobs, int njobs) {
+            if (njobs == 1)
+                return launch_linear_scan(jobs[0].src, jobs[0].dst, a.BH, H, steps, jobs[0].E, jobs[0].src_hs,
+                                          jobs[0].dst_hs, jobs[0].store_all != 0, gamma, seg_tokens, jobs[0].power,
+                                          st);
+            return launch_linear_scans(jobs, njobs, a.BH, H, steps, gamma, seg_tokens, st);
+        };
+        const size_t dsz = (size_t)d;
+        ScanJob first[kMaxScanJobs];
+        int nfirst = 0;
+        first[nfirst++] = {a.ws + L.SB, a.ws + L.Sin, dd, a.nsum * dd, p.nseg * dd, 1, 1};
         if (unmasked) {
             // unmasked monoid: C and m (in the Z and y slots) are plain decayed prefixes
-            if (launch_linear_scan(a.ws + L.ZB, a.ws + L.Zin, a.BH, H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true,
-                                   gamma, seg_tokens, 1, st) ||
-                ((normalize || want_final) &&
-                 launch_linear_scan(a.ws + L.yB, a.ws + L.yin, a.BH, H, steps, d, a.nsum * (size_t)d,
-                                    p.nseg * (size_t)d, true, gamma, seg_tokens, 1, st)))
-                return cuda_fail("query-value scan");
-        } else if (want_final) {
-            if (launch_linear_scan(a.ws + L.CB, a.ws + L.Clast, a.BH, H, steps, ddv, a.nsum * ddv, ddv, false,
-                                   gamma, seg_tokens, 1, st) ||
-                launch_linear_scan(a.ws + L.mB, a.ws + L.mlast, a.BH, H, steps, d, a.nsum * (size_t)d, d, false,
-                                   gamma, seg_tokens, 1, st))
-                return cuda_fail("query-value scan");
+            first[nfirst++] = {a.ws + L.ZB, a.ws + L.Zin, ddv, a.nsum * ddv, p.nseg * ddv, 1, 1};
+            if (normalize || want_final) first[nfirst++] = {a.ws + L.yB, a.ws + L.yin, dsz, a.nsum * dsz, p.nseg * dsz, 1, 1};
+        } else if (want_final) {  // C and m carried into the last segment
+            first[nfirst++] = {a.ws + L.CB, a.ws + L.Clast, ddv, a.nsum * ddv, ddv, 0, 1};
+            first[nfirst++] = {a.ws + L.mB, a.ws + L.mlast, dsz, a.nsum * dsz, dsz, 0, 1};
         }
+        if (scans(first, nfirst)) return cuda_fail("key-moment scan");
         // the denominator moment y is read only by the normalised output and the final state
         const bool with_y = normalize || want_final;
         if (!unmasked) {
             if (launch_cross(a, d, dv, with_y, st)) return cuda_fail("cross terms");
-            if (launch_linear_scan(a.ws + L.ZB, a.ws + L.Zin, a.BH, H, steps, ddv, a.nsum * ddv, p.nseg * ddv, true,
-                                   gamma, seg_tokens, 2, st) ||
-                (with_y && launch_linear_scan(a.ws + L.yB, a.ws + L.yin, a.BH, H, steps, d, a.nsum * (size_t)d,
-                                              p.nseg * (size_t)d, true, gamma, seg_tokens, 2, st)))
-                return cuda_fail("masked-summary scan");
+            const ScanJob second[2] = {{a.ws + L.ZB, a.ws + L.Zin, ddv, a.nsum * ddv, p.nseg * ddv, 1, 2},
+                                       {a.ws + L.yB, a.ws + L.yin, dsz, a.nsum * dsz, p.nseg * dsz, 1, 2}};
+            if (scans(second, with_y ? 2 : 1)) return cuda_fail("masked-summary scan");
         }
     } else {
         mark(2);

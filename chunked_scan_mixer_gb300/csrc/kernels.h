@@ -187,6 +187,22 @@ size_t fwd_chunk_simt_smem(int d, int dv, int W, bool track_cm);
 
 // Inter-segment scan and state conversion kernels (float32).
 int launch_init_carry(const ChunkArgs& a, int d, int dv, const float* init_state, cudaStream_t st);
+// One job of launch_linear_scans: a decayed prefix as launch_linear_scan computes it.
+struct ScanJob {
+    const float* src;
+    float* dst;
+    size_t E, src_hs, dst_hs;
+    int store_all, power;
+};
+constexpr int kMaxScanJobs = 3;
+struct ScanJobs {
+    ScanJob job[kMaxScanJobs];
+    int blocks[kMaxScanJobs];
+    int n;
+};
+// Up to kMaxScanJobs independent scans over the same heads and steps in one launch.
+int launch_linear_scans(const ScanJob* jobs, int njobs, int BH, int H, int nsteps, const float* gamma,
+                        int step_tokens, cudaStream_t st);
 int launch_linear_scan(const float* src, float* dst, int BH, int H, int nsteps, size_t E,
                        size_t src_head_stride, size_t dst_head_stride, bool store_all,
                        const float* gamma, int step_tokens, int power, cudaStream_t st);

@@ -105,6 +105,45 @@ __global__ void __launch_bounds__(kThreads)
     if (!store_all) d[0] = acc;
 }
 
+// Up to kMaxScanJobs independent linear scans (each as linear_scan_kernel) in one launch:
+// blocks [b_j, b_j + blocks_j) serve job j.
+__global__ void __launch_bounds__(kThreads)
+    linear_scans_kernel(const ScanJobs jobs, int BH, int H, int nsteps, const float* gamma, int step_tokens) {
+    pdl_trigger();
+    pdl_wait();
+    int j = 0, b = blockIdx.x;
+    while (j + 1 < jobs.n && b >= jobs.blocks[j]) b -= jobs.blocks[j++];
+    const ScanJob& J = jobs.job[j];
+    const size_t E = J.E;
+    const size_t gid = (size_t)b * kThreads + threadIdx.x;
+    if (gid >= (size_t)BH * E) return;
+    const int bh = (int)(gid / E);
+    const size_t e = gid % E;
+    const float rho = pow_decay(log2f(head_decay(gamma, bh, H)), (float)step_tokens * (float)J.power);
+    const float* src = J.src + (size_t)bh * J.src_hs + e;
+    float* dst = J.dst + (size_t)bh * J.dst_hs + e;
+    if (!HLA2_IN(e < E && (size_t)nsteps * E <= J.src_hs && (size_t)(J.store_all ? nsteps : 0) * E < J.dst_hs, 702))
+        return;
+    float acc = dst[0];
+    constexpr int U = 8;
+    int t = 0;
+    for (; t + U <= nsteps; t += U) {
+        float x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) x[u] = src[(size_t)(t + u) * E];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            acc = rho * acc + x[u];
+            if (J.store_all) dst[(size_t)(t + u + 1) * E] = acc;
+        }
+    }
+    for (; t < nsteps; ++t) {
+        acc = rho * acc + src[(size_t)t * E];
+        if (J.store_all) dst[(size_t)(t + 1) * E] = acc;
+    }
+    if (!J.store_all) dst[0] = acc;
+}
+
 // Copy n floats (n a multiple of 4, both pointers 16-byte aligned) from global to shared
 // memory: every load of a thread is issued before its first store, so that the L2 round
 // trips overlap.
@@ -314,41 +353,63 @@ __global__ void __launch_bounds__(kThreads) final_combine64_kernel(const ChunkAr
             acc[3] += av * bv.w;
         }
     };
+    // every global read of this thread issued before the first use: S_in and S_B rows, C_B and
+    // C_in (all rows), its Z_in and Z_B entries (float4 each)
+    constexpr int NC = D * D / 4 / kThreads;  // float4 of C per thread
+    static_assert(RB * D / 4 == kThreads && NC * 4 * kThreads == D * D, "one float4 of a row block per thread");
+    auto ld4 = [](const float* p) { return *reinterpret_cast<const float4*>(p); };
+    const float4 sin4 = ld4(Sin + (size_t)r0 * D + 4 * tid), sb4 = ld4(SB + (size_t)r0 * D + 4 * tid);
+    const size_t ez = (size_t)(r0 + r) * D + c4;
+    const float4 zin4 = ld4(Zin + ez), zb4 = ld4(ZB + ez);
+    float4 cb4[NC], cin4[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        cb4[k] = ld4(CB + 4 * (tid + kThreads * k));
+        cin4[k] = ld4(Cin + 4 * (tid + kThreads * k));
+    }
+    const float mb = tid < D ? mB[tid] : 0.f, mi = tid < D ? min_[tid] : 0.f;
+    const float yi = tid < RB ? yin[r0 + tid] : 0.f, yb = tid < RB ? yB[r0 + tid] : 0.f;
     // Z and y rows from the carry S_in and the last summary's C_B, m_B
-    copy_to_smem<RB * D>(Ss, Sin + (size_t)r0 * D, tid);
-    copy_to_smem<D * D>(Cs, CB, tid);
-    for (int i = tid; i < D; i += kThreads) ms[i] = mB[i];
+    *reinterpret_cast<float4*>(Ss + 4 * tid) = sin4;
+#pragma unroll
+    for (int k = 0; k < NC; ++k) *reinterpret_cast<float4*>(Cs + 4 * (tid + kThreads * k)) = cb4[k];
+    if (tid < D) ms[tid] = mb;
     __syncthreads();
     float zt[4], acc[4];
     product(acc);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const size_t e = (size_t)(r0 + r) * D + c4 + u;
-        zt[u] = rho2 * Zin[e] + ZB[e] + rho * acc[u];
-    }
+    zt[0] = rho2 * zin4.x + zb4.x + rho * acc[0];
+    zt[1] = rho2 * zin4.y + zb4.y + rho * acc[1];
+    zt[2] = rho2 * zin4.z + zb4.z + rho * acc[2];
+    zt[3] = rho2 * zin4.w + zb4.w + rho * acc[3];
     if (tid < RB) {
         float t = 0.f;
         for (int x = 0; x < D; ++x) t += Ss[tid * D + x] * ms[x];
-        ys[tid] = rho2 * yin[r0 + tid] + yB[r0 + tid] + rho * t;
+        ys[tid] = rho2 * yi + yb + rho * t;
     }
     __syncthreads();  // every product of S_in is done
     // S rows, all of C, and m after the last token (in place); this CTA writes its rows
-    for (int i = tid; i < RB * D; i += kThreads) {
-        Ss[i] = rho * Ss[i] + SB[(size_t)r0 * D + i];
-        o[po.S + (size_t)r0 * D + i] = Ss[i];
+    {
+        const float4 sv = make_float4(rho * sin4.x + sb4.x, rho * sin4.y + sb4.y, rho * sin4.z + sb4.z,
+                                      rho * sin4.w + sb4.w);
+        *reinterpret_cast<float4*>(Ss + 4 * tid) = sv;
+        *reinterpret_cast<float4*>(o + po.S + (size_t)r0 * D + 4 * tid) = sv;
     }
-    for (int i = tid; i < D * D; i += kThreads) {
-        Cs[i] = rho * Cin[i] + Cs[i];
-        if (i >= r0 * D && i < (r0 + RB) * D) o[po.C + i] = Cs[i];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int e = 4 * (tid + kThreads * k);
+        const float4 cv = make_float4(rho * cin4[k].x + cb4[k].x, rho * cin4[k].y + cb4[k].y,
+                                      rho * cin4[k].z + cb4[k].z, rho * cin4[k].w + cb4[k].w);
+        *reinterpret_cast<float4*>(Cs + e) = cv;
+        if (e >= r0 * D && e < (r0 + RB) * D) *reinterpret_cast<float4*>(o + po.C + e) = cv;
     }
-    for (int i = tid; i < D; i += kThreads) {
-        ms[i] = rho * min_[i] + ms[i];
-        if (i >= r0 && i < r0 + RB) o[po.m + i] = ms[i];
+    if (tid < D) {
+        ms[tid] = rho * mi + mb;
+        if (tid >= r0 && tid < r0 + RB) o[po.m + tid] = ms[tid];
     }
     __syncthreads();
     product(acc);  // G = S C - Z
 #pragma unroll
-    for (int u = 0; u < 4; ++u) o[po.G + (size_t)(r0 + r) * D + c4 + u] = acc[u] - zt[u];
+    for (int u = 0; u < 4; ++u) o[po.G + ez + u] = acc[u] - zt[u];
     if (tid < RB) {  // h = S m - y
         float t = 0.f;
         for (int x = 0; x < D; ++x) t += Ss[tid * D + x] * ms[x];
@@ -558,6 +619,24 @@ int launch_linear_scan(const float* src, float* dst, int BH, int H, int nsteps, 
     const unsigned blocks = (unsigned)((total + kThreads - 1) / kThreads);
     if (launch_pdl(linear_scan_kernel, dim3(blocks), dim3(kThreads), 0, st, src, dst, BH, H, nsteps, E, src_hs,
                    dst_hs, store_all ? 1 : 0, gamma, step_tokens, power) != cudaSuccess)
+        return -1;
+    return finish_launch();
+}
+
+int launch_linear_scans(const ScanJob* jobs, int njobs, int BH, int H, int nsteps, const float* gamma,
+                        int step_tokens, cudaStream_t st) {
+    if (njobs <= 0 || njobs > kMaxScanJobs) return -1;
+    if (BH <= 0 || nsteps <= 0) return 0;
+    ScanJobs J{};
+    unsigned total = 0;
+    for (int i = 0; i < njobs; ++i) {
+        J.job[i] = jobs[i];
+        J.blocks[i] = (int)(((size_t)BH * jobs[i].E + kThreads - 1) / kThreads);
+        total += (unsigned)J.blocks[i];
+    }
+    J.n = njobs;
+    if (launch_pdl(linear_scans_kernel, dim3(total), dim3(kThreads), 0, st, J, BH, H, nsteps, gamma, step_tokens) !=
+        cudaSuccess)
         return -1;
     return finish_launch();
 }
