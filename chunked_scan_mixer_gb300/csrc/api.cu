@@ -1500,6 +1500,17 @@ static int hla3_second_width(int dtype, int d, int dv, int chunk, int normalize,
     return 0;
 }
 
+// u = LA(q, k, v) on the d = 64 first-order scan kernels (bf16, d = w = 64, no first-order final
+// state): the (k, v) summaries of every segment, their prefix over the segments, one output
+// pass.  Workspace: the status word, then the summaries and the carries, [BH][nseg][64*64] fp32.
+static bool hla3_first_order_on_fo(bool bf, int d, int w, const float* final_P, const DevInfo& di) {
+    return bf && d == 64 && w == 64 && !final_P && fo_path(HLA2_BF16, 64, 64, 128, 0, di);
+}
+static size_t hla3_fo_bytes(int B, int H, int n, const DevInfo& di) {
+    const Plan p = fo_plan(B, H, n, 64, di);
+    return 256 + 2 * (size_t)p.BH * p.nseg * 64 * 64 * sizeof(float);
+}
+
 struct Hla3Layout {
     int W = 0;
     int W2 = 0;  // chunk width of the second-order passes
@@ -1530,6 +1541,10 @@ static Hla3Layout hla3_layout(int B, int H, int n, int d, int dv, int chunk, int
     size_t la = align64(L.Pin + BH * ns * (size_t)d * wmax) * sizeof(float);
     if (hla3_first_order_on_tc(dtype == HLA2_BF16, d, dv, di)) {
         const size_t t = ahla_layout(ahla_plan(B, H, n, d, 128)).total * sizeof(float);
+        la = la > t ? la : t;
+    }
+    if (dtype == HLA2_BF16 && d == 64 && dv == 64) {  // the first-order pass on the d = 64 scan kernels
+        const size_t t = hla3_fo_bytes(B, H, n, di);
         la = la > t ? la : t;
     }
     size_t f1 = hla2_forward_workspace_bytes(B, H, n, d, dv, chunk, dtype, 0, want_final);
@@ -1577,7 +1592,27 @@ extern "C" size_t hla2_hla3_forward_workspace_bytes(int B, int H, int n, int d, 
 // first-order pass u = masked linear attention (q, k, values) into `u`
 static int hla3_first_order(const void* q, const void* k, const void* vals, void* u, int B, int H, int n, int d,
                             int w, const Hla3Layout& L, void* ws, bool bf, cudaStream_t st, float* final_P) {
-    if (hla3_first_order_on_tc(bf, d, w, dev_info())) {
+    const DevInfo di = dev_info();
+    if (hla3_first_order_on_fo(bf, d, w, final_P, di)) {
+        const Plan pf = fo_plan(B, H, n, 64, di);
+        char* wsb = static_cast<char*>(ws);
+        const size_t E = 64 * 64;
+        float* SB = reinterpret_cast<float*>(wsb + 256);
+        float* Sin = SB + (size_t)pf.BH * pf.nseg * E;
+        FoArgs a = fo_args(pf, nullptr, wsb);
+        a.pow = 1;
+        a.summary = SB;
+        if (launch_fo_zero_first(Sin, pf.BH, pf.nseg, (int)E, a.status, st)) return cuda_fail("first-order carry-in");
+        if (fo_summary(a, 64, k, vals, false, st)) return cuda_fail("first-order summaries");
+        if (pf.nseg > 1 && launch_linear_scan(SB, Sin, pf.BH, pf.H, pf.nseg - 1, E, pf.nseg * E, pf.nseg * E, true,
+                                              nullptr, pf.seg_chunks * pf.W, 1, st))
+            return cuda_fail("first-order scan");
+        a.carry = Sin;
+        a.carry_mode = 0;
+        return fo_out(a, 64, q, k, vals, false, 0, nullptr, nullptr, u, false, st) ? cuda_fail("first-order pass")
+                                                                                  : HLA2_OK;
+    }
+    if (hla3_first_order_on_tc(bf, d, w, di)) {
         const Plan p = ahla_plan(B, H, n, d, 128);
         AhlaArgs a{};
         a.q = q;

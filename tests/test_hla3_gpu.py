@@ -74,9 +74,10 @@ def test_decay_is_refused():
 
 
 def test_bf16_first_order_paths_agree():
-    """bf16 d = dv = 64 runs the first-order pass on the AHLA tcgen05 kernel in its first-order
-    mode; with the tcgen05 kernels disabled it runs on the SIMT kernel.  Both against the
-    oracle, several segments."""
+    """bf16 d = dv = 64 without a final state runs the first-order pass on the d = 64 first-order
+    scan kernels (with a final state: the AHLA tcgen05 kernel in its first-order mode, covered by
+    the prefill tests below); with the tcgen05 kernels disabled it runs on the SIMT kernel.  Both
+    against the oracle, several segments."""
     import os
 
     x = inputs.make_custom(2, 4, 128 * 30 + 7, 64, 64, torch.bfloat16, seed=84)
