@@ -200,7 +200,17 @@ int blocks_per_sm(size_t smem, int threads, int cap, const DevInfo& di) {
 // waves x chunks-per-segment chunk steps, with waves = ceil(segments / resident CTAs).
 // The segment count per head minimises that (plus a small charge per segment for the
 // inter-segment scan), for `per_sm` resident CTAs per SM.
+// The same cut for a call whose passes run at two residencies: passes of weight wa at per_sm_a
+// resident CTAs and passes of weight wb at per_sm_b, cost = sum of weight x waves x chunks.
+Plan make_plan2(int B, int H, int n, int d, int dv, int W, int sms, int per_sm_a, double wa, int per_sm_b,
+                double wb);
+
 Plan make_plan(int B, int H, int n, int d, int dv, int W, int sms, int per_sm) {
+    return make_plan2(B, H, n, d, dv, W, sms, per_sm, 1.0, per_sm, 0.0);
+}
+
+Plan make_plan2(int B, int H, int n, int d, int dv, int W, int sms, int per_sm_a, double wa, int per_sm_b,
+                double wb) {
     Plan p;
     p.BH = B * H;
     p.H = H;
@@ -214,7 +224,9 @@ Plan make_plan(int B, int H, int n, int d, int dv, int W, int sms, int per_sm) {
         p.nseg = 0;
         return p;
     }
-    const long slots = (long)(per_sm < 1 ? 1 : per_sm) * (sms < 1 ? 1 : sms);
+    const long sm = sms < 1 ? 1 : sms;
+    const long slots_a = (long)(per_sm_a < 1 ? 1 : per_sm_a) * sm, slots_b = (long)(per_sm_b < 1 ? 1 : per_sm_b) * sm;
+    const long slots = slots_a > slots_b ? slots_a : slots_b;
     long max_ph = (4 * slots + p.BH - 1) / p.BH;
     if (max_ph < 1) max_ph = 1;
     if (max_ph > p.nchunks) max_ph = p.nchunks;
@@ -223,8 +235,9 @@ Plan make_plan(int B, int H, int n, int d, int dv, int W, int sms, int per_sm) {
     for (long ph = 1; ph <= max_ph; ++ph) {
         const long sc = (p.nchunks + ph - 1) / ph;
         const long ns = (p.nchunks + sc - 1) / sc;
-        const long waves = ((long)p.BH * ns + slots - 1) / slots;
-        const double cost = (double)waves * (double)sc + 0.05 * (double)ns;
+        const long waves_a = ((long)p.BH * ns + slots_a - 1) / slots_a;
+        const long waves_b = ((long)p.BH * ns + slots_b - 1) / slots_b;
+        const double cost = (wa * (double)waves_a + wb * (double)waves_b) * (double)sc + 0.05 * (double)ns;
         if (best < 0.0 || cost < best - 1e-9) {
             best = cost;
             best_sc = sc;
@@ -675,12 +688,6 @@ int backward_width_f32(int d, int dv, int chunk, const DevInfo& di) {
     return 0;
 }
 
-int backward_per_sm_f32(int d, int dv, int W, const DevInfo& di) {
-    const int b = blocks_per_sm(bwd_chunk_simt_smem(d, dv, W), 256, kSimtBwdCtas, di);
-    const int f = blocks_per_sm(fwd_chunk_simt_smem(d, dv, W, false), 256, kSimtFwdCtas, di);
-    return b < f ? b : f;
-}
-
 // Width, segmentation and workspace of an unnormalised backward call (W = 0: no kernel).
 struct BwdPlan {
     int W = 0;
@@ -694,8 +701,16 @@ BwdPlan backward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     bp.f32 = dtype == HLA2_F32;
     bp.W = bp.f32 ? backward_width_f32(d, dv, chunk, di) : backward_width(d, chunk, di);
     if (!bp.W) return bp;
-    const int per_sm = bp.f32 ? backward_per_sm_f32(d, dv, bp.W, di) : backward_per_sm(d, bp.W, di);
-    bp.p = make_plan(B, H, n, d, dv, bp.W, di.sms, per_sm);
+    if (bp.f32) {
+        // the two forward passes (segment summaries, state export) run at the forward kernel's
+        // residency, the two reverse passes at the reverse kernel's; per chunk the reverse pair
+        // costs about 1.5 times the forward pair (36 and 54 us at d = 64, dv = 80, W = 32)
+        const int f = blocks_per_sm(fwd_chunk_simt_smem(d, dv, bp.W, false), 256, kSimtFwdCtas, di);
+        const int b = blocks_per_sm(bwd_chunk_simt_smem(d, dv, bp.W), 256, kSimtBwdCtas, di);
+        bp.p = make_plan2(B, H, n, d, dv, bp.W, di.sms, f, 1.0, b, 1.5);
+    } else {
+        bp.p = make_plan(B, H, n, d, dv, bp.W, di.sms, backward_per_sm(d, bp.W, di));
+    }
     bp.L = bwd_layout(bp.p, bp.f32 ? sizeof(float) : sizeof(bf16));
     return bp;
 }
