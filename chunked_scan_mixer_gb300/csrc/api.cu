@@ -949,8 +949,10 @@ FoArgs fo_args(const Plan& p, const float* gamma, char* ws) {
 }
 
 // Forward scans up to the stored p: S summaries, S carries, p with the Z summaries, Z carries.
+// With final_sums (d = 128, a final state asked for) the (p, v) summaries come from one pass over
+// (q, p, v) that also forms the (q, v) summaries and the q and p moments the final state reads.
 int fo_forward_part(const void* q, const void* k, const void* v, const Plan& p, const float* gamma, char* ws,
-                    const FoLayout& L, cudaStream_t st) {
+                    const FoLayout& L, cudaStream_t st, bool final_sums = false) {
     auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
     const size_t E = (size_t)p.d * p.d;
     const int seg_tokens = p.seg_chunks * p.W;
@@ -968,10 +970,17 @@ int fo_forward_part(const void* q, const void* k, const void* v, const Plan& p, 
     a.carry = f(L.Sin);
     a.carry_mode = 0;
     if (fo_out(a, p.d, q, k, nullptr, false, 0, nullptr, nullptr, ws + L.P, false, st)) return cuda_fail("p pass");
-    a.pow = 2;
     a.carry = nullptr;
-    a.summary = f(L.ZB);
-    if (fo_summary(a, p.d, ws + L.P, v, false, st)) return cuda_fail("Z summaries");
+    if (final_sums) {
+        a.pow = 1;
+        a.summary = f(L.CB);
+        if (launch_fo_tc_summary_final(a, q, ws + L.P, v, f(L.ZB), f(L.mB), f(L.yB), st))
+            return cuda_fail("final-state summaries");
+    } else {
+        a.pow = 2;
+        a.summary = f(L.ZB);
+        if (fo_summary(a, p.d, ws + L.P, v, false, st)) return cuda_fail("Z summaries");
+    }
     if (launch_fo_zero_first(f(L.Zin), p.BH, p.nseg, (int)E, nullptr, st) ||
         (p.nseg > 1 && launch_linear_scan(f(L.ZB), f(L.Zin), p.BH, p.H, p.nseg - 1, E, p.nseg * E, p.nseg * E, true,
                                           gamma, seg_tokens, 2, st)))
@@ -1050,16 +1059,18 @@ size_t fo_forward_ws(int B, int H, int n, int d, int dv, int chunk, int dtype, i
 // moments (y from the stored full p), the carries of C, m, y into the last segment, and the
 // last segment's combine with G = S C - Z and h = S m - y.
 int fo_final_state(const void* q, const void* v, const Plan& p, const float* gamma, char* ws, const FoLayout& L,
-                   float* final_state, cudaStream_t st) {
+                   float* final_state, cudaStream_t st, bool sums_done = false) {
     auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
     const size_t E = (size_t)p.d * p.d;
     const int seg_tokens = p.seg_chunks * p.W;
-    FoArgs a = fo_args(p, gamma, ws);
-    a.pow = 1;
-    a.summary = f(L.CB);
-    if (fo_summary(a, p.d, q, v, false, st)) return cuda_fail("query-value summaries");
-    if (launch_fo_moments(q, ws + L.P, f(L.mB), f(L.yB), p.BH, p.H, p.n, p.d, p.nseg, seg_tokens, gamma, st))
-        return cuda_fail("segment moments");
+    if (!sums_done) {  // (q, v) summaries and the q, p moments (else formed by the forward part)
+        FoArgs a = fo_args(p, gamma, ws);
+        a.pow = 1;
+        a.summary = f(L.CB);
+        if (fo_summary(a, p.d, q, v, false, st)) return cuda_fail("query-value summaries");
+        if (launch_fo_moments(q, ws + L.P, f(L.mB), f(L.yB), p.BH, p.H, p.n, p.d, p.nseg, seg_tokens, gamma, st))
+            return cuda_fail("segment moments");
+    }
     // (one segment: the final-state kernel reads no carries)
     if (p.nseg > 1 && cudaMemsetAsync(ws + L.Cl, 0, L.carries_bytes, st) != cudaSuccess) return cuda_fail("carry reset");
     if (p.nseg > 1 &&
@@ -1111,11 +1122,12 @@ int fo_forward_call(const void* q, const void* k, const void* v, void* out, int 
     };
     cudaGetLastError();
     mark(0);
-    int rc = fo_forward_part(q, k, v, p, gamma, ws, L, st);
+    const bool fused = want_final && p.d == 128;  // the final state's summaries in the forward part's pass
+    int rc = fo_forward_part(q, k, v, p, gamma, ws, L, st, fused);
     mark(3);
     if (rc == HLA2_OK) rc = fo_output_pass(q, v, out, p, gamma, ws, L, st);
     mark(4);
-    if (rc == HLA2_OK && want_final) rc = fo_final_state(q, v, p, gamma, ws, L, opts->final_state, st);
+    if (rc == HLA2_OK && want_final) rc = fo_final_state(q, v, p, gamma, ws, L, opts->final_state, st, fused);
     mark(5);
     return rc == HLA2_OK ? succeed() : rc;
 }

@@ -731,6 +731,170 @@ __global__ void __launch_bounds__(la::kThreads, 1)
     if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
+// Final-state summaries in one pass over (q, p, v): per segment
+//   C_B = sum_i w_i q_i v_i^T,  Z_B = sum_i w_i^2 p_i v_i^T,  m_B = sum_i w_i q_i,  y_B = sum_i w_i^2 p_i,
+// with w_i = g^(t1-1-i) (decayed to the segment's end).  Two stages of (q, p, v) tiles; per chunk
+// the epilogue scales q by w and p by w^2 in place and keeps the moments' partial sums, and the
+// control thread accumulates Q~^T V (tensor-memory columns [0, 128)) and P~^T V ([128, 256)).
+// Epilogue thread e owns the 8-column group 8 (e % 16) .. of rows e / 16 + 16 i (i < 8).
+namespace las2 {
+constexpr uint32_t oQ = 0, oP = 2 * la::kTile, oV = 4 * la::kTile;  // 2 stages each
+constexpr uint32_t oRed = 6 * la::kTile;                             // moment partials [2][16][128] fp32
+constexpr uint32_t oBar = oRed + 2 * 16 * 128 * 4;
+constexpr uint32_t oMisc = oBar + 16 * 8;
+constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
+}  // namespace las2
+
+__global__ void __launch_bounds__(la::kThreads, 1)
+    fo_sum_final_tc_kernel(const __grid_constant__ la::Maps maps, const FoArgs a, float* zsum, float* msum,
+                           float* ysum) {
+    using namespace las2;
+    constexpr int kW = la::kW, kD = la::kD;
+    pdl_trigger();
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oBar);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sm + oMisc);
+    volatile int* abort = reinterpret_cast<volatile int*>(sm + oMisc + 4);
+    float* red = reinterpret_cast<float*>(sm + oRed);
+    int* status = a.status;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int seg = blockIdx.x, bh = blockIdx.y;
+    const FoSeg sg = la_seg(a, seg);
+    const int nit = sg.nit;
+    const float log2g = log2f(head_decay(a.gamma, bh, a.H));
+
+    if (tid == 0) {
+        for (int b = 0; b < las::kBarCount; ++b) tc::mbar_init(&bars[b], (b == las::T0 || b == las::T1) ? 8 : 1);
+        *abort = 0;
+        tc::mbar_fence_init();
+    }
+    pdl_wait();
+    if (warp == 0) tc::tmem_alloc(tmem_holder, 256);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0 && nit > 0) {
+            auto load = [&](int it) {
+                const int s = it & 1, c = sg.c_begin + it;
+                uint64_t* bar = &bars[las::F0 + s];
+                tc::mbar_arrive_expect_tx(bar, 3 * la::kTile);
+                const uint32_t o = s * la::kTile;
+                tc::tma_load_3d(sm + oQ + o, &maps.x, 0, c * kW, bh, bar);
+                tc::tma_load_3d(sm + oQ + o + la::kBlk, &maps.x, 64, c * kW, bh, bar);
+                tc::tma_load_3d(sm + oP + o, &maps.k, 0, c * kW, bh, bar);
+                tc::tma_load_3d(sm + oP + o + la::kBlk, &maps.k, 64, c * kW, bh, bar);
+                tc::tma_load_3d(sm + oV + o, &maps.v, 0, c * kW, bh, bar);
+                tc::tma_load_3d(sm + oV + o + la::kBlk, &maps.v, 64, c * kW, bh, bar);
+            };
+            constexpr uint32_t I_MM = tc::idesc_bf16(128, 128, 1, 1);
+            auto mdesc = [](uint32_t base, int ks) { return tc::smem_desc(base + 2048u * ks, la::kBlk, 1024); };
+            load(0);
+            if (nit > 1) load(1);
+            for (int it = 0; it < nit; ++it) {
+                const int s = it & 1;
+                const uint32_t ph = (it >> 1) & 1;
+                tc::mbar_wait(&bars[las::T0 + s], ph, abort, status, 131);  // Q~, P~ of this chunk written
+                tc::fence_after_sync();
+                const uint32_t o = s * la::kTile;
+                const uint32_t sQ = smem_u32(sm + oQ + o), sP = smem_u32(sm + oP + o), sV = smem_u32(sm + oV + o);
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem, mdesc(sQ, ks), mdesc(sV, ks), I_MM, (it > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem + 128, mdesc(sP, ks), mdesc(sV, ks), I_MM, (it > 0 || ks > 0) ? 1u : 0u);
+                tc::mma_commit(&bars[las::N0 + s]);
+                if (it + 2 < nit) {  // this stage's tiles are free once its products have run
+                    tc::mbar_wait(&bars[las::N0 + s], ph, abort, status, 132);
+                    load(it + 2);
+                }
+            }
+            volatile int never = 0;
+            tc::mbar_wait(&bars[las::N0 + ((nit - 1) & 1)], ((nit - 1) >> 1) & 1, &never, nullptr, 0);
+            if (nit > 1) tc::mbar_wait(&bars[las::N0 + ((nit - 2) & 1)], ((nit - 2) >> 1) & 1, &never, nullptr, 0);
+        }
+        __syncwarp();
+    } else {
+        const int e = tid - 32, cc = e % 16, b = cc / 8, j = cc % 8, r0 = e / 16;
+        float mq[8], yp[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mq[u] = yp[u] = 0.f;
+        for (int it = 0; it < nit; ++it) {
+            const int s = it & 1;
+            const uint32_t ph = (it >> 1) & 1;
+            const int c = sg.c_begin + it;
+            const int Wc = min(kW, a.n - c * kW);
+            tc::mbar_wait(&bars[las::F0 + s], ph, abort, status, 133);
+            unsigned char* sQ = sm + oQ + s * la::kTile;
+            unsigned char* sP = sm + oP + s * la::kTile;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = r0 + 16 * i;
+                const int pos = (c - sg.c_begin) * kW + r;
+                const float w1 = r < Wc ? pow_decay(log2g, (float)(sg.L - 1 - pos)) : 0.f, w2 = w1 * w1;
+                const uint32_t off = la_off(b, r, j);
+                const uint4 qc = *reinterpret_cast<const uint4*>(sQ + off);
+                const uint4 pc = *reinterpret_cast<const uint4*>(sP + off);
+                const uint32_t qw[4] = {qc.x, qc.y, qc.z, qc.w}, pw[4] = {pc.x, pc.y, pc.z, pc.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    mq[2 * u] += w1 * __uint_as_float(qw[u] << 16);
+                    mq[2 * u + 1] += w1 * __uint_as_float(qw[u] & 0xFFFF0000u);
+                    yp[2 * u] += w2 * __uint_as_float(pw[u] << 16);
+                    yp[2 * u + 1] += w2 * __uint_as_float(pw[u] & 0xFFFF0000u);
+                }
+                *reinterpret_cast<uint4*>(sQ + off) = la_scale_chunk(qc, w1);
+                *reinterpret_cast<uint4*>(sP + off) = la_scale_chunk(pc, w2);
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[las::T0 + s]);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            red[r0 * kD + 64 * b + 8 * j + u] = mq[u];
+            red[16 * kD + r0 * kD + 64 * b + 8 * j + u] = yp[u];
+        }
+        if (nit > 0 && HLA2_IN(bh < a.BH && seg < a.nseg, 805)) {  // C_B and Z_B rows of this warp's lanes
+            const int q4 = warp & 3, h = (warp - 1) >> 2;
+            const int r = 32 * q4 + lane;
+            const uint32_t lrow = tmem + ((uint32_t)(32 * q4) << 16);
+            tc::mbar_wait(&bars[las::N0 + ((nit - 1) & 1)], ((nit - 1) >> 1) & 1, abort, status, 134);
+            tc::fence_after_sync();
+            const size_t si = (size_t)bh * a.nseg + seg;
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                float* dst = (part ? zsum : a.summary) + si * kD * kD + (size_t)r * kD + 64 * h;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(lrow + 128 * part + 64 * h + 32 * p, v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + 32 * p + i) =
+                            make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                                        __uint_as_float(v[i + 3]));
+                }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid < 2 * kD && HLA2_IN(bh < a.BH && seg < a.nseg, 806)) {  // moments: the 16 row groups in a fixed order
+        const int part = tid / kD, col = tid % kD;
+        float t = 0.f;
+        for (int g = 0; g < 16; ++g) t += red[part * 16 * kD + g * kD + col];
+        (part ? ysum : msum)[((size_t)bh * a.nseg + seg) * kD + col] = t;
+    }
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
 // Zeroes the carry into segment 0 of every head ([BH][nseg][E], segment 0; E = d * d) and
 // clears the status word, before a forward linear scan fills the other segments.
 __global__ void fo_zero_first_kernel(float* carry, int nseg, int E, int BH, int* status) {
@@ -761,7 +925,7 @@ size_t fo_tc_max_smem() {
                               la::OutLayout<false, false, false, false>::kSmemBytes,  // o, Z dO, dv
                               la::OutLayout<true, false, false, false>::kSmemBytes,   // dk
                               la::OutLayout<false, true, false, true>::kSmemBytes,    // dq
-                              las::Layout<false>::kSmemBytes, las::Layout<true>::kSmemBytes};
+                              las::Layout<false>::kSmemBytes, las::Layout<true>::kSmemBytes, las2::kSmemBytes};
     uint32_t m = 0;
     for (uint32_t x : sizes) m = x > m ? x : m;
     return m;
@@ -770,6 +934,21 @@ size_t fo_tc_max_smem() {
 int launch_fo_zero_first(float* carry, int BH, int nseg, int E, int* status, cudaStream_t st) {
     if (BH <= 0) return 0;
     if (launch_pdl(fo_zero_first_kernel, dim3(BH), dim3(256), 0, st, carry, nseg, E, BH, status) != cudaSuccess)
+        return -1;
+    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_fo_tc_summary_final(const FoArgs& a, const void* q, const void* p, const void* v, float* zsum,
+                               float* msum, float* ysum, cudaStream_t st) {
+    if (a.BH <= 0 || a.nseg <= 0) return 0;
+    if (!a.summary || !zsum || !msum || !ysum) return -2;
+    la::Maps m{};
+    if (!la_map(&m.x, q, a.BH, a.n) || !la_map(&m.k, p, a.BH, a.n) || !la_map(&m.v, v, a.BH, a.n)) return -2;
+    if (cudaFuncSetAttribute(fo_sum_final_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)las2::kSmemBytes) != cudaSuccess)
+        return -1;
+    if (launch_pdl(fo_sum_final_tc_kernel, dim3(a.nseg, a.BH), dim3(la::kThreads), las2::kSmemBytes, st, m, a, zsum,
+                   msum, ysum) != cudaSuccess)
         return -1;
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

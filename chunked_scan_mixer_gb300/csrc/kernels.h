@@ -295,6 +295,11 @@ size_t fo_tc_max_smem();
 int launch_fo_zero_first(float* carry, int BH, int nseg, int E, int* status, cudaStream_t st);
 // summary[s] = sum_{i in s} g^(distance to the segment's end (forward) / start (reverse)) k_i v_i^T
 int launch_fo_tc_summary(const FoArgs& a, const void* k, const void* v, bool reverse, cudaStream_t st);
+// The final state's summaries in one pass over (q, p, v), d = dv = 128, per segment:
+// summary = sum_i w_i q_i v_i^T, zsum = sum_i w_i^2 p_i v_i^T, msum = sum_i w_i q_i,
+// ysum = sum_i w_i^2 p_i ([BH][nseg][128] for the moments), w_i = g^(distance to the segment's end).
+int launch_fo_tc_summary_final(const FoArgs& a, const void* q, const void* p, const void* v, float* zsum,
+                               float* msum, float* ysum, cudaStream_t st);
 // out = (R)LA(x, k, v) with the carry (v == NULL: the values are the keys); r2 adds the swapped
 // pair (v, k); next_sum 1 / 2 also writes the next summary over (out, the values) / (out, xv);
 // add != NULL adds that partial.
