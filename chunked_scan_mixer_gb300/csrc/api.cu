@@ -601,30 +601,34 @@ int hla2_forward_plan(int B, int H, int n, int d, int dv, int chunk, int dtype, 
     const int W = forward_width(dtype, d, dv, chunk, normalize, di);
     if (!W) return fail(HLA2_ERR_UNSUPPORTED, "no forward kernel for d %d, dv %d at chunk <= %d", d, dv, chunk);
     if (fo_forward_ws(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0)) {
-        // first-order scans: S summaries, zero + scan, p pass, zero + scan, output pass; with a
-        // final state also the (q, v) summaries, the moments, three scans and the final combine
+        // first-order scans: S summaries, zero (+ scan), p pass, (p, v) summaries (with a final
+        // state: the pass that also forms the (q, v) summaries and the moments), zero (+ scan),
+        // output pass; with a final state also the final combine (+ the last-only scans of C, m, y)
         const Plan p = fo_plan(B, H, n, d, di);
+        const bool many = p.nseg > 1;
         if (nseg) *nseg = p.nseg;
         if (seg_chunks) *seg_chunks = p.seg_chunks;
-        if (launches) *launches = p.nseg > 0 ? 7 + (want_final_state ? 3 + (p.nseg > 1 ? 3 : 0) : 0) : 0;
+        if (launches)
+            *launches = p.nseg > 0 ? 6 + (many ? 2 : 0) + (want_final_state ? 1 + (many ? 1 : 0) : 0) : 0;
         return succeed();
     }
     chunk = W;
     const Plan p = forward_plan(B, H, n, d, dv, chunk, dtype, normalize, want_final_state != 0, di);
     int l = 0;
     const bool tc = choose_forward_path(dtype, d, dv, chunk, normalize, want_final_state != 0, di) == Path::kTc;
+    // (the launch counts of the masked output; independent scans share one launch: S with C
+    // and m, Z with y)
     if (p.nseg > 0 && want_final_state && tc) {
-        // carry-in, summary (with the segment moments), output, final combine; S, C, m scans,
-        // cross terms, Z and y scans (the launch count of the masked output)
-        l = 4 + (p.nseg > 1 ? 6 : 0);
+        // carry-in, summary (with the segment moments), output, final combine; the S (C, m)
+        // scan, cross terms, the Z (y) scan
+        l = 4 + (p.nseg > 1 ? 3 : 0);
     } else if (p.nseg > 0 && normalize && tc) {
         // carry-in, summary (it stores p and forms the moments), output; S scan, cross terms,
-        // Z and y scans
-        l = 3 + (p.nseg > 1 ? 4 : 0);
+        // the Z (y) scan
+        l = 3 + (p.nseg > 1 ? 3 : 0);
     } else if (p.nseg > 0) {
         l = 2;                                                   // carry-in, output pass
-        if (p.nseg > 1)                                          // summary, S/Z scans, cross; y, C, m scans
-            l += 4 + (normalize || want_final_state ? 1 : 0) + (want_final_state ? 2 : 0);
+        if (p.nseg > 1) l += 4;                                  // summary, S (C, m) scan, cross, Z (y) scan
         if (want_final_state) l += 1 + (p.nseg > 1 ? 1 : 0);     // finalize, last-segment pass
     } else if (want_final_state && (long)B * H > 0) {
         l = 0;                                                   // a copy or memset only
@@ -1073,14 +1077,14 @@ int fo_final_state(const void* q, const void* v, const Plan& p, const float* gam
     }
     // (one segment: the final-state kernel reads no carries)
     if (p.nseg > 1 && cudaMemsetAsync(ws + L.Cl, 0, L.carries_bytes, st) != cudaSuccess) return cuda_fail("carry reset");
-    if (p.nseg > 1 &&
-        (launch_linear_scan(f(L.CB), f(L.Cl), p.BH, p.H, p.nseg - 1, E, p.nseg * E, E, false, gamma, seg_tokens, 1,
-                            st) ||
-         launch_linear_scan(f(L.mB), f(L.ml), p.BH, p.H, p.nseg - 1, p.d, p.nseg * (size_t)p.d, p.d, false, gamma,
-                            seg_tokens, 1, st) ||
-         launch_linear_scan(f(L.yB), f(L.yl), p.BH, p.H, p.nseg - 1, p.d, p.nseg * (size_t)p.d, p.d, false, gamma,
-                            seg_tokens, 2, st)))
-        return cuda_fail("last-segment carries");
+    if (p.nseg > 1) {  // C, m and y carried into the last segment, in one launch
+        const size_t dz = (size_t)p.d;
+        const ScanJob jobs[3] = {{f(L.CB), f(L.Cl), E, p.nseg * E, E, 0, 1},
+                                 {f(L.mB), f(L.ml), dz, p.nseg * dz, dz, 0, 1},
+                                 {f(L.yB), f(L.yl), dz, p.nseg * dz, dz, 0, 2}};
+        if (launch_linear_scans(jobs, 3, p.BH, p.H, p.nseg - 1, gamma, seg_tokens, st))
+            return cuda_fail("last-segment carries");
+    }
     FoFinal fin{};
     fin.SB = f(L.SB);
     fin.Sin = f(L.Sin);
