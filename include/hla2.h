@@ -214,13 +214,15 @@ size_t hla2_backward_workspace_bytes(int B, int H, int n, int d, int dv, int chu
  * run on the tensor-core kernels (chunk width <= 64, <= 32 at d = 128); float32 tensors of
  * any d, dv on SIMT float32 kernels (chunk width <= 32).
  * normalize == 0: gradients of the unnormalised output.  normalize == 1: gradients of
- * o / (den + opts->eps) by the quotient rule (section summary §5.1), as two unnormalised
- * passes -- one with (v, dout / (den + eps)), one with the value rows (1, 0, ..., 0)
- * and the upstream gradient -(dout . num) / (den + eps)^2 in column 0 -- after two
- * unnormalised forwards for num and den.  The two passes' dq and dk can each be tens of
- * times larger than their sum, so this composition always runs in float32 (bf16 tensors
- * are widened first and the gradients rounded at the end; any d, dv); the workspace then
- * also holds those float32 intermediates.  init_state and final_state in opts must be NULL
+ * o / (den + opts->eps) by the quotient rule (section summary §5.1).  num and den are the
+ * unnormalised outputs for the values v and for the value rows (1, 0, ..., 0), so the call
+ * runs one unnormalised backward with the widened values [v | 1 | 0 ...] (dv + 16 columns):
+ * its forward part gives [num | den], the upstream gradient is
+ * [dout / (den + eps) | -(dout . num) / (den + eps)^2 | 0 ...], and its reverse part gives dq,
+ * dk and [dv | .].  dq and dk are then the sum of a numerator part and a denominator part that
+ * can each be tens of times larger than the sum, so this composition always runs in float32
+ * (bf16 tensors are widened first and the gradients rounded at the end; any d, dv); the
+ * workspace then also holds those float32 intermediates.  init_state and final_state in opts must be NULL
  * (gradients start from the empty state); HLA2_FLAG_STATES_SAVED needs bf16 and
  * normalize == 0.
  */
