@@ -599,19 +599,21 @@ __global__ void __launch_bounds__(la::kThreadsOut, 1)
 
 // ----------------------------------------------------------------------------------------
 // Summary kernel: Sig_B[s] = sum_{i in s} w_i k_i v_i^T, w_i = g^(t1-1-i) (forward, decayed
-// to the segment's end) or g^(i-t0) (reverse, to its start).  Two stages of tiles; per chunk
-// the epilogue scales K into K~ and the control thread accumulates K~^T V in tensor memory.
+// to the segment's end) or g^(i-t0) (reverse, to its start).  Three stages of tiles (loads run
+// three chunks ahead); per chunk the epilogue scales K into K~ (in place, unless the keys are
+// also the values) and the control thread accumulates K~^T V in tensor memory.
 namespace las {
+constexpr int kStages = 3;
 template <bool KVS>
 struct Layout {
-    static constexpr uint32_t oK = 0;                                 // 2 stages
-    static constexpr uint32_t oV = KVS ? oK : oK + 2 * la::kTile;     // 2 stages
-    static constexpr uint32_t oKt = (KVS ? oK : oV) + 2 * la::kTile;  // 2 stages
-    static constexpr uint32_t oBar = oKt + 2 * la::kTile;
+    static constexpr uint32_t oK = 0;                                       // kStages stages
+    static constexpr uint32_t oV = KVS ? oK : oK + kStages * la::kTile;     // kStages stages
+    static constexpr uint32_t oKt = KVS ? oK + kStages * la::kTile : oK;    // KVS: its own stages
+    static constexpr uint32_t oBar = (KVS ? oKt : oV) + kStages * la::kTile;
     static constexpr uint32_t oMisc = oBar + 16 * 8;
     static constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
 };
-enum Bar { F0 = 0, F1, T0, T1, N0, N1, kBarCount };
+enum Bar { F0 = 0, T0 = F0 + kStages, N0 = T0 + kStages, kBarCount = N0 + kStages };
 }  // namespace las
 
 template <bool REV, bool KVS>
@@ -634,7 +636,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
     const float log2g = (float)a.pow * log2f(head_decay(a.gamma, bh, a.H));
 
     if (tid == 0) {
-        for (int b = 0; b < las::kBarCount; ++b) tc::mbar_init(&bars[b], (b == las::T0 || b == las::T1) ? 8 : 1);
+        for (int b = 0; b < las::kBarCount; ++b) tc::mbar_init(&bars[b], (b >= las::T0 && b < las::N0) ? 8 : 1);
         *abort = 0;
         tc::mbar_fence_init();
     }
@@ -649,7 +651,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
     if (warp == 0) {
         if (lane == 0 && nit > 0) {
             auto load = [&](int it) {
-                const int s = it & 1, c = chunk_of(it);
+                const int s = it % las::kStages, c = chunk_of(it);
                 uint64_t* bar = &bars[las::F0 + s];
                 tc::mbar_arrive_expect_tx(bar, (KVS ? 1 : 2) * la::kTile);
                 const uint32_t ok = Lay::oK + s * la::kTile, ov = Lay::oV + s * la::kTile;
@@ -662,11 +664,10 @@ __global__ void __launch_bounds__(la::kThreads, 1)
             };
             constexpr uint32_t I_MM = tc::idesc_bf16(128, 128, 1, 1);
             auto mdesc = [](uint32_t base, int ks) { return tc::smem_desc(base + 2048u * ks, la::kBlk, 1024); };
-            load(0);
-            if (nit > 1) load(1);
+            for (int it = 0; it < las::kStages && it < nit; ++it) load(it);
             for (int it = 0; it < nit; ++it) {
-                const int s = it & 1;
-                const uint32_t ph = (it >> 1) & 1;
+                const int s = it % las::kStages;
+                const uint32_t ph = (it / las::kStages) & 1;
                 tc::mbar_wait(&bars[las::T0 + s], ph, abort, status, 121);  // K~ of this chunk written
                 tc::fence_after_sync();
                 const uint32_t sKt = smem_u32(sm + Lay::oKt + s * la::kTile);
@@ -674,14 +675,14 @@ __global__ void __launch_bounds__(la::kThreads, 1)
                 for (int ks = 0; ks < 8; ++ks)
                     tc::mma_ss(tmem, mdesc(sKt, ks), mdesc(sV, ks), I_MM, (it > 0 || ks > 0) ? 1u : 0u);
                 tc::mma_commit(&bars[las::N0 + s]);
-                if (it + 2 < nit) {  // this stage's tiles are free once its product has run
+                if (it + las::kStages < nit) {  // this stage's tiles are free once its product has run
                     tc::mbar_wait(&bars[las::N0 + s], ph, abort, status, 122);
-                    load(it + 2);
+                    load(it + las::kStages);
                 }
             }
-            volatile int never = 0;
-            tc::mbar_wait(&bars[las::N0 + ((nit - 1) & 1)], ((nit - 1) >> 1) & 1, &never, nullptr, 0);
-            if (nit > 1) tc::mbar_wait(&bars[las::N0 + ((nit - 2) & 1)], ((nit - 2) >> 1) & 1, &never, nullptr, 0);
+            volatile int never = 0;  // the products not yet waited for (the last kStages chunks)
+            for (int it = nit - las::kStages < 0 ? 0 : nit - las::kStages; it < nit; ++it)
+                tc::mbar_wait(&bars[las::N0 + it % las::kStages], (it / las::kStages) & 1, &never, nullptr, 0);
         }
         __syncwarp();
     } else {
@@ -689,8 +690,8 @@ __global__ void __launch_bounds__(la::kThreads, 1)
         const int r = 32 * q4 + lane;
         const uint32_t lrow = tmem + ((uint32_t)(32 * q4) << 16);
         for (int it = 0; it < nit; ++it) {
-            const int s = it & 1;
-            const uint32_t ph = (it >> 1) & 1;
+            const int s = it % las::kStages;
+            const uint32_t ph = (it / las::kStages) & 1;
             const int c = chunk_of(it);
             const int Wc = min(kW, a.n - c * kW);
             tc::mbar_wait(&bars[las::F0 + s], ph, abort, status, 123);
@@ -709,7 +710,8 @@ __global__ void __launch_bounds__(la::kThreads, 1)
             if (lane == 0) tc::mbar_arrive(&bars[las::T0 + s]);
         }
         if (nit > 0 && HLA2_IN(bh < a.BH && seg < a.nseg, 803)) {
-            tc::mbar_wait(&bars[las::N0 + ((nit - 1) & 1)], ((nit - 1) >> 1) & 1, abort, status, 124);
+            tc::mbar_wait(&bars[las::N0 + (nit - 1) % las::kStages], ((nit - 1) / las::kStages) & 1, abort, status,
+                          124);
             tc::fence_after_sync();
             float* dst = a.summary + ((size_t)bh * a.nseg + seg) * la::kD * la::kD + (size_t)r * la::kD + 64 * h;
 #pragma unroll
@@ -766,7 +768,7 @@ __global__ void __launch_bounds__(la::kThreads, 1)
     const float log2g = log2f(head_decay(a.gamma, bh, a.H));
 
     if (tid == 0) {
-        for (int b = 0; b < las::kBarCount; ++b) tc::mbar_init(&bars[b], (b == las::T0 || b == las::T1) ? 8 : 1);
+        for (int b = 0; b < las::kBarCount; ++b) tc::mbar_init(&bars[b], (b >= las::T0 && b < las::N0) ? 8 : 1);
         *abort = 0;
         tc::mbar_fence_init();
     }
