@@ -746,6 +746,8 @@ __device__ __forceinline__ int segment_tokens(int s, int n, int W, int seg_chunk
 __global__ void __launch_bounds__(kThreads)
     reverse_scan_kernel(const float* __restrict__ src, float* __restrict__ dst, int BH, int H, int nseg,
                         size_t E, const float* gamma, int n, int W, int seg_chunks, int power) {
+    pdl_trigger();
+    pdl_wait();
     const size_t gid = (size_t)blockIdx.x * kThreads + threadIdx.x;
     if (gid >= (size_t)BH * E) return;
     const int bh = (int)(gid / E);
@@ -756,7 +758,20 @@ __global__ void __launch_bounds__(kThreads)
     if (!HLA2_IN(e < E && nseg >= 1, 702)) return;
     float acc = 0.f;
     d_[(size_t)(nseg - 1) * E] = 0.f;
-    for (int s = nseg - 1; s >= 1; --s) {
+    constexpr int U = 8;  // steps s .. s - U + 1: their loads issued before the first use
+    int s = nseg - 1;
+    for (; s - U + 1 >= 1; s -= U) {
+        float x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) x[u] = s_[(size_t)(s - u) * E];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float rho = pow_decay(log2g, (float)power * (float)segment_tokens(s - u, n, W, seg_chunks));
+            acc = rho * acc + x[u];
+            d_[(size_t)(s - u - 1) * E] = acc;
+        }
+    }
+    for (; s >= 1; --s) {
         const float rho = pow_decay(log2g, (float)power * (float)segment_tokens(s, n, W, seg_chunks));
         acc = rho * acc + s_[(size_t)s * E];
         d_[(size_t)(s - 1) * E] = acc;
@@ -846,8 +861,9 @@ int launch_reverse_scan(const float* src, float* dst, int BH, int H, int nseg, s
                         int n, int W, int seg_chunks, int power, cudaStream_t st) {
     const size_t total = (size_t)BH * E;
     if (total == 0 || nseg <= 0) return 0;
-    reverse_scan_kernel<<<(unsigned)((total + kThreads - 1) / kThreads), kThreads, 0, st>>>(
-        src, dst, BH, H, nseg, E, gamma, n, W, seg_chunks, power);
+    if (launch_pdl(reverse_scan_kernel, dim3((unsigned)((total + kThreads - 1) / kThreads)), dim3(kThreads), 0, st,
+                   src, dst, BH, H, nseg, E, gamma, n, W, seg_chunks, power) != cudaSuccess)
+        return -1;
     return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
