@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kThreads)
     const float rho = pow_decay(log2f(head_decay(gamma, bh, H)), (float)step_tokens * (float)J.power);
     const float* src = J.src + (size_t)bh * J.src_hs + e;
     float* dst = J.dst + (size_t)bh * J.dst_hs + e;
-    if (!HLA2_IN(e < E && (size_t)nsteps * E <= J.src_hs && (size_t)(J.store_all ? nsteps : 0) * E < J.dst_hs, 702))
+    if (!HLA2_IN(e < E && (size_t)nsteps * E <= J.src_hs && (size_t)(J.store_all ? nsteps : 0) * E < J.dst_hs, 703))
         return;
     float acc = dst[0];
     constexpr int U = 8;
