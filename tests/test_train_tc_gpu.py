@@ -125,7 +125,9 @@ def test_distinct_from_the_legacy_path(d):
     assert not all(torch.equal(a, b) for a, b in zip(tc, legacy))
 
 
-@pytest.mark.parametrize("B, H, n", [(1, 2, 1000), (2, 3, 129), (1, 1, 1), (1, 4, 3000)])
+# (2, 25, 2100): 3 segments of 6 chunks per head, the last chunk ragged, so that every
+# pipeline's stages are reused within a segment and carries cross the segments
+@pytest.mark.parametrize("B, H, n", [(1, 2, 1000), (2, 3, 129), (1, 1, 1), (1, 4, 3000), (2, 25, 2100)])
 @pytest.mark.parametrize("gamma", [None, (0.9, 0.999)])
 def test_forward_matches_oracle(B, H, n, gamma):
     """The plain forward (no state in or out) runs the same first-order passes."""
@@ -156,7 +158,8 @@ def test_forward_distinct_from_the_legacy_path():
     assert not torch.equal(tc, legacy)
 
 
-@pytest.mark.parametrize("B, H, n", [(1, 2, 1000), (2, 3, 129), (1, 1, 1), (1, 4, 3000), (2, 64, 700)])
+@pytest.mark.parametrize("B, H, n", [(1, 2, 1000), (2, 3, 129), (1, 1, 1), (1, 4, 3000), (2, 64, 700),
+                                     (2, 25, 2100)])
 @pytest.mark.parametrize("gamma", [None, (0.9, 0.999)])
 def test_forward_final_state_matches_oracle(B, H, n, gamma):
     """The d = 128 forward with the state after the last token, on the first-order scans: the
