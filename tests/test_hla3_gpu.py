@@ -44,6 +44,14 @@ def test_bf16(chunk, n):
     assert rel_err(np64(run(x, chunk=chunk)), ref) <= 2e-2
 
 
+def test_bf16_segments_of_several_chunks():
+    """24 heads of 2048 tokens: the first-order pass runs 6 segments of 3 chunks per head, so
+    its summary and output pipelines reuse their stages within a segment."""
+    x = inputs.make_custom(1, 24, 2048, 64, 64, torch.bfloat16, seed=85)
+    ref = O3.serial_forward(np64(x["q"]), np64(x["k"]), np64(x["v"]))
+    assert rel_err(np64(run(x, chunk=128)), ref) <= 2e-2
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_normalized(dtype):
     x = inputs.make_custom(2, 2, 260, 32, 32, dtype, seed=82, qk="softplus", v_scale="unit")
