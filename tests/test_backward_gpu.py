@@ -104,6 +104,21 @@ def test_fp32_lengths_and_segments(n):
         assert rel_err(np64(gg.cpu()), rr) <= 1e-4, (name, n)
 
 
+def test_fp32_segments_of_several_chunks():
+    """152 heads of 1024 tokens at width 32: the float32 forward and reverse passes run 4
+    segments of 8 chunks per head, so the states move from chunk to chunk within a segment."""
+    x = inputs.make_custom(8, 19, 1024, 64, 64, torch.float32, seed=13, gamma=(0.9, 0.999), with_dout=True)
+    nseg, seg_chunks, _ = hla.forward_plan(8, 19, 1024, 64, 64, 32, dtype=torch.float32)
+    assert seg_chunks >= 4 and nseg >= 2
+    g = x["gamma"].cuda()
+    o = hla.forward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), gamma=g, chunk=32)
+    ref_o = cref.forward(np32(x["q"]), np32(x["k"]), np32(x["v"]), x["gamma"].double().numpy())
+    assert rel_err(np64(o.cpu()), ref_o) <= 1e-4
+    got = run(x, 32)
+    for name, gg, rr in zip(("dq", "dk", "dv"), got, oracle(x)):
+        assert rel_err(np64(gg.cpu()), rr) <= 1e-4, name
+
+
 def test_fp32_no_decay_and_host_tensors():
     x = inputs.make_custom(2, 1, 300, 16, 32, torch.float32, seed=12, gamma=None, with_dout=True)
     got = hla.backward(x["q"], x["k"], x["v"], x["dout"], chunk=16)  # CPU tensors in and out
