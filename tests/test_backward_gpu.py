@@ -219,6 +219,20 @@ def test_normalized_gradients_short_memory(d):
         assert rel_err(np64(gg.cpu()), rr) <= 2e-2, (name, kk)
 
 
+def test_normalized_workload_gradients():
+    """The normalised workload itself (B=2 H=8 n=2048 d=dv=64 bf16, chunk 64): the float32 passes
+    run 16 segments of 4 chunks per head."""
+    import dataclasses
+
+    w = dataclasses.replace(inputs.WORKLOADS["normed"], with_dout=True)
+    x = inputs.make(w, seed=w.seed)
+    got = hla.backward(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), x["dout"].cuda(), gamma=x["gamma"].cuda(),
+                       chunk=w.chunk, normalize=True, eps=w.eps)
+    ref, kappa = _normalized_reference(x, w.eps)
+    for name, gg, rr, kk in zip(("dq", "dk", "dv"), got, ref, kappa):
+        assert rel_err(np64(gg.cpu()), rr) <= 2e-2, (name, kk)
+
+
 def test_normalized_gradients_bf16_unequal_dims():
     """The normalised backward composes float32 passes, so bf16 d != dv works too."""
     x = inputs.make_custom(1, 2, 260, 64, 32, torch.bfloat16, seed=77, qk="softplus", v_scale="unit",
