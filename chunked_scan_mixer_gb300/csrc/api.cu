@@ -1059,22 +1059,14 @@ size_t fo_forward_ws(int B, int H, int n, int d, int dv, int chunk, int dtype, i
     return want_final ? L.final_total : L.fwd_total;
 }
 
-// The state after the last token from the first-order scans: the (q, v) summaries, the m and y
-// moments (y from the stored full p), the carries of C, m, y into the last segment, and the
-// last segment's combine with G = S C - Z and h = S m - y.
-int fo_final_state(const void* q, const void* v, const Plan& p, const float* gamma, char* ws, const FoLayout& L,
-                   float* final_state, cudaStream_t st, bool sums_done = false) {
+// The state after the last token from the first-order scans, once the forward part has formed
+// the (q, v) summaries and the m and y moments (y from the stored full p): the carries of C, m, y
+// into the last segment, and the last segment's combine with G = S C - Z and h = S m - y.
+int fo_final_state(const Plan& p, const float* gamma, char* ws, const FoLayout& L, float* final_state,
+                   cudaStream_t st) {
     auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
     const size_t E = (size_t)p.d * p.d;
     const int seg_tokens = p.seg_chunks * p.W;
-    if (!sums_done) {  // (q, v) summaries and the q, p moments (else formed by the forward part)
-        FoArgs a = fo_args(p, gamma, ws);
-        a.pow = 1;
-        a.summary = f(L.CB);
-        if (fo_summary(a, p.d, q, v, false, st)) return cuda_fail("query-value summaries");
-        if (launch_fo_moments(q, ws + L.P, f(L.mB), f(L.yB), p.BH, p.H, p.n, p.d, p.nseg, seg_tokens, gamma, st))
-            return cuda_fail("segment moments");
-    }
     // (one segment: the final-state kernel reads no carries)
     if (p.nseg > 1 && cudaMemsetAsync(ws + L.Cl, 0, L.carries_bytes, st) != cudaSuccess) return cuda_fail("carry reset");
     if (p.nseg > 1) {  // C, m and y carried into the last segment, in one launch
@@ -1126,12 +1118,12 @@ int fo_forward_call(const void* q, const void* k, const void* v, void* out, int 
     };
     cudaGetLastError();
     mark(0);
-    const bool fused = want_final && p.d == 128;  // the final state's summaries in the forward part's pass
-    int rc = fo_forward_part(q, k, v, p, gamma, ws, L, st, fused);
+    // (d = 128 only: the final state's summaries come from the forward part's (p, v) pass)
+    int rc = fo_forward_part(q, k, v, p, gamma, ws, L, st, want_final);
     mark(3);
     if (rc == HLA2_OK) rc = fo_output_pass(q, v, out, p, gamma, ws, L, st);
     mark(4);
-    if (rc == HLA2_OK && want_final) rc = fo_final_state(q, v, p, gamma, ws, L, opts->final_state, st, fused);
+    if (rc == HLA2_OK && want_final) rc = fo_final_state(p, gamma, ws, L, opts->final_state, st);
     mark(5);
     return rc == HLA2_OK ? succeed() : rc;
 }

@@ -305,11 +305,10 @@ int launch_fo_tc_summary_final(const FoArgs& a, const void* q, const void* p, co
 // add != NULL adds that partial.
 int launch_fo_tc_out(const FoArgs& a, const void* x, const void* k, const void* v, bool r2, int next_sum,
                      const void* xv, const void* add, void* out, bool reverse, cudaStream_t st);
-// Final state of the first-order-scan forward (d = dv = 64 or 128).  Per segment s of head bh:
-//   mB[bh][s] = sum_t g^(L-1-t) q_t,  yB[bh][s] = sum_t g^(2(L-1-t)) p_t  (p the full p),
-// t the token's place in the segment of L tokens (seg_tokens, the last one shorter).
-int launch_fo_moments(const void* q, const void* p, float* mB, float* yB, int BH, int H, int n, int d, int nseg,
-                      int seg_tokens, const float* gamma, cudaStream_t st);
+// Final state of the first-order-scan forward (d = dv = 128).  Per segment s of head bh the
+// moments mB[bh][s] = sum_t g^(L-1-t) q_t and yB[bh][s] = sum_t g^(2(L-1-t)) p_t (p the full p,
+// t the token's place in the segment of L tokens) come from the summary pass
+// (launch_fo_tc_summary_final).
 struct FoFinal {
     const float *SB, *Sin, *ZB, *Zin, *CB;  // [BH][nseg][d][d]: summaries and carries (S, Z); C summaries
     const float *Cl, *ml, *yl;              // [BH][d][d], [BH][d]: carries of C, m, y into the last segment

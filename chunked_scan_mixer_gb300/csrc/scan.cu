@@ -417,66 +417,6 @@ __global__ void __launch_bounds__(kThreads) final_combine64_kernel(const ChunkAr
     }
 }
 
-// Segment moments of the first-order-scan forward: one CTA per (segment, head, 32 features);
-// thread (row, j) sums features 32 z + 8j .. +7 over tokens row, row + 64, ... of the segment,
-// then the 64 row partials are added in a fixed order.
-template <int D>
-__global__ void __launch_bounds__(kThreads) fo_moments_kernel(const bf16* __restrict__ q, const bf16* __restrict__ p,
-                                                              float* mB, float* yB, int H, int n, int nseg,
-                                                              int seg_tokens, const float* gamma) {
-    constexpr int HALF = 32, ROWS = kThreads / 4;
-    __shared__ float red_m[ROWS][HALF + 1], red_y[ROWS][HALF + 1];
-    pdl_trigger();
-    pdl_wait();
-    // the column quarters of a segment run next to each other, so that they read whole rows
-    const int z = blockIdx.x % (D / HALF), s = blockIdx.x / (D / HALF), bh = blockIdx.y, tid = threadIdx.x;
-    const int row = tid / 4, j = tid % 4;
-    const int t0 = s * seg_tokens, t1 = min(t0 + seg_tokens, n);
-    const float log2g = log2f(head_decay(gamma, bh, H));
-    const int f0 = HALF * z + 8 * j;
-    const bf16* qh = q + (size_t)bh * n * D + f0;
-    const bf16* ph = p + (size_t)bh * n * D + f0;
-    float am[8], ay[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) am[u] = ay[u] = 0.f;
-    constexpr int U = 4;  // rows of a thread whose loads are issued together
-    for (int tb = t0 + row; tb < t1; tb += U * ROWS) {
-        uint4 qv[U], pv[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int t = tb + u * ROWS;
-            qv[u] = t < t1 ? *reinterpret_cast<const uint4*>(qh + (size_t)t * D) : make_uint4(0, 0, 0, 0);
-            pv[u] = t < t1 ? *reinterpret_cast<const uint4*>(ph + (size_t)t * D) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int t = tb + u * ROWS;
-            const float w = t < t1 ? pow_decay(log2g, (float)(t1 - 1 - t)) : 0.f, w2 = w * w;
-            const uint32_t qw[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w}, pw[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                am[2 * e] += w * __uint_as_float(qw[e] << 16);
-                am[2 * e + 1] += w * __uint_as_float(qw[e] & 0xFFFF0000u);
-                ay[2 * e] += w2 * __uint_as_float(pw[e] << 16);
-                ay[2 * e + 1] += w2 * __uint_as_float(pw[e] & 0xFFFF0000u);
-            }
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        red_m[row][8 * j + u] = am[u];
-        red_y[row][8 * j + u] = ay[u];
-    }
-    __syncthreads();
-    if (tid < 2 * HALF) {
-        const int f = tid % HALF;
-        float (*red)[HALF + 1] = tid < HALF ? red_m : red_y;
-        float acc = 0.f;
-        for (int r = 0; r < ROWS; ++r) acc += red[r][f];
-        (tid < HALF ? mB : yB)[((size_t)bh * nseg + s) * D + HALF * z + f] = acc;
-    }
-}
-
 // Final state of the first-order-scan forward: CTA (rb, bh) forms rows 32 rb .. 32 rb + 31 of
 // every part.  The combined C (all D rows) and the CTA's rows of S sit in shared memory; the
 // rows of G = S C come from the register-tiled products of simt_tile.cuh.  Loads are float4 and
@@ -682,19 +622,6 @@ int launch_seg_moments64(const ChunkArgs& a, cudaStream_t st) {
     if (a.nsum <= 0 || a.BH <= 0) return 0;  // the summaries kept: every segment but the last, or all
     if (launch_pdl(seg_moments64_kernel, dim3(a.nsum, a.BH, 2), dim3(kThreads), 0, st, a) != cudaSuccess) return -1;
     return finish_launch();
-}
-
-int launch_fo_moments(const void* q, const void* p, float* mB, float* yB, int BH, int H, int n, int d, int nseg,
-                      int seg_tokens, const float* gamma, cudaStream_t st) {
-    if (nseg <= 0 || BH <= 0) return 0;
-    const dim3 grid(nseg * (d / 32), BH);
-    const bf16 *qq = static_cast<const bf16*>(q), *pp = static_cast<const bf16*>(p);
-    cudaError_t e = d == 64 ? launch_pdl(fo_moments_kernel<64>, grid, dim3(kThreads), 0, st, qq, pp, mB, yB, H, n, nseg,
-                                         seg_tokens, gamma)
-                  : d == 128 ? launch_pdl(fo_moments_kernel<128>, grid, dim3(kThreads), 0, st, qq, pp, mB, yB, H, n,
-                                          nseg, seg_tokens, gamma)
-                             : cudaErrorInvalidValue;
-    return e == cudaSuccess ? finish_launch() : -1;
 }
 
 int launch_fo_final_state(const FoFinal& f, float* final_state, cudaStream_t st) {
