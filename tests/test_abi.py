@@ -110,6 +110,49 @@ def test_decode_rejects_bad_arguments(L):
     assert rc == 0
 
 
+def _bwd(L, **kw):
+    # distinct (never dereferenced) addresses, 16-byte aligned
+    names = ("q", "k", "v", "dout", "dq", "dk", "dv_out")
+    args = {nm: ctypes.c_void_p(0x10000 * (i + 1)) for i, nm in enumerate(names)}
+    args.update(B=1, H=2, n=16, d=16, dv=16, normalize=0, chunk=16, opts=Opts(1, 1e-6, None, 0, None, None))
+    args.update(kw)
+    o = args["opts"]
+    rc = L.hla2_backward(*(args[nm] for nm in names), args["B"], args["H"], args["n"], args["d"], args["dv"],
+                         None, args["normalize"], args["chunk"], None, None if o is None else ctypes.byref(o))
+    return rc, L.hla2_last_error().decode()
+
+
+def test_backward_empty_is_ok(L):
+    """No heads or no tokens: nothing to compute, and the tensors may be NULL; the workspace
+    query answers 0."""
+    nulls = dict(q=None, k=None, v=None, dout=None, dq=None, dk=None, dv_out=None)
+    for kw in (dict(B=0), dict(H=0), dict(n=0), dict(n=0, normalize=1)):
+        rc, msg = _bwd(L, **kw, **nulls)
+        assert rc == 0, (kw, msg)
+    for normalize in (0, 1):
+        assert L.hla2_backward_workspace_bytes(1, 2, 0, 64, 64, 64, 1, normalize) == 0
+        assert L.hla2_backward_workspace_bytes(0, 2, 100, 64, 64, 64, 1, normalize) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(opts=None),
+    dict(d=48),
+    dict(chunk=24),
+    dict(n=-1),
+    dict(normalize=2),
+    dict(dq=None),
+    dict(dv_out=None),
+    dict(dk=ctypes.c_void_p(0x10008)),                               # not 16-byte aligned
+    dict(opts=Opts(1, 1e-6, None, 0, ctypes.c_void_p(16), None)),    # init_state
+    dict(opts=Opts(1, 1e-6, None, 0, None, ctypes.c_void_p(16))),    # final_state
+    dict(normalize=1, opts=Opts(1, float("nan"), None, 0, None, None)),
+])
+def test_backward_rejects_bad_arguments(L, kw):
+    rc, msg = _bwd(L, **kw)
+    assert rc == -1, msg
+    assert msg
+
+
 def test_normalized_backward_checks_before_launching(L):
     """The ratio-normalised backward is argument-checked on the host: it needs its larger
     workspace, finite eps, and cannot reuse saved (unnormalised) forward states."""
