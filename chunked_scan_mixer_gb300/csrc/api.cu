@@ -1789,10 +1789,11 @@ static AhlaBwdPlan ahla_bwd_plan(int B, int H, int n, int d, int chunk, const De
 //   dk = RLA_g(u, dO, q) + RLA_g(v, du, q),  dq = LA_g(dO, u, k) + LA_g(du, v, k),
 // whose carries are four summaries (some read transposed): KV = sum k v^T (F1, forward),
 // UK = sum u k^T (over the u pass's own output), QD = sum q dO^T (B1, reverse) and DQ =
-// sum du q^T (over the du pass's own output).
+// sum du q^T (over the du pass's own output).  dk and dq each take one pass over their two
+// query / key pairs, which share the values.
 struct AhlaFoLayout {
     size_t KVB, KVin, UKB, UKin, QDB, QDend, DQB, DQend;  // byte offsets, fp32 [BH][nseg][d][d]
-    size_t U, DU, DKA, DQA;                               // byte offsets, bf16 [BH][n][d]
+    size_t U, DU;                                         // byte offsets, bf16 [BH][n][d]
     size_t total;
 };
 
@@ -1807,7 +1808,7 @@ AhlaFoLayout ahla_fo_layout(const Plan& p) {
         *x = o;
         o = up(o + sum);
     }
-    size_t* toks[] = {&L.U, &L.DU, &L.DKA, &L.DQA};
+    size_t* toks[] = {&L.U, &L.DU};
     for (size_t* x : toks) {
         *x = o;
         o = up(o + tok);
@@ -1867,17 +1868,15 @@ int ahla_fo_backward(const void* q, const void* k, const void* v, const void* do
     // B4: dk = RLA(u, dO, q) [carry sum dO q^T] + RLA(v, du, q) [carry sum du q^T]
     a.carry = f(L.QDend);
     a.carry_mode = 1;
-    if (fo_out(a, p.d, U, dout, q, false, 0, nullptr, nullptr, ws + L.DKA, true, st)) return cuda_fail("AHLA dk pass");
-    a.carry = f(L.DQend);
-    a.carry_mode = 0;
-    if (fo_out(a, p.d, v, DU, q, false, 0, nullptr, ws + L.DKA, dk, true, st)) return cuda_fail("AHLA dk pass");
+    a.carry2 = f(L.DQend);
+    a.carry_mode2 = 0;
+    if (launch_fo64_tc_out2(a, U, dout, v, DU, q, dk, true, st)) return cuda_fail("AHLA dk pass");
     // B5: dq = LA(dO, u, k) [carry sum u k^T] + LA(du, v, k) [carry sum v k^T]
     a.carry = f(L.UKin);
     a.carry_mode = 0;
-    if (fo_out(a, p.d, dout, U, k, false, 0, nullptr, nullptr, ws + L.DQA, false, st)) return cuda_fail("AHLA dq pass");
-    a.carry = f(L.KVin);
-    a.carry_mode = 1;
-    if (fo_out(a, p.d, DU, v, k, false, 0, nullptr, ws + L.DQA, dq, false, st)) return cuda_fail("AHLA dq pass");
+    a.carry2 = f(L.KVin);
+    a.carry_mode2 = 1;
+    if (launch_fo64_tc_out2(a, dout, U, DU, v, k, dq, false, st)) return cuda_fail("AHLA dq pass");
     return HLA2_OK;
 }
 

@@ -13,7 +13,10 @@
 //   EPI-S  Sig <- g^Wc Sig + dSig (fp32, 16 a thread), bf16 Sig0 for the next chunk
 //   EPI-Y  Y (+ a partial read from global) -> bf16 tile -> one TMA tile store
 // Optional parts as in fo_tc.cu: the swapped second pair (R2), the next summary over the
-// output (NSUM; the values are the value tile or an extra tile), a partial output (ADD).  The
+// output (NSUM; the values are the value tile or an extra tile), a partial output (ADD).  Here
+// also a second query / key pair with the same values (ST): out = (R)LA(X, K, V) + (R)LA(X2, K2, V)
+// is one scan of the stacked pairs, G = X K^T + X2 K2^T, Y = [G~ | fX | fX2] [V ; Sig0 ; Sig0_2],
+// dSig = [K~^T ; K2~^T] V (the two 64 x 64 states as the row halves of one M = 128 product).  The
 // carry is read as stored, transposed or symmetrised.  The queries, keys and values (and the
 // extra and partial tiles) have two slots each: chunk j's loads go into slot j % 2 as soon as
 // chunk j - 2 has released it.  Without the second pair the G / Y tensor-memory region is
@@ -39,7 +42,9 @@ constexpr uint32_t kSig = 64 * 128;    // the [64][64] bf16 state (8 KB)
 constexpr uint32_t kTmemCols = 512;
 
 // TWOA: the scaled keys K~ and the bf16 state Sig0 have two slots as well (by chunk parity).
-template <bool R2, bool KVS, bool XVS, bool ADD, bool TWOA = false>
+// ST: the second pair's queries and keys (two slots each), its scaled keys beside K~ (the A
+// operand of the M = 128 state product), and the [128][64] stacked bf16 state.
+template <bool R2, bool KVS, bool XVS, bool ADD, bool TWOA = false, bool ST = false>
 struct OutLayout {
     static constexpr uint32_t oX = 0;                                   // 2 slots
     static constexpr uint32_t oK = oX + 2 * kTile;                      // 2 slots
@@ -47,12 +52,14 @@ struct OutLayout {
     static constexpr uint32_t oE0 = (KVS ? oK : oV) + 2 * kTile;
     static constexpr uint32_t oXV = XVS ? oE0 : oV;                     // 2 slots
     static constexpr uint32_t oAD = XVS ? oXV + 2 * kTile : oE0;        // 2 slots
-    static constexpr uint32_t oKt = ADD ? oAD + 2 * kTile : oAD;        // K~ (TWOA: 2 slots; V~ next for R2)
+    static constexpr uint32_t oX2 = ADD ? oAD + 2 * kTile : oAD;        // ST: 2 slots
+    static constexpr uint32_t oK2 = oX2 + 2 * kTile;                    // ST: 2 slots
+    static constexpr uint32_t oKt = ST ? oK2 + 2 * kTile : oX2;         // K~ (TWOA: 2 slots; V~ / K2~ next)
     static constexpr uint32_t oKt2 = oKt + kTile;
-    static constexpr uint32_t oST = R2 ? oKt2 + kTile : oKt + (TWOA ? 2 : 1) * kTile;  // output tile
+    static constexpr uint32_t oST = (R2 || ST) ? oKt2 + kTile : oKt + (TWOA ? 2 : 1) * kTile;  // output tile
     static constexpr bool kTwoST = TWOA && !ADD;                        // (2 slots where they fit)
     static constexpr uint32_t oS0 = oST + (kTwoST ? 2 : 1) * kTile;     // bf16 Sig0 (TWOA: 2 slots)
-    static constexpr uint32_t oGP = oS0 + (TWOA ? 2 : 1) * kSig;        // g^0 .. g^(2W)
+    static constexpr uint32_t oGP = oS0 + ((TWOA || ST) ? 2 : 1) * kSig;  // g^0 .. g^(2W)
     static constexpr uint32_t oBar = oGP + 1088;
     static constexpr uint32_t oMisc = oBar + 24 * 8;
     static constexpr uint32_t kSmemBytes = oMisc + 16 + 1024;
@@ -61,6 +68,8 @@ struct OutLayout {
     __host__ __device__ static constexpr uint32_t val(int j) { return KVS ? key(j) : oV + (uint32_t)(j & 1) * kTile; }
     __host__ __device__ static constexpr uint32_t xv(int j) { return XVS ? oXV + (uint32_t)(j & 1) * kTile : val(j); }
     __host__ __device__ static constexpr uint32_t ad(int j) { return oAD + (uint32_t)(j & 1) * kTile; }
+    __host__ __device__ static constexpr uint32_t x2(int j) { return oX2 + (uint32_t)(j & 1) * kTile; }
+    __host__ __device__ static constexpr uint32_t k2(int j) { return oK2 + (uint32_t)(j & 1) * kTile; }
     __host__ __device__ static constexpr uint32_t kt(int j) { return oKt + (TWOA ? (uint32_t)(j & 1) * kTile : 0u); }
     __host__ __device__ static constexpr uint32_t s0(int j) { return oS0 + (TWOA ? (uint32_t)(j & 1) * kSig : 0u); }
     __host__ __device__ static constexpr uint32_t st(int j) { return oST + (kTwoST ? (uint32_t)(j & 1) * kTile : 0u); }
@@ -70,16 +79,18 @@ struct OutLayout {
 // [128,192) or [192,256) (with a next summary: Y [128,192), the summary [192,256)); A operands
 // of chunk j in [256,352) or [352,448) (G~ 64 | fX 32); dSig [448,512).  Swapped pair: G1
 // [0,128), G2 [128,256); after EPI-1 Y [0,64) and dSig [128,192); A operands [256,416)
-// (G~1 | G~2 | fX).
-template <bool R2, bool NSUM>
+// (G~1 | G~2 | fX).  Stacked pairs (ST, one operand slot): G and then Y of chunk j in [0,128)
+// or [384,512) by chunk parity; dSig [128,192) over all 128 lanes (the two states); A operands
+// [256,384) (G~ | fX | fX2).
+template <bool R2, bool NSUM, bool ST = false>
 struct Cols {
     static constexpr bool kTwoG = !R2;
-    static constexpr bool kTwoA = !R2;
+    static constexpr bool kTwoA = !R2 && !ST;
     static constexpr bool kTwoY = kTwoA && !NSUM;
-    static constexpr uint32_t TS = R2 ? 128 : 448;
+    static constexpr uint32_t TS = (R2 || ST) ? 128 : 448;
     static constexpr uint32_t TN = 192;
-    __device__ static constexpr uint32_t TG(int j) { return 0u; }
-    __device__ static constexpr uint32_t TY(int j) { return kTwoA ? 128u + (kTwoY ? 64u * (uint32_t)(j & 1) : 0u) : 0u; }
+    __device__ static constexpr uint32_t TG(int j) { return kTwoG && !kTwoA && (j & 1) ? 384u : 0u; }
+    __device__ static constexpr uint32_t TY(int j) { return kTwoA ? 128u + (kTwoY ? 64u * (uint32_t)(j & 1) : 0u) : TG(j); }
     __device__ static constexpr uint32_t TA(int j) { return kTwoA && (j & 1) ? 352u : 256u; }
     __device__ static constexpr uint32_t TX(int j) { return TA(j) + (R2 ? 128u : 64u); }
 };
@@ -89,18 +100,20 @@ struct Cols {
 enum Bar { FX0 = 0, FX1, FK0, FK1, FV0, FV1, BG, BGT, BSU, BS, BYT, BN, BSF, BSF1, BYT1, BGT1, BSU1, kBarCount };
 
 struct Maps {
-    CUtensorMap x, k, v, xv, ad, out;
+    CUtensorMap x, k, v, xv, ad, out, x2, k2;
 };
 
 }  // namespace f64
 
 // ----------------------------------------------------------------------------------------
-template <bool REV, bool NSUM, bool R2, bool KVS, bool XVS, bool ADD>
+template <bool REV, bool NSUM, bool R2, bool KVS, bool XVS, bool ADD, bool ST = false>
 __global__ void __launch_bounds__(f64::kThreadsOut, 1)
     fo64_out_tc_kernel(const __grid_constant__ f64::Maps maps, const FoArgs a) {
-    using C = f64::Cols<R2, NSUM>;
+    using C = f64::Cols<R2, NSUM, ST>;
     constexpr bool kTwoG = C::kTwoG, kTwoA = C::kTwoA;
-    using Lay = f64::OutLayout<R2, KVS, XVS, ADD, kTwoA>;
+    using Lay = f64::OutLayout<R2, KVS, XVS, ADD, kTwoA, ST>;
+    static_assert(!ST || (!NSUM && !R2 && !KVS && !XVS && !ADD), "stacked pairs: plain values, one output");
+    static_assert(Lay::kSmemBytes <= 232448, "shared memory of one CTA");
     constexpr int kW = f64::kW, kD = f64::kD;
     pdl_trigger();
     extern __shared__ unsigned char smem_raw[];
@@ -132,30 +145,36 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
     pdl_wait();
 
     // epilogue thread: TMEM lane / token row r, column half h: tile columns 32h .. 32h+31
-    // (chunks 4h .. 4h+3); state row sr = r % 64, columns sc .. sc+15
+    // (chunks 4h .. 4h+3); state row sr = r % 64, columns sc .. sc+15 (ST: stacked state row r,
+    // columns 32h .. 32h+31)
     const int q4 = warp & 3, h = (warp - 1) >> 2;
     const int r = 32 * q4 + lane;
-    const int sr = r & 63, sc = 32 * h + 16 * (r >> 6);
-    float sig[16];
+    const int sr = ST ? r : r & 63, sc = ST ? 32 * h : 32 * h + 16 * (r >> 6);
+    constexpr int kSigN = ST ? 32 : 16;
+    float sig[kSigN];
     auto publish_sig = [&](int jn) {  // Sig0 of chunk jn
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int j = 0; j < kSigN / 8; ++j)
             *reinterpret_cast<uint4*>(sm + Lay::s0(jn) + tc::sw128_chunk(sr, sc / 8 + j)) = la_pack8(&sig[8 * j]);
     };
 
     if (warp == 0) {
         tc::tmem_alloc(tmem_holder, f64::kTmemCols);
     } else if (warp <= 8) {
-        if (a.carry && HLA2_IN(bh < a.BH && seg < a.nseg, 851)) {
-            const float* src = a.carry + ((size_t)bh * a.nseg + seg) * kD * kD;
+        // (ST: rows 0..63 of the stacked state carry the first pair, rows 64..127 the second)
+        const bool second = ST && r >= 64;
+        const float* carry = second ? a.carry2 : a.carry;
+        const int mode = second ? a.carry_mode2 : a.carry_mode, cr = sr & 63;
+        if (carry && HLA2_IN(bh < a.BH && seg < a.nseg, 851)) {
+            const float* src = carry + ((size_t)bh * a.nseg + seg) * kD * kD;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float x = src[(size_t)sr * kD + sc + j], xt = src[(size_t)(sc + j) * kD + sr];
-                sig[j] = a.carry_mode == 0 ? x : (a.carry_mode == 1 ? xt : x + xt);
+            for (int j = 0; j < kSigN; ++j) {
+                const float x = src[(size_t)cr * kD + sc + j], xt = src[(size_t)(sc + j) * kD + cr];
+                sig[j] = mode == 0 ? x : (mode == 1 ? xt : x + xt);
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) sig[j] = 0.f;
+            for (int j = 0; j < kSigN; ++j) sig[j] = 0.f;
         }
         publish_sig(0);
         tc::fence_proxy_async();
@@ -184,13 +203,16 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
             auto load1 = [&](uint32_t slot, const CUtensorMap* m, int c, uint64_t* bar) {
                 tc::tma_load_3d(sm + slot, m, 0, c * kW, bh, bar);
             };
+            // (ST: the second pair's tile comes with each, on the same barrier)
             auto load_x = [&](int j) {
-                tc::mbar_arrive_expect_tx(fx(j), f64::kTile);
+                tc::mbar_arrive_expect_tx(fx(j), (ST ? 2 : 1) * f64::kTile);
                 load1(Lay::x(j), &maps.x, chunk_of(j), fx(j));
+                if (ST) load1(Lay::x2(j), &maps.x2, chunk_of(j), fx(j));
             };
             auto load_k = [&](int j) {
-                tc::mbar_arrive_expect_tx(fk(j), f64::kTile);
+                tc::mbar_arrive_expect_tx(fk(j), (ST ? 2 : 1) * f64::kTile);
                 load1(Lay::key(j), &maps.k, chunk_of(j), fk(j));
+                if (ST) load1(Lay::k2(j), &maps.k2, chunk_of(j), fk(j));
             };
             auto load_v = [&](int j) {
                 if (kVTiles == 0) return;
@@ -219,6 +241,11 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
                     const uint32_t sV = smem_u32(sm + Lay::val(j));
                     for (int ks = 0; ks < 4; ++ks)
                         tc::mma_ss(tmem + C::TG(j) + 128, kdesc(sX, ks), kdesc(sV, ks), I_G, ks > 0);
+                }
+                if (ST) {  // G += X2 K2^T
+                    const uint32_t sX2 = smem_u32(sm + Lay::x2(j)), sK2 = smem_u32(sm + Lay::k2(j));
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_ss(tmem + C::TG(j), kdesc(sX2, ks), kdesc(sK2, ks), I_G, 1);
                 }
                 tc::mma_commit(&bars[f64::BG]);
             };
@@ -368,16 +395,19 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
                 tc::fence_after_sync();
                 const uint32_t sK = smem_u32(sm + Lay::key(j)), sV = smem_u32(sm + Lay::val(j));
                 const uint32_t sKt = smem_u32(sm + Lay::kt(j)), sS0 = smem_u32(sm + Lay::s0(j));
-                // MMA-Y: Y = [G~ | (G~2) | fX] [V ; (K) ; Sig0]
+                // MMA-Y: Y = [G~ | (G~2) | fX (| fX2)] [V ; (K) ; Sig0 (; Sig0_2)]
                 for (int ks = 0; ks < 8; ++ks)
                     tc::mma_ts(tmem + C::TY(j), tmem + C::TA(j) + 8 * ks, mdesc(sV, ks), I_Y, ks > 0);
                 if (R2)
                     for (int ks = 0; ks < 8; ++ks)
                         tc::mma_ts(tmem + C::TY(j), tmem + C::TA(j) + 64 + 8 * ks, mdesc(sK, ks), I_Y, 1);
-                for (int ks = 0; ks < 4; ++ks)
+                for (int ks = 0; ks < (ST ? 8 : 4); ++ks)
                     tc::mma_ts(tmem + C::TY(j), tmem + C::TX(j) + 8 * ks, mdesc(sS0, ks), I_Y, 1);
-                // MMA-S: dSig = [K~^T ; K~^T] V (R2: + [V~^T ; V~^T] K)
-                for (int ks = 0; ks < 8; ++ks) tc::mma_ss(tmem + C::TS, mdesc(sKt, ks), mdesc(sV, ks), I_S, ks > 0);
+                // MMA-S: dSig = [K~^T ; K~^T] V (R2: + [V~^T ; V~^T] K; ST: [K~^T ; K2~^T] V, the
+                // second row half read one tile on)
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_ss(tmem + C::TS, ST ? tc::smem_desc(sKt + 2048u * ks, f64::kTile, 1024) : mdesc(sKt, ks),
+                               mdesc(sV, ks), I_S, ks > 0);
                 if (R2)
                     for (int ks = 0; ks < 8; ++ks) tc::mma_ss(tmem + C::TS, mdesc(sKt2, ks), mdesc(sK, ks), I_S, 1);
                 tc::mma_commit(&bars[f64::BSU]);
@@ -453,24 +483,27 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
                     tc::tmem_st16(lrow + C::TA(j) + 64 * gi + cb / 2, pk);
                 }
             }
-            {  // fX: this thread's 32 features of row r -> 16 packed columns
+            // fX: this thread's 32 features of row r -> 16 packed columns (ST: fX2 32 columns on)
+#pragma unroll
+            for (int xi = 0; xi < (ST ? 2 : 1); ++xi) {
+                const unsigned char* sXi = xi == 0 ? sX : sm + Lay::x2(j);
                 const float f = live ? (REV ? gp[Wc - r] : gp[r + 1]) : 0.f;
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const uint4 x = la_scale_chunk(*reinterpret_cast<const uint4*>(sX + tc::sw128_chunk(r, 4 * h + i)), f);
+                    const uint4 x = la_scale_chunk(*reinterpret_cast<const uint4*>(sXi + tc::sw128_chunk(r, 4 * h + i)), f);
                     pk[4 * i] = x.x, pk[4 * i + 1] = x.y, pk[4 * i + 2] = x.z, pk[4 * i + 3] = x.w;
                 }
-                tc::tmem_st16(lrow + C::TX(j) + 16 * h, pk);
+                tc::tmem_st16(lrow + C::TX(j) + 32 * xi + 16 * h, pk);
             }
             const float w = live ? (REV ? gp[r] : gp[Wc - 1 - r]) : 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t off = tc::sw128_chunk(r, 4 * h + i);
                 *reinterpret_cast<uint4*>(sm + Lay::kt(j) + off) = la_scale_chunk(*reinterpret_cast<const uint4*>(sK + off), w);
-                if (R2)
+                if (R2 || ST)  // V~ (swapped pair) or K2~ (stacked pairs)
                     *reinterpret_cast<uint4*>(sm + Lay::oKt2 + off) =
-                        la_scale_chunk(*reinterpret_cast<const uint4*>(sV + off), w);
+                        la_scale_chunk(*reinterpret_cast<const uint4*>((ST ? sm + Lay::k2(j) : sV) + off), w);
             }
             tc::tmem_wait_st();
             tc::fence_proxy_async();
@@ -485,11 +518,14 @@ __global__ void __launch_bounds__(f64::kThreadsOut, 1)
             tc::mbar_wait(bsu(j), par(j), abort, status, 145);
             tc::fence_after_sync();
             const float rho = gp[Wc];
-            uint32_t v[16];
-            tc::tmem_ld16(lrow + C::TS + sc, v);
-            tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sig[i] = rho * sig[i] + __uint_as_float(v[i]);
+            for (int part = 0; part < kSigN / 16; ++part) {
+                uint32_t v[16];
+                tc::tmem_ld16(lrow + C::TS + sc + 16 * part, v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) sig[16 * part + i] = rho * sig[16 * part + i] + __uint_as_float(v[i]);
+            }
             if (j + 1 < nit) publish_sig(j + 1);  // the products that read this slot last have completed
             tc::fence_proxy_async();
             tc::fence_before_sync();
@@ -720,13 +756,14 @@ int f64_launch(K kfn, uint32_t smem, const f64::Maps& maps, const FoArgs& a, cud
 size_t fo64_tc_max_smem() {
     // the instantiated layouts: next summary over an extra tile (NSUM), plain (two slots for the
     // A-side operands), swapped pair, partial added (keys as values or not), next summary over
-    // the values (NSUM)
+    // the values (NSUM), stacked pairs
     const uint32_t sizes[] = {f64::OutLayout<false, true, true, false, true>::kSmemBytes,
                               f64::OutLayout<false, false, false, false, true>::kSmemBytes,
                               f64::OutLayout<true, false, false, false>::kSmemBytes,
                               f64::OutLayout<false, true, false, true, true>::kSmemBytes,
                               f64::OutLayout<false, false, false, true, true>::kSmemBytes,
                               f64::OutLayout<false, false, true, false, true>::kSmemBytes,
+                              f64::OutLayout<false, false, false, false, false, true>::kSmemBytes,
                               f64s::Layout<false>::kSmemBytes, f64s::Layout<true>::kSmemBytes};
     uint32_t m = 0;
     for (uint32_t x : sizes) m = x > m ? x : m;
@@ -776,6 +813,21 @@ int launch_fo64_tc_out(const FoArgs& a, const void* x, const void* k, const void
     HLA2_F64(false, false, false, false, false, true)  // dq = LA(du, v, k) + LA(dO, u, k)
 #undef HLA2_F64
     return -3;
+}
+
+int launch_fo64_tc_out2(const FoArgs& a, const void* x, const void* k, const void* x2, const void* k2, const void* v,
+                        void* out, bool reverse, cudaStream_t st) {
+    if (a.BH <= 0 || a.nseg <= 0) return 0;
+    f64::Maps m{};
+    if (!la_map(&m.x, x, a.BH, a.n, 64) || !la_map(&m.k, k, a.BH, a.n, 64) || !la_map(&m.x2, x2, a.BH, a.n, 64) ||
+        !la_map(&m.k2, k2, a.BH, a.n, 64) || !la_map(&m.v, v, a.BH, a.n, 64) || !la_map(&m.out, out, a.BH, a.n, 64))
+        return -2;
+    constexpr uint32_t smem = f64::OutLayout<false, false, false, false, false, true>::kSmemBytes;
+    // dk = RLA(u, dO, q) + RLA(v, du, q) (reverse);  dq = LA(dO, u, k) + LA(du, v, k) (forward)
+    return reverse ? f64_launch(fo64_out_tc_kernel<true, false, false, false, false, false, true>, smem, m, a, st,
+                                f64::kThreadsOut)
+                   : f64_launch(fo64_out_tc_kernel<false, false, false, false, false, false, true>, smem, m, a, st,
+                                f64::kThreadsOut);
 }
 
 }  // namespace hla2

@@ -288,6 +288,8 @@ struct FoArgs {
     int carry_mode;       // 0 as stored, 1 transposed, 2 symmetrised (carry + carry^T)
     float* summary;       // [BH][nseg][128*128] segment summaries written (summary launch / next summary)
     int* status;          // bounded-wait status word
+    const float* carry2;  // the second pair's carry (launch_fo64_tc_out2; NULL: zero)
+    int carry_mode2;      // as carry_mode, for carry2
 };
 bool fo_tc_available();
 size_t fo_tc_max_smem();
@@ -323,6 +325,11 @@ int launch_fo_final_state(const FoFinal& f, float* final_state, cudaStream_t st)
 // The same two launches for d = dv = 64 (fo64_tc.cu; [BH][nseg][64*64] summaries and carries).
 size_t fo64_tc_max_smem();
 int launch_fo64_tc_summary(const FoArgs& a, const void* k, const void* v, bool reverse, cudaStream_t st);
+// out = (R)LA(x, k, v) + (R)LA(x2, k2, v), d = dv = 64: two query / key pairs with the same values
+// in one pass, as one scan of the stacked pairs ([x | x2] . [k | k2], a 128 x 64 state whose row
+// halves carry a.carry (mode a.carry_mode) and a.carry2 (mode a.carry_mode2)).
+int launch_fo64_tc_out2(const FoArgs& a, const void* x, const void* k, const void* x2, const void* k2, const void* v,
+                        void* out, bool reverse, cudaStream_t st);
 int launch_fo64_tc_out(const FoArgs& a, const void* x, const void* k, const void* v, bool r2, int next_sum,
                        const void* xv, const void* add, void* out, bool reverse, cudaStream_t st);
 
