@@ -250,7 +250,8 @@ int hla2_decode_step(float* state, const void* q, const void* k, const void* v, 
  * dk, dv.  float32 or bf16 tensors [B, H, n, d], d == dv.  bf16 with d = dv = 64 and
  * chunk >= 128: tcgen05 first-order chunked scans at width 128 (the output is two chained
  * first-order scans with the same queries and keys, u = LA(q, k, v) and o = LA(q, k, u), and
- * its gradients six more, fp32 state, bf16 u and du between the passes).  Otherwise float32
+ * its gradients six more, dk and dq each two with the same values run as one pass; fp32 state,
+ * bf16 u and du between the passes).  Otherwise float32
  * arithmetic on SIMT kernels at a chunk width <= min(chunk, 32): the passes recompute the
  * forward (segment summaries P_B, E_B, R_B, the forward scan, the state at every chunk start)
  * and then run the reverse summaries, the reverse scan (cross term rho R_B^T Eh_end) and the
