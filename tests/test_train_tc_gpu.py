@@ -244,6 +244,26 @@ def test_ahla_backward_matches_oracle(B, H, n, gamma):
         assert rel_err(np64(gg.cpu()), rr) <= 2e-2, (name, B, H, n, gamma)
 
 
+def test_ahla_backward_long_context_sampled_heads():
+    """The AHLA backward at the long-context shapes (B=1 H=16 n=65536 d=dv=64 bf16, decay
+    linspace(0.99, 0.9999), chunk 128), the launch configuration of the bench's row (dk and dq
+    each one pass over two stacked query / key pairs): heads 0 and 15, the fastest and the
+    slowest decay (whose carries reach furthest across segments), against the oracle's reverse
+    sweep of the whole sequence."""
+    import dataclasses
+
+    w = dataclasses.replace(inputs.WORKLOADS["long"], with_dout=True)
+    x = inputs.make(w, seed=w.seed + 7)
+    got = [t.cpu() for t in _ahla_grads(x)]
+    g = _gamma_np(x)
+    for h in (0, w.H - 1):
+        sl = slice(h, h + 1)
+        ref = A.serial_backward(np32(x["q"][:, sl]), np32(x["k"][:, sl]), np32(x["v"][:, sl]),
+                                np32(x["dout"][:, sl]), g[sl])
+        for name, gg, rr in zip(("dq", "dk", "dv"), got, ref):
+            assert rel_err(np64(gg[:, sl]), rr) <= 2e-2, (name, h)
+
+
 def test_ahla_backward_distinct_from_the_simt_path():
     x = inputs.make_custom(1, 2, 600, 64, 64, torch.bfloat16, seed=12, gamma=(0.97, 0.999), with_dout=True)
     tc = _ahla_grads(x)
