@@ -1,8 +1,7 @@
 // Forward entry point for callers that cannot allocate device memory.
 //
 // hla2_forward takes its scratch space from the caller.  Some callers have no way to get
-// device memory for it: code running inside a CUDA graph capture where allocation calls
-// are not allowed, plug-in hosts that hand out only the input and output buffers, or
+// device memory for it: plug-in hosts that hand out only the input and output buffers, or
 // programs without a device allocator of their own.  hla2_forward_noalloc serves them: its
 // scratch is a fixed array in the library's device memory (kScratchBytes on every GPU on
 // which the library's kernels are loaded, held until the process exits), and it calls no

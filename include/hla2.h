@@ -380,17 +380,15 @@ int hla2_state_from_compact(const float* compact, float* state, int N, int H, in
 /*
  * hla2_forward for callers that cannot allocate device memory (no counterpart in the
  * paper: it exists for the library's users).  Some callers have no way to provide the
- * scratch workspace that hla2_forward needs: code running inside a CUDA graph capture,
- * where allocation calls are not allowed, plug-in hosts that hand a kernel only its input
- * and output buffers, or programs with no device allocator of their own.  This entry point
+ * scratch workspace that hla2_forward needs: plug-in hosts that hand a kernel only its
+ * input and output buffers, or programs with no device allocator of their own.  This entry point
  * takes the same tensors and flags as hla2_forward (dtype and eps given directly; no
  * initial or final state) and allocates nothing: its scratch is a fixed 32 MiB array in
  * the library's device memory, present on every GPU on which the library's kernels are
  * loaded and held until the process exits.
  *   - Sizes whose workspace (hla2_forward_workspace_bytes) exceeds 32 MiB are rejected
  *     with HLA2_ERR_WORKSPACE and a message; use hla2_forward with a workspace for them.
- *   - The first call on a device looks up the array's device address for that device;
- *     make that first call before any stream capture on the device.
+ *   - The first call on a device looks up the array's device address for that device.
  *   - All calls on a device share the array, which keeps the last call's contents (nothing
  *     in it needs to start at zero).  Calls whose executions overlap on the GPU (different
  *     streams, or graphs running concurrently) race on it and give wrong results:

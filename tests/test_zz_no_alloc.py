@@ -1,7 +1,8 @@
 """The allocation-free forward entry point (hla2_forward_noalloc), through the C ABI.
 
-It serves callers that cannot allocate device memory (graph captures, hosts that pass a
-kernel only its inputs and outputs): its scratch is a fixed array inside the library.  Its
+It serves callers that cannot allocate device memory (hosts that pass a kernel only its
+inputs and outputs, programs without a device allocator): its scratch is a fixed array inside
+the library.  Its
 output must match hla2_forward's (which takes a caller-provided workspace) and the float64
 oracle's within the bf16 parity tolerance, on two calls in a row (the array keeps the
 previous call's contents).  A bounded wait that gives up is reported through the array's
