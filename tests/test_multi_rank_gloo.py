@@ -88,6 +88,7 @@ def test_torchrun_reference_arm_prints_once():
     assert len(lines) == 1, r.stdout
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
+    assert abs(rec["ms_per_step"] - 1e3 * 16 * 65536 / rec["value"]) <= 1e-6 * rec["ms_per_step"]
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
 
 
