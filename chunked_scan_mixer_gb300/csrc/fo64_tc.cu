@@ -19,8 +19,11 @@
 // dSig = [K~^T ; K2~^T] V (the two 64 x 64 states as the row halves of one M = 128 product).  The
 // carry is read as stored, transposed or symmetrised.  The queries, keys and values (and the
 // extra and partial tiles) have two slots each: chunk j's loads go into slot j % 2 as soon as
-// chunk j - 2 has released it.  Without the second pair the G / Y tensor-memory region is
-// double-buffered as well, and the epilogue runs EPI-S(j), EPI-1(j+1), EPI-Y(j).
+// chunk j - 2 has released it.  One pair (the two-operand-slot order): one G region, Y, the A
+// operands, K~ and Sig0 in two slots by chunk parity; the epilogue runs EPI-1(j+1), EPI-S(j),
+// EPI-Y(j).  Stacked pairs (one operand slot): G and then Y in one tensor-memory region,
+// double-buffered by chunk parity; EPI-S(j), EPI-1(j+1), EPI-Y(j).  Swapped pair: one slot of
+// everything; EPI-S(j), EPI-Y(j), EPI-1(j+1).
 //
 // A summary kernel forms the segment summaries (no chain) the same way.  Roles, bounded waits
 // and one CTA per SM as in fo_tc.cu.
