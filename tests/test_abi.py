@@ -245,3 +245,31 @@ def test_debug_queries_report_a_normal_build():
     assert L.hla2_debug_status(0) == -2
     assert b"debug build" in L.hla2_last_error()
     assert L.hla2_debug_selftest(None) == -2
+
+
+def test_forward_plan_segments_cover_the_sequence():
+    """Host-side segment plans (no device: the planner's GB300 defaults): for seeded random
+    shapes the plan's segments of seg_chunks chunks, at some chunk width W <= chunk the kernels
+    run at, cover the n tokens with no segment left empty; an empty sequence plans nothing."""
+    import random
+
+    rng = random.Random(0)
+    checked = 0
+    for _ in range(300):
+        B, H, n = rng.randint(1, 4), rng.randint(1, 40), rng.randint(1, 70000)
+        d = rng.choice([16, 32, 64, 128])
+        dv = d if rng.random() < 0.7 else rng.choice([16, 32, 64, 128])
+        chunk = rng.choice([16, 32, 64, 128])
+        dtype = rng.choice([torch.bfloat16, torch.float32])
+        normalize, final = rng.random() < 0.2, rng.random() < 0.3
+        try:
+            nseg, seg_chunks, launches = hla.forward_plan(B, H, n, d, dv, chunk, dtype, normalize, final)
+        except (ValueError, hla.HLA2Error):
+            continue  # shapes no kernel covers
+        assert nseg >= 1 and seg_chunks >= 1 and launches >= 1
+        assert any((nseg - 1) * seg_chunks * W < n <= nseg * seg_chunks * W for W in (16, 32, 64, 128) if W <= chunk), \
+            (B, H, n, d, dv, chunk, dtype, normalize, final, nseg, seg_chunks)
+        checked += 1
+    assert checked > 200
+    nseg, _, launches = hla.forward_plan(1, 1, 0, 64, 64, 128)
+    assert nseg == 0 and launches == 0
